@@ -1,0 +1,128 @@
+"""The five synthetic CSA2 workloads and the recipe that draws their inputs.
+
+Sizes follow the statement of the problem for CSA2 decode in "DeepSeek-V4.1
+Flash: KVキャッシュ圧縮の限界を押し広げる" (section 2.3, CSA2; window 128, top-k 512,
+512-dim shared latent, 2:1 encoder merge) and the spec table of the
+ai.freelance-job.com summary (KV latent 512, window 128).
+
+Distributions (all seeded by the workload's index, one stream per tensor):
+  h        encoder hidden states   bf16  N(0,1)      [B, T, 512]
+  w0, w1   channel-wise merge      f32   U(0.3,0.7)  [512]
+  kraw     indexer-key rows        bf16  N(0,1)      [B, T/2, d_I]
+  iq[l]    indexer queries         f32   N(0,1)      [B, n_q, H_I, d_I]
+  w[l]     indexer head weights    f32   U(0,1)      [B, n_q, H_I]
+  q[l]     attention queries       bf16  N(0,1)      [B, n_q, H, 512]
+  win[l]   window rows of layer l  bf16  N(0,1)      [B, 128, 512]  (l >= 1; layer 0 reads h)
+Element i of a tensor is sample i of its stream, so one sequence's slice is
+drawn on its own.  Nothing in here merges, quantises or scores.
+"""
+from dataclasses import dataclass, field
+
+import numpy as np
+
+from . import normal_bf16, normal_f32, uniform_f32
+
+D_LAT = 512
+WINDOW = 128
+
+# stream ids
+S_H, S_W0, S_W1, S_KRAW = 1, 2, 3, 4
+S_IQ, S_WH, S_Q, S_WIN = 1000, 2000, 3000, 4000
+
+
+@dataclass(frozen=True)
+class Workload:
+    index: int
+    name: str
+    B: int                 # sequences
+    T: int                 # raw positions held in the cache (prefix + chunk)
+    H_I: int               # indexer heads
+    d_I: int               # indexer head dim
+    k: int                 # top-k
+    H: int                 # attention heads
+    layers: tuple          # per layer: "full" | "reindex" | "reuse"
+    pool_blocks: int = 0   # HSI blocks kept by the Full layer (0 = no pool)
+    pool_block_size: int = 8
+    chunk: int = 0         # >0: chunked prefill, the last `chunk` positions are queries and are written in the step
+
+    @property
+    def seed(self):
+        return self.index
+
+    @property
+    def n_entries(self):
+        return self.T // 2
+
+    @property
+    def prefix(self):
+        return self.T - self.chunk
+
+    @property
+    def n_q(self):
+        return self.chunk if self.chunk else 1
+
+    def q_positions(self):
+        """raw positions of the queries of one sequence"""
+        if self.chunk:
+            return np.arange(self.prefix, self.T, dtype=np.int64)
+        return np.array([self.T - 1], dtype=np.int64)
+
+    def n_elig(self, p):
+        """entries lying wholly before the window [p-127, p]"""
+        return max(0, (int(p) - (WINDOW - 1)) // 2)
+
+    def swa_range(self):
+        """(first raw position, count) of the window rows the queries read"""
+        first = max(0, int(self.q_positions()[0]) - (WINDOW - 1))
+        return first, self.T - first
+
+    # ---- input tensors (numpy, host) ----
+    def merge_weights(self):
+        return (uniform_f32(self.seed, S_W0, (D_LAT,), 0.3, 0.7),
+                uniform_f32(self.seed, S_W1, (D_LAT,), 0.3, 0.7))
+
+    def h(self, b, pos0, n_pos):
+        """bf16 hidden states of sequence b, raw positions [pos0, pos0+n_pos)"""
+        return normal_bf16(self.seed, S_H, (n_pos, D_LAT), offset=(b * self.T + pos0) * D_LAT)
+
+    def kraw(self, b, e0, n):
+        """bf16 raw indexer-key rows of sequence b, entries [e0, e0+n)"""
+        return normal_bf16(self.seed, S_KRAW, (n, self.d_I), offset=(b * self.n_entries + e0) * self.d_I)
+
+    def iq(self, layer, b):
+        n = self.n_q * self.H_I * self.d_I
+        return normal_f32(self.seed, S_IQ + layer, (self.n_q, self.H_I, self.d_I), offset=b * n)
+
+    def w_head(self, layer, b):
+        n = self.n_q * self.H_I
+        return uniform_f32(self.seed, S_WH + layer, (self.n_q, self.H_I), 0.0, 1.0, offset=b * n)
+
+    def q(self, layer, b, q0=0, nq=None):
+        nq = self.n_q if nq is None else nq
+        per_q = self.H * D_LAT
+        return normal_bf16(self.seed, S_Q + layer, (nq, self.H, D_LAT), offset=(b * self.n_q + q0) * per_q)
+
+    def window(self, layer, b):
+        """bf16 window rows [swa_count, 512] of sequence b for this layer"""
+        first, count = self.swa_range()
+        if layer == 0:
+            return self.h(b, first, count)
+        return normal_bf16(self.seed, S_WIN + layer, (count, D_LAT), offset=b * count * D_LAT)
+
+
+WORKLOADS = [
+    Workload(0, "tiny-2k-b1", B=1, T=2048, H_I=4, d_I=64, k=64, H=16, layers=("full",)),
+    Workload(1, "decode-32k-b16", B=16, T=32768, H_I=8, d_I=128, k=512, H=64, layers=("full",)),
+    Workload(2, "decode-128k-b64-20L", B=64, T=131072, H_I=8, d_I=128, k=512, H=64,
+             layers=("full",) + ("reindex",) * 9 + ("reuse",) * 10, pool_blocks=256, pool_block_size=8),
+    Workload(3, "decode-1m-b4", B=4, T=1048576, H_I=8, d_I=128, k=512, H=64, layers=("full",)),
+    Workload(4, "prefill-chunk-8k-after-120k", B=1, T=131072, H_I=8, d_I=128, k=512, H=64,
+             layers=("full",), chunk=8192),
+]
+
+
+def scaled(w, **kw):
+    """a copy of workload w with some sizes replaced (small parity cases)"""
+    d = dict(w.__dict__)
+    d.update(kw)
+    return Workload(**d)
