@@ -1,0 +1,340 @@
+"""CSA2 decode benchmark: query-tokens/s at 128K context over 20 layers that
+share one FP4 global KV (Full + HSI pool, 9 Reindex, 10 Reuse), batch 64 per
+GPU, plus the HBM-roofline fraction of the dominant entry point.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One JSON line on rank 0.  --impl reference times the fp64 CPU oracle (the
+only other implementation there is) on the host cores, on a bounded sample.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "CSA2 decode query-tokens/s at 128K ctx (indexer+top-k+attn); % of HBM roofline"
+UNIT = "query-tokens/s"
+WORKLOAD_INDEX = 2
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-sample-seqs", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(
+        os.environ.get("LOCAL_RANK", "0"))
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def config_of(wl):
+    return {"workload": wl.name, "batch_per_gpu": wl.B, "context": wl.T,
+            "layers": "1 Full (+HSI pool 256x8), 9 Reindex, 10 Reuse", "top_k": wl.k, "heads": wl.H,
+            "indexer": "%d heads x %d FP4" % (wl.H_I, wl.d_I), "window": 128, "latent": 512,
+            "l2": "inputs larger than L2 (%.2f GB FP4 cache per GPU)" % (wl.B * wl.n_entries * 360 / 1e9)}
+
+
+def algorithmic_bytes(wl):
+    """bytes the indexer scan plus the gathers must move per step: per
+    sequence n_elig*72 (Full scan) + 9*2048*72 (Reindex pool keys) +
+    20*(512*288 + 128*1024) (gathered latent rows + window rows)"""
+    n_elig = wl.n_elig(wl.T - 1)
+    n_re = sum(m == "reindex" for m in wl.layers)
+    per_seq = n_elig * 72 + n_re * wl.pool_blocks * wl.pool_block_size * 72 + len(wl.layers) * (
+        wl.k * 288 + 128 * 1024)
+    return wl.B * per_seq
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.rows = []
+        self.proc = None
+        self.dev = device_index
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            try:
+                sm.append(float(r[0]))
+                mx = float(r[1])
+                for n, v in zip(names, r[4:8]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+            except Exception:
+                pass
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- oracle timing
+
+def cpu_baseline(wl, n_seqs):
+    """the oracle as it stands on the host cores: n_seqs sequences through all
+    20 layers (cache built beforehand, outside the timed region)"""
+    import oracle
+    caches = [oracle.sequence_cache(wl, b) for b in range(n_seqs)]
+    t0 = time.perf_counter()
+    for b in range(n_seqs):
+        oracle.run_sequence(wl, b, cache=caches[b])
+    dt = time.perf_counter() - t0
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return {"value": n_seqs / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "%d of %d sequences, all %d layers, %.1f s" % (n_seqs, wl.B, len(wl.layers), dt)}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from synth.workloads import WORKLOADS
+    wl = WORKLOADS[WORKLOAD_INDEX]
+    import oracle
+    oracle.build()
+    n = 1
+    times = []
+    for s in range(args.warmup + args.steps):
+        b = s % wl.B
+        cache = oracle.sequence_cache(wl, b)
+        t0 = time.perf_counter()
+        oracle.run_sequence(wl, b, cache=cache)
+        dt = time.perf_counter() - t0
+        if s >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = len(times) * n / total
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_of(wl),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": "1 sequence of %d per step (all %d layers)" % (wl.B, len(wl.layers))},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our implementation
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import __graft_entry__
+    __graft_entry__.build()
+    import compressed_sparse_attention_decode_gb300 as csa
+    from compressed_sparse_attention_decode_gb300.synthetic import HostInputs, build_step
+    from synth.workloads import WORKLOADS
+    wl = WORKLOADS[WORKLOAD_INDEX]
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    step = build_step(wl)                  # every rank: its own 64 sequences (weak scaling, no exchange)
+    n0 = csa.csa2_launch_count()
+    step.capture()
+    launches_per_step = (csa.csa2_launch_count() - n0) // 2      # warm-up enqueue + captured enqueue
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        step.run()
+    barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step.run()
+        ev1.record(stream)
+        barrier()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    tokens_per_step = wl.B * world
+    value = tokens_per_step / (ms * 1e-3)
+
+    # per entry point device time (eager launches, events on the launching stream)
+    per_op = measure_ops(step, stream, reps=max(3, min(args.steps, 20)))
+    peak, peak_kind = measured_peak()
+    roof = roofline(wl, per_op, peak, peak_kind)
+
+    # end to end through the public API: pinned host inputs -> device, step, outputs -> host
+    host = HostInputs(step)
+    n_e2e = max(3, min(args.steps // 10, 30))
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        for name in host.names:
+            getattr(step, name).copy_(host.host[name], non_blocking=True)
+        step.run()
+        host.out.copy_(step.out, non_blocking=True)
+        torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - t0) / n_e2e
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_s], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": step_dtype(), "data": "synthetic", "config": config_of(wl),
+                "roofline": roof,
+                "step_roofline": {"algorithmic_bytes": algorithmic_bytes(wl),
+                                  "achieved_gbs": algorithmic_bytes(wl) / (ms * 1e-3) / 1e9, "peak": peak,
+                                  "frac": algorithmic_bytes(wl) / (ms * 1e-3) / 1e9 / peak,
+                                  "note": "whole step, %s peak" % peak_kind},
+                "per_op_ms": {k: v["ms"] for k, v in per_op.items()},
+                "e2e": {"value": tokens_per_step / e2e_s, "unit": UNIT, "h2d_bytes_per_step": host.h2d_bytes(),
+                        "d2h_bytes_per_step": host.d2h_bytes()},
+                "gpu_launches": launches_per_step * args.steps,
+                "clocks": clk.summary()}
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(wl, args.cpu_sample_seqs)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def step_dtype():
+    return "int32+f32+f64 (exact indexer), f32 attention"
+
+
+def measure_ops(step, stream, reps):
+    """device time of every entry point of one step, by CUDA events around
+    each call on the launching stream (no graph), averaged over reps steps"""
+    import torch
+    import compressed_sparse_attention_decode_gb300 as csa
+    from compressed_sparse_attention_decode_gb300.decode import REINDEX, REUSE
+    acc = {}
+
+    def timed(name, fn):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        acc.setdefault(name, []).append((a, b))
+
+    for _ in range(reps):
+        prev = None
+        t = 0
+        for l, mode in enumerate(step.layers):
+            idx_l = step.idx[l]
+            if mode == "reuse":
+                timed("reuse", lambda: csa.csa2_reindex(REUSE, step.cache, step.k, prev_idx=prev, idx_out=idx_l,
+                                                        n_q=step.n_q))
+            else:
+                timed("quantize_iq", lambda: csa.csa2_quantize_fp4(step.iq[t], step.iq_codes, step.iq_scales))
+                if mode == "full":
+                    timed("indexer_full", lambda: csa.csa2_indexer_topk(
+                        step.cache, step.iq_codes, step.iq_scales, step.w_head[t], step.q_pos, step.k,
+                        step.pool_blocks, step.bs, idx_out=idx_l, pool_out=step.pool, ws=step.ws_full))
+                else:
+                    timed("reindex", lambda: csa.csa2_reindex(REINDEX, step.cache, step.k, step.iq_codes,
+                                                              step.iq_scales, step.w_head[t], step.pool,
+                                                              idx_out=idx_l, ws=step.ws_re))
+                t += 1
+            timed("sparse_attn", lambda: csa.csa2_sparse_attn(step.cache, step.q[l], step.q_pos, idx_l, step.win[l],
+                                                              step.swa_pos0, out=step.out[l], ws=step.ws_attn))
+            prev = idx_l
+    torch.cuda.synchronize()
+    out = {}
+    for name, evs in acc.items():
+        ts = [a.elapsed_time(b) for a, b in evs]
+        out[name] = {"ms": sum(ts) / reps, "per_launch_ms": sum(ts) / len(ts), "launches_per_step": len(ts) // reps}
+    return out
+
+
+def roofline(wl, per_op, peak, peak_kind):
+    """HBM roofline of the entry point with the largest share of the step"""
+    n_elig = wl.n_elig(wl.T - 1)
+    bytes_per_launch = {
+        "indexer_full": wl.B * n_elig * 72,
+        "reindex": wl.B * wl.pool_blocks * wl.pool_block_size * 72,
+        "sparse_attn": wl.B * (wl.k * 288 + 128 * 1024),
+    }
+    name = max((n for n in per_op if n in bytes_per_launch), key=lambda n: per_op[n]["ms"])
+    t = per_op[name]["per_launch_ms"] * 1e-3
+    ach = bytes_per_launch[name] / t / 1e9
+    return {"bound": "hbm", "kernel": name, "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+            "traffic": None, "bytes_per_launch": bytes_per_launch[name],
+            "launch_ms": per_op[name]["per_launch_ms"], "peak_kind": peak_kind}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,607 @@
+// Lightweight indexer, exact top-k, HSI candidate pool, Reindex and Reuse
+// ("DeepSeek-v4.1 Flash: KVキャッシュ圧縮の限界を押し広げる", §2.3.1 indexer and
+// top-k, §2.3.2 Full / Reindex / Reuse, §2.3.4 HSI).
+//
+// Score of entry j for one query: S_j = sum_h w_h * ReLU(q_h . k_j) with q, k
+// the dequantised FP4 vectors; the ranking (S desc, j asc) must match an fp64
+// evaluation exactly.  The per-group sums G = sum_i 2q_i * 2k_i over 16-value
+// groups are exact integers (dp4a on doubled E2M1 values); each group term
+// t = G * s_q * s_k / 4 is exact in fp32.  The scan computes
+//     S~ = fp32 chain sum_h w_h max(sum_g t_hg, 0)
+//     E  = fac * sum_h |w_h| sum_g |t_hg|,  fac = 2 (2H + G + 8) 2^-24
+// so that the fp64-exact score lies in [S~ - E, S~ + E] (recursive-summation
+// error bounds).  Selection then needs exact scores only for entries whose
+// interval reaches the k-th largest lower bound: usually k plus a handful.
+#include "common.cuh"
+
+namespace csa2 {
+
+// ---------------------------------------------------------------- query staging
+
+template <int DI>
+struct QView {
+    int* qp;     // [H][DI/4] doubled E2M1 values, int8 x4
+    int* qn;     // [H][DI/4] their negations
+    float* qsc;  // [H][DI/16] E4M3 scales as float
+    float* w;    // [H]
+    __device__ static int words(int H) { return H * (DI / 4) * 2 + H * (DI / 16) + H; }
+    __device__ void bind(int* base, int H) {
+        qp = base;
+        qn = qp + H * (DI / 4);
+        qsc = reinterpret_cast<float*>(qn + H * (DI / 4));
+        w = qsc + H * (DI / 16);
+    }
+};
+
+template <int DI>
+__device__ void stage_query(QView<DI> v, const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
+                            const float* __restrict__ w, int H, int tid, int nthr) {
+    for (int i = tid; i < H * (DI / 4); i += nthr) {
+        uint32_t nib16 = reinterpret_cast<const uint16_t*>(codes)[i];
+        uint32_t p, n;
+        unpack4_signed(nib16, p, n);
+        v.qp[i] = (int)__vsub4(p, n);
+        v.qn[i] = (int)__vsub4(n, p);
+    }
+    for (int i = tid; i < H * (DI / 16); i += nthr) v.qsc[i] = e4m3_to_f32(scales[i]);
+    for (int i = tid; i < H; i += nthr) v.w[i] = w[i];
+}
+
+template <int DI>
+struct KeyRow {
+    uint32_t kp[DI / 4], kn[DI / 4];
+    float sk[DI / 16];
+    __device__ __forceinline__ void load(const uint8_t* __restrict__ kc, const uint8_t* __restrict__ ks) {
+#pragma unroll
+        for (int v = 0; v < DI / 32; ++v) {
+            uint4 c = __ldg(reinterpret_cast<const uint4*>(kc) + v);
+            const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                unpack4_signed(cw[t] & 0xffffu, kp[8 * v + 2 * t], kn[8 * v + 2 * t]);
+                unpack4_signed(cw[t] >> 16, kp[8 * v + 2 * t + 1], kn[8 * v + 2 * t + 1]);
+            }
+        }
+        if (DI == 128) {
+            uint2 s = __ldg(reinterpret_cast<const uint2*>(ks));
+#pragma unroll
+            for (int g = 0; g < 4; ++g) sk[g] = e4m3_to_f32((s.x >> (8 * g)) & 255u);
+#pragma unroll
+            for (int g = 0; g < DI / 16 - 4; ++g) sk[4 + g] = e4m3_to_f32((s.y >> (8 * g)) & 255u);
+        } else {
+            uint32_t s = __ldg(reinterpret_cast<const uint32_t*>(ks));
+#pragma unroll
+            for (int g = 0; g < DI / 16; ++g) sk[g] = e4m3_to_f32((s >> (8 * g)) & 255u);
+        }
+    }
+};
+
+// approximate score and its error bound (see the file header)
+template <int DI>
+__device__ __forceinline__ void approx_score(const KeyRow<DI>& k, QView<DI> q, int H, float fac, float& L,
+                                             float& U) {
+    float S = 0.0f, B = 0.0f;
+    for (int h = 0; h < H; ++h) {
+        float d = 0.0f, A = 0.0f;
+#pragma unroll
+        for (int g = 0; g < DI / 16; ++g) {
+            int G = group_dot4(q.qp + h * (DI / 4) + 4 * g, q.qn + h * (DI / 4) + 4 * g, k.kp + 4 * g, k.kn + 4 * g);
+            float c = q.qsc[h * (DI / 16) + g] * k.sk[g] * 0.25f;   // exact
+            float t = (float)G * c;                                  // exact
+            d += t;
+            A += fabsf(t);
+        }
+        S = __fmaf_rn(q.w[h], fmaxf(d, 0.0f), S);
+        B = __fmaf_rn(fabsf(q.w[h]), A, B);
+    }
+    float E = B * fac;
+    L = S - E;
+    U = S + E;
+}
+
+// the exact score: integer group sums, exact fp64 group terms and sum, fp64
+// fused multiply-add chain over heads in ascending order
+template <int DI>
+__device__ double exact_score(const uint8_t* __restrict__ kc, const uint8_t* __restrict__ ks, QView<DI> q, int H) {
+    KeyRow<DI> k;
+    k.load(kc, ks);
+    double S = 0.0;
+    for (int h = 0; h < H; ++h) {
+        double d = 0.0;
+#pragma unroll
+        for (int g = 0; g < DI / 16; ++g) {
+            int G = group_dot4(q.qp + h * (DI / 4) + 4 * g, q.qn + h * (DI / 4) + 4 * g, k.kp + 4 * g, k.kn + 4 * g);
+            d += (double)G * ((double)q.qsc[h * (DI / 16) + g] * (double)k.sk[g] * 0.25);
+        }
+        S = fma((double)q.w[h], d > 0.0 ? d : 0.0, S);
+    }
+    return S;
+}
+
+__device__ __forceinline__ int n_elig_of(int64_t p, int capacity) {
+    int64_t n = (p - (WINDOW - 1)) >> 1;
+    if (p < WINDOW - 1) n = 0;
+    return (int)(n < capacity ? n : capacity);
+}
+
+__host__ __device__ inline float bound_factor(int H, int DI) { return 2.0f * (float)(2 * H + DI / 16 + 8) * 0x1p-24f; }
+
+// ---------------------------------------------------------------- scans
+
+// Full scan: entries [0, n_elig) of each query; QB queries share one key load.
+template <int DI>
+__global__ void __launch_bounds__(256) k_scan_full(const uint8_t* __restrict__ kc_all, const uint8_t* __restrict__ ks_all,
+                                                   int capacity, const uint8_t* __restrict__ iq_codes,
+                                                   const uint8_t* __restrict__ iq_scales, const float* __restrict__ w_head,
+                                                   const int64_t* __restrict__ q_pos, int n_q, int q0, int n_qc, int H,
+                                                   int QB, float2* __restrict__ lu) {
+    extern __shared__ int smem[];
+    const int b = blockIdx.z;
+    const int qa = blockIdx.y * QB;
+    const int nqb = min(QB, n_qc - qa);
+    const int words = QView<DI>::words(H);
+    int* nel = smem;
+    for (int t = 0; t < nqb; ++t) {
+        QView<DI> v;
+        v.bind(smem + 32 + t * words, H);
+        int64_t gq = (int64_t)b * n_q + q0 + qa + t;
+        stage_query<DI>(v, iq_codes + gq * H * (DI / 2), iq_scales + gq * H * (DI / 16), w_head + gq * H, H,
+                        threadIdx.x, blockDim.x);
+        if (threadIdx.x == 0) nel[t] = n_elig_of(q_pos[gq], capacity);
+    }
+    __syncthreads();
+    const int j = blockIdx.x * blockDim.x + threadIdx.x;
+    int maxn = 0;
+    for (int t = 0; t < nqb; ++t) maxn = max(maxn, nel[t]);
+    if (j >= maxn) return;
+    KeyRow<DI> k;
+    const int64_t row = (int64_t)b * capacity + j;
+    k.load(kc_all + row * (DI / 2), ks_all + row * (DI / 16));
+    const float fac = bound_factor(H, DI);
+    for (int t = 0; t < nqb; ++t) {
+        if (j >= nel[t]) continue;
+        QView<DI> v;
+        v.bind(smem + 32 + t * words, H);
+        float L, U;
+        approx_score<DI>(k, v, H, fac, L, U);
+        lu[((int64_t)b * n_qc + qa + t) * capacity + j] = make_float2(L, U);
+    }
+}
+
+// Reindex scan: the pool slots of each query (entry id pool[t], -1 = empty).
+template <int DI>
+__global__ void __launch_bounds__(256) k_scan_pool(const uint8_t* __restrict__ kc_all, const uint8_t* __restrict__ ks_all,
+                                                   int capacity, const uint8_t* __restrict__ iq_codes,
+                                                   const uint8_t* __restrict__ iq_scales, const float* __restrict__ w_head,
+                                                   const int32_t* __restrict__ pool, int pool_len, int n_q, int H,
+                                                   float2* __restrict__ lu) {
+    extern __shared__ int smem[];
+    const int b = blockIdx.z, q = blockIdx.y;
+    const int64_t gq = (int64_t)b * n_q + q;
+    QView<DI> v;
+    v.bind(smem, H);
+    stage_query<DI>(v, iq_codes + gq * H * (DI / 2), iq_scales + gq * H * (DI / 16), w_head + gq * H, H, threadIdx.x,
+                    blockDim.x);
+    __syncthreads();
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= pool_len) return;
+    const int j = pool[gq * pool_len + t];
+    float L = -INFINITY, U = -INFINITY;
+    if (j >= 0 && j < capacity) {
+        KeyRow<DI> k;
+        const int64_t row = (int64_t)b * capacity + j;
+        k.load(kc_all + row * (DI / 2), ks_all + row * (DI / 16));
+        approx_score<DI>(k, v, H, bound_factor(H, DI), L, U);
+    }
+    lu[gq * pool_len + t] = make_float2(L, U);
+}
+
+// ---------------------------------------------------------------- block-wide selection helpers
+
+struct SelectSmem {
+    int hist[256];
+    int ctl[8];               // [0] counter, [1] digit, [2] krem, [3] misc
+    unsigned long long key[MAX_K];
+    int id[MAX_K];
+};
+
+// k-th largest key (k >= 1, at least k valid items) over items t in [0, n):
+// getkey(t, key) returns false for items that do not take part.  Returns the
+// key value and leaves in *krem how many items equal to it are needed.
+template <typename KeyT, typename Get>
+__device__ KeyT block_kth_largest(Get getkey, int n, int k, SelectSmem& sm, int* krem_out) {
+    constexpr int BITS = sizeof(KeyT) * 8;
+    KeyT prefix = 0, mask = 0;
+    int krem = k;
+    for (int shift = BITS - 8; shift >= 0; shift -= 8) {
+        for (int i = threadIdx.x; i < 256; i += blockDim.x) sm.hist[i] = 0;
+        __syncthreads();
+        for (int t = threadIdx.x; t < n; t += blockDim.x) {
+            KeyT key;
+            if (getkey(t, key) && (key & mask) == prefix) atomicAdd(&sm.hist[(int)((key >> shift) & 255)], 1);
+        }
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            const int lane = threadIdx.x;
+            int c = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) c += sm.hist[255 - 8 * lane - i];   // lane 0 holds the top bins
+            int incl = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            unsigned hit = __ballot_sync(0xffffffffu, incl >= krem);
+            int L = __ffs(hit) - 1;
+            if (lane == L) {
+                int cum = incl - c;
+                for (int i = 0; i < 8; ++i) {
+                    int d = 255 - 8 * lane - i;
+                    if (cum + sm.hist[d] >= krem) {
+                        sm.ctl[1] = d;
+                        sm.ctl[2] = krem - cum;
+                        break;
+                    }
+                    cum += sm.hist[d];
+                }
+            }
+        }
+        __syncthreads();
+        prefix |= (KeyT)sm.ctl[1] << shift;
+        mask |= (KeyT)255 << shift;
+        krem = sm.ctl[2];
+        __syncthreads();
+    }
+    *krem_out = krem;
+    return prefix;
+}
+
+// warp-aggregated append of the flagged items to list[], counter in sm.ctl[0]
+__device__ __forceinline__ void append_flagged(bool flag, int value, int* list, SelectSmem& sm) {
+    unsigned m = __ballot_sync(0xffffffffu, flag);
+    if (!m) return;
+    int lane = threadIdx.x & 31;
+    int leader = __ffs(m) - 1;
+    int base = 0;
+    if (lane == leader) base = atomicAdd(&sm.ctl[0], __popc(m));
+    base = __shfl_sync(0xffffffffu, base, leader);
+    if (flag) list[base + __popc(m & ((1u << lane) - 1u))] = value;
+}
+
+// Among m candidates (cid[t], ckey[t]) keep the k best by (key desc, id asc):
+// the kept ones end up in sm.key/sm.id[0..kept), unordered.  Returns kept.
+__device__ int keep_best(const int* cid, const unsigned long long* ckey, int m, int k, SelectSmem& sm) {
+    if (m <= k) {
+        for (int t = threadIdx.x; t < m; t += blockDim.x) {
+            sm.key[t] = ckey[t];
+            sm.id[t] = cid[t];
+        }
+        __syncthreads();
+        return m;
+    }
+    int krem;
+    unsigned long long kth = block_kth_largest<unsigned long long>(
+        [&](int t, unsigned long long& key) {
+            key = ckey[t];
+            return true;
+        },
+        m, k, sm, &krem);
+    // among the ties with key == kth keep the krem lowest ids
+    int krem2;
+    unsigned int idcut = block_kth_largest<unsigned int>(
+        [&](int t, unsigned int& key) {
+            key = ~(unsigned int)cid[t];
+            return ckey[t] == kth;
+        },
+        m, krem, sm, &krem2);
+    if (threadIdx.x == 0) sm.ctl[0] = 0;
+    __syncthreads();
+    for (int base = 0; base < m; base += blockDim.x) {
+        int t = base + threadIdx.x;
+        bool take = false;
+        if (t < m) take = ckey[t] > kth || (ckey[t] == kth && ~(unsigned int)cid[t] >= idcut);
+        unsigned msk = __ballot_sync(0xffffffffu, take);
+        int lane = threadIdx.x & 31, leader = msk ? __ffs(msk) - 1 : 0, pos = 0;
+        if (msk && lane == leader) pos = atomicAdd(&sm.ctl[0], __popc(msk));
+        pos = __shfl_sync(0xffffffffu, pos, leader);
+        if (take) {
+            int slot = pos + __popc(msk & ((1u << lane) - 1u));
+            sm.key[slot] = ckey[t];
+            sm.id[slot] = cid[t];
+        }
+    }
+    __syncthreads();
+    return k;
+}
+
+// bitonic sort of sm.key/sm.id[0..n) (n <= MAX_K), padded with sentinels.
+// desc_by_key: order (key desc, id asc); otherwise (id asc).
+__device__ void sort_kept(int n, bool desc_by_key, SelectSmem& sm) {
+    int N = 1;
+    while (N < n) N <<= 1;
+    for (int t = n + threadIdx.x; t < N; t += blockDim.x) {
+        sm.key[t] = 0ull;
+        sm.id[t] = 0x7fffffff;
+    }
+    __syncthreads();
+    for (int size = 2; size <= N; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int t = threadIdx.x; t < N / 2; t += blockDim.x) {
+                int i = 2 * t - (t & (stride - 1));
+                int j = i + stride;
+                bool up = ((i & size) == 0);
+                unsigned long long ki = sm.key[i], kj = sm.key[j];
+                int ii = sm.id[i], ij = sm.id[j];
+                // "i before j" in the target order
+                bool i_first = desc_by_key ? (ki > kj || (ki == kj && ii < ij)) : (ii < ij);
+                if (i_first != up) {
+                    sm.key[i] = kj;
+                    sm.key[j] = ki;
+                    sm.id[i] = ij;
+                    sm.id[j] = ii;
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+// ---------------------------------------------------------------- selection kernel
+
+// One block per (sequence, query).  Items t in [0, n_items): for Full the
+// entries 0..n_elig-1 (ids == nullptr), for Reindex the pool slots (entry id
+// ids[t], -1 = empty).  lu holds (S~-E, S~+E) per item.
+template <int DI>
+__global__ void __launch_bounds__(512) k_select(const float2* __restrict__ lu, int lu_stride,
+                                                 const int32_t* __restrict__ ids, int n_items_fixed,
+                                                 const uint8_t* __restrict__ kc_all, const uint8_t* __restrict__ ks_all,
+                                                 int capacity, const uint8_t* __restrict__ iq_codes,
+                                                 const uint8_t* __restrict__ iq_scales,
+                                                 const float* __restrict__ w_head, const int64_t* __restrict__ q_pos,
+                                                 int n_q, int q0, int n_qc, int H, int k, int32_t* __restrict__ idx_out,
+                                                 int pool_blocks, int bs, int32_t* __restrict__ pool_out,
+                                                 int* __restrict__ cand_id_ws, unsigned long long* __restrict__ cand_key_ws) {
+    extern __shared__ int qsm[];
+    __shared__ SelectSmem sm;
+    const int b = blockIdx.y, ql = blockIdx.x;
+    const int64_t gq = (int64_t)b * n_q + q0 + ql;     // global query row
+    const int64_t slab = (int64_t)b * n_qc + ql;        // workspace row
+    QView<DI> v;
+    v.bind(qsm, H);
+    stage_query<DI>(v, iq_codes + gq * H * (DI / 2), iq_scales + gq * H * (DI / 16), w_head + gq * H, H, threadIdx.x,
+                    blockDim.x);
+    const float2* L = lu + slab * lu_stride;
+    const int32_t* id = ids ? ids + gq * lu_stride : nullptr;
+    const int n_items = ids ? n_items_fixed : n_elig_of(q_pos[gq], capacity);
+    int* cid = cand_id_ws + slab * lu_stride;
+    unsigned long long* ckey = cand_key_ws + slab * lu_stride;
+    const uint8_t* kc = kc_all + (int64_t)b * capacity * (DI / 2);
+    const uint8_t* ks = ks_all + (int64_t)b * capacity * (DI / 16);
+    auto entry_of = [&](int t) -> int {
+        if (!id) return t;
+        int j = id[t];
+        return (j >= 0 && j < capacity) ? j : -1;
+    };
+    if (threadIdx.x == 0) {
+        sm.ctl[0] = 0;
+        sm.ctl[3] = 0;
+    }
+    __syncthreads();
+
+    // ---- 1. lower bound of the k-th best, candidates whose upper bound reaches it
+    int n_valid = n_items;
+    if (id) {
+        // count non-empty slots
+        int c = 0;
+        for (int t = threadIdx.x; t < n_items; t += blockDim.x) c += entry_of(t) >= 0;
+        c = __reduce_add_sync(0xffffffffu, c);
+        if ((threadIdx.x & 31) == 0) atomicAdd(&sm.ctl[3], c);
+        __syncthreads();
+        n_valid = sm.ctl[3];
+        __syncthreads();
+    }
+    unsigned int lam = 0u;
+    if (n_valid > k) {
+        int krem;
+        lam = block_kth_largest<unsigned int>(
+            [&](int t, unsigned int& key) {
+                key = f32_key(L[t].x);
+                return entry_of(t) >= 0;
+            },
+            n_items, k, sm, &krem);
+    }
+    if (threadIdx.x == 0) sm.ctl[0] = 0;
+    __syncthreads();
+    for (int base = 0; base < n_items; base += blockDim.x) {
+        int t = base + threadIdx.x;
+        bool f = t < n_items && entry_of(t) >= 0 && f32_key(L[t].y) >= lam;
+        append_flagged(f, t, cid, sm);
+    }
+    __syncthreads();
+    int m = sm.ctl[0];
+    __syncthreads();
+    // ---- 2. exact scores of the candidates
+    for (int t = threadIdx.x; t < m; t += blockDim.x) {
+        int j = entry_of(cid[t]);
+        double S = exact_score<DI>(kc + (int64_t)j * (DI / 2), ks + (int64_t)j * (DI / 16), v, H);
+        ckey[t] = f64_key(S);
+        cid[t] = j;     // from here on candidates carry entry ids
+    }
+    __syncthreads();
+    // ---- 3. the k best, in rank order
+    int kept = keep_best(cid, ckey, m, k, sm);
+    sort_kept(kept, true, sm);
+    int32_t* out = idx_out + gq * k;
+    for (int t = threadIdx.x; t < k; t += blockDim.x) out[t] = t < kept ? sm.id[t] : -1;
+    __syncthreads();
+
+    // ---- 4. HSI candidate pool (Full only)
+    if (pool_blocks <= 0 || ids) return;
+    const int P = pool_blocks * bs;
+    int32_t* pout = pool_out + gq * P;
+    const int nb = (n_items + bs - 1) / bs;
+    int nsel;
+    if (nb <= pool_blocks) {                 // every block fits
+        for (int t = threadIdx.x; t < nb; t += blockDim.x) sm.id[t] = t;
+        nsel = nb;
+        __syncthreads();
+    } else if (pool_blocks == 1) {           // one slot: the forced newest block
+        if (threadIdx.x == 0) sm.id[0] = nb - 1;
+        nsel = 1;
+        __syncthreads();
+    } else {
+        const int others = nb - 1;        // block nb-1 holds entry n_elig-1: forced in
+        auto blk_lu = [&](int blk, bool upper) {
+            float mx = -INFINITY;
+            for (int i = 0; i < bs; ++i) {
+                int j = blk * bs + i;
+                if (j < n_items) mx = fmaxf(mx, upper ? L[j].y : L[j].x);
+            }
+            return mx;
+        };
+        int krem;
+        unsigned int lamb = block_kth_largest<unsigned int>(
+            [&](int t, unsigned int& key) {
+                key = f32_key(blk_lu(t, false));
+                return true;
+            },
+            others, pool_blocks - 1, sm, &krem);
+        if (threadIdx.x == 0) sm.ctl[0] = 0;
+        __syncthreads();
+        for (int base = 0; base < others; base += blockDim.x) {
+            int t = base + threadIdx.x;
+            bool f = t < others && f32_key(blk_lu(t, true)) >= lamb;
+            append_flagged(f, t, cid, sm);
+        }
+        __syncthreads();
+        int mb = sm.ctl[0];
+        __syncthreads();
+        for (int t = threadIdx.x; t < mb; t += blockDim.x) ckey[t] = 0ull;
+        __syncthreads();
+        for (int u = threadIdx.x; u < mb * bs; u += blockDim.x) {
+            int t = u / bs, j = cid[t] * bs + u % bs;
+            double S = exact_score<DI>(kc + (int64_t)j * (DI / 2), ks + (int64_t)j * (DI / 16), v, H);
+            atomicMax(&ckey[t], f64_key(S));
+        }
+        __syncthreads();
+        keep_best(cid, ckey, mb, pool_blocks - 1, sm);
+        if (threadIdx.x == 0) {
+            sm.id[pool_blocks - 1] = nb - 1;
+            sm.key[pool_blocks - 1] = 0ull;
+        }
+        nsel = pool_blocks;
+        __syncthreads();
+    }
+    sort_kept(nsel, false, sm);
+    for (int u = threadIdx.x; u < P; u += blockDim.x) {
+        int t = u / bs;
+        int j = t < nsel ? sm.id[t] * bs + u % bs : -1;
+        // only the last kept block can run past n_elig; its tail slots are empty
+        pout[u] = (j >= 0 && j < n_items) ? j : -1;
+    }
+    // move the -1 slots of a partial last block to the end: they are already
+    // there, because the partial block has the largest id and sorts last
+}
+
+// Reuse: the latest indices, unchanged ("DeepSeek-v4.1 Flash" §2.3.2)
+__global__ void k_copy_idx(const int32_t* __restrict__ src, int32_t* __restrict__ dst, int64_t n) {
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) dst[i] = src[i];
+}
+
+// ---------------------------------------------------------------- launchers
+
+constexpr int SCAN_QB = 8;
+constexpr int QUERY_CHUNK = 256;
+
+size_t select_ws_per_item() { return sizeof(float2) + sizeof(int) + sizeof(unsigned long long); }
+
+template <int DI>
+cudaError_t launch_indexer_full_t(const csa2_cache& c, const uint8_t* iq_codes, const uint8_t* iq_scales,
+                                  const float* w_head, int n_q, const int64_t* q_pos, int H, int k, int32_t* idx_out,
+                                  int pool_blocks, int bs, int32_t* pool_out, void* ws, cudaStream_t st) {
+    const int qchunk = n_q < QUERY_CHUNK ? n_q : QUERY_CHUNK;
+    const int64_t items = (int64_t)c.batch * qchunk * c.capacity;
+    float2* lu = reinterpret_cast<float2*>(ws);
+    unsigned long long* ckey = reinterpret_cast<unsigned long long*>(lu + items);
+    int* cid = reinterpret_cast<int*>(ckey + items);
+    const size_t qwords = (size_t)QView<DI>::words(H) * sizeof(int);
+    for (int q0 = 0; q0 < n_q; q0 += qchunk) {
+        const int n_qc = (n_q - q0) < qchunk ? (n_q - q0) : qchunk;
+        const int QB = n_qc < SCAN_QB ? n_qc : SCAN_QB;
+        dim3 g1((c.capacity + 255) / 256, (n_qc + QB - 1) / QB, c.batch);
+        k_scan_full<DI><<<g1, 256, 32 * sizeof(int) + QB * qwords, st>>>(
+            c.ikey_codes, c.ikey_scales, c.capacity, iq_codes, iq_scales, w_head, q_pos, n_q, q0, n_qc, H, QB, lu);
+        note_launch();
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        dim3 g2(n_qc, c.batch);
+        k_select<DI><<<g2, 512, qwords, st>>>(lu, c.capacity, nullptr, 0, c.ikey_codes, c.ikey_scales, c.capacity,
+                                               iq_codes, iq_scales, w_head, q_pos, n_q, q0, n_qc, H, k, idx_out,
+                                               pool_blocks, bs, pool_out, cid, ckey);
+        note_launch();
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+template <int DI>
+cudaError_t launch_reindex_t(const csa2_cache& c, const uint8_t* iq_codes, const uint8_t* iq_scales,
+                             const float* w_head, int n_q, int H, const int32_t* pool, int pool_len, int k,
+                             int32_t* idx_out, void* ws, cudaStream_t st) {
+    const int64_t items = (int64_t)c.batch * n_q * pool_len;
+    float2* lu = reinterpret_cast<float2*>(ws);
+    unsigned long long* ckey = reinterpret_cast<unsigned long long*>(lu + items);
+    int* cid = reinterpret_cast<int*>(ckey + items);
+    const size_t qwords = (size_t)QView<DI>::words(H) * sizeof(int);
+    dim3 g1((pool_len + 255) / 256, n_q, c.batch);
+    k_scan_pool<DI><<<g1, 256, qwords, st>>>(c.ikey_codes, c.ikey_scales, c.capacity, iq_codes, iq_scales, w_head,
+                                             pool, pool_len, n_q, H, lu);
+    note_launch();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    dim3 g2(n_q, c.batch);
+    k_select<DI><<<g2, 512, qwords, st>>>(lu, pool_len, pool, pool_len, c.ikey_codes, c.ikey_scales, c.capacity,
+                                           iq_codes, iq_scales, w_head, nullptr, n_q, 0, n_q, H, k, idx_out, 0, 1,
+                                           nullptr, cid, ckey);
+    note_launch();
+    return cudaGetLastError();
+}
+
+size_t indexer_full_ws(int batch, int n_q, int64_t capacity) {
+    const int qchunk = n_q < QUERY_CHUNK ? n_q : QUERY_CHUNK;
+    return (size_t)batch * qchunk * capacity * select_ws_per_item();
+}
+
+size_t reindex_ws(int batch, int n_q, int64_t pool_len) {
+    return (size_t)batch * n_q * pool_len * select_ws_per_item();
+}
+
+cudaError_t launch_indexer_full(const csa2_cache& c, const uint8_t* iq_codes, const uint8_t* iq_scales,
+                                const float* w_head, int n_q, const int64_t* q_pos, int H, int k, int32_t* idx_out,
+                                int pool_blocks, int bs, int32_t* pool_out, void* ws, cudaStream_t st) {
+    if (c.d_idx == 128)
+        return launch_indexer_full_t<128>(c, iq_codes, iq_scales, w_head, n_q, q_pos, H, k, idx_out, pool_blocks, bs,
+                                          pool_out, ws, st);
+    return launch_indexer_full_t<64>(c, iq_codes, iq_scales, w_head, n_q, q_pos, H, k, idx_out, pool_blocks, bs,
+                                     pool_out, ws, st);
+}
+
+cudaError_t launch_reindex(const csa2_cache& c, const uint8_t* iq_codes, const uint8_t* iq_scales, const float* w_head,
+                           int n_q, int H, const int32_t* pool, int pool_len, int k, int32_t* idx_out, void* ws,
+                           cudaStream_t st) {
+    if (c.d_idx == 128)
+        return launch_reindex_t<128>(c, iq_codes, iq_scales, w_head, n_q, H, pool, pool_len, k, idx_out, ws, st);
+    return launch_reindex_t<64>(c, iq_codes, iq_scales, w_head, n_q, H, pool, pool_len, k, idx_out, ws, st);
+}
+
+cudaError_t launch_reuse(const int32_t* prev, int32_t* out, int64_t n, cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    k_copy_idx<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(prev, out, n);
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace csa2

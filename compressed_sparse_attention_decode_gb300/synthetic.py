@@ -1,0 +1,86 @@
+"""Fill a DecodeStep with one of the seeded synthetic workloads.
+
+Inputs are drawn on the host by the ``synth`` generator (the same bytes the
+oracle draws), copied to the device, and the context is written into the cache
+by the library's own cache-write kernel, one sequence at a time so that the
+host staging buffer stays small.
+"""
+import numpy as np
+import torch
+
+from synth.workloads import D_LAT
+
+from . import Cache, csa2_cache_write
+from .decode import DecodeStep
+
+
+def _bf16(a):
+    """uint16 bit patterns (numpy) -> torch bfloat16 tensor (host)"""
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+
+
+def seq_view(cache, b):
+    """a batch-1 Cache aliasing sequence b of `cache`"""
+    v = Cache.__new__(Cache)
+    v.batch, v.capacity, v.d_idx = 1, cache.capacity, cache.d_idx
+    v.lat_codes = cache.lat_codes[b:b + 1]
+    v.lat_scales = cache.lat_scales[b:b + 1]
+    v.ikey_codes = cache.ikey_codes[b:b + 1]
+    v.ikey_scales = cache.ikey_scales[b:b + 1]
+    return v
+
+
+class HostInputs:
+    """pinned host copies of one step's inputs (for the end-to-end timing)"""
+
+    def __init__(self, step):
+        pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        self.names = ["iq", "w_head", "q", "win", "q_pos"] + (["h_chunk", "kraw_chunk"] if step.chunk_len else [])
+        self.host = {n: pin(getattr(step, n)) for n in self.names}
+        self.out = pin(step.out)
+
+    def h2d_bytes(self):
+        return sum(t.numel() * t.element_size() for t in self.host.values())
+
+    def d2h_bytes(self):
+        return self.out.numel() * self.out.element_size()
+
+
+def build_step(wl, device="cuda", want_lse=False, seqs=None, capture_inputs=False):
+    """DecodeStep for workload wl with context, inputs and window rows loaded.
+    seqs: restrict to these sequence ids (default all wl.B)."""
+    seqs = list(range(wl.B)) if seqs is None else list(seqs)
+    B = len(seqs)
+    first, count = wl.swa_range()
+    step = DecodeStep(B, wl.n_entries, wl.n_q, wl.layers, H=wl.H, H_I=wl.H_I, d_I=wl.d_I, k=wl.k,
+                      pool_blocks=wl.pool_blocks, pool_block_size=wl.pool_block_size, swa_len=count,
+                      chunk_pos=wl.prefix, device=device, want_lse=want_lse)
+    step.swa_pos0 = first
+    w0, w1 = wl.merge_weights()
+    w0_d = torch.from_numpy(w0).to(device)
+    w1_d = torch.from_numpy(w1).to(device)
+    if wl.chunk:
+        step.set_chunk(wl.chunk, w0_d, w1_d)
+    qpos = torch.from_numpy(wl.q_positions())
+    step.q_pos.copy_(qpos[None, :].expand(B, -1))
+    for bi, b in enumerate(seqs):
+        # context written once, outside the step
+        n_ctx = wl.prefix
+        if n_ctx:
+            h = wl.h(b, 0, n_ctx)
+            kr = wl.kraw(b, 0, n_ctx // 2)
+            csa2_cache_write(seq_view(step.cache, bi), _bf16(h)[None].to(device), 0, w0_d, w1_d,
+                             _bf16(kr)[None].to(device))
+        if wl.chunk:
+            step.h_chunk[bi].copy_(_bf16(wl.h(b, wl.prefix, wl.chunk)))
+            step.kraw_chunk[bi].copy_(_bf16(wl.kraw(b, wl.prefix // 2, wl.chunk // 2)))
+        t = 0
+        for l, mode in enumerate(wl.layers):
+            step.win[l, bi].copy_(_bf16(wl.window(l, b)))
+            step.q[l, bi].copy_(_bf16(wl.q(l, b)))
+            if mode != "reuse":
+                step.iq[t, bi].copy_(torch.from_numpy(wl.iq(l, b)))
+                step.w_head[t, bi].copy_(torch.from_numpy(wl.w_head(l, b)))
+                t += 1
+    torch.cuda.synchronize()
+    return step

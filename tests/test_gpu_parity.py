@@ -1,0 +1,272 @@
+"""CUDA path vs the fp64 oracle, through the C ABI.
+
+Bar: cache bytes, FP4 codes, scales, top-k index lists and HSI pools
+bit-exact; attention outputs within a max relative error of 2e-3 per
+(sequence, query, head) row: max_i |o_i - o*_i| / max_i |o*_i|.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from synth.workloads import WORKLOADS, scaled
+
+pytestmark = pytest.mark.gpu
+
+ATTN_TOL = 2e-3
+
+
+@pytest.fixture(scope="module")
+def csa():
+    import compressed_sparse_attention_decode_gb300 as m
+    from compressed_sparse_attention_decode_gb300 import build as b
+    b.build()
+    m.load()
+    assert torch.cuda.is_available()
+    return m
+
+
+def bf16_t(a, dev="cuda"):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+def rel_err_rows(out, ref):
+    num = np.abs(out.astype(np.float64) - ref).max(-1)
+    den = np.abs(ref).max(-1)
+    return float((num / den).max())
+
+
+def host_cache(csa, planes, d_idx):
+    """upload host cache planes (numpy [B, n, ...]) into a Cache"""
+    lc, ls, kc, ks = planes
+    c = csa.Cache(lc.shape[0], lc.shape[1], d_idx)
+    for t, a in zip((c.lat_codes, c.lat_scales, c.ikey_codes, c.ikey_scales), planes):
+        t.copy_(torch.from_numpy(np.ascontiguousarray(a)))
+    return c
+
+
+# ---------------------------------------------------------------- cache write / codec
+
+def wide_range_rows(seed, rows, d):
+    """normal values times 2^e, e drawn per 16-group over [-40, 14]: E4M3
+    scales from subnormal to saturated, plus exact midpoints and zero groups"""
+    x = synth.normal_f32(seed, 1, (rows, d)).astype(np.float64)
+    e = np.floor(synth.uniform_f32(seed, 2, (rows, d // 16), -40, 14)).astype(np.float64)
+    x = x * np.repeat(2.0 ** e, 16, axis=1)
+    x[0, :16] = 0.0
+    s = 2.0 ** -3
+    x[1, :16] = np.array([6, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5, -0.25, -0.75, -1.25, -1.75, -2.5, -3.5, -5, 5.5]) * s
+    return x
+
+
+def test_quantize_fp4_bit_exact(csa):
+    x = wide_range_rows(31, 512, 128).astype(np.float32)
+    codes, scales = csa.csa2_quantize_fp4(torch.from_numpy(x).cuda())
+    rc, rs = oracle.quantize_rows(x)
+    assert np.array_equal(scales.cpu().numpy(), rs)
+    assert np.array_equal(codes.cpu().numpy(), rc)
+
+
+@pytest.mark.parametrize("d_idx", [64, 128])
+def test_cache_write_bit_exact_wide_range(csa, d_idx):
+    B, n_pos = 2, 256
+    h = wide_range_rows(32, B * n_pos, 512)
+    # round to bf16 (RNE) on the host
+    u = h.astype(np.float32).view(np.uint32).astype(np.uint64)
+    hb = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16).reshape(B, n_pos, 512)
+    kr = wide_range_rows(33, B * n_pos // 2, d_idx).astype(np.float32).view(np.uint32).astype(np.uint64)
+    kb = ((kr + 0x7FFF + ((kr >> 16) & 1)) >> 16).astype(np.uint16).reshape(B, n_pos // 2, d_idx)
+    w0 = synth.uniform_f32(33, 3, (512,), 0.3, 0.7)
+    w1 = synth.uniform_f32(33, 4, (512,), 0.3, 0.7)
+    cache = csa.Cache(B, n_pos // 2 + 10, d_idx)
+    csa.csa2_cache_write(cache, bf16_t(hb[:, :128]), 0, torch.from_numpy(w0).cuda(), torch.from_numpy(w1).cuda(),
+                         bf16_t(kb[:, :64]))
+    csa.csa2_cache_write(cache, bf16_t(hb[:, 128:]), 128, torch.from_numpy(w0).cuda(), torch.from_numpy(w1).cuda(),
+                         bf16_t(kb[:, 64:]))
+    for b in range(B):
+        lc, ls, kc, ks = oracle.cache_write(hb[b], w0, w1, kb[b])
+        n = n_pos // 2
+        assert np.array_equal(cache.lat_codes[b, :n].cpu().numpy(), lc)
+        assert np.array_equal(cache.lat_scales[b, :n].cpu().numpy(), ls)
+        assert np.array_equal(cache.ikey_codes[b, :n].cpu().numpy(), kc)
+        assert np.array_equal(cache.ikey_scales[b, :n].cpu().numpy(), ks)
+        assert not cache.lat_codes[b, n:].any()          # untouched rows stay zero
+
+
+# ---------------------------------------------------------------- whole walks on small workloads
+
+def check_walk(csa, wl, seqs, queries=None, layers=None):
+    from compressed_sparse_attention_decode_gb300.synthetic import build_step
+    step = build_step(wl, want_lse=True)
+    step.enqueue()
+    torch.cuda.synchronize()
+    for bi, b in enumerate(seqs):
+        lc, ls, kc, ks = (p.cpu().numpy()[bi] for p in (step.cache.lat_codes, step.cache.lat_scales,
+                                                          step.cache.ikey_codes, step.cache.ikey_scales))
+        ref_cache = oracle.sequence_cache(wl, b)
+        for got, want in zip((lc, ls, kc, ks), ref_cache):
+            assert np.array_equal(got, want)
+        ref = oracle.run_sequence(wl, b, cache=ref_cache, queries=queries, layers=layers)
+        qs = list(range(wl.n_q)) if queries is None else list(queries)
+        for l in ref["idx"]:
+            got = step.idx[l, bi].cpu().numpy()[qs]
+            assert np.array_equal(got, ref["idx"][l]), (wl.name, b, l)
+        for l in ref["pool"]:
+            assert np.array_equal(step.pool[bi].cpu().numpy()[qs], ref["pool"][l]), (wl.name, b, l)
+        for l in ref["out"]:
+            got = step.out[l, bi].cpu().numpy()[qs]
+            err = rel_err_rows(got, ref["out"][l])
+            assert err <= ATTN_TOL, (wl.name, b, l, err)
+            lse = step.lse[l, bi].cpu().numpy()[qs]
+            assert np.abs(lse - ref["lse"][l]).max() <= 1e-4 * max(1.0, np.abs(ref["lse"][l]).max())
+    return step
+
+
+def test_tiny_workload(csa):
+    check_walk(csa, WORKLOADS[0], [0])
+
+
+def test_decode_32k_all_sequences(csa):
+    check_walk(csa, WORKLOADS[1], list(range(WORKLOADS[1].B)))
+
+
+def test_layer_schedule_small(csa):
+    """Full (+HSI pool) -> Reindex x3 -> Reuse x3 on a small context, 3 sequences"""
+    wl = scaled(WORKLOADS[2], B=3, T=16384, layers=("full",) + ("reindex",) * 3 + ("reuse",) * 3)
+    step = check_walk(csa, wl, [0, 1, 2])
+    for l in (5, 6):
+        assert torch.equal(step.idx[l], step.idx[4])
+
+
+def test_pool_edge_cases(csa):
+    """fewer blocks than pool slots; a pool that is the whole context; k > n_elig"""
+    for T, pb, k in [(512, 256, 64), (2048 + 256, 64, 512), (4096 + 254, 16, 32)]:
+        wl = scaled(WORKLOADS[2], B=2, T=T, k=k, pool_blocks=pb, H=16,
+                    layers=("full", "reindex", "reuse"))
+        check_walk(csa, wl, [0, 1])
+
+
+def test_short_contexts_pad_with_minus_one(csa):
+    for T in (128, 130, 200, 256):
+        wl = scaled(WORKLOADS[0], T=T, k=64)
+        step = check_walk(csa, wl, [0])
+        n = wl.n_elig(T - 1)
+        idx = step.idx[0, 0, 0].cpu().numpy()
+        assert (idx[n:] == -1).all() and sorted(idx[:n].tolist()) == list(range(n))
+
+
+# ---------------------------------------------------------------- adversarial top-k
+
+def test_topk_ties_duplicates_and_zero_keys(csa):
+    n, d = 3000, 128
+    rng = np.random.default_rng(7)
+    base = synth.normal_f32(40, 1, (n, d))
+    base[1000:1500] = base[0:500]           # exact duplicates of lower rows
+    base[2000:2600] = 0.0                   # all-zero keys: score exactly 0
+    kc, ks = oracle.quantize_rows(base)
+    lat = oracle.quantize_rows(synth.normal_f32(40, 2, (n, 512)))
+    planes = [a[None] for a in (lat[0], lat[1], kc, ks)]
+    cache = host_cache(csa, planes, d)
+    iq = synth.normal_f32(40, 3, (1, 1, 8, d))
+    w = synth.uniform_f32(40, 4, (1, 1, 8), 0.0, 1.0)
+    for wv in (w, np.zeros_like(w)):        # zero head weights: every score ties at 0
+        qc, qs = oracle.quantize_rows(iq)
+        p = n * 2 + 127
+        for k in (512, 2048):
+            idx, _ = csa.csa2_indexer_topk(cache, torch.from_numpy(qc).cuda(), torch.from_numpy(qs).cuda(),
+                                           torch.from_numpy(wv).cuda(),
+                                           torch.tensor([[p]], dtype=torch.int64).cuda(), k)
+            S = oracle.index_scores(kc, ks, qc[0, 0], qs[0, 0], wv[0, 0], n=n)
+            assert np.array_equal(idx.cpu().numpy()[0, 0], oracle.topk(S, k))
+
+
+def test_reindex_pool_with_holes_and_reuse(csa):
+    n, d = 5000, 128
+    lat = oracle.quantize_rows(synth.normal_f32(41, 2, (n, 512)))
+    kc, ks = oracle.quantize_rows(synth.normal_f32(41, 1, (n, d)))
+    cache = host_cache(csa, [a[None] for a in (lat[0], lat[1], kc, ks)], d)
+    pool = np.full((1, 1, 2048), -1, np.int32)
+    ids = np.sort(np.random.default_rng(3).choice(n, 1500, replace=False)).astype(np.int32)
+    pool[0, 0, :1500] = ids
+    iq = synth.normal_f32(41, 3, (1, 1, 8, d))
+    w = synth.uniform_f32(41, 4, (1, 1, 8), 0.0, 1.0)
+    qc, qs = oracle.quantize_rows(iq)
+    for k in (512, 1500, 2000):
+        idx = csa.csa2_reindex(csa.REINDEX, cache, k, torch.from_numpy(qc).cuda(), torch.from_numpy(qs).cuda(),
+                               torch.from_numpy(w).cuda(), torch.from_numpy(pool).cuda())
+        S = oracle.index_scores(kc, ks, qc[0, 0], qs[0, 0], w[0, 0], ids=pool[0, 0])
+        want = oracle.topk(S, k, ids=pool[0, 0])
+        assert np.array_equal(idx.cpu().numpy()[0, 0], want)
+        again = csa.csa2_reindex(csa.REUSE, cache, k, prev_idx=idx)
+        assert torch.equal(again, idx)
+
+
+def test_attention_window_clipping_and_empty_selection(csa):
+    wl = WORKLOADS[0]
+    lc, ls, kc, ks = oracle.sequence_cache(wl, 0)
+    cache = host_cache(csa, [a[None] for a in (lc, ls, kc, ks)], wl.d_I)
+    q = wl.q(0, 0)
+    win = wl.window(0, 0)
+    p = wl.T - 1
+    for k_valid, clip in [(0, 0), (10, 0), (64, 100), (0, 127)]:
+        idx = np.full((1, 1, 64), -1, np.int32)
+        idx[0, 0, :k_valid] = np.arange(0, 3 * k_valid, 3)
+        swa = win[clip:]
+        out, lse = csa.csa2_sparse_attn(cache, bf16_t(q[None]), torch.tensor([[p]], dtype=torch.int64).cuda(),
+                                        torch.from_numpy(idx).cuda(), bf16_t(swa[None]), wl.T - 128 + clip,
+                                        want_lse=True)
+        ro, rl = oracle.sparse_attention(q[0], idx[0, 0], lc, ls, swa)
+        assert rel_err_rows(out.cpu().numpy()[0, 0], ro) <= ATTN_TOL
+        assert np.abs(lse.cpu().numpy()[0, 0] - rl).max() < 1e-4 * max(1, np.abs(rl).max())
+
+
+# ---------------------------------------------------------------- full sizes, sampled outputs
+
+def test_decode_128k_20_layers_full_size_sampled(csa):
+    """the benchmark's workload and launch configuration (one CUDA graph per
+    step), checked on three sequences across all 20 layers"""
+    from compressed_sparse_attention_decode_gb300.synthetic import build_step
+    wl = WORKLOADS[2]
+    step = build_step(wl)
+    step.capture()
+    step.run()
+    step.run()
+    torch.cuda.synchronize()
+    for b in (0, 37, 63):
+        ref = oracle.run_sequence(wl, b)
+        for l in range(len(wl.layers)):
+            assert np.array_equal(step.idx[l, b].cpu().numpy(), ref["idx"][l]), (b, l)
+            err = rel_err_rows(step.out[l, b].cpu().numpy(), ref["out"][l])
+            assert err <= ATTN_TOL, (b, l, err)
+        assert np.array_equal(step.pool[b].cpu().numpy(), ref["pool"][0])
+
+
+def test_decode_1m_full_size_sampled(csa):
+    from compressed_sparse_attention_decode_gb300.synthetic import build_step
+    wl = WORKLOADS[3]
+    step = build_step(wl)
+    step.enqueue()
+    torch.cuda.synchronize()
+    for b in (0, 3):
+        ref = oracle.run_sequence(wl, b)
+        assert np.array_equal(step.idx[0, b].cpu().numpy(), ref["idx"][0])
+        assert rel_err_rows(step.out[0, b].cpu().numpy(), ref["out"][0]) <= ATTN_TOL
+
+
+def test_chunked_prefill_full_size_sampled(csa):
+    """cache write of the 8,192-position chunk plus per-query causal top-512
+    and attention; queries checked: every 64th plus the first and the last"""
+    from compressed_sparse_attention_decode_gb300.synthetic import build_step
+    wl = WORKLOADS[4]
+    step = build_step(wl)
+    step.enqueue()
+    torch.cuda.synchronize()
+    ref_cache = oracle.sequence_cache(wl, 0)
+    for got, want in zip((step.cache.lat_codes, step.cache.lat_scales, step.cache.ikey_codes,
+                          step.cache.ikey_scales), ref_cache):
+        assert np.array_equal(got[0].cpu().numpy(), want)
+    qs = sorted(set(list(range(0, wl.n_q, 64)) + [1, wl.n_q - 1]))
+    ref = oracle.run_sequence(wl, 0, cache=ref_cache, queries=qs)
+    assert np.array_equal(step.idx[0, 0].cpu().numpy()[qs], ref["idx"][0])
+    assert rel_err_rows(step.out[0, 0].cpu().numpy()[qs], ref["out"][0]) <= ATTN_TOL
