@@ -150,11 +150,21 @@ cudaError_t launch_sparse_attn_simt(const csa2_cache& c, const uint16_t* q, int 
 
 namespace csa2 {
 
-size_t sparse_attn_ws(int, int, int, int) { return 0; }
+bool attn_tc_supported(int H);
+size_t attn_tc_ws(int batch, int n_q, int H, int k);
+cudaError_t launch_sparse_attn_tc(const csa2_cache& c, const uint16_t* q, int n_q, int H, const int64_t* q_pos,
+                                  const int32_t* idx, int k, const uint16_t* swa, int64_t swa_pos0, int swa_len,
+                                  float scale, float* out, float* lse, void* ws, cudaStream_t st);
 
+size_t sparse_attn_ws(int batch, int n_q, int H, int k) { return attn_tc_supported(H) ? attn_tc_ws(batch, n_q, H, k) : 0; }
+
+// tensor-core kernel for head counts it tiles (multiples of 16 up to 64, or of
+// 64 up to 128); the CUDA-core kernel otherwise
 cudaError_t launch_sparse_attn(const csa2_cache& c, const uint16_t* q, int n_q, int H, const int64_t* q_pos,
                                const int32_t* idx, int k, const uint16_t* swa, int64_t swa_pos0, int swa_len,
-                               float scale, float* out, float* lse, void*, size_t, cudaStream_t st) {
+                               float scale, float* out, float* lse, void* ws, size_t, cudaStream_t st) {
+    if (attn_tc_supported(H))
+        return launch_sparse_attn_tc(c, q, n_q, H, q_pos, idx, k, swa, swa_pos0, swa_len, scale, out, lse, ws, st);
     return launch_sparse_attn_simt(c, q, n_q, H, q_pos, idx, k, swa, swa_pos0, swa_len, scale, out, lse, st);
 }
 
