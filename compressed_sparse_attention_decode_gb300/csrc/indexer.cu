@@ -126,45 +126,208 @@ __device__ __forceinline__ int n_elig_of(int64_t p, int capacity) {
 
 __host__ __device__ inline float bound_factor(int H, int DI) { return 2.0f * (float)(2 * H + DI / 16 + 8) * 0x1p-24f; }
 
+// ---------------------------------------------------------------- block-wide radix selection
+
+struct RadixSmem {
+    int hist[256];
+    int ctl[8];   // [0] append counter, [1] digit, [2] krem, [3] scratch
+};
+
+// k-th largest key (1 <= k <= number of taking items) over items t in [0, n):
+// getkey(t, key) returns false for items that do not take part.  Returns the
+// key and sets *krem to how many items equal to it are needed.  Lanes with the
+// same digit are merged (match.any) before the shared-memory atomic, so heavy
+// ties do not serialise.
+template <typename KeyT, typename Get>
+__device__ KeyT block_kth_largest(Get getkey, int n, int k, RadixSmem& rs, int* krem_out) {
+    constexpr int BITS = sizeof(KeyT) * 8;
+    const int lane = threadIdx.x & 31;
+    KeyT prefix = 0, mask = 0;
+    int krem = k;
+    for (int shift = BITS - 8; shift >= 0; shift -= 8) {
+        for (int i = threadIdx.x; i < 256; i += blockDim.x) rs.hist[i] = 0;
+        __syncthreads();
+        for (int base = 0; base < n; base += blockDim.x) {
+            const int t = base + threadIdx.x;
+            KeyT key = 0;
+            int bin = -1;
+            if (t < n && getkey(t, key) && (key & mask) == prefix) bin = (int)((key >> shift) & 255);
+            const unsigned peers = __match_any_sync(0xffffffffu, bin);
+            if (bin >= 0 && lane == __ffs(peers) - 1) atomicAdd(&rs.hist[bin], __popc(peers));
+        }
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            int c = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) c += rs.hist[255 - 8 * lane - i];   // lane 0 holds the top bins
+            int incl = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const unsigned hit = __ballot_sync(0xffffffffu, incl >= krem);
+            const int L = __ffs(hit) - 1;
+            if (lane == L) {
+                int cum = incl - c;
+                for (int i = 0; i < 8; ++i) {
+                    const int d = 255 - 8 * lane - i;
+                    if (cum + rs.hist[d] >= krem) {
+                        rs.ctl[1] = d;
+                        rs.ctl[2] = krem - cum;
+                        break;
+                    }
+                    cum += rs.hist[d];
+                }
+            }
+        }
+        __syncthreads();
+        prefix |= (KeyT)rs.ctl[1] << shift;
+        mask |= (KeyT)255 << shift;
+        krem = rs.ctl[2];
+        __syncthreads();
+    }
+    *krem_out = krem;
+    return prefix;
+}
+
+// warp-aggregated append to a list whose counter lives at *ctr (shared or global)
+__device__ __forceinline__ int append_slot(bool flag, int* ctr) {
+    const unsigned m = __ballot_sync(0xffffffffu, flag);
+    if (!m) return -1;
+    const int lane = threadIdx.x & 31, leader = __ffs(m) - 1;
+    int base = 0;
+    if (lane == leader) base = atomicAdd(ctr, __popc(m));
+    base = __shfl_sync(0xffffffffu, base, leader);
+    return flag ? base + __popc(m & ((1u << lane) - 1u)) : -1;
+}
+
 // ---------------------------------------------------------------- scans
 
-// Full scan: entries [0, n_elig) of each query; QB queries share one key load.
+// Full scan with local selection.  One block per (sequence, QB queries,
+// chunk of E entries): the (S~-E, S~+E) bounds of the chunk stay in shared
+// memory; for each query the block finds the chunk's k-th largest lower bound
+// and forwards every entry whose upper bound reaches it (the global k-th
+// lower bound is never smaller, so nothing the exact top-k needs is dropped),
+// and likewise for HSI blocks (bounds = max of member bounds; the newest
+// block, always kept, is not forwarded).
 template <int DI>
 __global__ void __launch_bounds__(256) k_scan_full(const uint8_t* __restrict__ kc_all, const uint8_t* __restrict__ ks_all,
                                                    int capacity, const uint8_t* __restrict__ iq_codes,
                                                    const uint8_t* __restrict__ iq_scales, const float* __restrict__ w_head,
                                                    const int64_t* __restrict__ q_pos, int n_q, int q0, int n_qc, int H,
-                                                   int QB, float2* __restrict__ lu) {
+                                                   int QB, int E, int k, int pool_blocks, int bs,
+                                                   int* __restrict__ counts, int* __restrict__ cid,
+                                                   float2* __restrict__ clu, int* __restrict__ bid,
+                                                   float2* __restrict__ blu, int list_len) {
     extern __shared__ int smem[];
+    __shared__ RadixSmem rs;
     const int b = blockIdx.z;
     const int qa = blockIdx.y * QB;
     const int nqb = min(QB, n_qc - qa);
     const int words = QView<DI>::words(H);
     int* nel = smem;
+    float2* slu = reinterpret_cast<float2*>(smem + 32 + QB * words);
     for (int t = 0; t < nqb; ++t) {
         QView<DI> v;
         v.bind(smem + 32 + t * words, H);
-        int64_t gq = (int64_t)b * n_q + q0 + qa + t;
+        const int64_t gq = (int64_t)b * n_q + q0 + qa + t;
         stage_query<DI>(v, iq_codes + gq * H * (DI / 2), iq_scales + gq * H * (DI / 16), w_head + gq * H, H,
                         threadIdx.x, blockDim.x);
         if (threadIdx.x == 0) nel[t] = n_elig_of(q_pos[gq], capacity);
     }
     __syncthreads();
-    const int j = blockIdx.x * blockDim.x + threadIdx.x;
+    const int c0 = blockIdx.x * E;
     int maxn = 0;
     for (int t = 0; t < nqb; ++t) maxn = max(maxn, nel[t]);
-    if (j >= maxn) return;
-    KeyRow<DI> k;
-    const int64_t row = (int64_t)b * capacity + j;
-    k.load(kc_all + row * (DI / 2), ks_all + row * (DI / 16));
+    if (c0 >= maxn) return;                       // uniform over the block
     const float fac = bound_factor(H, DI);
+    for (int i = threadIdx.x; i < E; i += blockDim.x) {
+        const int j = c0 + i;
+        if (j < maxn) {
+            KeyRow<DI> kr;
+            const int64_t row = (int64_t)b * capacity + j;
+            kr.load(kc_all + row * (DI / 2), ks_all + row * (DI / 16));
+            for (int t = 0; t < nqb; ++t) {
+                float L = -INFINITY, U = -INFINITY;
+                if (j < nel[t]) {
+                    QView<DI> v;
+                    v.bind(smem + 32 + t * words, H);
+                    approx_score<DI>(kr, v, H, fac, L, U);
+                }
+                slu[t * E + i] = make_float2(L, U);
+            }
+        } else {
+            for (int t = 0; t < nqb; ++t) slu[t * E + i] = make_float2(-INFINITY, -INFINITY);
+        }
+    }
+    __syncthreads();
     for (int t = 0; t < nqb; ++t) {
-        if (j >= nel[t]) continue;
-        QView<DI> v;
-        v.bind(smem + 32 + t * words, H);
-        float L, U;
-        approx_score<DI>(k, v, H, fac, L, U);
-        lu[((int64_t)b * n_qc + qa + t) * capacity + j] = make_float2(L, U);
+        const int n_loc = min(max(nel[t] - c0, 0), E);
+        if (n_loc == 0) continue;                 // uniform
+        const int64_t slab = (int64_t)b * n_qc + qa + t;
+        const float2* lu = slu + t * E;
+        unsigned int lam = 0u;
+        if (n_loc > k) {
+            int krem;
+            lam = block_kth_largest<unsigned int>(
+                [&](int i, unsigned int& key) {
+                    key = f32_key(lu[i].x);
+                    return true;
+                },
+                n_loc, k, rs, &krem);
+        }
+        for (int base = 0; base < n_loc; base += blockDim.x) {
+            const int i = base + threadIdx.x;
+            const bool f = i < n_loc && f32_key(lu[i].y) >= lam;
+            const int pos = append_slot(f, counts + 2 * slab);
+            if (f) {
+                cid[slab * list_len + pos] = c0 + i;
+                clu[slab * list_len + pos] = lu[i];
+            }
+        }
+        if (pool_blocks > 1) {
+            const int nb = (nel[t] + bs - 1) / bs;          // blocks of this query
+            const int forced = nb - 1;
+            const int g0 = c0 / bs;                          // first block of the chunk (E is a multiple of bs)
+            const int nbl = min(E / bs, nb - g0);            // blocks of this chunk that exist
+            const int nvalid = nbl - ((forced >= g0 && forced < g0 + nbl) ? 1 : 0);
+            if (nb > pool_blocks && nvalid > 0) {
+                auto blk = [&](int bl, bool upper) {
+                    float mx = -INFINITY;
+                    for (int i = 0; i < bs; ++i) {
+                        const int e = bl * bs + i;
+                        if (e < n_loc) mx = fmaxf(mx, upper ? lu[e].y : lu[e].x);
+                    }
+                    return mx;
+                };
+                unsigned int lamb = 0u;
+                if (nvalid > pool_blocks - 1) {
+                    int krem;
+                    lamb = block_kth_largest<unsigned int>(
+                        [&](int bl, unsigned int& key) {
+                            key = f32_key(blk(bl, false));
+                            return g0 + bl != forced;
+                        },
+                        nbl, pool_blocks - 1, rs, &krem);
+                }
+                for (int base = 0; base < nbl; base += blockDim.x) {
+                    const int bl = base + threadIdx.x;
+                    float2 m2 = make_float2(-INFINITY, -INFINITY);
+                    bool f = false;
+                    if (bl < nbl && g0 + bl != forced) {
+                        m2 = make_float2(blk(bl, false), blk(bl, true));
+                        f = f32_key(m2.y) >= lamb;
+                    }
+                    const int pos = append_slot(f, counts + 2 * slab + 1);
+                    if (f) {
+                        bid[slab * list_len + pos] = g0 + bl;
+                        blu[slab * list_len + pos] = m2;
+                    }
+                }
+            }
+        }
+        __syncthreads();
     }
 }
 
@@ -188,86 +351,21 @@ __global__ void __launch_bounds__(256) k_scan_pool(const uint8_t* __restrict__ k
     const int j = pool[gq * pool_len + t];
     float L = -INFINITY, U = -INFINITY;
     if (j >= 0 && j < capacity) {
-        KeyRow<DI> k;
+        KeyRow<DI> kr;
         const int64_t row = (int64_t)b * capacity + j;
-        k.load(kc_all + row * (DI / 2), ks_all + row * (DI / 16));
-        approx_score<DI>(k, v, H, bound_factor(H, DI), L, U);
+        kr.load(kc_all + row * (DI / 2), ks_all + row * (DI / 16));
+        approx_score<DI>(kr, v, H, bound_factor(H, DI), L, U);
     }
     lu[gq * pool_len + t] = make_float2(L, U);
 }
 
-// ---------------------------------------------------------------- block-wide selection helpers
+// ---------------------------------------------------------------- exact selection
 
 struct SelectSmem {
-    int hist[256];
-    int ctl[8];               // [0] counter, [1] digit, [2] krem, [3] misc
+    RadixSmem rs;
     unsigned long long key[MAX_K];
     int id[MAX_K];
 };
-
-// k-th largest key (k >= 1, at least k valid items) over items t in [0, n):
-// getkey(t, key) returns false for items that do not take part.  Returns the
-// key value and leaves in *krem how many items equal to it are needed.
-template <typename KeyT, typename Get>
-__device__ KeyT block_kth_largest(Get getkey, int n, int k, SelectSmem& sm, int* krem_out) {
-    constexpr int BITS = sizeof(KeyT) * 8;
-    KeyT prefix = 0, mask = 0;
-    int krem = k;
-    for (int shift = BITS - 8; shift >= 0; shift -= 8) {
-        for (int i = threadIdx.x; i < 256; i += blockDim.x) sm.hist[i] = 0;
-        __syncthreads();
-        for (int t = threadIdx.x; t < n; t += blockDim.x) {
-            KeyT key;
-            if (getkey(t, key) && (key & mask) == prefix) atomicAdd(&sm.hist[(int)((key >> shift) & 255)], 1);
-        }
-        __syncthreads();
-        if (threadIdx.x < 32) {
-            const int lane = threadIdx.x;
-            int c = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) c += sm.hist[255 - 8 * lane - i];   // lane 0 holds the top bins
-            int incl = c;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                int y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            unsigned hit = __ballot_sync(0xffffffffu, incl >= krem);
-            int L = __ffs(hit) - 1;
-            if (lane == L) {
-                int cum = incl - c;
-                for (int i = 0; i < 8; ++i) {
-                    int d = 255 - 8 * lane - i;
-                    if (cum + sm.hist[d] >= krem) {
-                        sm.ctl[1] = d;
-                        sm.ctl[2] = krem - cum;
-                        break;
-                    }
-                    cum += sm.hist[d];
-                }
-            }
-        }
-        __syncthreads();
-        prefix |= (KeyT)sm.ctl[1] << shift;
-        mask |= (KeyT)255 << shift;
-        krem = sm.ctl[2];
-        __syncthreads();
-    }
-    *krem_out = krem;
-    return prefix;
-}
-
-// warp-aggregated append of the flagged items to list[], counter in sm.ctl[0]
-__device__ __forceinline__ void append_flagged(bool flag, int value, int* list, SelectSmem& sm) {
-    unsigned m = __ballot_sync(0xffffffffu, flag);
-    if (!m) return;
-    int lane = threadIdx.x & 31;
-    int leader = __ffs(m) - 1;
-    int base = 0;
-    if (lane == leader) base = atomicAdd(&sm.ctl[0], __popc(m));
-    base = __shfl_sync(0xffffffffu, base, leader);
-    if (flag) list[base + __popc(m & ((1u << lane) - 1u))] = value;
-}
 
 // Among m candidates (cid[t], ckey[t]) keep the k best by (key desc, id asc):
 // the kept ones end up in sm.key/sm.id[0..kept), unordered.  Returns kept.
@@ -281,32 +379,28 @@ __device__ int keep_best(const int* cid, const unsigned long long* ckey, int m, 
         return m;
     }
     int krem;
-    unsigned long long kth = block_kth_largest<unsigned long long>(
+    const unsigned long long kth = block_kth_largest<unsigned long long>(
         [&](int t, unsigned long long& key) {
             key = ckey[t];
             return true;
         },
-        m, k, sm, &krem);
+        m, k, sm.rs, &krem);
     // among the ties with key == kth keep the krem lowest ids
     int krem2;
-    unsigned int idcut = block_kth_largest<unsigned int>(
+    const unsigned int idcut = block_kth_largest<unsigned int>(
         [&](int t, unsigned int& key) {
             key = ~(unsigned int)cid[t];
             return ckey[t] == kth;
         },
-        m, krem, sm, &krem2);
-    if (threadIdx.x == 0) sm.ctl[0] = 0;
+        m, krem, sm.rs, &krem2);
+    if (threadIdx.x == 0) sm.rs.ctl[0] = 0;
     __syncthreads();
     for (int base = 0; base < m; base += blockDim.x) {
-        int t = base + threadIdx.x;
+        const int t = base + threadIdx.x;
         bool take = false;
         if (t < m) take = ckey[t] > kth || (ckey[t] == kth && ~(unsigned int)cid[t] >= idcut);
-        unsigned msk = __ballot_sync(0xffffffffu, take);
-        int lane = threadIdx.x & 31, leader = msk ? __ffs(msk) - 1 : 0, pos = 0;
-        if (msk && lane == leader) pos = atomicAdd(&sm.ctl[0], __popc(msk));
-        pos = __shfl_sync(0xffffffffu, pos, leader);
+        const int slot = append_slot(take, &sm.rs.ctl[0]);
         if (take) {
-            int slot = pos + __popc(msk & ((1u << lane) - 1u));
             sm.key[slot] = ckey[t];
             sm.id[slot] = cid[t];
         }
@@ -328,13 +422,12 @@ __device__ void sort_kept(int n, bool desc_by_key, SelectSmem& sm) {
     for (int size = 2; size <= N; size <<= 1) {
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
             for (int t = threadIdx.x; t < N / 2; t += blockDim.x) {
-                int i = 2 * t - (t & (stride - 1));
-                int j = i + stride;
-                bool up = ((i & size) == 0);
-                unsigned long long ki = sm.key[i], kj = sm.key[j];
-                int ii = sm.id[i], ij = sm.id[j];
-                // "i before j" in the target order
-                bool i_first = desc_by_key ? (ki > kj || (ki == kj && ii < ij)) : (ii < ij);
+                const int i = 2 * t - (t & (stride - 1));
+                const int j = i + stride;
+                const bool up = ((i & size) == 0);
+                const unsigned long long ki = sm.key[i], kj = sm.key[j];
+                const int ii = sm.id[i], ij = sm.id[j];
+                const bool i_first = desc_by_key ? (ki > kj || (ki == kj && ii < ij)) : (ii < ij);
                 if (i_first != up) {
                     sm.key[i] = kj;
                     sm.key[j] = ki;
@@ -347,21 +440,21 @@ __device__ void sort_kept(int n, bool desc_by_key, SelectSmem& sm) {
     }
 }
 
-// ---------------------------------------------------------------- selection kernel
-
-// One block per (sequence, query).  Items t in [0, n_items): for Full the
-// entries 0..n_elig-1 (ids == nullptr), for Reindex the pool slots (entry id
-// ids[t], -1 = empty).  lu holds (S~-E, S~+E) per item.
+// One block per (sequence, query).  Items t in [0, n): entry ids[t] (-1 =
+// empty) with bounds lu[t]; n is *count (Full: the forwarded candidates) or
+// n_fixed (Reindex: the pool slots).  Keeps the exact top k; with HSI (Full
+// only) also builds the pool from the forwarded block candidates.
 template <int DI>
-__global__ void __launch_bounds__(512) k_select(const float2* __restrict__ lu, int lu_stride,
-                                                 const int32_t* __restrict__ ids, int n_items_fixed,
-                                                 const uint8_t* __restrict__ kc_all, const uint8_t* __restrict__ ks_all,
-                                                 int capacity, const uint8_t* __restrict__ iq_codes,
-                                                 const uint8_t* __restrict__ iq_scales,
-                                                 const float* __restrict__ w_head, const int64_t* __restrict__ q_pos,
-                                                 int n_q, int q0, int n_qc, int H, int k, int32_t* __restrict__ idx_out,
-                                                 int pool_blocks, int bs, int32_t* __restrict__ pool_out,
-                                                 int* __restrict__ cand_id_ws, unsigned long long* __restrict__ cand_key_ws) {
+__global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids, const float2* __restrict__ lu,
+                                                const int* __restrict__ counts, int n_fixed, int list_len,
+                                                const uint8_t* __restrict__ kc_all, const uint8_t* __restrict__ ks_all,
+                                                int capacity, const uint8_t* __restrict__ iq_codes,
+                                                const uint8_t* __restrict__ iq_scales, const float* __restrict__ w_head,
+                                                const int64_t* __restrict__ q_pos, int n_q, int q0, int n_qc, int H,
+                                                int k, int32_t* __restrict__ idx_out, int pool_blocks, int bs,
+                                                int32_t* __restrict__ pool_out, const int32_t* __restrict__ bid,
+                                                const float2* __restrict__ blu, int* __restrict__ c2id,
+                                                unsigned long long* __restrict__ c2key) {
     extern __shared__ int qsm[];
     __shared__ SelectSmem sm;
     const int b = blockIdx.y, ql = blockIdx.x;
@@ -371,36 +464,31 @@ __global__ void __launch_bounds__(512) k_select(const float2* __restrict__ lu, i
     v.bind(qsm, H);
     stage_query<DI>(v, iq_codes + gq * H * (DI / 2), iq_scales + gq * H * (DI / 16), w_head + gq * H, H, threadIdx.x,
                     blockDim.x);
-    const float2* L = lu + slab * lu_stride;
-    const int32_t* id = ids ? ids + gq * lu_stride : nullptr;
-    const int n_items = ids ? n_items_fixed : n_elig_of(q_pos[gq], capacity);
-    int* cid = cand_id_ws + slab * lu_stride;
-    unsigned long long* ckey = cand_key_ws + slab * lu_stride;
+    const int32_t* id = ids + slab * list_len;
+    const float2* L = lu + slab * list_len;
+    const int n = counts ? counts[2 * slab] : n_fixed;
+    int* cid = c2id + slab * list_len;
+    unsigned long long* ckey = c2key + slab * list_len;
     const uint8_t* kc = kc_all + (int64_t)b * capacity * (DI / 2);
     const uint8_t* ks = ks_all + (int64_t)b * capacity * (DI / 16);
     auto entry_of = [&](int t) -> int {
-        if (!id) return t;
-        int j = id[t];
+        const int j = id[t];
         return (j >= 0 && j < capacity) ? j : -1;
     };
     if (threadIdx.x == 0) {
-        sm.ctl[0] = 0;
-        sm.ctl[3] = 0;
+        sm.rs.ctl[0] = 0;
+        sm.rs.ctl[3] = 0;
     }
     __syncthreads();
 
-    // ---- 1. lower bound of the k-th best, candidates whose upper bound reaches it
-    int n_valid = n_items;
-    if (id) {
-        // count non-empty slots
-        int c = 0;
-        for (int t = threadIdx.x; t < n_items; t += blockDim.x) c += entry_of(t) >= 0;
-        c = __reduce_add_sync(0xffffffffu, c);
-        if ((threadIdx.x & 31) == 0) atomicAdd(&sm.ctl[3], c);
-        __syncthreads();
-        n_valid = sm.ctl[3];
-        __syncthreads();
-    }
+    // ---- 1. k-th largest lower bound, candidates whose upper bound reaches it
+    int c = 0;
+    for (int t = threadIdx.x; t < n; t += blockDim.x) c += entry_of(t) >= 0;
+    c = __reduce_add_sync(0xffffffffu, c);
+    if ((threadIdx.x & 31) == 0) atomicAdd(&sm.rs.ctl[3], c);
+    __syncthreads();
+    const int n_valid = sm.rs.ctl[3];
+    __syncthreads();
     unsigned int lam = 0u;
     if (n_valid > k) {
         int krem;
@@ -409,38 +497,38 @@ __global__ void __launch_bounds__(512) k_select(const float2* __restrict__ lu, i
                 key = f32_key(L[t].x);
                 return entry_of(t) >= 0;
             },
-            n_items, k, sm, &krem);
+            n, k, sm.rs, &krem);
     }
-    if (threadIdx.x == 0) sm.ctl[0] = 0;
+    if (threadIdx.x == 0) sm.rs.ctl[0] = 0;
     __syncthreads();
-    for (int base = 0; base < n_items; base += blockDim.x) {
-        int t = base + threadIdx.x;
-        bool f = t < n_items && entry_of(t) >= 0 && f32_key(L[t].y) >= lam;
-        append_flagged(f, t, cid, sm);
+    for (int base = 0; base < n; base += blockDim.x) {
+        const int t = base + threadIdx.x;
+        const bool f = t < n && entry_of(t) >= 0 && f32_key(L[t].y) >= lam;
+        const int pos = append_slot(f, &sm.rs.ctl[0]);
+        if (f) cid[pos] = entry_of(t);
     }
     __syncthreads();
-    int m = sm.ctl[0];
+    const int m = sm.rs.ctl[0];
     __syncthreads();
     // ---- 2. exact scores of the candidates
     for (int t = threadIdx.x; t < m; t += blockDim.x) {
-        int j = entry_of(cid[t]);
-        double S = exact_score<DI>(kc + (int64_t)j * (DI / 2), ks + (int64_t)j * (DI / 16), v, H);
-        ckey[t] = f64_key(S);
-        cid[t] = j;     // from here on candidates carry entry ids
+        const int j = cid[t];
+        ckey[t] = f64_key(exact_score<DI>(kc + (int64_t)j * (DI / 2), ks + (int64_t)j * (DI / 16), v, H));
     }
     __syncthreads();
     // ---- 3. the k best, in rank order
-    int kept = keep_best(cid, ckey, m, k, sm);
+    const int kept = keep_best(cid, ckey, m, k, sm);
     sort_kept(kept, true, sm);
     int32_t* out = idx_out + gq * k;
     for (int t = threadIdx.x; t < k; t += blockDim.x) out[t] = t < kept ? sm.id[t] : -1;
     __syncthreads();
 
     // ---- 4. HSI candidate pool (Full only)
-    if (pool_blocks <= 0 || ids) return;
+    if (pool_blocks <= 0 || !counts) return;
+    const int n_elig = n_elig_of(q_pos[gq], capacity);
     const int P = pool_blocks * bs;
     int32_t* pout = pool_out + gq * P;
-    const int nb = (n_items + bs - 1) / bs;
+    const int nb = (n_elig + bs - 1) / bs;
     int nsel;
     if (nb <= pool_blocks) {                 // every block fits
         for (int t = threadIdx.x; t < nb; t += blockDim.x) sm.id[t] = t;
@@ -451,41 +539,38 @@ __global__ void __launch_bounds__(512) k_select(const float2* __restrict__ lu, i
         nsel = 1;
         __syncthreads();
     } else {
-        const int others = nb - 1;        // block nb-1 holds entry n_elig-1: forced in
-        auto blk_lu = [&](int blk, bool upper) {
-            float mx = -INFINITY;
-            for (int i = 0; i < bs; ++i) {
-                int j = blk * bs + i;
-                if (j < n_items) mx = fmaxf(mx, upper ? L[j].y : L[j].x);
-            }
-            return mx;
-        };
+        const int mb = counts[2 * slab + 1];
+        const int32_t* bi = bid + slab * list_len;
+        const float2* bl = blu + slab * list_len;
         int krem;
-        unsigned int lamb = block_kth_largest<unsigned int>(
-            [&](int t, unsigned int& key) {
-                key = f32_key(blk_lu(t, false));
-                return true;
-            },
-            others, pool_blocks - 1, sm, &krem);
-        if (threadIdx.x == 0) sm.ctl[0] = 0;
+        unsigned int lamb = 0u;
+        if (mb > pool_blocks - 1)
+            lamb = block_kth_largest<unsigned int>(
+                [&](int t, unsigned int& key) {
+                    key = f32_key(bl[t].x);
+                    return true;
+                },
+                mb, pool_blocks - 1, sm.rs, &krem);
+        if (threadIdx.x == 0) sm.rs.ctl[0] = 0;
         __syncthreads();
-        for (int base = 0; base < others; base += blockDim.x) {
-            int t = base + threadIdx.x;
-            bool f = t < others && f32_key(blk_lu(t, true)) >= lamb;
-            append_flagged(f, t, cid, sm);
+        for (int base = 0; base < mb; base += blockDim.x) {
+            const int t = base + threadIdx.x;
+            const bool f = t < mb && f32_key(bl[t].y) >= lamb;
+            const int pos = append_slot(f, &sm.rs.ctl[0]);
+            if (f) cid[pos] = bi[t];
         }
         __syncthreads();
-        int mb = sm.ctl[0];
+        const int mc = sm.rs.ctl[0];
         __syncthreads();
-        for (int t = threadIdx.x; t < mb; t += blockDim.x) ckey[t] = 0ull;
+        for (int t = threadIdx.x; t < mc; t += blockDim.x) ckey[t] = 0ull;
         __syncthreads();
-        for (int u = threadIdx.x; u < mb * bs; u += blockDim.x) {
-            int t = u / bs, j = cid[t] * bs + u % bs;
-            double S = exact_score<DI>(kc + (int64_t)j * (DI / 2), ks + (int64_t)j * (DI / 16), v, H);
+        for (int u = threadIdx.x; u < mc * bs; u += blockDim.x) {
+            const int t = u / bs, j = cid[t] * bs + u % bs;
+            const double S = exact_score<DI>(kc + (int64_t)j * (DI / 2), ks + (int64_t)j * (DI / 16), v, H);
             atomicMax(&ckey[t], f64_key(S));
         }
         __syncthreads();
-        keep_best(cid, ckey, mb, pool_blocks - 1, sm);
+        keep_best(cid, ckey, mc, pool_blocks - 1, sm);
         if (threadIdx.x == 0) {
             sm.id[pool_blocks - 1] = nb - 1;
             sm.key[pool_blocks - 1] = 0ull;
@@ -495,51 +580,96 @@ __global__ void __launch_bounds__(512) k_select(const float2* __restrict__ lu, i
     }
     sort_kept(nsel, false, sm);
     for (int u = threadIdx.x; u < P; u += blockDim.x) {
-        int t = u / bs;
-        int j = t < nsel ? sm.id[t] * bs + u % bs : -1;
-        // only the last kept block can run past n_elig; its tail slots are empty
-        pout[u] = (j >= 0 && j < n_items) ? j : -1;
+        const int t = u / bs;
+        const int j = t < nsel ? sm.id[t] * bs + u % bs : -1;
+        // only the newest block can run past n_elig; it has the largest id and sorts last
+        pout[u] = (j >= 0 && j < n_elig) ? j : -1;
     }
-    // move the -1 slots of a partial last block to the end: they are already
-    // there, because the partial block has the largest id and sorts last
 }
 
 // Reuse: the latest indices, unchanged ("DeepSeek-v4.1 Flash" §2.3.2)
 __global__ void k_copy_idx(const int32_t* __restrict__ src, int32_t* __restrict__ dst, int64_t n) {
-    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i < n) dst[i] = src[i];
 }
 
 // ---------------------------------------------------------------- launchers
 
-constexpr int SCAN_QB = 8;
-constexpr int QUERY_CHUNK = 256;
+constexpr int QUERY_CHUNK = 128;
 
-size_t select_ws_per_item() { return sizeof(float2) + sizeof(int) + sizeof(unsigned long long); }
+// workspace of one query slab with item lists of length n:
+// counts (2 ints, padded to 16 B) | ids n | lu n | c2id n | c2key n | bid n | blu n
+static size_t slab_bytes(int64_t n) { return (size_t)n * (4 + 8 + 4 + 8 + 4 + 8); }
+
+struct SelectWs {
+    int* counts;
+    int32_t* ids;
+    float2* lu;
+    int* c2id;
+    unsigned long long* c2key;
+    int32_t* bid;
+    float2* blu;
+};
+
+static SelectWs carve(void* ws, int64_t slabs, int64_t n) {
+    uint8_t* p = reinterpret_cast<uint8_t*>(ws);
+    SelectWs w;
+    w.counts = reinterpret_cast<int*>(p);
+    p += ((slabs * 2 * sizeof(int) + 255) / 256) * 256;
+    w.c2key = reinterpret_cast<unsigned long long*>(p);
+    p += slabs * n * 8;
+    w.lu = reinterpret_cast<float2*>(p);
+    p += slabs * n * 8;
+    w.blu = reinterpret_cast<float2*>(p);
+    p += slabs * n * 8;
+    w.ids = reinterpret_cast<int32_t*>(p);
+    p += slabs * n * 4;
+    w.c2id = reinterpret_cast<int*>(p);
+    p += slabs * n * 4;
+    w.bid = reinterpret_cast<int32_t*>(p);
+    return w;
+}
+
+static size_t ws_bytes(int64_t slabs, int64_t n) { return ((slabs * 2 * sizeof(int) + 255) / 256) * 256 + slabs * slab_bytes(n); }
+
+size_t indexer_full_ws(int batch, int n_q, int64_t capacity) {
+    const int qc = n_q < QUERY_CHUNK ? n_q : QUERY_CHUNK;
+    return ws_bytes((int64_t)batch * qc, capacity + 1);
+}
+
+size_t reindex_ws(int batch, int n_q, int64_t pool_len) { return ws_bytes((int64_t)batch * n_q, pool_len); }
 
 template <int DI>
 cudaError_t launch_indexer_full_t(const csa2_cache& c, const uint8_t* iq_codes, const uint8_t* iq_scales,
                                   const float* w_head, int n_q, const int64_t* q_pos, int H, int k, int32_t* idx_out,
                                   int pool_blocks, int bs, int32_t* pool_out, void* ws, cudaStream_t st) {
     const int qchunk = n_q < QUERY_CHUNK ? n_q : QUERY_CHUNK;
-    const int64_t items = (int64_t)c.batch * qchunk * c.capacity;
-    float2* lu = reinterpret_cast<float2*>(ws);
-    unsigned long long* ckey = reinterpret_cast<unsigned long long*>(lu + items);
-    int* cid = reinterpret_cast<int*>(ckey + items);
+    const int64_t list_len = (int64_t)c.capacity + 1;
+    const SelectWs w = carve(ws, (int64_t)c.batch * qchunk, list_len);
     const size_t qwords = (size_t)QView<DI>::words(H) * sizeof(int);
+    // queries per scan block and entries per chunk: one query and 4096 entries
+    // for decode, 8 queries sharing each key load (1024 entries) otherwise
+    const int QB = (n_q >= 8 && pool_blocks == 0) ? 8 : 1;
+    int E = QB == 1 ? 4096 : 1024;
+    if (pool_blocks > 0) E = bs * (4096 / bs > 0 ? 4096 / bs : 1);
+    const size_t smem1 = 32 * sizeof(int) + QB * qwords + (size_t)QB * E * sizeof(float2);
+    cudaError_t e = cudaFuncSetAttribute(k_scan_full<DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
+    if (e != cudaSuccess) return e;
     for (int q0 = 0; q0 < n_q; q0 += qchunk) {
         const int n_qc = (n_q - q0) < qchunk ? (n_q - q0) : qchunk;
-        const int QB = n_qc < SCAN_QB ? n_qc : SCAN_QB;
-        dim3 g1((c.capacity + 255) / 256, (n_qc + QB - 1) / QB, c.batch);
-        k_scan_full<DI><<<g1, 256, 32 * sizeof(int) + QB * qwords, st>>>(
-            c.ikey_codes, c.ikey_scales, c.capacity, iq_codes, iq_scales, w_head, q_pos, n_q, q0, n_qc, H, QB, lu);
+        e = cudaMemsetAsync(w.counts, 0, (size_t)c.batch * n_qc * 2 * sizeof(int), st);
+        if (e != cudaSuccess) return e;
+        dim3 g1((c.capacity + E - 1) / E, (n_qc + QB - 1) / QB, c.batch);
+        k_scan_full<DI><<<g1, 256, smem1, st>>>(c.ikey_codes, c.ikey_scales, c.capacity, iq_codes, iq_scales, w_head,
+                                                q_pos, n_q, q0, n_qc, H, QB, E, k, pool_blocks, bs, w.counts, w.ids,
+                                                w.lu, w.bid, w.blu, (int)list_len);
         note_launch();
-        cudaError_t e = cudaGetLastError();
+        e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         dim3 g2(n_qc, c.batch);
-        k_select<DI><<<g2, 512, qwords, st>>>(lu, c.capacity, nullptr, 0, c.ikey_codes, c.ikey_scales, c.capacity,
-                                               iq_codes, iq_scales, w_head, q_pos, n_q, q0, n_qc, H, k, idx_out,
-                                               pool_blocks, bs, pool_out, cid, ckey);
+        k_select<DI><<<g2, 512, qwords, st>>>(w.ids, w.lu, w.counts, 0, (int)list_len, c.ikey_codes, c.ikey_scales,
+                                              c.capacity, iq_codes, iq_scales, w_head, q_pos, n_q, q0, n_qc, H, k,
+                                              idx_out, pool_blocks, bs, pool_out, w.bid, w.blu, w.c2id, w.c2key);
         note_launch();
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
@@ -551,32 +681,20 @@ template <int DI>
 cudaError_t launch_reindex_t(const csa2_cache& c, const uint8_t* iq_codes, const uint8_t* iq_scales,
                              const float* w_head, int n_q, int H, const int32_t* pool, int pool_len, int k,
                              int32_t* idx_out, void* ws, cudaStream_t st) {
-    const int64_t items = (int64_t)c.batch * n_q * pool_len;
-    float2* lu = reinterpret_cast<float2*>(ws);
-    unsigned long long* ckey = reinterpret_cast<unsigned long long*>(lu + items);
-    int* cid = reinterpret_cast<int*>(ckey + items);
+    const SelectWs w = carve(ws, (int64_t)c.batch * n_q, pool_len);
     const size_t qwords = (size_t)QView<DI>::words(H) * sizeof(int);
     dim3 g1((pool_len + 255) / 256, n_q, c.batch);
     k_scan_pool<DI><<<g1, 256, qwords, st>>>(c.ikey_codes, c.ikey_scales, c.capacity, iq_codes, iq_scales, w_head,
-                                             pool, pool_len, n_q, H, lu);
+                                             pool, pool_len, n_q, H, w.lu);
     note_launch();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     dim3 g2(n_q, c.batch);
-    k_select<DI><<<g2, 512, qwords, st>>>(lu, pool_len, pool, pool_len, c.ikey_codes, c.ikey_scales, c.capacity,
-                                           iq_codes, iq_scales, w_head, nullptr, n_q, 0, n_q, H, k, idx_out, 0, 1,
-                                           nullptr, cid, ckey);
+    k_select<DI><<<g2, 512, qwords, st>>>(pool, w.lu, nullptr, pool_len, pool_len, c.ikey_codes, c.ikey_scales,
+                                          c.capacity, iq_codes, iq_scales, w_head, nullptr, n_q, 0, n_q, H, k,
+                                          idx_out, 0, 1, nullptr, nullptr, nullptr, w.c2id, w.c2key);
     note_launch();
     return cudaGetLastError();
-}
-
-size_t indexer_full_ws(int batch, int n_q, int64_t capacity) {
-    const int qchunk = n_q < QUERY_CHUNK ? n_q : QUERY_CHUNK;
-    return (size_t)batch * qchunk * capacity * select_ws_per_item();
-}
-
-size_t reindex_ws(int batch, int n_q, int64_t pool_len) {
-    return (size_t)batch * n_q * pool_len * select_ws_per_item();
 }
 
 cudaError_t launch_indexer_full(const csa2_cache& c, const uint8_t* iq_codes, const uint8_t* iq_scales,
