@@ -108,7 +108,7 @@ csa2_status csa2_indexer_topk(const csa2_cache* cache, const uint8_t* iq_codes, 
     csa2_status s = check_cache(cache, true);
     if (s != CSA2_OK) return s;
     if (!iq_codes || !iq_scales || !w_head || !q_pos || !idx_out) return CSA2_ERR_INVALID_ARG;
-    if (!aligned(iq_codes, 4) || !aligned(w_head, 4) || !aligned(q_pos, 8) || !aligned(idx_out, 4))
+    if (!aligned(iq_codes, 16) || !aligned(w_head, 4) || !aligned(q_pos, 8) || !aligned(idx_out, 4))
         return CSA2_ERR_INVALID_ARG;
     if (n_q < 1 || n_heads < 1 || n_heads > MAX_IDX_HEADS || k < 1 || k > MAX_K) return CSA2_ERR_INVALID_ARG;
     if (pool_blocks < 0) return CSA2_ERR_INVALID_ARG;

@@ -12,195 +12,9 @@
 // so that the fp64-exact score lies in [S~ - E, S~ + E] (recursive-summation
 // error bounds).  Selection then needs exact scores only for entries whose
 // interval reaches the k-th largest lower bound: usually k plus a handful.
-#include "common.cuh"
+#include "indexer_common.cuh"
 
 namespace csa2 {
-
-// ---------------------------------------------------------------- query staging
-
-template <int DI>
-struct QView {
-    int* qp;     // [H][DI/4] doubled E2M1 values, int8 x4
-    int* qn;     // [H][DI/4] their negations
-    float* qsc;  // [H][DI/16] E4M3 scales as float
-    float* w;    // [H]
-    __device__ static int words(int H) { return H * (DI / 4) * 2 + H * (DI / 16) + H; }
-    __device__ void bind(int* base, int H) {
-        qp = base;
-        qn = qp + H * (DI / 4);
-        qsc = reinterpret_cast<float*>(qn + H * (DI / 4));
-        w = qsc + H * (DI / 16);
-    }
-};
-
-template <int DI>
-__device__ void stage_query(QView<DI> v, const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
-                            const float* __restrict__ w, int H, int tid, int nthr) {
-    for (int i = tid; i < H * (DI / 4); i += nthr) {
-        uint32_t nib16 = reinterpret_cast<const uint16_t*>(codes)[i];
-        uint32_t p, n;
-        unpack4_signed(nib16, p, n);
-        v.qp[i] = (int)__vsub4(p, n);
-        v.qn[i] = (int)__vsub4(n, p);
-    }
-    for (int i = tid; i < H * (DI / 16); i += nthr) v.qsc[i] = e4m3_to_f32(scales[i]);
-    for (int i = tid; i < H; i += nthr) v.w[i] = w[i];
-}
-
-template <int DI>
-struct KeyRow {
-    uint32_t kp[DI / 4], kn[DI / 4];
-    float sk[DI / 16];
-    __device__ __forceinline__ void load(const uint8_t* __restrict__ kc, const uint8_t* __restrict__ ks) {
-#pragma unroll
-        for (int v = 0; v < DI / 32; ++v) {
-            uint4 c = __ldg(reinterpret_cast<const uint4*>(kc) + v);
-            const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                unpack4_signed(cw[t] & 0xffffu, kp[8 * v + 2 * t], kn[8 * v + 2 * t]);
-                unpack4_signed(cw[t] >> 16, kp[8 * v + 2 * t + 1], kn[8 * v + 2 * t + 1]);
-            }
-        }
-        if (DI == 128) {
-            uint2 s = __ldg(reinterpret_cast<const uint2*>(ks));
-#pragma unroll
-            for (int g = 0; g < 4; ++g) sk[g] = e4m3_to_f32((s.x >> (8 * g)) & 255u);
-#pragma unroll
-            for (int g = 0; g < DI / 16 - 4; ++g) sk[4 + g] = e4m3_to_f32((s.y >> (8 * g)) & 255u);
-        } else {
-            uint32_t s = __ldg(reinterpret_cast<const uint32_t*>(ks));
-#pragma unroll
-            for (int g = 0; g < DI / 16; ++g) sk[g] = e4m3_to_f32((s >> (8 * g)) & 255u);
-        }
-    }
-};
-
-// approximate score and its error bound (see the file header)
-template <int DI>
-__device__ __forceinline__ void approx_score(const KeyRow<DI>& k, QView<DI> q, int H, float fac, float& L,
-                                             float& U) {
-    float S = 0.0f, B = 0.0f;
-    for (int h = 0; h < H; ++h) {
-        float d = 0.0f, A = 0.0f;
-#pragma unroll
-        for (int g = 0; g < DI / 16; ++g) {
-            int G = group_dot4(q.qp + h * (DI / 4) + 4 * g, q.qn + h * (DI / 4) + 4 * g, k.kp + 4 * g, k.kn + 4 * g);
-            float c = q.qsc[h * (DI / 16) + g] * k.sk[g] * 0.25f;   // exact
-            float t = (float)G * c;                                  // exact
-            d += t;
-            A += fabsf(t);
-        }
-        S = __fmaf_rn(q.w[h], fmaxf(d, 0.0f), S);
-        B = __fmaf_rn(fabsf(q.w[h]), A, B);
-    }
-    float E = B * fac;
-    L = S - E;
-    U = S + E;
-}
-
-// the exact score: integer group sums, exact fp64 group terms and sum, fp64
-// fused multiply-add chain over heads in ascending order
-template <int DI>
-__device__ double exact_score(const uint8_t* __restrict__ kc, const uint8_t* __restrict__ ks, QView<DI> q, int H) {
-    KeyRow<DI> k;
-    k.load(kc, ks);
-    double S = 0.0;
-    for (int h = 0; h < H; ++h) {
-        double d = 0.0;
-#pragma unroll
-        for (int g = 0; g < DI / 16; ++g) {
-            int G = group_dot4(q.qp + h * (DI / 4) + 4 * g, q.qn + h * (DI / 4) + 4 * g, k.kp + 4 * g, k.kn + 4 * g);
-            d += (double)G * ((double)q.qsc[h * (DI / 16) + g] * (double)k.sk[g] * 0.25);
-        }
-        S = fma((double)q.w[h], d > 0.0 ? d : 0.0, S);
-    }
-    return S;
-}
-
-__device__ __forceinline__ int n_elig_of(int64_t p, int capacity) {
-    int64_t n = (p - (WINDOW - 1)) >> 1;
-    if (p < WINDOW - 1) n = 0;
-    return (int)(n < capacity ? n : capacity);
-}
-
-__host__ __device__ inline float bound_factor(int H, int DI) { return 2.0f * (float)(2 * H + DI / 16 + 8) * 0x1p-24f; }
-
-// ---------------------------------------------------------------- block-wide radix selection
-
-struct RadixSmem {
-    int hist[256];
-    int ctl[8];   // [0] append counter, [1] digit, [2] krem, [3] scratch
-};
-
-// k-th largest key (1 <= k <= number of taking items) over items t in [0, n):
-// getkey(t, key) returns false for items that do not take part.  Returns the
-// key and sets *krem to how many items equal to it are needed.  Lanes with the
-// same digit are merged (match.any) before the shared-memory atomic, so heavy
-// ties do not serialise.
-template <typename KeyT, typename Get>
-__device__ KeyT block_kth_largest(Get getkey, int n, int k, RadixSmem& rs, int* krem_out) {
-    constexpr int BITS = sizeof(KeyT) * 8;
-    const int lane = threadIdx.x & 31;
-    KeyT prefix = 0, mask = 0;
-    int krem = k;
-    for (int shift = BITS - 8; shift >= 0; shift -= 8) {
-        for (int i = threadIdx.x; i < 256; i += blockDim.x) rs.hist[i] = 0;
-        __syncthreads();
-        for (int base = 0; base < n; base += blockDim.x) {
-            const int t = base + threadIdx.x;
-            KeyT key = 0;
-            int bin = -1;
-            if (t < n && getkey(t, key) && (key & mask) == prefix) bin = (int)((key >> shift) & 255);
-            const unsigned peers = __match_any_sync(0xffffffffu, bin);
-            if (bin >= 0 && lane == __ffs(peers) - 1) atomicAdd(&rs.hist[bin], __popc(peers));
-        }
-        __syncthreads();
-        if (threadIdx.x < 32) {
-            int c = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) c += rs.hist[255 - 8 * lane - i];   // lane 0 holds the top bins
-            int incl = c;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                int y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            const unsigned hit = __ballot_sync(0xffffffffu, incl >= krem);
-            const int L = __ffs(hit) - 1;
-            if (lane == L) {
-                int cum = incl - c;
-                for (int i = 0; i < 8; ++i) {
-                    const int d = 255 - 8 * lane - i;
-                    if (cum + rs.hist[d] >= krem) {
-                        rs.ctl[1] = d;
-                        rs.ctl[2] = krem - cum;
-                        break;
-                    }
-                    cum += rs.hist[d];
-                }
-            }
-        }
-        __syncthreads();
-        prefix |= (KeyT)rs.ctl[1] << shift;
-        mask |= (KeyT)255 << shift;
-        krem = rs.ctl[2];
-        __syncthreads();
-    }
-    *krem_out = krem;
-    return prefix;
-}
-
-// warp-aggregated append to a list whose counter lives at *ctr (shared or global)
-__device__ __forceinline__ int append_slot(bool flag, int* ctr) {
-    const unsigned m = __ballot_sync(0xffffffffu, flag);
-    if (!m) return -1;
-    const int lane = threadIdx.x & 31, leader = __ffs(m) - 1;
-    int base = 0;
-    if (lane == leader) base = atomicAdd(ctr, __popc(m));
-    base = __shfl_sync(0xffffffffu, base, leader);
-    return flag ? base + __popc(m & ((1u << lane) - 1u)) : -1;
-}
 
 // ---------------------------------------------------------------- scans
 
@@ -263,70 +77,8 @@ __global__ void __launch_bounds__(256) k_scan_full(const uint8_t* __restrict__ k
     }
     __syncthreads();
     for (int t = 0; t < nqb; ++t) {
-        const int n_loc = min(max(nel[t] - c0, 0), E);
-        if (n_loc == 0) continue;                 // uniform
-        const int64_t slab = (int64_t)b * n_qc + qa + t;
-        const float2* lu = slu + t * E;
-        unsigned int lam = 0u;
-        if (n_loc > k) {
-            int krem;
-            lam = block_kth_largest<unsigned int>(
-                [&](int i, unsigned int& key) {
-                    key = f32_key(lu[i].x);
-                    return true;
-                },
-                n_loc, k, rs, &krem);
-        }
-        for (int base = 0; base < n_loc; base += blockDim.x) {
-            const int i = base + threadIdx.x;
-            const bool f = i < n_loc && f32_key(lu[i].y) >= lam;
-            const int pos = append_slot(f, counts + 2 * slab);
-            if (f) {
-                cid[slab * list_len + pos] = c0 + i;
-                clu[slab * list_len + pos] = lu[i];
-            }
-        }
-        if (pool_blocks > 1) {
-            const int nb = (nel[t] + bs - 1) / bs;          // blocks of this query
-            const int forced = nb - 1;
-            const int g0 = c0 / bs;                          // first block of the chunk (E is a multiple of bs)
-            const int nbl = min(E / bs, nb - g0);            // blocks of this chunk that exist
-            const int nvalid = nbl - ((forced >= g0 && forced < g0 + nbl) ? 1 : 0);
-            if (nb > pool_blocks && nvalid > 0) {
-                auto blk = [&](int bl, bool upper) {
-                    float mx = -INFINITY;
-                    for (int i = 0; i < bs; ++i) {
-                        const int e = bl * bs + i;
-                        if (e < n_loc) mx = fmaxf(mx, upper ? lu[e].y : lu[e].x);
-                    }
-                    return mx;
-                };
-                unsigned int lamb = 0u;
-                if (nvalid > pool_blocks - 1) {
-                    int krem;
-                    lamb = block_kth_largest<unsigned int>(
-                        [&](int bl, unsigned int& key) {
-                            key = f32_key(blk(bl, false));
-                            return g0 + bl != forced;
-                        },
-                        nbl, pool_blocks - 1, rs, &krem);
-                }
-                for (int base = 0; base < nbl; base += blockDim.x) {
-                    const int bl = base + threadIdx.x;
-                    float2 m2 = make_float2(-INFINITY, -INFINITY);
-                    bool f = false;
-                    if (bl < nbl && g0 + bl != forced) {
-                        m2 = make_float2(blk(bl, false), blk(bl, true));
-                        f = f32_key(m2.y) >= lamb;
-                    }
-                    const int pos = append_slot(f, counts + 2 * slab + 1);
-                    if (f) {
-                        bid[slab * list_len + pos] = g0 + bl;
-                        blu[slab * list_len + pos] = m2;
-                    }
-                }
-            }
-        }
+        forward_candidates(slu + t * E, c0, E, nel[t], k, pool_blocks, bs, (int64_t)b * n_qc + qa + t, list_len,
+                           counts, cid, clu, bid, blu, rs);
         __syncthreads();
     }
 }
@@ -602,6 +354,7 @@ constexpr int QUERY_CHUNK = 128;
 static size_t slab_bytes(int64_t n) { return (size_t)n * (4 + 8 + 4 + 8 + 4 + 8); }
 
 struct SelectWs {
+    int* err;
     int* counts;
     int32_t* ids;
     float2* lu;
@@ -615,7 +368,8 @@ static SelectWs carve(void* ws, int64_t slabs, int64_t n) {
     uint8_t* p = reinterpret_cast<uint8_t*>(ws);
     SelectWs w;
     w.counts = reinterpret_cast<int*>(p);
-    p += ((slabs * 2 * sizeof(int) + 255) / 256) * 256;
+    w.err = w.counts + slabs * 2;
+    p += (((slabs * 2 + 4) * sizeof(int) + 255) / 256) * 256;
     w.c2key = reinterpret_cast<unsigned long long*>(p);
     p += slabs * n * 8;
     w.lu = reinterpret_cast<float2*>(p);
@@ -630,7 +384,15 @@ static SelectWs carve(void* ws, int64_t slabs, int64_t n) {
     return w;
 }
 
-static size_t ws_bytes(int64_t slabs, int64_t n) { return ((slabs * 2 * sizeof(int) + 255) / 256) * 256 + slabs * slab_bytes(n); }
+static size_t ws_bytes(int64_t slabs, int64_t n) {
+    return (((slabs * 2 + 4) * sizeof(int) + 255) / 256) * 256 + slabs * slab_bytes(n);
+}
+
+bool scan_tc_supported(int d_idx, int H, int QB, int pool_blocks, int bs);
+cudaError_t launch_scan_full_tc(const csa2_cache& c, const uint8_t* iq_codes, const uint8_t* iq_scales,
+                                const float* w_head, int n_q, const int64_t* q_pos, int q0, int n_qc, int H, int k,
+                                int pool_blocks, int bs, int* counts, int* cid, float2* clu, int* bid, float2* blu,
+                                int list_len, int* err, cudaStream_t st);
 
 size_t indexer_full_ws(int batch, int n_q, int64_t capacity) {
     const int qc = n_q < QUERY_CHUNK ? n_q : QUERY_CHUNK;
@@ -657,14 +419,19 @@ cudaError_t launch_indexer_full_t(const csa2_cache& c, const uint8_t* iq_codes, 
     if (e != cudaSuccess) return e;
     for (int q0 = 0; q0 < n_q; q0 += qchunk) {
         const int n_qc = (n_q - q0) < qchunk ? (n_q - q0) : qchunk;
-        e = cudaMemsetAsync(w.counts, 0, (size_t)c.batch * n_qc * 2 * sizeof(int), st);
+        e = cudaMemsetAsync(w.counts, 0, ((size_t)c.batch * n_qc * 2 + 4) * sizeof(int), st);
         if (e != cudaSuccess) return e;
-        dim3 g1((c.capacity + E - 1) / E, (n_qc + QB - 1) / QB, c.batch);
-        k_scan_full<DI><<<g1, 256, smem1, st>>>(c.ikey_codes, c.ikey_scales, c.capacity, iq_codes, iq_scales, w_head,
-                                                q_pos, n_q, q0, n_qc, H, QB, E, k, pool_blocks, bs, w.counts, w.ids,
-                                                w.lu, w.bid, w.blu, (int)list_len);
-        note_launch();
-        e = cudaGetLastError();
+        if (scan_tc_supported(DI, H, QB, pool_blocks, bs)) {
+            e = launch_scan_full_tc(c, iq_codes, iq_scales, w_head, n_q, q_pos, q0, n_qc, H, k, pool_blocks, bs,
+                                    w.counts, w.ids, w.lu, w.bid, w.blu, (int)list_len, w.err, st);
+        } else {
+            dim3 g1((c.capacity + E - 1) / E, (n_qc + QB - 1) / QB, c.batch);
+            k_scan_full<DI><<<g1, 256, smem1, st>>>(c.ikey_codes, c.ikey_scales, c.capacity, iq_codes, iq_scales,
+                                                    w_head, q_pos, n_q, q0, n_qc, H, QB, E, k, pool_blocks, bs,
+                                                    w.counts, w.ids, w.lu, w.bid, w.blu, (int)list_len);
+            note_launch();
+            e = cudaGetLastError();
+        }
         if (e != cudaSuccess) return e;
         dim3 g2(n_qc, c.batch);
         k_select<DI><<<g2, 512, qwords, st>>>(w.ids, w.lu, w.counts, 0, (int)list_len, c.ikey_codes, c.ikey_scales,

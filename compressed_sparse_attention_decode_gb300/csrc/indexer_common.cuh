@@ -1,0 +1,269 @@
+// Indexer pieces shared by the CUDA-core and the tensor-core scans: query
+// staging, key rows, the approximate score with its rigorous error bound, the
+// exact fp64 score, block-wide radix selection and candidate forwarding.
+#pragma once
+#include "common.cuh"
+
+namespace csa2 {
+
+// ---------------------------------------------------------------- query staging
+
+template <int DI>
+struct QView {
+    int* qp;     // [H][DI/4] doubled E2M1 values, int8 x4
+    int* qn;     // [H][DI/4] their negations
+    float* qsc;  // [H][DI/16] E4M3 scales as float
+    float* w;    // [H]
+    __device__ static int words(int H) { return H * (DI / 4) * 2 + H * (DI / 16) + H; }
+    __device__ void bind(int* base, int H) {
+        qp = base;
+        qn = qp + H * (DI / 4);
+        qsc = reinterpret_cast<float*>(qn + H * (DI / 4));
+        w = qsc + H * (DI / 16);
+    }
+};
+
+template <int DI>
+__device__ void stage_query(QView<DI> v, const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
+                            const float* __restrict__ w, int H, int tid, int nthr) {
+    for (int i = tid; i < H * (DI / 4); i += nthr) {
+        uint32_t nib16 = reinterpret_cast<const uint16_t*>(codes)[i];
+        uint32_t p, n;
+        unpack4_signed(nib16, p, n);
+        v.qp[i] = (int)__vsub4(p, n);
+        v.qn[i] = (int)__vsub4(n, p);
+    }
+    for (int i = tid; i < H * (DI / 16); i += nthr) v.qsc[i] = e4m3_to_f32(scales[i]);
+    for (int i = tid; i < H; i += nthr) v.w[i] = w[i];
+}
+
+template <int DI>
+struct KeyRow {
+    uint32_t kp[DI / 4], kn[DI / 4];
+    float sk[DI / 16];
+    __device__ __forceinline__ void load(const uint8_t* __restrict__ kc, const uint8_t* __restrict__ ks) {
+#pragma unroll
+        for (int v = 0; v < DI / 32; ++v) {
+            uint4 c = __ldg(reinterpret_cast<const uint4*>(kc) + v);
+            const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                unpack4_signed(cw[t] & 0xffffu, kp[8 * v + 2 * t], kn[8 * v + 2 * t]);
+                unpack4_signed(cw[t] >> 16, kp[8 * v + 2 * t + 1], kn[8 * v + 2 * t + 1]);
+            }
+        }
+        if (DI == 128) {
+            uint2 s = __ldg(reinterpret_cast<const uint2*>(ks));
+#pragma unroll
+            for (int g = 0; g < 4; ++g) sk[g] = e4m3_to_f32((s.x >> (8 * g)) & 255u);
+#pragma unroll
+            for (int g = 0; g < DI / 16 - 4; ++g) sk[4 + g] = e4m3_to_f32((s.y >> (8 * g)) & 255u);
+        } else {
+            uint32_t s = __ldg(reinterpret_cast<const uint32_t*>(ks));
+#pragma unroll
+            for (int g = 0; g < DI / 16; ++g) sk[g] = e4m3_to_f32((s >> (8 * g)) & 255u);
+        }
+    }
+};
+
+// approximate score and its error bound (see the file header)
+template <int DI>
+__device__ __forceinline__ void approx_score(const KeyRow<DI>& k, QView<DI> q, int H, float fac, float& L,
+                                             float& U) {
+    float S = 0.0f, B = 0.0f;
+    for (int h = 0; h < H; ++h) {
+        float d = 0.0f, A = 0.0f;
+#pragma unroll
+        for (int g = 0; g < DI / 16; ++g) {
+            int G = group_dot4(q.qp + h * (DI / 4) + 4 * g, q.qn + h * (DI / 4) + 4 * g, k.kp + 4 * g, k.kn + 4 * g);
+            float c = q.qsc[h * (DI / 16) + g] * k.sk[g] * 0.25f;   // exact
+            float t = (float)G * c;                                  // exact
+            d += t;
+            A += fabsf(t);
+        }
+        S = __fmaf_rn(q.w[h], fmaxf(d, 0.0f), S);
+        B = __fmaf_rn(fabsf(q.w[h]), A, B);
+    }
+    float E = B * fac;
+    L = S - E;
+    U = S + E;
+}
+
+// the exact score: integer group sums, exact fp64 group terms and sum, fp64
+// fused multiply-add chain over heads in ascending order
+template <int DI>
+__device__ double exact_score(const uint8_t* __restrict__ kc, const uint8_t* __restrict__ ks, QView<DI> q, int H) {
+    KeyRow<DI> k;
+    k.load(kc, ks);
+    double S = 0.0;
+    for (int h = 0; h < H; ++h) {
+        double d = 0.0;
+#pragma unroll
+        for (int g = 0; g < DI / 16; ++g) {
+            int G = group_dot4(q.qp + h * (DI / 4) + 4 * g, q.qn + h * (DI / 4) + 4 * g, k.kp + 4 * g, k.kn + 4 * g);
+            d += (double)G * ((double)q.qsc[h * (DI / 16) + g] * (double)k.sk[g] * 0.25);
+        }
+        S = fma((double)q.w[h], d > 0.0 ? d : 0.0, S);
+    }
+    return S;
+}
+
+__device__ __forceinline__ int n_elig_of(int64_t p, int capacity) {
+    int64_t n = (p - (WINDOW - 1)) >> 1;
+    if (p < WINDOW - 1) n = 0;
+    return (int)(n < capacity ? n : capacity);
+}
+
+__host__ __device__ inline float bound_factor(int H, int DI) { return 2.0f * (float)(2 * H + DI / 16 + 8) * 0x1p-24f; }
+
+// ---------------------------------------------------------------- block-wide radix selection
+
+struct RadixSmem {
+    int hist[256];
+    int ctl[8];   // [0] append counter, [1] digit, [2] krem, [3] scratch
+};
+
+// k-th largest key (1 <= k <= number of taking items) over items t in [0, n):
+// getkey(t, key) returns false for items that do not take part.  Returns the
+// key and sets *krem to how many items equal to it are needed.  Lanes with the
+// same digit are merged (match.any) before the shared-memory atomic, so heavy
+// ties do not serialise.
+template <typename KeyT, typename Get>
+__device__ KeyT block_kth_largest(Get getkey, int n, int k, RadixSmem& rs, int* krem_out) {
+    constexpr int BITS = sizeof(KeyT) * 8;
+    const int lane = threadIdx.x & 31;
+    KeyT prefix = 0, mask = 0;
+    int krem = k;
+    for (int shift = BITS - 8; shift >= 0; shift -= 8) {
+        for (int i = threadIdx.x; i < 256; i += blockDim.x) rs.hist[i] = 0;
+        __syncthreads();
+        for (int base = 0; base < n; base += blockDim.x) {
+            const int t = base + threadIdx.x;
+            KeyT key = 0;
+            int bin = -1;
+            if (t < n && getkey(t, key) && (key & mask) == prefix) bin = (int)((key >> shift) & 255);
+            const unsigned peers = __match_any_sync(0xffffffffu, bin);
+            if (bin >= 0 && lane == __ffs(peers) - 1) atomicAdd(&rs.hist[bin], __popc(peers));
+        }
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            int c = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) c += rs.hist[255 - 8 * lane - i];   // lane 0 holds the top bins
+            int incl = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const unsigned hit = __ballot_sync(0xffffffffu, incl >= krem);
+            const int L = __ffs(hit) - 1;
+            if (lane == L) {
+                int cum = incl - c;
+                for (int i = 0; i < 8; ++i) {
+                    const int d = 255 - 8 * lane - i;
+                    if (cum + rs.hist[d] >= krem) {
+                        rs.ctl[1] = d;
+                        rs.ctl[2] = krem - cum;
+                        break;
+                    }
+                    cum += rs.hist[d];
+                }
+            }
+        }
+        __syncthreads();
+        prefix |= (KeyT)rs.ctl[1] << shift;
+        mask |= (KeyT)255 << shift;
+        krem = rs.ctl[2];
+        __syncthreads();
+    }
+    *krem_out = krem;
+    return prefix;
+}
+
+// warp-aggregated append to a list whose counter lives at *ctr (shared or global)
+__device__ __forceinline__ int append_slot(bool flag, int* ctr) {
+    const unsigned m = __ballot_sync(0xffffffffu, flag);
+    if (!m) return -1;
+    const int lane = threadIdx.x & 31, leader = __ffs(m) - 1;
+    int base = 0;
+    if (lane == leader) base = atomicAdd(ctr, __popc(m));
+    base = __shfl_sync(0xffffffffu, base, leader);
+    return flag ? base + __popc(m & ((1u << lane) - 1u)) : -1;
+}
+
+
+// After a scan block has the (S~-E, S~+E) bounds of its chunk in shared memory
+// (lu[0..E), entries c0..c0+E-1), forward to the query's global lists every
+// entry whose upper bound reaches the chunk's k-th largest lower bound, and
+// likewise for HSI blocks (bounds = max over members; the newest block, which
+// is always kept, is not forwarded).  The global k-th lower bound is never
+// smaller than a chunk's, so nothing the exact selection needs is dropped.
+static __device__ void forward_candidates(const float2* lu, int c0, int E, int n_elig, int k, int pool_blocks, int bs,
+                                   int64_t slab, int list_len, int* counts, int* cid, float2* clu, int* bid,
+                                   float2* blu, RadixSmem& rs) {
+    const int n_loc = min(max(n_elig - c0, 0), E);
+    if (n_loc == 0) return;                       // uniform
+    unsigned int lam = 0u;
+    if (n_loc > k) {
+        int krem;
+        lam = block_kth_largest<unsigned int>(
+            [&](int i, unsigned int& key) {
+                key = f32_key(lu[i].x);
+                return true;
+            },
+            n_loc, k, rs, &krem);
+    }
+    for (int base = 0; base < n_loc; base += blockDim.x) {
+        const int i = base + threadIdx.x;
+        const bool f = i < n_loc && f32_key(lu[i].y) >= lam;
+        const int pos = append_slot(f, counts + 2 * slab);
+        if (f) {
+            cid[slab * list_len + pos] = c0 + i;
+            clu[slab * list_len + pos] = lu[i];
+        }
+    }
+    if (pool_blocks > 1) {
+        const int nb = (n_elig + bs - 1) / bs;           // blocks of this query
+        const int forced = nb - 1;
+        const int g0 = c0 / bs;                           // first block of the chunk (E is a multiple of bs)
+        const int nbl = min(E / bs, nb - g0);             // blocks of this chunk that exist
+        const int nvalid = nbl - ((forced >= g0 && forced < g0 + nbl) ? 1 : 0);
+        if (nb > pool_blocks && nvalid > 0) {
+            auto blk = [&](int bl, bool upper) {
+                float mx = -INFINITY;
+                for (int i = 0; i < bs; ++i) {
+                    const int e = bl * bs + i;
+                    if (e < n_loc) mx = fmaxf(mx, upper ? lu[e].y : lu[e].x);
+                }
+                return mx;
+            };
+            unsigned int lamb = 0u;
+            if (nvalid > pool_blocks - 1) {
+                int krem;
+                lamb = block_kth_largest<unsigned int>(
+                    [&](int bl, unsigned int& key) {
+                        key = f32_key(blk(bl, false));
+                        return g0 + bl != forced;
+                    },
+                    nbl, pool_blocks - 1, rs, &krem);
+            }
+            for (int base = 0; base < nbl; base += blockDim.x) {
+                const int bl = base + threadIdx.x;
+                float2 m2 = make_float2(-INFINITY, -INFINITY);
+                bool f = false;
+                if (bl < nbl && g0 + bl != forced) {
+                    m2 = make_float2(blk(bl, false), blk(bl, true));
+                    f = f32_key(m2.y) >= lamb;
+                }
+                const int pos = append_slot(f, counts + 2 * slab + 1);
+                if (f) {
+                    bid[slab * list_len + pos] = g0 + bl;
+                    blu[slab * list_len + pos] = m2;
+                }
+            }
+        }
+    }
+}
+
+}  // namespace csa2

@@ -1,0 +1,223 @@
+// Full indexer scan on the tensor cores ("DeepSeek-v4.1 Flash: KVキャッシュ圧縮の
+// 限界を押し広げる", §2.3.1 lightweight indexer over FP4 keys).
+//
+// For one query and a chunk of 4096 entries, 128 entries at a time:
+//   A = key codes  [128 entries x d_I] FP4 E2M1 (kind::f8f6f4: each 16-value
+//       group is 8 packed bytes followed by 8 pad bytes in shared memory)
+//   B = block-diagonal query [H*G rows x d_I]: row (h, g) holds head h's codes
+//       of group g and zeros elsewhere
+//   D = A . B^T   M = 128, N = H*G, K = d_I   (fp32 in TMEM)
+// D[e][(h,g)] is the exact group sum sum_{i in g} k_i q_hi (multiples of 1/4,
+// |.| <= 576).  The epilogue forms t = D * s_q * s_k (exact) and the same fp32
+// score and error bound as the CUDA-core scan, bit for bit, then the chunk's
+// candidates are forwarded exactly as there.
+//
+// Warp roles (256 threads): warps 0-3 epilogue (one TMEM lane = one entry),
+// warp 4 lane 0 issues the MMAs, warps 5-7 load key rows.  Four A slots and two
+// TMEM accumulators keep loads, MMAs and epilogues overlapped.
+#include "indexer_common.cuh"
+#include "umma.cuh"
+
+namespace csa2 {
+
+constexpr int ITC_E = 4096;                 // entries per block
+constexpr int ITC_TILE = 128;
+constexpr int ITC_NBUF = 4;
+constexpr int ITC_DI = 128;
+constexpr int ITC_G = ITC_DI / 16;
+constexpr int ITC_LOADERS = 96;             // warps 5-7
+// shared memory (from the 1024-aligned base)
+constexpr int ITC_H = 8;                    // indexer heads taken by this kernel
+constexpr int ITC_N = ITC_H * ITC_G;        // MMA N: one column per (head, group)
+constexpr uint32_t IS_B = 0;                                  // query operand, 64 rows x 128 B
+constexpr uint32_t IS_A = ITC_N * 128;                        // 4 slots x 128 rows x 128 B
+constexpr uint32_t IS_SK = IS_A + ITC_NBUF * ITC_TILE * 128;  // 4 slots x 128 rows x 8 B scales
+constexpr uint32_t IS_LU = IS_SK + ITC_NBUF * ITC_TILE * 8;   // 4096 float2
+constexpr uint32_t IS_Q = IS_LU + ITC_E * 8;                  // sq [H][G] floats + w [H]
+constexpr uint32_t IS_END = IS_Q + 2048;
+constexpr uint32_t IS_DYN = IS_END + 1024;
+
+__device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t unit) { return row * 128 + ((unit ^ (row & 7)) << 4); }
+
+__global__ void __launch_bounds__(256, 2) k_scan_full_tc(
+    const uint8_t* __restrict__ kc_all, const uint8_t* __restrict__ ks_all, int capacity,
+    const uint8_t* __restrict__ iq_codes, const uint8_t* __restrict__ iq_scales, const float* __restrict__ w_head,
+    const int64_t* __restrict__ q_pos, int n_q, int q0, int n_qc, int H, int k, int pool_blocks, int bs,
+    int* __restrict__ counts, int* __restrict__ cid, float2* __restrict__ clu, int* __restrict__ bid,
+    float2* __restrict__ blu, int list_len, int* __restrict__ err) {
+    extern __shared__ uint8_t dyn[];
+    __shared__ RadixSmem rs;
+    __shared__ __align__(8) unsigned long long bar_full[ITC_NBUF], bar_empty[ITC_NBUF], bar_dfull[2], bar_dfree[2];
+    __shared__ uint32_t tmem_base;
+    __shared__ int s_nel;
+
+    const uint32_t raw = umma::smem_u32(dyn);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* sm = dyn + (base - raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int b = blockIdx.z, ql = blockIdx.y;
+    const int64_t gq = (int64_t)b * n_q + q0 + ql;
+    const int c0 = blockIdx.x * ITC_E;
+    constexpr int N = ITC_N;
+
+    if (tid == 0) {
+        s_nel = n_elig_of(q_pos[gq], capacity);
+        for (int i = 0; i < ITC_NBUF; ++i) {
+            umma::mbar_init(umma::smem_u32(&bar_full[i]), ITC_LOADERS);
+            umma::mbar_init(umma::smem_u32(&bar_empty[i]), 128);
+        }
+        for (int i = 0; i < 2; ++i) {
+            umma::mbar_init(umma::smem_u32(&bar_dfull[i]), 1);
+            umma::mbar_init(umma::smem_u32(&bar_dfree[i]), 128);
+        }
+        umma::fence_mbar_init();
+    }
+    // query operand: row n = (h, g) -> unit g holds head h's 8 code bytes of
+    // group g; every other byte of the row is zero
+    const uint8_t* qc = iq_codes + gq * H * (ITC_DI / 2);
+    for (int i = tid; i < N * 8; i += blockDim.x) {
+        const int n = i >> 3, u = i & 7, h = n / ITC_G, g = n % ITC_G;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (u == g) {
+            const uint2 c = *reinterpret_cast<const uint2*>(qc + h * (ITC_DI / 2) + g * 8);
+            v.x = c.x;
+            v.y = c.y;
+        }
+        *reinterpret_cast<uint4*>(sm + IS_B + swz128(n, u)) = v;
+    }
+    float* sq = reinterpret_cast<float*>(sm + IS_Q);          // [H][G]
+    float* ww = sq + H * ITC_G;                                // [H]
+    for (int i = tid; i < H * ITC_G; i += blockDim.x) sq[i] = e4m3_to_f32(iq_scales[gq * H * ITC_G + i]);
+    for (int i = tid; i < H; i += blockDim.x) ww[i] = w_head[gq * H + i];
+    // zero the A slots once: the pad half of every 16-byte unit stays zero
+    for (int i = tid; i < ITC_NBUF * ITC_TILE * 8; i += blockDim.x)
+        reinterpret_cast<uint4*>(sm + IS_A)[i] = make_uint4(0, 0, 0, 0);
+    if (warp == 0) umma::tmem_alloc(umma::smem_u32(&tmem_base), 128);
+    umma::fence_proxy_async();
+    umma::fence_before();
+    __syncthreads();
+    umma::fence_after();
+    const uint32_t tmem = tmem_base;
+    const int n_elig = s_nel;
+    const int n_loc = min(max(n_elig - c0, 0), ITC_E);
+    const int n_tiles = (n_loc + ITC_TILE - 1) / ITC_TILE;
+    float2* slu = reinterpret_cast<float2*>(sm + IS_LU);
+    bool ok = true;
+
+    if (warp >= 5) {
+        // ---- loaders: codes (8 bytes per group -> the data half of a unit) and scales
+        const int lt = tid - 160;
+        for (int t = 0; t < n_tiles; ++t) {
+            const int s = t % ITC_NBUF;
+            if (t >= ITC_NBUF) ok &= umma::mbar_wait(umma::smem_u32(&bar_empty[s]), ((t / ITC_NBUF) - 1) & 1);
+            uint8_t* a = sm + IS_A + s * (ITC_TILE * 128);
+            const int e0 = c0 + t * ITC_TILE;
+            const uint8_t* src = kc_all + ((int64_t)b * capacity + e0) * (ITC_DI / 2);
+            for (int c = lt; c < ITC_TILE * 4; c += ITC_LOADERS) {       // 16-byte chunks of codes
+                const int r = c >> 2, q4 = c & 3;
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (e0 + r < n_elig) v = __ldg(reinterpret_cast<const uint4*>(src) + c);
+                *reinterpret_cast<uint2*>(a + swz128(r, 2 * q4)) = make_uint2(v.x, v.y);
+                *reinterpret_cast<uint2*>(a + swz128(r, 2 * q4 + 1)) = make_uint2(v.z, v.w);
+            }
+            const uint8_t* ssrc = ks_all + ((int64_t)b * capacity + e0) * ITC_G;
+            uint8_t* sk = sm + IS_SK + s * (ITC_TILE * 8);
+            for (int r = lt; r < ITC_TILE; r += ITC_LOADERS) {             // 8 scale bytes per row
+                uint2 v = make_uint2(0, 0);
+                if (e0 + r < n_elig) v = __ldg(reinterpret_cast<const uint2*>(ssrc) + r);
+                reinterpret_cast<uint2*>(sk)[r] = v;
+            }
+            umma::fence_proxy_async();
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(umma::smem_u32(&bar_full[s])) : "memory");
+        }
+    } else if (warp == 4) {
+        // ---- MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = (1u << 4) | (5u << 7) | (5u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+            for (int t = 0; t < n_tiles; ++t) {
+                const int s = t % ITC_NBUF, d = t & 1;
+                ok &= umma::mbar_wait(umma::smem_u32(&bar_full[s]), (t / ITC_NBUF) & 1);
+                if (t >= 2) ok &= umma::mbar_wait(umma::smem_u32(&bar_dfree[d]), ((t >> 1) - 1) & 1);
+                umma::fence_after();
+#pragma unroll
+                for (int ks = 0; ks < ITC_DI / 32; ++ks) {
+                    const uint64_t ad = umma::desc(base + IS_A + s * (ITC_TILE * 128) + ks * 32, 16, 1024, umma::LAYOUT_SW128);
+                    const uint64_t bd = umma::desc(base + IS_B + ks * 32, 16, 1024, umma::LAYOUT_SW128);
+                    asm volatile(
+                        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+                        " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}" ::"r"(tmem + 64 * d),
+                        "l"(ad), "l"(bd), "r"(idesc), "r"(ks));
+                }
+                umma::commit(umma::smem_u32(&bar_dfull[d]));
+            }
+        }
+    } else {
+        // ---- epilogue: one entry per thread
+        const float fac = bound_factor(H, ITC_DI);
+        for (int t = 0; t < n_tiles; ++t) {
+            const int s = t % ITC_NBUF, d = t & 1;
+            ok &= umma::mbar_wait(umma::smem_u32(&bar_dfull[d]), (t >> 1) & 1);
+            umma::fence_after();
+            float dv[64];
+            const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16) + 64 * d;
+#pragma unroll
+            for (int c = 0; c < N; c += 16) umma::tmem_ld16(lane_base + c, dv + c);
+            umma::tmem_wait_ld();
+            umma::fence_before();
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(umma::smem_u32(&bar_dfree[d])) : "memory");
+            const int r = tid;                          // row of the tile = TMEM lane
+            const uint2 skw = *reinterpret_cast<const uint2*>(sm + IS_SK + s * (ITC_TILE * 8) + r * 8);
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(umma::smem_u32(&bar_empty[s])) : "memory");
+            float skf[ITC_G];
+#pragma unroll
+            for (int g = 0; g < ITC_G; ++g) skf[g] = e4m3_to_f32(((g < 4 ? skw.x : skw.y) >> (8 * (g & 3))) & 255u);
+            float S = 0.0f, B = 0.0f;
+#pragma unroll
+            for (int h = 0; h < ITC_H; ++h) {
+                {
+                    float dd = 0.0f, A = 0.0f;
+#pragma unroll
+                    for (int g = 0; g < ITC_G; ++g) {
+                        const float tv = dv[h * ITC_G + g] * (sq[h * ITC_G + g] * skf[g]);   // exact
+                        dd += tv;
+                        A += fabsf(tv);
+                    }
+                    S = __fmaf_rn(ww[h], fmaxf(dd, 0.0f), S);
+                    B = __fmaf_rn(fabsf(ww[h]), A, B);
+                }
+            }
+            const float E = B * fac;
+            const int i = t * ITC_TILE + r;
+            slu[i] = (i < n_loc) ? make_float2(S - E, S + E) : make_float2(-INFINITY, -INFINITY);
+        }
+    }
+    if (!ok) atomicExch(err, 1);
+    umma::fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        umma::fence_after();
+        umma::tmem_dealloc(tmem, 128);
+    }
+    forward_candidates(slu, c0, ITC_E, n_elig, k, pool_blocks, bs, (int64_t)b * n_qc + ql, list_len, counts, cid, clu,
+                       bid, blu, rs);
+}
+
+bool scan_tc_supported(int d_idx, int H, int QB, int pool_blocks, int bs) {
+    return d_idx == ITC_DI && QB == 1 && H == ITC_H && (pool_blocks == 0 || ITC_E % bs == 0);
+}
+
+cudaError_t launch_scan_full_tc(const csa2_cache& c, const uint8_t* iq_codes, const uint8_t* iq_scales,
+                                const float* w_head, int n_q, const int64_t* q_pos, int q0, int n_qc, int H, int k,
+                                int pool_blocks, int bs, int* counts, int* cid, float2* clu, int* bid, float2* blu,
+                                int list_len, int* err, cudaStream_t st) {
+    cudaError_t e = cudaFuncSetAttribute(k_scan_full_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)IS_DYN);
+    if (e != cudaSuccess) return e;
+    dim3 grid((c.capacity + ITC_E - 1) / ITC_E, n_qc, c.batch);
+    k_scan_full_tc<<<grid, 256, IS_DYN, st>>>(c.ikey_codes, c.ikey_scales, c.capacity, iq_codes, iq_scales, w_head,
+                                              q_pos, n_q, q0, n_qc, H, k, pool_blocks, bs, counts, cid, clu, bid, blu,
+                                              list_len, err);
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace csa2

@@ -112,7 +112,7 @@ csa2_status csa2_quantize_fp4(const float* x, int64_t n_rows, int32_t d, uint8_t
  * -inf), the block holding entry n_elig-1 forced to +inf, the best
  * pool_blocks blocks (ties to the lower block), expanded to their eligible
  * entries in ascending order.
- *   iq_codes  uint8 [batch][n_q][n_heads][d_idx/2]   FP4 indexer queries
+ *   iq_codes  uint8 [batch][n_q][n_heads][d_idx/2]   FP4 indexer queries (16-byte aligned)
  *   iq_scales uint8 [batch][n_q][n_heads][d_idx/16]
  *   w_head    fp32  [batch][n_q][n_heads]
  *   q_pos     int64 [batch][n_q]  raw position of each query (device memory);
