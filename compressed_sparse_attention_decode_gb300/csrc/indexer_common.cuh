@@ -14,7 +14,7 @@ struct QView {
     int* qn;     // [H][DI/4] their negations
     float* qsc;  // [H][DI/16] E4M3 scales as float
     float* w;    // [H]
-    __device__ static int words(int H) { return H * (DI / 4) * 2 + H * (DI / 16) + H; }
+    __host__ __device__ static int words(int H) { return H * (DI / 4) * 2 + H * (DI / 16) + H; }
     __device__ void bind(int* base, int H) {
         qp = base;
         qn = qp + H * (DI / 4);
