@@ -45,8 +45,9 @@ csa2_status check_cache(const csa2_cache* c, bool need_ikey) {
     if (c->d_idx != 64 && c->d_idx != 128) return CSA2_ERR_UNSUPPORTED;
     if (!c->lat_codes || !c->lat_scales || !aligned(c->lat_codes, 16) || !aligned(c->lat_scales, 16))
         return CSA2_ERR_INVALID_ARG;
+    // indexer-key scale rows are d_idx/16 bytes: that is all the alignment their loads need
     if (need_ikey && (!c->ikey_codes || !c->ikey_scales || !aligned(c->ikey_codes, 16) ||
-                      !aligned(c->ikey_scales, 16)))
+                      !aligned(c->ikey_scales, (size_t)(c->d_idx / 16))))
         return CSA2_ERR_INVALID_ARG;
     return CSA2_OK;
 }

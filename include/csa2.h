@@ -63,8 +63,9 @@ enum { CSA2_OP_INDEXER_TOPK = 1, CSA2_OP_REINDEX = 2, CSA2_OP_SPARSE_ATTN = 3 };
  *   ikey_codes  [batch][capacity][d_idx/2]   E2M1 codes of the indexer key
  *   ikey_scales [batch][capacity][d_idx/16]  E4M3 scales of the indexer key
  * Entry i merges raw positions 2i and 2i+1 (encoder compression ratio 2).
- * All four base pointers must be 16-byte aligned.  d_lat must be 512; d_idx
- * must be 64 or 128.
+ * lat_codes, lat_scales and ikey_codes must be 16-byte aligned, ikey_scales
+ * d_idx/16-byte aligned (so a batch-1 view of one sequence of a larger cache
+ * is always valid).  d_lat must be 512; d_idx must be 64 or 128.
  */
 typedef struct {
     uint8_t* lat_codes;
