@@ -39,7 +39,8 @@ class _CacheStruct(ctypes.Structure):
 
 _lib = None
 EXPORTS = ("csa2_cache_write", "csa2_quantize_fp4", "csa2_indexer_topk", "csa2_reindex", "csa2_sparse_attn",
-           "csa2_workspace_size", "csa2_status_string", "csa2_abi_version", "csa2_launch_count")
+           "csa2_workspace_size", "csa2_status_string", "csa2_abi_version", "csa2_launch_count",
+           "csa2_reindex_noalloc")
 
 
 def load(path=None):
@@ -58,6 +59,8 @@ def load(path=None):
     lib.csa2_indexer_topk.argtypes = [cp, vp, vp, vp, i32, vp, i32, i32, vp, i32, i32, vp, vp, sz, vp]
     lib.csa2_reindex.argtypes = [i32, cp, vp, vp, vp, i32, i32, vp, i32, vp, i32, vp, vp, sz, vp]
     lib.csa2_sparse_attn.argtypes = [cp, vp, i32, i32, vp, vp, i32, vp, i64, i32, ctypes.c_float, vp, vp, vp, sz, vp]
+    lib.csa2_reindex_noalloc.argtypes = [cp, vp, vp, vp, i32, i32, vp, i32, i32, vp, vp]
+    lib.csa2_reindex_noalloc.restype = ctypes.c_int
     lib.csa2_workspace_size.argtypes = [i32, i32, i32, i32, i32, i64]
     lib.csa2_workspace_size.restype = sz
     lib.csa2_status_string.argtypes = [ctypes.c_int]
@@ -182,6 +185,19 @@ def csa2_reindex(mode, cache, k, iq_codes=None, iq_scales=None, w_head=None, poo
                              _ptr(pool), pool_len, _ptr(prev_idx), k, _ptr(idx_out), _ptr(ws),
                              ws.numel() if ws is not None else 0, _stream(stream))
     _check(st, "csa2_reindex")
+    return idx_out
+
+
+def csa2_reindex_noalloc(cache, k, iq_codes, iq_scales, w_head, pool, idx_out=None, stream=None):
+    """Reindex with the library's built-in scratch instead of a workspace (for
+    callers that cannot allocate device memory; see include/csa2.h)."""
+    B, n_q, H = iq_codes.shape[0], iq_codes.shape[1], iq_codes.shape[2]
+    if idx_out is None:
+        idx_out = torch.empty((B, n_q, k), dtype=torch.int32, device=iq_codes.device)
+    c = cache.struct()
+    st = load().csa2_reindex_noalloc(ctypes.byref(c), _ptr(iq_codes), _ptr(iq_scales), _ptr(w_head), n_q, H,
+                                     _ptr(pool), pool.shape[-1], k, _ptr(idx_out), _stream(stream))
+    _check(st, "csa2_reindex_noalloc")
     return idx_out
 
 

@@ -167,6 +167,32 @@ csa2_status csa2_sparse_attn(const csa2_cache* cache, const uint16_t* q, int32_t
                              int64_t swa_pos0, int32_t swa_len, float scale, float* out, float* lse,
                              void* workspace, size_t ws_bytes, void* stream);
 
+/*
+ * Reindex without a workspace, for callers that cannot allocate device memory:
+ * for instance a plug-in inside a host application that owns and budgets all
+ * device memory, or a real-time decode loop that must not hit the implicit
+ * device-wide synchronisation of cudaMalloc / cudaFree.  The pages have no
+ * counterpart of this entry point; it is a deployment convenience.
+ *
+ * Same arguments and results as csa2_reindex(CSA2_REINDEX, ...) minus the
+ * workspace (and minus prev_idx, which only Reuse reads).  The scratch is a
+ * fixed 8 MiB array inside the library's device image: every GPU that loads
+ * the library holds those 8 MiB until the process exits.  Requests needing
+ * more (batch * n_q * pool_len above about 233,000 pool slots) return
+ * CSA2_ERR_WORKSPACE and enqueue nothing.  The call allocates and frees
+ * nothing.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array and it keeps the last
+ *     call's contents.  No part of it needs to start at zero.  Calls that can
+ *     overlap on the GPU (different streams, no ordering between them) race
+ *     on it: order them, or give one of them a workspace via csa2_reindex.
+ */
+csa2_status csa2_reindex_noalloc(const csa2_cache* cache, const uint8_t* iq_codes, const uint8_t* iq_scales,
+                                 const float* w_head, int32_t n_q, int32_t n_heads, const int32_t* pool,
+                                 int32_t pool_len, int32_t k, int32_t* idx_out, void* stream);
+
 /* Workspace bytes an operation needs (0 if none).  capacity = entries per
  * sequence of the cache; for CSA2_OP_REINDEX pass pool_len as `capacity`. */
 size_t csa2_workspace_size(int32_t op, int32_t batch, int32_t n_q, int32_t n_heads, int32_t k, int64_t capacity);
