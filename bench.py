@@ -33,7 +33,20 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-sample-seqs", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="decode-128k-b64-20L",
+                    help="decode-128k-b64-20L (the benchmark), or profile-16k-b64-20L: the same 20-layer shape "
+                         "at 16K context (189 MB cache, still larger than L2) for ncu captures")
     return ap.parse_args()
+
+
+def workload_of(name):
+    from synth.workloads import WORKLOADS, scaled
+    wl = WORKLOADS[WORKLOAD_INDEX]
+    if name == wl.name:
+        return wl
+    if name == "profile-16k-b64-20L":
+        return scaled(wl, name=name, T=16384)
+    raise SystemExit("unknown workload %r" % name)
 
 
 def dist_env():
@@ -143,8 +156,7 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    from synth.workloads import WORKLOADS
-    wl = WORKLOADS[WORKLOAD_INDEX]
+    wl = workload_of(args.workload)
     import oracle
     oracle.build()
     n = 1
@@ -184,8 +196,7 @@ def run_ours(args):
     __graft_entry__.build()
     import compressed_sparse_attention_decode_gb300 as csa
     from compressed_sparse_attention_decode_gb300.synthetic import HostInputs, build_step
-    from synth.workloads import WORKLOADS
-    wl = WORKLOADS[WORKLOAD_INDEX]
+    wl = workload_of(args.workload)
 
     def barrier():
         if world > 1:

@@ -156,13 +156,25 @@ cudaError_t launch_sparse_attn_tc(const csa2_cache& c, const uint16_t* q, int n_
                                   const int32_t* idx, int k, const uint16_t* swa, int64_t swa_pos0, int swa_len,
                                   float scale, float* out, float* lse, void* ws, cudaStream_t st);
 
-size_t sparse_attn_ws(int batch, int n_q, int H, int k) { return attn_tc_supported(H) ? attn_tc_ws(batch, n_q, H, k) : 0; }
+bool attn_pair_supported(int H);
+cudaError_t launch_sparse_attn_pair(const csa2_cache& c, const uint16_t* q, int n_q, const int64_t* q_pos,
+                                    const int32_t* idx, int k, const uint16_t* swa, int64_t swa_pos0, int swa_len,
+                                    float scale, float* out, float* lse, int* err, cudaStream_t st);
 
-// tensor-core kernel for head counts it tiles (multiples of 16 up to 64, or of
-// 64 up to 128); the CUDA-core kernel otherwise
+size_t sparse_attn_ws(int batch, int n_q, int H, int k) {
+    if (attn_pair_supported(H)) return 256;
+    return attn_tc_supported(H) ? attn_tc_ws(batch, n_q, H, k) : 0;
+}
+
+// 64 heads: the CTA-pair tensor-core kernel; other head counts the tensor-core
+// tiles take (multiples of 16 up to 64, of 64 up to 128): the per-tile kernel
+// with a combine pass; anything else: the CUDA-core kernel
 cudaError_t launch_sparse_attn(const csa2_cache& c, const uint16_t* q, int n_q, int H, const int64_t* q_pos,
                                const int32_t* idx, int k, const uint16_t* swa, int64_t swa_pos0, int swa_len,
                                float scale, float* out, float* lse, void* ws, size_t, cudaStream_t st) {
+    if (attn_pair_supported(H))
+        return launch_sparse_attn_pair(c, q, n_q, q_pos, idx, k, swa, swa_pos0, swa_len, scale, out, lse,
+                                       reinterpret_cast<int*>(ws), st);
     if (attn_tc_supported(H))
         return launch_sparse_attn_tc(c, q, n_q, H, q_pos, idx, k, swa, swa_pos0, swa_len, scale, out, lse, ws, st);
     return launch_sparse_attn_simt(c, q, n_q, H, q_pos, idx, k, swa, swa_pos0, swa_len, scale, out, lse, st);

@@ -96,12 +96,24 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sparse_attn_tc(
     }
     if (warp == 0) umma::tmem_alloc(umma::smem_u32(&tmem_base), TM_COLS);
 
-    // ---- Q: heads hg*HG .. +HG, bf16 -> fp16, swizzled K-major
-    for (int i = tid; i < HG * 64; i += TC_THREADS) {
-        const int h = i >> 6, c = i & 63;
-        uint4 v = __ldg(reinterpret_cast<const uint4*>(q + ((gq * H + hg * HG + h) * D_LAT + c * 8)));
-        uint4 o = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
-        *reinterpret_cast<uint4*>(sm + SM_Q + (c >> 3) * (HG * 128) + swz(h, c & 7)) = o;
+    // ---- Q: heads hg*HG .. +HG, bf16 -> fp16, swizzled K-major.  All of a
+    // thread's loads are issued before any conversion, so the CTA pays one
+    // memory round trip for Q rather than one per chunk.
+    {
+        constexpr int QCH = HG * 64 / TC_THREADS;           // 16-byte chunks per thread
+        uint4 qv[QCH];
+#pragma unroll
+        for (int u = 0; u < QCH; ++u) {
+            const int i = tid + u * TC_THREADS, h = i >> 6, c = i & 63;
+            qv[u] = __ldg(reinterpret_cast<const uint4*>(q + ((gq * H + hg * HG + h) * D_LAT + c * 8)));
+        }
+#pragma unroll
+        for (int u = 0; u < QCH; ++u) {
+            const int i = tid + u * TC_THREADS, h = i >> 6, c = i & 63;
+            const uint4 v = qv[u];
+            uint4 o = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
+            *reinterpret_cast<uint4*>(sm + SM_Q + (c >> 3) * (HG * 128) + swz(h, c & 7)) = o;
+        }
     }
     // ---- ones (fp16 1.0) for the column sums
     reinterpret_cast<uint4*>(sm + SM_ONES)[tid] = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
@@ -155,13 +167,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sparse_attn_tc(
             }
         } else if (kind == 2) {
             const uint4* wp = reinterpret_cast<const uint4*>(swa + row * D_LAT + half * 256);
-#pragma unroll 8
-            for (int v = 0; v < 32; ++v) {
-                uint4 u = __ldg(wp + v);
-                uint4 o = make_uint4(bf16x2_to_f16x2(u.x), bf16x2_to_f16x2(u.y), bf16x2_to_f16x2(u.z),
-                                     bf16x2_to_f16x2(u.w));
-                const int c = half * 32 + v;
-                *reinterpret_cast<uint4*>(dst + (c >> 3) * SLAB_L + swz(r, c & 7)) = o;
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {          // two batches of 16 loads
+                uint4 wv[16];
+#pragma unroll
+                for (int v = 0; v < 16; ++v) wv[v] = __ldg(wp + part * 16 + v);
+#pragma unroll
+                for (int v = 0; v < 16; ++v) {
+                    const uint4 u = wv[v];
+                    uint4 o = make_uint4(bf16x2_to_f16x2(u.x), bf16x2_to_f16x2(u.y), bf16x2_to_f16x2(u.z),
+                                         bf16x2_to_f16x2(u.w));
+                    const int c = half * 32 + part * 16 + v;
+                    *reinterpret_cast<uint4*>(dst + (c >> 3) * SLAB_L + swz(r, c & 7)) = o;
+                }
             }
         } else {
 #pragma unroll 8

@@ -83,34 +83,6 @@ __global__ void __launch_bounds__(256) k_scan_full(const uint8_t* __restrict__ k
     }
 }
 
-// Reindex scan: the pool slots of each query (entry id pool[t], -1 = empty).
-template <int DI>
-__global__ void __launch_bounds__(256) k_scan_pool(const uint8_t* __restrict__ kc_all, const uint8_t* __restrict__ ks_all,
-                                                   int capacity, const uint8_t* __restrict__ iq_codes,
-                                                   const uint8_t* __restrict__ iq_scales, const float* __restrict__ w_head,
-                                                   const int32_t* __restrict__ pool, int pool_len, int n_q, int H,
-                                                   float2* __restrict__ lu) {
-    extern __shared__ int smem[];
-    const int b = blockIdx.z, q = blockIdx.y;
-    const int64_t gq = (int64_t)b * n_q + q;
-    QView<DI> v;
-    v.bind(smem, H);
-    stage_query<DI>(v, iq_codes + gq * H * (DI / 2), iq_scales + gq * H * (DI / 16), w_head + gq * H, H, threadIdx.x,
-                    blockDim.x);
-    __syncthreads();
-    const int t = blockIdx.x * blockDim.x + threadIdx.x;
-    if (t >= pool_len) return;
-    const int j = pool[gq * pool_len + t];
-    float L = -INFINITY, U = -INFINITY;
-    if (j >= 0 && j < capacity) {
-        KeyRow<DI> kr;
-        const int64_t row = (int64_t)b * capacity + j;
-        kr.load(kc_all + row * (DI / 2), ks_all + row * (DI / 16));
-        approx_score<DI>(kr, v, H, bound_factor(H, DI), L, U);
-    }
-    lu[gq * pool_len + t] = make_float2(L, U);
-}
-
 // ---------------------------------------------------------------- exact selection
 
 struct SelectSmem {
@@ -192,10 +164,32 @@ __device__ void sort_kept(int n, bool desc_by_key, SelectSmem& sm) {
     }
 }
 
+// The k best of m candidates (cid[t], ckey[t]) by (key desc, id asc), sorted,
+// in sm.key/sm.id[0..kept).  When every candidate fits in shared memory (the
+// usual case: k plus the few entries whose bounds straddle the threshold) one
+// bitonic sort does it; otherwise a radix selection cuts them to k first.
+__device__ int best_sorted(const int* cid, const unsigned long long* ckey, int m, int k, SelectSmem& sm) {
+    if (m <= MAX_K) {
+        for (int t = threadIdx.x; t < m; t += blockDim.x) {
+            sm.key[t] = ckey[t];
+            sm.id[t] = cid[t];
+        }
+        __syncthreads();
+        sort_kept(m, true, sm);
+        return m < k ? m : k;
+    }
+    const int kept = keep_best(cid, ckey, m, k, sm);
+    sort_kept(kept, true, sm);
+    return kept;
+}
+
 // One block per (sequence, query).  Items t in [0, n): entry ids[t] (-1 =
 // empty) with bounds lu[t]; n is *count (Full: the forwarded candidates) or
 // n_fixed (Reindex: the pool slots).  Keeps the exact top k; with HSI (Full
-// only) also builds the pool from the forwarded block candidates.
+// only) also builds the pool from the forwarded block candidates.  With lu ==
+// nullptr (Reindex) the block first scores its own pool slots, keeping their
+// bounds in shared memory after the staged query: a pool is small enough that
+// scan and selection fit one launch.
 template <int DI>
 __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids, const float2* __restrict__ lu,
                                                 const int* __restrict__ counts, int n_fixed, int list_len,
@@ -217,7 +211,7 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
     stage_query<DI>(v, iq_codes + gq * H * (DI / 2), iq_scales + gq * H * (DI / 16), w_head + gq * H, H, threadIdx.x,
                     blockDim.x);
     const int32_t* id = ids + slab * list_len;
-    const float2* L = lu + slab * list_len;
+    const float2* L = lu ? lu + slab * list_len : reinterpret_cast<const float2*>(qsm + ((QView<DI>::words(H) + 3) & ~3));
     const int n = counts ? counts[2 * slab] : n_fixed;
     int* cid = c2id + slab * list_len;
     unsigned long long* ckey = c2key + slab * list_len;
@@ -232,6 +226,22 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
         sm.rs.ctl[3] = 0;
     }
     __syncthreads();
+    if (!lu) {
+        // ---- 0. bounds of the pool slots (Reindex)
+        float2* sl = const_cast<float2*>(L);
+        const float fac = bound_factor(H, DI);
+        for (int t = threadIdx.x; t < n; t += blockDim.x) {
+            const int j = entry_of(t);
+            float lo = -INFINITY, hi = -INFINITY;
+            if (j >= 0) {
+                KeyRow<DI> kr;
+                kr.load(kc + (int64_t)j * (DI / 2), ks + (int64_t)j * (DI / 16));
+                approx_score<DI>(kr, v, H, fac, lo, hi);
+            }
+            sl[t] = make_float2(lo, hi);
+        }
+        __syncthreads();
+    }
 
     // ---- 1. k-th largest lower bound, candidates whose upper bound reaches it
     int c = 0;
@@ -269,8 +279,7 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
     }
     __syncthreads();
     // ---- 3. the k best, in rank order
-    const int kept = keep_best(cid, ckey, m, k, sm);
-    sort_kept(kept, true, sm);
+    const int kept = best_sorted(cid, ckey, m, k, sm);
     int32_t* out = idx_out + gq * k;
     for (int t = threadIdx.x; t < k; t += blockDim.x) out[t] = t < kept ? sm.id[t] : -1;
     __syncthreads();
@@ -322,7 +331,8 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
             atomicMax(&ckey[t], f64_key(S));
         }
         __syncthreads();
-        keep_best(cid, ckey, mc, pool_blocks - 1, sm);
+        best_sorted(cid, ckey, mc, pool_blocks - 1, sm);
+        __syncthreads();
         if (threadIdx.x == 0) {
             sm.id[pool_blocks - 1] = nb - 1;
             sm.key[pool_blocks - 1] = 0ull;
@@ -449,17 +459,14 @@ cudaError_t launch_reindex_t(const csa2_cache& c, const uint8_t* iq_codes, const
                              const float* w_head, int n_q, int H, const int32_t* pool, int pool_len, int k,
                              int32_t* idx_out, void* ws, cudaStream_t st) {
     const SelectWs w = carve(ws, (int64_t)c.batch * n_q, pool_len);
-    const size_t qwords = (size_t)QView<DI>::words(H) * sizeof(int);
-    dim3 g1((pool_len + 255) / 256, n_q, c.batch);
-    k_scan_pool<DI><<<g1, 256, qwords, st>>>(c.ikey_codes, c.ikey_scales, c.capacity, iq_codes, iq_scales, w_head,
-                                             pool, pool_len, n_q, H, w.lu);
-    note_launch();
-    cudaError_t e = cudaGetLastError();
+    const size_t qwords = (size_t)((QView<DI>::words(H) + 3) & ~3) * sizeof(int);
+    const size_t smem = qwords + (size_t)pool_len * sizeof(float2);
+    cudaError_t e = cudaFuncSetAttribute(k_select<DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    dim3 g2(n_q, c.batch);
-    k_select<DI><<<g2, 512, qwords, st>>>(pool, w.lu, nullptr, pool_len, pool_len, c.ikey_codes, c.ikey_scales,
-                                          c.capacity, iq_codes, iq_scales, w_head, nullptr, n_q, 0, n_q, H, k,
-                                          idx_out, 0, 1, nullptr, nullptr, nullptr, w.c2id, w.c2key);
+    dim3 g(n_q, c.batch);
+    k_select<DI><<<g, 512, smem, st>>>(pool, nullptr, nullptr, pool_len, pool_len, c.ikey_codes, c.ikey_scales,
+                                       c.capacity, iq_codes, iq_scales, w_head, nullptr, n_q, 0, n_q, H, k, idx_out, 0,
+                                       1, nullptr, nullptr, nullptr, w.c2id, w.c2key);
     note_launch();
     return cudaGetLastError();
 }

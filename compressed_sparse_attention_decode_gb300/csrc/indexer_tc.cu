@@ -13,8 +13,10 @@
 // candidates are forwarded exactly as there.
 //
 // Warp roles (256 threads): warps 0-3 epilogue (one TMEM lane = one entry),
-// warp 4 lane 0 issues the MMAs, warps 5-7 load key rows.  Four A slots and two
-// TMEM accumulators keep loads, MMAs and epilogues overlapped.
+// warp 4 lane 0 issues the MMAs, warp 5 lane 0 issues 1-D bulk copies of each
+// tile's contiguous key rows (8 KB codes + 1 KB scales, four tiles in flight),
+// warps 6-7 expand the packed codes into the padded MMA layout.  Two A slots
+// and two TMEM accumulators keep copies, MMAs and epilogues overlapped.
 #include "indexer_common.cuh"
 #include "umma.cuh"
 
@@ -22,17 +24,19 @@ namespace csa2 {
 
 constexpr int ITC_E = 4096;                 // entries per block
 constexpr int ITC_TILE = 128;
-constexpr int ITC_NBUF = 4;
+constexpr int ITC_NR = 4;                   // raw staging slots (bulk-copy depth)
+constexpr int ITC_NA = 2;                   // MMA-layout A slots
 constexpr int ITC_DI = 128;
 constexpr int ITC_G = ITC_DI / 16;
-constexpr int ITC_LOADERS = 96;             // warps 5-7
+constexpr int ITC_XFORM = 64;               // warps 6-7 expand raw codes into the MMA layout
 // shared memory (from the 1024-aligned base)
 constexpr int ITC_H = 8;                    // indexer heads taken by this kernel
 constexpr int ITC_N = ITC_H * ITC_G;        // MMA N: one column per (head, group)
 constexpr uint32_t IS_B = 0;                                  // query operand, 64 rows x 128 B
-constexpr uint32_t IS_A = ITC_N * 128;                        // 4 slots x 128 rows x 128 B
-constexpr uint32_t IS_SK = IS_A + ITC_NBUF * ITC_TILE * 128;  // 4 slots x 128 rows x 8 B scales
-constexpr uint32_t IS_LU = IS_SK + ITC_NBUF * ITC_TILE * 8;   // 4096 float2
+constexpr uint32_t IS_A = ITC_N * 128;                        // 2 slots x 128 rows x 128 B
+constexpr uint32_t RAW_SLOT = ITC_TILE * (ITC_DI / 2) + ITC_TILE * 8;   // codes 8 KB + scales 1 KB
+constexpr uint32_t IS_RAW = IS_A + ITC_NA * ITC_TILE * 128;   // 4 slots of raw rows
+constexpr uint32_t IS_LU = IS_RAW + ITC_NR * RAW_SLOT;        // 4096 float2
 constexpr uint32_t IS_Q = IS_LU + ITC_E * 8;                  // sq [H][G] floats + w [H]
 constexpr uint32_t IS_END = IS_Q + 2048;
 constexpr uint32_t IS_DYN = IS_END + 1024;
@@ -47,7 +51,8 @@ __global__ void __launch_bounds__(256, 2) k_scan_full_tc(
     float2* __restrict__ blu, int list_len, int* __restrict__ err) {
     extern __shared__ uint8_t dyn[];
     __shared__ RadixSmem rs;
-    __shared__ __align__(8) unsigned long long bar_full[ITC_NBUF], bar_empty[ITC_NBUF], bar_dfull[2], bar_dfree[2];
+    __shared__ __align__(8) unsigned long long bar_rfull[ITC_NR], bar_rfree[ITC_NR], bar_afull[ITC_NA], bar_afree[ITC_NA],
+        bar_dfull[2], bar_dfree[2];
     __shared__ uint32_t tmem_base;
     __shared__ int s_nel;
 
@@ -62,9 +67,13 @@ __global__ void __launch_bounds__(256, 2) k_scan_full_tc(
 
     if (tid == 0) {
         s_nel = n_elig_of(q_pos[gq], capacity);
-        for (int i = 0; i < ITC_NBUF; ++i) {
-            umma::mbar_init(umma::smem_u32(&bar_full[i]), ITC_LOADERS);
-            umma::mbar_init(umma::smem_u32(&bar_empty[i]), 128);
+        for (int i = 0; i < ITC_NR; ++i) {
+            umma::mbar_init(umma::smem_u32(&bar_rfull[i]), 1);
+            umma::mbar_init(umma::smem_u32(&bar_rfree[i]), 128);
+        }
+        for (int i = 0; i < ITC_NA; ++i) {
+            umma::mbar_init(umma::smem_u32(&bar_afull[i]), ITC_XFORM);
+            umma::mbar_init(umma::smem_u32(&bar_afree[i]), 1);
         }
         for (int i = 0; i < 2; ++i) {
             umma::mbar_init(umma::smem_u32(&bar_dfull[i]), 1);
@@ -90,7 +99,7 @@ __global__ void __launch_bounds__(256, 2) k_scan_full_tc(
     for (int i = tid; i < H * ITC_G; i += blockDim.x) sq[i] = e4m3_to_f32(iq_scales[gq * H * ITC_G + i]);
     for (int i = tid; i < H; i += blockDim.x) ww[i] = w_head[gq * H + i];
     // zero the A slots once: the pad half of every 16-byte unit stays zero
-    for (int i = tid; i < ITC_NBUF * ITC_TILE * 8; i += blockDim.x)
+    for (int i = tid; i < ITC_NA * ITC_TILE * 8; i += blockDim.x)
         reinterpret_cast<uint4*>(sm + IS_A)[i] = make_uint4(0, 0, 0, 0);
     if (warp == 0) umma::tmem_alloc(umma::smem_u32(&tmem_base), 128);
     umma::fence_proxy_async();
@@ -104,44 +113,58 @@ __global__ void __launch_bounds__(256, 2) k_scan_full_tc(
     float2* slu = reinterpret_cast<float2*>(sm + IS_LU);
     bool ok = true;
 
-    if (warp >= 5) {
-        // ---- loaders: codes (8 bytes per group -> the data half of a unit) and scales
-        const int lt = tid - 160;
-        for (int t = 0; t < n_tiles; ++t) {
-            const int s = t % ITC_NBUF;
-            if (t >= ITC_NBUF) ok &= umma::mbar_wait(umma::smem_u32(&bar_empty[s]), ((t / ITC_NBUF) - 1) & 1);
-            uint8_t* a = sm + IS_A + s * (ITC_TILE * 128);
-            const int e0 = c0 + t * ITC_TILE;
-            const uint8_t* src = kc_all + ((int64_t)b * capacity + e0) * (ITC_DI / 2);
-            for (int c = lt; c < ITC_TILE * 4; c += ITC_LOADERS) {       // 16-byte chunks of codes
-                const int r = c >> 2, q4 = c & 3;
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (e0 + r < n_elig) v = __ldg(reinterpret_cast<const uint4*>(src) + c);
-                *reinterpret_cast<uint2*>(a + swz128(r, 2 * q4)) = make_uint2(v.x, v.y);
-                *reinterpret_cast<uint2*>(a + swz128(r, 2 * q4 + 1)) = make_uint2(v.z, v.w);
+    // scale rows are 8 bytes; a bulk copy needs a 16-byte aligned source
+    const uint8_t* ks_seq = ks_all + ((int64_t)b * capacity + c0) * ITC_G;
+    const bool bulk_scales = ((reinterpret_cast<uintptr_t>(ks_seq) & 15u) == 0);
+    if (warp == 5) {
+        // ---- bulk-copy issuer
+        if (lane == 0) {
+            for (int t = 0; t < n_tiles; ++t) {
+                const int r = t % ITC_NR;
+                if (t >= ITC_NR) ok &= umma::mbar_wait(umma::smem_u32(&bar_rfree[r]), ((t / ITC_NR) - 1) & 1);
+                const int e0 = c0 + t * ITC_TILE;
+                const int rows = min(ITC_TILE, n_elig - e0);
+                const uint32_t cb = (uint32_t)rows * (ITC_DI / 2);
+                const uint32_t sbytes = bulk_scales ? (uint32_t)(rows & ~1) * ITC_G : 0u;
+                const uint32_t mb = umma::smem_u32(&bar_rfull[r]);
+                const uint32_t dst = base + IS_RAW + r * RAW_SLOT;
+                umma::mbar_arrive_expect_tx(mb, cb + sbytes);
+                umma::bulk_g2s(dst, kc_all + ((int64_t)b * capacity + e0) * (ITC_DI / 2), cb, mb);
+                if (sbytes) umma::bulk_g2s(dst + ITC_TILE * (ITC_DI / 2), ks_all + ((int64_t)b * capacity + e0) * ITC_G, sbytes, mb);
             }
-            const uint8_t* ssrc = ks_all + ((int64_t)b * capacity + e0) * ITC_G;
-            uint8_t* sk = sm + IS_SK + s * (ITC_TILE * 8);
-            for (int r = lt; r < ITC_TILE; r += ITC_LOADERS) {             // 8 scale bytes per row
-                uint2 v = make_uint2(0, 0);
-                if (e0 + r < n_elig) v = __ldg(reinterpret_cast<const uint2*>(ssrc) + r);
-                reinterpret_cast<uint2*>(sk)[r] = v;
+        }
+    } else if (warp >= 6) {
+        // ---- expand packed codes (8 bytes per 16-value group) into the data half of each 16-byte unit
+        const int xt = tid - 192;
+        for (int t = 0; t < n_tiles; ++t) {
+            const int r = t % ITC_NR, a = t % ITC_NA;
+            ok &= umma::mbar_wait(umma::smem_u32(&bar_rfull[r]), (t / ITC_NR) & 1);
+            if (t >= ITC_NA) ok &= umma::mbar_wait(umma::smem_u32(&bar_afree[a]), ((t / ITC_NA) - 1) & 1);
+            const uint4* raw = reinterpret_cast<const uint4*>(sm + IS_RAW + r * RAW_SLOT);
+            uint8_t* as = sm + IS_A + a * (ITC_TILE * 128);
+#pragma unroll 4
+            for (int c = xt; c < ITC_TILE * 4; c += ITC_XFORM) {
+                const int row = c >> 2, q4 = c & 3;
+                const uint4 v = raw[c];
+                *reinterpret_cast<uint2*>(as + swz128(row, 2 * q4)) = make_uint2(v.x, v.y);
+                *reinterpret_cast<uint2*>(as + swz128(row, 2 * q4 + 1)) = make_uint2(v.z, v.w);
             }
             umma::fence_proxy_async();
-            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(umma::smem_u32(&bar_full[s])) : "memory");
+            umma::mbar_arrive(umma::smem_u32(&bar_afull[a]));
         }
     } else if (warp == 4) {
         // ---- MMA issuer
         if (lane == 0) {
             const uint32_t idesc = (1u << 4) | (5u << 7) | (5u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
             for (int t = 0; t < n_tiles; ++t) {
-                const int s = t % ITC_NBUF, d = t & 1;
-                ok &= umma::mbar_wait(umma::smem_u32(&bar_full[s]), (t / ITC_NBUF) & 1);
+                const int s = t % ITC_NA, d = t & 1;
+                ok &= umma::mbar_wait(umma::smem_u32(&bar_afull[s]), (t / ITC_NA) & 1);
                 if (t >= 2) ok &= umma::mbar_wait(umma::smem_u32(&bar_dfree[d]), ((t >> 1) - 1) & 1);
                 umma::fence_after();
 #pragma unroll
                 for (int ks = 0; ks < ITC_DI / 32; ++ks) {
-                    const uint64_t ad = umma::desc(base + IS_A + s * (ITC_TILE * 128) + ks * 32, 16, 1024, umma::LAYOUT_SW128);
+                    const uint64_t ad = umma::desc(base + IS_A + s * (ITC_TILE * 128) + ks * 32, 16, 1024,
+                                                   umma::LAYOUT_SW128);
                     const uint64_t bd = umma::desc(base + IS_B + ks * 32, 16, 1024, umma::LAYOUT_SW128);
                     asm volatile(
                         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
@@ -149,13 +172,14 @@ __global__ void __launch_bounds__(256, 2) k_scan_full_tc(
                         "l"(ad), "l"(bd), "r"(idesc), "r"(ks));
                 }
                 umma::commit(umma::smem_u32(&bar_dfull[d]));
+                umma::commit(umma::smem_u32(&bar_afree[s]));
             }
         }
     } else {
         // ---- epilogue: one entry per thread
         const float fac = bound_factor(H, ITC_DI);
         for (int t = 0; t < n_tiles; ++t) {
-            const int s = t % ITC_NBUF, d = t & 1;
+            const int s = t % ITC_NR, d = t & 1;
             ok &= umma::mbar_wait(umma::smem_u32(&bar_dfull[d]), (t >> 1) & 1);
             umma::fence_after();
             float dv[64];
@@ -164,10 +188,18 @@ __global__ void __launch_bounds__(256, 2) k_scan_full_tc(
             for (int c = 0; c < N; c += 16) umma::tmem_ld16(lane_base + c, dv + c);
             umma::tmem_wait_ld();
             umma::fence_before();
-            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(umma::smem_u32(&bar_dfree[d])) : "memory");
+            umma::mbar_arrive(umma::smem_u32(&bar_dfree[d]));
             const int r = tid;                          // row of the tile = TMEM lane
-            const uint2 skw = *reinterpret_cast<const uint2*>(sm + IS_SK + s * (ITC_TILE * 8) + r * 8);
-            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(umma::smem_u32(&bar_empty[s])) : "memory");
+            const int e0 = c0 + t * ITC_TILE;
+            const int rows = min(ITC_TILE, n_elig - e0);
+            uint2 skw = make_uint2(0, 0);
+            // the scales landed with this slot's bulk copy: observe that barrier phase too
+            if (bulk_scales) ok &= umma::mbar_wait(umma::smem_u32(&bar_rfull[s]), (t / ITC_NR) & 1);
+            if (bulk_scales && r < (rows & ~1))
+                skw = *reinterpret_cast<const uint2*>(sm + IS_RAW + s * RAW_SLOT + ITC_TILE * (ITC_DI / 2) + r * 8);
+            else if (r < rows)
+                skw = __ldg(reinterpret_cast<const uint2*>(ks_all + ((int64_t)b * capacity + e0 + r) * ITC_G));
+            umma::mbar_arrive(umma::smem_u32(&bar_rfree[s]));
             float skf[ITC_G];
 #pragma unroll
             for (int g = 0; g < ITC_G; ++g) skf[g] = e4m3_to_f32(((g < 4 ? skw.x : skw.y) >> (8 * (g & 3))) & 255u);
