@@ -147,6 +147,12 @@ def test_pool_edge_cases(csa):
         check_walk(csa, wl, [0, 1])
 
 
+def test_pages_hsi_example_pool_of_16384(csa):
+    """the pool size of the pages' own example: 2048 blocks x 8 entries"""
+    wl = scaled(WORKLOADS[2], B=2, T=65536, pool_blocks=2048, layers=("full", "reindex", "reuse"))
+    check_walk(csa, wl, [0, 1])
+
+
 def test_short_contexts_pad_with_minus_one(csa):
     for T in (128, 130, 200, 256):
         wl = scaled(WORKLOADS[0], T=T, k=64)
