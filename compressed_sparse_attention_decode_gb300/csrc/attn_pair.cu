@@ -220,44 +220,63 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
             const uint32_t id1 = umma::idesc_f16(128, AP_H, 0, 0);
             const uint32_t id2 = umma::idesc_f16(128, AP_H, 1, 1);
             const uint32_t id3 = umma::idesc_f16(128, AP_H, 0, 1);
-            auto gemm1 = [&](int t) {
-                const int buf = t & 1;
-                ok &= umma::mbar_wait(sa(&b_lfull[buf]), (t >> 1) & 1);
-                if (t >= 2) ok &= umma::mbar_wait(sa(&b_sfree[buf]), ((t >> 1) - 1) & 1);
-                umma::fence_after();
-                const uint32_t Lb = base + AP_SL + buf * AP_LBUF;
+            // Two independent streams: GEMM1 of tile t needs its half rows loaded
+            // (lfull) and its score buffer released (sfree of tile t-2); GEMM2 of
+            // tile t needs P (pfull).  Serve whichever is ready, so a slow load of
+            // tile t+1 never holds back the value GEMM of tile t.
+            int n1 = 0, n2 = 0;
+            uint32_t spins = 0;
+            while (n2 < T) {
+                bool progressed = false;
+                if (n1 < T && n1 <= n2 + 1) {
+                    const int buf = n1 & 1;
+                    if (umma::mbar_test(sa(&b_lfull[buf]), (n1 >> 1) & 1) &&
+                        (n1 < 2 || umma::mbar_test(sa(&b_sfree[buf]), ((n1 >> 1) - 1) & 1))) {
+                        umma::fence_after();
+                        const uint32_t Lb = base + AP_SL + buf * AP_LBUF;
 #pragma unroll
-                for (int ks = 0; ks < 16; ++ks) {
-                    const uint64_t a = umma::desc(Lb + (ks >> 2) * AP_SLAB + (ks & 3) * 32, 16, 1024, umma::LAYOUT_SW128);
-                    const uint64_t bq = umma::desc(base + AP_SQ + (ks >> 2) * (AP_H * 128) + (ks & 3) * 32, 16, 1024,
-                                                   umma::LAYOUT_SW128);
-                    umma::mma_f16(tmem + APT_S + 64 * buf, a, bq, id1, ks > 0);
-                }
-                umma::commit(sa(&b_sfull[buf]));
-            };
-            gemm1(0);
-            for (int t = 0; t < T; ++t) {
-                if (t + 1 < T) gemm1(t + 1);
-                ok &= umma::mbar_wait(sa(&b_pfull), t & 1);
-                umma::fence_after();
-                const int buf = t & 1;
-                const uint32_t Lb = base + AP_SL + buf * AP_LBUF;
-                for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint64_t a = umma::desc(Lb + (2 * mt) * AP_SLAB + ks * 2048, AP_SLAB, 1024, umma::LAYOUT_SW128);
-                        const uint64_t bp = umma::desc(base + AP_SP + ks * 2048, 8192, 1024, umma::LAYOUT_SW128);
-                        umma::mma_f16(tmem + APT_O + 64 * mt, a, bp, id2, (t > 0 || ks > 0) ? 1u : 0u);
+                        for (int ks = 0; ks < 16; ++ks) {
+                            const uint64_t a = umma::desc(Lb + (ks >> 2) * AP_SLAB + (ks & 3) * 32, 16, 1024,
+                                                          umma::LAYOUT_SW128);
+                            const uint64_t bq = umma::desc(base + AP_SQ + (ks >> 2) * (AP_H * 128) + (ks & 3) * 32, 16,
+                                                           1024, umma::LAYOUT_SW128);
+                            umma::mma_f16(tmem + APT_S + 64 * buf, a, bq, id1, ks > 0);
+                        }
+                        umma::commit(sa(&b_sfull[buf]));
+                        ++n1;
+                        progressed = true;
                     }
                 }
+                if (n2 < n1 && umma::mbar_test(sa(&b_pfull), n2 & 1)) {
+                    umma::fence_after();
+                    const int buf = n2 & 1;
+                    const uint32_t Lb = base + AP_SL + buf * AP_LBUF;
+                    for (int mt = 0; mt < 2; ++mt) {
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint64_t a = umma::desc(base + AP_SONES, 128, 256, umma::LAYOUT_NONE);
-                    const uint64_t bp = umma::desc(base + AP_SP + ks * 2048, 8192, 1024, umma::LAYOUT_SW128);
-                    umma::mma_f16(tmem + APT_L, a, bp, id3, (t > 0 || ks > 0) ? 1u : 0u);
+                        for (int ks = 0; ks < 8; ++ks) {
+                            const uint64_t a = umma::desc(Lb + (2 * mt) * AP_SLAB + ks * 2048, AP_SLAB, 1024,
+                                                          umma::LAYOUT_SW128);
+                            const uint64_t bp = umma::desc(base + AP_SP + ks * 2048, 8192, 1024, umma::LAYOUT_SW128);
+                            umma::mma_f16(tmem + APT_O + 64 * mt, a, bp, id2, (n2 > 0 || ks > 0) ? 1u : 0u);
+                        }
+                    }
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint64_t a = umma::desc(base + AP_SONES, 128, 256, umma::LAYOUT_NONE);
+                        const uint64_t bp = umma::desc(base + AP_SP + ks * 2048, 8192, 1024, umma::LAYOUT_SW128);
+                        umma::mma_f16(tmem + APT_L, a, bp, id3, (n2 > 0 || ks > 0) ? 1u : 0u);
+                    }
+                    umma::commit(sa(&b_odone));
+                    umma::commit(sa(&b_lfree[buf]));
+                    ++n2;
+                    progressed = true;
                 }
-                umma::commit(sa(&b_odone));
-                umma::commit(sa(&b_lfree[buf]));
+                if (progressed) {
+                    spins = 0;
+                } else if (++spins > (1u << 26)) {     // nothing moved for far too long: give up
+                    ok = false;
+                    break;
+                }
             }
         }
     } else {

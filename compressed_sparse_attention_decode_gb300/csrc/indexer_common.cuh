@@ -8,18 +8,27 @@ namespace csa2 {
 
 // ---------------------------------------------------------------- query staging
 
+// E4M3 value times 2^9: every E4M3 value is a multiple of 2^-9 (the smallest
+// subnormal), so this is an integer; at most 448 * 512 = 229,376
+__device__ __forceinline__ int e4m3_times_512(uint32_t b) {
+    const uint32_t e = (b >> 3) & 15u, m = b & 7u;
+    return e ? (int)((8u + m) << (e - 1u)) : (int)m;
+}
+
 template <int DI>
 struct QView {
     int* qp;     // [H][DI/4] doubled E2M1 values, int8 x4
     int* qn;     // [H][DI/4] their negations
     float* qsc;  // [H][DI/16] E4M3 scales as float
+    int* qsi;    // [H][DI/16] the same scales times 2^9 (integers < 2^18)
     float* w;    // [H]
-    __host__ __device__ static int words(int H) { return H * (DI / 4) * 2 + H * (DI / 16) + H; }
+    __host__ __device__ static int words(int H) { return H * (DI / 4) * 2 + 2 * H * (DI / 16) + H; }
     __device__ void bind(int* base, int H) {
         qp = base;
         qn = qp + H * (DI / 4);
         qsc = reinterpret_cast<float*>(qn + H * (DI / 4));
-        w = qsc + H * (DI / 16);
+        qsi = reinterpret_cast<int*>(qsc + H * (DI / 16));
+        w = reinterpret_cast<float*>(qsi + H * (DI / 16));
     }
 };
 
@@ -33,7 +42,10 @@ __device__ void stage_query(QView<DI> v, const uint8_t* __restrict__ codes, cons
         v.qp[i] = (int)__vsub4(p, n);
         v.qn[i] = (int)__vsub4(n, p);
     }
-    for (int i = tid; i < H * (DI / 16); i += nthr) v.qsc[i] = e4m3_to_f32(scales[i]);
+    for (int i = tid; i < H * (DI / 16); i += nthr) {
+        v.qsc[i] = e4m3_to_f32(scales[i]);
+        v.qsi[i] = e4m3_times_512(scales[i]);
+    }
     for (int i = tid; i < H; i += nthr) v.w[i] = w[i];
 }
 
@@ -89,20 +101,34 @@ __device__ __forceinline__ void approx_score(const KeyRow<DI>& k, QView<DI> q, i
     U = S + E;
 }
 
-// the exact score: integer group sums, exact fp64 group terms and sum, fp64
-// fused multiply-add chain over heads in ascending order
+// The exact score.  With 2^9-scaled integer scales Sq, Sk and the doubled-code
+// group sum G4 = sum 2q*2k, a group term is G4 * Sq * Sk * 2^-20 exactly, so
+// d_h * 2^20 is an integer (|.| < 2^51) summed in int64 and converted to fp64
+// without rounding; then the fp64 fused multiply-add chain over heads in
+// ascending order.  Only 2-3 fp64 operations per head remain.
 template <int DI>
 __device__ double exact_score(const uint8_t* __restrict__ kc, const uint8_t* __restrict__ ks, QView<DI> q, int H) {
     KeyRow<DI> k;
     k.load(kc, ks);
+    int ski[DI / 16];
+    if (DI == 128) {
+        const uint2 s = __ldg(reinterpret_cast<const uint2*>(ks));
+#pragma unroll
+        for (int g = 0; g < DI / 16; ++g) ski[g] = e4m3_times_512(((g < 4 ? s.x : s.y) >> (8 * (g & 3))) & 255u);
+    } else {
+        const uint32_t s = __ldg(reinterpret_cast<const uint32_t*>(ks));
+#pragma unroll
+        for (int g = 0; g < DI / 16; ++g) ski[g] = e4m3_times_512((s >> (8 * (g & 3))) & 255u);
+    }
     double S = 0.0;
     for (int h = 0; h < H; ++h) {
-        double d = 0.0;
+        long long D = 0;
 #pragma unroll
         for (int g = 0; g < DI / 16; ++g) {
-            int G = group_dot4(q.qp + h * (DI / 4) + 4 * g, q.qn + h * (DI / 4) + 4 * g, k.kp + 4 * g, k.kn + 4 * g);
-            d += (double)G * ((double)q.qsc[h * (DI / 16) + g] * (double)k.sk[g] * 0.25);
+            const int G4 = group_dot4(q.qp + h * (DI / 4) + 4 * g, q.qn + h * (DI / 4) + 4 * g, k.kp + 4 * g, k.kn + 4 * g);
+            D += (long long)(G4 * q.qsi[h * (DI / 16) + g]) * ski[g];     // |G4*Sq| < 2^30
         }
+        const double d = (double)D * 0x1p-20;                               // exact: |D| < 2^51
         S = fma((double)q.w[h], d > 0.0 ? d : 0.0, S);
     }
     return S;

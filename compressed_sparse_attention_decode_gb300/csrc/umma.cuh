@@ -53,6 +53,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, uint32
     return false;
 }
 
+// one non-blocking test of an mbarrier phase
+__device__ __forceinline__ bool mbar_test(uint32_t mbar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(done)
+        : "r"(mbar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
 // wait with cluster-scope acquire (the arrivals come from the peer CTA)
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t mbar, uint32_t parity, uint32_t max_iter = 1u << 24) {
     uint32_t done = 0;
