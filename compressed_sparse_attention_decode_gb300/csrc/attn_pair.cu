@@ -14,9 +14,10 @@
 // tile overlap the MMAs and softmax of this one; nothing goes through global
 // memory between tiles and each CTA writes its 256 output dims at the end.
 //
-// Warps: 0-3 softmax / epilogue (TMEM lane = key row, later = output dim),
-// warp 4 issues the MMAs, warps 5-15 gather rows.  Tile 0 holds the window
-// rows (bf16, loaded while Q is staged), tiles 1.. the selected FP4 entries.
+// Warps: 0-7 softmax / epilogue (warp w reads TMEM lanes 32(w%4).. = key rows,
+// later output dims, for heads 32(w/4)..+31), warp 8 issues the MMAs, warps
+// 9-15 gather rows.  Tiles 0.. hold the selected FP4 entries, the last tile the
+// window rows (bf16), whose slower load then overlaps earlier tiles' work.
 #include "common.cuh"
 #include "umma.cuh"
 
@@ -25,7 +26,10 @@ namespace csa2 {
 constexpr int AP_TILE = 128;
 constexpr int AP_H = 64;
 constexpr int AP_THREADS = 512;
-constexpr int AP_LOADERS = 352;                      // warps 5-15
+constexpr int AP_SMW = 8;                            // softmax warps 0-7: lane quadrant x head half
+constexpr int AP_SMT = AP_SMW * 32;
+constexpr int AP_MMAW = 8;                           // warp 8 issues the MMAs
+constexpr int AP_LOADERS = 224;                      // warps 9-15
 constexpr uint32_t AP_SLAB = AP_TILE * 128;          // 64 dims x 128 keys x fp16
 constexpr uint32_t AP_SQ = 0;                        // Q half: 4 slabs x 64 heads x 128 B = 32 KB
 constexpr uint32_t AP_SL = 32 * 1024;                // 2 buffers x 4 slabs (128 KB)
@@ -101,12 +105,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
             umma::mbar_init(sa(&b_lfull[i]), AP_LOADERS);
             umma::mbar_init(sa(&b_lfree[i]), 1);
             umma::mbar_init(sa(&b_sfull[i]), 1);
-            umma::mbar_init(sa(&b_sfree[i]), 128);
+            umma::mbar_init(sa(&b_sfree[i]), AP_SMT);
         }
-        umma::mbar_init(sa(&b_pfull), 128);
+        umma::mbar_init(sa(&b_pfull), AP_SMT);
         umma::mbar_init(sa(&b_odone), 1);
-        umma::mbar_init(sa(&b_xfull), 128);
-        umma::mbar_init(sa(&b_xfree), 128);
+        umma::mbar_init(sa(&b_xfull), AP_SMT);
+        umma::mbar_init(sa(&b_xfree), AP_SMT);
         umma::fence_mbar_init();
     }
     if (warp == 0) umma::tmem_alloc(sa(&tmem_base), APT_COLS);
@@ -140,14 +144,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
     const uint32_t tmem = tmem_base;
     bool ok = true;
 
-    if (warp >= 5) {
+    if (warp > AP_MMAW) {
         // ================= loaders
-        const int lt = tid - 160;
+        const int lt = tid - (AP_MMAW + 1) * 32;
         for (int t = 0; t < T; ++t) {
             const int buf = t & 1;
             if (t >= 2) ok &= umma::mbar_wait(sa(&b_lfree[buf]), ((t >> 1) - 1) & 1);
             uint8_t* L = sm + AP_SL + buf * AP_LBUF;
-            if (t == 0) {
+            if (t == T - 1) {
                 // window rows: 128 rows x 4 units of 64 dims (8 x 16 B of bf16)
                 for (int u = lt; u < AP_TILE * 4; u += AP_LOADERS) {
                     const int r = u >> 2, part = u & 3;
@@ -170,51 +174,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                     }
                     if (part == 0) rowok[buf][r] = valid;
                 }
-            } else {
-                // selected FP4 entries: 128 rows x 2 units of 128 dims (64 B codes + 8 B scales)
-                if (lt < AP_TILE * 2) {
-                    const int r = lt >> 1, part = lt & 1;
-                    const int slot = (t - 1) * AP_TILE + r;
-                    int j = -1;
-                    if (slot < k) {
-                        j = idx[gq * k + slot];
-                        if (j < 0 || j >= capacity) j = -1;
-                    }
-                    uint4 cw[4];
-                    uint2 sc = make_uint2(0, 0);
-                    if (j >= 0) {
-                        const int64_t row = (int64_t)b * capacity + j;
-                        const uint4* cp = reinterpret_cast<const uint4*>(lat_codes + row * (D_LAT / 2) + (d0 + part * 128) / 2);
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) cw[v] = __ldg(cp + v);
-                        sc = __ldg(reinterpret_cast<const uint2*>(lat_scales + row * (D_LAT / 16) + (d0 + part * 128) / 16));
-                    }
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) {            // 32 dims = 2 scale groups
-                        const uint32_t words[4] = {cw[v].x, cw[v].y, cw[v].z, cw[v].w};
-#pragma unroll
-                        for (int w = 0; w < 4; ++w) {        // 8 dims = one 16-byte chunk
-                            uint4 o = make_uint4(0, 0, 0, 0);
-                            if (j >= 0) {
-                                const int g = 2 * v + (w >> 1);
-                                const float sf = e4m3_to_f32(((g < 4 ? sc.x : sc.y) >> (8 * (g & 3))) & 255u);
-                                const __half2 s2 = __float2half2_rn(sf);
-                                uint32_t f[4];
-                                ap_e2m1x8(words[w], f);
-                                o = make_uint4(ap_hmul2(f[0], s2), ap_hmul2(f[1], s2), ap_hmul2(f[2], s2),
-                                               ap_hmul2(f[3], s2));
-                            }
-                            const int c = part * 16 + v * 4 + w;   // 8-dim chunk 0..31
-                            *reinterpret_cast<uint4*>(L + (c >> 3) * AP_SLAB + apswz(r, c & 7)) = o;
-                        }
-                    }
-                    if (part == 0) rowok[buf][r] = j >= 0;
+            } else if (lt < AP_TILE) {
+                // selected FP4 entries: one row per thread, this CTA's 256 dims (128 B codes + 16 B scales)
+                const int r = lt;
+                const int slot = t * AP_TILE + r;
+                int j = -1;
+                if (slot < k) {
+                    j = idx[gq * k + slot];
+                    if (j < 0 || j >= capacity) j = -1;
                 }
+                uint4 cw[8];
+                uint4 sc = make_uint4(0, 0, 0, 0);
+                if (j >= 0) {
+                    const int64_t row = (int64_t)b * capacity + j;
+                    const uint4* cp = reinterpret_cast<const uint4*>(lat_codes + row * (D_LAT / 2) + d0 / 2);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) cw[v] = __ldg(cp + v);
+                    sc = __ldg(reinterpret_cast<const uint4*>(lat_scales + row * (D_LAT / 16) + d0 / 16));
+                }
+                const uint32_t sw[4] = {sc.x, sc.y, sc.z, sc.w};
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {            // 32 dims = 2 scale groups
+                    const uint32_t words[4] = {cw[v].x, cw[v].y, cw[v].z, cw[v].w};
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {        // 8 dims = one 16-byte chunk
+                        uint4 o = make_uint4(0, 0, 0, 0);
+                        if (j >= 0) {
+                            const int g = 2 * v + (w >> 1);
+                            const float sf = e4m3_to_f32((sw[g >> 2] >> (8 * (g & 3))) & 255u);
+                            const __half2 s2 = __float2half2_rn(sf);
+                            uint32_t f[4];
+                            ap_e2m1x8(words[w], f);
+                            o = make_uint4(ap_hmul2(f[0], s2), ap_hmul2(f[1], s2), ap_hmul2(f[2], s2),
+                                           ap_hmul2(f[3], s2));
+                        }
+                        const int c = v * 4 + w;                 // 8-dim chunk 0..31
+                        *reinterpret_cast<uint4*>(L + (c >> 3) * AP_SLAB + apswz(r, c & 7)) = o;
+                    }
+                }
+                rowok[buf][r] = j >= 0;
             }
             umma::fence_proxy_async();
             umma::mbar_arrive(sa(&b_lfull[buf]));
         }
-    } else if (warp == 4) {
+    } else if (warp == AP_MMAW) {
         // ================= MMA issuer
         if (lane == 0) {
             const uint32_t id1 = umma::idesc_f16(128, AP_H, 0, 0);
@@ -279,35 +282,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                 }
             }
         }
-    } else {
-        // ================= softmax (thread = key row of the tile)
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    } else if (warp < AP_SMW) {
+        // ================= softmax: thread = key row 32*(warp%4)+lane, heads hh*32 .. +31
+        const int qd = warp & 3, hh = warp >> 2;
+        const int row = qd * 32 + lane;
+        const int hc = hh * 32;
+        const uint32_t lane_base = tmem + ((uint32_t)(qd * 32) << 16);
         const uint32_t sx_peer = umma::mapa(base + AP_SX, peer);
         const uint32_t xfull_peer = umma::mapa(sa(&b_xfull), peer);
         const uint32_t xfree_peer = umma::mapa(sa(&b_xfree), peer);
-        float* red = reinterpret_cast<float*>(sm + AP_RED);
+        float* red = reinterpret_cast<float*>(sm + AP_RED);           // [4 quadrants][64 heads]
         const float* sx = reinterpret_cast<const float*>(sm + AP_SX);
         for (int t = 0; t < T; ++t) {
             const int buf = t & 1;
-            float x[AP_H];
+            float x[32];
             ok &= umma::mbar_wait(sa(&b_sfull[buf]), (t >> 1) & 1);
             umma::fence_after();
-#pragma unroll
-            for (int c = 0; c < AP_H; c += 16) umma::tmem_ld16(lane_base + APT_S + 64 * buf + c, x + c);
+            umma::tmem_ld16(lane_base + APT_S + 64 * buf + hc, x);
+            umma::tmem_ld16(lane_base + APT_S + 64 * buf + hc + 16, x + 16);
             umma::tmem_wait_ld();
             umma::fence_before();
             umma::mbar_arrive(sa(&b_sfree[buf]));
-            // swap partial scores with the peer (chunks swizzled by row to spread banks)
+            // swap partial scores with the peer (16-byte chunks swizzled by row to spread banks)
             if (t >= 1) ok &= umma::mbar_wait_cluster(sa(&b_xfree), (t - 1) & 1);
 #pragma unroll
-            for (int c = 0; c < 16; ++c)
-                umma::st_cluster_v4(sx_peer + tid * 256 + ((c ^ (tid & 15)) << 4), x[4 * c], x[4 * c + 1], x[4 * c + 2],
-                                    x[4 * c + 3]);
+            for (int c = 0; c < 8; ++c)
+                umma::st_cluster_v4(sx_peer + row * 256 + (((hh * 8 + c) ^ (row & 15)) << 4), x[4 * c], x[4 * c + 1],
+                                    x[4 * c + 2], x[4 * c + 3]);
             umma::mbar_arrive_remote(xfull_peer);
             ok &= umma::mbar_wait_cluster(sa(&b_xfull), t & 1);
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const float4 v = *reinterpret_cast<const float4*>(sx + tid * 64 + ((c ^ (tid & 15)) << 2));
+            for (int c = 0; c < 8; ++c) {
+                const float4 v = *reinterpret_cast<const float4*>(sx + row * 64 + (((hh * 8 + c) ^ (row & 15)) << 2));
                 // S = S_0 + S_1 in both CTAs (addition is commutative, so the bits agree)
                 x[4 * c] += v.x;
                 x[4 * c + 1] += v.y;
@@ -317,14 +323,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
             umma::mbar_arrive_remote(xfree_peer);
             // row validity was written by the loaders of this buffer: observe their barrier too
             ok &= umma::mbar_wait(sa(&b_lfull[buf]), (t >> 1) & 1);
-            const bool valid = rowok[buf][tid] != 0;
+            const bool valid = rowok[buf][row] != 0;
 #pragma unroll
-            for (int h = 0; h < AP_H; ++h) {
+            for (int h = 0; h < 32; ++h) {
                 x[h] = valid ? x[h] * scale_log2e : -INFINITY;
                 const uint32_t mk = __reduce_max_sync(0xffffffffu, ap_ord(x[h]));
-                if (lane == 0) red[warp * AP_H + h] = ap_unord(mk);
+                if (lane == 0) red[qd * AP_H + hc + h] = ap_unord(mk);
             }
-            asm volatile("bar.sync 1, 128;" ::: "memory");
+            asm volatile("bar.sync 1, 256;" ::: "memory");
             if (tid < AP_H) {
                 const float mt = fmaxf(fmaxf(red[tid], red[AP_H + tid]), fmaxf(red[2 * AP_H + tid], red[3 * AP_H + tid]));
                 const float mo = m_run[tid];
@@ -338,63 +344,64 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                 if (lane == 0) flag[warp] = any != 0;
             }
             if (t >= 1) ok &= umma::mbar_wait(sa(&b_odone), (t - 1) & 1);   // previous P and O are settled
-            asm volatile("bar.sync 1, 128;" ::: "memory");
+            asm volatile("bar.sync 1, 256;" ::: "memory");
             umma::fence_after();
             if (t >= 1 && (flag[0] | flag[1])) {
-                // raise the running max: scale O^T (both dim tiles) and l, column = head
+                // raise the running max: scale O^T (both dim tiles) and l in this thread's 32 head columns
 #pragma unroll 1
                 for (int blk = 0; blk < 3; ++blk) {
-                    const uint32_t col0 = blk < 2 ? APT_O + 64 * blk : APT_L;
+                    const uint32_t col0 = (blk < 2 ? APT_O + 64 * blk : APT_L) + hc;
 #pragma unroll
-                    for (int c = 0; c < AP_H; c += 16) {
+                    for (int c = 0; c < 32; c += 16) {
                         float v[16];
                         umma::tmem_ld16(lane_base + col0 + c, v);
                         umma::tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] *= fac[c + i];
+                        for (int i = 0; i < 16; ++i) v[i] *= fac[hc + c + i];
                         umma::tmem_st16(lane_base + col0 + c, v);
                     }
                 }
                 umma::tmem_wait_st();
             }
-            // P = exp2(x - m_run), fp16, row = key (MN-major B operand)
+            // P = exp2(x - m_run), fp16, row = key (MN-major B operand), this thread's 4 chunks
 #pragma unroll
-            for (int c = 0; c < AP_H / 8; ++c) {
+            for (int c = 0; c < 4; ++c) {
                 uint32_t w[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int h = 8 * c + 2 * e;
-                    const float m0 = m_run[h], m1 = m_run[h + 1];
+                    const float m0 = m_run[hc + h], m1 = m_run[hc + h + 1];
                     const float p0 = (x[h] == -INFINITY || m0 == -INFINITY) ? 0.0f : umma::ex2(x[h] - m0);
                     const float p1 = (x[h + 1] == -INFINITY || m1 == -INFINITY) ? 0.0f : umma::ex2(x[h + 1] - m1);
                     __half2 hp = __floats2half2_rn(p0, p1);
                     w[e] = *reinterpret_cast<uint32_t*>(&hp);
                 }
-                *reinterpret_cast<uint4*>(sm + AP_SP + apswz(tid, c)) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4*>(sm + AP_SP + apswz(row, hh * 4 + c)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
             umma::fence_proxy_async();
             umma::fence_before();
             umma::mbar_arrive(sa(&b_pfull));
         }
-        // ================= epilogue: thread = output dim within each 128-dim tile
+        // ================= epilogue: thread = output dim 32*(warp%4)+lane of each 128-dim tile, its 32 heads
         ok &= umma::mbar_wait(sa(&b_odone), (T - 1) & 1);
         umma::fence_after();
-        float inv[AP_H];                     // 1/l per head (every lane holds the same l row)
-#pragma unroll
-        for (int c = 0; c < AP_H; c += 16) umma::tmem_ld16(lane_base + APT_L + c, inv + c);
+        float inv[32];
+        umma::tmem_ld16(lane_base + APT_L + hc, inv);
+        umma::tmem_ld16(lane_base + APT_L + hc + 16, inv + 16);
         umma::tmem_wait_ld();
-        if (lse != nullptr && rank == 0 && tid == 0)
+        if (lse != nullptr && rank == 0 && qd == 0 && lane == 0)
 #pragma unroll
-            for (int h = 0; h < AP_H; ++h)
-                lse[gq * AP_H + h] = inv[h] > 0.0f ? (m_run[h] + log2f(inv[h])) * 0.69314718055994531f : -INFINITY;
+            for (int h = 0; h < 32; ++h)
+                lse[gq * AP_H + hc + h] =
+                    inv[h] > 0.0f ? (m_run[hc + h] + log2f(inv[h])) * 0.69314718055994531f : -INFINITY;
 #pragma unroll
-        for (int h = 0; h < AP_H; ++h) inv[h] = inv[h] > 0.0f ? 1.0f / inv[h] : 0.0f;
+        for (int h = 0; h < 32; ++h) inv[h] = inv[h] > 0.0f ? 1.0f / inv[h] : 0.0f;
         for (int mt = 0; mt < 2; ++mt) {
-            float* op = out + gq * AP_H * D_LAT + d0 + mt * 128 + tid;
+            float* op = out + (gq * AP_H + hc) * D_LAT + d0 + mt * 128 + row;
 #pragma unroll
-            for (int c = 0; c < AP_H; c += 16) {
+            for (int c = 0; c < 32; c += 16) {
                 float o[16];
-                umma::tmem_ld16(lane_base + APT_O + 64 * mt + c, o);
+                umma::tmem_ld16(lane_base + APT_O + 64 * mt + hc + c, o);
                 umma::tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 16; ++i)

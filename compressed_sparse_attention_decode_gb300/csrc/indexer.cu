@@ -42,6 +42,7 @@ __global__ void __launch_bounds__(256) k_scan_full(const uint8_t* __restrict__ k
     const int words = QView<DI>::words(H);
     int* nel = smem;
     float2* slu = reinterpret_cast<float2*>(smem + 32 + QB * words);
+    rs.whist = reinterpret_cast<int*>(slu + QB * E);         // 8 warps x 256
     for (int t = 0; t < nqb; ++t) {
         QView<DI> v;
         v.bind(smem + 32 + t * words, H);
@@ -87,6 +88,7 @@ __global__ void __launch_bounds__(256) k_scan_full(const uint8_t* __restrict__ k
 
 struct SelectSmem {
     RadixSmem rs;
+    int whist[16 * 256];          // per-warp radix histograms (up to 512 threads)
     unsigned long long key[MAX_K];
     int id[MAX_K];
 };
@@ -225,6 +227,7 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
         sm.rs.ctl[0] = 0;
         sm.rs.ctl[3] = 0;
     }
+    sm.rs.whist = sm.whist;
     __syncthreads();
     if (!lu) {
         // ---- 0. bounds of the pool slots (Reindex)
@@ -424,7 +427,7 @@ cudaError_t launch_indexer_full_t(const csa2_cache& c, const uint8_t* iq_codes, 
     const int QB = (n_q >= 8 && pool_blocks == 0) ? 8 : 1;
     int E = QB == 1 ? 4096 : 1024;
     if (pool_blocks > 0) E = bs * (4096 / bs > 0 ? 4096 / bs : 1);
-    const size_t smem1 = 32 * sizeof(int) + QB * qwords + (size_t)QB * E * sizeof(float2);
+    const size_t smem1 = 32 * sizeof(int) + QB * qwords + (size_t)QB * E * sizeof(float2) + 8 * 256 * sizeof(int);
     cudaError_t e = cudaFuncSetAttribute(k_scan_full<DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
     if (e != cudaSuccess) return e;
     for (int q0 = 0; q0 < n_q; q0 += qchunk) {

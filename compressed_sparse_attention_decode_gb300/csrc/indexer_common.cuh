@@ -147,29 +147,33 @@ __host__ __device__ inline float bound_factor(int H, int DI) { return 2.0f * (fl
 struct RadixSmem {
     int hist[256];
     int ctl[8];   // [0] append counter, [1] digit, [2] krem, [3] scratch
+    int* whist;   // per-warp histograms, (blockDim.x / 32) x 256 ints, set by the caller
 };
 
 // k-th largest key (1 <= k <= number of taking items) over items t in [0, n):
 // getkey(t, key) returns false for items that do not take part.  Returns the
-// key and sets *krem to how many items equal to it are needed.  Lanes with the
-// same digit are merged (match.any) before the shared-memory atomic, so heavy
-// ties do not serialise.
+// key and sets *krem to how many items equal to it are needed.  Each warp
+// counts into its own histogram (shared-memory atomics, so equal digits from
+// one warp only contend within that warp), then the warps' counts are summed.
 template <typename KeyT, typename Get>
 __device__ KeyT block_kth_largest(Get getkey, int n, int k, RadixSmem& rs, int* krem_out) {
     constexpr int BITS = sizeof(KeyT) * 8;
-    const int lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    int* wh = rs.whist + (threadIdx.x >> 5) * 256;
     KeyT prefix = 0, mask = 0;
     int krem = k;
     for (int shift = BITS - 8; shift >= 0; shift -= 8) {
-        for (int i = threadIdx.x; i < 256; i += blockDim.x) rs.hist[i] = 0;
+        for (int i = threadIdx.x; i < nw * 256; i += blockDim.x) rs.whist[i] = 0;
         __syncthreads();
-        for (int base = 0; base < n; base += blockDim.x) {
-            const int t = base + threadIdx.x;
-            KeyT key = 0;
-            int bin = -1;
-            if (t < n && getkey(t, key) && (key & mask) == prefix) bin = (int)((key >> shift) & 255);
-            const unsigned peers = __match_any_sync(0xffffffffu, bin);
-            if (bin >= 0 && lane == __ffs(peers) - 1) atomicAdd(&rs.hist[bin], __popc(peers));
+        for (int t = threadIdx.x; t < n; t += blockDim.x) {
+            KeyT key;
+            if (getkey(t, key) && (key & mask) == prefix) atomicAdd(&wh[(int)((key >> shift) & 255)], 1);
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < 256; i += blockDim.x) {
+            int c = 0;
+            for (int w = 0; w < nw; ++w) c += rs.whist[w * 256 + i];
+            rs.hist[i] = c;
         }
         __syncthreads();
         if (threadIdx.x < 32) {

@@ -230,6 +230,7 @@ __global__ void __launch_bounds__(256, 2) k_scan_full_tc(
         umma::fence_after();
         umma::tmem_dealloc(tmem, 128);
     }
+    rs.whist = reinterpret_cast<int*>(sm + IS_A);       // the A slots are idle now: 8 warps x 256 counters
     forward_candidates(slu, c0, ITC_E, n_elig, k, pool_blocks, bs, (int64_t)b * n_qc + ql, list_len, counts, cid, clu,
                        bid, blu, rs);
 }
