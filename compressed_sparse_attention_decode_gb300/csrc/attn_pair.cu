@@ -5,19 +5,22 @@
 // CTA r of the pair owns latent dims [256r, 256r+256).  Per 128-key tile:
 //   S_r = L[:, dims_r] . Q[:, dims_r]^T   (tcgen05, M = 128 keys, N = 64 heads,
 //                                          K = 256, fp32 in TMEM)
-//   the two partial scores are swapped through distributed shared memory and
-//   added (S = S_0 + S_1, the same bits in both CTAs), then an online softmax
-//   with a lazy running max (rescale only when a head's max grows by > 2^8)
-//   writes P (fp16) and both CTAs accumulate their own output dims:
-//   O_r^T += L[:, dims_r]^T . P,  l += 1^T . P   (TMEM, across all tiles)
-// Half-tiles are double-buffered, so the gather and dequantisation of the next
-// tile overlap the MMAs and softmax of this one; nothing goes through global
-// memory between tiles and each CTA writes its 256 output dims at the end.
+//   each CTA sends its partial scores to the other with asynchronous remote
+//   stores counted on the receiver's mbarrier, and adds the other's
+//   (S = S_0 + S_1, the same bits in both CTAs); an online softmax with a lazy
+//   running max (a max reduction runs only when some score rises more than 2^8
+//   above the running max) writes P (fp16), and both CTAs accumulate their own
+//   output dims: O_r^T += L[:, dims_r]^T . P (TMEM, across all tiles).  The
+//   row sums l come from the same fp16 P, reduced across each warp's rows by
+//   shuffles.
+// The query's top-k indices are staged in shared memory at the start and every
+// row the CTA will read is prefetched into L2, so the tile gathers that follow
+// (double-buffered, overlapping the MMAs and softmax) are single L2 round trips.
 //
 // Warps: 0-7 softmax / epilogue (warp w reads TMEM lanes 32(w%4).. = key rows,
 // later output dims, for heads 32(w/4)..+31), warp 8 issues the MMAs, warps
 // 9-15 gather rows.  Tiles 0.. hold the selected FP4 entries, the last tile the
-// window rows (bf16), whose slower load then overlaps earlier tiles' work.
+// window rows (bf16).
 #include "common.cuh"
 #include "umma.cuh"
 
@@ -35,12 +38,13 @@ constexpr uint32_t AP_SQ = 0;                        // Q half: 4 slabs x 64 hea
 constexpr uint32_t AP_SL = 32 * 1024;                // 2 buffers x 4 slabs (128 KB)
 constexpr uint32_t AP_LBUF = 4 * AP_SLAB;
 constexpr uint32_t AP_SP = AP_SL + 2 * AP_LBUF;      // P: 128 keys x 64 heads fp16 (16 KB)
-constexpr uint32_t AP_SONES = AP_SP + 16 * 1024;     // ones, 128 x 16 fp16 (4 KB)
-constexpr uint32_t AP_SX = AP_SONES + 4 * 1024;      // the peer's partial scores, 128 x 64 f32 (32 KB)
-constexpr uint32_t AP_RED = AP_SX + 32 * 1024;       // column maxima, 4 warps x 64
-constexpr uint32_t AP_MISC = AP_RED + 1024;          // m_run[64], fac[64], flag
+constexpr uint32_t AP_SX = AP_SP + 16 * 1024;        // the peer's partial scores, 128 x 64 f32 (32 KB)
+constexpr uint32_t AP_SIDX = AP_SX + 32 * 1024;      // the query's indices, MAX_K ints
+constexpr uint32_t AP_RED = AP_SIDX + MAX_K * 4;     // column maxima / row sums, 4 quadrants x 64
+constexpr uint32_t AP_MISC = AP_RED + 1024;          // m_run[64], fac[64], flags
 constexpr uint32_t AP_DYN = AP_MISC + 1024 + 1024;
-constexpr uint32_t APT_S = 0, APT_O = 128, APT_L = 256, APT_COLS = 512;
+constexpr uint32_t AP_XBYTES = AP_TILE * AP_H * 4;   // partial scores one CTA sends per tile
+constexpr uint32_t APT_S = 0, APT_O = 128, APT_COLS = 256;
 constexpr float AP_LAZY = 8.0f;                      // log2 headroom before the running max is raised
 
 __device__ __forceinline__ uint32_t apswz(uint32_t row, uint32_t chunk) { return row * 128 + ((chunk ^ (row & 7)) << 4); }
@@ -105,13 +109,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
             umma::mbar_init(sa(&b_lfull[i]), AP_LOADERS);
             umma::mbar_init(sa(&b_lfree[i]), 1);
             umma::mbar_init(sa(&b_sfull[i]), 1);
-            umma::mbar_init(sa(&b_sfree[i]), AP_SMT);
+            umma::mbar_init(sa(&b_sfree[i]), AP_SMW);
         }
-        umma::mbar_init(sa(&b_pfull), AP_SMT);
+        umma::mbar_init(sa(&b_pfull), AP_SMW);
         umma::mbar_init(sa(&b_odone), 1);
-        umma::mbar_init(sa(&b_xfull), AP_SMT);
-        umma::mbar_init(sa(&b_xfree), AP_SMT);
+        umma::mbar_init(sa(&b_xfull), 1);          // armed by this CTA, filled by the peer's stores
+        umma::mbar_init(sa(&b_xfree), AP_SMW);     // one arrival per peer softmax warp
         umma::fence_mbar_init();
+        umma::mbar_arrive_expect_tx(sa(&b_xfull), AP_XBYTES);
     }
     if (warp == 0) umma::tmem_alloc(sa(&tmem_base), APT_COLS);
     // ---- Q half: 64 heads x 256 dims, bf16 -> fp16, one round of loads
@@ -131,7 +136,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                            ap_bf16x2_to_f16x2(v.w));
         }
     }
-    if (tid < 256) reinterpret_cast<uint4*>(sm + AP_SONES)[tid] = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
     float* m_run = reinterpret_cast<float*>(sm + AP_MISC);
     float* fac = m_run + AP_H;
     int* flag = reinterpret_cast<int*>(fac + AP_H);
@@ -139,7 +143,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
     umma::fence_proxy_async();
     umma::fence_before();
     __syncthreads();
-    umma::cluster_sync();              // both CTAs' barriers exist before any remote arrive
+    umma::cluster_sync();              // both CTAs' barriers exist before any remote store or arrive
     umma::fence_after();
     const uint32_t tmem = tmem_base;
     bool ok = true;
@@ -147,72 +151,93 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
     if (warp > AP_MMAW) {
         // ================= loaders
         const int lt = tid - (AP_MMAW + 1) * 32;
+        int* sidx = reinterpret_cast<int*>(sm + AP_SIDX);
+        const uint8_t* codes_b = lat_codes + (int64_t)b * capacity * (D_LAT / 2) + d0 / 2;
+        const uint8_t* scales_b = lat_scales + (int64_t)b * capacity * (D_LAT / 16) + d0 / 16;
+        const uint16_t* win_b = swa + ((int64_t)b * swa_len + (wlo - swa_pos0)) * D_LAT + d0;
+        for (int s = lt; s < k; s += AP_LOADERS) {
+            const int j = idx[gq * k + s];
+            sidx[s] = (j >= 0 && j < capacity) ? j : -1;
+        }
+        umma::bar_named(2, AP_LOADERS);
+        // every row this CTA reads, into L2 now: the gathers below then hit L2
+        for (int s = lt; s < k; s += AP_LOADERS) {
+            const int j = sidx[s];
+            if (j >= 0) {
+                umma::prefetch_l2(codes_b + (int64_t)j * (D_LAT / 2));
+                umma::prefetch_l2(scales_b + (int64_t)j * (D_LAT / 16));
+            }
+        }
+        for (int u = lt; u < nwin * 4; u += AP_LOADERS) umma::prefetch_l2(win_b + (int64_t)(u >> 2) * D_LAT + (u & 3) * 64);
         for (int t = 0; t < T; ++t) {
             const int buf = t & 1;
             if (t >= 2) ok &= umma::mbar_wait(sa(&b_lfree[buf]), ((t >> 1) - 1) & 1);
             uint8_t* L = sm + AP_SL + buf * AP_LBUF;
             if (t == T - 1) {
-                // window rows: 128 rows x 4 units of 64 dims (8 x 16 B of bf16)
-                for (int u = lt; u < AP_TILE * 4; u += AP_LOADERS) {
-                    const int r = u >> 2, part = u & 3;
-                    const bool valid = r < nwin;
+                // window rows: 128 rows x 32 chunks of 8 dims (bf16 -> fp16), 8 loads in flight per thread
+                for (int u0 = lt; u0 < AP_TILE * 32; u0 += AP_LOADERS * 8) {
                     uint4 wv[8];
-                    if (valid) {
-                        const uint4* wp = reinterpret_cast<const uint4*>(
-                            swa + ((int64_t)b * swa_len + (wlo + r - swa_pos0)) * D_LAT + d0 + part * 64);
 #pragma unroll
-                        for (int v = 0; v < 8; ++v) wv[v] = __ldg(wp + v);
+                    for (int i = 0; i < 8; ++i) {
+                        const int u = u0 + i * AP_LOADERS, r = u >> 5, c = u & 31;
+                        wv[i] = make_uint4(0, 0, 0, 0);
+                        if (u < AP_TILE * 32 && r < nwin)
+                            wv[i] = __ldg(reinterpret_cast<const uint4*>(win_b + (int64_t)r * D_LAT + c * 8));
                     }
 #pragma unroll
-                    for (int v = 0; v < 8; ++v) {
-                        uint4 o = make_uint4(0, 0, 0, 0);
-                        if (valid)
-                            o = make_uint4(ap_bf16x2_to_f16x2(wv[v].x), ap_bf16x2_to_f16x2(wv[v].y),
-                                           ap_bf16x2_to_f16x2(wv[v].z), ap_bf16x2_to_f16x2(wv[v].w));
-                        const int c = part * 8 + v;                       // 8-dim chunk 0..31
-                        *reinterpret_cast<uint4*>(L + (c >> 3) * AP_SLAB + apswz(r, c & 7)) = o;
-                    }
-                    if (part == 0) rowok[buf][r] = valid;
-                }
-            } else if (lt < AP_TILE) {
-                // selected FP4 entries: one row per thread, this CTA's 256 dims (128 B codes + 16 B scales)
-                const int r = lt;
-                const int slot = t * AP_TILE + r;
-                int j = -1;
-                if (slot < k) {
-                    j = idx[gq * k + slot];
-                    if (j < 0 || j >= capacity) j = -1;
-                }
-                uint4 cw[8];
-                uint4 sc = make_uint4(0, 0, 0, 0);
-                if (j >= 0) {
-                    const int64_t row = (int64_t)b * capacity + j;
-                    const uint4* cp = reinterpret_cast<const uint4*>(lat_codes + row * (D_LAT / 2) + d0 / 2);
-#pragma unroll
-                    for (int v = 0; v < 8; ++v) cw[v] = __ldg(cp + v);
-                    sc = __ldg(reinterpret_cast<const uint4*>(lat_scales + row * (D_LAT / 16) + d0 / 16));
-                }
-                const uint32_t sw[4] = {sc.x, sc.y, sc.z, sc.w};
-#pragma unroll
-                for (int v = 0; v < 8; ++v) {            // 32 dims = 2 scale groups
-                    const uint32_t words[4] = {cw[v].x, cw[v].y, cw[v].z, cw[v].w};
-#pragma unroll
-                    for (int w = 0; w < 4; ++w) {        // 8 dims = one 16-byte chunk
-                        uint4 o = make_uint4(0, 0, 0, 0);
-                        if (j >= 0) {
-                            const int g = 2 * v + (w >> 1);
-                            const float sf = e4m3_to_f32((sw[g >> 2] >> (8 * (g & 3))) & 255u);
-                            const __half2 s2 = __float2half2_rn(sf);
-                            uint32_t f[4];
-                            ap_e2m1x8(words[w], f);
-                            o = make_uint4(ap_hmul2(f[0], s2), ap_hmul2(f[1], s2), ap_hmul2(f[2], s2),
-                                           ap_hmul2(f[3], s2));
+                    for (int i = 0; i < 8; ++i) {
+                        const int u = u0 + i * AP_LOADERS, r = u >> 5, c = u & 31;
+                        if (u < AP_TILE * 32) {
+                            const uint4 v = wv[i];
+                            *reinterpret_cast<uint4*>(L + (c >> 3) * AP_SLAB + apswz(r, c & 7)) =
+                                make_uint4(ap_bf16x2_to_f16x2(v.x), ap_bf16x2_to_f16x2(v.y),
+                                           ap_bf16x2_to_f16x2(v.z), ap_bf16x2_to_f16x2(v.w));
+                            if (c == 0) rowok[buf][r] = r < nwin;
                         }
-                        const int c = v * 4 + w;                 // 8-dim chunk 0..31
-                        *reinterpret_cast<uint4*>(L + (c >> 3) * AP_SLAB + apswz(r, c & 7)) = o;
                     }
                 }
-                rowok[buf][r] = j >= 0;
+            } else {
+                // selected FP4 rows: 128 rows x 8 units of 32 dims (16 B of codes + 2 scale bytes)
+                constexpr int NU = (AP_TILE * 8 + AP_LOADERS - 1) / AP_LOADERS;
+                uint4 cw[NU];
+                uint32_t sc[NU];
+#pragma unroll
+                for (int i = 0; i < NU; ++i) {
+                    const int u = lt + i * AP_LOADERS, r = u >> 3, c = u & 7;
+                    const int slot = t * AP_TILE + r;
+                    cw[i] = make_uint4(0, 0, 0, 0);
+                    sc[i] = 0u;
+                    if (u < AP_TILE * 8 && slot < k) {
+                        const int j = sidx[slot];
+                        if (j >= 0) {
+                            cw[i] = __ldg(reinterpret_cast<const uint4*>(codes_b + (int64_t)j * (D_LAT / 2)) + c);
+                            sc[i] = __ldg(reinterpret_cast<const uint16_t*>(scales_b + (int64_t)j * (D_LAT / 16)) + c);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < NU; ++i) {
+                    const int u = lt + i * AP_LOADERS, r = u >> 3, c = u & 7;
+                    if (u < AP_TILE * 8) {
+                        const int slot = t * AP_TILE + r;
+                        const bool valid = slot < k && sidx[slot] >= 0;
+                        const uint32_t words[4] = {cw[i].x, cw[i].y, cw[i].z, cw[i].w};
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {        // 8 dims per word; scale group 2c + w/2
+                            uint4 o = make_uint4(0, 0, 0, 0);
+                            if (valid) {
+                                const __half2 s2 = __float2half2_rn(e4m3_to_f32((sc[i] >> (8 * (w >> 1))) & 255u));
+                                uint32_t f[4];
+                                ap_e2m1x8(words[w], f);
+                                o = make_uint4(ap_hmul2(f[0], s2), ap_hmul2(f[1], s2), ap_hmul2(f[2], s2),
+                                               ap_hmul2(f[3], s2));
+                            }
+                            const int cc = c * 4 + w;                // 8-dim chunk 0..31
+                            *reinterpret_cast<uint4*>(L + (cc >> 3) * AP_SLAB + apswz(r, cc & 7)) = o;
+                        }
+                        if (c == 0) rowok[buf][r] = valid;
+                    }
+                }
             }
             umma::fence_proxy_async();
             umma::mbar_arrive(sa(&b_lfull[buf]));
@@ -222,7 +247,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
         if (lane == 0) {
             const uint32_t id1 = umma::idesc_f16(128, AP_H, 0, 0);
             const uint32_t id2 = umma::idesc_f16(128, AP_H, 1, 1);
-            const uint32_t id3 = umma::idesc_f16(128, AP_H, 0, 1);
             // Two independent streams: GEMM1 of tile t needs its half rows loaded
             // (lfull) and its score buffer released (sfree of tile t-2); GEMM2 of
             // tile t needs P (pfull).  Serve whichever is ready, so a slow load of
@@ -263,12 +287,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                             umma::mma_f16(tmem + APT_O + 64 * mt, a, bp, id2, (n2 > 0 || ks > 0) ? 1u : 0u);
                         }
                     }
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint64_t a = umma::desc(base + AP_SONES, 128, 256, umma::LAYOUT_NONE);
-                        const uint64_t bp = umma::desc(base + AP_SP + ks * 2048, 8192, 1024, umma::LAYOUT_SW128);
-                        umma::mma_f16(tmem + APT_L, a, bp, id3, (n2 > 0 || ks > 0) ? 1u : 0u);
-                    }
                     umma::commit(sa(&b_odone));
                     umma::commit(sa(&b_lfree[buf]));
                     ++n2;
@@ -293,6 +311,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
         const uint32_t xfree_peer = umma::mapa(sa(&b_xfree), peer);
         float* red = reinterpret_cast<float*>(sm + AP_RED);           // [4 quadrants][64 heads]
         const float* sx = reinterpret_cast<const float*>(sm + AP_SX);
+        float lsum = 0.0f;          // sum of P over this warp's rows, head hc + lane, all tiles so far
         for (int t = 0; t < T; ++t) {
             const int buf = t & 1;
             float x[32];
@@ -302,15 +321,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
             umma::tmem_ld16(lane_base + APT_S + 64 * buf + hc + 16, x + 16);
             umma::tmem_wait_ld();
             umma::fence_before();
-            umma::mbar_arrive(sa(&b_sfree[buf]));
-            // swap partial scores with the peer (16-byte chunks swizzled by row to spread banks)
+            __syncwarp();
+            if (lane == 0) umma::mbar_arrive(sa(&b_sfree[buf]));
+            // send the partial scores to the peer (16-byte chunks swizzled by row
+            // to spread banks), once it has read the previous ones
             if (t >= 1) ok &= umma::mbar_wait_cluster(sa(&b_xfree), (t - 1) & 1);
 #pragma unroll
             for (int c = 0; c < 8; ++c)
-                umma::st_cluster_v4(sx_peer + row * 256 + (((hh * 8 + c) ^ (row & 15)) << 4), x[4 * c], x[4 * c + 1],
-                                    x[4 * c + 2], x[4 * c + 3]);
-            umma::mbar_arrive_remote(xfull_peer);
+                umma::st_async_v4(sx_peer + row * 256 + (((hh * 8 + c) ^ (row & 15)) << 4), x[4 * c], x[4 * c + 1],
+                                  x[4 * c + 2], x[4 * c + 3], xfull_peer);
             ok &= umma::mbar_wait_cluster(sa(&b_xfull), t & 1);
+            if (tid == 0 && t + 1 < T) umma::mbar_arrive_expect_tx(sa(&b_xfull), AP_XBYTES);   // arm the next tile
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 const float4 v = *reinterpret_cast<const float4*>(sx + row * 64 + (((hh * 8 + c) ^ (row & 15)) << 2));
@@ -320,50 +341,65 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                 x[4 * c + 2] += v.z;
                 x[4 * c + 3] += v.w;
             }
-            umma::mbar_arrive_remote(xfree_peer);
+            __syncwarp();
+            if (lane == 0) umma::mbar_arrive_remote(xfree_peer);
             // row validity was written by the loaders of this buffer: observe their barrier too
             ok &= umma::mbar_wait(sa(&b_lfull[buf]), (t >> 1) & 1);
             const bool valid = rowok[buf][row] != 0;
+            bool exceed = false;
 #pragma unroll
             for (int h = 0; h < 32; ++h) {
                 x[h] = valid ? x[h] * scale_log2e : -INFINITY;
-                const uint32_t mk = __reduce_max_sync(0xffffffffu, ap_ord(x[h]));
-                if (lane == 0) red[qd * AP_H + hc + h] = ap_unord(mk);
+                exceed |= x[h] > m_run[hc + h] + AP_LAZY;
             }
-            asm volatile("bar.sync 1, 256;" ::: "memory");
-            if (tid < AP_H) {
-                const float mt = fmaxf(fmaxf(red[tid], red[AP_H + tid]), fmaxf(red[2 * AP_H + tid], red[3 * AP_H + tid]));
-                const float mo = m_run[tid];
-                float f = 1.0f;
-                if (mt > -INFINITY && (mo == -INFINITY || mt > mo + AP_LAZY)) {
-                    f = (mo == -INFINITY) ? 0.0f : umma::ex2(mo - mt);
-                    m_run[tid] = mt;
+            // both CTAs hold the same scores, so they take the same branch
+            const bool raise = umma::bar_red_or(1, AP_SMT, exceed);
+            if (raise) {
+                // new running max for the heads that rose too far: column maxima of the tile
+#pragma unroll
+                for (int h = 0; h < 32; ++h) {
+                    const uint32_t mk = __reduce_max_sync(0xffffffffu, ap_ord(x[h]));
+                    if (lane == 0) red[qd * AP_H + hc + h] = ap_unord(mk);
                 }
-                fac[tid] = f;
-                const unsigned any = __ballot_sync(0xffffffffu, f != 1.0f);
-                if (lane == 0) flag[warp] = any != 0;
-            }
-            if (t >= 1) ok &= umma::mbar_wait(sa(&b_odone), (t - 1) & 1);   // previous P and O are settled
-            asm volatile("bar.sync 1, 256;" ::: "memory");
-            umma::fence_after();
-            if (t >= 1 && (flag[0] | flag[1])) {
-                // raise the running max: scale O^T (both dim tiles) and l in this thread's 32 head columns
-#pragma unroll 1
-                for (int blk = 0; blk < 3; ++blk) {
-                    const uint32_t col0 = (blk < 2 ? APT_O + 64 * blk : APT_L) + hc;
-#pragma unroll
-                    for (int c = 0; c < 32; c += 16) {
-                        float v[16];
-                        umma::tmem_ld16(lane_base + col0 + c, v);
-                        umma::tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] *= fac[hc + c + i];
-                        umma::tmem_st16(lane_base + col0 + c, v);
+                umma::bar_named(1, AP_SMT);
+                if (tid < AP_H) {
+                    const float mt = fmaxf(fmaxf(red[tid], red[AP_H + tid]), fmaxf(red[2 * AP_H + tid], red[3 * AP_H + tid]));
+                    const float mo = m_run[tid];
+                    float f = 1.0f;
+                    if (mt > -INFINITY && (mo == -INFINITY || mt > mo + AP_LAZY)) {
+                        f = (mo == -INFINITY) ? 0.0f : umma::ex2(mo - mt);
+                        m_run[tid] = mt;
                     }
+                    fac[tid] = f;
+                    const unsigned any = __ballot_sync(0xffffffffu, f != 1.0f);
+                    if (lane == 0) flag[warp] = any != 0;
                 }
-                umma::tmem_wait_st();
+                if (t >= 1) ok &= umma::mbar_wait(sa(&b_odone), (t - 1) & 1);   // previous P and O are settled
+                umma::bar_named(1, AP_SMT);
+                umma::fence_after();
+                if (t >= 1 && (flag[0] | flag[1])) {
+                    // rescale O^T (both dim tiles) in this thread's 32 head columns
+#pragma unroll 1
+                    for (int blk = 0; blk < 2; ++blk) {
+                        const uint32_t col0 = APT_O + 64 * blk + hc;
+#pragma unroll
+                        for (int c = 0; c < 32; c += 16) {
+                            float v[16];
+                            umma::tmem_ld16(lane_base + col0 + c, v);
+                            umma::tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) v[i] *= fac[hc + c + i];
+                            umma::tmem_st16(lane_base + col0 + c, v);
+                        }
+                    }
+                    umma::tmem_wait_st();
+                }
+                lsum *= fac[hc + lane];
+            } else if (t >= 1) {
+                ok &= umma::mbar_wait(sa(&b_odone), (t - 1) & 1);             // GEMM2 of t-1 has read P
             }
-            // P = exp2(x - m_run), fp16, row = key (MN-major B operand), this thread's 4 chunks
+            // P = exp2(x - m_run), fp16, row = key (MN-major B operand), this thread's 4 chunks;
+            // x keeps the rounded values for the row sums
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t w[4];
@@ -373,22 +409,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                     const float m0 = m_run[hc + h], m1 = m_run[hc + h + 1];
                     const float p0 = (x[h] == -INFINITY || m0 == -INFINITY) ? 0.0f : umma::ex2(x[h] - m0);
                     const float p1 = (x[h + 1] == -INFINITY || m1 == -INFINITY) ? 0.0f : umma::ex2(x[h + 1] - m1);
-                    __half2 hp = __floats2half2_rn(p0, p1);
-                    w[e] = *reinterpret_cast<uint32_t*>(&hp);
+                    const __half2 hp = __floats2half2_rn(p0, p1);
+                    w[e] = *reinterpret_cast<const uint32_t*>(&hp);
+                    const float2 back = __half22float2(hp);
+                    x[h] = back.x;
+                    x[h + 1] = back.y;
                 }
                 *reinterpret_cast<uint4*>(sm + AP_SP + apswz(row, hh * 4 + c)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
             umma::fence_proxy_async();
             umma::fence_before();
-            umma::mbar_arrive(sa(&b_pfull));
+            __syncwarp();
+            if (lane == 0) umma::mbar_arrive(sa(&b_pfull));
+            // sum of the rounded P over the warp's 32 rows: after the butterfly, lane L holds head hc + L
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) {
+                const bool upper = (lane & o) != 0;
+#pragma unroll
+                for (int i = 0; i < o; ++i) {
+                    const float send = upper ? x[i] : x[i + o];
+                    const float keep = upper ? x[i + o] : x[i];
+                    x[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                }
+            }
+            lsum += x[0];
         }
         // ================= epilogue: thread = output dim 32*(warp%4)+lane of each 128-dim tile, its 32 heads
+        red[qd * AP_H + hc + lane] = lsum;
+        umma::bar_named(1, AP_SMT);
         ok &= umma::mbar_wait(sa(&b_odone), (T - 1) & 1);
         umma::fence_after();
         float inv[32];
-        umma::tmem_ld16(lane_base + APT_L + hc, inv);
-        umma::tmem_ld16(lane_base + APT_L + hc + 16, inv + 16);
-        umma::tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < 32; ++h)
+            inv[h] = (red[hc + h] + red[AP_H + hc + h]) + (red[2 * AP_H + hc + h] + red[3 * AP_H + hc + h]);
         if (lse != nullptr && rank == 0 && qd == 0 && lane == 0)
 #pragma unroll
             for (int h = 0; h < 32; ++h)

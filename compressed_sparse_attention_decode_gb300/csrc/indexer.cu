@@ -91,7 +91,12 @@ struct SelectSmem {
     int whist[16 * 256];          // per-warp radix histograms (up to 512 threads)
     unsigned long long key[MAX_K];
     int id[MAX_K];
+    unsigned long long* key2;     // merge buffers, MAX_K each (dynamic shared memory)
+    int* id2;
+    int* din;                     // HSI blocks that are in for sure, MAX_K (dynamic shared memory)
 };
+// dynamic shared memory of k_select after the staged query: key2 | id2 | din
+constexpr size_t SEL_DYN_EXTRA = (size_t)MAX_K * (8 + 4 + 4);
 
 // Among m candidates (cid[t], ckey[t]) keep the k best by (key desc, id asc):
 // the kept ones end up in sm.key/sm.id[0..kept), unordered.  Returns kept.
@@ -135,34 +140,82 @@ __device__ int keep_best(const int* cid, const unsigned long long* ckey, int m, 
     return k;
 }
 
-// bitonic sort of sm.key/sm.id[0..n) (n <= MAX_K), padded with sentinels.
-// desc_by_key: order (key desc, id asc); otherwise (id asc).
-__device__ void sort_kept(int n, bool desc_by_key, SelectSmem& sm) {
-    int N = 1;
+__device__ __forceinline__ bool sel_before(unsigned long long ka, int ia, unsigned long long kb, int ib, bool by_key) {
+    return by_key ? (ka > kb || (ka == kb && ia < ib)) : (ia < ib);
+}
+
+// Sort sm.key/sm.id[0..n) (n <= MAX_K), padded with sentinels (key 0, id max)
+// to N = a power of two >= 32.  by_key: order (key desc, id asc); otherwise
+// (id asc).  Each warp sorts runs of 32 in registers (bitonic network over
+// shuffles); then runs are merged pairwise, every element going to its index
+// in its run plus the number of sibling-run elements ahead of it (binary
+// search; ties between runs go to the left run), alternating with key2/id2.
+__device__ void sort_kept(int n, bool by_key, SelectSmem& sm) {
+    int N = 32;
     while (N < n) N <<= 1;
     for (int t = n + threadIdx.x; t < N; t += blockDim.x) {
         sm.key[t] = 0ull;
         sm.id[t] = 0x7fffffff;
     }
     __syncthreads();
-    for (int size = 2; size <= N; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int t = threadIdx.x; t < N / 2; t += blockDim.x) {
-                const int i = 2 * t - (t & (stride - 1));
-                const int j = i + stride;
-                const bool up = ((i & size) == 0);
-                const unsigned long long ki = sm.key[i], kj = sm.key[j];
-                const int ii = sm.id[i], ij = sm.id[j];
-                const bool i_first = desc_by_key ? (ki > kj || (ki == kj && ii < ij)) : (ii < ij);
-                if (i_first != up) {
-                    sm.key[i] = kj;
-                    sm.key[j] = ki;
-                    sm.id[i] = ij;
-                    sm.id[j] = ii;
+    const int lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    for (int r = threadIdx.x >> 5; r < N / 32; r += nw) {
+        unsigned long long k = sm.key[r * 32 + lane];
+        int id = sm.id[r * 32 + lane];
+#pragma unroll
+        for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+            for (int j = size >> 1; j > 0; j >>= 1) {
+                const unsigned long long ko = __shfl_xor_sync(0xffffffffu, k, j);
+                const int io = __shfl_xor_sync(0xffffffffu, id, j);
+                const bool lower = (lane & j) == 0, up = (lane & size) == 0;
+                const bool mine_first = sel_before(k, id, ko, io, by_key);
+                if (mine_first != (lower == up)) {
+                    k = ko;
+                    id = io;
                 }
             }
-            __syncthreads();
         }
+        sm.key[r * 32 + lane] = k;
+        sm.id[r * 32 + lane] = id;
+    }
+    __syncthreads();
+    unsigned long long *ka = sm.key, *kb = sm.key2;
+    int *ia = sm.id, *ib = sm.id2;
+    for (int L = 32; L < N; L <<= 1) {
+        for (int e = threadIdx.x; e < N; e += blockDim.x) {
+            const int r = e / L, i = e - r * L;
+            const unsigned long long x = ka[e];
+            const int xi = ia[e];
+            const unsigned long long* ks = ka + (r ^ 1) * L;
+            const int* is = ia + (r ^ 1) * L;
+            const bool left = (r & 1) == 0;
+            int lo = 0, hi = L;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                const bool ahead = left ? sel_before(ks[mid], is[mid], x, xi, by_key)
+                                        : !sel_before(x, xi, ks[mid], is[mid], by_key);
+                if (ahead) lo = mid + 1;
+                else hi = mid;
+            }
+            const int o = (r & ~1) * L + i + lo;
+            kb[o] = x;
+            ib[o] = xi;
+        }
+        __syncthreads();
+        unsigned long long* tk = ka;
+        ka = kb;
+        kb = tk;
+        int* ti = ia;
+        ia = ib;
+        ib = ti;
+    }
+    if (ka != sm.key) {
+        for (int t = threadIdx.x; t < n; t += blockDim.x) {
+            sm.key[t] = ka[t];
+            sm.id[t] = ia[t];
+        }
+        __syncthreads();
     }
 }
 
@@ -185,13 +238,43 @@ __device__ int best_sorted(const int* cid, const unsigned long long* ckey, int m
     return kept;
 }
 
+// Reindex, first pass: the (S~-E, S~+E) bounds of every pool slot (-inf for
+// an empty slot), one thread per slot, blockIdx.z taking 512 slots of the
+// query's pool ("DeepSeek-v4.1 Flash" §2.3.2, the indexer re-run on the pool).
+template <int DI>
+__global__ void __launch_bounds__(512) k_pool_bounds(const int32_t* __restrict__ pool, int pool_len,
+                                                     const uint8_t* __restrict__ kc_all,
+                                                     const uint8_t* __restrict__ ks_all, int capacity,
+                                                     const uint8_t* __restrict__ iq_codes,
+                                                     const uint8_t* __restrict__ iq_scales,
+                                                     const float* __restrict__ w_head, int n_q, int H,
+                                                     float2* __restrict__ lu) {
+    extern __shared__ int qsm[];
+    const int ql = blockIdx.x, b = blockIdx.y;
+    const int64_t gq = (int64_t)b * n_q + ql;
+    QView<DI> v;
+    v.bind(qsm, H);
+    stage_query<DI>(v, iq_codes + gq * H * (DI / 2), iq_scales + gq * H * (DI / 16), w_head + gq * H, H, threadIdx.x,
+                    blockDim.x);
+    __syncthreads();
+    const int t = blockIdx.z * blockDim.x + threadIdx.x;
+    if (t >= pool_len) return;
+    const int j = pool[gq * pool_len + t];
+    float lo = -INFINITY, hi = -INFINITY;
+    if (j >= 0 && j < capacity) {
+        KeyRow<DI> kr;
+        const int64_t row = (int64_t)b * capacity + j;
+        kr.load(kc_all + row * (DI / 2), ks_all + row * (DI / 16));
+        approx_score<DI>(kr, v, H, bound_factor(H, DI), lo, hi);
+    }
+    lu[gq * pool_len + t] = make_float2(lo, hi);
+}
+
 // One block per (sequence, query).  Items t in [0, n): entry ids[t] (-1 =
 // empty) with bounds lu[t]; n is *count (Full: the forwarded candidates) or
-// n_fixed (Reindex: the pool slots).  Keeps the exact top k; with HSI (Full
-// only) also builds the pool from the forwarded block candidates.  With lu ==
-// nullptr (Reindex) the block first scores its own pool slots, keeping their
-// bounds in shared memory after the staged query: a pool is small enough that
-// scan and selection fit one launch.
+// n_fixed (Reindex: the pool slots, bounds from k_pool_bounds).  Keeps the
+// exact top k; with HSI (Full only) also builds the pool from the forwarded
+// block candidates.
 template <int DI>
 __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids, const float2* __restrict__ lu,
                                                 const int* __restrict__ counts, int n_fixed, int list_len,
@@ -213,7 +296,11 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
     stage_query<DI>(v, iq_codes + gq * H * (DI / 2), iq_scales + gq * H * (DI / 16), w_head + gq * H, H, threadIdx.x,
                     blockDim.x);
     const int32_t* id = ids + slab * list_len;
-    const float2* L = lu ? lu + slab * list_len : reinterpret_cast<const float2*>(qsm + ((QView<DI>::words(H) + 3) & ~3));
+    uint8_t* extra = reinterpret_cast<uint8_t*>(qsm + QView<DI>::words(H));
+    sm.key2 = reinterpret_cast<unsigned long long*>(extra);
+    sm.id2 = reinterpret_cast<int*>(extra + (size_t)MAX_K * 8);
+    sm.din = sm.id2 + MAX_K;
+    const float2* L = lu + slab * list_len;
     const int n = counts ? counts[2 * slab] : n_fixed;
     int* cid = c2id + slab * list_len;
     unsigned long long* ckey = c2key + slab * list_len;
@@ -229,26 +316,16 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
     }
     sm.rs.whist = sm.whist;
     __syncthreads();
-    if (!lu) {
-        // ---- 0. bounds of the pool slots (Reindex)
-        float2* sl = const_cast<float2*>(L);
-        const float fac = bound_factor(H, DI);
-        for (int t = threadIdx.x; t < n; t += blockDim.x) {
-            const int j = entry_of(t);
-            float lo = -INFINITY, hi = -INFINITY;
-            if (j >= 0) {
-                KeyRow<DI> kr;
-                kr.load(kc + (int64_t)j * (DI / 2), ks + (int64_t)j * (DI / 16));
-                approx_score<DI>(kr, v, H, fac, lo, hi);
-            }
-            sl[t] = make_float2(lo, hi);
-        }
-        __syncthreads();
-    }
-
-    // ---- 1. k-th largest lower bound, candidates whose upper bound reaches it
+    // ---- 1. k-th largest lower bound, candidates whose upper bound reaches it.
+    // Every forwarded item (Full) is a real entry; an empty pool slot (Reindex)
+    // has bounds (-inf, -inf), below every real entry, so the selection may
+    // count it as long as more than k real entries exist.
     int c = 0;
-    for (int t = threadIdx.x; t < n; t += blockDim.x) c += entry_of(t) >= 0;
+    if (counts) {
+        c = threadIdx.x == 0 ? n : 0;
+    } else {
+        for (int t = threadIdx.x; t < n; t += blockDim.x) c += L[t].y != -INFINITY;
+    }
     c = __reduce_add_sync(0xffffffffu, c);
     if ((threadIdx.x & 31) == 0) atomicAdd(&sm.rs.ctl[3], c);
     __syncthreads();
@@ -260,7 +337,7 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
         lam = block_kth_largest<unsigned int>(
             [&](int t, unsigned int& key) {
                 key = f32_key(L[t].x);
-                return entry_of(t) >= 0;
+                return true;
             },
             n, k, sm.rs, &krem);
     }
@@ -268,21 +345,37 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
     __syncthreads();
     for (int base = 0; base < n; base += blockDim.x) {
         const int t = base + threadIdx.x;
-        const bool f = t < n && entry_of(t) >= 0 && f32_key(L[t].y) >= lam;
+        const bool f = t < n && f32_key(L[t].y) >= lam && L[t].y != -INFINITY && entry_of(t) >= 0;
         const int pos = append_slot(f, &sm.rs.ctl[0]);
-        if (f) cid[pos] = entry_of(t);
+        if (f) {
+            const int j = entry_of(t);
+            cid[pos] = j;
+            if (pos < MAX_K) sm.id[pos] = j;
+        }
     }
     __syncthreads();
     const int m = sm.rs.ctl[0];
     __syncthreads();
-    // ---- 2. exact scores of the candidates
-    for (int t = threadIdx.x; t < m; t += blockDim.x) {
-        const int j = cid[t];
-        ckey[t] = f64_key(exact_score<DI>(kc + (int64_t)j * (DI / 2), ks + (int64_t)j * (DI / 16), v, H));
+    // ---- 2. exact scores of the candidates, 3. the k best in rank order
+    // (in shared memory when they fit, the usual case: k plus the few entries
+    // whose bounds straddle the threshold)
+    int kept;
+    if (m <= MAX_K) {
+        for (int t = threadIdx.x; t < m; t += blockDim.x) {
+            const int j = sm.id[t];
+            sm.key[t] = f64_key(exact_score<DI>(kc + (int64_t)j * (DI / 2), ks + (int64_t)j * (DI / 16), v, H));
+        }
+        __syncthreads();
+        sort_kept(m, true, sm);
+        kept = m < k ? m : k;
+    } else {
+        for (int t = threadIdx.x; t < m; t += blockDim.x) {
+            const int j = cid[t];
+            ckey[t] = f64_key(exact_score<DI>(kc + (int64_t)j * (DI / 2), ks + (int64_t)j * (DI / 16), v, H));
+        }
+        __syncthreads();
+        kept = best_sorted(cid, ckey, m, k, sm);
     }
-    __syncthreads();
-    // ---- 3. the k best, in rank order
-    const int kept = best_sorted(cid, ckey, m, k, sm);
     int32_t* out = idx_out + gq * k;
     for (int t = threadIdx.x; t < k; t += blockDim.x) out[t] = t < kept ? sm.id[t] : -1;
     __syncthreads();
@@ -303,42 +396,93 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
         nsel = 1;
         __syncthreads();
     } else {
+        const int Kp = pool_blocks - 1;      // blocks chosen by score besides the forced newest one
         const int mb = counts[2 * slab + 1];
         const int32_t* bi = bid + slab * list_len;
         const float2* bl = blu + slab * list_len;
         int krem;
         unsigned int lamb = 0u;
-        if (mb > pool_blocks - 1)
+        if (mb > Kp)
             lamb = block_kth_largest<unsigned int>(
                 [&](int t, unsigned int& key) {
                     key = f32_key(bl[t].x);
                     return true;
                 },
-                mb, pool_blocks - 1, sm.rs, &krem);
+                mb, Kp, sm.rs, &krem);
+        // candidates: blocks whose upper bound reaches the Kp-th largest lower
+        // bound, with their (upper, lower) bound keys packed in ckey
         if (threadIdx.x == 0) sm.rs.ctl[0] = 0;
         __syncthreads();
         for (int base = 0; base < mb; base += blockDim.x) {
             const int t = base + threadIdx.x;
-            const bool f = t < mb && f32_key(bl[t].y) >= lamb;
+            const float2 b2 = t < mb ? bl[t] : make_float2(0.0f, 0.0f);
+            const bool f = t < mb && f32_key(b2.y) >= lamb;
             const int pos = append_slot(f, &sm.rs.ctl[0]);
-            if (f) cid[pos] = bi[t];
+            if (f) {
+                cid[pos] = bi[t];
+                ckey[pos] = ((unsigned long long)f32_key(b2.y) << 32) | f32_key(b2.x);
+            }
         }
         __syncthreads();
         const int mc = sm.rs.ctl[0];
         __syncthreads();
-        for (int t = threadIdx.x; t < mc; t += blockDim.x) ckey[t] = 0ull;
-        __syncthreads();
-        for (int u = threadIdx.x; u < mc * bs; u += blockDim.x) {
-            const int t = u / bs, j = cid[t] * bs + u % bs;
-            const double S = exact_score<DI>(kc + (int64_t)j * (DI / 2), ks + (int64_t)j * (DI / 16), v, H);
-            atomicMax(&ckey[t], f64_key(S));
+        if (mc <= Kp) {
+            // all of them (there are never fewer than Kp)
+            for (int t = threadIdx.x; t < mc; t += blockDim.x) sm.id[t] = cid[t];
+        } else {
+            // mu = the (Kp+1)-th largest upper bound.  A block whose lower bound
+            // is above mu can be outranked only by blocks whose upper bound is
+            // above mu too, at most Kp-1 others: it is in.  Only the rest get
+            // exact block maxima, and fill the remaining slots by (max desc, id asc).
+            const unsigned int mu = block_kth_largest<unsigned int>(
+                [&](int t, unsigned int& key) {
+                    key = (unsigned int)(ckey[t] >> 32);
+                    return true;
+                },
+                mc, Kp + 1, sm.rs, &krem);
+            if (threadIdx.x == 0) {
+                sm.rs.ctl[0] = 0;
+                sm.rs.ctl[3] = 0;
+            }
+            __syncthreads();
+            // in-place compaction of the undecided ones: a window is read in full
+            // before any of it is written, and no slot beyond the window is written
+            for (int base = 0; base < mc; base += blockDim.x) {
+                const int t = base + threadIdx.x;
+                int j = 0;
+                bool in = false, und = false;
+                if (t < mc) {
+                    j = cid[t];
+                    in = (unsigned int)ckey[t] > mu;
+                    und = !in;
+                }
+                __syncthreads();
+                const int pd = append_slot(in, &sm.rs.ctl[3]);
+                if (in) sm.din[pd] = j;
+                const int pu = append_slot(und, &sm.rs.ctl[0]);
+                if (und) {
+                    cid[pu] = j;
+                    ckey[pu] = 0ull;
+                }
+            }
+            __syncthreads();
+            const int nu = sm.rs.ctl[0], nd = sm.rs.ctl[3];
+            __syncthreads();
+            for (int u = threadIdx.x; u < nu * bs; u += blockDim.x) {
+                const int t = u / bs, j = cid[t] * bs + u % bs;
+                const double S = exact_score<DI>(kc + (int64_t)j * (DI / 2), ks + (int64_t)j * (DI / 16), v, H);
+                atomicMax(&ckey[t], f64_key(S));
+            }
+            __syncthreads();
+            const int r = Kp - nd;               // 0 <= r < nu
+            if (r > 0) best_sorted(cid, ckey, nu, r, sm);
+            __syncthreads();
+            for (int t = threadIdx.x; t < nd; t += blockDim.x) sm.id[r + t] = sm.din[t];
         }
         __syncthreads();
-        best_sorted(cid, ckey, mc, pool_blocks - 1, sm);
-        __syncthreads();
         if (threadIdx.x == 0) {
-            sm.id[pool_blocks - 1] = nb - 1;
-            sm.key[pool_blocks - 1] = 0ull;
+            sm.id[Kp] = nb - 1;
+            sm.key[Kp] = 0ull;
         }
         nsel = pool_blocks;
         __syncthreads();
@@ -447,7 +591,10 @@ cudaError_t launch_indexer_full_t(const csa2_cache& c, const uint8_t* iq_codes, 
         }
         if (e != cudaSuccess) return e;
         dim3 g2(n_qc, c.batch);
-        k_select<DI><<<g2, 512, qwords, st>>>(w.ids, w.lu, w.counts, 0, (int)list_len, c.ikey_codes, c.ikey_scales,
+        const size_t smem2 = qwords + SEL_DYN_EXTRA;
+        e = cudaFuncSetAttribute(k_select<DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
+        if (e != cudaSuccess) return e;
+        k_select<DI><<<g2, 512, smem2, st>>>(w.ids, w.lu, w.counts, 0, (int)list_len, c.ikey_codes, c.ikey_scales,
                                               c.capacity, iq_codes, iq_scales, w_head, q_pos, n_q, q0, n_qc, H, k,
                                               idx_out, pool_blocks, bs, pool_out, w.bid, w.blu, w.c2id, w.c2key);
         note_launch();
@@ -462,12 +609,18 @@ cudaError_t launch_reindex_t(const csa2_cache& c, const uint8_t* iq_codes, const
                              const float* w_head, int n_q, int H, const int32_t* pool, int pool_len, int k,
                              int32_t* idx_out, void* ws, cudaStream_t st) {
     const SelectWs w = carve(ws, (int64_t)c.batch * n_q, pool_len);
-    const size_t qwords = (size_t)((QView<DI>::words(H) + 3) & ~3) * sizeof(int);
-    const size_t smem = qwords + (size_t)pool_len * sizeof(float2);
-    cudaError_t e = cudaFuncSetAttribute(k_select<DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const size_t qwords = (size_t)QView<DI>::words(H) * sizeof(int);
+    dim3 g0(n_q, c.batch, (pool_len + 511) / 512);
+    k_pool_bounds<DI><<<g0, 512, qwords, st>>>(pool, pool_len, c.ikey_codes, c.ikey_scales, c.capacity, iq_codes,
+                                                iq_scales, w_head, n_q, H, w.lu);
+    note_launch();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const size_t smem = qwords + SEL_DYN_EXTRA;
+    e = cudaFuncSetAttribute(k_select<DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 g(n_q, c.batch);
-    k_select<DI><<<g, 512, smem, st>>>(pool, nullptr, nullptr, pool_len, pool_len, c.ikey_codes, c.ikey_scales,
+    k_select<DI><<<g, 512, smem, st>>>(pool, w.lu, nullptr, pool_len, pool_len, c.ikey_codes, c.ikey_scales,
                                        c.capacity, iq_codes, iq_scales, w_head, nullptr, n_q, 0, n_q, H, k, idx_out, 0,
                                        1, nullptr, nullptr, nullptr, w.c2id, w.c2key);
     note_launch();

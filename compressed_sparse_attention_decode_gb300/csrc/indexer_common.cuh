@@ -22,13 +22,17 @@ struct QView {
     float* qsc;  // [H][DI/16] E4M3 scales as float
     int* qsi;    // [H][DI/16] the same scales times 2^9 (integers < 2^18)
     float* w;    // [H]
-    __host__ __device__ static int words(int H) { return H * (DI / 4) * 2 + 2 * H * (DI / 16) + H; }
+    double* wd;  // [H] the weights times 2^-20 in fp64 (exact)
+    // 32-bit words of one view; a multiple of 4, so consecutive views stay 16-byte aligned
+    __host__ __device__ static int head_words(int H) { return (H * (DI / 4) * 2 + 2 * H * (DI / 16) + H + 1) & ~1; }
+    __host__ __device__ static int words(int H) { return (head_words(H) + 2 * H + 3) & ~3; }
     __device__ void bind(int* base, int H) {
         qp = base;
         qn = qp + H * (DI / 4);
         qsc = reinterpret_cast<float*>(qn + H * (DI / 4));
         qsi = reinterpret_cast<int*>(qsc + H * (DI / 16));
         w = reinterpret_cast<float*>(qsi + H * (DI / 16));
+        wd = reinterpret_cast<double*>(base + head_words(H));
     }
 };
 
@@ -46,7 +50,10 @@ __device__ void stage_query(QView<DI> v, const uint8_t* __restrict__ codes, cons
         v.qsc[i] = e4m3_to_f32(scales[i]);
         v.qsi[i] = e4m3_times_512(scales[i]);
     }
-    for (int i = tid; i < H; i += nthr) v.w[i] = w[i];
+    for (int i = tid; i < H; i += nthr) {
+        v.w[i] = w[i];
+        v.wd[i] = (double)w[i] * 0x1p-20;
+    }
 }
 
 template <int DI>
@@ -101,11 +108,23 @@ __device__ __forceinline__ void approx_score(const KeyRow<DI>& k, QView<DI> q, i
     U = S + E;
 }
 
+// 0 <= D < 2^53 to fp64 exactly, by integer operations (the conversion
+// instruction runs on the scarce fp64 units)
+__device__ __forceinline__ double u53_to_f64(long long D) {
+    if (D <= 0) return 0.0;
+    const unsigned long long u = (unsigned long long)D;
+    const int e = 63 - __clzll((long long)u);                    // 0 .. 52
+    const unsigned long long man = (u << (52 - e)) & 0x000FFFFFFFFFFFFFull;
+    return __longlong_as_double((long long)(((unsigned long long)(1023 + e) << 52) | man));
+}
+
 // The exact score.  With 2^9-scaled integer scales Sq, Sk and the doubled-code
 // group sum G4 = sum 2q*2k, a group term is G4 * Sq * Sk * 2^-20 exactly, so
-// d_h * 2^20 is an integer (|.| < 2^51) summed in int64 and converted to fp64
-// without rounding; then the fp64 fused multiply-add chain over heads in
-// ascending order.  Only 2-3 fp64 operations per head remain.
+// D_h = d_h * 2^20 is an integer (|.| < 2^51) summed in int64.  The ReLU is
+// taken on D_h, D_h goes to fp64 without rounding, and the head chain
+// S = fma(w_h, d_h, S) in ascending h is evaluated as fma(w_h 2^-20, D_h, S):
+// the same exact product, so the same rounded result, with one fp64
+// operation per head.
 template <int DI>
 __device__ double exact_score(const uint8_t* __restrict__ kc, const uint8_t* __restrict__ ks, QView<DI> q, int H) {
     KeyRow<DI> k;
@@ -128,8 +147,7 @@ __device__ double exact_score(const uint8_t* __restrict__ kc, const uint8_t* __r
             const int G4 = group_dot4(q.qp + h * (DI / 4) + 4 * g, q.qn + h * (DI / 4) + 4 * g, k.kp + 4 * g, k.kn + 4 * g);
             D += (long long)(G4 * q.qsi[h * (DI / 16) + g]) * ski[g];     // |G4*Sq| < 2^30
         }
-        const double d = (double)D * 0x1p-20;                               // exact: |D| < 2^51
-        S = fma((double)q.w[h], d > 0.0 ? d : 0.0, S);
+        S = fma(q.wd[h], u53_to_f64(D), S);
     }
     return S;
 }
@@ -146,28 +164,107 @@ __host__ __device__ inline float bound_factor(int H, int DI) { return 2.0f * (fl
 
 struct RadixSmem {
     int hist[256];
-    int ctl[8];   // [0] append counter, [1] digit, [2] krem, [3] scratch
+    int ctl[8];   // [0] append counter, [1] digit, [2] krem, [3] scratch, [4] [5] global append
+    unsigned long long kmin, kmax;
     int* whist;   // per-warp histograms, (blockDim.x / 32) x 256 ints, set by the caller
 };
 
+template <typename KeyT>
+__device__ __forceinline__ KeyT warp_min_key(KeyT v) {
+    if constexpr (sizeof(KeyT) == 4) {
+        return (KeyT)__reduce_min_sync(0xffffffffu, (unsigned int)v);
+    } else {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const KeyT w = __shfl_xor_sync(0xffffffffu, v, o);
+            v = w < v ? w : v;
+        }
+        return v;
+    }
+}
+template <typename KeyT>
+__device__ __forceinline__ KeyT warp_max_key(KeyT v) {
+    if constexpr (sizeof(KeyT) == 4) {
+        return (KeyT)__reduce_max_sync(0xffffffffu, (unsigned int)v);
+    } else {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const KeyT w = __shfl_xor_sync(0xffffffffu, v, o);
+            v = w > v ? w : v;
+        }
+        return v;
+    }
+}
+
 // k-th largest key (1 <= k <= number of taking items) over items t in [0, n):
 // getkey(t, key) returns false for items that do not take part.  Returns the
-// key and sets *krem to how many items equal to it are needed.  Each warp
-// counts into its own histogram (shared-memory atomics, so equal digits from
-// one warp only contend within that warp), then the warps' counts are summed.
+// key and sets *krem to how many items equal to it are needed.  A first pass
+// finds the keys' range; the bits above the highest bit in which the smallest
+// and largest keys differ are common to every key, so the digit passes (8 bits
+// each) start right below them, where the keys spread.  Each warp counts into
+// its own histogram (shared-memory atomics), then the warps' counts are summed.
 template <typename KeyT, typename Get>
 __device__ KeyT block_kth_largest(Get getkey, int n, int k, RadixSmem& rs, int* krem_out) {
     constexpr int BITS = sizeof(KeyT) * 8;
     const int lane = threadIdx.x & 31, nw = blockDim.x >> 5;
     int* wh = rs.whist + (threadIdx.x >> 5) * 256;
-    KeyT prefix = 0, mask = 0;
+    // ---- key range
+    if (threadIdx.x == 0) {
+        rs.kmin = ~0ull;
+        rs.kmax = 0ull;
+    }
+    __syncthreads();
+    {
+        KeyT lo = (KeyT)~(KeyT)0, hi = 0;
+        for (int t0 = threadIdx.x; t0 < n; t0 += 8 * blockDim.x) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int t = t0 + u * blockDim.x;
+                KeyT key;
+                if (t < n && getkey(t, key)) {
+                    lo = key < lo ? key : lo;
+                    hi = key > hi ? key : hi;
+                }
+            }
+        }
+        lo = warp_min_key(lo);
+        hi = warp_max_key(hi);
+        if (lane == 0) {
+            atomicMin(&rs.kmin, (unsigned long long)lo);
+            atomicMax(&rs.kmax, (unsigned long long)hi);
+        }
+    }
+    __syncthreads();
+    const KeyT kmin = (KeyT)rs.kmin, kmax = (KeyT)rs.kmax;
+    const KeyT diff = kmin ^ kmax;
     int krem = k;
-    for (int shift = BITS - 8; shift >= 0; shift -= 8) {
+    if (diff == 0 || kmin > kmax) {               // one distinct key (or nothing takes part)
+        __syncthreads();
+        *krem_out = krem;
+        return kmax;
+    }
+    int top = BITS - 1;                           // highest bit not yet fixed
+    while (((diff >> top) & 1) == 0) --top;
+    const KeyT common = top == BITS - 1 ? (KeyT)0 : (KeyT)(~(KeyT)0) << (top + 1);
+    KeyT prefix = kmin & common, mask = common;
+    while (top >= 0) {
+        const int width = top + 1 < 8 ? top + 1 : 8;
+        const int shift = top - width + 1;
+        const KeyT dmask = (KeyT)((1u << width) - 1u);
         for (int i = threadIdx.x; i < nw * 256; i += blockDim.x) rs.whist[i] = 0;
         __syncthreads();
-        for (int t = threadIdx.x; t < n; t += blockDim.x) {
-            KeyT key;
-            if (getkey(t, key) && (key & mask) == prefix) atomicAdd(&wh[(int)((key >> shift) & 255)], 1);
+        // keys fetched 8 at a time ahead of the atomics, so their loads overlap
+        for (int t0 = threadIdx.x; t0 < n; t0 += 8 * blockDim.x) {
+            KeyT kk[8];
+            bool in[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int t = t0 + u * blockDim.x;
+                in[u] = t < n && getkey(t, kk[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (in[u] && (kk[u] & mask) == prefix) atomicAdd(&wh[(int)((kk[u] >> shift) & dmask)], 1);
         }
         __syncthreads();
         for (int i = threadIdx.x; i < 256; i += blockDim.x) {
@@ -203,9 +300,10 @@ __device__ KeyT block_kth_largest(Get getkey, int n, int k, RadixSmem& rs, int* 
         }
         __syncthreads();
         prefix |= (KeyT)rs.ctl[1] << shift;
-        mask |= (KeyT)255 << shift;
+        mask |= dmask << shift;
         krem = rs.ctl[2];
         __syncthreads();
+        top = shift - 1;
     }
     *krem_out = krem;
     return prefix;
@@ -223,6 +321,36 @@ __device__ __forceinline__ int append_slot(bool flag, int* ctr) {
 }
 
 
+// Block-wide append of the items i in [0, n) with flag(i) to a list in global
+// memory whose length counter is *gctr: the block counts its items, reserves
+// them with ONE global atomic, then places them (put(slot, i)) at positions
+// taken from a shared-memory counter.  Every thread of the block calls it;
+// rs.ctl[4] must be 0 on entry and is 0 again on return.
+template <typename Flag, typename Put>
+__device__ void block_append_global(int n, Flag flag, Put put, int* gctr, RadixSmem& rs) {
+    int c = 0;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) c += flag(i) ? 1 : 0;
+    c = __reduce_add_sync(0xffffffffu, c);
+    if ((threadIdx.x & 31) == 0 && c) atomicAdd(&rs.ctl[4], c);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const int tot = rs.ctl[4];
+        rs.ctl[5] = tot ? atomicAdd(gctr, tot) : 0;
+        rs.ctl[4] = 0;
+    }
+    __syncthreads();
+    const int g = rs.ctl[5];
+    for (int base = 0; base < n; base += blockDim.x) {
+        const int i = base + threadIdx.x;
+        const bool f = i < n && flag(i);
+        const int pos = append_slot(f, &rs.ctl[4]);
+        if (f) put(g + pos, i);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) rs.ctl[4] = 0;
+    __syncthreads();
+}
+
 // After a scan block has the (S~-E, S~+E) bounds of its chunk in shared memory
 // (lu[0..E), entries c0..c0+E-1), forward to the query's global lists every
 // entry whose upper bound reaches the chunk's k-th largest lower bound, and
@@ -234,6 +362,8 @@ static __device__ void forward_candidates(const float2* lu, int c0, int E, int n
                                    float2* blu, RadixSmem& rs) {
     const int n_loc = min(max(n_elig - c0, 0), E);
     if (n_loc == 0) return;                       // uniform
+    if (threadIdx.x == 0) rs.ctl[4] = 0;
+    __syncthreads();
     unsigned int lam = 0u;
     if (n_loc > k) {
         int krem;
@@ -244,15 +374,13 @@ static __device__ void forward_candidates(const float2* lu, int c0, int E, int n
             },
             n_loc, k, rs, &krem);
     }
-    for (int base = 0; base < n_loc; base += blockDim.x) {
-        const int i = base + threadIdx.x;
-        const bool f = i < n_loc && f32_key(lu[i].y) >= lam;
-        const int pos = append_slot(f, counts + 2 * slab);
-        if (f) {
+    block_append_global(
+        n_loc, [&](int i) { return f32_key(lu[i].y) >= lam; },
+        [&](int pos, int i) {
             cid[slab * list_len + pos] = c0 + i;
             clu[slab * list_len + pos] = lu[i];
-        }
-    }
+        },
+        counts + 2 * slab, rs);
     if (pool_blocks > 1) {
         const int nb = (n_elig + bs - 1) / bs;           // blocks of this query
         const int forced = nb - 1;
@@ -278,20 +406,13 @@ static __device__ void forward_candidates(const float2* lu, int c0, int E, int n
                     },
                     nbl, pool_blocks - 1, rs, &krem);
             }
-            for (int base = 0; base < nbl; base += blockDim.x) {
-                const int bl = base + threadIdx.x;
-                float2 m2 = make_float2(-INFINITY, -INFINITY);
-                bool f = false;
-                if (bl < nbl && g0 + bl != forced) {
-                    m2 = make_float2(blk(bl, false), blk(bl, true));
-                    f = f32_key(m2.y) >= lamb;
-                }
-                const int pos = append_slot(f, counts + 2 * slab + 1);
-                if (f) {
+            block_append_global(
+                nbl, [&](int bl) { return g0 + bl != forced && f32_key(blk(bl, true)) >= lamb; },
+                [&](int pos, int bl) {
                     bid[slab * list_len + pos] = g0 + bl;
-                    blu[slab * list_len + pos] = m2;
-                }
-            }
+                    blu[slab * list_len + pos] = make_float2(blk(bl, false), blk(bl, true));
+                },
+                counts + 2 * slab + 1, rs);
         }
     }
 }
