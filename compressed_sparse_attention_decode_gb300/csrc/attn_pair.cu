@@ -10,9 +10,9 @@
 //   (S = S_0 + S_1, the same bits in both CTAs); an online softmax with a lazy
 //   running max (a max reduction runs only when some score rises more than 2^8
 //   above the running max) writes P (fp16), and both CTAs accumulate their own
-//   output dims: O_r^T += L[:, dims_r]^T . P (TMEM, across all tiles).  The
-//   row sums l come from the same fp16 P, reduced across each warp's rows by
-//   shuffles.
+//   output dims: O_r^T += L[:, dims_r]^T . P, l += 1^T . P (TMEM, across all
+//   tiles).  One thread per CTA waits on the barriers the peer fills (cluster
+//   scope) and passes them on through a named barrier of the softmax warps.
 // The query's top-k indices are staged in shared memory at the start and every
 // row the CTA will read is prefetched into L2, so the tile gathers that follow
 // (double-buffered, overlapping the MMAs and softmax) are single L2 round trips.
@@ -38,13 +38,14 @@ constexpr uint32_t AP_SQ = 0;                        // Q half: 4 slabs x 64 hea
 constexpr uint32_t AP_SL = 32 * 1024;                // 2 buffers x 4 slabs (128 KB)
 constexpr uint32_t AP_LBUF = 4 * AP_SLAB;
 constexpr uint32_t AP_SP = AP_SL + 2 * AP_LBUF;      // P: 128 keys x 64 heads fp16 (16 KB)
-constexpr uint32_t AP_SX = AP_SP + 16 * 1024;        // the peer's partial scores, 128 x 64 f32 (32 KB)
+constexpr uint32_t AP_SONES = AP_SP + 16 * 1024;     // ones, 128 x 16 fp16 (4 KB)
+constexpr uint32_t AP_SX = AP_SONES + 4 * 1024;      // the peer's partial scores, 128 x 64 f32 (32 KB)
 constexpr uint32_t AP_SIDX = AP_SX + 32 * 1024;      // the query's indices, MAX_K ints
 constexpr uint32_t AP_RED = AP_SIDX + MAX_K * 4;     // column maxima / row sums, 4 quadrants x 64
 constexpr uint32_t AP_MISC = AP_RED + 1024;          // m_run[64], fac[64], flags
 constexpr uint32_t AP_DYN = AP_MISC + 1024 + 1024;
 constexpr uint32_t AP_XBYTES = AP_TILE * AP_H * 4;   // partial scores one CTA sends per tile
-constexpr uint32_t APT_S = 0, APT_O = 128, APT_COLS = 256;
+constexpr uint32_t APT_S = 0, APT_O = 128, APT_L = 256, APT_COLS = 512;
 constexpr float AP_LAZY = 8.0f;                      // log2 headroom before the running max is raised
 
 __device__ __forceinline__ uint32_t apswz(uint32_t row, uint32_t chunk) { return row * 128 + ((chunk ^ (row & 7)) << 4); }
@@ -114,7 +115,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
         umma::mbar_init(sa(&b_pfull), AP_SMW);
         umma::mbar_init(sa(&b_odone), 1);
         umma::mbar_init(sa(&b_xfull), 1);          // armed by this CTA, filled by the peer's stores
-        umma::mbar_init(sa(&b_xfree), AP_SMW);     // one arrival per peer softmax warp
+        umma::mbar_init(sa(&b_xfree), 1);          // the peer's thread 0, once it has read the scores
         umma::fence_mbar_init();
         umma::mbar_arrive_expect_tx(sa(&b_xfull), AP_XBYTES);
     }
@@ -136,6 +137,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                            ap_bf16x2_to_f16x2(v.w));
         }
     }
+    if (tid < 256) reinterpret_cast<uint4*>(sm + AP_SONES)[tid] = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
     float* m_run = reinterpret_cast<float*>(sm + AP_MISC);
     float* fac = m_run + AP_H;
     int* flag = reinterpret_cast<int*>(fac + AP_H);
@@ -247,6 +249,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
         if (lane == 0) {
             const uint32_t id1 = umma::idesc_f16(128, AP_H, 0, 0);
             const uint32_t id2 = umma::idesc_f16(128, AP_H, 1, 1);
+            const uint32_t id3 = umma::idesc_f16(128, AP_H, 0, 1);
             // Two independent streams: GEMM1 of tile t needs its half rows loaded
             // (lfull) and its score buffer released (sfree of tile t-2); GEMM2 of
             // tile t needs P (pfull).  Serve whichever is ready, so a slow load of
@@ -287,6 +290,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                             umma::mma_f16(tmem + APT_O + 64 * mt, a, bp, id2, (n2 > 0 || ks > 0) ? 1u : 0u);
                         }
                     }
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint64_t a = umma::desc(base + AP_SONES, 128, 256, umma::LAYOUT_NONE);
+                        const uint64_t bp = umma::desc(base + AP_SP + ks * 2048, 8192, 1024, umma::LAYOUT_SW128);
+                        umma::mma_f16(tmem + APT_L, a, bp, id3, (n2 > 0 || ks > 0) ? 1u : 0u);
+                    }
                     umma::commit(sa(&b_odone));
                     umma::commit(sa(&b_lfree[buf]));
                     ++n2;
@@ -311,7 +320,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
         const uint32_t xfree_peer = umma::mapa(sa(&b_xfree), peer);
         float* red = reinterpret_cast<float*>(sm + AP_RED);           // [4 quadrants][64 heads]
         const float* sx = reinterpret_cast<const float*>(sm + AP_SX);
-        float lsum = 0.0f;          // sum of P over this warp's rows, head hc + lane, all tiles so far
         for (int t = 0; t < T; ++t) {
             const int buf = t & 1;
             float x[32];
@@ -325,13 +333,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
             if (lane == 0) umma::mbar_arrive(sa(&b_sfree[buf]));
             // send the partial scores to the peer (16-byte chunks swizzled by row
             // to spread banks), once it has read the previous ones
-            if (t >= 1) ok &= umma::mbar_wait_cluster(sa(&b_xfree), (t - 1) & 1);
+            if (t >= 1) {
+                if (tid == 0) ok &= umma::mbar_wait_cluster(sa(&b_xfree), (t - 1) & 1);
+                umma::bar_named(1, AP_SMT);
+            }
 #pragma unroll
             for (int c = 0; c < 8; ++c)
                 umma::st_async_v4(sx_peer + row * 256 + (((hh * 8 + c) ^ (row & 15)) << 4), x[4 * c], x[4 * c + 1],
                                   x[4 * c + 2], x[4 * c + 3], xfull_peer);
-            ok &= umma::mbar_wait_cluster(sa(&b_xfull), t & 1);
-            if (tid == 0 && t + 1 < T) umma::mbar_arrive_expect_tx(sa(&b_xfull), AP_XBYTES);   // arm the next tile
+            if (tid == 0) {
+                ok &= umma::mbar_wait_cluster(sa(&b_xfull), t & 1);
+                if (t + 1 < T) umma::mbar_arrive_expect_tx(sa(&b_xfull), AP_XBYTES);   // arm the next tile
+            }
+            umma::bar_named(1, AP_SMT);
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 const float4 v = *reinterpret_cast<const float4*>(sx + row * 64 + (((hh * 8 + c) ^ (row & 15)) << 2));
@@ -341,8 +355,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                 x[4 * c + 2] += v.z;
                 x[4 * c + 3] += v.w;
             }
-            __syncwarp();
-            if (lane == 0) umma::mbar_arrive_remote(xfree_peer);
             // row validity was written by the loaders of this buffer: observe their barrier too
             ok &= umma::mbar_wait(sa(&b_lfull[buf]), (t >> 1) & 1);
             const bool valid = rowok[buf][row] != 0;
@@ -352,8 +364,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                 x[h] = valid ? x[h] * scale_log2e : -INFINITY;
                 exceed |= x[h] > m_run[hc + h] + AP_LAZY;
             }
-            // both CTAs hold the same scores, so they take the same branch
+            // both CTAs hold the same scores, so they take the same branch; past
+            // this barrier every warp has read the peer's scores
             const bool raise = umma::bar_red_or(1, AP_SMT, exceed);
+            if (tid == 0) umma::mbar_arrive_remote(xfree_peer);
             if (raise) {
                 // new running max for the heads that rose too far: column maxima of the tile
 #pragma unroll
@@ -378,10 +392,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                 umma::bar_named(1, AP_SMT);
                 umma::fence_after();
                 if (t >= 1 && (flag[0] | flag[1])) {
-                    // rescale O^T (both dim tiles) in this thread's 32 head columns
+                    // rescale O^T (both dim tiles) and l in this thread's 32 head columns
 #pragma unroll 1
-                    for (int blk = 0; blk < 2; ++blk) {
-                        const uint32_t col0 = APT_O + 64 * blk + hc;
+                    for (int blk = 0; blk < 3; ++blk) {
+                        const uint32_t col0 = (blk < 2 ? APT_O + 64 * blk : APT_L) + hc;
 #pragma unroll
                         for (int c = 0; c < 32; c += 16) {
                             float v[16];
@@ -394,12 +408,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                     }
                     umma::tmem_wait_st();
                 }
-                lsum *= fac[hc + lane];
             } else if (t >= 1) {
                 ok &= umma::mbar_wait(sa(&b_odone), (t - 1) & 1);             // GEMM2 of t-1 has read P
             }
-            // P = exp2(x - m_run), fp16, row = key (MN-major B operand), this thread's 4 chunks;
-            // x keeps the rounded values for the row sums
+            // P = exp2(x - m_run), fp16, row = key (MN-major B operand), this thread's 4 chunks
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t w[4];
@@ -411,9 +423,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                     const float p1 = (x[h + 1] == -INFINITY || m1 == -INFINITY) ? 0.0f : umma::ex2(x[h + 1] - m1);
                     const __half2 hp = __floats2half2_rn(p0, p1);
                     w[e] = *reinterpret_cast<const uint32_t*>(&hp);
-                    const float2 back = __half22float2(hp);
-                    x[h] = back.x;
-                    x[h + 1] = back.y;
                 }
                 *reinterpret_cast<uint4*>(sm + AP_SP + apswz(row, hh * 4 + c)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
@@ -421,28 +430,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
             umma::fence_before();
             __syncwarp();
             if (lane == 0) umma::mbar_arrive(sa(&b_pfull));
-            // sum of the rounded P over the warp's 32 rows: after the butterfly, lane L holds head hc + L
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) {
-                const bool upper = (lane & o) != 0;
-#pragma unroll
-                for (int i = 0; i < o; ++i) {
-                    const float send = upper ? x[i] : x[i + o];
-                    const float keep = upper ? x[i + o] : x[i];
-                    x[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-                }
-            }
-            lsum += x[0];
         }
         // ================= epilogue: thread = output dim 32*(warp%4)+lane of each 128-dim tile, its 32 heads
-        red[qd * AP_H + hc + lane] = lsum;
-        umma::bar_named(1, AP_SMT);
         ok &= umma::mbar_wait(sa(&b_odone), (T - 1) & 1);
         umma::fence_after();
         float inv[32];
-#pragma unroll
-        for (int h = 0; h < 32; ++h)
-            inv[h] = (red[hc + h] + red[AP_H + hc + h]) + (red[2 * AP_H + hc + h] + red[3 * AP_H + hc + h]);
+        umma::tmem_ld16(lane_base + APT_L + hc, inv);
+        umma::tmem_ld16(lane_base + APT_L + hc + 16, inv + 16);
+        umma::tmem_wait_ld();
         if (lse != nullptr && rank == 0 && qd == 0 && lane == 0)
 #pragma unroll
             for (int h = 0; h < 32; ++h)

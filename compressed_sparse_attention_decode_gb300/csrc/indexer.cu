@@ -331,16 +331,14 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
     __syncthreads();
     const int n_valid = sm.rs.ctl[3];
     __syncthreads();
-    unsigned int lam = 0u;
-    if (n_valid > k) {
-        int krem;
-        lam = block_kth_largest<unsigned int>(
+    unsigned int lam = 0u;                       // <= the k-th largest lower bound
+    if (n_valid > k)
+        lam = block_kth_bound(
             [&](int t, unsigned int& key) {
                 key = f32_key(L[t].x);
                 return true;
             },
-            n, k, sm.rs, &krem);
-    }
+            n, k, false, sm.rs);
     if (threadIdx.x == 0) sm.rs.ctl[0] = 0;
     __syncthreads();
     for (int base = 0; base < n; base += blockDim.x) {
@@ -400,15 +398,14 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
         const int mb = counts[2 * slab + 1];
         const int32_t* bi = bid + slab * list_len;
         const float2* bl = blu + slab * list_len;
-        int krem;
         unsigned int lamb = 0u;
-        if (mb > Kp)
-            lamb = block_kth_largest<unsigned int>(
+        if (mb > Kp)                          // <= the Kp-th largest lower bound
+            lamb = block_kth_bound(
                 [&](int t, unsigned int& key) {
                     key = f32_key(bl[t].x);
                     return true;
                 },
-                mb, Kp, sm.rs, &krem);
+                mb, Kp, false, sm.rs);
         // candidates: blocks whose upper bound reaches the Kp-th largest lower
         // bound, with their (upper, lower) bound keys packed in ckey
         if (threadIdx.x == 0) sm.rs.ctl[0] = 0;
@@ -430,16 +427,16 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
             // all of them (there are never fewer than Kp)
             for (int t = threadIdx.x; t < mc; t += blockDim.x) sm.id[t] = cid[t];
         } else {
-            // mu = the (Kp+1)-th largest upper bound.  A block whose lower bound
+            // mu >= the (Kp+1)-th largest upper bound.  A block whose lower bound
             // is above mu can be outranked only by blocks whose upper bound is
             // above mu too, at most Kp-1 others: it is in.  Only the rest get
             // exact block maxima, and fill the remaining slots by (max desc, id asc).
-            const unsigned int mu = block_kth_largest<unsigned int>(
+            const unsigned int mu = block_kth_bound(    // >= the (Kp+1)-th largest upper bound
                 [&](int t, unsigned int& key) {
                     key = (unsigned int)(ckey[t] >> 32);
                     return true;
                 },
-                mc, Kp + 1, sm.rs, &krem);
+                mc, Kp + 1, true, sm.rs);
             if (threadIdx.x == 0) {
                 sm.rs.ctl[0] = 0;
                 sm.rs.ctl[3] = 0;

@@ -309,6 +309,118 @@ __device__ KeyT block_kth_largest(Get getkey, int n, int k, RadixSmem& rs, int* 
     return prefix;
 }
 
+// A bound on the k-th largest of the 32-bit keys (1 <= k <= number taking
+// part): a key <= it (upper == false) or >= it (upper == true).  The keys'
+// range is cut into 256 buckets of equal width (the bucket index never
+// decreases as the key grows, so every key of a higher bucket is larger); the
+// bucket holding the k-th largest is found from the top; while it still holds
+// more than 64 keys its own range is cut again (at most four levels).  The
+// bound is the smallest (largest) key of the last bucket.  Used where the
+// caller only filters with the value: equal-width buckets spread the
+// shared-memory atomics even when the keys share their leading bits, and the
+// refinement keeps the bound within a few dozen keys of the exact one.
+template <typename Get>
+__device__ unsigned int block_kth_bound(Get getkey, int n, int k, bool upper, RadixSmem& rs) {
+    const int lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    int* wh = rs.whist + (threadIdx.x >> 5) * 256;
+    // min / max of the keys in [lo, hi] whose bucket is bsel (bsel < 0: all of them), into rs.kmin / rs.kmax
+    auto range_pass = [&](unsigned int lo, unsigned int hi, float scale, int bsel) {
+        unsigned int mn = ~0u, mx = 0u;
+        for (int t0 = threadIdx.x; t0 < n; t0 += 8 * blockDim.x) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int t = t0 + u * blockDim.x;
+                unsigned int key;
+                if (t < n && getkey(t, key) && key >= lo && key <= hi &&
+                    (bsel < 0 || min((int)((float)(key - lo) * scale), 255) == bsel)) {
+                    mn = min(mn, key);
+                    mx = max(mx, key);
+                }
+            }
+        }
+        mn = __reduce_min_sync(0xffffffffu, mn);
+        mx = __reduce_max_sync(0xffffffffu, mx);
+        if (lane == 0) {
+            atomicMin(&rs.kmin, (unsigned long long)mn);
+            atomicMax(&rs.kmax, (unsigned long long)mx);
+        }
+    };
+    if (threadIdx.x == 0) {
+        rs.kmin = ~0ull;
+        rs.kmax = 0ull;
+    }
+    __syncthreads();
+    range_pass(0u, ~0u, 0.0f, -1);
+    __syncthreads();
+    unsigned int lo = (unsigned int)rs.kmin, hi = (unsigned int)rs.kmax;
+    int need = k;
+    for (int level = 0; level < 4 && lo < hi; ++level) {
+        for (int i = threadIdx.x; i < nw * 256; i += blockDim.x) rs.whist[i] = 0;
+        __syncthreads();
+        const float scale = 256.0f / ((float)(hi - lo) + 1.0f);
+        for (int t0 = threadIdx.x; t0 < n; t0 += 8 * blockDim.x) {
+            unsigned int kk[8];
+            bool in[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int t = t0 + u * blockDim.x;
+                in[u] = t < n && getkey(t, kk[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (in[u] && kk[u] >= lo && kk[u] <= hi) atomicAdd(&wh[min((int)((float)(kk[u] - lo) * scale), 255)], 1);
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < 256; i += blockDim.x) {
+            int c = 0;
+            for (int w = 0; w < nw; ++w) c += rs.whist[w * 256 + i];
+            rs.hist[i] = c;
+        }
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            int c = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) c += rs.hist[255 - 8 * lane - i];   // lane 0 holds the top bins
+            int incl = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const unsigned hit = __ballot_sync(0xffffffffu, incl >= need);
+            const int L = hit ? __ffs(hit) - 1 : 31;
+            if (lane == L) {
+                int cum = incl - c, d = 255 - 8 * lane - 7;
+                for (int i = 0; i < 8; ++i) {
+                    const int dd = 255 - 8 * lane - i;
+                    if (cum + rs.hist[dd] >= need) {
+                        d = dd;
+                        break;
+                    }
+                    cum += rs.hist[dd];
+                }
+                rs.ctl[1] = d;
+                rs.ctl[2] = need - cum;
+                rs.ctl[3] = rs.hist[d];
+            }
+            if (lane == 0) {
+                rs.kmin = ~0ull;
+                rs.kmax = 0ull;
+            }
+        }
+        __syncthreads();
+        const int bstar = rs.ctl[1], cnt = rs.ctl[3];
+        need = rs.ctl[2];
+        range_pass(lo, hi, scale, bstar);
+        __syncthreads();
+        lo = (unsigned int)rs.kmin;
+        hi = (unsigned int)rs.kmax;
+        if (cnt <= 64) break;
+    }
+    __syncthreads();
+    return upper ? hi : lo;
+}
+
 // warp-aggregated append to a list whose counter lives at *ctr (shared or global)
 __device__ __forceinline__ int append_slot(bool flag, int* ctr) {
     const unsigned m = __ballot_sync(0xffffffffu, flag);
@@ -353,7 +465,8 @@ __device__ void block_append_global(int n, Flag flag, Put put, int* gctr, RadixS
 
 // After a scan block has the (S~-E, S~+E) bounds of its chunk in shared memory
 // (lu[0..E), entries c0..c0+E-1), forward to the query's global lists every
-// entry whose upper bound reaches the chunk's k-th largest lower bound, and
+// entry whose upper bound reaches (a lower bound of) the chunk's k-th largest
+// lower bound, and
 // likewise for HSI blocks (bounds = max over members; the newest block, which
 // is always kept, is not forwarded).  The global k-th lower bound is never
 // smaller than a chunk's, so nothing the exact selection needs is dropped.
@@ -364,16 +477,14 @@ static __device__ void forward_candidates(const float2* lu, int c0, int E, int n
     if (n_loc == 0) return;                       // uniform
     if (threadIdx.x == 0) rs.ctl[4] = 0;
     __syncthreads();
-    unsigned int lam = 0u;
-    if (n_loc > k) {
-        int krem;
-        lam = block_kth_largest<unsigned int>(
+    unsigned int lam = 0u;                        // <= the chunk's k-th largest lower bound
+    if (n_loc > k)
+        lam = block_kth_bound(
             [&](int i, unsigned int& key) {
                 key = f32_key(lu[i].x);
                 return true;
             },
-            n_loc, k, rs, &krem);
-    }
+            n_loc, k, false, rs);
     block_append_global(
         n_loc, [&](int i) { return f32_key(lu[i].y) >= lam; },
         [&](int pos, int i) {
@@ -397,15 +508,13 @@ static __device__ void forward_candidates(const float2* lu, int c0, int E, int n
                 return mx;
             };
             unsigned int lamb = 0u;
-            if (nvalid > pool_blocks - 1) {
-                int krem;
-                lamb = block_kth_largest<unsigned int>(
+            if (nvalid > pool_blocks - 1)
+                lamb = block_kth_bound(
                     [&](int bl, unsigned int& key) {
                         key = f32_key(blk(bl, false));
                         return g0 + bl != forced;
                     },
-                    nbl, pool_blocks - 1, rs, &krem);
-            }
+                    nbl, pool_blocks - 1, false, rs);
             block_append_global(
                 nbl, [&](int bl) { return g0 + bl != forced && f32_key(blk(bl, true)) >= lamb; },
                 [&](int pos, int bl) {
