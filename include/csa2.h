@@ -118,7 +118,7 @@ csa2_status csa2_quantize_fp4(const float* x, int64_t n_rows, int32_t d, uint8_t
  *   w_head    fp32  [batch][n_q][n_heads]
  *   q_pos     int64 [batch][n_q]  raw position of each query (device memory);
  *             n_elig is clamped to capacity
- *   idx_out   int32 [batch][n_q][k]  entry ids in rank order, -1 padded
+ *   idx_out   int32 [batch][n_q][k]  the chosen entry ids in ascending order, -1 padded
  *   pool_out  int32 [batch][n_q][pool_blocks*pool_block_size] or NULL when
  *             pool_blocks == 0; -1 padded
  * 1 <= k <= 2048; 1 <= n_heads <= 32; pool_blocks*pool_block_size <= 16384.
@@ -132,7 +132,7 @@ csa2_status csa2_indexer_topk(const csa2_cache* cache, const uint8_t* iq_codes, 
 /*
  * Reindex / Reuse ("DeepSeek-v4.1 Flash" §2.3.2 and §2.3.4).
  *   mode CSA2_REINDEX: score only the pool entries with this layer's indexer
- *     queries and keep the top k inside the pool (rank order, -1 padded);
+ *     queries and keep the top k inside the pool (ascending entry order, -1 padded);
  *     pool int32 [batch][n_q][pool_len] (-1 slots ignored), pool_len <= 16384.
  *   mode CSA2_REUSE: idx_out = prev_idx, bit for bit (a device copy); the
  *     indexer arguments and the pool may be NULL.

@@ -155,6 +155,7 @@ def index_scores(kcodes, kscales, qcodes, qscales, w, ids=None, n=None):
 
 
 def topk(S, k, ids=None):
+    """the k best ids by (S desc, id asc), written in ascending id order, -1 padded"""
     S, sp = _c(S, np.float64)
     if ids is not None:
         ids, idp = _c(ids, np.int32)

@@ -220,8 +220,15 @@ static int by_score_desc_id_asc(const void* a, const void* b) {
     return (x->id < y->id) ? -1 : (x->id > y->id);
 }
 
-/* Top-k by a full sort of (score desc, id asc); entries with negative id are
- * not candidates; missing slots are -1.  Output is in rank order. */
+static int by_id_asc(const void* a, const void* b) {
+    const int32_t x = *(const int32_t*)a, y = *(const int32_t*)b;
+    return (x > y) - (x < y);
+}
+
+/* Top-k: the k best entries by a full sort of (score desc, id asc); entries
+ * with negative id are not candidates.  The selection is a set of positions:
+ * it is written in ascending entry order (as the pages print the read
+ * positions of their toy example), missing slots -1 at the end. */
 void orc_topk(const double* S, const int32_t* ids, int64_t n, int k, int32_t* out) {
     scored* v = (scored*)malloc(sizeof(scored) * (n > 0 ? n : 1));
     int64_t m = 0;
@@ -233,7 +240,10 @@ void orc_topk(const double* S, const int32_t* ids, int64_t n, int k, int32_t* ou
         ++m;
     }
     qsort(v, (size_t)m, sizeof(scored), by_score_desc_id_asc);
-    for (int i = 0; i < k; ++i) out[i] = (i < m) ? v[i].id : -1;
+    int64_t kept = m < k ? m : k;
+    for (int64_t i = 0; i < kept; ++i) out[i] = v[i].id;
+    qsort(out, (size_t)kept, sizeof(int32_t), by_id_asc);
+    for (int64_t i = kept; i < k; ++i) out[i] = -1;
     free(v);
 }
 

@@ -84,7 +84,7 @@ def test_topk_brute_force_and_heap_select():
         got = oracle.topk(S, k)
         ref = sorted(range(n), key=lambda j: (-S[j], j))[:k]
         heap = [j for _, j in heapq.nsmallest(k, [(-S[j], j) for j in range(n)])]
-        want = ref + [-1] * (k - len(ref))
+        want = sorted(ref) + [-1] * (k - len(ref))        # the chosen set, ascending
         assert got.tolist() == want and heap == ref
 
 
@@ -172,7 +172,7 @@ def test_toy_full_reindex_reuse_example():
     re[3] = 50.0                                        # not in the pool: must not be picked
     S_pool = re[pool]
     idx = oracle.topk(S_pool, 4, ids=pool)
-    assert sorted(idx.tolist()) == read and idx.tolist() == [10, 23, 15, 2]
+    assert idx.tolist() == read                         # the pages' read positions, in their order
     reuse = idx.copy()                                  # Reuse: same entries, new weights
     assert reuse.tolist() == idx.tolist()
 
