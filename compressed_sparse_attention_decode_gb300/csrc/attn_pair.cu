@@ -61,6 +61,12 @@ __device__ __forceinline__ void ap_e2m1x8(uint32_t w, uint32_t* o) {
         : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
         : "r"(w));
 }
+// two E4M3 bytes (low byte -> low half) to fp16x2, exactly
+__device__ __forceinline__ __half2 ap_e4m3x2(uint32_t two) {
+    uint32_t r;
+    asm("{\n .reg .b16 t;\n cvt.u16.u32 t, %1;\n cvt.rn.f16x2.e4m3x2 %0, t;\n}" : "=r"(r) : "r"(two));
+    return *reinterpret_cast<__half2*>(&r);
+}
 __device__ __forceinline__ uint32_t ap_hmul2(uint32_t a, __half2 s) {
     __half2 x = __hmul2(*reinterpret_cast<__half2*>(&a), s);
     return *reinterpret_cast<uint32_t*>(&x);
@@ -224,16 +230,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                         const int slot = t * AP_TILE + r;
                         const bool valid = slot < k && sidx[slot] >= 0;
                         const uint32_t words[4] = {cw[i].x, cw[i].y, cw[i].z, cw[i].w};
+                        // an empty slot has zero codes and zero scales, so it expands to zeros
+                        const __half2 sp = ap_e4m3x2(sc[i]);
+                        const __half2 s_lo = __low2half2(sp), s_hi = __high2half2(sp);
 #pragma unroll
                         for (int w = 0; w < 4; ++w) {        // 8 dims per word; scale group 2c + w/2
-                            uint4 o = make_uint4(0, 0, 0, 0);
-                            if (valid) {
-                                const __half2 s2 = __float2half2_rn(e4m3_to_f32((sc[i] >> (8 * (w >> 1))) & 255u));
-                                uint32_t f[4];
-                                ap_e2m1x8(words[w], f);
-                                o = make_uint4(ap_hmul2(f[0], s2), ap_hmul2(f[1], s2), ap_hmul2(f[2], s2),
-                                               ap_hmul2(f[3], s2));
-                            }
+                            const __half2 s2 = (w >> 1) ? s_hi : s_lo;
+                            uint32_t f[4];
+                            ap_e2m1x8(words[w], f);
+                            const uint4 o = make_uint4(ap_hmul2(f[0], s2), ap_hmul2(f[1], s2), ap_hmul2(f[2], s2),
+                                                       ap_hmul2(f[3], s2));
                             const int cc = c * 4 + w;                // 8-dim chunk 0..31
                             *reinterpret_cast<uint4*>(L + (cc >> 3) * AP_SLAB + apswz(r, cc & 7)) = o;
                         }
@@ -360,14 +366,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
             const bool valid = rowok[buf][row] != 0;
             bool exceed = false;
 #pragma unroll
-            for (int h = 0; h < 32; ++h) {
-                x[h] = valid ? x[h] * scale_log2e : -INFINITY;
-                exceed |= x[h] > m_run[hc + h] + AP_LAZY;
+            for (int q4 = 0; q4 < 8; ++q4) {
+                const float4 mm = *reinterpret_cast<const float4*>(m_run + hc + 4 * q4);
+                const float mv[4] = {mm.x, mm.y, mm.z, mm.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int h = 4 * q4 + e;
+                    x[h] = valid ? x[h] * scale_log2e : -INFINITY;
+                    exceed |= x[h] > mv[e] + AP_LAZY;
+                }
             }
-            // both CTAs hold the same scores, so they take the same branch; past
-            // this barrier every warp has read the peer's scores
+            // both CTAs hold the same scores, so they take the same branch
             const bool raise = umma::bar_red_or(1, AP_SMT, exceed);
-            if (tid == 0) umma::mbar_arrive_remote(xfree_peer);
             if (raise) {
                 // new running max for the heads that rose too far: column maxima of the tile
 #pragma unroll
@@ -415,10 +425,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t w[4];
+                const float4 ma = *reinterpret_cast<const float4*>(m_run + hc + 8 * c);
+                const float4 mb = *reinterpret_cast<const float4*>(m_run + hc + 8 * c + 4);
+                const float mv[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int h = 8 * c + 2 * e;
-                    const float m0 = m_run[hc + h], m1 = m_run[hc + h + 1];
+                    const float m0 = mv[2 * e], m1 = mv[2 * e + 1];
                     const float p0 = (x[h] == -INFINITY || m0 == -INFINITY) ? 0.0f : umma::ex2(x[h] - m0);
                     const float p1 = (x[h + 1] == -INFINITY || m1 == -INFINITY) ? 0.0f : umma::ex2(x[h + 1] - m1);
                     const __half2 hp = __floats2half2_rn(p0, p1);
@@ -430,6 +443,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
             umma::fence_before();
             __syncwarp();
             if (lane == 0) umma::mbar_arrive(sa(&b_pfull));
+            // every warp read the peer's scores before the barrier above: let it send the next ones
+            if (tid == 0) umma::mbar_arrive_remote(xfree_peer);
         }
         // ================= epilogue: thread = output dim 32*(warp%4)+lane of each 128-dim tile, its 32 heads
         ok &= umma::mbar_wait(sa(&b_odone), (T - 1) & 1);

@@ -93,10 +93,121 @@ struct SelectSmem {
     int id[MAX_K];
     unsigned long long* key2;     // merge buffers, MAX_K each (dynamic shared memory)
     int* id2;
-    int* din;                     // HSI blocks that are in for sure, MAX_K (dynamic shared memory)
+    int* din;                     // MAX_K ints of scratch (dynamic shared memory)
+    unsigned int* bitmap;         // SEL_BITMAP_BITS bits (dynamic shared memory, k_select only)
 };
-// dynamic shared memory of k_select after the staged query: key2 | id2 | din
+// dynamic shared memory of k_select after the staged query: key2 | id2 | din | bitmap
 constexpr size_t SEL_DYN_EXTRA = (size_t)MAX_K * (8 + 4 + 4);
+constexpr int SEL_BITMAP_BITS = 1 << 19;
+constexpr size_t SEL_BITMAP_BYTES = SEL_BITMAP_BITS / 8;
+
+// the double whose order-preserving key (f64_key) is u
+__device__ __forceinline__ double f64_of_key(unsigned long long u) {
+    return __longlong_as_double((long long)((u & 0x8000000000000000ull) ? (u & 0x7fffffffffffffffull) : ~u));
+}
+
+// exclusive prefix sum of v over the block; *total gets the sum.  ws: 65 ints
+// of shared memory; every thread calls it.
+__device__ int block_exclusive_scan(int v, int* total, int* ws) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) ws[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int s0 = lane < nw ? ws[lane] : 0;
+        int inc2 = s0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, inc2, o);
+            if (lane >= o) inc2 += y;
+        }
+        if (lane < nw) ws[32 + lane] = inc2 - s0;
+        if (lane == nw - 1) ws[64] = inc2;
+    }
+    __syncthreads();
+    const int r = ws[32 + warp] + incl - v;
+    *total = ws[64];
+    __syncthreads();
+    return r;
+}
+
+// Flags (sm.id2[t] = 1) the k best of the n <= MAX_K items sm.key/sm.id[t] by
+// (key desc, id asc); key 0 marks a slot that holds no entry.  A band of float
+// images of the scores around the k-th (block_kth_band) splits the items into
+// sure (above the band), out (below) and the band, whose members are ranked
+// exactly by counting.  Returns the number flagged, min(k, entries).
+__device__ int select_best_set(int n, int k, SelectSmem& sm) {
+    int* flag = sm.id2;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) sm.rs.ctl[3] = 0;
+    __syncthreads();
+    int c = 0;
+    for (int t = threadIdx.x; t < n; t += blockDim.x) {
+        flag[t] = 0;
+        c += sm.key[t] != 0ull;
+    }
+    c = __reduce_add_sync(0xffffffffu, c);
+    if (lane == 0) atomicAdd(&sm.rs.ctl[3], c);
+    __syncthreads();
+    const int n_ent = sm.rs.ctl[3];
+    if (n_ent <= k) {
+        for (int t = threadIdx.x; t < n; t += blockDim.x) flag[t] = sm.key[t] != 0ull;
+        __syncthreads();
+        return n_ent;
+    }
+    auto fk = [&](int t, unsigned int& key) {
+        const unsigned long long u = sm.key[t];
+        if (u == 0ull) return false;
+        key = f32_key((float)f64_of_key(u));
+        return true;
+    };
+    const uint2 band = block_kth_band(fk, n, k, sm.rs);
+    if (threadIdx.x == 0) {
+        sm.rs.ctl[0] = 0;
+        sm.rs.ctl[3] = 0;
+    }
+    __syncthreads();
+    int above = 0;
+    for (int t0 = 0; t0 < n; t0 += blockDim.x) {
+        const int t = t0 + threadIdx.x;
+        bool inband = false;
+        unsigned int f;
+        if (t < n && fk(t, f)) {
+            if (f > band.y) {
+                flag[t] = 1;
+                ++above;
+            } else if (f >= band.x) {
+                inband = true;
+            }
+        }
+        const int pos = append_slot(inband, &sm.rs.ctl[0]);
+        if (inband) sm.din[pos] = t;
+    }
+    above = __reduce_add_sync(0xffffffffu, above);
+    if (lane == 0) atomicAdd(&sm.rs.ctl[3], above);
+    __syncthreads();
+    const int nb = sm.rs.ctl[0], r = k - sm.rs.ctl[3];
+    for (int i = threadIdx.x; i < nb; i += blockDim.x) {
+        const int t = sm.din[i];
+        const unsigned long long key = sm.key[t];
+        const int id = sm.id[t];
+        int rank = 0;
+        for (int j = 0; j < nb; ++j) {
+            const int tj = sm.din[j];
+            const unsigned long long kj = sm.key[tj];
+            rank += (kj > key) || (kj == key && sm.id[tj] < id);
+        }
+        flag[t] = rank < r;
+    }
+    __syncthreads();
+    return k;
+}
+
 
 // Among m candidates (cid[t], ckey[t]) keep the k best by (key desc, id asc):
 // the kept ones end up in sm.key/sm.id[0..kept), unordered.  Returns kept.
@@ -219,6 +330,58 @@ __device__ void sort_kept(int n, bool by_key, SelectSmem& sm) {
     }
 }
 
+// The distinct ids ids[t] (t < n) with flags[t] != 0 (flags == nullptr: all),
+// all in [0, id_bound), written to dst[0..cnt) in ascending order; returns cnt.
+// Through a bitmap of id_bound bits and a block prefix sum over its words when
+// that fits SEL_BITMAP_BITS, else by sort_kept.  dst must not alias ids.
+__device__ int ascending_ids(const int* ids, const int* flags, int n, int id_bound, int* dst, SelectSmem& sm) {
+    int total;
+    if (id_bound <= SEL_BITMAP_BITS) {
+        const int W = (id_bound + 31) >> 5;
+        for (int w = threadIdx.x; w < W; w += blockDim.x) sm.bitmap[w] = 0u;
+        __syncthreads();
+        for (int t = threadIdx.x; t < n; t += blockDim.x)
+            if (!flags || flags[t]) {
+                const int id = ids[t];
+                atomicOr(&sm.bitmap[id >> 5], 1u << (id & 31));
+            }
+        __syncthreads();
+        const int per = (W + blockDim.x - 1) / blockDim.x;
+        const int w0 = threadIdx.x * per, w1 = min(W, w0 + per);
+        int c = 0;
+        for (int w = w0; w < w1; ++w) c += __popc(sm.bitmap[w]);
+        int pos = block_exclusive_scan(c, &total, sm.rs.hist);
+        for (int w = w0; w < w1; ++w) {
+            unsigned int bits = sm.bitmap[w];
+            while (bits) {
+                dst[pos++] = (w << 5) + __ffs(bits) - 1;
+                bits &= bits - 1u;
+            }
+        }
+        __syncthreads();
+        return total;
+    }
+    if (threadIdx.x == 0) sm.rs.ctl[0] = 0;
+    __syncthreads();
+    for (int t0 = 0; t0 < n; t0 += blockDim.x) {
+        const int t = t0 + threadIdx.x;
+        const bool f = t < n && (!flags || flags[t]);
+        const int pos = append_slot(f, &sm.rs.ctl[0]);
+        if (f) dst[pos] = ids[t];
+    }
+    __syncthreads();
+    total = sm.rs.ctl[0];
+    for (int t = threadIdx.x; t < total; t += blockDim.x) {
+        sm.id[t] = dst[t];
+        sm.key[t] = 0ull;
+    }
+    __syncthreads();
+    sort_kept(total, false, sm);
+    for (int t = threadIdx.x; t < total; t += blockDim.x) dst[t] = sm.id[t];
+    __syncthreads();
+    return total;
+}
+
 // The k best of m candidates (cid[t], ckey[t]) by (key desc, id asc), sorted,
 // in sm.key/sm.id[0..kept).  When every candidate fits in shared memory (the
 // usual case: k plus the few entries whose bounds straddle the threshold) one
@@ -270,6 +433,63 @@ __global__ void __launch_bounds__(512) k_pool_bounds(const int32_t* __restrict__
     lu[gq * pool_len + t] = make_float2(lo, hi);
 }
 
+// Reindex over a pool that fits one block's sort (pool_len <= MAX_K): every
+// slot's exact score, one thread per slot, blockIdx.z taking 512 slots; an
+// empty slot gets key 0, below every real score's key.
+template <int DI>
+__global__ void __launch_bounds__(512) k_pool_exact(const int32_t* __restrict__ pool, int pool_len,
+                                                    const uint8_t* __restrict__ kc_all,
+                                                    const uint8_t* __restrict__ ks_all, int capacity,
+                                                    const uint8_t* __restrict__ iq_codes,
+                                                    const uint8_t* __restrict__ iq_scales,
+                                                    const float* __restrict__ w_head, int n_q, int H,
+                                                    unsigned long long* __restrict__ keys) {
+    extern __shared__ int qsm[];
+    const int ql = blockIdx.x, b = blockIdx.y;
+    const int64_t gq = (int64_t)b * n_q + ql;
+    QView<DI> v;
+    v.bind(qsm, H);
+    stage_query<DI>(v, iq_codes + gq * H * (DI / 2), iq_scales + gq * H * (DI / 16), w_head + gq * H, H, threadIdx.x,
+                    blockDim.x);
+    __syncthreads();
+    const int t = blockIdx.z * blockDim.x + threadIdx.x;
+    if (t >= pool_len) return;
+    const int j = pool[gq * pool_len + t];
+    unsigned long long key = 0ull;
+    if (j >= 0 && j < capacity) {
+        const int64_t row = (int64_t)b * capacity + j;
+        key = f64_key(exact_score<DI>(kc_all + row * (DI / 2), ks_all + row * (DI / 16), v, H));
+    }
+    keys[gq * pool_len + t] = key;
+}
+
+// Reindex, second pass for such a pool: one block per query keeps the k best
+// slots by (exact score desc, entry asc) and writes their entries in ascending
+// order, -1 where fewer than k slots hold an entry.
+__global__ void __launch_bounds__(512) k_pool_rank(const int32_t* __restrict__ pool, int pool_len,
+                                                   const unsigned long long* __restrict__ keys, int capacity, int k,
+                                                   int32_t* __restrict__ idx_out) {
+    extern __shared__ unsigned long long sdyn[];
+    __shared__ SelectSmem sm;
+    const int64_t gq = (int64_t)blockIdx.y * gridDim.x + blockIdx.x;
+    sm.key2 = sdyn;
+    sm.id2 = reinterpret_cast<int*>(sdyn + MAX_K);
+    sm.din = sm.id2 + MAX_K;
+    sm.bitmap = reinterpret_cast<unsigned int*>(sm.din + MAX_K);
+    sm.rs.whist = sm.whist;
+    for (int t = threadIdx.x; t < pool_len; t += blockDim.x) {
+        const int j = pool[gq * pool_len + t];
+        const bool ok = j >= 0 && j < capacity;
+        sm.key[t] = ok ? keys[gq * pool_len + t] : 0ull;
+        sm.id[t] = ok ? j : 0;
+    }
+    __syncthreads();
+    select_best_set(pool_len, k, sm);
+    const int kept = ascending_ids(sm.id, sm.id2, pool_len, capacity, sm.din, sm);
+    int32_t* out = idx_out + gq * k;
+    for (int t = threadIdx.x; t < k; t += blockDim.x) out[t] = t < kept ? sm.din[t] : -1;
+}
+
 // One block per (sequence, query).  Items t in [0, n): entry ids[t] (-1 =
 // empty) with bounds lu[t]; n is *count (Full: the forwarded candidates) or
 // n_fixed (Reindex: the pool slots, bounds from k_pool_bounds).  Keeps the
@@ -300,6 +520,7 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
     sm.key2 = reinterpret_cast<unsigned long long*>(extra);
     sm.id2 = reinterpret_cast<int*>(extra + (size_t)MAX_K * 8);
     sm.din = sm.id2 + MAX_K;
+    sm.bitmap = reinterpret_cast<unsigned int*>(extra + SEL_DYN_EXTRA);
     const float2* L = lu + slab * list_len;
     const int n = counts ? counts[2 * slab] : n_fixed;
     int* cid = c2id + slab * list_len;
@@ -354,9 +575,10 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
     __syncthreads();
     const int m = sm.rs.ctl[0];
     __syncthreads();
-    // ---- 2. exact scores of the candidates, 3. the k best in rank order
-    // (in shared memory when they fit, the usual case: k plus the few entries
-    // whose bounds straddle the threshold)
+    // ---- 2. exact scores of the candidates, 3. the k best, written in
+    // ascending entry order (in shared memory when they fit, the usual case:
+    // k plus the few entries whose bounds straddle the threshold)
+    const int id_bound = counts ? n_elig_of(q_pos[gq], capacity) : capacity;
     int kept;
     if (m <= MAX_K) {
         for (int t = threadIdx.x; t < m; t += blockDim.x) {
@@ -364,8 +586,8 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
             sm.key[t] = f64_key(exact_score<DI>(kc + (int64_t)j * (DI / 2), ks + (int64_t)j * (DI / 16), v, H));
         }
         __syncthreads();
-        sort_kept(m, true, sm);
-        kept = m < k ? m : k;
+        select_best_set(m, k, sm);
+        kept = ascending_ids(sm.id, sm.id2, m, id_bound, sm.din, sm);
     } else {
         for (int t = threadIdx.x; t < m; t += blockDim.x) {
             const int j = cid[t];
@@ -373,9 +595,10 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
         }
         __syncthreads();
         kept = best_sorted(cid, ckey, m, k, sm);
+        kept = ascending_ids(sm.id, nullptr, kept, id_bound, sm.din, sm);
     }
     int32_t* out = idx_out + gq * k;
-    for (int t = threadIdx.x; t < k; t += blockDim.x) out[t] = t < kept ? sm.id[t] : -1;
+    for (int t = threadIdx.x; t < k; t += blockDim.x) out[t] = t < kept ? sm.din[t] : -1;
     __syncthreads();
 
     // ---- 4. HSI candidate pool (Full only)
@@ -484,10 +707,10 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
         nsel = pool_blocks;
         __syncthreads();
     }
-    sort_kept(nsel, false, sm);
+    ascending_ids(sm.id, nullptr, nsel, nb, sm.din, sm);
     for (int u = threadIdx.x; u < P; u += blockDim.x) {
         const int t = u / bs;
-        const int j = t < nsel ? sm.id[t] * bs + u % bs : -1;
+        const int j = t < nsel ? sm.din[t] * bs + u % bs : -1;
         // only the newest block can run past n_elig; it has the largest id and sorts last
         pout[u] = (j >= 0 && j < n_elig) ? j : -1;
     }
@@ -588,7 +811,7 @@ cudaError_t launch_indexer_full_t(const csa2_cache& c, const uint8_t* iq_codes, 
         }
         if (e != cudaSuccess) return e;
         dim3 g2(n_qc, c.batch);
-        const size_t smem2 = qwords + SEL_DYN_EXTRA;
+        const size_t smem2 = qwords + SEL_DYN_EXTRA + SEL_BITMAP_BYTES;
         e = cudaFuncSetAttribute(k_select<DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
         if (e != cudaSuccess) return e;
         k_select<DI><<<g2, 512, smem2, st>>>(w.ids, w.lu, w.counts, 0, (int)list_len, c.ikey_codes, c.ikey_scales,
@@ -608,12 +831,26 @@ cudaError_t launch_reindex_t(const csa2_cache& c, const uint8_t* iq_codes, const
     const SelectWs w = carve(ws, (int64_t)c.batch * n_q, pool_len);
     const size_t qwords = (size_t)QView<DI>::words(H) * sizeof(int);
     dim3 g0(n_q, c.batch, (pool_len + 511) / 512);
+    if (pool_len <= MAX_K) {
+        // small pool: exact scores for every slot, then one sort per query
+        k_pool_exact<DI><<<g0, 512, qwords, st>>>(pool, pool_len, c.ikey_codes, c.ikey_scales, c.capacity, iq_codes,
+                                                   iq_scales, w_head, n_q, H, w.c2key);
+        note_launch();
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        const size_t smr = SEL_DYN_EXTRA + SEL_BITMAP_BYTES;
+        e = cudaFuncSetAttribute(k_pool_rank, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smr);
+        if (e != cudaSuccess) return e;
+        k_pool_rank<<<dim3(n_q, c.batch), 512, smr, st>>>(pool, pool_len, w.c2key, c.capacity, k, idx_out);
+        note_launch();
+        return cudaGetLastError();
+    }
     k_pool_bounds<DI><<<g0, 512, qwords, st>>>(pool, pool_len, c.ikey_codes, c.ikey_scales, c.capacity, iq_codes,
                                                 iq_scales, w_head, n_q, H, w.lu);
     note_launch();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const size_t smem = qwords + SEL_DYN_EXTRA;
+    const size_t smem = qwords + SEL_DYN_EXTRA + SEL_BITMAP_BYTES;
     e = cudaFuncSetAttribute(k_select<DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 g(n_q, c.batch);

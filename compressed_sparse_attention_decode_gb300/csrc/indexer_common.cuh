@@ -309,30 +309,40 @@ __device__ KeyT block_kth_largest(Get getkey, int n, int k, RadixSmem& rs, int* 
     return prefix;
 }
 
-// A bound on the k-th largest of the 32-bit keys (1 <= k <= number taking
-// part): a key <= it (upper == false) or >= it (upper == true).  The keys'
-// range is cut into 256 buckets of equal width (the bucket index never
-// decreases as the key grows, so every key of a higher bucket is larger); the
-// bucket holding the k-th largest is found from the top; while it still holds
-// more than 64 keys its own range is cut again (at most four levels).  The
-// bound is the smallest (largest) key of the last bucket.  Used where the
-// caller only filters with the value: equal-width buckets spread the
-// shared-memory atomics even when the keys share their leading bits, and the
-// refinement keeps the bound within a few dozen keys of the exact one.
+// the float whose order-preserving key (f32_key) is k
+__device__ __forceinline__ float key_value(unsigned int k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// A band [lo, hi] of keys that holds the k-th largest of the keys
+// (order-preserving images of finite floats, 1 <= k <= number of finite ones
+// taking part): every key above hi is among the k largest, every key below lo
+// is not.  The value range of the keys is
+// cut into 256 buckets of equal width in value (the bucket index never
+// decreases as the value grows, so every key of a higher bucket is larger);
+// the bucket holding the k-th largest is found from the top; while it still
+// holds more than 64 keys its own range is cut again (at most four levels).
+// The band is the smallest and largest key of the last bucket.  Non-finite keys
+// (an empty slot's -inf) stay below every bucket.  Used where the caller only
+// filters with it: even buckets spread the shared-memory atomics, and the
+// refinement keeps the band to a few dozen keys.
 template <typename Get>
-__device__ unsigned int block_kth_bound(Get getkey, int n, int k, bool upper, RadixSmem& rs) {
+__device__ uint2 block_kth_band(Get getkey, int n, int k, RadixSmem& rs) {
     const int lane = threadIdx.x & 31, nw = blockDim.x >> 5;
     int* wh = rs.whist + (threadIdx.x >> 5) * 256;
-    // min / max of the keys in [lo, hi] whose bucket is bsel (bsel < 0: all of them), into rs.kmin / rs.kmax
-    auto range_pass = [&](unsigned int lo, unsigned int hi, float scale, int bsel) {
+    auto bucket_of = [](unsigned int key, float vlo, float scale) {
+        return min((int)((key_value(key) - vlo) * scale), 255);
+    };
+    // min / max of the finite keys in [lo, hi] whose bucket is bsel (bsel < 0: all of them)
+    auto range_pass = [&](unsigned int lo, unsigned int hi, float vlo, float scale, int bsel) {
         unsigned int mn = ~0u, mx = 0u;
         for (int t0 = threadIdx.x; t0 < n; t0 += 8 * blockDim.x) {
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int t = t0 + u * blockDim.x;
                 unsigned int key;
-                if (t < n && getkey(t, key) && key >= lo && key <= hi &&
-                    (bsel < 0 || min((int)((float)(key - lo) * scale), 255) == bsel)) {
+                if (t < n && getkey(t, key) && key >= lo && key <= hi && isfinite(key_value(key)) &&
+                    (bsel < 0 || bucket_of(key, vlo, scale) == bsel)) {
                     mn = min(mn, key);
                     mx = max(mx, key);
                 }
@@ -350,14 +360,16 @@ __device__ unsigned int block_kth_bound(Get getkey, int n, int k, bool upper, Ra
         rs.kmax = 0ull;
     }
     __syncthreads();
-    range_pass(0u, ~0u, 0.0f, -1);
+    range_pass(0u, ~0u, 0.0f, 0.0f, -1);
     __syncthreads();
     unsigned int lo = (unsigned int)rs.kmin, hi = (unsigned int)rs.kmax;
     int need = k;
     for (int level = 0; level < 4 && lo < hi; ++level) {
         for (int i = threadIdx.x; i < nw * 256; i += blockDim.x) rs.whist[i] = 0;
         __syncthreads();
-        const float scale = 256.0f / ((float)(hi - lo) + 1.0f);
+        const float vlo = key_value(lo);
+        float scale = 256.0f / (key_value(hi) - vlo);
+        if (!(scale > 0.0f && scale < INFINITY)) scale = 0.0f;       // degenerate range: one bucket
         for (int t0 = threadIdx.x; t0 < n; t0 += 8 * blockDim.x) {
             unsigned int kk[8];
             bool in[8];
@@ -368,7 +380,7 @@ __device__ unsigned int block_kth_bound(Get getkey, int n, int k, bool upper, Ra
             }
 #pragma unroll
             for (int u = 0; u < 8; ++u)
-                if (in[u] && kk[u] >= lo && kk[u] <= hi) atomicAdd(&wh[min((int)((float)(kk[u] - lo) * scale), 255)], 1);
+                if (in[u] && kk[u] >= lo && kk[u] <= hi) atomicAdd(&wh[bucket_of(kk[u], vlo, scale)], 1);
         }
         __syncthreads();
         for (int i = threadIdx.x; i < 256; i += blockDim.x) {
@@ -411,14 +423,21 @@ __device__ unsigned int block_kth_bound(Get getkey, int n, int k, bool upper, Ra
         __syncthreads();
         const int bstar = rs.ctl[1], cnt = rs.ctl[3];
         need = rs.ctl[2];
-        range_pass(lo, hi, scale, bstar);
+        range_pass(lo, hi, vlo, scale, bstar);
         __syncthreads();
         lo = (unsigned int)rs.kmin;
         hi = (unsigned int)rs.kmax;
-        if (cnt <= 64) break;
+        if (cnt <= 64 || scale == 0.0f) break;
     }
     __syncthreads();
-    return upper ? hi : lo;
+    return make_uint2(lo, hi);
+}
+
+// the band's lower end (a key <= the k-th largest) or upper end (>= it)
+template <typename Get>
+__device__ unsigned int block_kth_bound(Get getkey, int n, int k, bool upper, RadixSmem& rs) {
+    const uint2 band = block_kth_band(getkey, n, k, rs);
+    return upper ? band.y : band.x;
 }
 
 // warp-aggregated append to a list whose counter lives at *ctr (shared or global)

@@ -133,7 +133,8 @@ csa2_status csa2_indexer_topk(const csa2_cache* cache, const uint8_t* iq_codes, 
  * Reindex / Reuse ("DeepSeek-v4.1 Flash" §2.3.2 and §2.3.4).
  *   mode CSA2_REINDEX: score only the pool entries with this layer's indexer
  *     queries and keep the top k inside the pool (ascending entry order, -1 padded);
- *     pool int32 [batch][n_q][pool_len] (-1 slots ignored), pool_len <= 16384.
+ *     pool int32 [batch][n_q][pool_len] (-1 slots ignored, entries distinct as
+ *     in an HSI pool), pool_len <= 16384.
  *   mode CSA2_REUSE: idx_out = prev_idx, bit for bit (a device copy); the
  *     indexer arguments and the pool may be NULL.
  *   prev_idx, idx_out int32 [batch][n_q][k].
