@@ -2,51 +2,54 @@
 // query ("DeepSeek-v4.1 Flash: KVキャッシュ圧縮の限界を押し広げる", §2.3.1 top-k
 // entries plus the local window; §1.1 one 512-dim latent shared by every head).
 //
-// CTA r of the pair owns latent dims [256r, 256r+256).  Per 128-key tile:
-//   S_r = L[:, dims_r] . Q[:, dims_r]^T   (tcgen05, M = 128 keys, N = 64 heads,
-//                                          K = 256, fp32 in TMEM)
-//   each CTA sends its partial scores to the other with asynchronous remote
-//   stores counted on the receiver's mbarrier, and adds the other's
-//   (S = S_0 + S_1, the same bits in both CTAs); an online softmax with a lazy
-//   running max (a max reduction runs only when some score rises more than 2^8
-//   above the running max) writes P (fp16), and both CTAs accumulate their own
-//   output dims: O_r^T += L[:, dims_r]^T . P, l += 1^T . P (TMEM, across all
-//   tiles).  One thread per CTA waits on the barriers the peer fills (cluster
-//   scope) and passes them on through a named barrier of the softmax warps.
-// The query's top-k indices are staged in shared memory at the start and every
-// row the CTA will read is prefetched into L2, so the tile gathers that follow
-// (double-buffered, overlapping the MMAs and softmax) are single L2 round trips.
+// The pair splits the keys: CTA r takes the 64-key tiles r, r+2, .. of the
+// selected FP4 entries and window rows [64r, 64r+64), with all 512 latent
+// dims.  Per tile:
+//   S^T = Q . L^T        (tcgen05, M = 64 heads, N = 64 keys, K = 512, fp32 in
+//                         TMEM: head h in lane 32(h/16) + h%16)
+//   an online softmax in which each thread owns one head and 32 of the tile's
+//   keys (two threads per head): the running max is checked per thread and
+//   raised only when a score rises more than 2^8 above it (then O is rescaled
+//   in TMEM); P^T goes to shared memory in fp16 and its row sums stay in
+//   registers;
+//   O^T += L^T . P       (M = 128 dims x 4, N = 64 heads, K = 64 keys)
+// Tiles are double-buffered (L, S, P), so the gather and dequantisation of the
+// next tile overlap the MMAs and softmax of this one.  At the end the two CTAs
+// swap their per-head running max and row sum through distributed shared
+// memory, scale their partial O to the common max, and each writes half of
+// the output dims after adding the other CTA's share, passed through a
+// workspace in global memory (L2).
 //
-// Warps: 0-7 softmax / epilogue (warp w reads TMEM lanes 32(w%4).. = key rows,
-// later output dims, for heads 32(w/4)..+31), warp 8 issues the MMAs, warps
-// 9-15 gather rows.  Tiles 0.. hold the selected FP4 entries, the last tile the
-// window rows (bf16).
+// Warps: 0-7 softmax / epilogue (warp w: TMEM lane quarter w%4, key half
+// w/4), warp 8 issues the MMAs, warps 9-15 gather rows.  The query's indices
+// are staged in shared memory and every row the CTA reads is prefetched into
+// L2 first, so the tile gathers are single L2 round trips.
 #include "common.cuh"
 #include "umma.cuh"
 
 namespace csa2 {
 
-constexpr int AP_TILE = 128;
+constexpr int AP_TILE = 64;                          // keys per tile
 constexpr int AP_H = 64;
 constexpr int AP_THREADS = 512;
-constexpr int AP_SMW = 8;                            // softmax warps 0-7: lane quadrant x head half
+constexpr int AP_SMW = 8;                            // softmax warps 0-7
 constexpr int AP_SMT = AP_SMW * 32;
 constexpr int AP_MMAW = 8;                           // warp 8 issues the MMAs
 constexpr int AP_LOADERS = 224;                      // warps 9-15
-constexpr uint32_t AP_SLAB = AP_TILE * 128;          // 64 dims x 128 keys x fp16
-constexpr uint32_t AP_SQ = 0;                        // Q half: 4 slabs x 64 heads x 128 B = 32 KB
-constexpr uint32_t AP_SL = 32 * 1024;                // 2 buffers x 4 slabs (128 KB)
-constexpr uint32_t AP_LBUF = 4 * AP_SLAB;
-constexpr uint32_t AP_SP = AP_SL + 2 * AP_LBUF;      // P: 128 keys x 64 heads fp16 (16 KB)
-constexpr uint32_t AP_SONES = AP_SP + 16 * 1024;     // ones, 128 x 16 fp16 (4 KB)
-constexpr uint32_t AP_SX = AP_SONES + 4 * 1024;      // the peer's partial scores, 128 x 64 f32 (32 KB)
-constexpr uint32_t AP_SIDX = AP_SX + 32 * 1024;      // the query's indices, MAX_K ints
-constexpr uint32_t AP_RED = AP_SIDX + MAX_K * 4;     // column maxima / row sums, 4 quadrants x 64
-constexpr uint32_t AP_MISC = AP_RED + 1024;          // m_run[64], fac[64], flags
-constexpr uint32_t AP_DYN = AP_MISC + 1024 + 1024;
-constexpr uint32_t AP_XBYTES = AP_TILE * AP_H * 4;   // partial scores one CTA sends per tile
-constexpr uint32_t APT_S = 0, APT_O = 128, APT_L = 256, APT_COLS = 512;
+constexpr uint32_t AP_QSLAB = AP_H * 128;            // 64 heads x 64 dims fp16
+constexpr uint32_t AP_LSLAB = AP_TILE * 128;         // 64 keys x 64 dims fp16
+constexpr uint32_t AP_SQ = 0;                        // Q: 8 slabs (64 KB)
+constexpr uint32_t AP_SL = 8 * AP_QSLAB;             // L: 2 buffers x 8 slabs (128 KB)
+constexpr uint32_t AP_LBUF = 8 * AP_LSLAB;
+constexpr uint32_t AP_SP = AP_SL + 2 * AP_LBUF;      // P^T: 2 buffers x 64 heads x 64 keys fp16
+constexpr uint32_t AP_PBUF = AP_H * 128;
+constexpr uint32_t AP_SIDX = AP_SP + 2 * AP_PBUF;    // the query's indices, MAX_K ints
+constexpr uint32_t AP_RED = AP_SIDX + MAX_K * 4;     // per key half x 64 heads (max, then row sums)
+constexpr uint32_t AP_MISC = AP_RED + 1024;          // m_run[64], fac[64], flags[8], own m/l, peer m/l, scale
+constexpr uint32_t AP_DYN = AP_MISC + 3072 + 1024;
+constexpr uint32_t APT_S = 0, APT_O = 128, APT_COLS = 512;
 constexpr float AP_LAZY = 8.0f;                      // log2 headroom before the running max is raised
+constexpr size_t AP_SCRATCH = (size_t)2 * AP_H * 256 * sizeof(float);   // per query: each CTA's share for the other
 
 __device__ __forceinline__ uint32_t apswz(uint32_t row, uint32_t chunk) { return row * 128 + ((chunk ^ (row & 7)) << 4); }
 
@@ -71,24 +74,20 @@ __device__ __forceinline__ uint32_t ap_hmul2(uint32_t a, __half2 s) {
     __half2 x = __hmul2(*reinterpret_cast<__half2*>(&a), s);
     return *reinterpret_cast<uint32_t*>(&x);
 }
-__device__ __forceinline__ uint32_t ap_ord(float f) {
-    uint32_t u = __float_as_uint(f);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float ap_unord(uint32_t k) {
-    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_sparse_attn_pair(
     const uint8_t* __restrict__ lat_codes, const uint8_t* __restrict__ lat_scales, int capacity,
     const uint16_t* __restrict__ q, int n_q, int q0, const int64_t* __restrict__ q_pos,
     const int32_t* __restrict__ idx, int k, const uint16_t* __restrict__ swa, int64_t swa_pos0, int swa_len,
-    float scale_log2e, float* __restrict__ out, float* __restrict__ lse, int* __restrict__ err) {
+    float scale_log2e, float* __restrict__ out, float* __restrict__ lse, int* __restrict__ err,
+    float* __restrict__ scratch) {
     extern __shared__ uint8_t dyn[];
-    __shared__ __align__(8) unsigned long long b_lfull[2], b_lfree[2], b_sfull[2], b_sfree[2], b_pfull, b_odone, b_xfull,
-        b_xfree;
+    __shared__ __align__(8) unsigned long long b_lfull[2], b_lfree[2], b_sfull[2], b_sfree[2], b_pfull[2], b_odone[2];
     __shared__ uint32_t tmem_base;
-    __shared__ int rowok[2][AP_TILE];
+    __shared__ __align__(16) int rowok[2][AP_TILE];
 
     const uint32_t raw = umma::smem_u32(dyn);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -96,11 +95,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = umma::cluster_rank();
     const uint32_t peer = rank ^ 1u;
-    const int d0 = (int)rank * 256;
     const int qi = q0 + blockIdx.y, b = blockIdx.z;
     const int64_t gq = (int64_t)b * n_q + qi;
 
-    // window of this query (clipped to the rows present) and tile count
+    // window of this query (clipped to the rows present); this CTA's tiles:
+    // FP4 tiles rank, rank+2, .. of the T4 tiles of k entries, then its half of the window
     const int64_t p = q_pos[gq];
     int64_t wlo = p - (WINDOW - 1);
     if (wlo < 0) wlo = 0;
@@ -108,7 +107,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
     int64_t whi = p;
     if (whi > swa_pos0 + swa_len - 1) whi = swa_pos0 + swa_len - 1;
     const int nwin = whi >= wlo ? (int)(whi - wlo + 1) : 0;
-    const int T = 1 + (k + AP_TILE - 1) / AP_TILE;
+    const int T4 = (k + AP_TILE - 1) / AP_TILE;
+    const int n4 = (T4 + 1 - (int)rank) / 2;
+    const int T = n4 + 1;
+
+    float* m_run = reinterpret_cast<float*>(sm + AP_MISC);          // [64]
+    float* fac = m_run + AP_H;                                       // [64]
+    int* flag = reinterpret_cast<int*>(fac + AP_H);                  // [8]
+    float* own_ml = reinterpret_cast<float*>(flag + 8);              // m[64], l[64]
+    float* peer_ml = own_ml + 2 * AP_H;                              // written by the peer
+    float* fown = peer_ml + 2 * AP_H;                                // this CTA's final scale per head
+    float* red = reinterpret_cast<float*>(sm + AP_RED);              // [2 halves][64 heads]
 
     auto sa = [&](const void* x) { return umma::smem_u32(x); };
     if (tid == 0) {
@@ -117,41 +126,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
             umma::mbar_init(sa(&b_lfree[i]), 1);
             umma::mbar_init(sa(&b_sfull[i]), 1);
             umma::mbar_init(sa(&b_sfree[i]), AP_SMW);
+            umma::mbar_init(sa(&b_pfull[i]), AP_SMW);
+            umma::mbar_init(sa(&b_odone[i]), 1);
         }
-        umma::mbar_init(sa(&b_pfull), AP_SMW);
-        umma::mbar_init(sa(&b_odone), 1);
-        umma::mbar_init(sa(&b_xfull), 1);          // armed by this CTA, filled by the peer's stores
-        umma::mbar_init(sa(&b_xfree), 1);          // the peer's thread 0, once it has read the scores
         umma::fence_mbar_init();
-        umma::mbar_arrive_expect_tx(sa(&b_xfull), AP_XBYTES);
     }
     if (warp == 0) umma::tmem_alloc(sa(&tmem_base), APT_COLS);
-    // ---- Q half: 64 heads x 256 dims, bf16 -> fp16, one round of loads
+    // ---- Q: 64 heads x 512 dims, bf16 -> fp16, K-major slabs of 64 dims (A operand)
     {
-        uint4 qv[4];
+        uint4 qv[8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int i = tid + u * AP_THREADS, h = i >> 5, c = i & 31;
-            qv[u] = __ldg(reinterpret_cast<const uint4*>(q + ((gq * AP_H + h) * D_LAT + d0 + c * 8)));
+        for (int u = 0; u < 8; ++u) {
+            const int i = tid + u * AP_THREADS, h = i >> 6, c = i & 63;
+            qv[u] = __ldg(reinterpret_cast<const uint4*>(q + ((gq * AP_H + h) * D_LAT + c * 8)));
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int i = tid + u * AP_THREADS, h = i >> 5, c = i & 31;
+        for (int u = 0; u < 8; ++u) {
+            const int i = tid + u * AP_THREADS, h = i >> 6, c = i & 63;
             const uint4 v = qv[u];
-            *reinterpret_cast<uint4*>(sm + AP_SQ + (c >> 3) * (AP_H * 128) + apswz(h, c & 7)) =
+            *reinterpret_cast<uint4*>(sm + AP_SQ + (c >> 3) * AP_QSLAB + apswz(h, c & 7)) =
                 make_uint4(ap_bf16x2_to_f16x2(v.x), ap_bf16x2_to_f16x2(v.y), ap_bf16x2_to_f16x2(v.z),
                            ap_bf16x2_to_f16x2(v.w));
         }
     }
-    if (tid < 256) reinterpret_cast<uint4*>(sm + AP_SONES)[tid] = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
-    float* m_run = reinterpret_cast<float*>(sm + AP_MISC);
-    float* fac = m_run + AP_H;
-    int* flag = reinterpret_cast<int*>(fac + AP_H);
     if (tid < AP_H) m_run[tid] = -INFINITY;
     umma::fence_proxy_async();
     umma::fence_before();
     __syncthreads();
-    umma::cluster_sync();              // both CTAs' barriers exist before any remote store or arrive
+    umma::cluster_sync();              // both CTAs have started (their shared memory exists)
     umma::fence_after();
     const uint32_t tmem = tmem_base;
     bool ok = true;
@@ -160,62 +162,69 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
         // ================= loaders
         const int lt = tid - (AP_MMAW + 1) * 32;
         int* sidx = reinterpret_cast<int*>(sm + AP_SIDX);
-        const uint8_t* codes_b = lat_codes + (int64_t)b * capacity * (D_LAT / 2) + d0 / 2;
-        const uint8_t* scales_b = lat_scales + (int64_t)b * capacity * (D_LAT / 16) + d0 / 16;
-        const uint16_t* win_b = swa + ((int64_t)b * swa_len + (wlo - swa_pos0)) * D_LAT + d0;
+        const uint8_t* codes_b = lat_codes + (int64_t)b * capacity * (D_LAT / 2);
+        const uint8_t* scales_b = lat_scales + (int64_t)b * capacity * (D_LAT / 16);
+        const uint16_t* win_b = swa + ((int64_t)b * swa_len + (wlo - swa_pos0)) * D_LAT;
         for (int s = lt; s < k; s += AP_LOADERS) {
             const int j = idx[gq * k + s];
             sidx[s] = (j >= 0 && j < capacity) ? j : -1;
         }
         umma::bar_named(2, AP_LOADERS);
         // every row this CTA reads, into L2 now: the gathers below then hit L2
-        for (int s = lt; s < k; s += AP_LOADERS) {
-            const int j = sidx[s];
+        for (int u = lt; u < n4 * AP_TILE; u += AP_LOADERS) {
+            const int s = (2 * (u / AP_TILE) + (int)rank) * AP_TILE + u % AP_TILE;
+            const int j = s < k ? sidx[s] : -1;
             if (j >= 0) {
                 umma::prefetch_l2(codes_b + (int64_t)j * (D_LAT / 2));
+                umma::prefetch_l2(codes_b + (int64_t)j * (D_LAT / 2) + 128);
                 umma::prefetch_l2(scales_b + (int64_t)j * (D_LAT / 16));
             }
         }
-        for (int u = lt; u < nwin * 4; u += AP_LOADERS) umma::prefetch_l2(win_b + (int64_t)(u >> 2) * D_LAT + (u & 3) * 64);
+        for (int u = lt; u < AP_TILE * 8; u += AP_LOADERS) {
+            const int r = (int)rank * AP_TILE + (u >> 3);
+            if (r < nwin) umma::prefetch_l2(win_b + (int64_t)r * D_LAT + (u & 7) * 64);
+        }
         for (int t = 0; t < T; ++t) {
             const int buf = t & 1;
             if (t >= 2) ok &= umma::mbar_wait(sa(&b_lfree[buf]), ((t >> 1) - 1) & 1);
             uint8_t* L = sm + AP_SL + buf * AP_LBUF;
             if (t == T - 1) {
-                // window rows: 128 rows x 32 chunks of 8 dims (bf16 -> fp16), 8 loads in flight per thread
-                for (int u0 = lt; u0 < AP_TILE * 32; u0 += AP_LOADERS * 8) {
+                // window rows 64*rank .. +63: 64 rows x 64 chunks of 8 dims (bf16 -> fp16), 8 loads in flight
+                for (int u0 = lt; u0 < AP_TILE * 64; u0 += AP_LOADERS * 8) {
                     uint4 wv[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        const int u = u0 + i * AP_LOADERS, r = u >> 5, c = u & 31;
+                        const int u = u0 + i * AP_LOADERS, r = u >> 6, c = u & 63;
+                        const int wr = (int)rank * AP_TILE + r;
                         wv[i] = make_uint4(0, 0, 0, 0);
-                        if (u < AP_TILE * 32 && r < nwin)
-                            wv[i] = __ldg(reinterpret_cast<const uint4*>(win_b + (int64_t)r * D_LAT + c * 8));
+                        if (u < AP_TILE * 64 && wr < nwin)
+                            wv[i] = __ldg(reinterpret_cast<const uint4*>(win_b + (int64_t)wr * D_LAT + c * 8));
                     }
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        const int u = u0 + i * AP_LOADERS, r = u >> 5, c = u & 31;
-                        if (u < AP_TILE * 32) {
+                        const int u = u0 + i * AP_LOADERS, r = u >> 6, c = u & 63;
+                        if (u < AP_TILE * 64) {
                             const uint4 v = wv[i];
-                            *reinterpret_cast<uint4*>(L + (c >> 3) * AP_SLAB + apswz(r, c & 7)) =
+                            *reinterpret_cast<uint4*>(L + (c >> 3) * AP_LSLAB + apswz(r, c & 7)) =
                                 make_uint4(ap_bf16x2_to_f16x2(v.x), ap_bf16x2_to_f16x2(v.y),
                                            ap_bf16x2_to_f16x2(v.z), ap_bf16x2_to_f16x2(v.w));
-                            if (c == 0) rowok[buf][r] = r < nwin;
+                            if (c == 0) rowok[buf][r] = (int)rank * AP_TILE + r < nwin;
                         }
                     }
                 }
             } else {
-                // selected FP4 rows: 128 rows x 8 units of 32 dims (16 B of codes + 2 scale bytes)
-                constexpr int NU = (AP_TILE * 8 + AP_LOADERS - 1) / AP_LOADERS;
+                // selected FP4 rows: 64 rows x 16 units of 32 dims (16 B of codes + 2 scale bytes)
+                constexpr int NU = (AP_TILE * 16 + AP_LOADERS - 1) / AP_LOADERS;
+                const int slot0 = (2 * t + (int)rank) * AP_TILE;
                 uint4 cw[NU];
                 uint32_t sc[NU];
 #pragma unroll
                 for (int i = 0; i < NU; ++i) {
-                    const int u = lt + i * AP_LOADERS, r = u >> 3, c = u & 7;
-                    const int slot = t * AP_TILE + r;
+                    const int u = lt + i * AP_LOADERS, r = u >> 4, c = u & 15;
+                    const int slot = slot0 + r;
                     cw[i] = make_uint4(0, 0, 0, 0);
                     sc[i] = 0u;
-                    if (u < AP_TILE * 8 && slot < k) {
+                    if (u < AP_TILE * 16 && slot < k) {
                         const int j = sidx[slot];
                         if (j >= 0) {
                             cw[i] = __ldg(reinterpret_cast<const uint4*>(codes_b + (int64_t)j * (D_LAT / 2)) + c);
@@ -225,9 +234,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                 }
 #pragma unroll
                 for (int i = 0; i < NU; ++i) {
-                    const int u = lt + i * AP_LOADERS, r = u >> 3, c = u & 7;
-                    if (u < AP_TILE * 8) {
-                        const int slot = t * AP_TILE + r;
+                    const int u = lt + i * AP_LOADERS, r = u >> 4, c = u & 15;
+                    if (u < AP_TILE * 16) {
+                        const int slot = slot0 + r;
                         const bool valid = slot < k && sidx[slot] >= 0;
                         const uint32_t words[4] = {cw[i].x, cw[i].y, cw[i].z, cw[i].w};
                         // an empty slot has zero codes and zero scales, so it expands to zeros
@@ -240,8 +249,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                             ap_e2m1x8(words[w], f);
                             const uint4 o = make_uint4(ap_hmul2(f[0], s2), ap_hmul2(f[1], s2), ap_hmul2(f[2], s2),
                                                        ap_hmul2(f[3], s2));
-                            const int cc = c * 4 + w;                // 8-dim chunk 0..31
-                            *reinterpret_cast<uint4*>(L + (cc >> 3) * AP_SLAB + apswz(r, cc & 7)) = o;
+                            const int cc = c * 4 + w;                // 8-dim chunk 0..63
+                            *reinterpret_cast<uint4*>(L + (cc >> 3) * AP_LSLAB + apswz(r, cc & 7)) = o;
                         }
                         if (c == 0) rowok[buf][r] = valid;
                     }
@@ -253,56 +262,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
     } else if (warp == AP_MMAW) {
         // ================= MMA issuer
         if (lane == 0) {
-            const uint32_t id1 = umma::idesc_f16(128, AP_H, 0, 0);
-            const uint32_t id2 = umma::idesc_f16(128, AP_H, 1, 1);
-            const uint32_t id3 = umma::idesc_f16(128, AP_H, 0, 1);
-            // Two independent streams: GEMM1 of tile t needs its half rows loaded
-            // (lfull) and its score buffer released (sfree of tile t-2); GEMM2 of
-            // tile t needs P (pfull).  Serve whichever is ready, so a slow load of
-            // tile t+1 never holds back the value GEMM of tile t.
+            const uint32_t id1 = umma::idesc_f16(64, AP_TILE, 0, 0);
+            const uint32_t id2 = umma::idesc_f16(128, AP_H, 1, 0);
+            // Two streams: GEMM1 of tile t needs its rows loaded (lfull) and its
+            // score buffer released (sfree of tile t-2); GEMM2 of tile t needs
+            // P (pfull).  Serve whichever is ready.
             int n1 = 0, n2 = 0;
             uint32_t spins = 0;
             while (n2 < T) {
                 bool progressed = false;
-                if (n1 < T && n1 <= n2 + 1) {
+                if (n1 < T && n1 < n2 + 2) {
                     const int buf = n1 & 1;
                     if (umma::mbar_test(sa(&b_lfull[buf]), (n1 >> 1) & 1) &&
                         (n1 < 2 || umma::mbar_test(sa(&b_sfree[buf]), ((n1 >> 1) - 1) & 1))) {
                         umma::fence_after();
                         const uint32_t Lb = base + AP_SL + buf * AP_LBUF;
 #pragma unroll
-                        for (int ks = 0; ks < 16; ++ks) {
-                            const uint64_t a = umma::desc(Lb + (ks >> 2) * AP_SLAB + (ks & 3) * 32, 16, 1024,
-                                                          umma::LAYOUT_SW128);
-                            const uint64_t bq = umma::desc(base + AP_SQ + (ks >> 2) * (AP_H * 128) + (ks & 3) * 32, 16,
-                                                           1024, umma::LAYOUT_SW128);
-                            umma::mma_f16(tmem + APT_S + 64 * buf, a, bq, id1, ks > 0);
+                        for (int ks = 0; ks < 32; ++ks) {
+                            const uint64_t a = umma::desc(base + AP_SQ + (ks >> 2) * AP_QSLAB + (ks & 3) * 32, 16,
+                                                          1024, umma::LAYOUT_SW128);
+                            const uint64_t bl = umma::desc(Lb + (ks >> 2) * AP_LSLAB + (ks & 3) * 32, 16, 1024,
+                                                           umma::LAYOUT_SW128);
+                            umma::mma_f16(tmem + APT_S + 64 * buf, a, bl, id1, ks > 0);
                         }
                         umma::commit(sa(&b_sfull[buf]));
                         ++n1;
                         progressed = true;
                     }
                 }
-                if (n2 < n1 && umma::mbar_test(sa(&b_pfull), n2 & 1)) {
+                if (n2 < n1 && umma::mbar_test(sa(&b_pfull[n2 & 1]), (n2 >> 1) & 1)) {
                     umma::fence_after();
                     const int buf = n2 & 1;
                     const uint32_t Lb = base + AP_SL + buf * AP_LBUF;
-                    for (int mt = 0; mt < 2; ++mt) {
+                    const uint32_t Pb = base + AP_SP + buf * AP_PBUF;
+#pragma unroll 1
+                    for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
-                        for (int ks = 0; ks < 8; ++ks) {
-                            const uint64_t a = umma::desc(Lb + (2 * mt) * AP_SLAB + ks * 2048, AP_SLAB, 1024,
+                        for (int ks = 0; ks < 4; ++ks) {
+                            const uint64_t a = umma::desc(Lb + (2 * mt) * AP_LSLAB + ks * 2048, AP_LSLAB, 1024,
                                                           umma::LAYOUT_SW128);
-                            const uint64_t bp = umma::desc(base + AP_SP + ks * 2048, 8192, 1024, umma::LAYOUT_SW128);
+                            const uint64_t bp = umma::desc(Pb + ks * 32, 16, 1024, umma::LAYOUT_SW128);
                             umma::mma_f16(tmem + APT_O + 64 * mt, a, bp, id2, (n2 > 0 || ks > 0) ? 1u : 0u);
                         }
                     }
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint64_t a = umma::desc(base + AP_SONES, 128, 256, umma::LAYOUT_NONE);
-                        const uint64_t bp = umma::desc(base + AP_SP + ks * 2048, 8192, 1024, umma::LAYOUT_SW128);
-                        umma::mma_f16(tmem + APT_L, a, bp, id3, (n2 > 0 || ks > 0) ? 1u : 0u);
-                    }
-                    umma::commit(sa(&b_odone));
+                    umma::commit(sa(&b_odone[buf]));
                     umma::commit(sa(&b_lfree[buf]));
                     ++n2;
                     progressed = true;
@@ -315,168 +318,174 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                 }
             }
         }
-    } else if (warp < AP_SMW) {
-        // ================= softmax: thread = key row 32*(warp%4)+lane, heads hh*32 .. +31
-        const int qd = warp & 3, hh = warp >> 2;
-        const int row = qd * 32 + lane;
-        const int hc = hh * 32;
+    } else {
+        // ================= softmax: warp w reads TMEM lane quarter w%4; lanes 0-15 own head
+        // 16(w%4)+lane; key half w/4 covers keys 32(w/4) .. +31 of each tile
+        const int qd = warp & 3, half = warp >> 2;
+        const bool active = lane < 16;
+        const int h = qd * 16 + (lane & 15);
         const uint32_t lane_base = tmem + ((uint32_t)(qd * 32) << 16);
-        const uint32_t sx_peer = umma::mapa(base + AP_SX, peer);
-        const uint32_t xfull_peer = umma::mapa(sa(&b_xfull), peer);
-        const uint32_t xfree_peer = umma::mapa(sa(&b_xfree), peer);
-        float* red = reinterpret_cast<float*>(sm + AP_RED);           // [4 quadrants][64 heads]
-        const float* sx = reinterpret_cast<const float*>(sm + AP_SX);
+        float lsum = 0.0f;                   // sum of P over this thread's keys, all tiles so far
         for (int t = 0; t < T; ++t) {
             const int buf = t & 1;
             float x[32];
             ok &= umma::mbar_wait(sa(&b_sfull[buf]), (t >> 1) & 1);
             umma::fence_after();
-            umma::tmem_ld16(lane_base + APT_S + 64 * buf + hc, x);
-            umma::tmem_ld16(lane_base + APT_S + 64 * buf + hc + 16, x + 16);
+            umma::tmem_ld16(lane_base + APT_S + 64 * buf + 32 * half, x);
+            umma::tmem_ld16(lane_base + APT_S + 64 * buf + 32 * half + 16, x + 16);
             umma::tmem_wait_ld();
             umma::fence_before();
             __syncwarp();
             if (lane == 0) umma::mbar_arrive(sa(&b_sfree[buf]));
-            // send the partial scores to the peer (16-byte chunks swizzled by row
-            // to spread banks), once it has read the previous ones
-            if (t >= 1) {
-                if (tid == 0) ok &= umma::mbar_wait_cluster(sa(&b_xfree), (t - 1) & 1);
-                umma::bar_named(1, AP_SMT);
-            }
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                umma::st_async_v4(sx_peer + row * 256 + (((hh * 8 + c) ^ (row & 15)) << 4), x[4 * c], x[4 * c + 1],
-                                  x[4 * c + 2], x[4 * c + 3], xfull_peer);
-            if (tid == 0) {
-                ok &= umma::mbar_wait_cluster(sa(&b_xfull), t & 1);
-                if (t + 1 < T) umma::mbar_arrive_expect_tx(sa(&b_xfull), AP_XBYTES);   // arm the next tile
-            }
-            umma::bar_named(1, AP_SMT);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const float4 v = *reinterpret_cast<const float4*>(sx + row * 64 + (((hh * 8 + c) ^ (row & 15)) << 2));
-                // S = S_0 + S_1 in both CTAs (addition is commutative, so the bits agree)
-                x[4 * c] += v.x;
-                x[4 * c + 1] += v.y;
-                x[4 * c + 2] += v.z;
-                x[4 * c + 3] += v.w;
-            }
-            // row validity was written by the loaders of this buffer: observe their barrier too
+            // key validity was written by the loaders of this buffer: observe their barrier too
             ok &= umma::mbar_wait(sa(&b_lfull[buf]), (t >> 1) & 1);
-            const bool valid = rowok[buf][row] != 0;
+            const float mh = m_run[h];
             bool exceed = false;
 #pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) {
-                const float4 mm = *reinterpret_cast<const float4*>(m_run + hc + 4 * q4);
-                const float mv[4] = {mm.x, mm.y, mm.z, mm.w};
+            for (int c = 0; c < 8; ++c) {
+                const int4 v4 = *reinterpret_cast<const int4*>(&rowok[buf][32 * half + 4 * c]);
+                const int vv[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int h = 4 * q4 + e;
-                    x[h] = valid ? x[h] * scale_log2e : -INFINITY;
-                    exceed |= x[h] > mv[e] + AP_LAZY;
+                    const int i = 4 * c + e;
+                    x[i] = vv[e] ? x[i] * scale_log2e : -INFINITY;
+                    exceed |= x[i] > mh + AP_LAZY;
                 }
             }
-            // both CTAs hold the same scores, so they take the same branch
-            const bool raise = umma::bar_red_or(1, AP_SMT, exceed);
+            const bool raise = umma::bar_red_or(1, AP_SMT, active && exceed);
             if (raise) {
-                // new running max for the heads that rose too far: column maxima of the tile
+                // new running max for the heads that rose too far: max over both key halves
+                float mx = -INFINITY;
 #pragma unroll
-                for (int h = 0; h < 32; ++h) {
-                    const uint32_t mk = __reduce_max_sync(0xffffffffu, ap_ord(x[h]));
-                    if (lane == 0) red[qd * AP_H + hc + h] = ap_unord(mk);
-                }
+                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, x[i]);
+                if (active) red[half * AP_H + h] = mx;
                 umma::bar_named(1, AP_SMT);
-                if (tid < AP_H) {
-                    const float mt = fmaxf(fmaxf(red[tid], red[AP_H + tid]), fmaxf(red[2 * AP_H + tid], red[3 * AP_H + tid]));
-                    const float mo = m_run[tid];
+                if (half == 0 && qd < 4) {
                     float f = 1.0f;
-                    if (mt > -INFINITY && (mo == -INFINITY || mt > mo + AP_LAZY)) {
-                        f = (mo == -INFINITY) ? 0.0f : umma::ex2(mo - mt);
-                        m_run[tid] = mt;
+                    if (active) {
+                        const float mt = fmaxf(red[h], red[AP_H + h]);
+                        const float mo = m_run[h];
+                        if (mt > -INFINITY && (mo == -INFINITY || mt > mo + AP_LAZY)) {
+                            f = (mo == -INFINITY) ? 0.0f : umma::ex2(mo - mt);
+                            m_run[h] = mt;
+                        }
+                        fac[h] = f;
                     }
-                    fac[tid] = f;
                     const unsigned any = __ballot_sync(0xffffffffu, f != 1.0f);
-                    if (lane == 0) flag[warp] = any != 0;
+                    if (lane == 0) flag[qd] = any != 0;
                 }
-                if (t >= 1) ok &= umma::mbar_wait(sa(&b_odone), (t - 1) & 1);   // previous P and O are settled
+                if (t >= 1) ok &= umma::mbar_wait(sa(&b_odone[(t - 1) & 1]), ((t - 1) >> 1) & 1);   // O settled
                 umma::bar_named(1, AP_SMT);
                 umma::fence_after();
-                if (t >= 1 && (flag[0] | flag[1])) {
-                    // rescale O^T (both dim tiles) and l in this thread's 32 head columns
+                if (t >= 1 && (flag[0] | flag[1] | flag[2] | flag[3])) {
+                    // rescale O^T: this warp's lane quarter of dim tiles 2*half and 2*half+1, all 64 heads
 #pragma unroll 1
-                    for (int blk = 0; blk < 3; ++blk) {
-                        const uint32_t col0 = (blk < 2 ? APT_O + 64 * blk : APT_L) + hc;
-#pragma unroll
-                        for (int c = 0; c < 32; c += 16) {
+                    for (int mt = 2 * half; mt < 2 * half + 2; ++mt) {
+#pragma unroll 1
+                        for (int c = 0; c < AP_H; c += 16) {
                             float v[16];
-                            umma::tmem_ld16(lane_base + col0 + c, v);
+                            umma::tmem_ld16(lane_base + APT_O + 64 * mt + c, v);
                             umma::tmem_wait_ld();
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) v[i] *= fac[hc + c + i];
-                            umma::tmem_st16(lane_base + col0 + c, v);
+                            for (int i = 0; i < 16; ++i) v[i] *= fac[c + i];
+                            umma::tmem_st16(lane_base + APT_O + 64 * mt + c, v);
                         }
                     }
                     umma::tmem_wait_st();
                 }
-            } else if (t >= 1) {
-                ok &= umma::mbar_wait(sa(&b_odone), (t - 1) & 1);             // GEMM2 of t-1 has read P
+                if (active) lsum *= fac[h];
             }
-            // P = exp2(x - m_run), fp16, row = key (MN-major B operand), this thread's 4 chunks
+            // the P buffer of this tile was last read by GEMM2 of tile t-2
+            if (t >= 2) ok &= umma::mbar_wait(sa(&b_odone[buf]), ((t >> 1) - 1) & 1);
+            const float m = m_run[h];
+            // P^T row h, keys 32*half .. +31 (4 chunks of 8 keys), fp16
+            uint8_t* P = sm + AP_SP + buf * AP_PBUF;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t w[4];
-                const float4 ma = *reinterpret_cast<const float4*>(m_run + hc + 8 * c);
-                const float4 mb = *reinterpret_cast<const float4*>(m_run + hc + 8 * c + 4);
-                const float mv[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int h = 8 * c + 2 * e;
-                    const float m0 = mv[2 * e], m1 = mv[2 * e + 1];
-                    const float p0 = (x[h] == -INFINITY || m0 == -INFINITY) ? 0.0f : umma::ex2(x[h] - m0);
-                    const float p1 = (x[h + 1] == -INFINITY || m1 == -INFINITY) ? 0.0f : umma::ex2(x[h + 1] - m1);
+                    const int i = 8 * c + 2 * e;
+                    const float p0 = (x[i] == -INFINITY || m == -INFINITY) ? 0.0f : umma::ex2(x[i] - m);
+                    const float p1 = (x[i + 1] == -INFINITY || m == -INFINITY) ? 0.0f : umma::ex2(x[i + 1] - m);
                     const __half2 hp = __floats2half2_rn(p0, p1);
                     w[e] = *reinterpret_cast<const uint32_t*>(&hp);
+                    lsum += p0 + p1;
                 }
-                *reinterpret_cast<uint4*>(sm + AP_SP + apswz(row, hh * 4 + c)) = make_uint4(w[0], w[1], w[2], w[3]);
+                if (active)
+                    *reinterpret_cast<uint4*>(P + apswz(h, 4 * half + c)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
             umma::fence_proxy_async();
             umma::fence_before();
             __syncwarp();
-            if (lane == 0) umma::mbar_arrive(sa(&b_pfull));
-            // every warp read the peer's scores before the barrier above: let it send the next ones
-            if (tid == 0) umma::mbar_arrive_remote(xfree_peer);
+            if (lane == 0) umma::mbar_arrive(sa(&b_pfull[buf]));
         }
-        // ================= epilogue: thread = output dim 32*(warp%4)+lane of each 128-dim tile, its 32 heads
-        ok &= umma::mbar_wait(sa(&b_odone), (T - 1) & 1);
+        // ---- per-head max and row sum of this CTA, to the peer
+        if (active) red[half * AP_H + h] = lsum;
+        umma::bar_named(1, AP_SMT);
+        if (tid < AP_H) {
+            const float l = red[tid] + red[AP_H + tid];
+            own_ml[tid] = m_run[tid];
+            own_ml[AP_H + tid] = l;
+            st_cluster_f32(umma::mapa(sa(peer_ml + tid), peer), m_run[tid]);
+            st_cluster_f32(umma::mapa(sa(peer_ml + AP_H + tid), peer), l);
+        }
+    }
+    // ================= combine the pair (every thread of both CTAs takes part in the cluster barriers)
+    umma::cluster_sync();              // the max / row sums of both CTAs are in place
+    if (warp < AP_SMW) {
+        if (tid < AP_H) {
+            const float m0 = own_ml[tid], l0 = own_ml[AP_H + tid], m1 = peer_ml[tid], l1 = peer_ml[AP_H + tid];
+            const float mm = fmaxf(m0, m1);
+            const float s0 = (m0 == -INFINITY) ? 0.0f : umma::ex2(m0 - mm);
+            const float s1 = (m1 == -INFINITY) ? 0.0f : umma::ex2(m1 - mm);
+            const float Lt = l0 * s0 + l1 * s1;
+            fown[tid] = Lt > 0.0f ? s0 / Lt : 0.0f;
+            if (lse != nullptr && rank == 0)
+                lse[gq * AP_H + tid] = Lt > 0.0f ? (mm + log2f(Lt)) * 0.69314718055994531f : -INFINITY;
+        }
+        umma::bar_named(1, AP_SMT);
+        ok &= umma::mbar_wait(sa(&b_odone[(T - 1) & 1]), ((T - 1) >> 1) & 1);   // every GEMM2 is done
         umma::fence_after();
-        float inv[32];
-        umma::tmem_ld16(lane_base + APT_L + hc, inv);
-        umma::tmem_ld16(lane_base + APT_L + hc + 16, inv + 16);
-        umma::tmem_wait_ld();
-        if (lse != nullptr && rank == 0 && qd == 0 && lane == 0)
+        // this CTA's share of the peer's dims: dim tile 2*peer + half, this warp's lane quarter
+        const int qd = warp & 3, half = warp >> 2;
+        const int mt = 2 * (int)peer + half;
+        float* sc = scratch + ((gq * 2 + rank) * AP_H) * 256 + half * 128 + qd * 32 + lane;
+#pragma unroll 1
+        for (int c = 0; c < AP_H; c += 16) {
+            float v[16];
+            umma::tmem_ld16(tmem + ((uint32_t)(qd * 32) << 16) + APT_O + 64 * mt + c, v);
+            umma::tmem_wait_ld();
 #pragma unroll
-            for (int h = 0; h < 32; ++h)
-                lse[gq * AP_H + hc + h] =
-                    inv[h] > 0.0f ? (m_run[hc + h] + log2f(inv[h])) * 0.69314718055994531f : -INFINITY;
+            for (int i = 0; i < 16; ++i) sc[(int64_t)(c + i) * 256] = v[i] * fown[c + i];
+        }
+    }
+    umma::fence_before();
+    umma::cluster_sync();              // each CTA's share is in the workspace
+    if (warp < AP_SMW) {
+        umma::fence_after();
+        const int qd = warp & 3, half = warp >> 2;
+        const int mt = 2 * (int)rank + half;
+        const int dl = half * 128 + qd * 32 + lane;                  // dim within this CTA's half
+        const float* sp = scratch + ((gq * 2 + peer) * AP_H) * 256 + dl;
+        float* op = out + (gq * AP_H) * D_LAT + (int)rank * 256 + dl;
+#pragma unroll 1
+        for (int c = 0; c < AP_H; c += 16) {
+            float v[16], pv[16];
 #pragma unroll
-        for (int h = 0; h < 32; ++h) inv[h] = inv[h] > 0.0f ? 1.0f / inv[h] : 0.0f;
-        for (int mt = 0; mt < 2; ++mt) {
-            float* op = out + (gq * AP_H + hc) * D_LAT + d0 + mt * 128 + row;
+            for (int i = 0; i < 16; ++i) pv[i] = sp[(int64_t)(c + i) * 256];     // all loads before any store
+            umma::tmem_ld16(tmem + ((uint32_t)(qd * 32) << 16) + APT_O + 64 * mt + c, v);
+            umma::tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 32; c += 16) {
-                float o[16];
-                umma::tmem_ld16(lane_base + APT_O + 64 * mt + hc + c, o);
-                umma::tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    op[(int64_t)(c + i) * D_LAT] = ok ? o[i] * inv[c + i] : __int_as_float(0x7fc00000);
+            for (int i = 0; i < 16; ++i) {
+                const float o = v[i] * fown[c + i] + pv[i];
+                op[(int64_t)(c + i) * D_LAT] = ok ? o : __int_as_float(0x7fc00000);
             }
         }
     }
     if (!ok) atomicExch(err, 1);
     umma::fence_before();
     __syncthreads();
-    umma::cluster_sync();              // the peer is done with this CTA's shared memory
     if (warp == 0) {
         umma::fence_after();
         umma::tmem_dealloc(tmem, APT_COLS);
@@ -485,17 +494,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
 
 bool attn_pair_supported(int H) { return H == AP_H; }
 
+size_t attn_pair_ws(int batch, int n_q) { return 256 + (size_t)batch * n_q * AP_SCRATCH; }
+
 cudaError_t launch_sparse_attn_pair(const csa2_cache& c, const uint16_t* q, int n_q, const int64_t* q_pos,
                                     const int32_t* idx, int k, const uint16_t* swa, int64_t swa_pos0, int swa_len,
-                                    float scale, float* out, float* lse, int* err, cudaStream_t st) {
+                                    float scale, float* out, float* lse, void* ws, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(k_sparse_attn_pair, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)AP_DYN);
     if (e != cudaSuccess) return e;
+    int* err = reinterpret_cast<int*>(ws);
+    float* scratch = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + 256);
     const float scale_log2e = scale * 1.4426950408889634f;
     for (int q0 = 0; q0 < n_q; q0 += 65535) {
         const int nqc = (n_q - q0) < 65535 ? (n_q - q0) : 65535;
         dim3 grid(2, nqc, c.batch);
         k_sparse_attn_pair<<<grid, AP_THREADS, AP_DYN, st>>>(c.lat_codes, c.lat_scales, c.capacity, q, n_q, q0, q_pos,
-                                                             idx, k, swa, swa_pos0, swa_len, scale_log2e, out, lse, err);
+                                                             idx, k, swa, swa_pos0, swa_len, scale_log2e, out, lse, err,
+                                                             scratch);
         note_launch();
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;

@@ -157,12 +157,13 @@ cudaError_t launch_sparse_attn_tc(const csa2_cache& c, const uint16_t* q, int n_
                                   float scale, float* out, float* lse, void* ws, cudaStream_t st);
 
 bool attn_pair_supported(int H);
+size_t attn_pair_ws(int batch, int n_q);
 cudaError_t launch_sparse_attn_pair(const csa2_cache& c, const uint16_t* q, int n_q, const int64_t* q_pos,
                                     const int32_t* idx, int k, const uint16_t* swa, int64_t swa_pos0, int swa_len,
-                                    float scale, float* out, float* lse, int* err, cudaStream_t st);
+                                    float scale, float* out, float* lse, void* ws, cudaStream_t st);
 
 size_t sparse_attn_ws(int batch, int n_q, int H, int k) {
-    if (attn_pair_supported(H)) return 256;
+    if (attn_pair_supported(H)) return attn_pair_ws(batch, n_q);
     return attn_tc_supported(H) ? attn_tc_ws(batch, n_q, H, k) : 0;
 }
 
@@ -173,8 +174,7 @@ cudaError_t launch_sparse_attn(const csa2_cache& c, const uint16_t* q, int n_q, 
                                const int32_t* idx, int k, const uint16_t* swa, int64_t swa_pos0, int swa_len,
                                float scale, float* out, float* lse, void* ws, size_t, cudaStream_t st) {
     if (attn_pair_supported(H))
-        return launch_sparse_attn_pair(c, q, n_q, q_pos, idx, k, swa, swa_pos0, swa_len, scale, out, lse,
-                                       reinterpret_cast<int*>(ws), st);
+        return launch_sparse_attn_pair(c, q, n_q, q_pos, idx, k, swa, swa_pos0, swa_len, scale, out, lse, ws, st);
     if (attn_tc_supported(H))
         return launch_sparse_attn_tc(c, q, n_q, H, q_pos, idx, k, swa, swa_pos0, swa_len, scale, out, lse, ws, st);
     return launch_sparse_attn_simt(c, q, n_q, H, q_pos, idx, k, swa, swa_pos0, swa_len, scale, out, lse, st);
