@@ -87,7 +87,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
     extern __shared__ uint8_t dyn[];
     __shared__ __align__(8) unsigned long long b_lfull[2], b_lfree[2], b_sfull[2], b_sfree[2], b_pfull[2], b_odone[2];
     __shared__ uint32_t tmem_base;
-    __shared__ __align__(16) int rowok[2][AP_TILE];
+    __shared__ __align__(16) uint8_t rowok[2][AP_TILE];
 
     const uint32_t raw = umma::smem_u32(dyn);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -208,7 +208,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                             *reinterpret_cast<uint4*>(L + (c >> 3) * AP_LSLAB + apswz(r, c & 7)) =
                                 make_uint4(ap_bf16x2_to_f16x2(v.x), ap_bf16x2_to_f16x2(v.y),
                                            ap_bf16x2_to_f16x2(v.z), ap_bf16x2_to_f16x2(v.w));
-                            if (c == 0) rowok[buf][r] = (int)rank * AP_TILE + r < nwin;
+                            if (c == 0) rowok[buf][r] = (int)rank * AP_TILE + r < nwin ? 1 : 0;
                         }
                     }
                 }
@@ -252,7 +252,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                             const int cc = c * 4 + w;                // 8-dim chunk 0..63
                             *reinterpret_cast<uint4*>(L + (cc >> 3) * AP_LSLAB + apswz(r, cc & 7)) = o;
                         }
-                        if (c == 0) rowok[buf][r] = valid;
+                        if (c == 0) rowok[buf][r] = valid ? 1 : 0;
                     }
                 }
             }
@@ -319,20 +319,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
             }
         }
     } else {
-        // ================= softmax: warp w reads TMEM lane quarter w%4; lanes 0-15 own head
-        // 16(w%4)+lane; key half w/4 covers keys 32(w/4) .. +31 of each tile
+        // ================= softmax: warp w reads the 16 score rows (heads) of TMEM lane
+        // quarter w%4 with the 16x64b shape, for keys 32(w/4) .. +31 of each tile: lane t
+        // holds head 16(w%4) + t/4 + 8(t%2) and the keys of parity par = (t/2)%2
         const int qd = warp & 3, half = warp >> 2;
-        const bool active = lane < 16;
-        const int h = qd * 16 + (lane & 15);
+        const int h = qd * 16 + (lane >> 2) + 8 * (lane & 1);
+        const int par = (lane >> 1) & 1;
         const uint32_t lane_base = tmem + ((uint32_t)(qd * 32) << 16);
         float lsum = 0.0f;                   // sum of P over this thread's keys, all tiles so far
         for (int t = 0; t < T; ++t) {
             const int buf = t & 1;
-            float x[32];
+            float x[16];                     // keys 32*half + par + 2i
             ok &= umma::mbar_wait(sa(&b_sfull[buf]), (t >> 1) & 1);
             umma::fence_after();
-            umma::tmem_ld16(lane_base + APT_S + 64 * buf + 32 * half, x);
-            umma::tmem_ld16(lane_base + APT_S + 64 * buf + 32 * half + 16, x + 16);
+            umma::tmem_ld16x64b_x16(lane_base + APT_S + 64 * buf + 32 * half, x);
             umma::tmem_wait_ld();
             umma::fence_before();
             __syncwarp();
@@ -341,28 +341,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
             ok &= umma::mbar_wait(sa(&b_lfull[buf]), (t >> 1) & 1);
             const float mh = m_run[h];
             bool exceed = false;
+            {
+                const uint4 v0 = *reinterpret_cast<const uint4*>(&rowok[buf][32 * half]);
+                const uint4 v1 = *reinterpret_cast<const uint4*>(&rowok[buf][32 * half + 16]);
+                const uint32_t vw[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const int4 v4 = *reinterpret_cast<const int4*>(&rowok[buf][32 * half + 4 * c]);
-                const int vv[4] = {v4.x, v4.y, v4.z, v4.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int i = 4 * c + e;
-                    x[i] = vv[e] ? x[i] * scale_log2e : -INFINITY;
+                for (int i = 0; i < 16; ++i) {
+                    const int key = par + 2 * i;                       // within the half
+                    const bool valid = (vw[key >> 2] >> (8 * (key & 3))) & 0xffu;
+                    x[i] = valid ? x[i] * scale_log2e : -INFINITY;
                     exceed |= x[i] > mh + AP_LAZY;
                 }
             }
-            const bool raise = umma::bar_red_or(1, AP_SMT, active && exceed);
+            const bool raise = umma::bar_red_or(1, AP_SMT, exceed);
             if (raise) {
-                // new running max for the heads that rose too far: max over both key halves
+                // new running max for the heads that rose too far: max over the head's four threads
                 float mx = -INFINITY;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, x[i]);
-                if (active) red[half * AP_H + h] = mx;
+                for (int i = 0; i < 16; ++i) mx = fmaxf(mx, x[i]);
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                if (par == 0) red[half * AP_H + h] = mx;
                 umma::bar_named(1, AP_SMT);
-                if (half == 0 && qd < 4) {
+                if (half == 0) {
                     float f = 1.0f;
-                    if (active) {
+                    if (par == 0) {
                         const float mt = fmaxf(red[h], red[AP_H + h]);
                         const float mo = m_run[h];
                         if (mt > -INFINITY && (mo == -INFINITY || mt > mo + AP_LAZY)) {
@@ -393,35 +395,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                     }
                     umma::tmem_wait_st();
                 }
-                if (active) lsum *= fac[h];
+                lsum *= fac[h];
             }
             // the P buffer of this tile was last read by GEMM2 of tile t-2
             if (t >= 2) ok &= umma::mbar_wait(sa(&b_odone[buf]), ((t >> 1) - 1) & 1);
             const float m = m_run[h];
-            // P^T row h, keys 32*half .. +31 (4 chunks of 8 keys), fp16
-            uint8_t* P = sm + AP_SP + buf * AP_PBUF;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int i = 8 * c + 2 * e;
-                    const float p0 = (x[i] == -INFINITY || m == -INFINITY) ? 0.0f : umma::ex2(x[i] - m);
-                    const float p1 = (x[i + 1] == -INFINITY || m == -INFINITY) ? 0.0f : umma::ex2(x[i + 1] - m);
-                    const __half2 hp = __floats2half2_rn(p0, p1);
-                    w[e] = *reinterpret_cast<const uint32_t*>(&hp);
-                    lsum += p0 + p1;
-                }
-                if (active)
-                    *reinterpret_cast<uint4*>(P + apswz(h, 4 * half + c)) = make_uint4(w[0], w[1], w[2], w[3]);
+            for (int i = 0; i < 16; ++i) {
+                x[i] = (x[i] == -INFINITY || m == -INFINITY) ? 0.0f : umma::ex2(x[i] - m);
+                lsum += x[i];
             }
+            // P^T row h, keys 32*half + 16*par .. +15 from this thread: trade half of the values with
+            // the lane of the other parity so that each holds 16 consecutive keys
+            float rv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) rv[i] = __shfl_xor_sync(0xffffffffu, par ? x[i] : x[8 + i], 2);
+            uint32_t w[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const __half2 hp = par ? __floats2half2_rn(rv[j], x[8 + j]) : __floats2half2_rn(x[j], rv[j]);
+                w[j] = *reinterpret_cast<const uint32_t*>(&hp);
+            }
+            uint8_t* P = sm + AP_SP + buf * AP_PBUF;
+            *reinterpret_cast<uint4*>(P + apswz(h, 4 * half + 2 * par)) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(P + apswz(h, 4 * half + 2 * par + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
             umma::fence_proxy_async();
             umma::fence_before();
             __syncwarp();
             if (lane == 0) umma::mbar_arrive(sa(&b_pfull[buf]));
         }
+        lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
         // ---- per-head max and row sum of this CTA, to the peer
-        if (active) red[half * AP_H + h] = lsum;
+        if (par == 0) red[half * AP_H + h] = lsum;
         umma::bar_named(1, AP_SMT);
         if (tid < AP_H) {
             const float l = red[tid] + red[AP_H + tid];
