@@ -153,7 +153,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
     umma::fence_proxy_async();
     umma::fence_before();
     __syncthreads();
-    umma::cluster_sync();              // both CTAs have started (their shared memory exists)
+    umma::cluster_arrive_relaxed();    // waited for before the first access to the peer's shared memory
     umma::fence_after();
     const uint32_t tmem = tmem_base;
     bool ok = true;
@@ -186,9 +186,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
         }
         for (int t = 0; t < T; ++t) {
             const int buf = t & 1;
-            if (t >= 2) ok &= umma::mbar_wait(sa(&b_lfree[buf]), ((t >> 1) - 1) & 1);
             uint8_t* L = sm + AP_SL + buf * AP_LBUF;
             if (t == T - 1) {
+                if (t >= 2) ok &= umma::mbar_wait(sa(&b_lfree[buf]), ((t >> 1) - 1) & 1);
                 // window rows 64*rank .. +63: 64 rows x 64 chunks of 8 dims (bf16 -> fp16), 8 loads in flight
                 for (int u0 = lt; u0 < AP_TILE * 64; u0 += AP_LOADERS * 8) {
                     uint4 wv[8];
@@ -213,7 +213,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                     }
                 }
             } else {
-                // selected FP4 rows: 64 rows x 16 units of 32 dims (16 B of codes + 2 scale bytes)
+                // selected FP4 rows: 64 rows x 16 units of 32 dims (16 B of codes + 2 scale bytes),
+                // fetched before waiting for the buffer so that the round trip overlaps the wait
                 constexpr int NU = (AP_TILE * 16 + AP_LOADERS - 1) / AP_LOADERS;
                 const int slot0 = (2 * t + (int)rank) * AP_TILE;
                 uint4 cw[NU];
@@ -232,6 +233,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                         }
                     }
                 }
+                if (t >= 2) ok &= umma::mbar_wait(sa(&b_lfree[buf]), ((t >> 1) - 1) & 1);
 #pragma unroll
                 for (int i = 0; i < NU; ++i) {
                     const int u = lt + i * AP_LOADERS, r = u >> 4, c = u & 15;
@@ -428,6 +430,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
         // ---- per-head max and row sum of this CTA, to the peer
         if (par == 0) red[half * AP_H + h] = lsum;
         umma::bar_named(1, AP_SMT);
+    }
+    umma::cluster_wait();              // both CTAs have started: the peer's shared memory exists
+    if (warp < AP_SMW) {
         if (tid < AP_H) {
             const float l = red[tid] + red[AP_H + tid];
             own_ml[tid] = m_run[tid];
