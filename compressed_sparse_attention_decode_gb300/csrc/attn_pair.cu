@@ -140,6 +140,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
             const int i = tid + u * AP_THREADS, h = i >> 6, c = i & 63;
             qv[u] = __ldg(reinterpret_cast<const uint4*>(q + ((gq * AP_H + h) * D_LAT + c * 8)));
         }
+        if (warp > AP_MMAW) {
+            // the loaders stage this CTA's indices meanwhile (the round trips overlap)
+            int* sidx = reinterpret_cast<int*>(sm + AP_SIDX);
+            for (int u = tid - (AP_MMAW + 1) * 32; u < n4 * AP_TILE; u += AP_LOADERS) {
+                const int s = (2 * (u / AP_TILE) + (int)rank) * AP_TILE + u % AP_TILE;
+                if (s < k) {
+                    const int j = idx[gq * k + s];
+                    sidx[s] = (j >= 0 && j < capacity) ? j : -1;
+                }
+            }
+        }
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const int i = tid + u * AP_THREADS, h = i >> 6, c = i & 63;
@@ -165,25 +176,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
         const uint8_t* codes_b = lat_codes + (int64_t)b * capacity * (D_LAT / 2);
         const uint8_t* scales_b = lat_scales + (int64_t)b * capacity * (D_LAT / 16);
         const uint16_t* win_b = swa + ((int64_t)b * swa_len + (wlo - swa_pos0)) * D_LAT;
-        for (int s = lt; s < k; s += AP_LOADERS) {
-            const int j = idx[gq * k + s];
-            sidx[s] = (j >= 0 && j < capacity) ? j : -1;
-        }
-        umma::bar_named(2, AP_LOADERS);
-        // every row this CTA reads, into L2 now: the gathers below then hit L2
-        for (int u = lt; u < n4 * AP_TILE; u += AP_LOADERS) {
-            const int s = (2 * (u / AP_TILE) + (int)rank) * AP_TILE + u % AP_TILE;
-            const int j = s < k ? sidx[s] : -1;
-            if (j >= 0) {
-                umma::prefetch_l2(codes_b + (int64_t)j * (D_LAT / 2));
-                umma::prefetch_l2(codes_b + (int64_t)j * (D_LAT / 2) + 128);
-                umma::prefetch_l2(scales_b + (int64_t)j * (D_LAT / 16));
+        // every row of the later tiles, into L2 now (called once the first tile's gathers are
+        // in flight): those gathers then hit L2
+        auto prefetch_rest = [&]() {
+            for (int u = AP_TILE + lt; u < n4 * AP_TILE; u += AP_LOADERS) {
+                const int s = (2 * (u / AP_TILE) + (int)rank) * AP_TILE + u % AP_TILE;
+                const int j = s < k ? sidx[s] : -1;
+                if (j >= 0) {
+                    umma::prefetch_l2(codes_b + (int64_t)j * (D_LAT / 2));
+                    umma::prefetch_l2(codes_b + (int64_t)j * (D_LAT / 2) + 128);
+                    umma::prefetch_l2(scales_b + (int64_t)j * (D_LAT / 16));
+                }
             }
-        }
-        for (int u = lt; u < AP_TILE * 8; u += AP_LOADERS) {
-            const int r = (int)rank * AP_TILE + (u >> 3);
-            if (r < nwin) umma::prefetch_l2(win_b + (int64_t)r * D_LAT + (u & 7) * 64);
-        }
+            for (int u = lt; u < AP_TILE * 8; u += AP_LOADERS) {
+                const int r = (int)rank * AP_TILE + (u >> 3);
+                if (r < nwin) umma::prefetch_l2(win_b + (int64_t)r * D_LAT + (u & 7) * 64);
+            }
+        };
+        if (n4 == 0) prefetch_rest();
         for (int t = 0; t < T; ++t) {
             const int buf = t & 1;
             uint8_t* L = sm + AP_SL + buf * AP_LBUF;
@@ -233,6 +243,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                         }
                     }
                 }
+                if (t == 0) prefetch_rest();
                 if (t >= 2) ok &= umma::mbar_wait(sa(&b_lfree[buf]), ((t >> 1) - 1) & 1);
 #pragma unroll
                 for (int i = 0; i < NU; ++i) {
