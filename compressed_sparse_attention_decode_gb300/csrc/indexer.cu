@@ -553,13 +553,22 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
     const int n_valid = sm.rs.ctl[3];
     __syncthreads();
     unsigned int lam = 0u;                       // <= the k-th largest lower bound
-    if (n_valid > k)
+    if (n_valid > k) {
+        // the lower-bound keys, staged once in shared memory (the bitmap region is idle
+        // here) when they fit, so the passes of the selection do not go back to L2
+        unsigned int* stage = sm.bitmap;
+        const bool staged = n <= SEL_BITMAP_BITS / 32;
+        if (staged) {
+            for (int t = threadIdx.x; t < n; t += blockDim.x) stage[t] = f32_key(L[t].x);
+            __syncthreads();
+        }
         lam = block_kth_bound(
             [&](int t, unsigned int& key) {
-                key = f32_key(L[t].x);
+                key = staged ? stage[t] : f32_key(L[t].x);
                 return true;
             },
             n, k, false, sm.rs);
+    }
     if (threadIdx.x == 0) sm.rs.ctl[0] = 0;
     __syncthreads();
     for (int base = 0; base < n; base += blockDim.x) {
@@ -622,13 +631,20 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
         const int32_t* bi = bid + slab * list_len;
         const float2* bl = blu + slab * list_len;
         unsigned int lamb = 0u;
-        if (mb > Kp)                          // <= the Kp-th largest lower bound
+        if (mb > Kp) {                        // <= the Kp-th largest lower bound
+            unsigned int* stage = sm.bitmap;
+            const bool staged = mb <= SEL_BITMAP_BITS / 32;
+            if (staged) {
+                for (int t = threadIdx.x; t < mb; t += blockDim.x) stage[t] = f32_key(bl[t].x);
+                __syncthreads();
+            }
             lamb = block_kth_bound(
                 [&](int t, unsigned int& key) {
-                    key = f32_key(bl[t].x);
+                    key = staged ? stage[t] : f32_key(bl[t].x);
                     return true;
                 },
                 mb, Kp, false, sm.rs);
+        }
         // candidates: blocks whose upper bound reaches the Kp-th largest lower
         // bound, with their (upper, lower) bound keys packed in ckey
         if (threadIdx.x == 0) sm.rs.ctl[0] = 0;

@@ -324,12 +324,11 @@ __device__ __forceinline__ float key_value(unsigned int k) {
 // holds more than 64 keys its own range is cut again (at most four levels).
 // The band is the smallest and largest key of the last bucket.  Non-finite keys
 // (an empty slot's -inf) stay below every bucket.  Used where the caller only
-// filters with it: even buckets spread the shared-memory atomics, and the
-// refinement keeps the band to a few dozen keys.
+// filters with it: even buckets spread the shared-memory atomics (one
+// histogram for the block), and the refinement keeps the band to a few dozen keys.
 template <typename Get>
 __device__ uint2 block_kth_band(Get getkey, int n, int k, RadixSmem& rs) {
-    const int lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-    int* wh = rs.whist + (threadIdx.x >> 5) * 256;
+    const int lane = threadIdx.x & 31;
     auto bucket_of = [](unsigned int key, float vlo, float scale) {
         return min((int)((key_value(key) - vlo) * scale), 255);
     };
@@ -365,7 +364,7 @@ __device__ uint2 block_kth_band(Get getkey, int n, int k, RadixSmem& rs) {
     unsigned int lo = (unsigned int)rs.kmin, hi = (unsigned int)rs.kmax;
     int need = k;
     for (int level = 0; level < 4 && lo < hi; ++level) {
-        for (int i = threadIdx.x; i < nw * 256; i += blockDim.x) rs.whist[i] = 0;
+        for (int i = threadIdx.x; i < 256; i += blockDim.x) rs.hist[i] = 0;
         __syncthreads();
         const float vlo = key_value(lo);
         float scale = 256.0f / (key_value(hi) - vlo);
@@ -380,13 +379,7 @@ __device__ uint2 block_kth_band(Get getkey, int n, int k, RadixSmem& rs) {
             }
 #pragma unroll
             for (int u = 0; u < 8; ++u)
-                if (in[u] && kk[u] >= lo && kk[u] <= hi) atomicAdd(&wh[bucket_of(kk[u], vlo, scale)], 1);
-        }
-        __syncthreads();
-        for (int i = threadIdx.x; i < 256; i += blockDim.x) {
-            int c = 0;
-            for (int w = 0; w < nw; ++w) c += rs.whist[w * 256 + i];
-            rs.hist[i] = c;
+                if (in[u] && kk[u] >= lo && kk[u] <= hi) atomicAdd(&rs.hist[bucket_of(kk[u], vlo, scale)], 1);
         }
         __syncthreads();
         if (threadIdx.x < 32) {
@@ -518,13 +511,40 @@ static __device__ void forward_candidates(const float2* lu, int c0, int E, int n
         const int nbl = min(E / bs, nb - g0);             // blocks of this chunk that exist
         const int nvalid = nbl - ((forced >= g0 && forced < g0 + nbl) ? 1 : 0);
         if (nb > pool_blocks && nvalid > 0) {
-            auto blk = [&](int bl, bool upper) {
-                float mx = -INFINITY;
+            // block bounds (max over members) computed once and written over lu[0..nbl) when
+            // every thread holds at most four blocks (each reads its members before any is
+            // overwritten); otherwise taken from the members at each use
+            float2* lub = const_cast<float2*>(lu);
+            const bool cached = nbl <= 4 * (int)blockDim.x;
+            auto members = [&](int bl) {
+                float2 m2 = make_float2(-INFINITY, -INFINITY);
                 for (int i = 0; i < bs; ++i) {
                     const int e = bl * bs + i;
-                    if (e < n_loc) mx = fmaxf(mx, upper ? lu[e].y : lu[e].x);
+                    if (e < n_loc) {
+                        m2.x = fmaxf(m2.x, lu[e].x);
+                        m2.y = fmaxf(m2.y, lu[e].y);
+                    }
                 }
-                return mx;
+                return m2;
+            };
+            if (cached) {
+                float2 mine[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int bl = threadIdx.x + q * blockDim.x;
+                    mine[q] = bl < nbl ? members(bl) : make_float2(-INFINITY, -INFINITY);
+                }
+                __syncthreads();
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int bl = threadIdx.x + q * blockDim.x;
+                    if (bl < nbl) lub[bl] = mine[q];
+                }
+                __syncthreads();
+            }
+            auto blk = [&](int bl, bool upper) {
+                const float2 m2 = cached ? lub[bl] : members(bl);
+                return upper ? m2.y : m2.x;
             };
             unsigned int lamb = 0u;
             if (nvalid > pool_blocks - 1)
