@@ -166,6 +166,7 @@ struct RadixSmem {
     int hist[256];
     int ctl[8];   // [0] append counter, [1] digit, [2] krem, [3] scratch, [4] [5] global append
     unsigned long long kmin, kmax;
+    unsigned int kmin32, kmax32;  // the same for 32-bit keys (native shared-memory atomics)
     int* whist;   // per-warp histograms, (blockDim.x / 32) x 256 ints, set by the caller
 };
 
@@ -350,18 +351,18 @@ __device__ uint2 block_kth_band(Get getkey, int n, int k, RadixSmem& rs) {
         mn = __reduce_min_sync(0xffffffffu, mn);
         mx = __reduce_max_sync(0xffffffffu, mx);
         if (lane == 0) {
-            atomicMin(&rs.kmin, (unsigned long long)mn);
-            atomicMax(&rs.kmax, (unsigned long long)mx);
+            atomicMin(&rs.kmin32, mn);
+            atomicMax(&rs.kmax32, mx);
         }
     };
     if (threadIdx.x == 0) {
-        rs.kmin = ~0ull;
-        rs.kmax = 0ull;
+        rs.kmin32 = ~0u;
+        rs.kmax32 = 0u;
     }
     __syncthreads();
     range_pass(0u, ~0u, 0.0f, 0.0f, -1);
     __syncthreads();
-    unsigned int lo = (unsigned int)rs.kmin, hi = (unsigned int)rs.kmax;
+    unsigned int lo = rs.kmin32, hi = rs.kmax32;
     int need = k;
     for (int level = 0; level < 4 && lo < hi; ++level) {
         for (int i = threadIdx.x; i < 256; i += blockDim.x) rs.hist[i] = 0;
@@ -409,8 +410,8 @@ __device__ uint2 block_kth_band(Get getkey, int n, int k, RadixSmem& rs) {
                 rs.ctl[3] = rs.hist[d];
             }
             if (lane == 0) {
-                rs.kmin = ~0ull;
-                rs.kmax = 0ull;
+                rs.kmin32 = ~0u;
+                rs.kmax32 = 0u;
             }
         }
         __syncthreads();
@@ -418,8 +419,8 @@ __device__ uint2 block_kth_band(Get getkey, int n, int k, RadixSmem& rs) {
         need = rs.ctl[2];
         range_pass(lo, hi, vlo, scale, bstar);
         __syncthreads();
-        lo = (unsigned int)rs.kmin;
-        hi = (unsigned int)rs.kmax;
+        lo = rs.kmin32;
+        hi = rs.kmax32;
         if (cnt <= 64 || scale == 0.0f) break;
     }
     __syncthreads();
