@@ -72,15 +72,26 @@ def config_of(wl):
             "l2": "inputs larger than L2 (%.2f GB FP4 cache per GPU)" % (wl.B * wl.n_entries * 360 / 1e9)}
 
 
+def attn_bytes_per_query(wl):
+    """what the attention of one query must move: its k gathered FP4 rows (256 B codes + 32 B
+    scales), the window rows (bf16), the query (64 heads x 512 bf16), its k indices, and the
+    fp32 output (64 heads x 512)"""
+    return wl.k * 288 + 128 * 1024 + wl.H * 512 * 2 + wl.k * 4 + wl.H * 512 * 4
+
+
 def algorithmic_bytes(wl):
-    """bytes the indexer scan plus the gathers must move per step: per
-    sequence n_elig*72 (Full scan) + 9*2048*72 (Reindex pool keys) +
-    20*(512*288 + 128*1024) (gathered latent rows + window rows)"""
+    """bytes one step must move per sequence: the Full scan's eligible keys (n_elig x 72 B), the
+    Reindex layers' pool keys (pool x 72 B each) and every layer's attention traffic"""
     n_elig = wl.n_elig(wl.T - 1)
     n_re = sum(m == "reindex" for m in wl.layers)
-    per_seq = n_elig * 72 + n_re * wl.pool_blocks * wl.pool_block_size * 72 + len(wl.layers) * (
-        wl.k * 288 + 128 * 1024)
+    per_seq = n_elig * 72 + n_re * wl.pool_blocks * wl.pool_block_size * 72 + len(wl.layers) * attn_bytes_per_query(wl)
     return wl.B * per_seq
+
+
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture of the
+# current attention kernel (64 queries, k = 512, 64 heads); the attention moves the same bytes at any
+# context length.  Only valid while that kernel is unchanged.
+MEASURED_TRAFFIC = {"sparse_attn": 24039680 + 15360}
 
 
 # ---------------------------------------------------------------- clocks
@@ -351,13 +362,14 @@ def roofline(wl, per_op, peak, peak_kind):
     bytes_per_launch = {
         "indexer_full": wl.B * n_elig * 72,
         "reindex": wl.B * wl.pool_blocks * wl.pool_block_size * 72,
-        "sparse_attn": wl.B * (wl.k * 288 + 128 * 1024),
+        "sparse_attn": wl.B * attn_bytes_per_query(wl),
     }
     name = max((n for n in per_op if n in bytes_per_launch), key=lambda n: per_op[n]["ms"])
     t = per_op[name]["per_launch_ms"] * 1e-3
     ach = bytes_per_launch[name] / t / 1e9
+    traffic = MEASURED_TRAFFIC.get(name) if (wl.k, wl.H, wl.B) == (512, 64, 64) else None
     return {"bound": "hbm", "kernel": name, "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
-            "traffic": None, "bytes_per_launch": bytes_per_launch[name],
+            "traffic": traffic, "bytes_per_launch": bytes_per_launch[name],
             "launch_ms": per_op[name]["per_launch_ms"], "peak_kind": peak_kind}
 
 
