@@ -16,9 +16,9 @@
 // Tiles are double-buffered (L, S, P), so the gather and dequantisation of the
 // next tile overlap the MMAs and softmax of this one.  At the end the two CTAs
 // swap their per-head running max and row sum through distributed shared
-// memory, scale their partial O to the common max, and each writes half of
-// the output dims after adding the other CTA's share, passed through a
-// workspace in global memory (L2).
+// memory and scale their partial O to the common max and normaliser; each
+// stores its share of its own half of the output dims and, after a cluster
+// barrier, adds its share of the other half with reductions in L2.
 //
 // Warps: 0-7 softmax / epilogue (warp w: TMEM lane quarter w%4, key half
 // w/4), warp 8 issues the MMAs, warps 9-15 gather rows.  The query's indices
@@ -49,7 +49,6 @@ constexpr uint32_t AP_MISC = AP_RED + 1024;          // m_run[64], fac[64], flag
 constexpr uint32_t AP_DYN = AP_MISC + 3072 + 1024;
 constexpr uint32_t APT_S = 0, APT_O = 128, APT_COLS = 512;
 constexpr float AP_LAZY = 8.0f;                      // log2 headroom before the running max is raised
-constexpr size_t AP_SCRATCH = (size_t)2 * AP_H * 256 * sizeof(float);   // per query: each CTA's share for the other
 
 __device__ __forceinline__ uint32_t apswz(uint32_t row, uint32_t chunk) { return row * 128 + ((chunk ^ (row & 7)) << 4); }
 
@@ -82,8 +81,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
     const uint8_t* __restrict__ lat_codes, const uint8_t* __restrict__ lat_scales, int capacity,
     const uint16_t* __restrict__ q, int n_q, int q0, const int64_t* __restrict__ q_pos,
     const int32_t* __restrict__ idx, int k, const uint16_t* __restrict__ swa, int64_t swa_pos0, int swa_len,
-    float scale_log2e, float* __restrict__ out, float* __restrict__ lse, int* __restrict__ err,
-    float* __restrict__ scratch) {
+    float scale_log2e, float* __restrict__ out, float* __restrict__ lse, int* __restrict__ err) {
     extern __shared__ uint8_t dyn[];
     __shared__ __align__(8) unsigned long long b_lfull[2], b_lfree[2], b_sfull[2], b_sfree[2], b_pfull[2], b_odone[2];
     __shared__ uint32_t tmem_base;
@@ -468,40 +466,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
         umma::bar_named(1, AP_SMT);
         ok &= umma::mbar_wait(sa(&b_odone[(T - 1) & 1]), ((T - 1) >> 1) & 1);   // every GEMM2 is done
         umma::fence_after();
-        // this CTA's share of the peer's dims: dim tile 2*peer + half, this warp's lane quarter
+        // this CTA's share of its own half of the dims (dim tile 2*rank + half, this warp's
+        // lane quarter) is stored; the peer adds its share after the barrier
         const int qd = warp & 3, half = warp >> 2;
-        const int mt = 2 * (int)peer + half;
-        float* sc = scratch + ((gq * 2 + rank) * AP_H) * 256 + half * 128 + qd * 32 + lane;
+        const int mt = 2 * (int)rank + half;
+        float* op = out + (gq * AP_H) * D_LAT + (int)rank * 256 + half * 128 + qd * 32 + lane;
 #pragma unroll 1
         for (int c = 0; c < AP_H; c += 16) {
             float v[16];
             umma::tmem_ld16(tmem + ((uint32_t)(qd * 32) << 16) + APT_O + 64 * mt + c, v);
             umma::tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) sc[(int64_t)(c + i) * 256] = v[i] * fown[c + i];
+            for (int i = 0; i < 16; ++i) op[(int64_t)(c + i) * D_LAT] = ok ? v[i] * fown[c + i] : __int_as_float(0x7fc00000);
         }
     }
     umma::fence_before();
-    umma::cluster_sync();              // each CTA's share is in the workspace
+    umma::cluster_sync();              // both halves of the output hold one CTA's share
     if (warp < AP_SMW) {
         umma::fence_after();
+        // add this CTA's share of the peer's half (reductions in L2, nothing read back)
         const int qd = warp & 3, half = warp >> 2;
-        const int mt = 2 * (int)rank + half;
-        const int dl = half * 128 + qd * 32 + lane;                  // dim within this CTA's half
-        const float* sp = scratch + ((gq * 2 + peer) * AP_H) * 256 + dl;
-        float* op = out + (gq * AP_H) * D_LAT + (int)rank * 256 + dl;
+        const int mt = 2 * (int)peer + half;
+        float* op = out + (gq * AP_H) * D_LAT + (int)peer * 256 + half * 128 + qd * 32 + lane;
 #pragma unroll 1
         for (int c = 0; c < AP_H; c += 16) {
-            float v[16], pv[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) pv[i] = sp[(int64_t)(c + i) * 256];     // all loads before any store
+            float v[16];
             umma::tmem_ld16(tmem + ((uint32_t)(qd * 32) << 16) + APT_O + 64 * mt + c, v);
             umma::tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float o = v[i] * fown[c + i] + pv[i];
-                op[(int64_t)(c + i) * D_LAT] = ok ? o : __int_as_float(0x7fc00000);
-            }
+            for (int i = 0; i < 16; ++i) atomicAdd(op + (int64_t)(c + i) * D_LAT, ok ? v[i] * fown[c + i] : __int_as_float(0x7fc00000));
         }
     }
     if (!ok) atomicExch(err, 1);
@@ -515,7 +508,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
 
 bool attn_pair_supported(int H) { return H == AP_H; }
 
-size_t attn_pair_ws(int batch, int n_q) { return 256 + (size_t)batch * n_q * AP_SCRATCH; }
+size_t attn_pair_ws(int, int) { return 256; }
 
 cudaError_t launch_sparse_attn_pair(const csa2_cache& c, const uint16_t* q, int n_q, const int64_t* q_pos,
                                     const int32_t* idx, int k, const uint16_t* swa, int64_t swa_pos0, int swa_len,
@@ -523,14 +516,12 @@ cudaError_t launch_sparse_attn_pair(const csa2_cache& c, const uint16_t* q, int 
     cudaError_t e = cudaFuncSetAttribute(k_sparse_attn_pair, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)AP_DYN);
     if (e != cudaSuccess) return e;
     int* err = reinterpret_cast<int*>(ws);
-    float* scratch = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + 256);
     const float scale_log2e = scale * 1.4426950408889634f;
     for (int q0 = 0; q0 < n_q; q0 += 65535) {
         const int nqc = (n_q - q0) < 65535 ? (n_q - q0) : 65535;
         dim3 grid(2, nqc, c.batch);
         k_sparse_attn_pair<<<grid, AP_THREADS, AP_DYN, st>>>(c.lat_codes, c.lat_scales, c.capacity, q, n_q, q0, q_pos,
-                                                             idx, k, swa, swa_pos0, swa_len, scale_log2e, out, lse, err,
-                                                             scratch);
+                                                             idx, k, swa, swa_pos0, swa_len, scale_log2e, out, lse, err);
         note_launch();
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;

@@ -161,9 +161,7 @@ csa2_status csa2_reindex(int32_t mode, const csa2_cache* cache, const uint8_t* i
  *   out   fp32 [batch][n_q][n_heads][d_lat]
  *   lse   fp32 [batch][n_q][n_heads] or NULL
  * 1 <= n_heads <= 128, k <= 2048.
- * workspace: csa2_workspace_size(CSA2_OP_SPARSE_ATTN, ...) bytes (may be 0 for
- *   some head counts; 64 heads: 256 B + 128 KiB per query, where the two CTAs
- *   of a query pass each other their share of the output).
+ * workspace: csa2_workspace_size(CSA2_OP_SPARSE_ATTN, ...) bytes (may be 0).
  */
 csa2_status csa2_sparse_attn(const csa2_cache* cache, const uint16_t* q, int32_t n_q, int32_t n_heads,
                              const int64_t* q_pos, const int32_t* idx, int32_t k, const uint16_t* swa,
