@@ -129,43 +129,54 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
         }
         umma::fence_mbar_init();
     }
-    if (warp == 0) umma::tmem_alloc(sa(&tmem_base), APT_COLS);
-    // ---- Q: 64 heads x 512 dims, bf16 -> fp16, K-major slabs of 64 dims (A operand)
-    {
-        uint4 qv[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int i = tid + u * AP_THREADS, h = i >> 6, c = i & 63;
-            qv[u] = __ldg(reinterpret_cast<const uint4*>(q + ((gq * AP_H + h) * D_LAT + c * 8)));
-        }
-        if (warp > AP_MMAW) {
-            // the loaders stage this CTA's indices meanwhile (the round trips overlap)
-            int* sidx = reinterpret_cast<int*>(sm + AP_SIDX);
-            for (int u = tid - (AP_MMAW + 1) * 32; u < n4 * AP_TILE; u += AP_LOADERS) {
-                const int s = (2 * (u / AP_TILE) + (int)rank) * AP_TILE + u % AP_TILE;
-                if (s < k) {
-                    const int j = idx[gq * k + s];
-                    sidx[s] = (j >= 0 && j < capacity) ? j : -1;
-                }
+    // The loaders wait only for the barrier set-up (named barrier 3, with warp 0) and start on the
+    // first tile at once; warps 0-8 stage Q and the TMEM allocation among themselves (barrier 4).
+    constexpr uint32_t AP_QT = (AP_MMAW + 1) * 32;
+    if (warp == 0) {
+        __syncwarp();
+        umma::bar_arrive(3, 32 + AP_LOADERS);
+        umma::tmem_alloc(sa(&tmem_base), APT_COLS);
+    }
+    umma::cluster_arrive_relaxed();    // waited for before the first access to the peer's shared memory
+    bool ok = true;
+    uint32_t tmem = 0;
+    if (warp > AP_MMAW) {
+        umma::bar_named(3, 32 + AP_LOADERS);
+        int* sidx = reinterpret_cast<int*>(sm + AP_SIDX);
+        for (int u = tid - (int)AP_QT; u < n4 * AP_TILE; u += AP_LOADERS) {
+            const int s = (2 * (u / AP_TILE) + (int)rank) * AP_TILE + u % AP_TILE;
+            if (s < k) {
+                const int j = idx[gq * k + s];
+                sidx[s] = (j >= 0 && j < capacity) ? j : -1;
             }
         }
+        umma::bar_named(2, AP_LOADERS);
+    } else {
+        // ---- Q: 64 heads x 512 dims, bf16 -> fp16, K-major slabs of 64 dims (A operand), by warps 0-8
+        for (int u0 = 0; u0 < (AP_H * 64 + (int)AP_QT - 1) / (int)AP_QT; u0 += 8) {
+            uint4 qv[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int i = tid + u * AP_THREADS, h = i >> 6, c = i & 63;
-            const uint4 v = qv[u];
-            *reinterpret_cast<uint4*>(sm + AP_SQ + (c >> 3) * AP_QSLAB + apswz(h, c & 7)) =
-                make_uint4(ap_bf16x2_to_f16x2(v.x), ap_bf16x2_to_f16x2(v.y), ap_bf16x2_to_f16x2(v.z),
-                           ap_bf16x2_to_f16x2(v.w));
+            for (int u = 0; u < 8; ++u) {
+                const int i = tid + (u0 + u) * (int)AP_QT, h = i >> 6, c = i & 63;
+                if (i < AP_H * 64) qv[u] = __ldg(reinterpret_cast<const uint4*>(q + ((gq * AP_H + h) * D_LAT + c * 8)));
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = tid + (u0 + u) * (int)AP_QT, h = i >> 6, c = i & 63;
+                const uint4 v = qv[u];
+                if (i < AP_H * 64)
+                    *reinterpret_cast<uint4*>(sm + AP_SQ + (c >> 3) * AP_QSLAB + apswz(h, c & 7)) =
+                        make_uint4(ap_bf16x2_to_f16x2(v.x), ap_bf16x2_to_f16x2(v.y), ap_bf16x2_to_f16x2(v.z),
+                                   ap_bf16x2_to_f16x2(v.w));
+            }
         }
+        if (tid < AP_H) m_run[tid] = -INFINITY;
+        umma::fence_proxy_async();
+        umma::fence_before();
+        umma::bar_named(4, AP_QT);
+        umma::fence_after();
+        tmem = tmem_base;
     }
-    if (tid < AP_H) m_run[tid] = -INFINITY;
-    umma::fence_proxy_async();
-    umma::fence_before();
-    __syncthreads();
-    umma::cluster_arrive_relaxed();    // waited for before the first access to the peer's shared memory
-    umma::fence_after();
-    const uint32_t tmem = tmem_base;
-    bool ok = true;
 
     if (warp > AP_MMAW) {
         // ================= loaders
@@ -174,24 +185,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
         const uint8_t* codes_b = lat_codes + (int64_t)b * capacity * (D_LAT / 2);
         const uint8_t* scales_b = lat_scales + (int64_t)b * capacity * (D_LAT / 16);
         const uint16_t* win_b = swa + ((int64_t)b * swa_len + (wlo - swa_pos0)) * D_LAT;
-        // every row of the later tiles, into L2 now (called once the first tile's gathers are
-        // in flight): those gathers then hit L2
-        auto prefetch_rest = [&]() {
-            for (int u = AP_TILE + lt; u < n4 * AP_TILE; u += AP_LOADERS) {
-                const int s = (2 * (u / AP_TILE) + (int)rank) * AP_TILE + u % AP_TILE;
-                const int j = s < k ? sidx[s] : -1;
-                if (j >= 0) {
-                    umma::prefetch_l2(codes_b + (int64_t)j * (D_LAT / 2));
-                    umma::prefetch_l2(codes_b + (int64_t)j * (D_LAT / 2) + 128);
-                    umma::prefetch_l2(scales_b + (int64_t)j * (D_LAT / 16));
+        // the rows of tile t (the window for t = n4) into L2, one tile ahead of the gathers: the
+        // gathers then hit L2, and DRAM serves the tiles in the order they are needed
+        auto prefetch_tile = [&](int t) {
+            if (t < n4) {
+                for (int u = lt; u < AP_TILE; u += AP_LOADERS) {
+                    const int s = (2 * t + (int)rank) * AP_TILE + u;
+                    const int j = s < k ? sidx[s] : -1;
+                    if (j >= 0) {
+                        umma::prefetch_l2(codes_b + (int64_t)j * (D_LAT / 2));
+                        umma::prefetch_l2(codes_b + (int64_t)j * (D_LAT / 2) + 128);
+                        umma::prefetch_l2(scales_b + (int64_t)j * (D_LAT / 16));
+                    }
+                }
+            } else if (t == n4) {
+                for (int u = lt; u < AP_TILE * 8; u += AP_LOADERS) {
+                    const int r = (int)rank * AP_TILE + (u >> 3);
+                    if (r < nwin) umma::prefetch_l2(win_b + (int64_t)r * D_LAT + (u & 7) * 64);
                 }
             }
-            for (int u = lt; u < AP_TILE * 8; u += AP_LOADERS) {
-                const int r = (int)rank * AP_TILE + (u >> 3);
-                if (r < nwin) umma::prefetch_l2(win_b + (int64_t)r * D_LAT + (u & 7) * 64);
-            }
         };
-        if (n4 == 0) prefetch_rest();
+        if (n4 == 0) prefetch_tile(0);
         for (int t = 0; t < T; ++t) {
             const int buf = t & 1;
             uint8_t* L = sm + AP_SL + buf * AP_LBUF;
@@ -241,7 +255,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                         }
                     }
                 }
-                if (t == 0) prefetch_rest();
+                prefetch_tile(t + 1);
                 if (t >= 2) ok &= umma::mbar_wait(sa(&b_lfree[buf]), ((t >> 1) - 1) & 1);
 #pragma unroll
                 for (int i = 0; i < NU; ++i) {

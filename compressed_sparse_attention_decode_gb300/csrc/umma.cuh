@@ -120,6 +120,10 @@ __device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t count, bool pre
 __device__ __forceinline__ void bar_named(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+// arrive on a named barrier without waiting (the waiting threads use bar_named with the same count)
+__device__ __forceinline__ void bar_arrive(uint32_t id, uint32_t count) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 __device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 
 // the two halves of a cluster barrier, for work to go on in between
