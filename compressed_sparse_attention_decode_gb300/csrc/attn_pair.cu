@@ -21,9 +21,9 @@
 // barrier, adds its share of the other half with reductions in L2.
 //
 // Warps: 0-7 softmax / epilogue (warp w: TMEM lane quarter w%4, key half
-// w/4), warp 8 issues the MMAs, warps 9-15 gather rows.  The query's indices
-// are staged in shared memory and every row the CTA reads is prefetched into
-// L2 first, so the tile gathers are single L2 round trips.
+// w/4), warp 8 issues the MMAs, warps 9-15 gather rows.  Tile 0 is the CTA's
+// window rows (contiguous: one bulk copy); the FP4 tiles follow, their rows
+// prefetched into L2 one tile ahead, so the gathers are single L2 round trips.
 #include "common.cuh"
 #include "umma.cuh"
 
@@ -83,7 +83,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
     const int32_t* __restrict__ idx, int k, const uint16_t* __restrict__ swa, int64_t swa_pos0, int swa_len,
     float scale_log2e, float* __restrict__ out, float* __restrict__ lse, int* __restrict__ err) {
     extern __shared__ uint8_t dyn[];
-    __shared__ __align__(8) unsigned long long b_lfull[2], b_lfree[2], b_sfull[2], b_sfree[2], b_pfull[2], b_odone[2];
+    __shared__ __align__(8) unsigned long long b_lfull[2], b_lfree[2], b_sfull[2], b_sfree[2], b_pfull[2], b_odone[2],
+        b_wfull;
     __shared__ uint32_t tmem_base;
     __shared__ __align__(16) uint8_t rowok[2][AP_TILE];
 
@@ -105,6 +106,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
     int64_t whi = p;
     if (whi > swa_pos0 + swa_len - 1) whi = swa_pos0 + swa_len - 1;
     const int nwin = whi >= wlo ? (int)(whi - wlo + 1) : 0;
+    const int nwr = max(0, min(AP_TILE, nwin - (int)rank * AP_TILE));   // window rows of this CTA
     const int T4 = (k + AP_TILE - 1) / AP_TILE;
     const int n4 = (T4 + 1 - (int)rank) / 2;
     const int T = n4 + 1;
@@ -127,6 +129,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
             umma::mbar_init(sa(&b_pfull[i]), AP_SMW);
             umma::mbar_init(sa(&b_odone[i]), 1);
         }
+        umma::mbar_init(sa(&b_wfull), 1);
         umma::fence_mbar_init();
     }
     // The loaders wait only for the barrier set-up (named barrier 3, with warp 0) and start on the
@@ -142,6 +145,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
     uint32_t tmem = 0;
     if (warp > AP_MMAW) {
         umma::bar_named(3, 32 + AP_LOADERS);
+        if (tid == (int)AP_QT) {
+            // this CTA's window rows are contiguous: one bulk copy, raw bf16, into L buffer 1
+            umma::mbar_arrive_expect_tx(sa(&b_wfull), (uint32_t)nwr * 1024u);
+            if (nwr > 0)
+                umma::bulk_g2s(base + AP_SL + AP_LBUF,
+                               swa + ((int64_t)b * swa_len + (wlo - swa_pos0) + (int64_t)rank * AP_TILE) * D_LAT,
+                               (uint32_t)nwr * 1024u, sa(&b_wfull));
+        }
         int* sidx = reinterpret_cast<int*>(sm + AP_SIDX);
         for (int u = tid - (int)AP_QT; u < n4 * AP_TILE; u += AP_LOADERS) {
             const int s = (2 * (u / AP_TILE) + (int)rank) * AP_TILE + u % AP_TILE;
@@ -185,12 +196,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
         const uint8_t* codes_b = lat_codes + (int64_t)b * capacity * (D_LAT / 2);
         const uint8_t* scales_b = lat_scales + (int64_t)b * capacity * (D_LAT / 16);
         const uint16_t* win_b = swa + ((int64_t)b * swa_len + (wlo - swa_pos0)) * D_LAT;
-        // the rows of tile t (the window for t = n4) into L2, one tile ahead of the gathers: the
-        // gathers then hit L2, and DRAM serves the tiles in the order they are needed
-        auto prefetch_tile = [&](int t) {
-            if (t < n4) {
+        // the rows of FP4 tile f into L2, one tile ahead of the gathers: the gathers then hit L2,
+        // and DRAM serves the tiles in the order they are needed
+        auto prefetch_tile = [&](int f) {
+            if (f < n4)
                 for (int u = lt; u < AP_TILE; u += AP_LOADERS) {
-                    const int s = (2 * t + (int)rank) * AP_TILE + u;
+                    const int s = (2 * f + (int)rank) * AP_TILE + u;
                     const int j = s < k ? sidx[s] : -1;
                     if (j >= 0) {
                         umma::prefetch_l2(codes_b + (int64_t)j * (D_LAT / 2));
@@ -198,47 +209,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                         umma::prefetch_l2(scales_b + (int64_t)j * (D_LAT / 16));
                     }
                 }
-            } else if (t == n4) {
-                for (int u = lt; u < AP_TILE * 8; u += AP_LOADERS) {
-                    const int r = (int)rank * AP_TILE + (u >> 3);
-                    if (r < nwin) umma::prefetch_l2(win_b + (int64_t)r * D_LAT + (u & 7) * 64);
-                }
-            }
         };
-        if (n4 == 0) prefetch_tile(0);
+        prefetch_tile(0);
         for (int t = 0; t < T; ++t) {
             const int buf = t & 1;
             uint8_t* L = sm + AP_SL + buf * AP_LBUF;
-            if (t == T - 1) {
-                if (t >= 2) ok &= umma::mbar_wait(sa(&b_lfree[buf]), ((t >> 1) - 1) & 1);
-                // window rows 64*rank .. +63: 64 rows x 64 chunks of 8 dims (bf16 -> fp16), 8 loads in flight
+            if (t == 0) {
+                // tile 0 = the window rows: bf16 rows from L buffer 1 (bulk copy) to fp16 slabs in buffer 0
+                ok &= umma::mbar_wait(sa(&b_wfull), 0);
+                const uint8_t* R = sm + AP_SL + AP_LBUF;
                 for (int u0 = lt; u0 < AP_TILE * 64; u0 += AP_LOADERS * 8) {
-                    uint4 wv[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int u = u0 + i * AP_LOADERS, r = u >> 6, c = u & 63;
-                        const int wr = (int)rank * AP_TILE + r;
-                        wv[i] = make_uint4(0, 0, 0, 0);
-                        if (u < AP_TILE * 64 && wr < nwin)
-                            wv[i] = __ldg(reinterpret_cast<const uint4*>(win_b + (int64_t)wr * D_LAT + c * 8));
-                    }
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const int u = u0 + i * AP_LOADERS, r = u >> 6, c = u & 63;
                         if (u < AP_TILE * 64) {
-                            const uint4 v = wv[i];
+                            uint4 v = make_uint4(0, 0, 0, 0);
+                            if (r < nwr) v = *reinterpret_cast<const uint4*>(R + r * 1024 + c * 16);
                             *reinterpret_cast<uint4*>(L + (c >> 3) * AP_LSLAB + apswz(r, c & 7)) =
                                 make_uint4(ap_bf16x2_to_f16x2(v.x), ap_bf16x2_to_f16x2(v.y),
                                            ap_bf16x2_to_f16x2(v.z), ap_bf16x2_to_f16x2(v.w));
-                            if (c == 0) rowok[buf][r] = (int)rank * AP_TILE + r < nwin ? 1 : 0;
+                            if (c == 0) rowok[buf][r] = r < nwr ? 1 : 0;
                         }
                     }
                 }
+                umma::bar_named(2, AP_LOADERS);          // buffer 1 read in full before tile 1 overwrites it
             } else {
                 // selected FP4 rows: 64 rows x 16 units of 32 dims (16 B of codes + 2 scale bytes),
                 // fetched before waiting for the buffer so that the round trip overlaps the wait
                 constexpr int NU = (AP_TILE * 16 + AP_LOADERS - 1) / AP_LOADERS;
-                const int slot0 = (2 * t + (int)rank) * AP_TILE;
+                const int f = t - 1;                        // FP4 tile f of this CTA
+                const int slot0 = (2 * f + (int)rank) * AP_TILE;
                 uint4 cw[NU];
                 uint32_t sc[NU];
 #pragma unroll
@@ -255,7 +255,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                         }
                     }
                 }
-                prefetch_tile(t + 1);
+                prefetch_tile(f + 1);
                 if (t >= 2) ok &= umma::mbar_wait(sa(&b_lfree[buf]), ((t >> 1) - 1) & 1);
 #pragma unroll
                 for (int i = 0; i < NU; ++i) {
