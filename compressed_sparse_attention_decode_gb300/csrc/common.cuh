@@ -83,17 +83,20 @@ __device__ __forceinline__ void unpack4_signed(uint32_t nib16, uint32_t& pos, ui
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(neg) : "r"(lo), "r"(hi), "r"(nib16 ^ 0x8888u));
 }
 
-// 4 * (sum over a 16-group of q_i * k_i) for E2M1 values, exact in int32.
-// qp/qn: the query's doubled values and their negations (int8 x4 per word);
-// kp/kn: the key's words from unpack4_signed.
-__device__ __forceinline__ int group_dot4(const int* qp, const int* qn, const uint32_t* kp, const uint32_t* kn) {
+// 4 * (sum over a 16-group of q_i * k_i) for E2M1 values, exact in int32:
+// q and k as doubled values in signed int8 x4 words (|.| <= 12)
+__device__ __forceinline__ int group_dot4(const int* q, const uint32_t* k) {
     int acc = 0;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-        acc = __dp4a(qp[w], (int)kp[w], acc);
-        acc = __dp4a(qn[w], (int)kn[w], acc);
-    }
+    for (int w = 0; w < 4; ++w) acc = __dp4a(q[w], (int)k[w], acc);
     return acc;
+}
+
+// four E2M1 codes (16 bits) -> their doubled values as signed int8 x4
+__device__ __forceinline__ uint32_t unpack4_int8(uint32_t nib16) {
+    uint32_t p, n;
+    unpack4_signed(nib16, p, n);
+    return __vsub4(p, n);
 }
 
 // process-wide count of kernel launches enqueued by the library

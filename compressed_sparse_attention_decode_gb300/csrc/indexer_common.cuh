@@ -17,19 +17,17 @@ __device__ __forceinline__ int e4m3_times_512(uint32_t b) {
 
 template <int DI>
 struct QView {
-    int* qp;     // [H][DI/4] doubled E2M1 values, int8 x4
-    int* qn;     // [H][DI/4] their negations
+    int* qp;     // [H][DI/4] doubled E2M1 values, signed int8 x4
     float* qsc;  // [H][DI/16] E4M3 scales as float
     int* qsi;    // [H][DI/16] the same scales times 2^9 (integers < 2^18)
     float* w;    // [H]
     double* wd;  // [H] the weights times 2^-20 in fp64 (exact)
     // 32-bit words of one view; a multiple of 4, so consecutive views stay 16-byte aligned
-    __host__ __device__ static int head_words(int H) { return (H * (DI / 4) * 2 + 2 * H * (DI / 16) + H + 1) & ~1; }
+    __host__ __device__ static int head_words(int H) { return (H * (DI / 4) + 2 * H * (DI / 16) + H + 1) & ~1; }
     __host__ __device__ static int words(int H) { return (head_words(H) + 2 * H + 3) & ~3; }
     __device__ void bind(int* base, int H) {
         qp = base;
-        qn = qp + H * (DI / 4);
-        qsc = reinterpret_cast<float*>(qn + H * (DI / 4));
+        qsc = reinterpret_cast<float*>(qp + H * (DI / 4));
         qsi = reinterpret_cast<int*>(qsc + H * (DI / 16));
         w = reinterpret_cast<float*>(qsi + H * (DI / 16));
         wd = reinterpret_cast<double*>(base + head_words(H));
@@ -39,13 +37,7 @@ struct QView {
 template <int DI>
 __device__ void stage_query(QView<DI> v, const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
                             const float* __restrict__ w, int H, int tid, int nthr) {
-    for (int i = tid; i < H * (DI / 4); i += nthr) {
-        uint32_t nib16 = reinterpret_cast<const uint16_t*>(codes)[i];
-        uint32_t p, n;
-        unpack4_signed(nib16, p, n);
-        v.qp[i] = (int)__vsub4(p, n);
-        v.qn[i] = (int)__vsub4(n, p);
-    }
+    for (int i = tid; i < H * (DI / 4); i += nthr) v.qp[i] = (int)unpack4_int8(reinterpret_cast<const uint16_t*>(codes)[i]);
     for (int i = tid; i < H * (DI / 16); i += nthr) {
         v.qsc[i] = e4m3_to_f32(scales[i]);
         v.qsi[i] = e4m3_times_512(scales[i]);
@@ -58,7 +50,7 @@ __device__ void stage_query(QView<DI> v, const uint8_t* __restrict__ codes, cons
 
 template <int DI>
 struct KeyRow {
-    uint32_t kp[DI / 4], kn[DI / 4];
+    uint32_t kv[DI / 4];         // doubled key values, signed int8 x4
     float sk[DI / 16];
     __device__ __forceinline__ void load(const uint8_t* __restrict__ kc, const uint8_t* __restrict__ ks) {
 #pragma unroll
@@ -67,8 +59,8 @@ struct KeyRow {
             const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
-                unpack4_signed(cw[t] & 0xffffu, kp[8 * v + 2 * t], kn[8 * v + 2 * t]);
-                unpack4_signed(cw[t] >> 16, kp[8 * v + 2 * t + 1], kn[8 * v + 2 * t + 1]);
+                kv[8 * v + 2 * t] = unpack4_int8(cw[t] & 0xffffu);
+                kv[8 * v + 2 * t + 1] = unpack4_int8(cw[t] >> 16);
             }
         }
         if (DI == 128) {
@@ -94,7 +86,7 @@ __device__ __forceinline__ void approx_score(const KeyRow<DI>& k, QView<DI> q, i
         float d = 0.0f, A = 0.0f;
 #pragma unroll
         for (int g = 0; g < DI / 16; ++g) {
-            int G = group_dot4(q.qp + h * (DI / 4) + 4 * g, q.qn + h * (DI / 4) + 4 * g, k.kp + 4 * g, k.kn + 4 * g);
+            int G = group_dot4(q.qp + h * (DI / 4) + 4 * g, k.kv + 4 * g);
             float c = q.qsc[h * (DI / 16) + g] * k.sk[g] * 0.25f;   // exact
             float t = (float)G * c;                                  // exact
             d += t;
@@ -144,7 +136,7 @@ __device__ double exact_score(const uint8_t* __restrict__ kc, const uint8_t* __r
         long long D = 0;
 #pragma unroll
         for (int g = 0; g < DI / 16; ++g) {
-            const int G4 = group_dot4(q.qp + h * (DI / 4) + 4 * g, q.qn + h * (DI / 4) + 4 * g, k.kp + 4 * g, k.kn + 4 * g);
+            const int G4 = group_dot4(q.qp + h * (DI / 4) + 4 * g, k.kv + 4 * g);
             D += (long long)(G4 * q.qsi[h * (DI / 16) + g]) * ski[g];     // |G4*Sq| < 2^30
         }
         S = fma(q.wd[h], u53_to_f64(D), S);
