@@ -437,7 +437,7 @@ __global__ void __launch_bounds__(512) k_pool_bounds(const int32_t* __restrict__
 // slot's exact score, one thread per slot, blockIdx.z taking 512 slots; an
 // empty slot gets key 0, below every real score's key.
 template <int DI>
-__global__ void __launch_bounds__(512) k_pool_exact(const int32_t* __restrict__ pool, int pool_len,
+__global__ void __launch_bounds__(512, 2) k_pool_exact(const int32_t* __restrict__ pool, int pool_len,
                                                     const uint8_t* __restrict__ kc_all,
                                                     const uint8_t* __restrict__ ks_all, int capacity,
                                                     const uint8_t* __restrict__ iq_codes,
