@@ -140,16 +140,21 @@ __device__ int block_exclusive_scan(int v, int* total, int* ws) {
 // (key desc, id asc); key 0 marks a slot that holds no entry.  A band of float
 // images of the scores around the k-th (block_kth_band) splits the items into
 // sure (above the band), out (below) and the band, whose members are ranked
-// exactly by counting.  Returns the number flagged, min(k, entries).
+// exactly by counting.  The float images are computed once into key2 (viewed
+// as 32-bit words; 0 for an empty slot, which the band skips as non-finite).
+// Returns the number flagged, min(k, entries).
 __device__ int select_best_set(int n, int k, SelectSmem& sm) {
     int* flag = sm.id2;
+    unsigned int* fkey = reinterpret_cast<unsigned int*>(sm.key2);
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) sm.rs.ctl[3] = 0;
     __syncthreads();
     int c = 0;
     for (int t = threadIdx.x; t < n; t += blockDim.x) {
+        const unsigned long long u = sm.key[t];
         flag[t] = 0;
-        c += sm.key[t] != 0ull;
+        c += u != 0ull;
+        fkey[t] = u != 0ull ? f32_key((float)f64_of_key(u)) : 0u;
     }
     c = __reduce_add_sync(0xffffffffu, c);
     if (lane == 0) atomicAdd(&sm.rs.ctl[3], c);
@@ -161,10 +166,8 @@ __device__ int select_best_set(int n, int k, SelectSmem& sm) {
         return n_ent;
     }
     auto fk = [&](int t, unsigned int& key) {
-        const unsigned long long u = sm.key[t];
-        if (u == 0ull) return false;
-        key = f32_key((float)f64_of_key(u));
-        return true;
+        key = fkey[t];
+        return key != 0u;
     };
     const uint2 band = block_kth_band(fk, n, k, sm.rs);
     if (threadIdx.x == 0) {
