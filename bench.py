@@ -312,47 +312,61 @@ def step_dtype():
 
 
 def measure_ops(step, stream, reps):
-    """device time of every entry point of one step, by CUDA events around
-    each call on the launching stream (no graph), averaged over reps steps"""
+    """device time of every entry point of one step: the calls an entry point
+    makes in one step (in step order, on the step's own inputs) are captured as
+    one CUDA graph, which is replayed reps times between CUDA events on the
+    launching stream; no host launch time is inside the measurement"""
     import torch
     import compressed_sparse_attention_decode_gb300 as csa
     from compressed_sparse_attention_decode_gb300.decode import REINDEX, REUSE
-    acc = {}
+    calls = {}
 
-    def timed(name, fn):
+    def add(name, fn):
+        calls.setdefault(name, []).append(fn)
+
+    prev = None
+    t = 0
+    for l, mode in enumerate(step.layers):
+        idx_l = step.idx[l]
+        if mode == "reuse":
+            add("reuse", lambda p=prev, o=idx_l: csa.csa2_reindex(REUSE, step.cache, step.k, prev_idx=p, idx_out=o,
+                                                                   n_q=step.n_q))
+        else:
+            add("quantize_iq", lambda t=t: csa.csa2_quantize_fp4(step.iq[t], step.iq_codes, step.iq_scales))
+            if mode == "full":
+                add("indexer_full", lambda t=t, o=idx_l: csa.csa2_indexer_topk(
+                    step.cache, step.iq_codes, step.iq_scales, step.w_head[t], step.q_pos, step.k,
+                    step.pool_blocks, step.bs, idx_out=o, pool_out=step.pool, ws=step.ws_full))
+            else:
+                add("reindex", lambda t=t, o=idx_l: csa.csa2_reindex(REINDEX, step.cache, step.k, step.iq_codes,
+                                                                     step.iq_scales, step.w_head[t], step.pool,
+                                                                     idx_out=o, ws=step.ws_re))
+            t += 1
+        add("sparse_attn", lambda l=l, i=idx_l: csa.csa2_sparse_attn(step.cache, step.q[l], step.q_pos, i, step.win[l],
+                                                                     step.swa_pos0, out=step.out[l], ws=step.ws_attn))
+        prev = idx_l
+    out = {}
+    for name, fns in calls.items():
+        for fn in fns:               # eager warm-up of this entry point's calls
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for fn in fns:
+                fn()
+        g.replay()
+        torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        fn()
+        for _ in range(reps):
+            g.replay()
         b.record(stream)
-        acc.setdefault(name, []).append((a, b))
-
-    for _ in range(reps):
-        prev = None
-        t = 0
-        for l, mode in enumerate(step.layers):
-            idx_l = step.idx[l]
-            if mode == "reuse":
-                timed("reuse", lambda: csa.csa2_reindex(REUSE, step.cache, step.k, prev_idx=prev, idx_out=idx_l,
-                                                        n_q=step.n_q))
-            else:
-                timed("quantize_iq", lambda: csa.csa2_quantize_fp4(step.iq[t], step.iq_codes, step.iq_scales))
-                if mode == "full":
-                    timed("indexer_full", lambda: csa.csa2_indexer_topk(
-                        step.cache, step.iq_codes, step.iq_scales, step.w_head[t], step.q_pos, step.k,
-                        step.pool_blocks, step.bs, idx_out=idx_l, pool_out=step.pool, ws=step.ws_full))
-                else:
-                    timed("reindex", lambda: csa.csa2_reindex(REINDEX, step.cache, step.k, step.iq_codes,
-                                                              step.iq_scales, step.w_head[t], step.pool,
-                                                              idx_out=idx_l, ws=step.ws_re))
-                t += 1
-            timed("sparse_attn", lambda: csa.csa2_sparse_attn(step.cache, step.q[l], step.q_pos, idx_l, step.win[l],
-                                                              step.swa_pos0, out=step.out[l], ws=step.ws_attn))
-            prev = idx_l
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        out[name] = {"ms": ms, "per_launch_ms": ms / len(fns), "launches_per_step": len(fns)}
+        del g
+    step.run()                       # leave the step's outputs as one full step wrote them
     torch.cuda.synchronize()
-    out = {}
-    for name, evs in acc.items():
-        ts = [a.elapsed_time(b) for a, b in evs]
-        out[name] = {"ms": sum(ts) / reps, "per_launch_ms": sum(ts) / len(ts), "launches_per_step": len(ts) // reps}
     return out
 
 

@@ -241,9 +241,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                 const int slot0 = (2 * f + (int)rank) * AP_TILE;
                 uint4 cw[NU];
                 uint32_t sc[NU];
+                // unit u of the tile (row r, 32-dim unit c): a warp takes 8 rows x 4 units, so that
+                // each row's 64 B are one coalesced piece and the 8 threads of a quarter warp (8 rows,
+                // one unit) write 8 different bank groups of the swizzled slab
+                auto unit_rc = [](int u, int& r, int& c) {
+                    const int q = u >> 5, l = u & 31;
+                    r = 8 * (q & 7) + (l & 7);
+                    c = 4 * (q >> 3) + (l >> 3);
+                };
 #pragma unroll
                 for (int i = 0; i < NU; ++i) {
-                    const int u = lt + i * AP_LOADERS, r = u >> 4, c = u & 15;
+                    const int u = lt + i * AP_LOADERS;
+                    int r, c;
+                    unit_rc(u, r, c);
                     const int slot = slot0 + r;
                     cw[i] = make_uint4(0, 0, 0, 0);
                     sc[i] = 0u;
@@ -259,7 +269,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                 if (t >= 2) ok &= umma::mbar_wait(sa(&b_lfree[buf]), ((t >> 1) - 1) & 1);
 #pragma unroll
                 for (int i = 0; i < NU; ++i) {
-                    const int u = lt + i * AP_LOADERS, r = u >> 4, c = u & 15;
+                    const int u = lt + i * AP_LOADERS;
+                    int r, c;
+                    unit_rc(u, r, c);
                     if (u < AP_TILE * 16) {
                         const int slot = slot0 + r;
                         const bool valid = slot < k && sidx[slot] >= 0;
