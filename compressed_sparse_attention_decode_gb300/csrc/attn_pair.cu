@@ -21,7 +21,9 @@
 // barrier, adds its share of the other half with reductions in L2.
 //
 // Warps: 0-7 softmax / epilogue (warp w: TMEM lane quarter w%4, key half
-// w/4), warp 8 issues the MMAs, warps 9-15 gather rows.  Tile 0 is the CTA's
+// w/4), warp 8 issues the score MMAs and warp 9 the output MMAs (one issuing
+// thread issues about one MMA per 50 cycles, so the two streams get a thread
+// each), warps 10-16 gather rows.  Tile 0 is the CTA's
 // window rows (contiguous: one bulk copy); the FP4 tiles follow, their rows
 // prefetched into L2 one tile ahead, so the gathers are single L2 round trips.
 #include "common.cuh"
@@ -31,11 +33,12 @@ namespace csa2 {
 
 constexpr int AP_TILE = 64;                          // keys per tile
 constexpr int AP_H = 64;
-constexpr int AP_THREADS = 512;
+constexpr int AP_THREADS = 544;
 constexpr int AP_SMW = 8;                            // softmax warps 0-7
 constexpr int AP_SMT = AP_SMW * 32;
-constexpr int AP_MMAW = 8;                           // warp 8 issues the MMAs
-constexpr int AP_LOADERS = 224;                      // warps 9-15
+constexpr int AP_MMAW = 8;                           // warp 8 issues the score MMAs (GEMM1)
+constexpr int AP_MMA2 = 9;                           // warp 9 issues the output MMAs (GEMM2)
+constexpr int AP_LOADERS = 224;                      // warps 10-16
 constexpr uint32_t AP_QSLAB = AP_H * 128;            // 64 heads x 64 dims fp16
 constexpr uint32_t AP_LSLAB = AP_TILE * 128;         // 64 keys x 64 dims fp16
 constexpr uint32_t AP_SQ = 0;                        // Q: 8 slabs (64 KB)
@@ -134,7 +137,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
     }
     // The loaders wait only for the barrier set-up (named barrier 3, with warp 0) and start on the
     // first tile at once; warps 0-8 stage Q and the TMEM allocation among themselves (barrier 4).
-    constexpr uint32_t AP_QT = (AP_MMAW + 1) * 32;
+    constexpr uint32_t AP_QT = (AP_MMA2 + 1) * 32;
     if (warp == 0) {
         __syncwarp();
         umma::bar_arrive(3, 32 + AP_LOADERS);
@@ -143,7 +146,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
     umma::cluster_arrive_relaxed();    // waited for before the first access to the peer's shared memory
     bool ok = true;
     uint32_t tmem = 0;
-    if (warp > AP_MMAW) {
+    if (warp > AP_MMA2) {
         umma::bar_named(3, 32 + AP_LOADERS);
         if (tid == (int)AP_QT) {
             // this CTA's window rows are contiguous: one bulk copy, raw bf16, into L buffer 1
@@ -189,9 +192,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
         tmem = tmem_base;
     }
 
-    if (warp > AP_MMAW) {
+    if (warp > AP_MMA2) {
         // ================= loaders
-        const int lt = tid - (AP_MMAW + 1) * 32;
+        const int lt = tid - (int)AP_QT;
         int* sidx = reinterpret_cast<int*>(sm + AP_SIDX);
         const uint8_t* codes_b = lat_codes + (int64_t)b * capacity * (D_LAT / 2);
         const uint8_t* scales_b = lat_scales + (int64_t)b * capacity * (D_LAT / 16);
@@ -297,62 +300,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
             umma::mbar_arrive(sa(&b_lfull[buf]));
         }
     } else if (warp == AP_MMAW) {
-        // ================= MMA issuer
+        // ================= GEMM1 issuer: S^T of tile t once its rows are expanded (lfull) and
+        // the softmax has read the scores of tile t-2 out of the same TMEM buffer (sfree)
         if (lane == 0) {
             const uint32_t id1 = umma::idesc_f16(64, AP_TILE, 0, 0);
+            const uint64_t qd0 = umma::desc(base + AP_SQ, 16, 1024, umma::LAYOUT_SW128);
+            for (int t = 0; t < T && ok; ++t) {
+                const int buf = t & 1;
+                ok &= umma::mbar_wait(sa(&b_lfull[buf]), (t >> 1) & 1);
+                if (t >= 2) ok &= umma::mbar_wait(sa(&b_sfree[buf]), ((t >> 1) - 1) & 1);
+                if (!ok) break;
+                umma::fence_after();
+                const uint64_t ld0 = umma::desc(base + AP_SL + buf * AP_LBUF, 16, 1024, umma::LAYOUT_SW128);
+                // K-step ks: 16 dims at byte (ks/4) * slab + (ks%4) * 32 of both operands (Q and L
+                // slabs have the same size), i.e. a constant added to the descriptors' address field
+#pragma unroll
+                for (int ks = 0; ks < 32; ++ks) {
+                    const uint64_t off = (uint64_t)(((ks >> 2) * AP_QSLAB + (ks & 3) * 32) >> 4);
+                    umma::mma_f16(tmem + APT_S + 64 * buf, qd0 + off, ld0 + off, id1, ks > 0);
+                }
+                umma::commit(sa(&b_sfull[buf]));
+            }
+        }
+    } else if (warp == AP_MMA2) {
+        // ================= GEMM2 issuer: O^T += L^T . P of tile t once P is written (pfull);
+        // its completion releases the L buffer (lfree) and the P buffer (odone)
+        if (lane == 0) {
             const uint32_t id2 = umma::idesc_f16(128, AP_H, 1, 0);
-            // Two streams: GEMM1 of tile t needs its rows loaded (lfull) and its
-            // score buffer released (sfree of tile t-2); GEMM2 of tile t needs
-            // P (pfull).  Serve whichever is ready.
-            int n1 = 0, n2 = 0;
-            uint32_t spins = 0;
-            while (n2 < T) {
-                bool progressed = false;
-                if (n1 < T && n1 < n2 + 2) {
-                    const int buf = n1 & 1;
-                    if (umma::mbar_test(sa(&b_lfull[buf]), (n1 >> 1) & 1) &&
-                        (n1 < 2 || umma::mbar_test(sa(&b_sfree[buf]), ((n1 >> 1) - 1) & 1))) {
-                        umma::fence_after();
-                        const uint32_t Lb = base + AP_SL + buf * AP_LBUF;
+            for (int t = 0; t < T && ok; ++t) {
+                const int buf = t & 1;
+                ok &= umma::mbar_wait(sa(&b_pfull[buf]), (t >> 1) & 1);
+                if (!ok) break;
+                umma::fence_after();
+                const uint64_t la0 = umma::desc(base + AP_SL + buf * AP_LBUF, AP_LSLAB, 1024, umma::LAYOUT_SW128);
+                const uint64_t pb0 = umma::desc(base + AP_SP + buf * AP_PBUF, 16, 1024, umma::LAYOUT_SW128);
 #pragma unroll
-                        for (int ks = 0; ks < 32; ++ks) {
-                            const uint64_t a = umma::desc(base + AP_SQ + (ks >> 2) * AP_QSLAB + (ks & 3) * 32, 16,
-                                                          1024, umma::LAYOUT_SW128);
-                            const uint64_t bl = umma::desc(Lb + (ks >> 2) * AP_LSLAB + (ks & 3) * 32, 16, 1024,
-                                                           umma::LAYOUT_SW128);
-                            umma::mma_f16(tmem + APT_S + 64 * buf, a, bl, id1, ks > 0);
-                        }
-                        umma::commit(sa(&b_sfull[buf]));
-                        ++n1;
-                        progressed = true;
+                for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint64_t offa = (uint64_t)(((2 * mt) * AP_LSLAB + ks * 2048) >> 4);
+                        const uint64_t offp = (uint64_t)((ks * 32) >> 4);
+                        umma::mma_f16(tmem + APT_O + 64 * mt, la0 + offa, pb0 + offp, id2, (t > 0 || ks > 0) ? 1u : 0u);
                     }
                 }
-                if (n2 < n1 && umma::mbar_test(sa(&b_pfull[n2 & 1]), (n2 >> 1) & 1)) {
-                    umma::fence_after();
-                    const int buf = n2 & 1;
-                    const uint32_t Lb = base + AP_SL + buf * AP_LBUF;
-                    const uint32_t Pb = base + AP_SP + buf * AP_PBUF;
-#pragma unroll 1
-                    for (int mt = 0; mt < 4; ++mt) {
-#pragma unroll
-                        for (int ks = 0; ks < 4; ++ks) {
-                            const uint64_t a = umma::desc(Lb + (2 * mt) * AP_LSLAB + ks * 2048, AP_LSLAB, 1024,
-                                                          umma::LAYOUT_SW128);
-                            const uint64_t bp = umma::desc(Pb + ks * 32, 16, 1024, umma::LAYOUT_SW128);
-                            umma::mma_f16(tmem + APT_O + 64 * mt, a, bp, id2, (n2 > 0 || ks > 0) ? 1u : 0u);
-                        }
-                    }
-                    umma::commit(sa(&b_odone[buf]));
-                    umma::commit(sa(&b_lfree[buf]));
-                    ++n2;
-                    progressed = true;
-                }
-                if (progressed) {
-                    spins = 0;
-                } else if (++spins > (1u << 26)) {     // nothing moved for far too long: give up
-                    ok = false;
-                    break;
-                }
+                umma::commit(sa(&b_odone[buf]));
+                umma::commit(sa(&b_lfree[buf]));
             }
         }
     } else {
