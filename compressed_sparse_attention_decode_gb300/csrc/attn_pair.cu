@@ -21,9 +21,11 @@
 // barrier, adds its share of the other half with reductions in L2.
 //
 // Warps: 0-7 softmax / epilogue (warp w: TMEM lane quarter w%4, key half
-// w/4), warp 8 issues the score MMAs and warp 9 the output MMAs (one issuing
-// thread issues about one MMA per 50 cycles, so the two streams get a thread
-// each), warps 10-16 gather rows.  Tile 0 is the CTA's
+// w/4), warps 8 and 9 issue the score MMAs (K = dims 0-255 and 256-511 into
+// two TMEM partials that the softmax adds; the first half starts as soon as
+// its dims are expanded) and warp 10 the output MMAs: one thread issues about
+// one MMA per 50 cycles, so the streams get a thread each.  Warps 11-17 gather
+// rows.  Tile 0 is the CTA's
 // window rows (contiguous: one bulk copy); the FP4 tiles follow, their rows
 // prefetched into L2 one tile ahead, so the gathers are single L2 round trips.
 #include "common.cuh"
@@ -33,12 +35,12 @@ namespace csa2 {
 
 constexpr int AP_TILE = 64;                          // keys per tile
 constexpr int AP_H = 64;
-constexpr int AP_THREADS = 544;
+constexpr int AP_THREADS = 576;
 constexpr int AP_SMW = 8;                            // softmax warps 0-7
 constexpr int AP_SMT = AP_SMW * 32;
-constexpr int AP_MMAW = 8;                           // warp 8 issues the score MMAs (GEMM1)
-constexpr int AP_MMA2 = 9;                           // warp 9 issues the output MMAs (GEMM2)
-constexpr int AP_LOADERS = 224;                      // warps 10-16
+constexpr int AP_MMAW = 8;                           // warps 8, 9 issue the score MMAs (GEMM1), dims 0-255 / 256-511
+constexpr int AP_MMA2 = 10;                          // warp 10 issues the output MMAs (GEMM2)
+constexpr int AP_LOADERS = 224;                      // warps 11-17
 constexpr uint32_t AP_QSLAB = AP_H * 128;            // 64 heads x 64 dims fp16
 constexpr uint32_t AP_LSLAB = AP_TILE * 128;         // 64 keys x 64 dims fp16
 constexpr uint32_t AP_SQ = 0;                        // Q: 8 slabs (64 KB)
@@ -50,7 +52,7 @@ constexpr uint32_t AP_SIDX = AP_SP + 2 * AP_PBUF;    // the query's indices, MAX
 constexpr uint32_t AP_RED = AP_SIDX + MAX_K * 4;     // per key half x 64 heads (max, then row sums)
 constexpr uint32_t AP_MISC = AP_RED + 1024;          // m_run[64], fac[64], flags[8], own m/l, peer m/l, scale
 constexpr uint32_t AP_DYN = AP_MISC + 3072 + 1024;
-constexpr uint32_t APT_S = 0, APT_O = 128, APT_COLS = 512;
+constexpr uint32_t APT_S = 0, APT_O = 256, APT_COLS = 512;   // S^T partial p of buffer b at APT_S + 64 (2b + p)
 constexpr float AP_LAZY = 8.0f;                      // log2 headroom before the running max is raised
 
 __device__ __forceinline__ uint32_t apswz(uint32_t row, uint32_t chunk) { return row * 128 + ((chunk ^ (row & 7)) << 4); }
@@ -86,8 +88,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
     const int32_t* __restrict__ idx, int k, const uint16_t* __restrict__ swa, int64_t swa_pos0, int swa_len,
     float scale_log2e, float* __restrict__ out, float* __restrict__ lse, int* __restrict__ err) {
     extern __shared__ uint8_t dyn[];
-    __shared__ __align__(8) unsigned long long b_lfull[2], b_lfree[2], b_sfull[2], b_sfree[2], b_pfull[2], b_odone[2],
-        b_wfull;
+    __shared__ __align__(8) unsigned long long b_lhalf[2], b_lfull[2], b_lfree[2], b_sfull[2], b_sfree[2], b_pfull[2],
+        b_odone[2], b_wfull;
     __shared__ uint32_t tmem_base;
     __shared__ __align__(16) uint8_t rowok[2][AP_TILE];
 
@@ -125,9 +127,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
     auto sa = [&](const void* x) { return umma::smem_u32(x); };
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
-            umma::mbar_init(sa(&b_lfull[i]), AP_LOADERS);
+            umma::mbar_init(sa(&b_lhalf[i]), AP_LOADERS);     // dims 0-255 of the tile expanded
+            umma::mbar_init(sa(&b_lfull[i]), AP_LOADERS);     // all of it
             umma::mbar_init(sa(&b_lfree[i]), 1);
-            umma::mbar_init(sa(&b_sfull[i]), 1);
+            umma::mbar_init(sa(&b_sfull[i]), 2);              // both K halves of the scores
             umma::mbar_init(sa(&b_sfree[i]), AP_SMW);
             umma::mbar_init(sa(&b_pfull[i]), AP_SMW);
             umma::mbar_init(sa(&b_odone[i]), 1);
@@ -236,6 +239,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                     }
                 }
                 umma::bar_named(2, AP_LOADERS);          // buffer 1 read in full before tile 1 overwrites it
+                umma::fence_proxy_async();
+                umma::mbar_arrive(sa(&b_lhalf[buf]));
             } else {
                 // selected FP4 rows: 64 rows x 16 units of 32 dims (16 B of codes + 2 scale bytes),
                 // fetched before waiting for the buffer so that the round trip overlaps the wait
@@ -270,12 +275,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                 }
                 prefetch_tile(f + 1);
                 if (t >= 2) ok &= umma::mbar_wait(sa(&b_lfree[buf]), ((t >> 1) - 1) & 1);
+                // units u < 512 hold dims 0-255 (c < 8): expanded first, so that the first half of
+                // the score MMAs can start while the second half is expanded
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
                 for (int i = 0; i < NU; ++i) {
                     const int u = lt + i * AP_LOADERS;
                     int r, c;
                     unit_rc(u, r, c);
-                    if (u < AP_TILE * 16) {
+                    if (u < AP_TILE * 16 && (u >= AP_TILE * 8) == (hf == 1)) {
                         const int slot = slot0 + r;
                         const bool valid = slot < k && sidx[slot] >= 0;
                         const uint32_t words[4] = {cw[i].x, cw[i].y, cw[i].z, cw[i].w};
@@ -295,19 +304,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                         if (c == 0) rowok[buf][r] = valid ? 1 : 0;
                     }
                 }
+                if (hf == 0) {
+                    umma::fence_proxy_async();
+                    umma::mbar_arrive(sa(&b_lhalf[buf]));
+                }
+                }
             }
             umma::fence_proxy_async();
             umma::mbar_arrive(sa(&b_lfull[buf]));
         }
-    } else if (warp == AP_MMAW) {
-        // ================= GEMM1 issuer: S^T of tile t once its rows are expanded (lfull) and
-        // the softmax has read the scores of tile t-2 out of the same TMEM buffer (sfree)
+    } else if (warp == AP_MMAW || warp == AP_MMAW + 1) {
+        // ================= GEMM1 issuers: warp 8 + p takes dims 256p .. 256p+255 of S^T of tile t
+        // into its own TMEM partial once those dims are expanded (lhalf / lfull) and the softmax
+        // has read the scores of tile t-2 out of the same buffer (sfree)
         if (lane == 0) {
+            const int part = warp - AP_MMAW;
             const uint32_t id1 = umma::idesc_f16(64, AP_TILE, 0, 0);
             const uint64_t qd0 = umma::desc(base + AP_SQ, 16, 1024, umma::LAYOUT_SW128);
+            unsigned long long* ready = part == 0 ? b_lhalf : b_lfull;
             for (int t = 0; t < T && ok; ++t) {
                 const int buf = t & 1;
-                ok &= umma::mbar_wait(sa(&b_lfull[buf]), (t >> 1) & 1);
+                ok &= umma::mbar_wait(sa(&ready[buf]), (t >> 1) & 1);
                 if (t >= 2) ok &= umma::mbar_wait(sa(&b_sfree[buf]), ((t >> 1) - 1) & 1);
                 if (!ok) break;
                 umma::fence_after();
@@ -315,9 +332,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                 // K-step ks: 16 dims at byte (ks/4) * slab + (ks%4) * 32 of both operands (Q and L
                 // slabs have the same size), i.e. a constant added to the descriptors' address field
 #pragma unroll
-                for (int ks = 0; ks < 32; ++ks) {
+                for (int kk = 0; kk < 16; ++kk) {
+                    const int ks = 16 * part + kk;
                     const uint64_t off = (uint64_t)(((ks >> 2) * AP_QSLAB + (ks & 3) * 32) >> 4);
-                    umma::mma_f16(tmem + APT_S + 64 * buf, qd0 + off, ld0 + off, id1, ks > 0);
+                    umma::mma_f16(tmem + APT_S + 64 * (2 * buf + part), qd0 + off, ld0 + off, id1, kk > 0);
                 }
                 umma::commit(sa(&b_sfull[buf]));
             }
@@ -361,8 +379,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
             float x[16];                     // keys 32*half + par + 2i
             ok &= umma::mbar_wait(sa(&b_sfull[buf]), (t >> 1) & 1);
             umma::fence_after();
-            umma::tmem_ld16x64b_x16(lane_base + APT_S + 64 * buf + 32 * half, x);
-            umma::tmem_wait_ld();
+            {
+                float x1[16];
+                umma::tmem_ld16x64b_x16(lane_base + APT_S + 64 * (2 * buf) + 32 * half, x);
+                umma::tmem_ld16x64b_x16(lane_base + APT_S + 64 * (2 * buf + 1) + 32 * half, x1);
+                umma::tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) x[i] += x1[i];
+            }
             umma::fence_before();
             __syncwarp();
             if (lane == 0) umma::mbar_arrive(sa(&b_sfree[buf]));
