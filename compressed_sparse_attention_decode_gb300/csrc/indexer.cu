@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(256) k_scan_full(const uint8_t* __restrict__ k
 
 struct SelectSmem {
     RadixSmem rs;
-    int whist[16 * 256];          // per-warp radix histograms (up to 512 threads)
+    __align__(16) int whist[16 * 256];   // per-warp radix histograms (up to 512 threads)
     unsigned long long key[MAX_K];
     int id[MAX_K];
     unsigned long long* key2;     // merge buffers, MAX_K each (dynamic shared memory)
@@ -104,6 +104,20 @@ constexpr size_t SEL_BITMAP_BYTES = SEL_BITMAP_BITS / 8;
 // the double whose order-preserving key (f64_key) is u
 __device__ __forceinline__ double f64_of_key(unsigned long long u) {
     return __longlong_as_double((long long)((u & 0x8000000000000000ull) ? (u & 0x7fffffffffffffffull) : ~u));
+}
+
+// An order-preserving 32-bit image of the double whose key (f64_key) is u:
+// the double truncated to float precision by integer operations.  Truncation
+// of the magnitude is monotone in the value, so a larger double never gets a
+// smaller image; magnitudes below the smallest normal float map to the image
+// of zero, above the largest finite float to that float.
+__device__ __forceinline__ uint32_t f32_image_of_key(unsigned long long u) {
+    const unsigned long long b = (u & 0x8000000000000000ull) ? (u & 0x7fffffffffffffffull) : ~u;
+    const uint32_t sgn = (uint32_t)(b >> 63);
+    const int e = (int)((b >> 52) & 0x7ffu) - (1023 - 127);
+    if (e <= 0) return 0x80000000u;
+    const uint32_t mag = e > 254 ? 0x7f7fffffu : ((uint32_t)e << 23) | (uint32_t)((b >> 29) & 0x7fffffu);
+    return sgn ? ~mag : (mag | 0x80000000u);
 }
 
 // exclusive prefix sum of v over the block; *total gets the sum.  ws: 65 ints
@@ -147,17 +161,35 @@ __device__ int select_best_set(int n, int k, SelectSmem& sm) {
     int* flag = sm.id2;
     unsigned int* fkey = reinterpret_cast<unsigned int*>(sm.key2);
     const int lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) sm.rs.ctl[3] = 0;
+    if (threadIdx.x == 0) {
+        sm.rs.ctl[3] = 0;
+        sm.rs.kmin32 = ~0u;
+        sm.rs.kmax32 = 0u;
+    }
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) sm.rs.hist[i] = 0;
     __syncthreads();
+    // one pass: images, the number of entries and the range of their images
     int c = 0;
+    unsigned int mn = ~0u, mx = 0u;
     for (int t = threadIdx.x; t < n; t += blockDim.x) {
         const unsigned long long u = sm.key[t];
         flag[t] = 0;
-        c += u != 0ull;
-        fkey[t] = u != 0ull ? f32_key((float)f64_of_key(u)) : 0u;
+        const unsigned int f = u != 0ull ? f32_image_of_key(u) : 0u;
+        fkey[t] = f;
+        if (u != 0ull) {
+            ++c;
+            mn = min(mn, f);
+            mx = max(mx, f);
+        }
     }
     c = __reduce_add_sync(0xffffffffu, c);
-    if (lane == 0) atomicAdd(&sm.rs.ctl[3], c);
+    mn = __reduce_min_sync(0xffffffffu, mn);
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if (lane == 0) {
+        atomicAdd(&sm.rs.ctl[3], c);
+        atomicMin(&sm.rs.kmin32, mn);
+        atomicMax(&sm.rs.kmax32, mx);
+    }
     __syncthreads();
     const int n_ent = sm.rs.ctl[3];
     if (n_ent <= k) {
@@ -169,12 +201,16 @@ __device__ int select_best_set(int n, int k, SelectSmem& sm) {
         key = fkey[t];
         return key != 0u;
     };
-    const uint2 band = block_kth_band(fk, n, k, sm.rs);
+    const uint2 band = block_kth_band_from(fk, n, k, sm.rs.kmin32, sm.rs.kmax32, sm.rs);
     if (threadIdx.x == 0) {
         sm.rs.ctl[0] = 0;
         sm.rs.ctl[3] = 0;
     }
     __syncthreads();
+    // above the band: in; in the band: listed with (key, id, slot), contiguously in the
+    // per-warp histogram space (idle here) when they fit, else by slot only
+    uint4* bl = reinterpret_cast<uint4*>(sm.whist);
+    constexpr int BL_CAP = (int)(sizeof(sm.whist) / sizeof(uint4));
     int above = 0;
     for (int t0 = 0; t0 < n; t0 += blockDim.x) {
         const int t = t0 + threadIdx.x;
@@ -189,23 +225,46 @@ __device__ int select_best_set(int n, int k, SelectSmem& sm) {
             }
         }
         const int pos = append_slot(inband, &sm.rs.ctl[0]);
-        if (inband) sm.din[pos] = t;
+        if (inband) {
+            sm.din[pos] = t;
+            if (pos < BL_CAP) {
+                const unsigned long long key = sm.key[t];
+                bl[pos] = make_uint4((unsigned int)key, (unsigned int)(key >> 32), (unsigned int)sm.id[t], (unsigned int)t);
+            }
+        }
     }
     above = __reduce_add_sync(0xffffffffu, above);
     if (lane == 0) atomicAdd(&sm.rs.ctl[3], above);
     __syncthreads();
+    // exact rank of each band member among the band by (key desc, id asc); the r best are in
     const int nb = sm.rs.ctl[0], r = k - sm.rs.ctl[3];
-    for (int i = threadIdx.x; i < nb; i += blockDim.x) {
-        const int t = sm.din[i];
-        const unsigned long long key = sm.key[t];
-        const int id = sm.id[t];
-        int rank = 0;
-        for (int j = 0; j < nb; ++j) {
-            const int tj = sm.din[j];
-            const unsigned long long kj = sm.key[tj];
-            rank += (kj > key) || (kj == key && sm.id[tj] < id);
+    if (nb <= BL_CAP) {
+        for (int i = threadIdx.x; i < nb; i += blockDim.x) {
+            const uint4 me = bl[i];
+            const unsigned long long key = ((unsigned long long)me.y << 32) | me.x;
+            const int id = (int)me.z;
+            int rank = 0;
+#pragma unroll 4
+            for (int j = 0; j < nb; ++j) {
+                const uint4 o = bl[j];
+                const unsigned long long kj = ((unsigned long long)o.y << 32) | o.x;
+                rank += (kj > key) || (kj == key && (int)o.z < id);
+            }
+            flag[me.w] = rank < r;
         }
-        flag[t] = rank < r;
+    } else {
+        for (int i = threadIdx.x; i < nb; i += blockDim.x) {
+            const int t = sm.din[i];
+            const unsigned long long key = sm.key[t];
+            const int id = sm.id[t];
+            int rank = 0;
+            for (int j = 0; j < nb; ++j) {
+                const int tj = sm.din[j];
+                const unsigned long long kj = sm.key[tj];
+                rank += (kj > key) || (kj == key && sm.id[tj] < id);
+            }
+            flag[t] = rank < r;
+        }
     }
     __syncthreads();
     return k;
@@ -335,14 +394,19 @@ __device__ void sort_kept(int n, bool by_key, SelectSmem& sm) {
 
 // The distinct ids ids[t] (t < n) with flags[t] != 0 (flags == nullptr: all),
 // all in [0, id_bound), written to dst[0..cnt) in ascending order; returns cnt.
+// bitmap_clear: the caller has zeroed the bitmap's first ceil(id_bound / 32)
+// words, with a block barrier since.
 // Through a bitmap of id_bound bits and a block prefix sum over its words when
 // that fits SEL_BITMAP_BITS, else by sort_kept.  dst must not alias ids.
-__device__ int ascending_ids(const int* ids, const int* flags, int n, int id_bound, int* dst, SelectSmem& sm) {
+__device__ int ascending_ids(const int* ids, const int* flags, int n, int id_bound, int* dst, SelectSmem& sm,
+                             bool bitmap_clear = false) {
     int total;
     if (id_bound <= SEL_BITMAP_BITS) {
         const int W = (id_bound + 31) >> 5;
-        for (int w = threadIdx.x; w < W; w += blockDim.x) sm.bitmap[w] = 0u;
-        __syncthreads();
+        if (!bitmap_clear) {
+            for (int w = threadIdx.x; w < W; w += blockDim.x) sm.bitmap[w] = 0u;
+            __syncthreads();
+        }
         for (int t = threadIdx.x; t < n; t += blockDim.x)
             if (!flags || flags[t]) {
                 const int id = ids[t];
@@ -486,9 +550,12 @@ __global__ void __launch_bounds__(512) k_pool_rank(const int32_t* __restrict__ p
         sm.key[t] = ok ? keys[gq * pool_len + t] : 0ull;
         sm.id[t] = ok ? j : 0;
     }
+    const bool clear = capacity <= SEL_BITMAP_BITS;      // the bitmap of ascending_ids, zeroed meanwhile
+    if (clear)
+        for (int w = threadIdx.x; w < (capacity + 31) >> 5; w += blockDim.x) sm.bitmap[w] = 0u;
     __syncthreads();
     select_best_set(pool_len, k, sm);
-    const int kept = ascending_ids(sm.id, sm.id2, pool_len, capacity, sm.din, sm);
+    const int kept = ascending_ids(sm.id, sm.id2, pool_len, capacity, sm.din, sm, clear);
     int32_t* out = idx_out + gq * k;
     for (int t = threadIdx.x; t < k; t += blockDim.x) out[t] = t < kept ? sm.din[t] : -1;
 }

@@ -319,46 +319,19 @@ __device__ __forceinline__ float key_value(unsigned int k) {
 // (an empty slot's -inf) stay below every bucket.  Used where the caller only
 // filters with it: even buckets spread the shared-memory atomics (one
 // histogram for the block), and the refinement keeps the band to a few dozen keys.
+// The band search from a known range: lo / hi are the smallest and largest
+// finite keys taking part, rs.hist is zero and a block barrier has passed since
+// both were set.  Each level is three block phases: histogram, scan (warp 0),
+// then the range of the chosen bucket (which also clears the histogram for the
+// next level).
 template <typename Get>
-__device__ uint2 block_kth_band(Get getkey, int n, int k, RadixSmem& rs) {
+__device__ uint2 block_kth_band_from(Get getkey, int n, int k, unsigned int lo, unsigned int hi, RadixSmem& rs) {
     const int lane = threadIdx.x & 31;
     auto bucket_of = [](unsigned int key, float vlo, float scale) {
         return min((int)((key_value(key) - vlo) * scale), 255);
     };
-    // min / max of the finite keys in [lo, hi] whose bucket is bsel (bsel < 0: all of them)
-    auto range_pass = [&](unsigned int lo, unsigned int hi, float vlo, float scale, int bsel) {
-        unsigned int mn = ~0u, mx = 0u;
-        for (int t0 = threadIdx.x; t0 < n; t0 += 8 * blockDim.x) {
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int t = t0 + u * blockDim.x;
-                unsigned int key;
-                if (t < n && getkey(t, key) && key >= lo && key <= hi && isfinite(key_value(key)) &&
-                    (bsel < 0 || bucket_of(key, vlo, scale) == bsel)) {
-                    mn = min(mn, key);
-                    mx = max(mx, key);
-                }
-            }
-        }
-        mn = __reduce_min_sync(0xffffffffu, mn);
-        mx = __reduce_max_sync(0xffffffffu, mx);
-        if (lane == 0) {
-            atomicMin(&rs.kmin32, mn);
-            atomicMax(&rs.kmax32, mx);
-        }
-    };
-    if (threadIdx.x == 0) {
-        rs.kmin32 = ~0u;
-        rs.kmax32 = 0u;
-    }
-    __syncthreads();
-    range_pass(0u, ~0u, 0.0f, 0.0f, -1);
-    __syncthreads();
-    unsigned int lo = rs.kmin32, hi = rs.kmax32;
     int need = k;
     for (int level = 0; level < 4 && lo < hi; ++level) {
-        for (int i = threadIdx.x; i < 256; i += blockDim.x) rs.hist[i] = 0;
-        __syncthreads();
         const float vlo = key_value(lo);
         float scale = 256.0f / (key_value(hi) - vlo);
         if (!(scale > 0.0f && scale < INFINITY)) scale = 0.0f;       // degenerate range: one bucket
@@ -409,7 +382,27 @@ __device__ uint2 block_kth_band(Get getkey, int n, int k, RadixSmem& rs) {
         __syncthreads();
         const int bstar = rs.ctl[1], cnt = rs.ctl[3];
         need = rs.ctl[2];
-        range_pass(lo, hi, vlo, scale, bstar);
+        for (int i = threadIdx.x; i < 256; i += blockDim.x) rs.hist[i] = 0;
+        // min / max of the keys of bucket bstar
+        unsigned int mn = ~0u, mx = 0u;
+        for (int t0 = threadIdx.x; t0 < n; t0 += 8 * blockDim.x) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int t = t0 + u * blockDim.x;
+                unsigned int key;
+                if (t < n && getkey(t, key) && key >= lo && key <= hi && isfinite(key_value(key)) &&
+                    bucket_of(key, vlo, scale) == bstar) {
+                    mn = min(mn, key);
+                    mx = max(mx, key);
+                }
+            }
+        }
+        mn = __reduce_min_sync(0xffffffffu, mn);
+        mx = __reduce_max_sync(0xffffffffu, mx);
+        if (lane == 0) {
+            atomicMin(&rs.kmin32, mn);
+            atomicMax(&rs.kmax32, mx);
+        }
         __syncthreads();
         lo = rs.kmin32;
         hi = rs.kmax32;
@@ -417,6 +410,49 @@ __device__ uint2 block_kth_band(Get getkey, int n, int k, RadixSmem& rs) {
     }
     __syncthreads();
     return make_uint2(lo, hi);
+}
+
+// A band [lo, hi] of keys that holds the k-th largest of the keys
+// (order-preserving images of finite floats, 1 <= k <= number of finite ones
+// taking part): every key above hi is among the k largest, every key below lo
+// is not.  The value range of the keys is
+// cut into 256 buckets of equal width in value (the bucket index never
+// decreases as the value grows, so every key of a higher bucket is larger);
+// the bucket holding the k-th largest is found from the top; while it still
+// holds more than 64 keys its own range is cut again (at most four levels).
+// The band is the smallest and largest key of the last bucket.  Non-finite keys
+// (an empty slot's -inf) stay below every bucket.  Used where the caller only
+// filters with it: even buckets spread the shared-memory atomics (one
+// histogram for the block), and the refinement keeps the band to a few dozen keys.
+template <typename Get>
+__device__ uint2 block_kth_band(Get getkey, int n, int k, RadixSmem& rs) {
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        rs.kmin32 = ~0u;
+        rs.kmax32 = 0u;
+    }
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) rs.hist[i] = 0;
+    __syncthreads();
+    unsigned int mn = ~0u, mx = 0u;
+    for (int t0 = threadIdx.x; t0 < n; t0 += 8 * blockDim.x) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int t = t0 + u * blockDim.x;
+            unsigned int key;
+            if (t < n && getkey(t, key) && isfinite(key_value(key))) {
+                mn = min(mn, key);
+                mx = max(mx, key);
+            }
+        }
+    }
+    mn = __reduce_min_sync(0xffffffffu, mn);
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if (lane == 0) {
+        atomicMin(&rs.kmin32, mn);
+        atomicMax(&rs.kmax32, mx);
+    }
+    __syncthreads();
+    return block_kth_band_from(getkey, n, k, rs.kmin32, rs.kmax32, rs);
 }
 
 // the band's lower end (a key <= the k-th largest) or upper end (>= it)

@@ -160,7 +160,8 @@ csa2_status csa2_reindex(int32_t mode, const csa2_cache* cache, const uint8_t* i
  *         window of a query is clipped to the rows present
  *   out   fp32 [batch][n_q][n_heads][d_lat]
  *   lse   fp32 [batch][n_q][n_heads] or NULL
- * 1 <= n_heads <= 128, k <= 2048.
+ * 1 <= n_heads <= 128, k <= 2048.  q, swa and out 16-byte aligned, q_pos 8, idx
+ * and lse 4 (CSA2_ERR_INVALID_ARG otherwise).
  * workspace: csa2_workspace_size(CSA2_OP_SPARSE_ATTN, ...) bytes (may be 0).
  */
 csa2_status csa2_sparse_attn(const csa2_cache* cache, const uint16_t* q, int32_t n_q, int32_t n_heads,
