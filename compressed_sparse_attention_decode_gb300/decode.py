@@ -98,6 +98,20 @@ class DecodeStep:
                              lse=None if self.lse is None else self.lse[l], ws=self.ws_attn, stream=stream)
             prev = idx_l
 
+    def twin(self):
+        """a second step over the same cache, intermediates and workspaces with
+        its own inputs (iq, w_head, q, win, q_pos) and outputs (idx, out, lse),
+        so that one step's copies can overlap the other's compute; the two must
+        not run concurrently on the device"""
+        t = object.__new__(DecodeStep)
+        t.__dict__.update(self.__dict__)
+        for name in ("iq", "w_head", "q", "win", "q_pos", "idx", "out"):
+            setattr(t, name, getattr(self, name).clone())
+        if self.lse is not None:
+            t.lse = self.lse.clone()
+        t.graph = None
+        return t
+
     def capture(self):
         """record one step as a CUDA graph (replayed by run())"""
         s = torch.cuda.Stream()

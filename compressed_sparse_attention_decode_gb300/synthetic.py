@@ -31,16 +31,35 @@ def seq_view(cache, b):
 
 
 class HostInputs:
-    """pinned host copies of one step's inputs (for the end-to-end timing)"""
+    """pinned host copies of one step's inputs (for the end-to-end timing).
+
+    The per-step inputs are the queries of every layer (q, iq, w_head), the
+    query positions and, for the sliding window, only the newest row of every
+    (layer, sequence): the window is device-resident KV state to which a
+    decode step appends one row, like the compressed cache itself."""
 
     def __init__(self, step):
         pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-        self.names = ["iq", "w_head", "q", "win", "q_pos"] + (["h_chunk", "kraw_chunk"] if step.chunk_len else [])
+        self.names = ["iq", "w_head", "q", "q_pos"] + (["h_chunk", "kraw_chunk"] if step.chunk_len else [])
         self.host = {n: pin(getattr(step, n)) for n in self.names}
+        self.win_new = pin(step.win[:, :, -1])
+        self.win_dev = {}
         self.out = pin(step.out)
 
+    def copy_in(self, step):
+        """enqueue this step's host -> device copies on the current stream (the
+        newest window rows land in a contiguous device buffer, then in place)"""
+        for n in self.names:
+            getattr(step, n).copy_(self.host[n], non_blocking=True)
+        key = id(step)
+        if key not in self.win_dev:
+            self.win_dev[key] = torch.empty(self.win_new.shape, dtype=self.win_new.dtype, device=step.win.device)
+        self.win_dev[key].copy_(self.win_new, non_blocking=True)
+        step.win[:, :, -1].copy_(self.win_dev[key])
+
     def h2d_bytes(self):
-        return sum(t.numel() * t.element_size() for t in self.host.values())
+        return sum(t.numel() * t.element_size() for t in self.host.values()) + \
+            self.win_new.numel() * self.win_new.element_size()
 
     def d2h_bytes(self):
         return self.out.numel() * self.out.element_size()
