@@ -87,6 +87,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
     const uint16_t* __restrict__ q, int n_q, int q0, const int64_t* __restrict__ q_pos,
     const int32_t* __restrict__ idx, int k, const uint16_t* __restrict__ swa, int64_t swa_pos0, int swa_len,
     float scale_log2e, float* __restrict__ out, float* __restrict__ lse, int* __restrict__ err) {
+    pdl_launch_next();
+    pdl_wait();
     extern __shared__ uint8_t dyn[];
     __shared__ __align__(8) unsigned long long b_lhalf[2], b_lfull[2], b_lfree[2], b_sfull[2], b_sfree[2], b_pfull[2],
         b_odone[2], b_wfull;
@@ -562,7 +564,7 @@ cudaError_t launch_sparse_attn_pair(const csa2_cache& c, const uint16_t* q, int 
     for (int q0 = 0; q0 < n_q; q0 += 65535) {
         const int nqc = (n_q - q0) < 65535 ? (n_q - q0) : 65535;
         dim3 grid(2, nqc, c.batch);
-        k_sparse_attn_pair<<<grid, AP_THREADS, AP_DYN, st>>>(c.lat_codes, c.lat_scales, c.capacity, q, n_q, q0, q_pos,
+        launch_k(k_sparse_attn_pair, grid, AP_THREADS, AP_DYN, st, c.lat_codes, c.lat_scales, c.capacity, q, n_q, q0, q_pos,
                                                              idx, k, swa, swa_pos0, swa_len, scale_log2e, out, lse, err);
         note_launch();
         e = cudaGetLastError();

@@ -36,6 +36,8 @@ __global__ void __launch_bounds__(256) k_sparse_attn_simt(
     const uint16_t* __restrict__ q, int n_q, int H, const int64_t* __restrict__ q_pos, const int32_t* __restrict__ idx,
     int k, const uint16_t* __restrict__ swa, int64_t swa_pos0, int swa_len, float scale, float* __restrict__ out,
     float* __restrict__ lse) {
+    pdl_launch_next();
+    pdl_wait();
     extern __shared__ float sm[];
     float* qs = sm;                                  // [8][512]
     float* tile = qs + SIMT_HEADS * D_LAT;           // [32][512]
@@ -140,7 +142,7 @@ cudaError_t launch_sparse_attn_simt(const csa2_cache& c, const uint16_t* q, int 
     cudaError_t e = cudaFuncSetAttribute(k_sparse_attn_simt, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((H + SIMT_HEADS - 1) / SIMT_HEADS, n_q, c.batch);
-    k_sparse_attn_simt<<<grid, 256, smem, st>>>(c.lat_codes, c.lat_scales, c.capacity, q, n_q, H, q_pos, idx, k, swa,
+    launch_k(k_sparse_attn_simt, grid, 256, smem, st, c.lat_codes, c.lat_scales, c.capacity, q, n_q, H, q_pos, idx, k, swa,
                                                 swa_pos0, swa_len, scale, out, lse);
     note_launch();
     return cudaGetLastError();

@@ -75,6 +75,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sparse_attn_tc(
     const uint16_t* __restrict__ q, int n_q, int q0, int H, const int64_t* __restrict__ q_pos,
     const int32_t* __restrict__ idx, int k, const uint16_t* __restrict__ swa, int64_t swa_pos0, int swa_len,
     float scale_log2e, int n_tiles, float* __restrict__ part_o, float2* __restrict__ part_ml, int* __restrict__ err) {
+    pdl_launch_next();
+    pdl_wait();
     extern __shared__ uint8_t dyn[];
     __shared__ __align__(8) unsigned long long mbar;
     __shared__ uint32_t tmem_base;
@@ -307,6 +309,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sparse_attn_tc(
 __global__ void __launch_bounds__(128) k_attn_combine(const float* __restrict__ part_o,
                                                       const float2* __restrict__ part_ml, int n_q, int q0, int H,
                                                       int n_tiles, float* __restrict__ out, float* __restrict__ lse) {
+    pdl_launch_next();
+    pdl_wait();
     const int h = blockIdx.x, ql = blockIdx.y, b = blockIdx.z;
     const int nqc = gridDim.y;
     const int64_t s0 = ((int64_t)b * nqc + ql) * n_tiles;
@@ -359,13 +363,13 @@ cudaError_t launch_sparse_attn_tc(const csa2_cache& c, const uint16_t* q, int n_
     for (int q0 = 0; q0 < n_q; q0 += qc) {
         const int nqc = (n_q - q0) < qc ? (n_q - q0) : qc;
         dim3 g1(n_tiles * (H / HG), nqc, c.batch);
-        kern<<<g1, TC_THREADS, SM_DYN, st>>>(c.lat_codes, c.lat_scales, c.capacity, q, n_q, q0, H, q_pos, idx, k,
+        launch_k(kern, g1, TC_THREADS, SM_DYN, st, c.lat_codes, c.lat_scales, c.capacity, q, n_q, q0, H, q_pos, idx, k,
                                              swa, swa_pos0, swa_len, scale_log2e, n_tiles, part_o, part_ml, err);
         note_launch();
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         dim3 g2(H, nqc, c.batch);
-        k_attn_combine<<<g2, 128, 0, st>>>(part_o, part_ml, n_q, q0, H, n_tiles, out, lse);
+        launch_k(k_attn_combine, g2, 128, 0, st, part_o, part_ml, n_q, q0, H, n_tiles, out, lse);
         note_launch();
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;

@@ -17,6 +17,8 @@ __global__ void __launch_bounds__(256) k_cache_write(uint8_t* __restrict__ lat_c
                                                      int64_t entry0, int n_ent, const float* __restrict__ w0,
                                                      const float* __restrict__ w1,
                                                      const uint16_t* __restrict__ ikey_raw) {
+    pdl_launch_next();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int i = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int b = blockIdx.y;
@@ -70,6 +72,8 @@ __global__ void __launch_bounds__(256) k_cache_write(uint8_t* __restrict__ lat_c
 // one thread per 16-value group
 __global__ void __launch_bounds__(256) k_quantize_fp4(const float* __restrict__ x, int64_t n_groups,
                                                       uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+    pdl_launch_next();
+    pdl_wait();
     int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (g >= n_groups) return;
     float v[16];
@@ -91,7 +95,7 @@ cudaError_t launch_cache_write(const csa2_cache& c, const uint16_t* h, int64_t e
                                const float* w1, const uint16_t* ikey_raw, cudaStream_t st) {
     if (n_ent == 0) return cudaSuccess;
     dim3 grid((n_ent + 7) / 8, c.batch);
-    k_cache_write<<<grid, 256, 0, st>>>(c.lat_codes, c.lat_scales, c.ikey_codes, c.ikey_scales, c.capacity, c.d_idx,
+    launch_k(k_cache_write, grid, 256, 0, st, c.lat_codes, c.lat_scales, c.ikey_codes, c.ikey_scales, c.capacity, c.d_idx,
                                         h, entry0, n_ent, w0, w1, ikey_raw);
     note_launch();
     return cudaGetLastError();
@@ -101,7 +105,7 @@ cudaError_t launch_quantize_fp4(const float* x, int64_t n_rows, int d, uint8_t* 
                                 cudaStream_t st) {
     int64_t n_groups = n_rows * (d / 16);
     if (n_groups == 0) return cudaSuccess;
-    k_quantize_fp4<<<(unsigned)((n_groups + 255) / 256), 256, 0, st>>>(x, n_groups, codes, scales);
+    launch_k(k_quantize_fp4, (unsigned)((n_groups + 255) / 256), 256, 0, st, x, n_groups, codes, scales);
     note_launch();
     return cudaGetLastError();
 }

@@ -9,6 +9,31 @@
 
 namespace csa2 {
 
+// ---------------------------------------------------------------- launches
+// Every kernel of the library is launched with programmatic stream
+// serialisation: the next kernel in the stream may be scheduled while this one
+// still runs (each kernel lets its successor in as it starts), and waits at its
+// top until its predecessor has completed and that grid's memory is visible.
+// Outside such a launch both instructions do nothing.
+__device__ __forceinline__ void pdl_launch_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                            Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 constexpr int D_LAT = 512;
 constexpr int WINDOW = 128;
 constexpr int MAX_K = 2048;

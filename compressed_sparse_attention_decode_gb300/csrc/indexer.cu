@@ -34,6 +34,8 @@ __global__ void __launch_bounds__(256) k_scan_full(const uint8_t* __restrict__ k
                                                    int* __restrict__ counts, int* __restrict__ cid,
                                                    float2* __restrict__ clu, int* __restrict__ bid,
                                                    float2* __restrict__ blu, int list_len) {
+    pdl_launch_next();
+    pdl_wait();
     extern __shared__ int smem[];
     __shared__ RadixSmem rs;
     const int b = blockIdx.z;
@@ -479,6 +481,8 @@ __global__ void __launch_bounds__(512) k_pool_bounds(const int32_t* __restrict__
                                                      const uint8_t* __restrict__ iq_scales,
                                                      const float* __restrict__ w_head, int n_q, int H,
                                                      float2* __restrict__ lu) {
+    pdl_launch_next();
+    pdl_wait();
     extern __shared__ int qsm[];
     const int ql = blockIdx.x, b = blockIdx.y;
     const int64_t gq = (int64_t)b * n_q + ql;
@@ -511,6 +515,8 @@ __global__ void __launch_bounds__(512, 2) k_pool_exact(const int32_t* __restrict
                                                     const uint8_t* __restrict__ iq_scales,
                                                     const float* __restrict__ w_head, int n_q, int H,
                                                     unsigned long long* __restrict__ keys) {
+    pdl_launch_next();
+    pdl_wait();
     extern __shared__ int qsm[];
     const int ql = blockIdx.x, b = blockIdx.y;
     const int64_t gq = (int64_t)b * n_q + ql;
@@ -536,6 +542,8 @@ __global__ void __launch_bounds__(512, 2) k_pool_exact(const int32_t* __restrict
 __global__ void __launch_bounds__(512) k_pool_rank(const int32_t* __restrict__ pool, int pool_len,
                                                    const unsigned long long* __restrict__ keys, int capacity, int k,
                                                    int32_t* __restrict__ idx_out) {
+    pdl_launch_next();
+    pdl_wait();
     extern __shared__ unsigned long long sdyn[];
     __shared__ SelectSmem sm;
     const int64_t gq = (int64_t)blockIdx.y * gridDim.x + blockIdx.x;
@@ -576,6 +584,8 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
                                                 int32_t* __restrict__ pool_out, const int32_t* __restrict__ bid,
                                                 const float2* __restrict__ blu, int* __restrict__ c2id,
                                                 unsigned long long* __restrict__ c2key) {
+    pdl_launch_next();
+    pdl_wait();
     extern __shared__ int qsm[];
     __shared__ SelectSmem sm;
     const int b = blockIdx.y, ql = blockIdx.x;
@@ -804,6 +814,8 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
 
 // Reuse: the latest indices, unchanged ("DeepSeek-v4.1 Flash" §2.3.2)
 __global__ void k_copy_idx(const int32_t* __restrict__ src, int32_t* __restrict__ dst, int64_t n) {
+    pdl_launch_next();
+    pdl_wait();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i < n) dst[i] = src[i];
 }
@@ -889,7 +901,7 @@ cudaError_t launch_indexer_full_t(const csa2_cache& c, const uint8_t* iq_codes, 
                                     w.counts, w.ids, w.lu, w.bid, w.blu, (int)list_len, w.err, st);
         } else {
             dim3 g1((c.capacity + E - 1) / E, (n_qc + QB - 1) / QB, c.batch);
-            k_scan_full<DI><<<g1, 256, smem1, st>>>(c.ikey_codes, c.ikey_scales, c.capacity, iq_codes, iq_scales,
+            launch_k(k_scan_full<DI>, g1, 256, smem1, st, c.ikey_codes, c.ikey_scales, c.capacity, iq_codes, iq_scales,
                                                     w_head, q_pos, n_q, q0, n_qc, H, QB, E, k, pool_blocks, bs,
                                                     w.counts, w.ids, w.lu, w.bid, w.blu, (int)list_len);
             note_launch();
@@ -900,7 +912,7 @@ cudaError_t launch_indexer_full_t(const csa2_cache& c, const uint8_t* iq_codes, 
         const size_t smem2 = qwords + SEL_DYN_EXTRA + SEL_BITMAP_BYTES;
         e = cudaFuncSetAttribute(k_select<DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
         if (e != cudaSuccess) return e;
-        k_select<DI><<<g2, 512, smem2, st>>>(w.ids, w.lu, w.counts, 0, (int)list_len, c.ikey_codes, c.ikey_scales,
+        launch_k(k_select<DI>, g2, 512, smem2, st, w.ids, w.lu, w.counts, 0, (int)list_len, c.ikey_codes, c.ikey_scales,
                                               c.capacity, iq_codes, iq_scales, w_head, q_pos, n_q, q0, n_qc, H, k,
                                               idx_out, pool_blocks, bs, pool_out, w.bid, w.blu, w.c2id, w.c2key);
         note_launch();
@@ -919,7 +931,7 @@ cudaError_t launch_reindex_t(const csa2_cache& c, const uint8_t* iq_codes, const
     dim3 g0(n_q, c.batch, (pool_len + 511) / 512);
     if (pool_len <= MAX_K) {
         // small pool: exact scores for every slot, then one sort per query
-        k_pool_exact<DI><<<g0, 512, qwords, st>>>(pool, pool_len, c.ikey_codes, c.ikey_scales, c.capacity, iq_codes,
+        launch_k(k_pool_exact<DI>, g0, 512, qwords, st, pool, pool_len, c.ikey_codes, c.ikey_scales, c.capacity, iq_codes,
                                                    iq_scales, w_head, n_q, H, w.c2key);
         note_launch();
         cudaError_t e = cudaGetLastError();
@@ -927,11 +939,11 @@ cudaError_t launch_reindex_t(const csa2_cache& c, const uint8_t* iq_codes, const
         const size_t smr = SEL_DYN_EXTRA + SEL_BITMAP_BYTES;
         e = cudaFuncSetAttribute(k_pool_rank, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smr);
         if (e != cudaSuccess) return e;
-        k_pool_rank<<<dim3(n_q, c.batch), 512, smr, st>>>(pool, pool_len, w.c2key, c.capacity, k, idx_out);
+        launch_k(k_pool_rank, dim3(n_q, c.batch), 512, smr, st, pool, pool_len, w.c2key, c.capacity, k, idx_out);
         note_launch();
         return cudaGetLastError();
     }
-    k_pool_bounds<DI><<<g0, 512, qwords, st>>>(pool, pool_len, c.ikey_codes, c.ikey_scales, c.capacity, iq_codes,
+    launch_k(k_pool_bounds<DI>, g0, 512, qwords, st, pool, pool_len, c.ikey_codes, c.ikey_scales, c.capacity, iq_codes,
                                                 iq_scales, w_head, n_q, H, w.lu);
     note_launch();
     cudaError_t e = cudaGetLastError();
@@ -940,7 +952,7 @@ cudaError_t launch_reindex_t(const csa2_cache& c, const uint8_t* iq_codes, const
     e = cudaFuncSetAttribute(k_select<DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 g(n_q, c.batch);
-    k_select<DI><<<g, 512, smem, st>>>(pool, w.lu, nullptr, pool_len, pool_len, c.ikey_codes, c.ikey_scales,
+    launch_k(k_select<DI>, g, 512, smem, st, pool, w.lu, nullptr, pool_len, pool_len, c.ikey_codes, c.ikey_scales,
                                        c.capacity, iq_codes, iq_scales, w_head, nullptr, n_q, 0, n_q, H, k, idx_out, 0,
                                        1, nullptr, nullptr, nullptr, w.c2id, w.c2key);
     note_launch();
@@ -967,7 +979,7 @@ cudaError_t launch_reindex(const csa2_cache& c, const uint8_t* iq_codes, const u
 
 cudaError_t launch_reuse(const int32_t* prev, int32_t* out, int64_t n, cudaStream_t st) {
     if (n == 0) return cudaSuccess;
-    k_copy_idx<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(prev, out, n);
+    launch_k(k_copy_idx, (unsigned)((n + 255) / 256), 256, 0, st, prev, out, n);
     note_launch();
     return cudaGetLastError();
 }

@@ -49,6 +49,7 @@ __global__ void __launch_bounds__(256, 2) k_scan_full_tc(
     const int64_t* __restrict__ q_pos, int n_q, int q0, int n_qc, int H, int k, int pool_blocks, int bs,
     int* __restrict__ counts, int* __restrict__ cid, float2* __restrict__ clu, int* __restrict__ bid,
     float2* __restrict__ blu, int list_len, int* __restrict__ err) {
+    pdl_wait();             // the selection that follows is let in only as the scan's blocks exit
     extern __shared__ uint8_t dyn[];
     __shared__ RadixSmem rs;
     __shared__ __align__(8) unsigned long long bar_rfull[ITC_NR], bar_rfree[ITC_NR], bar_afull[ITC_NA], bar_afree[ITC_NA],
@@ -246,7 +247,7 @@ cudaError_t launch_scan_full_tc(const csa2_cache& c, const uint8_t* iq_codes, co
     cudaError_t e = cudaFuncSetAttribute(k_scan_full_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)IS_DYN);
     if (e != cudaSuccess) return e;
     dim3 grid((c.capacity + ITC_E - 1) / ITC_E, n_qc, c.batch);
-    k_scan_full_tc<<<grid, 256, IS_DYN, st>>>(c.ikey_codes, c.ikey_scales, c.capacity, iq_codes, iq_scales, w_head,
+    launch_k(k_scan_full_tc, grid, 256, IS_DYN, st, c.ikey_codes, c.ikey_scales, c.capacity, iq_codes, iq_scales, w_head,
                                               q_pos, n_q, q0, n_qc, H, k, pool_blocks, bs, counts, cid, clu, bid, blu,
                                               list_len, err);
     note_launch();
