@@ -87,8 +87,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
     const uint16_t* __restrict__ q, int n_q, int q0, const int64_t* __restrict__ q_pos,
     const int32_t* __restrict__ idx, int k, const uint16_t* __restrict__ swa, int64_t swa_pos0, int swa_len,
     float scale_log2e, float* __restrict__ out, float* __restrict__ lse, int* __restrict__ err) {
+    // Programmatic launch: everything up to the indices (Q, the window rows and their tile, the
+    // TMEM and barrier set-up) overlaps the preceding kernel; only the loaders wait for it, before
+    // they read idx.  Nothing this kernel writes is read by that kernel.
     pdl_launch_next();
-    pdl_wait();
     extern __shared__ uint8_t dyn[];
     __shared__ __align__(8) unsigned long long b_lhalf[2], b_lfull[2], b_lfree[2], b_sfull[2], b_sfree[2], b_pfull[2],
         b_odone[2], b_wfull;
@@ -161,6 +163,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                                swa + ((int64_t)b * swa_len + (wlo - swa_pos0) + (int64_t)rank * AP_TILE) * D_LAT,
                                (uint32_t)nwr * 1024u, sa(&b_wfull));
         }
+        {
+            // tile 0 = the window rows: bf16 rows from L buffer 1 (bulk copy) to fp16 slabs in buffer 0
+            const int lt = tid - (int)AP_QT;
+            ok &= umma::mbar_wait(sa(&b_wfull), 0);
+            const uint8_t* R = sm + AP_SL + AP_LBUF;
+            uint8_t* L = sm + AP_SL;
+            for (int u0 = lt; u0 < AP_TILE * 64; u0 += AP_LOADERS * 8) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int u = u0 + i * AP_LOADERS, r = u >> 6, c = u & 63;
+                    if (u < AP_TILE * 64) {
+                        uint4 v = make_uint4(0, 0, 0, 0);
+                        if (r < nwr) v = *reinterpret_cast<const uint4*>(R + r * 1024 + c * 16);
+                        *reinterpret_cast<uint4*>(L + (c >> 3) * AP_LSLAB + apswz(r, c & 7)) =
+                            make_uint4(ap_bf16x2_to_f16x2(v.x), ap_bf16x2_to_f16x2(v.y), ap_bf16x2_to_f16x2(v.z),
+                                       ap_bf16x2_to_f16x2(v.w));
+                        if (c == 0) rowok[0][r] = r < nwr ? 1 : 0;
+                    }
+                }
+            }
+            umma::fence_proxy_async();
+            umma::mbar_arrive(sa(&b_lhalf[0]));
+            umma::mbar_arrive(sa(&b_lfull[0]));
+        }
+        // the indices are the preceding kernel's output
+        pdl_wait();
         int* sidx = reinterpret_cast<int*>(sm + AP_SIDX);
         for (int u = tid - (int)AP_QT; u < n4 * AP_TILE; u += AP_LOADERS) {
             const int s = (2 * (u / AP_TILE) + (int)rank) * AP_TILE + u % AP_TILE;
@@ -169,7 +197,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                 sidx[s] = (j >= 0 && j < capacity) ? j : -1;
             }
         }
-        umma::bar_named(2, AP_LOADERS);
+        umma::bar_named(2, AP_LOADERS);          // sidx staged; buffer 1 read in full before tile 1 overwrites it
     } else {
         // ---- Q: 64 heads x 512 dims, bf16 -> fp16, K-major slabs of 64 dims (A operand), by warps 0-8
         for (int u0 = 0; u0 < (AP_H * 64 + (int)AP_QT - 1) / (int)AP_QT; u0 += 8) {
@@ -203,7 +231,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
         int* sidx = reinterpret_cast<int*>(sm + AP_SIDX);
         const uint8_t* codes_b = lat_codes + (int64_t)b * capacity * (D_LAT / 2);
         const uint8_t* scales_b = lat_scales + (int64_t)b * capacity * (D_LAT / 16);
-        const uint16_t* win_b = swa + ((int64_t)b * swa_len + (wlo - swa_pos0)) * D_LAT;
         // the rows of FP4 tile f into L2, one tile ahead of the gathers: the gathers then hit L2,
         // and DRAM serves the tiles in the order they are needed
         auto prefetch_tile = [&](int f) {
@@ -219,31 +246,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                 }
         };
         prefetch_tile(0);
-        for (int t = 0; t < T; ++t) {
+        for (int t = 1; t < T; ++t) {
             const int buf = t & 1;
             uint8_t* L = sm + AP_SL + buf * AP_LBUF;
-            if (t == 0) {
-                // tile 0 = the window rows: bf16 rows from L buffer 1 (bulk copy) to fp16 slabs in buffer 0
-                ok &= umma::mbar_wait(sa(&b_wfull), 0);
-                const uint8_t* R = sm + AP_SL + AP_LBUF;
-                for (int u0 = lt; u0 < AP_TILE * 64; u0 += AP_LOADERS * 8) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int u = u0 + i * AP_LOADERS, r = u >> 6, c = u & 63;
-                        if (u < AP_TILE * 64) {
-                            uint4 v = make_uint4(0, 0, 0, 0);
-                            if (r < nwr) v = *reinterpret_cast<const uint4*>(R + r * 1024 + c * 16);
-                            *reinterpret_cast<uint4*>(L + (c >> 3) * AP_LSLAB + apswz(r, c & 7)) =
-                                make_uint4(ap_bf16x2_to_f16x2(v.x), ap_bf16x2_to_f16x2(v.y),
-                                           ap_bf16x2_to_f16x2(v.z), ap_bf16x2_to_f16x2(v.w));
-                            if (c == 0) rowok[buf][r] = r < nwr ? 1 : 0;
-                        }
-                    }
-                }
-                umma::bar_named(2, AP_LOADERS);          // buffer 1 read in full before tile 1 overwrites it
-                umma::fence_proxy_async();
-                umma::mbar_arrive(sa(&b_lhalf[buf]));
-            } else {
+            {
                 // selected FP4 rows: 64 rows x 16 units of 32 dims (16 B of codes + 2 scale bytes),
                 // fetched before waiting for the buffer so that the round trip overlaps the wait
                 constexpr int NU = (AP_TILE * 16 + AP_LOADERS - 1) / AP_LOADERS;
