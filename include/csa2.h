@@ -35,10 +35,9 @@
  *     the stream produced.  Before that wait it reads only caller inputs that
  *     no kernel of this library writes (the queries q and their positions
  *     q_pos, the window rows swa, the values to quantise x); a caller that
- *     writes those with a kernel of
- *     its own that itself lets its successor start early must make that
- *     kernel complete first.  Kernels not launched this way (any caller
- *     kernel by default) are waited for as usual.
+ *     writes those with a kernel of its own that itself lets its successor
+ *     start early must make that kernel complete first.  Kernels not launched
+ *     this way (any caller kernel by default) are waited for as usual.
  */
 #ifndef CSA2_H
 #define CSA2_H
