@@ -475,32 +475,45 @@ __device__ __forceinline__ int append_slot(bool flag, int* ctr) {
 
 
 // Block-wide append of the items i in [0, n) with flag(i) to a list in global
-// memory whose length counter is *gctr: the block counts its items, reserves
-// them with ONE global atomic, then places them (put(slot, i)) at positions
-// taken from a shared-memory counter.  Every thread of the block calls it;
-// rs.ctl[4] must be 0 on entry and is 0 again on return.
+// memory whose length counter is *gctr: the block counts its items per warp,
+// reserves them with ONE global atomic, then every warp places its items
+// (put(slot, i)) in order from its own offset, by ballots (no atomics).
+// Every thread of the block calls it; rs.hist serves as scratch (the band
+// searches clear it before use).
 template <typename Flag, typename Put>
 __device__ void block_append_global(int n, Flag flag, Put put, int* gctr, RadixSmem& rs) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     int c = 0;
-    for (int i = threadIdx.x; i < n; i += blockDim.x) c += flag(i) ? 1 : 0;
+    for (int i0 = 0; i0 < n; i0 += blockDim.x) {
+        const int i = i0 + threadIdx.x;
+        c += (i < n && flag(i)) ? 1 : 0;
+    }
     c = __reduce_add_sync(0xffffffffu, c);
-    if ((threadIdx.x & 31) == 0 && c) atomicAdd(&rs.ctl[4], c);
+    if (lane == 0) rs.hist[warp] = c;
     __syncthreads();
-    if (threadIdx.x == 0) {
-        const int tot = rs.ctl[4];
-        rs.ctl[5] = tot ? atomicAdd(gctr, tot) : 0;
-        rs.ctl[4] = 0;
+    if (warp == 0) {
+        const int v = lane < nw ? rs.hist[lane] : 0;
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const int tot = __shfl_sync(0xffffffffu, incl, 31);
+        int g = 0;
+        if (lane == 0 && tot) g = atomicAdd(gctr, tot);
+        g = __shfl_sync(0xffffffffu, g, 0);
+        if (lane < nw) rs.hist[32 + lane] = g + incl - v;
     }
     __syncthreads();
-    const int g = rs.ctl[5];
-    for (int base = 0; base < n; base += blockDim.x) {
-        const int i = base + threadIdx.x;
+    int pos = rs.hist[32 + warp];
+    for (int i0 = 0; i0 < n; i0 += blockDim.x) {
+        const int i = i0 + threadIdx.x;
         const bool f = i < n && flag(i);
-        const int pos = append_slot(f, &rs.ctl[4]);
-        if (f) put(g + pos, i);
+        const unsigned m = __ballot_sync(0xffffffffu, f);
+        if (f) put(pos + __popc(m & ((1u << lane) - 1u)), i);
+        pos += __popc(m);
     }
-    __syncthreads();
-    if (threadIdx.x == 0) rs.ctl[4] = 0;
     __syncthreads();
 }
 
