@@ -91,7 +91,7 @@ def algorithmic_bytes(wl):
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture of the
 # current attention kernel (64 queries, k = 512, 64 heads); the attention moves the same bytes at any
 # context length.  Only valid while that kernel is unchanged.
-MEASURED_TRAFFIC = {"sparse_attn": 24052224 + 512}
+MEASURED_TRAFFIC = {"sparse_attn": 24050432 + 512}
 
 
 # ---------------------------------------------------------------- clocks
