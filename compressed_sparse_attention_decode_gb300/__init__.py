@@ -6,7 +6,7 @@ PyTorch supplies device memory and the current stream.  There is no CPU
 fallback: if the library is not built, every call raises.
 
 Entry points (same names as the C ABI):
-    csa2_cache_write, csa2_quantize_fp4, csa2_indexer_topk, csa2_reindex,
+    csa2_cache_write, csa2_quantize_fp4, csa2_indexer_topk, csa2_reindex, csa2_reindex_f32,
     csa2_sparse_attn, csa2_workspace_size
 plus ``Cache``, which owns the four cache planes as torch tensors.
 """
@@ -40,7 +40,7 @@ class _CacheStruct(ctypes.Structure):
 _lib = None
 EXPORTS = ("csa2_cache_write", "csa2_quantize_fp4", "csa2_indexer_topk", "csa2_reindex", "csa2_sparse_attn",
            "csa2_workspace_size", "csa2_status_string", "csa2_abi_version", "csa2_launch_count",
-           "csa2_reindex_noalloc")
+           "csa2_reindex_noalloc", "csa2_reindex_f32")
 
 
 def load(path=None):
@@ -58,6 +58,7 @@ def load(path=None):
     lib.csa2_quantize_fp4.argtypes = [vp, i64, i32, vp, vp, vp]
     lib.csa2_indexer_topk.argtypes = [cp, vp, vp, vp, i32, vp, i32, i32, vp, i32, i32, vp, vp, sz, vp]
     lib.csa2_reindex.argtypes = [i32, cp, vp, vp, vp, i32, i32, vp, i32, vp, i32, vp, vp, sz, vp]
+    lib.csa2_reindex_f32.argtypes = [cp, vp, vp, i32, i32, vp, i32, i32, vp, vp, sz, vp]
     lib.csa2_sparse_attn.argtypes = [cp, vp, i32, i32, vp, vp, i32, vp, i64, i32, ctypes.c_float, vp, vp, vp, sz, vp]
     lib.csa2_reindex_noalloc.argtypes = [cp, vp, vp, vp, i32, i32, vp, i32, i32, vp, vp]
     lib.csa2_reindex_noalloc.restype = ctypes.c_int
@@ -67,7 +68,8 @@ def load(path=None):
     lib.csa2_status_string.restype = ctypes.c_char_p
     lib.csa2_abi_version.restype = i32
     lib.csa2_launch_count.restype = i64
-    for name in ("csa2_cache_write", "csa2_quantize_fp4", "csa2_indexer_topk", "csa2_reindex", "csa2_sparse_attn"):
+    for name in ("csa2_cache_write", "csa2_quantize_fp4", "csa2_indexer_topk", "csa2_reindex", "csa2_reindex_f32",
+                 "csa2_sparse_attn"):
         getattr(lib, name).restype = ctypes.c_int
     if path is None:
         _lib = lib
@@ -185,6 +187,23 @@ def csa2_reindex(mode, cache, k, iq_codes=None, iq_scales=None, w_head=None, poo
                              _ptr(pool), pool_len, _ptr(prev_idx), k, _ptr(idx_out), _ptr(ws),
                              ws.numel() if ws is not None else 0, _stream(stream))
     _check(st, "csa2_reindex")
+    return idx_out
+
+
+def csa2_reindex_f32(cache, k, iq, w_head, pool, idx_out=None, ws=None, stream=None):
+    """Reindex from fp32 indexer queries iq [B, n_q, H, d_idx]: the query
+    quantisation runs inside the Reindex kernels (same results as
+    csa2_quantize_fp4 followed by csa2_reindex)."""
+    B, n_q, H = iq.shape[0], iq.shape[1], iq.shape[2]
+    if idx_out is None:
+        idx_out = torch.empty((B, n_q, k), dtype=torch.int32, device=iq.device)
+    pool_len = pool.shape[-1]
+    if ws is None:
+        ws = workspace(OP_REINDEX, cache.batch, n_q, H, k, pool_len, iq.device)
+    c = cache.struct()
+    st = load().csa2_reindex_f32(ctypes.byref(c), _ptr(iq), _ptr(w_head), n_q, H, _ptr(pool), pool_len, k,
+                                 _ptr(idx_out), _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "csa2_reindex_f32")
     return idx_out
 
 

@@ -13,9 +13,9 @@ cudaError_t launch_quantize_fp4(const float* x, int64_t n_rows, int d, uint8_t* 
 cudaError_t launch_indexer_full(const csa2_cache& c, const uint8_t* iq_codes, const uint8_t* iq_scales,
                                 const float* w_head, int n_q, const int64_t* q_pos, int H, int k, int32_t* idx_out,
                                 int pool_blocks, int bs, int32_t* pool_out, void* ws, cudaStream_t st);
-cudaError_t launch_reindex(const csa2_cache& c, const uint8_t* iq_codes, const uint8_t* iq_scales, const float* w_head,
-                           int n_q, int H, const int32_t* pool, int pool_len, int k, int32_t* idx_out, void* ws,
-                           cudaStream_t st);
+cudaError_t launch_reindex(const csa2_cache& c, const uint8_t* iq_codes, const uint8_t* iq_scales, const float* iq_raw,
+                           const float* w_head, int n_q, int H, const int32_t* pool, int pool_len, int k,
+                           int32_t* idx_out, void* ws, cudaStream_t st);
 cudaError_t launch_reuse(const int32_t* prev, int32_t* out, int64_t n, cudaStream_t st);
 cudaError_t launch_sparse_attn(const csa2_cache& c, const uint16_t* q, int n_q, int H, const int64_t* q_pos,
                                const int32_t* idx, int k, const uint16_t* swa, int64_t swa_pos0, int swa_len,
@@ -143,7 +143,22 @@ csa2_status csa2_reindex(int32_t mode, const csa2_cache* cache, const uint8_t* i
     if (n_heads < 1 || n_heads > MAX_IDX_HEADS || pool_len < 1 || pool_len > 16384) return CSA2_ERR_INVALID_ARG;
     size_t need = reindex_ws(cache->batch, n_q, pool_len);
     if (!workspace || ws_bytes < need || !aligned(workspace, 16)) return CSA2_ERR_WORKSPACE;
-    return from_cuda(launch_reindex(*cache, iq_codes, iq_scales, w_head, n_q, n_heads, pool, pool_len, k, idx_out,
+    return from_cuda(launch_reindex(*cache, iq_codes, iq_scales, nullptr, w_head, n_q, n_heads, pool, pool_len, k, idx_out,
+                                    workspace, (cudaStream_t)stream));
+}
+
+csa2_status csa2_reindex_f32(const csa2_cache* cache, const float* iq, const float* w_head, int32_t n_q,
+                             int32_t n_heads, const int32_t* pool, int32_t pool_len, int32_t k, int32_t* idx_out,
+                             void* workspace, size_t ws_bytes, void* stream) {
+    csa2_status s = check_cache(cache, true);
+    if (s != CSA2_OK) return s;
+    if (n_q < 1 || k < 1 || k > MAX_K || !idx_out || !aligned(idx_out, 4)) return CSA2_ERR_INVALID_ARG;
+    if (!iq || !w_head || !pool || !aligned(iq, 16) || !aligned(w_head, 4) || !aligned(pool, 4))
+        return CSA2_ERR_INVALID_ARG;
+    if (n_heads < 1 || n_heads > MAX_IDX_HEADS || pool_len < 1 || pool_len > 16384) return CSA2_ERR_INVALID_ARG;
+    size_t need = reindex_ws(cache->batch, n_q, pool_len);
+    if (!workspace || ws_bytes < need || !aligned(workspace, 16)) return CSA2_ERR_WORKSPACE;
+    return from_cuda(launch_reindex(*cache, nullptr, nullptr, iq, w_head, n_q, n_heads, pool, pool_len, k, idx_out,
                                     workspace, (cudaStream_t)stream));
 }
 

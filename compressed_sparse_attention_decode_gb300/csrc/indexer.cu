@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(256) k_scan_full(const uint8_t* __restrict__ k
         QView<DI> v;
         v.bind(smem + 32 + t * words, H);
         const int64_t gq = (int64_t)b * n_q + q0 + qa + t;
-        stage_query<DI>(v, iq_codes + gq * H * (DI / 2), iq_scales + gq * H * (DI / 16), w_head + gq * H, H,
+        stage_query<DI>(v, iq_codes + gq * H * (DI / 2), iq_scales + gq * H * (DI / 16), nullptr, w_head + gq * H, H,
                         threadIdx.x, blockDim.x);
         if (threadIdx.x == 0) nel[t] = n_elig_of(q_pos[gq], capacity);
     }
@@ -478,7 +478,7 @@ __global__ void __launch_bounds__(512) k_pool_bounds(const int32_t* __restrict__
                                                      const uint8_t* __restrict__ kc_all,
                                                      const uint8_t* __restrict__ ks_all, int capacity,
                                                      const uint8_t* __restrict__ iq_codes,
-                                                     const uint8_t* __restrict__ iq_scales,
+                                                     const uint8_t* __restrict__ iq_scales, const float* __restrict__ iq_raw,
                                                      const float* __restrict__ w_head, int n_q, int H,
                                                      float2* __restrict__ lu) {
     pdl_launch_next();
@@ -488,7 +488,8 @@ __global__ void __launch_bounds__(512) k_pool_bounds(const int32_t* __restrict__
     const int64_t gq = (int64_t)b * n_q + ql;
     QView<DI> v;
     v.bind(qsm, H);
-    stage_query<DI>(v, iq_codes + gq * H * (DI / 2), iq_scales + gq * H * (DI / 16), w_head + gq * H, H, threadIdx.x,
+    stage_query<DI>(v, iq_codes + gq * H * (DI / 2), iq_scales + gq * H * (DI / 16),
+                    iq_raw ? iq_raw + gq * H * DI : nullptr, w_head + gq * H, H, threadIdx.x,
                     blockDim.x);
     __syncthreads();
     const int t = blockIdx.z * blockDim.x + threadIdx.x;
@@ -512,7 +513,7 @@ __global__ void __launch_bounds__(512, 2) k_pool_exact(const int32_t* __restrict
                                                     const uint8_t* __restrict__ kc_all,
                                                     const uint8_t* __restrict__ ks_all, int capacity,
                                                     const uint8_t* __restrict__ iq_codes,
-                                                    const uint8_t* __restrict__ iq_scales,
+                                                    const uint8_t* __restrict__ iq_scales, const float* __restrict__ iq_raw,
                                                     const float* __restrict__ w_head, int n_q, int H,
                                                     unsigned long long* __restrict__ keys) {
     pdl_launch_next();
@@ -522,7 +523,8 @@ __global__ void __launch_bounds__(512, 2) k_pool_exact(const int32_t* __restrict
     const int64_t gq = (int64_t)b * n_q + ql;
     QView<DI> v;
     v.bind(qsm, H);
-    stage_query<DI>(v, iq_codes + gq * H * (DI / 2), iq_scales + gq * H * (DI / 16), w_head + gq * H, H, threadIdx.x,
+    stage_query<DI>(v, iq_codes + gq * H * (DI / 2), iq_scales + gq * H * (DI / 16),
+                    iq_raw ? iq_raw + gq * H * DI : nullptr, w_head + gq * H, H, threadIdx.x,
                     blockDim.x);
     __syncthreads();
     const int t = blockIdx.z * blockDim.x + threadIdx.x;
@@ -578,7 +580,8 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
                                                 const int* __restrict__ counts, int n_fixed, int list_len,
                                                 const uint8_t* __restrict__ kc_all, const uint8_t* __restrict__ ks_all,
                                                 int capacity, const uint8_t* __restrict__ iq_codes,
-                                                const uint8_t* __restrict__ iq_scales, const float* __restrict__ w_head,
+                                                const uint8_t* __restrict__ iq_scales, const float* __restrict__ iq_raw,
+                                                const float* __restrict__ w_head,
                                                 const int64_t* __restrict__ q_pos, int n_q, int q0, int n_qc, int H,
                                                 int k, int32_t* __restrict__ idx_out, int pool_blocks, int bs,
                                                 int32_t* __restrict__ pool_out, const int32_t* __restrict__ bid,
@@ -593,7 +596,8 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
     const int64_t slab = (int64_t)b * n_qc + ql;        // workspace row
     QView<DI> v;
     v.bind(qsm, H);
-    stage_query<DI>(v, iq_codes + gq * H * (DI / 2), iq_scales + gq * H * (DI / 16), w_head + gq * H, H, threadIdx.x,
+    stage_query<DI>(v, iq_codes + gq * H * (DI / 2), iq_scales + gq * H * (DI / 16),
+                    iq_raw ? iq_raw + gq * H * DI : nullptr, w_head + gq * H, H, threadIdx.x,
                     blockDim.x);
     const int32_t* id = ids + slab * list_len;
     uint8_t* extra = reinterpret_cast<uint8_t*>(qsm + QView<DI>::words(H));
@@ -913,7 +917,7 @@ cudaError_t launch_indexer_full_t(const csa2_cache& c, const uint8_t* iq_codes, 
         e = cudaFuncSetAttribute(k_select<DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
         if (e != cudaSuccess) return e;
         launch_k(k_select<DI>, g2, 512, smem2, st, w.ids, w.lu, w.counts, 0, (int)list_len, c.ikey_codes, c.ikey_scales,
-                                              c.capacity, iq_codes, iq_scales, w_head, q_pos, n_q, q0, n_qc, H, k,
+                                              c.capacity, iq_codes, iq_scales, (const float*)nullptr, w_head, q_pos, n_q, q0, n_qc, H, k,
                                               idx_out, pool_blocks, bs, pool_out, w.bid, w.blu, w.c2id, w.c2key);
         note_launch();
         e = cudaGetLastError();
@@ -924,15 +928,15 @@ cudaError_t launch_indexer_full_t(const csa2_cache& c, const uint8_t* iq_codes, 
 
 template <int DI>
 cudaError_t launch_reindex_t(const csa2_cache& c, const uint8_t* iq_codes, const uint8_t* iq_scales,
-                             const float* w_head, int n_q, int H, const int32_t* pool, int pool_len, int k,
-                             int32_t* idx_out, void* ws, cudaStream_t st) {
+                             const float* iq_raw, const float* w_head, int n_q, int H, const int32_t* pool, int pool_len,
+                             int k, int32_t* idx_out, void* ws, cudaStream_t st) {
     const SelectWs w = carve(ws, (int64_t)c.batch * n_q, pool_len);
     const size_t qwords = (size_t)QView<DI>::words(H) * sizeof(int);
     dim3 g0(n_q, c.batch, (pool_len + 511) / 512);
     if (pool_len <= MAX_K) {
         // small pool: exact scores for every slot, then one sort per query
         launch_k(k_pool_exact<DI>, g0, 512, qwords, st, pool, pool_len, c.ikey_codes, c.ikey_scales, c.capacity, iq_codes,
-                                                   iq_scales, w_head, n_q, H, w.c2key);
+                                                   iq_scales, iq_raw, w_head, n_q, H, w.c2key);
         note_launch();
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
@@ -944,7 +948,7 @@ cudaError_t launch_reindex_t(const csa2_cache& c, const uint8_t* iq_codes, const
         return cudaGetLastError();
     }
     launch_k(k_pool_bounds<DI>, g0, 512, qwords, st, pool, pool_len, c.ikey_codes, c.ikey_scales, c.capacity, iq_codes,
-                                                iq_scales, w_head, n_q, H, w.lu);
+                                                iq_scales, iq_raw, w_head, n_q, H, w.lu);
     note_launch();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -953,7 +957,7 @@ cudaError_t launch_reindex_t(const csa2_cache& c, const uint8_t* iq_codes, const
     if (e != cudaSuccess) return e;
     dim3 g(n_q, c.batch);
     launch_k(k_select<DI>, g, 512, smem, st, pool, w.lu, nullptr, pool_len, pool_len, c.ikey_codes, c.ikey_scales,
-                                       c.capacity, iq_codes, iq_scales, w_head, nullptr, n_q, 0, n_q, H, k, idx_out, 0,
+                                       c.capacity, iq_codes, iq_scales, iq_raw, w_head, nullptr, n_q, 0, n_q, H, k, idx_out, 0,
                                        1, nullptr, nullptr, nullptr, w.c2id, w.c2key);
     note_launch();
     return cudaGetLastError();
@@ -969,12 +973,13 @@ cudaError_t launch_indexer_full(const csa2_cache& c, const uint8_t* iq_codes, co
                                      pool_out, ws, st);
 }
 
-cudaError_t launch_reindex(const csa2_cache& c, const uint8_t* iq_codes, const uint8_t* iq_scales, const float* w_head,
-                           int n_q, int H, const int32_t* pool, int pool_len, int k, int32_t* idx_out, void* ws,
-                           cudaStream_t st) {
+// iq_raw != nullptr: fp32 queries [batch][n_q][H][d_idx], quantised inside the kernels (codes unused)
+cudaError_t launch_reindex(const csa2_cache& c, const uint8_t* iq_codes, const uint8_t* iq_scales, const float* iq_raw,
+                           const float* w_head, int n_q, int H, const int32_t* pool, int pool_len, int k,
+                           int32_t* idx_out, void* ws, cudaStream_t st) {
     if (c.d_idx == 128)
-        return launch_reindex_t<128>(c, iq_codes, iq_scales, w_head, n_q, H, pool, pool_len, k, idx_out, ws, st);
-    return launch_reindex_t<64>(c, iq_codes, iq_scales, w_head, n_q, H, pool, pool_len, k, idx_out, ws, st);
+        return launch_reindex_t<128>(c, iq_codes, iq_scales, iq_raw, w_head, n_q, H, pool, pool_len, k, idx_out, ws, st);
+    return launch_reindex_t<64>(c, iq_codes, iq_scales, iq_raw, w_head, n_q, H, pool, pool_len, k, idx_out, ws, st);
 }
 
 cudaError_t launch_reuse(const int32_t* prev, int32_t* out, int64_t n, cudaStream_t st) {

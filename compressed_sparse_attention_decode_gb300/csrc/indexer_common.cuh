@@ -34,13 +34,39 @@ struct QView {
     }
 };
 
+// One query's view: from its FP4 codes and scales, or (raw != nullptr) from
+// its unquantised fp32 values, which are quantised here exactly as the query
+// quantisation kernel does it (quant_group16, one 16-value group per thread).
 template <int DI>
 __device__ void stage_query(QView<DI> v, const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
-                            const float* __restrict__ w, int H, int tid, int nthr) {
-    for (int i = tid; i < H * (DI / 4); i += nthr) v.qp[i] = (int)unpack4_int8(reinterpret_cast<const uint16_t*>(codes)[i]);
-    for (int i = tid; i < H * (DI / 16); i += nthr) {
-        v.qsc[i] = e4m3_to_f32(scales[i]);
-        v.qsi[i] = e4m3_times_512(scales[i]);
+                            const float* __restrict__ raw, const float* __restrict__ w, int H, int tid, int nthr) {
+    if (raw != nullptr) {
+        for (int g = tid; g < H * (DI / 16); g += nthr) {
+            float x[16];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const float4 p = __ldg(reinterpret_cast<const float4*>(raw + (int64_t)g * 16) + t);
+                x[4 * t] = p.x;
+                x[4 * t + 1] = p.y;
+                x[4 * t + 2] = p.z;
+                x[4 * t + 3] = p.w;
+            }
+            uint32_t c0, c1, sb;
+            quant_group16(x, c0, c1, sb);
+            v.qp[4 * g] = (int)unpack4_int8(c0 & 0xffffu);
+            v.qp[4 * g + 1] = (int)unpack4_int8(c0 >> 16);
+            v.qp[4 * g + 2] = (int)unpack4_int8(c1 & 0xffffu);
+            v.qp[4 * g + 3] = (int)unpack4_int8(c1 >> 16);
+            v.qsc[g] = e4m3_to_f32(sb);
+            v.qsi[g] = e4m3_times_512(sb);
+        }
+    } else {
+        for (int i = tid; i < H * (DI / 4); i += nthr)
+            v.qp[i] = (int)unpack4_int8(reinterpret_cast<const uint16_t*>(codes)[i]);
+        for (int i = tid; i < H * (DI / 16); i += nthr) {
+            v.qsc[i] = e4m3_to_f32(scales[i]);
+            v.qsi[i] = e4m3_times_512(scales[i]);
+        }
     }
     for (int i = tid; i < H; i += nthr) {
         v.w[i] = w[i];

@@ -17,9 +17,9 @@
 
 namespace csa2 {
 size_t reindex_ws(int batch, int n_q, int64_t pool_len);
-cudaError_t launch_reindex(const csa2_cache& c, const uint8_t* iq_codes, const uint8_t* iq_scales, const float* w_head,
-                           int n_q, int H, const int32_t* pool, int pool_len, int k, int32_t* idx_out, void* ws,
-                           cudaStream_t st);
+cudaError_t launch_reindex(const csa2_cache& c, const uint8_t* iq_codes, const uint8_t* iq_scales, const float* iq_raw,
+                           const float* w_head, int n_q, int H, const int32_t* pool, int pool_len, int k,
+                           int32_t* idx_out, void* ws, cudaStream_t st);
 }  // namespace csa2
 
 // Shared by every call on a device; it keeps whatever the last call left in it.
@@ -76,7 +76,7 @@ extern "C" csa2_status csa2_reindex_noalloc(const csa2_cache* cache, const uint8
     if (scratch_for_current_device(&scratch) != cudaSuccess) return CSA2_ERR_CUDA;
     // Nothing in the scratch has to start at zero: every byte a Reindex call
     // reads there was written earlier in the same call.
-    cudaError_t e = launch_reindex(*cache, iq_codes, iq_scales, w_head, n_q, n_heads, pool, pool_len, k, idx_out,
+    cudaError_t e = launch_reindex(*cache, iq_codes, iq_scales, nullptr, w_head, n_q, n_heads, pool, pool_len, k, idx_out,
                                    scratch, (cudaStream_t)stream);
     return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA;
 }

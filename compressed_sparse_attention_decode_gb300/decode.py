@@ -13,7 +13,7 @@ is a C-ABI entry point of libcsa2; this module only sequences them.
 import torch
 
 from . import (FULL, REINDEX, REUSE, OP_INDEXER_TOPK, OP_REINDEX, OP_SPARSE_ATTN, Cache, csa2_cache_write,
-               csa2_indexer_topk, csa2_quantize_fp4, csa2_reindex, csa2_sparse_attn, workspace)
+               csa2_indexer_topk, csa2_quantize_fp4, csa2_reindex, csa2_reindex_f32, csa2_sparse_attn, workspace)
 
 _MODES = {"full": FULL, "reindex": REINDEX, "reuse": REUSE}
 
@@ -84,15 +84,16 @@ class DecodeStep:
             idx_l = self.idx[l]
             if mode == "reuse":
                 csa2_reindex(REUSE, self.cache, self.k, prev_idx=prev, idx_out=idx_l, stream=stream, n_q=self.n_q)
-            else:
+            elif mode == "full":
                 csa2_quantize_fp4(self.iq[t], self.iq_codes, self.iq_scales, stream=stream)
-                if mode == "full":
-                    csa2_indexer_topk(self.cache, self.iq_codes, self.iq_scales, self.w_head[t], self.q_pos, self.k,
-                                      self.pool_blocks, self.bs, idx_out=idx_l, pool_out=self.pool, ws=self.ws_full,
-                                      stream=stream)
-                else:
-                    csa2_reindex(REINDEX, self.cache, self.k, self.iq_codes, self.iq_scales, self.w_head[t],
-                                 self.pool, idx_out=idx_l, ws=self.ws_re, stream=stream)
+                csa2_indexer_topk(self.cache, self.iq_codes, self.iq_scales, self.w_head[t], self.q_pos, self.k,
+                                  self.pool_blocks, self.bs, idx_out=idx_l, pool_out=self.pool, ws=self.ws_full,
+                                  stream=stream)
+                t += 1
+            else:
+                # the Reindex kernels quantise this layer's queries themselves
+                csa2_reindex_f32(self.cache, self.k, self.iq[t], self.w_head[t], self.pool, idx_out=idx_l,
+                                 ws=self.ws_re, stream=stream)
                 t += 1
             csa2_sparse_attn(self.cache, self.q[l], self.q_pos, idx_l, self.win[l], self.swa_pos0, out=self.out[l],
                              lse=None if self.lse is None else self.lse[l], ws=self.ws_attn, stream=stream)

@@ -155,6 +155,20 @@ csa2_status csa2_reindex(int32_t mode, const csa2_cache* cache, const uint8_t* i
                          void* stream);
 
 /*
+ * Reindex from unquantised indexer queries: the same results as
+ * csa2_quantize_fp4(iq -> codes, scales) followed by csa2_reindex(CSA2_REINDEX,
+ * codes, scales, ...), bit for bit, with the FP4 quantisation of the queries
+ * done by the Reindex kernels as they stage each query, so a Reindex layer
+ * takes one launch fewer.  The pages have no separate counterpart: it is the
+ * Reindex step with its query quantisation fused.
+ *   iq fp32 [batch][n_q][n_heads][d_idx], 16-byte aligned; the other arguments
+ *   as for csa2_reindex(CSA2_REINDEX, ...), same workspace size.
+ */
+csa2_status csa2_reindex_f32(const csa2_cache* cache, const float* iq, const float* w_head, int32_t n_q,
+                             int32_t n_heads, const int32_t* pool, int32_t pool_len, int32_t k, int32_t* idx_out,
+                             void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * Sparse attention over the selected entries plus the sliding window
  * ("DeepSeek-v4.1 Flash" §2.3.1: each query attends to its top-k entries and
  * to the local SWA window; §1.1: all heads share one 512-dim latent, which is

@@ -206,6 +206,38 @@ def test_reindex_pool_with_holes_and_reuse(csa):
         assert np.array_equal(idx.cpu().numpy()[0, 0], want)
         again = csa.csa2_reindex(csa.REUSE, cache, k, prev_idx=idx)
         assert torch.equal(again, idx)
+        # the same from the unquantised queries (quantised inside the Reindex kernels)
+        idx32 = csa.csa2_reindex_f32(cache, k, torch.from_numpy(iq).cuda(), torch.from_numpy(w).cuda(),
+                                     torch.from_numpy(pool).cuda())
+        assert torch.equal(idx32, idx)
+
+
+def test_reindex_from_fp32_queries_large_pool(csa):
+    """csa2_reindex_f32 through the bounds + selection path (pool above 2,048 slots), against the
+    oracle and against csa2_quantize_fp4 + csa2_reindex"""
+    n, d = 9000, 128
+    lat = oracle.quantize_rows(synth.normal_f32(43, 2, (n, 512)))
+    kc, ks = oracle.quantize_rows(synth.normal_f32(43, 1, (n, d)))
+    cache = host_cache(csa, [a[None] for a in (lat[0], lat[1], kc, ks)], d)
+    pool = np.full((1, 2, 6000), -1, np.int32)
+    rng = np.random.default_rng(5)
+    for q in range(2):
+        pool[0, q, :5800] = rng.choice(n, 5800, replace=False).astype(np.int32)
+    iq = synth.normal_f32(43, 3, (1, 2, 8, d))
+    w = synth.uniform_f32(43, 4, (1, 2, 8), 0.0, 1.0)
+    qc, qs = oracle.quantize_rows(iq)
+    k = 512
+    idx32 = csa.csa2_reindex_f32(cache, k, torch.from_numpy(iq).cuda(), torch.from_numpy(w).cuda(),
+                                 torch.from_numpy(pool).cuda())
+    codes = torch.empty((1, 2, 8, d // 2), dtype=torch.uint8, device="cuda")
+    scales = torch.empty((1, 2, 8, d // 16), dtype=torch.uint8, device="cuda")
+    csa.csa2_quantize_fp4(torch.from_numpy(iq).cuda(), codes, scales)
+    idx = csa.csa2_reindex(csa.REINDEX, cache, k, codes, scales, torch.from_numpy(w).cuda(),
+                           torch.from_numpy(pool).cuda())
+    assert torch.equal(idx32, idx)
+    for q in range(2):
+        S = oracle.index_scores(kc, ks, qc[0, q], qs[0, q], w[0, q], ids=pool[0, q])
+        assert np.array_equal(idx32.cpu().numpy()[0, q], oracle.topk(S, k, ids=pool[0, q]))
 
 
 def test_attention_window_clipping_and_empty_selection(csa):
