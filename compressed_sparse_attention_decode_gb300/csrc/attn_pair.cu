@@ -502,7 +502,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
     }
     // ================= combine the pair (every thread of both CTAs takes part in the cluster barriers)
     umma::cluster_sync();              // the max / row sums of both CTAs are in place
-    float pv[AP_H];                    // this CTA's partial of the peer's output half (TMEM reads)
     if (warp < AP_SMW) {
         if (tid < AP_H) {
             const float m0 = own_ml[tid], l0 = own_ml[AP_H + tid], m1 = peer_ml[tid], l1 = peer_ml[AP_H + tid];
@@ -518,32 +517,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
         ok &= umma::mbar_wait(sa(&b_odone[(T - 1) & 1]), ((T - 1) >> 1) & 1);   // every GEMM2 is done
         umma::fence_after();
         // this CTA's share of its own half of the dims (dim tile 2*rank + half, this warp's
-        // lane quarter) is stored; the peer adds its share after the barrier.  Each half's 64
-        // columns are read with one wait; the peer half's reads are in flight across the barrier.
+        // lane quarter) is stored; the peer adds its share after the barrier
         const int qd = warp & 3, half = warp >> 2;
-        const uint32_t lrow = tmem + ((uint32_t)(qd * 32) << 16);
-        {
-            float v[AP_H];
-#pragma unroll
-            for (int c = 0; c < AP_H; c += 16) umma::tmem_ld16(lrow + APT_O + 64 * (2 * (int)rank + half) + c, v + c);
+        const int mt = 2 * (int)rank + half;
+        float* op = out + (gq * AP_H) * D_LAT + (int)rank * 256 + half * 128 + qd * 32 + lane;
+#pragma unroll 1
+        for (int c = 0; c < AP_H; c += 16) {
+            float v[16];
+            umma::tmem_ld16(tmem + ((uint32_t)(qd * 32) << 16) + APT_O + 64 * mt + c, v);
             umma::tmem_wait_ld();
-            float* op = out + (gq * AP_H) * D_LAT + (int)rank * 256 + half * 128 + qd * 32 + lane;
 #pragma unroll
-            for (int i = 0; i < AP_H; ++i) op[(int64_t)i * D_LAT] = ok ? v[i] * fown[i] : __int_as_float(0x7fc00000);
+            for (int i = 0; i < 16; ++i) op[(int64_t)(c + i) * D_LAT] = ok ? v[i] * fown[c + i] : __int_as_float(0x7fc00000);
         }
-#pragma unroll
-        for (int c = 0; c < AP_H; c += 16) umma::tmem_ld16(lrow + APT_O + 64 * (2 * (int)peer + half) + c, pv + c);
     }
     umma::fence_before();
     umma::cluster_sync();              // both halves of the output hold one CTA's share
     if (warp < AP_SMW) {
         umma::fence_after();
-        umma::tmem_wait_ld();
         // add this CTA's share of the peer's half (reductions in L2, nothing read back)
         const int qd = warp & 3, half = warp >> 2;
+        const int mt = 2 * (int)peer + half;
         float* op = out + (gq * AP_H) * D_LAT + (int)peer * 256 + half * 128 + qd * 32 + lane;
+#pragma unroll 1
+        for (int c = 0; c < AP_H; c += 16) {
+            float v[16];
+            umma::tmem_ld16(tmem + ((uint32_t)(qd * 32) << 16) + APT_O + 64 * mt + c, v);
+            umma::tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < AP_H; ++i) atomicAdd(op + (int64_t)i * D_LAT, ok ? pv[i] * fown[i] : __int_as_float(0x7fc00000));
+            for (int i = 0; i < 16; ++i) atomicAdd(op + (int64_t)(c + i) * D_LAT, ok ? v[i] * fown[c + i] : __int_as_float(0x7fc00000));
+        }
     }
     if (!ok) atomicExch(err, 1);
     umma::fence_before();
