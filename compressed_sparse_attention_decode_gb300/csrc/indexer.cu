@@ -586,11 +586,15 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
                                                 int k, int32_t* __restrict__ idx_out, int pool_blocks, int bs,
                                                 int32_t* __restrict__ pool_out, const int32_t* __restrict__ bid,
                                                 const float2* __restrict__ blu, int* __restrict__ c2id,
-                                                unsigned long long* __restrict__ c2key) {
+                                                unsigned long long* __restrict__ c2key, int* __restrict__ h2id,
+                                                unsigned long long* __restrict__ h2key) {
     pdl_launch_next();
     pdl_wait();
     extern __shared__ int qsm[];
     __shared__ SelectSmem sm;
+    // gridDim.z == 2 (Full layer with an HSI pool): block z = 0 keeps the top k, z = 1 builds the
+    // pool, side by side; the pool block's scratch (h2id, h2key) is its own
+    const bool split = gridDim.z == 2;
     const int b = blockIdx.y, ql = blockIdx.x;
     const int64_t gq = (int64_t)b * n_q + q0 + ql;     // global query row
     const int64_t slab = (int64_t)b * n_qc + ql;        // workspace row
@@ -607,8 +611,9 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
     sm.bitmap = reinterpret_cast<unsigned int*>(extra + SEL_DYN_EXTRA);
     const float2* L = lu + slab * list_len;
     const int n = counts ? counts[2 * slab] : n_fixed;
-    int* cid = c2id + slab * list_len;
-    unsigned long long* ckey = c2key + slab * list_len;
+    int* cid = split && blockIdx.z == 1 ? h2id + slab * list_len + list_len / 2 : c2id + slab * list_len;
+    unsigned long long* ckey =
+        split && blockIdx.z == 1 ? h2key + slab * list_len + list_len / 2 : c2key + slab * list_len;
     const uint8_t* kc = kc_all + (int64_t)b * capacity * (DI / 2);
     const uint8_t* ks = ks_all + (int64_t)b * capacity * (DI / 16);
     auto entry_of = [&](int t) -> int {
@@ -621,6 +626,7 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
     }
     sm.rs.whist = sm.whist;
     __syncthreads();
+    if (!split || blockIdx.z == 0) {
     // ---- 1. k-th largest lower bound, candidates whose upper bound reaches it.
     // Every forwarded item (Full) is a real entry; an empty pool slot (Reindex)
     // has bounds (-inf, -inf), below every real entry, so the selection may
@@ -693,9 +699,10 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
     int32_t* out = idx_out + gq * k;
     for (int t = threadIdx.x; t < k; t += blockDim.x) out[t] = t < kept ? sm.din[t] : -1;
     __syncthreads();
+    }
 
     // ---- 4. HSI candidate pool (Full only)
-    if (pool_blocks <= 0 || !counts) return;
+    if (pool_blocks <= 0 || !counts || (split && blockIdx.z == 0)) return;
     const int n_elig = n_elig_of(q_pos[gq], capacity);
     const int P = pool_blocks * bs;
     int32_t* pout = pool_out + gq * P;
@@ -912,13 +919,17 @@ cudaError_t launch_indexer_full_t(const csa2_cache& c, const uint8_t* iq_codes, 
             e = cudaGetLastError();
         }
         if (e != cudaSuccess) return e;
-        dim3 g2(n_qc, c.batch);
+        // with an HSI pool the top k and the pool are built by two blocks per query at once; the
+        // pool block's scratch is the upper half of the block-candidate lists (a query has at most
+        // ceil(capacity / bs) <= list_len / 2 block candidates when bs >= 2)
+        dim3 g2(n_qc, c.batch, (pool_blocks > 1 && bs >= 2) ? 2 : 1);
         const size_t smem2 = qwords + SEL_DYN_EXTRA + SEL_BITMAP_BYTES;
         e = cudaFuncSetAttribute(k_select<DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
         if (e != cudaSuccess) return e;
         launch_k(k_select<DI>, g2, 512, smem2, st, w.ids, w.lu, w.counts, 0, (int)list_len, c.ikey_codes, c.ikey_scales,
                                               c.capacity, iq_codes, iq_scales, (const float*)nullptr, w_head, q_pos, n_q, q0, n_qc, H, k,
-                                              idx_out, pool_blocks, bs, pool_out, w.bid, w.blu, w.c2id, w.c2key);
+                                              idx_out, pool_blocks, bs, pool_out, w.bid, w.blu, w.c2id, w.c2key,
+                                              w.bid, reinterpret_cast<unsigned long long*>(w.blu));
         note_launch();
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
@@ -958,7 +969,8 @@ cudaError_t launch_reindex_t(const csa2_cache& c, const uint8_t* iq_codes, const
     dim3 g(n_q, c.batch);
     launch_k(k_select<DI>, g, 512, smem, st, pool, w.lu, nullptr, pool_len, pool_len, c.ikey_codes, c.ikey_scales,
                                        c.capacity, iq_codes, iq_scales, iq_raw, w_head, nullptr, n_q, 0, n_q, H, k, idx_out, 0,
-                                       1, nullptr, nullptr, nullptr, w.c2id, w.c2key);
+                                       1, nullptr, nullptr, nullptr, w.c2id, w.c2key, (int*)nullptr,
+                                       (unsigned long long*)nullptr);
     note_launch();
     return cudaGetLastError();
 }
