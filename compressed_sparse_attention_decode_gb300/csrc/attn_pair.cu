@@ -25,9 +25,11 @@
 // two TMEM partials that the softmax adds; the first half starts as soon as
 // its dims are expanded) and warp 10 the output MMAs: one thread issues about
 // one MMA per 50 cycles, so the streams get a thread each.  Warps 11-17 gather
-// rows.  Tile 0 is the CTA's
-// window rows (contiguous: one bulk copy); the FP4 tiles follow, their rows
-// prefetched into L2 one tile ahead, so the gathers are single L2 round trips.
+// rows.  Tile 0 is the CTA's window rows (contiguous: one bulk copy); the FP4
+// tiles follow, their rows prefetched into L2 one tile ahead, so the gathers
+// are single L2 round trips.  Everything before the indices (Q, the window
+// tile, TMEM and barriers) overlaps the preceding kernel of the stream
+// (programmatic launch); only the loaders wait for it.
 #include "common.cuh"
 #include "umma.cuh"
 
