@@ -36,8 +36,8 @@ __global__ void __launch_bounds__(256) k_sparse_attn_simt(
     const uint16_t* __restrict__ q, int n_q, int H, const int64_t* __restrict__ q_pos, const int32_t* __restrict__ idx,
     int k, const uint16_t* __restrict__ swa, int64_t swa_pos0, int swa_len, float scale, float* __restrict__ out,
     float* __restrict__ lse) {
-    pdl_launch_next();
     pdl_wait();
+    pdl_launch_next();
     extern __shared__ float sm[];
     float* qs = sm;                                  // [8][512]
     float* tile = qs + SIMT_HEADS * D_LAT;           // [32][512]

@@ -75,8 +75,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sparse_attn_tc(
     const uint16_t* __restrict__ q, int n_q, int q0, int H, const int64_t* __restrict__ q_pos,
     const int32_t* __restrict__ idx, int k, const uint16_t* __restrict__ swa, int64_t swa_pos0, int swa_len,
     float scale_log2e, int n_tiles, float* __restrict__ part_o, float2* __restrict__ part_ml, int* __restrict__ err) {
-    pdl_launch_next();
     pdl_wait();
+    pdl_launch_next();
     extern __shared__ uint8_t dyn[];
     __shared__ __align__(8) unsigned long long mbar;
     __shared__ uint32_t tmem_base;
@@ -309,8 +309,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_sparse_attn_tc(
 __global__ void __launch_bounds__(128) k_attn_combine(const float* __restrict__ part_o,
                                                       const float2* __restrict__ part_ml, int n_q, int q0, int H,
                                                       int n_tiles, float* __restrict__ out, float* __restrict__ lse) {
-    pdl_launch_next();
     pdl_wait();
+    pdl_launch_next();
     const int h = blockIdx.x, ql = blockIdx.y, b = blockIdx.z;
     const int nqc = gridDim.y;
     const int64_t s0 = ((int64_t)b * nqc + ql) * n_tiles;

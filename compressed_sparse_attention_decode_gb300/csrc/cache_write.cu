@@ -17,8 +17,8 @@ __global__ void __launch_bounds__(256) k_cache_write(uint8_t* __restrict__ lat_c
                                                      int64_t entry0, int n_ent, const float* __restrict__ w0,
                                                      const float* __restrict__ w1,
                                                      const uint16_t* __restrict__ ikey_raw) {
-    pdl_launch_next();
     pdl_wait();
+    pdl_launch_next();
     const int lane = threadIdx.x & 31;
     const int i = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int b = blockIdx.y;
@@ -72,9 +72,7 @@ __global__ void __launch_bounds__(256) k_cache_write(uint8_t* __restrict__ lat_c
 // one thread per 16-value group
 __global__ void __launch_bounds__(256) k_quantize_fp4(const float* __restrict__ x, int64_t n_groups,
                                                       uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
-    // x is an input of the step, never written by a kernel of this library: it is read while the
-    // preceding kernel still runs; the codes are written only after that kernel has completed
-    // (it may still read the previous codes)
+    pdl_wait();
     pdl_launch_next();
     int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (g >= n_groups) return;
@@ -87,7 +85,6 @@ __global__ void __launch_bounds__(256) k_quantize_fp4(const float* __restrict__ 
         v[4 * t + 2] = p.z;
         v[4 * t + 3] = p.w;
     }
-    pdl_wait();
     uint32_t q0, q1, sb;
     quant_group16(v, q0, q1, sb);
     reinterpret_cast<uint2*>(codes)[g] = make_uint2(q0, q1);

@@ -11,10 +11,11 @@ namespace csa2 {
 
 // ---------------------------------------------------------------- launches
 // Every kernel of the library is launched with programmatic stream
-// serialisation: the next kernel in the stream may be scheduled while this one
-// still runs (each kernel lets its successor in as it starts), and waits at its
-// top until its predecessor has completed and that grid's memory is visible.
-// Outside such a launch both instructions do nothing.
+// serialisation: a kernel waits at its top until its predecessor has completed
+// and that grid's memory is visible, then lets its own successor be scheduled,
+// so a successor overlaps only its immediate predecessor (and may do work that
+// needs nothing the stream produced before it waits).  Outside such a launch
+// both instructions do nothing.
 __device__ __forceinline__ void pdl_launch_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 

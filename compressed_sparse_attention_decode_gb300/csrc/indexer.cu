@@ -34,8 +34,8 @@ __global__ void __launch_bounds__(256) k_scan_full(const uint8_t* __restrict__ k
                                                    int* __restrict__ counts, int* __restrict__ cid,
                                                    float2* __restrict__ clu, int* __restrict__ bid,
                                                    float2* __restrict__ blu, int list_len) {
-    pdl_launch_next();
     pdl_wait();
+    pdl_launch_next();
     extern __shared__ int smem[];
     __shared__ RadixSmem rs;
     const int b = blockIdx.z;
@@ -481,8 +481,8 @@ __global__ void __launch_bounds__(512) k_pool_bounds(const int32_t* __restrict__
                                                      const uint8_t* __restrict__ iq_scales, const float* __restrict__ iq_raw,
                                                      const float* __restrict__ w_head, int n_q, int H,
                                                      float2* __restrict__ lu) {
-    pdl_launch_next();
     pdl_wait();
+    pdl_launch_next();
     extern __shared__ int qsm[];
     const int ql = blockIdx.x, b = blockIdx.y;
     const int64_t gq = (int64_t)b * n_q + ql;
@@ -516,8 +516,8 @@ __global__ void __launch_bounds__(512, 2) k_pool_exact(const int32_t* __restrict
                                                     const uint8_t* __restrict__ iq_scales, const float* __restrict__ iq_raw,
                                                     const float* __restrict__ w_head, int n_q, int H,
                                                     unsigned long long* __restrict__ keys) {
-    pdl_launch_next();
     pdl_wait();
+    pdl_launch_next();
     extern __shared__ int qsm[];
     const int ql = blockIdx.x, b = blockIdx.y;
     const int64_t gq = (int64_t)b * n_q + ql;
@@ -544,8 +544,8 @@ __global__ void __launch_bounds__(512, 2) k_pool_exact(const int32_t* __restrict
 __global__ void __launch_bounds__(512) k_pool_rank(const int32_t* __restrict__ pool, int pool_len,
                                                    const unsigned long long* __restrict__ keys, int capacity, int k,
                                                    int32_t* __restrict__ idx_out) {
-    pdl_launch_next();
     pdl_wait();
+    pdl_launch_next();
     extern __shared__ unsigned long long sdyn[];
     __shared__ SelectSmem sm;
     const int64_t gq = (int64_t)blockIdx.y * gridDim.x + blockIdx.x;
@@ -588,8 +588,8 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
                                                 const float2* __restrict__ blu, int* __restrict__ c2id,
                                                 unsigned long long* __restrict__ c2key, int* __restrict__ h2id,
                                                 unsigned long long* __restrict__ h2key) {
-    pdl_launch_next();
     pdl_wait();
+    pdl_launch_next();
     extern __shared__ int qsm[];
     __shared__ SelectSmem sm;
     // gridDim.z == 2 (Full layer with an HSI pool): block z = 0 keeps the top k, z = 1 builds the
@@ -825,8 +825,8 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
 
 // Reuse: the latest indices, unchanged ("DeepSeek-v4.1 Flash" §2.3.2)
 __global__ void k_copy_idx(const int32_t* __restrict__ src, int32_t* __restrict__ dst, int64_t n) {
-    pdl_launch_next();
     pdl_wait();
+    pdl_launch_next();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i < n) dst[i] = src[i];
 }

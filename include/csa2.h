@@ -30,14 +30,15 @@
  *   - bf16 values are passed as uint16_t bit patterns.
  *   - Threading: calls are re-entrant; calls on one stream run in order.
  *   - Kernels are launched with programmatic stream serialisation: a kernel of
- *     this library may be scheduled while the kernel before it in the stream
- *     still runs, and waits for that kernel's completion before it reads what
- *     the stream produced.  Before that wait it reads only caller inputs that
- *     no kernel of this library writes (the queries q and their positions
- *     q_pos, the window rows swa, the values to quantise x); a caller that
- *     writes those with a kernel of its own that itself lets its successor
- *     start early must make that kernel complete first.  Kernels not launched
- *     this way (any caller kernel by default) are waited for as usual.
+ *     this library may be scheduled while the kernel just before it in the
+ *     stream still runs, and waits for that kernel's completion before it
+ *     reads what the stream produced; it lets its own successor start only
+ *     after that wait, so it never overlaps any earlier work.  Before the wait
+ *     the attention reads only caller inputs that no kernel of this library
+ *     writes (the queries q and their positions q_pos, the window rows swa); a
+ *     caller that writes those with a kernel of its own that itself lets its
+ *     successor start early must make that kernel complete first.  Kernels not
+ *     launched this way (any caller kernel by default) are waited for as usual.
  */
 #ifndef CSA2_H
 #define CSA2_H
