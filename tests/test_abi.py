@@ -65,6 +65,12 @@ def test_host_side_validation_needs_no_gpu(lib):
     assert lib.csa2_indexer_topk(ctypes.byref(c), p, p, p, 1, p, 8, 64, p, 0, 8, None, p, 0,
                                  None) == csa.ERR_WORKSPACE                                   # no workspace
     assert lib.csa2_reindex(7, ctypes.byref(c), p, p, p, 1, 8, p, 8, p, 4, p, None, 0, None) == csa.ERR_INVALID_ARG
+    # Reindex from fp32 queries: NULL or misaligned queries, bad pool sizes, missing workspace
+    assert lib.csa2_reindex_f32(ctypes.byref(c), None, p, 1, 8, p, 8, 4, p, p, 1 << 30, None) == csa.ERR_INVALID_ARG
+    assert lib.csa2_reindex_f32(ctypes.byref(c), ctypes.c_void_p(260), p, 1, 8, p, 8, 4, p, p, 1 << 30,
+                                None) == csa.ERR_INVALID_ARG                                  # iq not 16-aligned
+    assert lib.csa2_reindex_f32(ctypes.byref(c), p, p, 1, 8, p, 0, 4, p, p, 1 << 30, None) == csa.ERR_INVALID_ARG
+    assert lib.csa2_reindex_f32(ctypes.byref(c), p, p, 1, 8, p, 8, 4, p, None, 0, None) == csa.ERR_WORKSPACE
     assert lib.csa2_quantize_fp4(p, 4, 24, p, p, None) == csa.ERR_INVALID_ARG                  # d not /16
     assert lib.csa2_workspace_size(csa.OP_INDEXER_TOPK, 2, 1, 8, 512, 1000) > 0
     assert lib.csa2_launch_count() >= 0
