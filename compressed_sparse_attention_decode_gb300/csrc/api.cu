@@ -35,9 +35,11 @@ void note_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 using namespace csa2;
 
 namespace {
-
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+}  // namespace
 
+namespace csa2 {
+// The cache checks of every entry point (the no-workspace Reindex too).
 csa2_status check_cache(const csa2_cache* c, bool need_ikey) {
     if (!c) return CSA2_ERR_INVALID_ARG;
     if (c->batch < 1 || c->capacity < 1) return CSA2_ERR_INVALID_ARG;
@@ -51,7 +53,9 @@ csa2_status check_cache(const csa2_cache* c, bool need_ikey) {
         return CSA2_ERR_INVALID_ARG;
     return CSA2_OK;
 }
+}  // namespace csa2
 
+namespace {
 csa2_status from_cuda(cudaError_t e) { return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA; }
 
 }  // namespace

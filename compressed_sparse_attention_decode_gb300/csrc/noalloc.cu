@@ -16,6 +16,7 @@
 #define CSA2_NOALLOC_SCRATCH_BYTES (8u << 20)
 
 namespace csa2 {
+csa2_status check_cache(const csa2_cache* c, bool need_ikey);
 size_t reindex_ws(int batch, int n_q, int64_t pool_len);
 cudaError_t launch_reindex(const csa2_cache& c, const uint8_t* iq_codes, const uint8_t* iq_scales, const float* iq_raw,
                            const float* w_head, int n_q, int H, const int32_t* pool, int pool_len, int k,
@@ -33,7 +34,9 @@ void* g_scratch_ptr[kMaxDevices] = {nullptr};
 
 // Device address of the scratch array on the current device, looked up once
 // per device.  In host code the array's name is only a host-side stand-in, so
-// the kernels must be given this address, never the symbol itself.
+// the kernels must be given this address, never the symbol itself.  The cached
+// address belongs to the device's current context: after cudaDeviceReset it
+// is stale, so the library must not be used across a device reset.
 cudaError_t scratch_for_current_device(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -59,11 +62,9 @@ extern "C" csa2_status csa2_reindex_noalloc(const csa2_cache* cache, const uint8
                                             int32_t n_heads, const int32_t* pool, int32_t pool_len, int32_t k,
                                             int32_t* idx_out, void* stream) {
     using namespace csa2;
-    if (!cache || cache->batch < 1 || cache->capacity < 1) return CSA2_ERR_INVALID_ARG;
-    if (cache->d_lat != D_LAT || (cache->d_idx != 64 && cache->d_idx != 128)) return CSA2_ERR_UNSUPPORTED;
-    if (!cache->ikey_codes || !cache->ikey_scales || !aligned_to(cache->ikey_codes, 16) ||
-        !aligned_to(cache->ikey_scales, (size_t)(cache->d_idx / 16)))
-        return CSA2_ERR_INVALID_ARG;
+    // the same cache checks as csa2_reindex
+    const csa2_status cs = check_cache(cache, true);
+    if (cs != CSA2_OK) return cs;
     if (n_q < 1 || k < 1 || k > MAX_K || n_heads < 1 || n_heads > MAX_IDX_HEADS || pool_len < 1 ||
         pool_len > 16384)
         return CSA2_ERR_INVALID_ARG;

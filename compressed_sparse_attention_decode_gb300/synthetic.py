@@ -39,10 +39,16 @@ class HostInputs:
     decode step appends one row, like the compressed cache itself."""
 
     def __init__(self, step):
+        """pinned host buffers holding the step's own inputs: the values the
+        device buffers of `step` hold now are copied out once, here, so every
+        timed step moves and computes the real workload"""
         pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
         self.names = ["iq", "w_head", "q", "q_pos"] + (["h_chunk", "kraw_chunk"] if step.chunk_len else [])
         self.host = {n: pin(getattr(step, n)) for n in self.names}
+        for n in self.names:
+            self.host[n].copy_(getattr(step, n))
         self.win_new = pin(step.win[:, :, -1])
+        self.win_new.copy_(step.win[:, :, -1])
         self.win_dev = {}
         self.out = pin(step.out)
 

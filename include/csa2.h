@@ -200,8 +200,8 @@ csa2_status csa2_sparse_attn(const csa2_cache* cache, const uint16_t* q, int32_t
  * device-wide synchronisation of cudaMalloc / cudaFree.  The pages have no
  * counterpart of this entry point; it is a deployment convenience.
  *
- * Same arguments and results as csa2_reindex(CSA2_REINDEX, ...) minus the
- * workspace (and minus prev_idx, which only Reuse reads).  The scratch is a
+ * Same arguments, checks and results as csa2_reindex(CSA2_REINDEX, ...) minus
+ * the workspace (and minus prev_idx, which only Reuse reads).  The scratch is a
  * fixed 8 MiB array inside the library's device image: every GPU that loads
  * the library holds those 8 MiB until the process exits.  Requests needing
  * more (batch * n_q * pool_len above about 233,000 pool slots) return
@@ -209,7 +209,8 @@ csa2_status csa2_sparse_attn(const csa2_cache* cache, const uint16_t* q, int32_t
  * nothing.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is kept for the life of the
+ *     process: do not use this entry point across cudaDeviceReset.
  *   - Every call on a device shares the one array and it keeps the last
  *     call's contents.  No part of it needs to start at zero.  Calls that can
  *     overlap on the GPU (different streams, no ordering between them) race

@@ -22,6 +22,20 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _lib = None
 
 SCALE = 1.0 / np.sqrt(512.0)
+WINDOW = 128
+
+
+def n_elig(p, ratio=2):
+    """Global entries a query at raw position p may attend to besides its window:
+    the entries lying wholly before the window [p-127, p] ("DeepSeek-v4.1 Flash"
+    §2.3.1: each query reads its selected global entries plus the local window;
+    §2.3.4: the indexer scores the causally visible entries).  Entry i covers raw
+    positions [ratio*i, ratio*i + ratio - 1], so it is eligible when
+    ratio*i + ratio - 1 < p - 127."""
+    p = int(p)
+    if p < WINDOW - 1:
+        return 0
+    return (p - (WINDOW - 1)) // ratio
 
 
 def build(force=False):
@@ -234,9 +248,9 @@ def run_sequence(wl, b, cache=None, queries=None, layers=None, want_out=True):
             if mode == "full" and wl.pool_blocks:
                 pool = np.empty((len(queries), wl.pool_blocks * wl.pool_block_size), np.int32)
             for t, qi in enumerate(queries):
-                n_elig = wl.n_elig(qpos[qi])
+                ne = n_elig(qpos[qi])
                 if mode == "full":
-                    S = index_scores(kc, ks, qc[t], qs[t], wh[qi], n=n_elig)
+                    S = index_scores(kc, ks, qc[t], qs[t], wh[qi], n=ne)
                     idx_l[t] = topk(S, wl.k)
                     if wl.pool_blocks:
                         pool[t] = hsi_pool(S, wl.pool_block_size, wl.pool_blocks)

@@ -67,10 +67,6 @@ class Workload:
             return np.arange(self.prefix, self.T, dtype=np.int64)
         return np.array([self.T - 1], dtype=np.int64)
 
-    def n_elig(self, p):
-        """entries lying wholly before the window [p-127, p]"""
-        return max(0, (int(p) - (WINDOW - 1)) // 2)
-
     def swa_range(self):
         """(first raw position, count) of the window rows the queries read"""
         first = max(0, int(self.q_positions()[0]) - (WINDOW - 1))

@@ -157,7 +157,7 @@ def test_short_contexts_pad_with_minus_one(csa):
     for T in (128, 130, 200, 256):
         wl = scaled(WORKLOADS[0], T=T, k=64)
         step = check_walk(csa, wl, [0])
-        n = wl.n_elig(T - 1)
+        n = oracle.n_elig(T - 1)
         idx = step.idx[0, 0, 0].cpu().numpy()
         assert (idx[n:] == -1).all() and sorted(idx[:n].tolist()) == list(range(n))
 

@@ -86,10 +86,11 @@ def test_sparse_with_k_covering_all_entries_equals_dense():
 def test_eligibility_rule_and_window_are_disjoint_and_cover_the_context():
     """global entry i covers raw positions 2i, 2i+1; a query at p reads entries
     lying wholly before its window [p-127, p] and the window rows themselves"""
-    from synth.workloads import WORKLOADS
-    wl = WORKLOADS[0]
+    # the decode queries of the workloads: T - 1 for T = 2048, 131072, 1048576
+    assert [oracle.n_elig(T - 1) for T in (2048, 131072, 1048576)] == [960, 65472, 524224]
+    assert oracle.n_elig(0) == 0 and oracle.n_elig(126) == 0 and oracle.n_elig(128) == 0
     for p in [127, 128, 129, 130, 255, 2047, 131071]:
-        n = wl.n_elig(p)
+        n = oracle.n_elig(p)
         covered = set(range(0, 2 * n))
         window = set(range(max(0, p - 127), p + 1))
         assert not covered & window
@@ -110,7 +111,7 @@ def test_tiny_workload_walk_and_dense_agreement():
     # with k covering every eligible entry the walk's output equals dense attention
     small = scaled(wl, T=512, k=256)
     res = oracle.run_sequence(small, 0)
-    n_elig = small.n_elig(small.T - 1)
+    n_elig = oracle.n_elig(small.T - 1)
     assert sorted(res["idx"][0][0][:n_elig].tolist()) == list(range(n_elig))
     lc, ls, _, _ = oracle.sequence_cache(small, 0)
     dense, _ = oracle.dense_attention(small.q(0, 0)[0], n_elig, lc, ls, small.window(0, 0))

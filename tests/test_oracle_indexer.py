@@ -186,5 +186,5 @@ def test_walk_reuse_copies_and_reindex_stays_in_pool():
     for l in (1, 2):
         assert set(res["idx"][l][0].tolist()) <= set(pool.tolist())
     assert np.array_equal(res["idx"][3], res["idx"][2]) and np.array_equal(res["idx"][4], res["idx"][2])
-    n_elig = wl.n_elig(wl.T - 1)
+    n_elig = oracle.n_elig(wl.T - 1)
     assert res["idx"][0].max() < n_elig

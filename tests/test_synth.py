@@ -51,9 +51,7 @@ def test_bf16_is_rne_of_f32():
 
 def test_workload_shapes():
     w0 = WORKLOADS[0]
-    assert w0.n_elig(w0.T - 1) == 960
-    assert WORKLOADS[2].n_elig(WORKLOADS[2].T - 1) == 65472
-    assert WORKLOADS[3].n_elig(WORKLOADS[3].T - 1) == 524224
+    assert (w0.T, WORKLOADS[2].T, WORKLOADS[3].T) == (2048, 131072, 1048576)
     w4 = WORKLOADS[4]
     assert w4.n_q == 8192 and w4.swa_range() == (122880 - 127, 8192 + 127)
     small = scaled(w0, T=512)

@@ -70,6 +70,41 @@ def test_noalloc_reindex_matches_workspace_reindex_twice(csa):
                        csa.csa2_reindex(csa.REINDEX, cache, 128, qc, qs, w, pool))
 
 
+def _noalloc(csa, cache, qc, qs, w, pool, k):
+    lib = csa.load()
+    B, n_q, pool_len = pool.shape
+    out = torch.full((B, n_q, k), -7, dtype=torch.int32, device="cuda")
+    c = cache.struct()
+    st = lib.csa2_reindex_noalloc(ctypes.byref(c), ctypes.c_void_p(qc.data_ptr()), ctypes.c_void_p(qs.data_ptr()),
+                                  ctypes.c_void_p(w.data_ptr()), n_q, 8, ctypes.c_void_p(pool.data_ptr()), pool_len,
+                                  k, ctypes.c_void_p(out.data_ptr()),
+                                  ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == csa.OK
+    torch.cuda.synchronize()
+    return out
+
+
+def test_noalloc_large_pool_after_a_differently_shaped_call_matches_the_oracle(csa):
+    """a pool above 2048 slots takes the bounds + selection kernels; run it right
+    after a small call, so it finds the scratch holding another call's data"""
+    cache, qc, qs, w, pool = _case(csa, 70, 2, 3, 3000, 300)
+    _noalloc(csa, cache, qc, qs, w, pool, 32)
+    B, n_q, n, pool_len, k = 2, 2, 9000, 5000, 512
+    cache, qc, qs, w, pool = _case(csa, 71, B, n_q, n, pool_len)
+    for _ in range(2):
+        out = _noalloc(csa, cache, qc, qs, w, pool, k)
+        assert torch.equal(out, csa.csa2_reindex(csa.REINDEX, cache, k, qc, qs, w, pool))
+    kc = cache.ikey_codes.cpu().numpy()
+    ks = cache.ikey_scales.cpu().numpy()
+    qcn, qsn, wn, pn = qc.cpu().numpy(), qs.cpu().numpy(), w.cpu().numpy(), pool.cpu().numpy()
+    for b in range(B):
+        for q in range(n_q):
+            ids = pn[b, q]
+            S = oracle.index_scores(kc[b], ks[b], qcn[b, q], qsn[b, q], wn[b, q], ids=ids)
+            S = np.where(ids >= 0, S, -np.inf)
+            assert np.array_equal(out[b, q].cpu().numpy(), oracle.topk(S, k, ids=ids))
+
+
 def test_noalloc_reindex_rejects_requests_beyond_its_scratch(csa):
     lib = csa.load()
     c = csa._CacheStruct(256, 256, 256, 256, 64, 100000, 512, 128)
