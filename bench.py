@@ -390,32 +390,27 @@ def measure_ops(step, stream, reps):
     launching stream; no host launch time is inside the measurement"""
     import torch
     import compressed_sparse_attention_decode_gb300 as csa
-    from compressed_sparse_attention_decode_gb300.decode import REUSE
     calls = {}
 
     def add(name, fn):
         calls.setdefault(name, []).append(fn)
 
-    prev = None
     t = 0
     for l, mode in enumerate(step.layers):
-        idx_l = step.idx[l]
-        if mode == "reuse":
-            add("reuse", lambda p=prev, o=idx_l: csa.csa2_reindex(REUSE, step.cache, step.k, prev_idx=p, idx_out=o,
-                                                                   n_q=step.n_q))
-        elif mode == "full":
+        idx_l = step.layer_idx(l)
+        if mode == "full":
             add("quantize_iq", lambda t=t: csa.csa2_quantize_fp4(step.iq[t], step.iq_codes, step.iq_scales))
             add("indexer_full", lambda t=t, o=idx_l: csa.csa2_indexer_topk(
                 step.cache, step.iq_codes, step.iq_scales, step.w_head[t], step.q_pos, step.k,
                 step.pool_blocks, step.bs, idx_out=o, pool_out=step.pool, ws=step.ws_full))
             t += 1
-        else:
+        elif mode == "reindex":
             add("reindex", lambda t=t, o=idx_l: csa.csa2_reindex_f32(step.cache, step.k, step.iq[t], step.w_head[t],
                                                                      step.pool, idx_out=o, ws=step.ws_re))
             t += 1
+        # a Reuse layer launches nothing: its attention reads the latest indices in place
         add("sparse_attn", lambda l=l, i=idx_l: csa.csa2_sparse_attn(step.cache, step.q[l], step.q_pos, i, step.win[l],
                                                                      step.swa_pos0, out=step.out[l], ws=step.ws_attn))
-        prev = idx_l
     out = {}
     for name, fns in calls.items():
         for fn in fns:               # eager warm-up of this entry point's calls

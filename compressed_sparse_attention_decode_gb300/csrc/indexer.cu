@@ -13,6 +13,7 @@
 // error bounds).  Selection then needs exact scores only for entries whose
 // interval reaches the k-th largest lower bound: usually k plus a handful.
 #include "indexer_common.cuh"
+#include "umma.cuh"
 
 namespace csa2 {
 
@@ -505,69 +506,191 @@ __global__ void __launch_bounds__(512) k_pool_bounds(const int32_t* __restrict__
     lu[gq * pool_len + t] = make_float2(lo, hi);
 }
 
-// Reindex over a pool that fits one block's sort (pool_len <= MAX_K): every
-// slot's exact score, one thread per slot, blockIdx.z taking 512 slots; an
-// empty slot gets key 0, below every real score's key.
+// Reindex over a pool of at most RX_POOL slots in one launch ("DeepSeek-v4.1
+// Flash" §2.3.2 and §2.3.4: the indexer re-run on the Full layer's candidate
+// pool).  A cluster of RX_CTAS blocks per query: block r bounds the exact
+// score of slots [512 r, 512 r + 512) (the same (S~-E, S~+E) interval as the
+// scans) and stores the bounds into the shared memory of block 0 (distributed
+// shared memory).  Block 0 then
+//   - finds lam <= the k-th largest lower bound and mu >= the (k+1)-th
+//     largest upper bound (value-bucket bands);
+//   - keeps every slot whose lower bound is above mu (at most k slots have an
+//     upper bound above mu, so it is among the k best), drops every slot whose
+//     upper bound is below lam (k slots have a lower bound at or above lam);
+//   - scores the undecided rest exactly and keeps the best of them by (exact
+//     score desc, entry asc) for the remaining places;
+//   - writes the chosen entries in ascending order, -1 padded.
+constexpr int RX_CTAS = 4;
+constexpr int RX_THREADS = 512;
+constexpr int RX_POOL = RX_CTAS * RX_THREADS;
+
+struct ReindexSmem {
+    float2 lu[RX_POOL];       // bounds of every slot (-inf, -inf for an empty slot)
+    int ent[RX_POOL];         // entry of every slot, -1 = empty
+    int und[RX_POOL];         // undecided slots
+    unsigned char chosen[RX_POOL];
+};
+
 template <int DI>
-__global__ void __launch_bounds__(512, 2) k_pool_exact(const int32_t* __restrict__ pool, int pool_len,
-                                                    const uint8_t* __restrict__ kc_all,
-                                                    const uint8_t* __restrict__ ks_all, int capacity,
-                                                    const uint8_t* __restrict__ iq_codes,
-                                                    const uint8_t* __restrict__ iq_scales, const float* __restrict__ iq_raw,
-                                                    const float* __restrict__ w_head, int n_q, int H,
-                                                    unsigned long long* __restrict__ keys) {
+__global__ void __launch_bounds__(RX_THREADS) k_reindex_fused(const int32_t* __restrict__ pool, int pool_len,
+                                                               const uint8_t* __restrict__ kc_all,
+                                                               const uint8_t* __restrict__ ks_all, int capacity,
+                                                               const uint8_t* __restrict__ iq_codes,
+                                                               const uint8_t* __restrict__ iq_scales,
+                                                               const float* __restrict__ iq_raw,
+                                                               const float* __restrict__ w_head, int n_q, int H, int k,
+                                                               int32_t* __restrict__ idx_out) {
     pdl_wait();
     pdl_launch_next();
+    // dynamic shared memory: the staged query | key2 | id2 | din | ReindexSmem
     extern __shared__ int qsm[];
-    const int ql = blockIdx.x, b = blockIdx.y;
+    __shared__ SelectSmem sm;
+    uint8_t* extra = reinterpret_cast<uint8_t*>(qsm + QView<DI>::words(H));
+    sm.key2 = reinterpret_cast<unsigned long long*>(extra);
+    sm.id2 = reinterpret_cast<int*>(extra + (size_t)MAX_K * 8);
+    sm.din = sm.id2 + MAX_K;
+    ReindexSmem& rx = *reinterpret_cast<ReindexSmem*>(extra + SEL_DYN_EXTRA);
+    const uint32_t rank = umma::cluster_rank();
+    const int ql = blockIdx.y, b = blockIdx.z;
     const int64_t gq = (int64_t)b * n_q + ql;
+    const int tid = threadIdx.x;
+    umma::cluster_arrive_relaxed();          // waited for before the first store into block 0
     QView<DI> v;
     v.bind(qsm, H);
     stage_query<DI>(v, iq_codes + gq * H * (DI / 2), iq_scales + gq * H * (DI / 16),
-                    iq_raw ? iq_raw + gq * H * DI : nullptr, w_head + gq * H, H, threadIdx.x,
-                    blockDim.x);
+                    iq_raw ? iq_raw + gq * H * DI : nullptr, w_head + gq * H, H, tid, RX_THREADS);
     __syncthreads();
-    const int t = blockIdx.z * blockDim.x + threadIdx.x;
-    if (t >= pool_len) return;
-    const int j = pool[gq * pool_len + t];
-    unsigned long long key = 0ull;
-    if (j >= 0 && j < capacity) {
-        const int64_t row = (int64_t)b * capacity + j;
-        key = f64_key(exact_score<DI>(kc_all + row * (DI / 2), ks_all + row * (DI / 16), v, H));
+    const int t = (int)rank * RX_THREADS + tid;
+    int j = -1;
+    float lo = -INFINITY, hi = -INFINITY;
+    if (t < pool_len) {
+        j = pool[gq * pool_len + t];
+        if (j >= 0 && j < capacity) {
+            KeyRow<DI> kr;
+            const int64_t row = (int64_t)b * capacity + j;
+            kr.load(kc_all + row * (DI / 2), ks_all + row * (DI / 16));
+            approx_score<DI>(kr, v, H, bound_factor(H, DI), lo, hi);
+        } else {
+            j = -1;
+        }
     }
-    keys[gq * pool_len + t] = key;
-}
+    umma::cluster_wait();
+    {
+        const uint32_t a_lu = umma::mapa(umma::smem_u32(&rx.lu[t]), 0);
+        const uint32_t a_id = umma::mapa(umma::smem_u32(&rx.ent[t]), 0);
+        asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(a_lu), "f"(lo), "f"(hi) : "memory");
+        asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(a_id), "r"(j) : "memory");
+    }
+    umma::cluster_sync();                    // every slot's bounds are in block 0
+    if (rank != 0) return;
 
-// Reindex, second pass for such a pool: one block per query keeps the k best
-// slots by (exact score desc, entry asc) and writes their entries in ascending
-// order, -1 where fewer than k slots hold an entry.
-__global__ void __launch_bounds__(512) k_pool_rank(const int32_t* __restrict__ pool, int pool_len,
-                                                   const unsigned long long* __restrict__ keys, int capacity, int k,
-                                                   int32_t* __restrict__ idx_out) {
-    pdl_wait();
-    pdl_launch_next();
-    extern __shared__ unsigned long long sdyn[];
-    __shared__ SelectSmem sm;
-    const int64_t gq = (int64_t)blockIdx.y * gridDim.x + blockIdx.x;
-    sm.key2 = sdyn;
-    sm.id2 = reinterpret_cast<int*>(sdyn + MAX_K);
-    sm.din = sm.id2 + MAX_K;
-    sm.bitmap = reinterpret_cast<unsigned int*>(sm.din + MAX_K);
+    const int n = pool_len < RX_POOL ? pool_len : RX_POOL;
     sm.rs.whist = sm.whist;
-    for (int t = threadIdx.x; t < pool_len; t += blockDim.x) {
-        const int j = pool[gq * pool_len + t];
-        const bool ok = j >= 0 && j < capacity;
-        sm.key[t] = ok ? keys[gq * pool_len + t] : 0ull;
-        sm.id[t] = ok ? j : 0;
+    if (tid == 0) {
+        sm.rs.ctl[0] = 0;
+        sm.rs.ctl[3] = 0;
     }
-    const bool clear = capacity <= SEL_BITMAP_BITS;      // the bitmap of ascending_ids, zeroed meanwhile
-    if (clear)
-        for (int w = threadIdx.x; w < (capacity + 31) >> 5; w += blockDim.x) sm.bitmap[w] = 0u;
     __syncthreads();
-    select_best_set(pool_len, k, sm);
-    const int kept = ascending_ids(sm.id, sm.id2, pool_len, capacity, sm.din, sm, clear);
+    int c = 0;
+    for (int u = tid; u < n; u += RX_THREADS) {
+        rx.chosen[u] = 0;
+        c += rx.ent[u] >= 0;
+    }
+    c = __reduce_add_sync(0xffffffffu, c);
+    if ((tid & 31) == 0) atomicAdd(&sm.rs.ctl[3], c);
+    __syncthreads();
+    const int n_valid = sm.rs.ctl[3];
+    __syncthreads();
+    if (n_valid <= k) {
+        for (int u = tid; u < n; u += RX_THREADS) rx.chosen[u] = rx.ent[u] >= 0;
+    } else {
+        const unsigned int lam = block_kth_bound(
+            [&](int u, unsigned int& key) {
+                key = f32_key(rx.lu[u].x);
+                return true;
+            },
+            n, k, false, sm.rs);
+        const unsigned int mu = block_kth_bound(
+            [&](int u, unsigned int& key) {
+                key = f32_key(rx.lu[u].y);
+                return true;
+            },
+            n, k + 1, true, sm.rs);
+        // sure-in and undecided slots (empty slots have -inf bounds: never in, never undecided)
+        if (tid == 0) {
+            sm.rs.ctl[0] = 0;
+            sm.rs.ctl[3] = 0;
+        }
+        __syncthreads();
+        int ns = 0;
+        for (int u0 = 0; u0 < n; u0 += RX_THREADS) {
+            const int u = u0 + tid;
+            bool und = false;
+            if (u < n && rx.ent[u] >= 0) {
+                const float2 b2 = rx.lu[u];
+                if (f32_key(b2.x) > mu) {
+                    rx.chosen[u] = 1;
+                    ++ns;
+                } else if (f32_key(b2.y) >= lam) {
+                    und = true;
+                }
+            }
+            const int pos = append_slot(und, &sm.rs.ctl[0]);
+            if (und) rx.und[pos] = u;
+        }
+        ns = __reduce_add_sync(0xffffffffu, ns);
+        if ((tid & 31) == 0) atomicAdd(&sm.rs.ctl[3], ns);
+        __syncthreads();
+        const int nu = sm.rs.ctl[0], r = k - sm.rs.ctl[3];
+        __syncthreads();
+        if (r > 0) {
+            // exact scores of the undecided slots, then the r best of them
+            const uint8_t* kc = kc_all + (int64_t)b * capacity * (DI / 2);
+            const uint8_t* ks = ks_all + (int64_t)b * capacity * (DI / 16);
+            for (int i = tid; i < nu; i += RX_THREADS) {
+                const int jj = rx.ent[rx.und[i]];
+                sm.key[i] = f64_key(exact_score<DI>(kc + (int64_t)jj * (DI / 2), ks + (int64_t)jj * (DI / 16), v, H));
+                sm.id[i] = jj;
+            }
+            __syncthreads();
+            select_best_set(nu, r, sm);
+            for (int i = tid; i < nu; i += RX_THREADS)
+                if (sm.id2[i]) rx.chosen[rx.und[i]] = 1;
+        }
+    }
+    __syncthreads();
+    // the chosen entries in slot order (each thread takes consecutive slots), then in ascending
+    // entry order: an HSI pool is already ascending, any other pool is sorted here
+    constexpr int PER = RX_POOL / RX_THREADS;
+    int cnt = 0;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int u = tid * PER + i;
+        cnt += (u < n && rx.chosen[u]) ? 1 : 0;
+    }
+    int kept;
+    int pos = block_exclusive_scan(cnt, &kept, sm.rs.hist);
+    int* list = sm.din;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int u = tid * PER + i;
+        if (u < n && rx.chosen[u]) list[pos++] = rx.ent[u];
+    }
+    __syncthreads();
+    bool unordered = false;
+    for (int i = tid; i + 1 < kept; i += RX_THREADS) unordered |= list[i] >= list[i + 1];
+    if (__syncthreads_or(unordered)) {
+        for (int i = tid; i < kept; i += RX_THREADS) {
+            sm.id[i] = list[i];
+            sm.key[i] = 0ull;
+        }
+        __syncthreads();
+        sort_kept(kept, false, sm);
+        for (int i = tid; i < kept; i += RX_THREADS) list[i] = sm.id[i];
+        __syncthreads();
+    }
     int32_t* out = idx_out + gq * k;
-    for (int t = threadIdx.x; t < k; t += blockDim.x) out[t] = t < kept ? sm.din[t] : -1;
+    for (int i = tid; i < k; i += RX_THREADS) out[i] = i < kept ? list[i] : -1;
 }
 
 // One block per (sequence, query).  Items t in [0, n): entry ids[t] (-1 =
@@ -875,6 +998,10 @@ static size_t ws_bytes(int64_t slabs, int64_t n) {
 }
 
 bool scan_tc_supported(int d_idx, int H, int QB, int pool_blocks, int bs);
+bool reindex_tc_supported(int d_idx, int H, int pool_len);
+cudaError_t launch_reindex_tc(const csa2_cache& c, const uint8_t* iq_codes, const uint8_t* iq_scales,
+                              const float* iq_raw, const float* w_head, int n_q, const int32_t* pool, int pool_len,
+                              int k, int32_t* idx_out, int* err, cudaStream_t st);
 cudaError_t launch_scan_full_tc(const csa2_cache& c, const uint8_t* iq_codes, const uint8_t* iq_scales,
                                 const float* w_head, int n_q, const int64_t* q_pos, int q0, int n_qc, int H, int k,
                                 int pool_blocks, int bs, int* counts, int* cid, float2* clu, int* bid, float2* blu,
@@ -943,21 +1070,35 @@ cudaError_t launch_reindex_t(const csa2_cache& c, const uint8_t* iq_codes, const
                              int k, int32_t* idx_out, void* ws, cudaStream_t st) {
     const SelectWs w = carve(ws, (int64_t)c.batch * n_q, pool_len);
     const size_t qwords = (size_t)QView<DI>::words(H) * sizeof(int);
-    dim3 g0(n_q, c.batch, (pool_len + 511) / 512);
-    if (pool_len <= MAX_K) {
-        // small pool: exact scores for every slot, then one sort per query
-        launch_k(k_pool_exact<DI>, g0, 512, qwords, st, pool, pool_len, c.ikey_codes, c.ikey_scales, c.capacity, iq_codes,
-                                                   iq_scales, iq_raw, w_head, n_q, H, w.c2key);
-        note_launch();
-        cudaError_t e = cudaGetLastError();
+    if (reindex_tc_supported(DI, H, pool_len))
+        return launch_reindex_tc(c, iq_codes, iq_scales, iq_raw, w_head, n_q, pool, pool_len, k, idx_out, w.err, st);
+    if (pool_len <= RX_POOL) {
+        // one launch: a cluster of RX_CTAS blocks per query
+        const size_t smem = qwords + SEL_DYN_EXTRA + sizeof(ReindexSmem);
+        cudaError_t e = cudaFuncSetAttribute(k_reindex_fused<DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        const size_t smr = SEL_DYN_EXTRA + SEL_BITMAP_BYTES;
-        e = cudaFuncSetAttribute(k_pool_rank, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smr);
-        if (e != cudaSuccess) return e;
-        launch_k(k_pool_rank, dim3(n_q, c.batch), 512, smr, st, pool, pool_len, w.c2key, c.capacity, k, idx_out);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(RX_CTAS, n_q, c.batch);
+        cfg.blockDim = dim3(RX_THREADS);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = RX_CTAS;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        e = cudaLaunchKernelEx(&cfg, k_reindex_fused<DI>, pool, pool_len, (const uint8_t*)c.ikey_codes,
+                               (const uint8_t*)c.ikey_scales, c.capacity, iq_codes, iq_scales, iq_raw, w_head, n_q, H, k,
+                               idx_out);
         note_launch();
+        if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }
+    dim3 g0(n_q, c.batch, (pool_len + 511) / 512);
     launch_k(k_pool_bounds<DI>, g0, 512, qwords, st, pool, pool_len, c.ikey_codes, c.ikey_scales, c.capacity, iq_codes,
                                                 iq_scales, iq_raw, w_head, n_q, H, w.lu);
     note_launch();

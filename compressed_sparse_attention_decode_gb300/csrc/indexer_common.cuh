@@ -37,9 +37,12 @@ struct QView {
 // One query's view: from its FP4 codes and scales, or (raw != nullptr) from
 // its unquantised fp32 values, which are quantised here exactly as the query
 // quantisation kernel does it (quant_group16, one 16-value group per thread).
+// packed != nullptr also receives each group's 8 code bytes (the FP4 codes as
+// the tensor-core operands take them).
 template <int DI>
 __device__ void stage_query(QView<DI> v, const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
-                            const float* __restrict__ raw, const float* __restrict__ w, int H, int tid, int nthr) {
+                            const float* __restrict__ raw, const float* __restrict__ w, int H, int tid, int nthr,
+                            uint2* packed = nullptr) {
     if (raw != nullptr) {
         for (int g = tid; g < H * (DI / 16); g += nthr) {
             float x[16];
@@ -53,6 +56,7 @@ __device__ void stage_query(QView<DI> v, const uint8_t* __restrict__ codes, cons
             }
             uint32_t c0, c1, sb;
             quant_group16(x, c0, c1, sb);
+            if (packed) packed[g] = make_uint2(c0, c1);
             v.qp[4 * g] = (int)unpack4_int8(c0 & 0xffffu);
             v.qp[4 * g + 1] = (int)unpack4_int8(c0 >> 16);
             v.qp[4 * g + 2] = (int)unpack4_int8(c1 & 0xffffu);
@@ -66,6 +70,7 @@ __device__ void stage_query(QView<DI> v, const uint8_t* __restrict__ codes, cons
         for (int i = tid; i < H * (DI / 16); i += nthr) {
             v.qsc[i] = e4m3_to_f32(scales[i]);
             v.qsi[i] = e4m3_times_512(scales[i]);
+            if (packed) packed[i] = *reinterpret_cast<const uint2*>(codes + (size_t)i * 8);
         }
     }
     for (int i = tid; i < H; i += nthr) {

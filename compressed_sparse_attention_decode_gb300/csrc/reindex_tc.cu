@@ -1,0 +1,509 @@
+// Reindex on the tensor cores: the indexer re-run on the Full layer's
+// candidate pool, top k kept ("DeepSeek-v4.1 Flash: KVキャッシュ圧縮の限界を押し
+// 広げる", §2.3.2 Reindex mode, §2.3.4 HSI pool).  One launch per layer.
+//
+// A cluster of RT_CTAS blocks per query; block r takes pool slots
+// [512 r, 512 r + 512) as four tiles of 128 (one slot per thread):
+//   - the key rows of its slots are gathered (8-byte asynchronous copies) into
+//     the kind::f8f6f4 operand layout (each 16-value group: 8 code bytes, 8
+//     zero bytes), the query's codes into a block-diagonal operand (row
+//     (head, group) holds that head's codes of that group, zeros elsewhere);
+//   - D = keys . query^T (M = 128 slots, N = 8 heads x 8 groups, K = 128) holds
+//     the exact group sums in TMEM, from which every slot gets the same fp32
+//     score and rigorous error bound as the scans: the exact score lies in
+//     [lo, hi];
+//   - the bounds go into the shared memory of block 0, and each block adds the
+//     count, smallest lower and largest upper bound of its slots into block 0
+//     (cluster-scope atomics).
+// Block 0 then selects with a few block-wide phases:
+//   - one pass builds two histograms of 1024 equal-width value buckets, of the
+//     lower and of the upper bounds; bucket b_lam holds the k-th largest lower
+//     bound, bucket b_mu the (k+1)-th largest upper bound;
+//   - a slot whose lower bound lies in a bucket above b_mu is in (at most k
+//     slots have an upper bound in those buckets, itself included); a slot
+//     whose upper bound lies in a bucket below b_lam is out (at least k slots
+//     have a lower bound in bucket b_lam or above, all larger than it);
+//   - the undecided rest is scored exactly (one warp per slot: int64 group
+//     terms, then the fp64 head chain in ascending head order) and ranked by
+//     (exact score desc, entry asc) for the places left;
+//   - the chosen entries are written in ascending entry order, -1 padded.
+#include "indexer_common.cuh"
+#include "umma.cuh"
+
+namespace csa2 {
+
+constexpr int RT_CTAS = 4;
+constexpr int RT_THREADS = 512;
+constexpr int RT_TILE = 128;
+constexpr int RT_TILES = 4;
+constexpr int RT_SLOTS = RT_TILE * RT_TILES;       // 512 slots per block
+constexpr int RT_POOL = RT_CTAS * RT_SLOTS;        // 2048 slots per query
+constexpr int RT_DI = 128, RT_G = 8, RT_H = 8, RT_N = RT_H * RT_G;
+constexpr int RT_NB = 1024;                        // histogram buckets
+
+// shared memory, from a 1024-byte aligned base
+constexpr uint32_t RT_A = 0;                                     // 4 tiles x 128 rows x 128 B
+constexpr uint32_t RT_B = RT_A + RT_TILES * RT_TILE * 128;       // 64 rows x 128 B
+constexpr uint32_t RT_SC = RT_B + RT_N * 128;                    // key scales, 8 B per slot
+constexpr uint32_t RT_ENT = RT_SC + RT_SLOTS * 8;                // entry of each slot of the block
+constexpr uint32_t RT_Q = RT_ENT + RT_SLOTS * 4;                 // QView<128>, packed codes, sq
+constexpr uint32_t RT_LU = RT_Q + 4096;                          // block 0: bounds of every pool slot
+constexpr uint32_t RT_PENT = RT_LU + RT_POOL * 8;                // block 0: entry of every pool slot
+constexpr uint32_t RT_END = RT_PENT + RT_POOL * 4;
+constexpr uint32_t RT_DYN = RT_END + 1024;
+
+// Block 0's selection state, laid over its A tiles once its MMAs are done.
+struct RtSel {
+    int und[RT_POOL];
+    unsigned long long ukey[RT_POOL];
+    int hist[2 * RT_NB];           // lower-bound and upper-bound buckets; then the output list
+    unsigned char chosen[RT_POOL];
+    int wtot[RT_POOL / RT_THREADS][RT_THREADS / 32];   // chosen slots per (chunk, warp)
+    int ctl[8];                    // [0] undecided count [1] sure-in count [2] valid count [3] b_lam [4] b_mu
+    unsigned int kmin, kmax;
+};
+static_assert(sizeof(RtSel) <= RT_TILES * RT_TILE * 128, "selection state must fit the A tiles");
+
+__device__ __forceinline__ uint32_t rt_swz(uint32_t row, uint32_t unit) { return row * 128 + ((unit ^ (row & 7)) << 4); }
+
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ int rt_bucket(float x, float vmin, float scale) {
+    return min((int)((x - vmin) * scale), RT_NB - 1);
+}
+
+// warp-wide search of the bucket of hist[RT_NB] in which the count from the top
+// first reaches `need`: lane l sums its 32 buckets, a warp scan finds the
+// lane, then the warp scans that lane's 32 buckets one per lane
+__device__ int rt_find_bucket(const int* hist, int need) {
+    const int lane = threadIdx.x & 31;
+    constexpr int PER = RT_NB / 32;
+    const int top = RT_NB - PER * lane;            // lane 0 holds the top buckets
+    int c = 0;
+#pragma unroll
+    for (int i = 1; i <= PER; ++i) c += hist[top - i];
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    unsigned hit = __ballot_sync(0xffffffffu, incl >= need);
+    const int L = hit ? __ffs(hit) - 1 : 31;
+    const int before = __shfl_sync(0xffffffffu, incl - c, L);
+    // lane i takes bucket (top of lane L) - 1 - i
+    const int bk = RT_NB - PER * L - 1 - lane;
+    int cum = hist[bk];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, cum, o);
+        if (lane >= o) cum += y;
+    }
+    hit = __ballot_sync(0xffffffffu, before + cum >= need);
+    const int i = hit ? __ffs(hit) - 1 : 31;
+    return RT_NB - PER * L - 1 - i;
+}
+
+// The query's FP4 codes and its view for the exact scores, from its fp32
+// values: four threads per 16-value group (each takes four values), with the
+// arithmetic of the query quantisation kernel (the group's scale from its
+// largest magnitude; nearest E2M1 code by exact threshold comparisons).
+__device__ void rt_quantize_query(QView<RT_DI> v, uint2* packed, const float* __restrict__ raw, int tid) {
+    const int g = tid >> 2, q4 = tid & 3;                  // group g, values 4 q4 .. 4 q4 + 3
+    const float4 x4 = __ldg(reinterpret_cast<const float4*>(raw + (int64_t)g * 16) + q4);
+    const float x[4] = {x4.x, x4.y, x4.z, x4.w};
+    float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const uint32_t sb = f32_to_e4m3_satfinite(__fdiv_rn(amax, 6.0f));
+    const float sc = e4m3_to_f32(sb);
+    uint32_t nib = 0u;
+    if (sc > 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) nib |= e2m1_code(x[i], sc) << (4 * i);
+    }
+    v.qp[4 * g + q4] = (int)unpack4_int8(nib);
+    const uint32_t n1 = __shfl_xor_sync(0xffffffffu, nib, 1);
+    const uint32_t n2 = __shfl_xor_sync(0xffffffffu, nib, 2);
+    const uint32_t n3 = __shfl_xor_sync(0xffffffffu, nib, 3);
+    if (q4 == 0) {
+        packed[g] = make_uint2(nib | (n1 << 16), n2 | (n3 << 16));
+        v.qsc[g] = sc;
+        v.qsi[g] = e4m3_times_512(sb);
+    }
+}
+
+__device__ __forceinline__ void red_cluster_u32(uint32_t addr, uint32_t val, int op) {
+    if (op == 0) asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(val) : "memory");
+    else if (op == 1) asm volatile("red.shared::cluster.min.u32 [%0], %1;" ::"r"(addr), "r"(val) : "memory");
+    else asm volatile("red.shared::cluster.max.u32 [%0], %1;" ::"r"(addr), "r"(val) : "memory");
+}
+
+__global__ void __launch_bounds__(RT_THREADS, 2) k_reindex_tc(const int32_t* __restrict__ pool, int pool_len,
+                                                               const uint8_t* __restrict__ kc_all,
+                                                               const uint8_t* __restrict__ ks_all, int capacity,
+                                                               const uint8_t* __restrict__ iq_codes,
+                                                               const uint8_t* __restrict__ iq_scales,
+                                                               const float* __restrict__ iq_raw,
+                                                               const float* __restrict__ w_head, int n_q, int k,
+                                                               int32_t* __restrict__ idx_out, int* __restrict__ err) {
+    pdl_wait();
+    pdl_launch_next();
+    extern __shared__ uint8_t dyn[];
+    __shared__ __align__(8) unsigned long long bar_mma;
+    __shared__ uint32_t tmem_base;
+    __shared__ unsigned int s_stat[3];        // block 0: valid slots, smallest lower / largest upper bound key
+    __shared__ unsigned int l_stat[3];        // this block's own
+    const uint32_t raw_base = umma::smem_u32(dyn);
+    const uint32_t base = (raw_base + 1023u) & ~1023u;
+    uint8_t* sm = dyn + (base - raw_base);
+    const uint32_t rank = umma::cluster_rank();
+    const int ql = blockIdx.y, b = blockIdx.z;
+    const int64_t gq = (int64_t)b * n_q + ql;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int s0 = (int)rank * RT_SLOTS;                    // first pool slot of this block
+    int* ent = reinterpret_cast<int*>(sm + RT_ENT);
+    uint8_t* scl = sm + RT_SC;
+    QView<RT_DI> v;
+    v.bind(reinterpret_cast<int*>(sm + RT_Q), RT_H);
+    uint2* packed = reinterpret_cast<uint2*>(sm + RT_Q + QView<RT_DI>::words(RT_H) * 4);
+    float* sq = reinterpret_cast<float*>(packed + RT_N);
+    bool ok = true;
+
+    if (tid == 0) {
+        umma::mbar_init(umma::smem_u32(&bar_mma), 1);
+        umma::fence_mbar_init();
+        s_stat[0] = 0u;
+        s_stat[1] = ~0u;
+        s_stat[2] = 0u;
+        l_stat[0] = 0u;
+        l_stat[1] = ~0u;
+        l_stat[2] = 0u;
+    }
+    // block 0's counters are set before any block adds into them
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    if (warp == 0) umma::tmem_alloc(umma::smem_u32(&tmem_base), RT_TILES * 64);
+    const int sl = tid;                                     // this thread's slot of the block
+    int j = -1;
+    if (s0 + sl < pool_len) {
+        j = pool[gq * pool_len + s0 + sl];
+        if (j < 0 || j >= capacity) j = -1;
+    }
+    // zero the A tiles (the pad half of every 16-byte unit, and the rows of empty slots)
+    for (int i = tid; i < RT_TILES * RT_TILE * 8; i += RT_THREADS)
+        reinterpret_cast<uint4*>(sm + RT_A)[i] = make_uint4(0, 0, 0, 0);
+    __syncthreads();
+    // gather this slot's key row: the codes of group g into the data half of unit g
+    ent[sl] = j;
+    if (j >= 0) {
+        const uint8_t* kc = kc_all + ((int64_t)b * capacity + j) * (RT_DI / 2);
+        const uint32_t row = base + RT_A + (sl / RT_TILE) * (RT_TILE * 128);
+#pragma unroll
+        for (int g = 0; g < RT_G; ++g) cp_async8(row + rt_swz(sl % RT_TILE, g), kc + 8 * g);
+        cp_async8(base + RT_SC + sl * 8, ks_all + ((int64_t)b * capacity + j) * RT_G);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    // meanwhile: the query, and its block-diagonal operand
+    if (iq_raw) {
+        if (tid < RT_N * 4) rt_quantize_query(v, packed, iq_raw + gq * RT_H * RT_DI, tid);
+        if (tid < RT_H) {
+            v.w[tid] = w_head[gq * RT_H + tid];
+            v.wd[tid] = (double)v.w[tid] * 0x1p-20;
+        }
+    } else {
+        stage_query<RT_DI>(v, iq_codes + gq * RT_H * (RT_DI / 2), iq_scales + gq * RT_H * RT_G, nullptr,
+                           w_head + gq * RT_H, RT_H, tid, RT_THREADS, packed);
+    }
+    __syncthreads();
+    {
+        const int n = tid >> 3, u = tid & 7, g = n % RT_G;    // 64 rows x 8 units: one unit per thread
+        uint4 val = make_uint4(0, 0, 0, 0);
+        if (u == g) {
+            const uint2 c = packed[n];
+            val.x = c.x;
+            val.y = c.y;
+        }
+        *reinterpret_cast<uint4*>(sm + RT_B + rt_swz(n, u)) = val;
+        if (tid < RT_N) sq[tid] = v.qsc[tid];
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    umma::fence_proxy_async();
+    umma::fence_before();
+    __syncthreads();
+    umma::fence_after();
+    const uint32_t tmem = tmem_base;
+    if (tid == 0) {
+        const uint32_t idesc = (1u << 4) | (5u << 7) | (5u << 10) | ((uint32_t)(RT_N >> 3) << 17) |
+                               ((uint32_t)(RT_TILE >> 4) << 24);
+        for (int t = 0; t < RT_TILES; ++t) {
+            if (s0 + t * RT_TILE >= pool_len) break;
+#pragma unroll
+            for (int ks = 0; ks < RT_DI / 32; ++ks) {
+                const uint64_t ad = umma::desc(base + RT_A + t * (RT_TILE * 128) + ks * 32, 16, 1024, umma::LAYOUT_SW128);
+                const uint64_t bd = umma::desc(base + RT_B + ks * 32, 16, 1024, umma::LAYOUT_SW128);
+                asm volatile(
+                    "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+                    " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}" ::"r"(tmem + 64 * t),
+                    "l"(ad), "l"(bd), "r"(idesc), "r"(ks));
+            }
+        }
+        umma::commit(umma::smem_u32(&bar_mma));
+    }
+    ok &= umma::mbar_wait(umma::smem_u32(&bar_mma), 0);
+    umma::fence_after();
+    // bounds: warp w reads TMEM lane quarter w % 4 of tile w / 4; thread = tile row
+    const int t_ep = warp >> 2;
+    const int sl_ep = t_ep * RT_TILE + (warp & 3) * 32 + lane;
+    float2 mine = make_float2(-INFINITY, -INFINITY);
+    if (s0 + t_ep * RT_TILE < pool_len) {                    // warp-uniform
+        const uint32_t lb = tmem + ((uint32_t)((warp & 3) * 32) << 16) + 64 * t_ep;
+        const bool valid = ent[sl_ep] >= 0;
+        const uint2 skw = *reinterpret_cast<const uint2*>(scl + sl_ep * 8);
+        float skf[RT_G];
+#pragma unroll
+        for (int g = 0; g < RT_G; ++g) skf[g] = e4m3_to_f32(((g < 4 ? skw.x : skw.y) >> (8 * (g & 3))) & 255u);
+        float S = 0.0f, B = 0.0f;
+#pragma unroll
+        for (int hh = 0; hh < RT_H; hh += 4) {
+            float dv[4 * RT_G];
+#pragma unroll
+            for (int c = 0; c < 4 * RT_G; c += 16) umma::tmem_ld16(lb + hh * RT_G + c, dv + c);
+            umma::tmem_wait_ld();
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                float dd = 0.0f, A = 0.0f;
+#pragma unroll
+                for (int g = 0; g < RT_G; ++g) {
+                    const float tv = dv[h * RT_G + g] * (sq[(hh + h) * RT_G + g] * skf[g]);   // exact
+                    dd += tv;
+                    A += fabsf(tv);
+                }
+                S = __fmaf_rn(v.w[hh + h], fmaxf(dd, 0.0f), S);
+                B = __fmaf_rn(fabsf(v.w[hh + h]), A, B);
+            }
+        }
+        if (valid) {
+            const float E = B * bound_factor(RT_H, RT_DI);
+            mine = make_float2(S - E, S + E);
+        }
+    }
+    // this block's count and range of its slots' bounds
+    {
+        const bool valid = ent[sl_ep] >= 0 && s0 + sl_ep < pool_len;
+        const unsigned c = __popc(__ballot_sync(0xffffffffu, valid));
+        const unsigned mn = __reduce_min_sync(0xffffffffu, valid ? f32_key(mine.x) : ~0u);
+        const unsigned mx = __reduce_max_sync(0xffffffffu, valid ? f32_key(mine.y) : 0u);
+        if (lane == 0 && c) {
+            atomicAdd(&l_stat[0], c);
+            atomicMin(&l_stat[1], mn);
+            atomicMax(&l_stat[2], mx);
+        }
+    }
+    umma::fence_before();
+    __syncthreads();
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");   // block 0 exists and is set up
+    float2* glu = reinterpret_cast<float2*>(sm + RT_LU);    // meaningful in block 0
+    int* gent = reinterpret_cast<int*>(sm + RT_PENT);
+    {
+        const uint32_t a_lu = umma::mapa(umma::smem_u32(&glu[s0 + sl_ep]), 0);
+        const uint32_t a_en = umma::mapa(umma::smem_u32(&gent[s0 + sl_ep]), 0);
+        asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(a_lu), "f"(mine.x), "f"(mine.y) : "memory");
+        asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(a_en), "r"(ent[sl_ep]) : "memory");
+        if (tid < 3 && l_stat[0] > 0) red_cluster_u32(umma::mapa(umma::smem_u32(&s_stat[tid]), 0), l_stat[tid], tid);
+    }
+    umma::cluster_sync();                      // every slot's bounds, the counts and the range are in block 0
+    if (warp == 0) {
+        umma::fence_after();
+        umma::tmem_dealloc(tmem, RT_TILES * 64);
+    }
+    if (!ok) atomicExch(err, 1);
+    if (rank != 0) return;
+    RtSel& sel = *reinterpret_cast<RtSel*>(sm + RT_A);     // block 0's MMAs are done: its A tiles are free
+
+    // ================= block 0: selection over the n slots of the pool (slot u = c * 512 + tid)
+    const int n = pool_len < RT_POOL ? pool_len : RT_POOL;
+    constexpr int NCH = RT_POOL / RT_THREADS;
+    const int n_valid = (int)s_stat[0];
+    if (tid < 8) sel.ctl[tid] = 0;
+#pragma unroll
+    for (int ch = 0; ch < NCH; ++ch) sel.chosen[ch * RT_THREADS + tid] = 0;
+    for (int i = tid; i < 2 * RT_NB; i += RT_THREADS) sel.hist[i] = 0;
+    __syncthreads();
+    if (n_valid <= k) {
+        for (int u = tid; u < n; u += RT_THREADS) sel.chosen[u] = gent[u] >= 0;
+    } else {
+        const float vmin = key_value(s_stat[1]), vmax = key_value(s_stat[2]);
+        float scale = (float)RT_NB / (vmax - vmin);
+        if (!(scale > 0.0f && scale < INFINITY)) scale = 0.0f;      // one bucket
+        int blo[NCH], bhi[NCH];
+#pragma unroll
+        for (int ch = 0; ch < NCH; ++ch) {
+            const int u = ch * RT_THREADS + tid;
+            blo[ch] = -1;
+            bhi[ch] = -1;
+            if (u < n && gent[u] >= 0) {
+                const float2 b2 = glu[u];
+                blo[ch] = rt_bucket(b2.x, vmin, scale);
+                bhi[ch] = rt_bucket(b2.y, vmin, scale);
+                atomicAdd(&sel.hist[blo[ch]], 1);
+                atomicAdd(&sel.hist[RT_NB + bhi[ch]], 1);
+            }
+        }
+        __syncthreads();
+        if (warp == 0) {
+            const int bl = rt_find_bucket(sel.hist, k);
+            if (lane == 0) sel.ctl[3] = bl;
+        } else if (warp == 1) {
+            const int bm = rt_find_bucket(sel.hist + RT_NB, k + 1);
+            if (lane == 0) sel.ctl[4] = bm;
+        }
+        __syncthreads();
+        const int b_lam = sel.ctl[3], b_mu = sel.ctl[4];
+        int ns = 0;
+#pragma unroll
+        for (int ch = 0; ch < NCH; ++ch) {
+            const int u = ch * RT_THREADS + tid;
+            bool und = false;
+            if (blo[ch] >= 0) {
+                if (blo[ch] > b_mu) {
+                    sel.chosen[u] = 1;
+                    ++ns;
+                } else if (bhi[ch] >= b_lam) {
+                    und = true;
+                }
+            }
+            const int pos = append_slot(und, &sel.ctl[0]);
+            if (und) sel.und[pos] = u;
+        }
+        ns = __reduce_add_sync(0xffffffffu, ns);
+        if (lane == 0) atomicAdd(&sel.ctl[1], ns);
+        __syncthreads();
+        const int nu = sel.ctl[0], r = k - sel.ctl[1];
+        if (r > 0) {
+            // exact score of each undecided slot, one warp per slot: lane l takes the group
+            // terms of (head l/8, group l%8) and (head l/8 + 4, group l%8)
+            const uint8_t* kc = kc_all + (int64_t)b * capacity * (RT_DI / 2);
+            const uint8_t* ks = ks_all + (int64_t)b * capacity * RT_G;
+            const int g = lane & 7, h1 = lane >> 3, h2 = h1 + 4;
+            for (int i = warp; i < nu; i += RT_THREADS / 32) {
+                const int jj = gent[sel.und[i]];
+                const uint2 cw = __ldg(reinterpret_cast<const uint2*>(kc + (int64_t)jj * (RT_DI / 2)) + g);
+                const int ski = e4m3_times_512(__ldg(ks + (int64_t)jj * RT_G + g));
+                const uint32_t kv[4] = {unpack4_int8(cw.x & 0xffffu), unpack4_int8(cw.x >> 16),
+                                        unpack4_int8(cw.y & 0xffffu), unpack4_int8(cw.y >> 16)};
+                long long d1 = (long long)(group_dot4(v.qp + h1 * (RT_DI / 4) + 4 * g, kv) * v.qsi[h1 * RT_G + g]) * ski;
+                long long d2 = (long long)(group_dot4(v.qp + h2 * (RT_DI / 4) + 4 * g, kv) * v.qsi[h2 * RT_G + g]) * ski;
+#pragma unroll
+                for (int o = 1; o < 8; o <<= 1) {
+                    d1 += __shfl_xor_sync(0xffffffffu, d1, o);
+                    d2 += __shfl_xor_sync(0xffffffffu, d2, o);
+                }
+                // D_h sits in lanes 8(h%4) (d1 for h < 4, d2 otherwise): the head chain in
+                // ascending order
+                double S = 0.0;
+#pragma unroll
+                for (int h = 0; h < RT_H; ++h) {
+                    const long long D = __shfl_sync(0xffffffffu, h < 4 ? d1 : d2, 8 * (h & 3));
+                    S = fma(v.wd[h], u53_to_f64(D), S);
+                }
+                if (lane == 0) sel.ukey[i] = f64_key(S);
+            }
+            __syncthreads();
+            // the r best undecided slots by (exact score desc, entry asc)
+            for (int i = tid; i < nu; i += RT_THREADS) {
+                const unsigned long long key = sel.ukey[i];
+                const int id = gent[sel.und[i]];
+                int rk = 0;
+                for (int m = 0; m < nu; ++m) {
+                    const unsigned long long km = sel.ukey[m];
+                    rk += (km > key) || (km == key && gent[sel.und[m]] < id);
+                }
+                if (rk < r) sel.chosen[sel.und[i]] = 1;
+            }
+        }
+    }
+    __syncthreads();
+    // the chosen entries in slot order (ballots per chunk and warp), then in ascending
+    // entry order: an HSI pool is ascending already, any other pool is ordered by counting
+    unsigned int mask[NCH];
+#pragma unroll
+    for (int ch = 0; ch < NCH; ++ch) {
+        const int u = ch * RT_THREADS + tid;
+        mask[ch] = __ballot_sync(0xffffffffu, u < n && sel.chosen[u]);
+        if (lane == 0) sel.wtot[ch][warp] = __popc(mask[ch]);
+    }
+    __syncthreads();
+    // exclusive prefix of the (chunk, warp) counts in slot order, by one warp
+    constexpr int NW = RT_THREADS / 32;
+    static_assert(NCH * NW == 64, "two (chunk, warp) counts per lane");
+    if (warp == 0) {
+        int* wt = &sel.wtot[0][0];
+        const int a = wt[2 * lane], b2 = wt[2 * lane + 1];
+        int incl = a + b2;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        wt[2 * lane] = incl - a - b2;
+        wt[2 * lane + 1] = incl - b2;
+        if (lane == 31) sel.ctl[5] = incl;
+    }
+    __syncthreads();
+    int* list = reinterpret_cast<int*>(sel.hist);
+#pragma unroll
+    for (int ch = 0; ch < NCH; ++ch)
+        if ((mask[ch] >> lane) & 1u)
+            list[sel.wtot[ch][warp] + __popc(mask[ch] & ((1u << lane) - 1u))] = gent[ch * RT_THREADS + tid];
+    const int kept = sel.ctl[5];
+    __syncthreads();
+    bool unordered = false;
+    for (int i = tid; i + 1 < kept; i += RT_THREADS) unordered |= list[i] >= list[i + 1];
+    int32_t* out = idx_out + gq * k;
+    if (__syncthreads_or(unordered)) {
+        for (int i = tid; i < kept; i += RT_THREADS) {
+            const int id = list[i];
+            int p = 0;
+            for (int m = 0; m < kept; ++m) p += list[m] < id;
+            out[p] = id;
+        }
+        for (int i = kept + tid; i < k; i += RT_THREADS) out[i] = -1;
+    } else {
+        for (int i = tid; i < k; i += RT_THREADS) out[i] = i < kept ? list[i] : -1;
+    }
+}
+
+bool reindex_tc_supported(int d_idx, int H, int pool_len) {
+    return d_idx == RT_DI && H == RT_H && pool_len <= RT_POOL;
+}
+
+cudaError_t launch_reindex_tc(const csa2_cache& c, const uint8_t* iq_codes, const uint8_t* iq_scales,
+                              const float* iq_raw, const float* w_head, int n_q, const int32_t* pool, int pool_len,
+                              int k, int32_t* idx_out, int* err, cudaStream_t st) {
+    cudaError_t e = cudaFuncSetAttribute(k_reindex_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)RT_DYN);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(RT_CTAS, n_q, c.batch);
+    cfg.blockDim = dim3(RT_THREADS);
+    cfg.dynamicSmemBytes = RT_DYN;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = RT_CTAS;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    e = cudaLaunchKernelEx(&cfg, k_reindex_tc, pool, pool_len, (const uint8_t*)c.ikey_codes,
+                           (const uint8_t*)c.ikey_scales, c.capacity, iq_codes, iq_scales, iq_raw, w_head, n_q, k,
+                           idx_out, err);
+    note_launch();
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace csa2

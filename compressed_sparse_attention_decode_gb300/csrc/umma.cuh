@@ -125,6 +125,7 @@ __device__ __forceinline__ void bar_arrive(uint32_t id, uint32_t count) {
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 __device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+__device__ __forceinline__ void prefetch_l1(const void* p) { asm volatile("prefetch.global.L1 [%0];" ::"l"(p)); }
 
 // the two halves of a cluster barrier, for work to go on in between
 __device__ __forceinline__ void cluster_arrive_relaxed() {

@@ -13,7 +13,7 @@ is a C-ABI entry point of libcsa2; this module only sequences them.
 import torch
 
 from . import (FULL, REINDEX, REUSE, OP_INDEXER_TOPK, OP_REINDEX, OP_SPARSE_ATTN, Cache, csa2_cache_write,
-               csa2_indexer_topk, csa2_quantize_fp4, csa2_reindex, csa2_reindex_f32, csa2_sparse_attn, workspace)
+               csa2_indexer_topk, csa2_quantize_fp4, csa2_reindex_f32, csa2_sparse_attn, workspace)
 
 _MODES = {"full": FULL, "reindex": REINDEX, "reuse": REUSE}
 
@@ -24,7 +24,8 @@ class DecodeStep:
     layers: tuple of "full" / "reindex" / "reuse"; B sequences, n_q queries
     each at raw positions q_pos; the cache holds `capacity` entries per
     sequence.  Per layer l the step reads iq[l] (fp32, quantised on device),
-    w_head[l], q[l] and win[l] and writes idx[l] and out[l] (+ lse[l])."""
+    w_head[l], q[l] and win[l] and writes out[l] (+ lse[l]); a Full or Reindex
+    layer writes idx[l], a Reuse layer reads layer_idx(l) in place."""
 
     def __init__(self, B, capacity, n_q, layers, H=64, H_I=8, d_I=128, k=512, pool_blocks=0, pool_block_size=8,
                  swa_len=128, chunk_pos=0, device="cuda", want_lse=False):
@@ -78,12 +79,11 @@ class DecodeStep:
         if self.chunk_len:
             csa2_cache_write(self.cache, self.h_chunk, self.chunk_pos, self.w0, self.w1, self.kraw_chunk,
                              stream=stream)
-        prev = None
         t = 0
         for l, mode in enumerate(self.layers):
-            idx_l = self.idx[l]
+            idx_l = self.layer_idx(l)
             if mode == "reuse":
-                csa2_reindex(REUSE, self.cache, self.k, prev_idx=prev, idx_out=idx_l, stream=stream, n_q=self.n_q)
+                pass                 # the latest indices, read in place: no copy, no launch
             elif mode == "full":
                 csa2_quantize_fp4(self.iq[t], self.iq_codes, self.iq_scales, stream=stream)
                 csa2_indexer_topk(self.cache, self.iq_codes, self.iq_scales, self.w_head[t], self.q_pos, self.k,
@@ -97,7 +97,16 @@ class DecodeStep:
                 t += 1
             csa2_sparse_attn(self.cache, self.q[l], self.q_pos, idx_l, self.win[l], self.swa_pos0, out=self.out[l],
                              lse=None if self.lse is None else self.lse[l], ws=self.ws_attn, stream=stream)
-            prev = idx_l
+
+    def layer_idx(self, l):
+        """the index list layer l attends with: its own for a Full or Reindex
+        layer; for a Reuse layer the latest one before it, read in place
+        ("DeepSeek-v4.1 Flash" §2.3.2: Reuse takes the latest indices unchanged).
+        Only the layers that compute indices write their slot of self.idx."""
+        src = l
+        while src > 0 and self.layers[src] == "reuse":
+            src -= 1
+        return self.idx[src]
 
     def twin(self):
         """a second step over the same cache, intermediates and workspaces with

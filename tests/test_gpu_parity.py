@@ -110,7 +110,7 @@ def check_walk(csa, wl, seqs, queries=None, layers=None):
         ref = oracle.run_sequence(wl, b, cache=ref_cache, queries=queries, layers=layers)
         qs = list(range(wl.n_q)) if queries is None else list(queries)
         for l in ref["idx"]:
-            got = step.idx[l, bi].cpu().numpy()[qs]
+            got = step.layer_idx(l)[bi].cpu().numpy()[qs]
             assert np.array_equal(got, ref["idx"][l]), (wl.name, b, l)
         for l in ref["pool"]:
             assert np.array_equal(step.pool[bi].cpu().numpy()[qs], ref["pool"][l]), (wl.name, b, l)
@@ -136,7 +136,7 @@ def test_layer_schedule_small(csa):
     wl = scaled(WORKLOADS[2], B=3, T=16384, layers=("full",) + ("reindex",) * 3 + ("reuse",) * 3)
     step = check_walk(csa, wl, [0, 1, 2])
     for l in (5, 6):
-        assert torch.equal(step.idx[l], step.idx[4])
+        assert step.layer_idx(l).data_ptr() == step.idx[3].data_ptr()
 
 
 def test_pool_edge_cases(csa):
@@ -212,6 +212,48 @@ def test_reindex_pool_with_holes_and_reuse(csa):
         assert torch.equal(idx32, idx)
 
 
+@pytest.mark.parametrize("d,H,pool_len", [(128, 8, 2048), (128, 8, 700), (64, 4, 2048), (128, 16, 1024),
+                                          (64, 8, 3000)])
+def test_reindex_paths_ties_holes_and_unordered_pools(csa, d, H, pool_len):
+    """every Reindex path (tensor-core group sums for d_idx 128 with 8 heads, the CUDA-core
+    kernel otherwise, bounds + selection above 2,048 slots) on pools with empty slots, in
+    ascending and in shuffled order, over keys with exact duplicates and all-zero rows, with
+    random and with all-zero head weights (every score ties)"""
+    n, B, n_q = 6000, 2, 3
+    base = synth.normal_f32(44, 1, (B * n, d))
+    base[700:900] = base[100:300]             # duplicated rows: equal scores, lower entry first
+    base[1200:1800] = 0.0                     # zero rows: score exactly 0
+    kc, ks = oracle.quantize_rows(base)
+    lat = oracle.quantize_rows(synth.normal_f32(44, 2, (B * n, 512)))
+    planes = [a.reshape(B, n, -1) for a in (lat[0], lat[1], kc, ks)]
+    cache = host_cache(csa, planes, d)
+    rng = np.random.default_rng(9)
+    pool = np.full((B, n_q, pool_len), -1, np.int32)
+    for b in range(B):
+        for q in range(n_q):
+            m = pool_len - 37 * q
+            ids = rng.choice(np.arange(0, max(2100, m + 100) if q == 0 else n), m, replace=False).astype(np.int32)
+            if q == 1:
+                ids = np.sort(ids)                # an ascending pool (as the HSI pool is) ...
+            pool[b, q, :m] = ids                  # ... and two in no order
+            if q == 2:
+                rng.shuffle(pool[b, q])           # empty slots anywhere
+    iq = synth.normal_f32(45, 3, (B, n_q, H, d))
+    w = synth.uniform_f32(45, 4, (B, n_q, H), 0.0, 1.0)
+    qc, qs = oracle.quantize_rows(iq)
+    for wv in (w, np.zeros_like(w)):
+        for k in (64, 512):
+            idx = csa.csa2_reindex_f32(cache, k, torch.from_numpy(iq).cuda(), torch.from_numpy(wv).cuda(),
+                                       torch.from_numpy(pool).cuda())
+            got = idx.cpu().numpy()
+            for b in range(B):
+                for q in range(n_q):
+                    ids = pool[b, q]
+                    S = oracle.index_scores(kc.reshape(B, n, -1)[b], ks.reshape(B, n, -1)[b], qc[b, q], qs[b, q],
+                                            wv[b, q], ids=ids)
+                    assert np.array_equal(got[b, q], oracle.topk(S, k, ids=ids)), (d, H, pool_len, k, b, q)
+
+
 def test_reindex_from_fp32_queries_large_pool(csa):
     """csa2_reindex_f32 through the bounds + selection path (pool above 2,048 slots), against the
     oracle and against csa2_quantize_fp4 + csa2_reindex"""
@@ -274,7 +316,7 @@ def test_decode_128k_20_layers_full_size_sampled(csa):
     for b in (0, 37, 63):
         ref = oracle.run_sequence(wl, b)
         for l in range(len(wl.layers)):
-            assert np.array_equal(step.idx[l, b].cpu().numpy(), ref["idx"][l]), (b, l)
+            assert np.array_equal(step.layer_idx(l)[b].cpu().numpy(), ref["idx"][l]), (b, l)
             err = rel_err_rows(step.out[l, b].cpu().numpy(), ref["out"][l])
             assert err <= ATTN_TOL, (b, l, err)
         assert np.array_equal(step.pool[b].cpu().numpy(), ref["pool"][0])
