@@ -23,13 +23,22 @@
 // Warps: 0-7 softmax / epilogue (warp w: TMEM lane quarter w%4, key half
 // w/4), warps 8 and 9 issue the score MMAs (K = dims 0-255 and 256-511 into
 // two TMEM partials that the softmax adds; the first half starts as soon as
-// its dims are expanded) and warp 10 the output MMAs: one thread issues about
-// one MMA per 50 cycles, so the streams get a thread each.  Warps 11-17 gather
-// rows.  Tile 0 is the CTA's window rows (contiguous: one bulk copy); the FP4
-// tiles follow, their rows prefetched into L2 one tile ahead, so the gathers
-// are single L2 round trips.  Everything before the indices (Q, the window
-// tile, TMEM and barriers) overlaps the preceding kernel of the stream
-// (programmatic launch); only the loaders wait for it.
+// its dims are expanded), warps 10 and 11 the output MMAs (dim tiles 0-1 and
+// 2-3): one thread issues about one MMA per 55 cycles, two keep the tensor
+// pipe busy.  Warps 12-18 gather rows.  Q (one 64 KB bulk copy, converted in
+// place by warps 0-11) and tile 0, the CTA's window rows (contiguous: one
+// bulk copy), come first; the FP4 tiles follow, their rows prefetched into L2
+// one tile ahead, so the gathers are single L2 round trips.  Everything before
+// the indices (Q, the window tile, TMEM and barriers) overlaps the preceding
+// kernel of the stream (programmatic launch); only the loaders wait for it.
+//
+// Range: fp16 operands hold every FP4 latent value exactly, and bf16 q and
+// window values exactly as long as they lie in [2^-14, 65504].  Any finite
+// bf16 input is taken: a head of q whose largest magnitude falls outside
+// [2^-10, 2^15) is scaled by a power of two into [2^14, 2^15) and its scores
+// scaled back (exact); the same holds for the CTA's window rows, whose
+// contribution to O is brought back to the common scale before the first FP4
+// tile's values are added (or in the final scale when there is none).
 #include "common.cuh"
 #include "umma.cuh"
 
@@ -37,12 +46,13 @@ namespace csa2 {
 
 constexpr int AP_TILE = 64;                          // keys per tile
 constexpr int AP_H = 64;
-constexpr int AP_THREADS = 576;
+constexpr int AP_THREADS = 608;
 constexpr int AP_SMW = 8;                            // softmax warps 0-7
 constexpr int AP_SMT = AP_SMW * 32;
 constexpr int AP_MMAW = 8;                           // warps 8, 9 issue the score MMAs (GEMM1), dims 0-255 / 256-511
-constexpr int AP_MMA2 = 10;                          // warp 10 issues the output MMAs (GEMM2)
-constexpr int AP_LOADERS = 224;                      // warps 11-17
+constexpr int AP_MMA2 = 10;                          // warps 10, 11 issue the output MMAs (GEMM2), dim tiles 0-1 / 2-3
+constexpr int AP_LOADW = 12;                         // warps 12-18 gather rows
+constexpr int AP_LOADERS = 224;
 constexpr uint32_t AP_QSLAB = AP_H * 128;            // 64 heads x 64 dims fp16
 constexpr uint32_t AP_LSLAB = AP_TILE * 128;         // 64 keys x 64 dims fp16
 constexpr uint32_t AP_SQ = 0;                        // Q: 8 slabs (64 KB)
@@ -62,6 +72,30 @@ __device__ __forceinline__ uint32_t apswz(uint32_t row, uint32_t chunk) { return
 __device__ __forceinline__ uint32_t ap_bf16x2_to_f16x2(uint32_t v) {
     __half2 h = __floats2half2_rn(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
     return *reinterpret_cast<uint32_t*>(&h);
+}
+// bf16 pair -> fp16 pair after scaling by d (a power of two): exact unless a value leaves fp16's range
+__device__ __forceinline__ uint32_t ap_bf16x2_to_f16x2_scaled(uint32_t v, float d) {
+    __half2 h = __floats2half2_rn(__uint_as_float(v << 16) * d, __uint_as_float(v & 0xffff0000u) * d);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+// the largest bf16 magnitude (as bits, sign cleared) of the eight values in v
+__device__ __forceinline__ uint32_t ap_absmax4(const uint4& v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t m = 0u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) m = max(m, max(w[i] & 0x7fffu, (w[i] >> 16) & 0x7fffu));
+    return m;
+}
+// 2^e as a float, for -126 <= e <= 127
+__device__ __forceinline__ float ap_pow2(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
+// The power-of-two exponent E by which values whose largest magnitude has bf16 bits `mx` are
+// divided before they go to fp16: 0 while that magnitude lies in [2^-10, 2^15) (or is 0), else
+// the E that brings it into [2^14, 2^15), kept within [-100, 100].
+__device__ __forceinline__ int ap_range_exp(uint32_t mx) {
+    if (mx == 0u) return 0;
+    const int e = (int)((mx >> 7) & 0xffu) - 127;          // largest magnitude in [2^e, 2^(e+1))
+    if (e >= -10 && e < 15) return 0;
+    return max(-100, min(100, e - 14));
 }
 __device__ __forceinline__ void ap_e2m1x8(uint32_t w, uint32_t* o) {
     asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
@@ -123,11 +157,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
     const int T = n4 + 1;
 
     float* m_run = reinterpret_cast<float*>(sm + AP_MISC);          // [64]
-    float* fac = m_run + AP_H;                                       // [64]
+    float* fac = m_run + AP_H;                                       // [64] running-max factor
     int* flag = reinterpret_cast<int*>(fac + AP_H);                  // [8]
     float* own_ml = reinterpret_cast<float*>(flag + 8);              // m[64], l[64]
     float* peer_ml = own_ml + 2 * AP_H;                              // written by the peer
     float* fown = peer_ml + 2 * AP_H;                                // this CTA's final scale per head
+    float* ofac = fown + AP_H;                                       // [64] factor applied to O
+    unsigned int* qmax = reinterpret_cast<unsigned int*>(ofac + AP_H);   // [64] exponent E of each head of q
+    int* wexp = reinterpret_cast<int*>(qmax + AP_H);                 // [0] window exponent, [1] largest |window| bits
     float* red = reinterpret_cast<float*>(sm + AP_RED);              // [2 halves][64 heads]
 
     auto sa = [&](const void* x) { return umma::smem_u32(x); };
@@ -135,18 +172,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
         for (int i = 0; i < 2; ++i) {
             umma::mbar_init(sa(&b_lhalf[i]), AP_LOADERS);     // dims 0-255 of the tile expanded
             umma::mbar_init(sa(&b_lfull[i]), AP_LOADERS);     // all of it
-            umma::mbar_init(sa(&b_lfree[i]), 1);
+            umma::mbar_init(sa(&b_lfree[i]), 2);              // both GEMM2 issuers done with the tile
             umma::mbar_init(sa(&b_sfull[i]), 2);              // both K halves of the scores
             umma::mbar_init(sa(&b_sfree[i]), AP_SMW);
             umma::mbar_init(sa(&b_pfull[i]), AP_SMW);
-            umma::mbar_init(sa(&b_odone[i]), 1);
+            umma::mbar_init(sa(&b_odone[i]), 2);
         }
         umma::mbar_init(sa(&b_wfull), 1);
         umma::fence_mbar_init();
+        // the window's largest magnitude starts at 0 before the loaders (past b_wfull) add to it
+        wexp[1] = 0;
+        // this CTA's window rows are contiguous: one bulk copy, raw bf16, into L buffer 1
+        umma::mbar_arrive_expect_tx(sa(&b_wfull), (uint32_t)nwr * 1024u);
+        if (nwr > 0)
+            umma::bulk_g2s(base + AP_SL + AP_LBUF,
+                           swa + ((int64_t)b * swa_len + (wlo - swa_pos0) + (int64_t)rank * AP_TILE) * D_LAT,
+                           (uint32_t)nwr * 1024u, sa(&b_wfull));
     }
     // The loaders wait only for the barrier set-up (named barrier 3, with warp 0) and start on the
-    // first tile at once; warps 0-8 stage Q and the TMEM allocation among themselves (barrier 4).
-    constexpr uint32_t AP_QT = (AP_MMA2 + 1) * 32;
+    // first tile at once; warps 0-11 stage Q and allocate TMEM among themselves (barrier 4).
+    constexpr uint32_t AP_QT = AP_LOADW * 32;
     if (warp == 0) {
         __syncwarp();
         umma::bar_arrive(3, 32 + AP_LOADERS);
@@ -155,36 +200,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
     umma::cluster_arrive_relaxed();    // waited for before the first access to the peer's shared memory
     bool ok = true;
     uint32_t tmem = 0;
-    if (warp > AP_MMA2) {
+    if (warp >= AP_LOADW) {
         umma::bar_named(3, 32 + AP_LOADERS);
-        if (tid == (int)AP_QT) {
-            // this CTA's window rows are contiguous: one bulk copy, raw bf16, into L buffer 1
-            umma::mbar_arrive_expect_tx(sa(&b_wfull), (uint32_t)nwr * 1024u);
-            if (nwr > 0)
-                umma::bulk_g2s(base + AP_SL + AP_LBUF,
-                               swa + ((int64_t)b * swa_len + (wlo - swa_pos0) + (int64_t)rank * AP_TILE) * D_LAT,
-                               (uint32_t)nwr * 1024u, sa(&b_wfull));
-        }
         {
-            // tile 0 = the window rows: bf16 rows from L buffer 1 (bulk copy) to fp16 slabs in buffer 0
+            // tile 0 = the window rows: bf16 rows from L buffer 1 (bulk copy) to fp16 slabs in buffer 0;
+            // their largest magnitude is tracked on the way, and should it lie outside
+            // [2^-10, 2^15) each thread converts its own units again, scaled by 2^-E
             const int lt = tid - (int)AP_QT;
             ok &= umma::mbar_wait(sa(&b_wfull), 0);
             const uint8_t* R = sm + AP_SL + AP_LBUF;
             uint8_t* L = sm + AP_SL;
-            for (int u0 = lt; u0 < AP_TILE * 64; u0 += AP_LOADERS * 8) {
+            uint32_t mx = 0u;
+            auto convert_window = [&](int ew) {
+                const float wdown = ap_pow2(-ew);
+                for (int u0 = lt; u0 < AP_TILE * 64; u0 += AP_LOADERS * 8) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int u = u0 + i * AP_LOADERS, r = u >> 6, c = u & 63;
-                    if (u < AP_TILE * 64) {
-                        uint4 v = make_uint4(0, 0, 0, 0);
-                        if (r < nwr) v = *reinterpret_cast<const uint4*>(R + r * 1024 + c * 16);
-                        *reinterpret_cast<uint4*>(L + (c >> 3) * AP_LSLAB + apswz(r, c & 7)) =
-                            make_uint4(ap_bf16x2_to_f16x2(v.x), ap_bf16x2_to_f16x2(v.y), ap_bf16x2_to_f16x2(v.z),
-                                       ap_bf16x2_to_f16x2(v.w));
-                        if (c == 0) rowok[0][r] = r < nwr ? 1 : 0;
+                    for (int i = 0; i < 8; ++i) {
+                        const int u = u0 + i * AP_LOADERS, r = u >> 6, c = u & 63;
+                        if (u < AP_TILE * 64) {
+                            uint4 v = make_uint4(0, 0, 0, 0);
+                            if (r < nwr) v = *reinterpret_cast<const uint4*>(R + r * 1024 + c * 16);
+                            uint4 o;
+                            if (ew == 0) {
+                                o = make_uint4(ap_bf16x2_to_f16x2(v.x), ap_bf16x2_to_f16x2(v.y),
+                                               ap_bf16x2_to_f16x2(v.z), ap_bf16x2_to_f16x2(v.w));
+                                mx = max(mx, ap_absmax4(v));
+                            } else {
+                                o = make_uint4(ap_bf16x2_to_f16x2_scaled(v.x, wdown), ap_bf16x2_to_f16x2_scaled(v.y, wdown),
+                                               ap_bf16x2_to_f16x2_scaled(v.z, wdown), ap_bf16x2_to_f16x2_scaled(v.w, wdown));
+                            }
+                            *reinterpret_cast<uint4*>(L + (c >> 3) * AP_LSLAB + apswz(r, c & 7)) = o;
+                            if (c == 0) rowok[0][r] = r < nwr ? 1 : 0;
+                        }
                     }
                 }
-            }
+            };
+            convert_window(0);
+            mx = __reduce_max_sync(0xffffffffu, mx);
+            if (lane == 0 && mx) atomicMax(reinterpret_cast<unsigned int*>(&wexp[1]), mx);
+            umma::bar_named(2, AP_LOADERS);
+            const int ew = ap_range_exp((uint32_t)wexp[1]);
+            if (lt == 0) wexp[0] = ew;
+            if (ew != 0) convert_window(ew);
             umma::fence_proxy_async();
             umma::mbar_arrive(sa(&b_lhalf[0]));
             umma::mbar_arrive(sa(&b_lfull[0]));
@@ -201,22 +258,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
         }
         umma::bar_named(2, AP_LOADERS);          // sidx staged; buffer 1 read in full before tile 1 overwrites it
     } else {
-        // ---- Q: 64 heads x 512 dims, bf16 -> fp16, K-major slabs of 64 dims (A operand), by warps 0-8
-        for (int u0 = 0; u0 < (AP_H * 64 + (int)AP_QT - 1) / (int)AP_QT; u0 += 8) {
-            uint4 qv[8];
+        // ---- Q: 64 heads x 512 dims, bf16 -> fp16, K-major slabs of 64 dims (A operand), by warps
+        // 0-11: warp w takes heads w, w+12, .. (lane l: 16-byte chunks l and l+32 of each), all
+        // loads in flight at once; a head whose largest magnitude lies outside [2^-10, 2^15) is
+        // scaled by 2^-E on the way (the warp sees the whole head)
+        constexpr int QW = AP_LOADW;                                   // warps staging Q
+        constexpr int QHPW = (AP_H + QW - 1) / QW;                     // heads per warp (at most)
+        uint4 qv[QHPW][2];
+        const uint4* qsrc = reinterpret_cast<const uint4*>(q + gq * AP_H * D_LAT);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int i = tid + (u0 + u) * (int)AP_QT, h = i >> 6, c = i & 63;
-                if (i < AP_H * 64) qv[u] = __ldg(reinterpret_cast<const uint4*>(q + ((gq * AP_H + h) * D_LAT + c * 8)));
+        for (int r = 0; r < QHPW; ++r) {
+            const int h = warp + QW * r;
+            if (h < AP_H) {
+                qv[r][0] = __ldg(qsrc + h * 64 + lane);
+                qv[r][1] = __ldg(qsrc + h * 64 + 32 + lane);
             }
+        }
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int i = tid + (u0 + u) * (int)AP_QT, h = i >> 6, c = i & 63;
-                const uint4 v = qv[u];
-                if (i < AP_H * 64)
-                    *reinterpret_cast<uint4*>(sm + AP_SQ + (c >> 3) * AP_QSLAB + apswz(h, c & 7)) =
-                        make_uint4(ap_bf16x2_to_f16x2(v.x), ap_bf16x2_to_f16x2(v.y), ap_bf16x2_to_f16x2(v.z),
-                                   ap_bf16x2_to_f16x2(v.w));
+        for (int r = 0; r < QHPW; ++r) {
+            const int h = warp + QW * r;
+            if (h < AP_H) {                      // warp-uniform
+                const uint32_t mx = __reduce_max_sync(0xffffffffu, max(ap_absmax4(qv[r][0]), ap_absmax4(qv[r][1])));
+                const int eh = ap_range_exp(mx);
+                const float d = ap_pow2(-eh);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int c = lane + 32 * hh;
+                    const uint4 v = qv[r][hh];
+                    uint4 o;
+                    if (eh == 0)
+                        o = make_uint4(ap_bf16x2_to_f16x2(v.x), ap_bf16x2_to_f16x2(v.y), ap_bf16x2_to_f16x2(v.z),
+                                       ap_bf16x2_to_f16x2(v.w));
+                    else
+                        o = make_uint4(ap_bf16x2_to_f16x2_scaled(v.x, d), ap_bf16x2_to_f16x2_scaled(v.y, d),
+                                       ap_bf16x2_to_f16x2_scaled(v.z, d), ap_bf16x2_to_f16x2_scaled(v.w, d));
+                    *reinterpret_cast<uint4*>(sm + AP_SQ + (c >> 3) * AP_QSLAB + apswz(h, c & 7)) = o;
+                }
+                if (lane == 0) qmax[h] = (uint32_t)eh;     // the head's exponent
             }
         }
         if (tid < AP_H) m_run[tid] = -INFINITY;
@@ -227,7 +305,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
         tmem = tmem_base;
     }
 
-    if (warp > AP_MMA2) {
+    if (warp >= AP_LOADW) {
         // ================= loaders
         const int lt = tid - (int)AP_QT;
         int* sidx = reinterpret_cast<int*>(sm + AP_SIDX);
@@ -350,10 +428,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                 umma::commit(sa(&b_sfull[buf]));
             }
         }
-    } else if (warp == AP_MMA2) {
-        // ================= GEMM2 issuer: O^T += L^T . P of tile t once P is written (pfull);
-        // its completion releases the L buffer (lfree) and the P buffer (odone)
+    } else if (warp == AP_MMA2 || warp == AP_MMA2 + 1) {
+        // ================= GEMM2 issuers: warp 10 + p adds dim tiles 2p, 2p+1 of O^T += L^T . P of
+        // tile t once P is written (pfull); the completion of both releases the L buffer (lfree)
+        // and the P buffer (odone)
         if (lane == 0) {
+            const int part = warp - AP_MMA2;
             const uint32_t id2 = umma::idesc_f16(128, AP_H, 1, 0);
             for (int t = 0; t < T && ok; ++t) {
                 const int buf = t & 1;
@@ -363,7 +443,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                 const uint64_t la0 = umma::desc(base + AP_SL + buf * AP_LBUF, AP_LSLAB, 1024, umma::LAYOUT_SW128);
                 const uint64_t pb0 = umma::desc(base + AP_SP + buf * AP_PBUF, 16, 1024, umma::LAYOUT_SW128);
 #pragma unroll
-                for (int mt = 0; mt < 4; ++mt) {
+                for (int mt = 2 * part; mt < 2 * part + 2; ++mt) {
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {
                         const uint64_t offa = (uint64_t)(((2 * mt) * AP_LSLAB + ks * 2048) >> 4);
@@ -383,7 +463,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
         const int h = qd * 16 + (lane >> 2) + 8 * (lane & 1);
         const int par = (lane >> 1) & 1;
         const uint32_t lane_base = tmem + ((uint32_t)(qd * 32) << 16);
+        const float hmul = scale_log2e * ap_pow2((int)qmax[h]);   // times this head's q exponent
         float lsum = 0.0f;                   // sum of P over this thread's keys, all tiles so far
+        int ew = 0;                          // exponent of the window rows (known once tile 0 is in)
         for (int t = 0; t < T; ++t) {
             const int buf = t & 1;
             float x[16];                     // keys 32*half + par + 2i
@@ -402,6 +484,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
             if (lane == 0) umma::mbar_arrive(sa(&b_sfree[buf]));
             // key validity was written by the loaders of this buffer: observe their barrier too
             ok &= umma::mbar_wait(sa(&b_lfull[buf]), (t >> 1) & 1);
+            if (t == 0) ew = wexp[0];
+            const float mul = t == 0 ? hmul * ap_pow2(ew) : hmul;
+            // the window tile's part of O is brought to the common scale before tile 1 adds to it
+            const bool force = t == 1 && ew != 0;
             const float mh = m_run[h];
             bool exceed = false;
             {
@@ -412,12 +498,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                 for (int i = 0; i < 16; ++i) {
                     const int key = par + 2 * i;                       // within the half
                     const bool valid = (vw[key >> 2] >> (8 * (key & 3))) & 0xffu;
-                    x[i] = valid ? x[i] * scale_log2e : -INFINITY;
+                    x[i] = valid ? x[i] * mul : -INFINITY;
                     exceed |= x[i] > mh + AP_LAZY;
                 }
             }
             const bool raise = umma::bar_red_or(1, AP_SMT, exceed);
-            if (raise) {
+            if (raise || force) {
                 // new running max for the heads that rose too far: max over the head's four threads
                 float mx = -INFINITY;
 #pragma unroll
@@ -435,8 +521,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                             m_run[h] = mt;
                         }
                         fac[h] = f;
+                        ofac[h] = force ? f * ap_pow2(ew) : f;
                     }
-                    const unsigned any = __ballot_sync(0xffffffffu, f != 1.0f);
+                    const float of = force ? f * ap_pow2(ew) : f;
+                    const unsigned any = __ballot_sync(0xffffffffu, of != 1.0f);
                     if (lane == 0) flag[qd] = any != 0;
                 }
                 if (t >= 1) ok &= umma::mbar_wait(sa(&b_odone[(t - 1) & 1]), ((t - 1) >> 1) & 1);   // O settled
@@ -452,7 +540,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                             umma::tmem_ld16(lane_base + APT_O + 64 * mt + c, v);
                             umma::tmem_wait_ld();
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) v[i] *= fac[c + i];
+                            for (int i = 0; i < 16; ++i) v[i] *= ofac[c + i];
                             umma::tmem_st16(lane_base + APT_O + 64 * mt + c, v);
                         }
                     }
@@ -511,7 +599,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
             const float s0 = (m0 == -INFINITY) ? 0.0f : umma::ex2(m0 - mm);
             const float s1 = (m1 == -INFINITY) ? 0.0f : umma::ex2(m1 - mm);
             const float Lt = l0 * s0 + l1 * s1;
-            fown[tid] = Lt > 0.0f ? s0 / Lt : 0.0f;
+            // O still carries the window rows' exponent when no FP4 tile followed them
+            fown[tid] = Lt > 0.0f ? s0 / Lt * (T == 1 ? ap_pow2(wexp[0]) : 1.0f) : 0.0f;
             if (lse != nullptr && rank == 0)
                 lse[gq * AP_H + tid] = Lt > 0.0f ? (mm + log2f(Lt)) * 0.69314718055994531f : -INFINITY;
         }

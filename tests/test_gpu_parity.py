@@ -282,6 +282,43 @@ def test_reindex_from_fp32_queries_large_pool(csa):
         assert np.array_equal(idx32.cpu().numpy()[0, q], oracle.topk(S, k, ids=pool[0, q]))
 
 
+def _scaled_bf16(a, e):
+    """bf16 bit patterns times 2^e (exact: only the exponent field moves)"""
+    f = synth.bf16_to_f32(a).astype(np.float64) * 2.0 ** e
+    u = f.astype(np.float32).view(np.uint32)
+    return (u >> 16).astype(np.uint16)
+
+
+@pytest.mark.parametrize("H", [64])
+def test_attention_inputs_far_outside_fp16_range(csa, H):
+    """q heads and window rows scaled by 2^20 and 2^-30 (far outside fp16's range) must still
+    match the fp64 oracle"""
+    n, k = 2000, 512
+    lat = oracle.quantize_rows(synth.normal_f32(46, 2, (n, 512)))
+    kc, ks = oracle.quantize_rows(synth.normal_f32(46, 1, (n, 128)))
+    cache = host_cache(csa, [a[None] for a in (lat[0], lat[1], kc, ks)], 128)
+    p = 2 * n + 127
+    idx = np.sort(np.random.default_rng(11).choice(n, k, replace=False)).astype(np.int32)[None, None]
+    q0 = synth.normal_bf16(46, 3, (H, 512))
+    w0 = synth.normal_bf16(46, 4, (128, 512))
+    cases = []
+    qa = q0.copy()
+    qa[: H // 2] = _scaled_bf16(q0[: H // 2], 20)
+    qa[H // 2:] = _scaled_bf16(q0[H // 2:], -30)
+    cases.append((qa, w0))
+    cases.append((q0, _scaled_bf16(w0, 20)))
+    cases.append((q0, _scaled_bf16(w0, -30)))
+    wm = w0.copy()
+    wm[:64] = _scaled_bf16(w0[:64], 20)          # one CTA's half of the window far up, the other as drawn
+    cases.append((_scaled_bf16(q0, 12), wm))
+    for qb, win in cases:
+        out, lse = csa.csa2_sparse_attn(cache, bf16_t(qb[None, None]), torch.tensor([[p]], dtype=torch.int64).cuda(),
+                                        torch.from_numpy(idx).cuda(), bf16_t(win[None]), p - 127, want_lse=True)
+        ro, rl = oracle.sparse_attention(qb, idx[0, 0], lat[0], lat[1], win)
+        assert np.isfinite(out.cpu().numpy()).all()
+        assert rel_err_rows(out.cpu().numpy()[0, 0], ro) <= ATTN_TOL
+
+
 def test_attention_window_clipping_and_empty_selection(csa):
     wl = WORKLOADS[0]
     lc, ls, kc, ks = oracle.sequence_cache(wl, 0)
