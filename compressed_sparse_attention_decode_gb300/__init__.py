@@ -7,7 +7,7 @@ fallback: if the library is not built, every call raises.
 
 Entry points (same names as the C ABI):
     csa2_cache_write, csa2_quantize_fp4, csa2_indexer_topk, csa2_reindex, csa2_reindex_f32,
-    csa2_sparse_attn, csa2_workspace_size
+    csa2_sparse_attn, csa2_workspace_size, csa2_poll_error, csa2_selftest_wait_timeout
 plus ``Cache``, which owns the four cache planes as torch tensors.
 """
 import ctypes
@@ -18,7 +18,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libcsa2.so")
 
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE = 0, 1, 2, 3, 4
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE, ERR_TIMEOUT = 0, 1, 2, 3, 4, 5
 FULL, REINDEX, REUSE = 0, 1, 2
 OP_INDEXER_TOPK, OP_REINDEX, OP_SPARSE_ATTN = 1, 2, 3
 D_LAT = 512
@@ -40,7 +40,7 @@ class _CacheStruct(ctypes.Structure):
 _lib = None
 EXPORTS = ("csa2_cache_write", "csa2_quantize_fp4", "csa2_indexer_topk", "csa2_reindex", "csa2_sparse_attn",
            "csa2_workspace_size", "csa2_status_string", "csa2_abi_version", "csa2_launch_count",
-           "csa2_reindex_noalloc", "csa2_reindex_f32")
+           "csa2_reindex_noalloc", "csa2_reindex_f32", "csa2_poll_error", "csa2_selftest_wait_timeout")
 
 
 def load(path=None):
@@ -62,6 +62,10 @@ def load(path=None):
     lib.csa2_sparse_attn.argtypes = [cp, vp, i32, i32, vp, vp, i32, vp, i64, i32, ctypes.c_float, vp, vp, vp, sz, vp]
     lib.csa2_reindex_noalloc.argtypes = [cp, vp, vp, vp, i32, i32, vp, i32, i32, vp, vp]
     lib.csa2_reindex_noalloc.restype = ctypes.c_int
+    lib.csa2_poll_error.argtypes = [vp, sz, vp]
+    lib.csa2_poll_error.restype = ctypes.c_int
+    lib.csa2_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp, sz, vp]
+    lib.csa2_selftest_wait_timeout.restype = ctypes.c_int
     lib.csa2_workspace_size.argtypes = [i32, i32, i32, i32, i32, i64]
     lib.csa2_workspace_size.restype = sz
     lib.csa2_status_string.argtypes = [ctypes.c_int]
@@ -124,8 +128,24 @@ def csa2_workspace_size(op, batch, n_q, n_heads, k, capacity):
 
 
 def workspace(op, batch, n_q, n_heads, k, capacity, device="cuda"):
+    """a workspace for the operation, its error word cleared"""
     n = csa2_workspace_size(op, batch, n_q, n_heads, k, capacity)
-    return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+    ws = torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+    ws[:16].zero_()
+    return ws
+
+
+def csa2_poll_error(ws, stream=None):
+    """reads and clears the error word of a workspace: OK, or ERR_TIMEOUT if a
+    kernel that used it gave up on a bounded wait (synchronises the stream)"""
+    return load().csa2_poll_error(_ptr(ws), ws.numel(), _stream(stream))
+
+
+def csa2_selftest_wait_timeout(max_polls, ws, stream=None):
+    """a kernel waits on a barrier nothing signals, with at most max_polls polls,
+    gives up and records it in ws's error word"""
+    _check(load().csa2_selftest_wait_timeout(int(max_polls), _ptr(ws), ws.numel(), _stream(stream)),
+           "csa2_selftest_wait_timeout")
 
 
 def csa2_cache_write(cache, h, pos0, w0, w1, ikey_raw=None, stream=None):

@@ -23,6 +23,7 @@ cudaError_t launch_sparse_attn(const csa2_cache& c, const uint16_t* q, int n_q, 
 size_t sparse_attn_ws(int batch, int n_q, int H, int k);
 size_t indexer_full_ws(int batch, int n_q, int64_t capacity);
 size_t reindex_ws(int batch, int n_q, int64_t pool_len);
+cudaError_t launch_selftest_wait(uint32_t max_polls, int* err, cudaStream_t st);
 }  // namespace csa2
 
 #include <atomic>
@@ -73,6 +74,7 @@ const char* csa2_status_string(csa2_status s) {
         case CSA2_ERR_UNSUPPORTED: return "unsupported configuration";
         case CSA2_ERR_CUDA: return "CUDA error";
         case CSA2_ERR_WORKSPACE: return "workspace missing or too small";
+        case CSA2_ERR_TIMEOUT: return "a kernel gave up on a bounded wait";
     }
     return "unknown status";
 }
@@ -85,6 +87,23 @@ size_t csa2_workspace_size(int32_t op, int32_t batch, int32_t n_q, int32_t n_hea
         case CSA2_OP_SPARSE_ATTN: return sparse_attn_ws(batch, n_q, n_heads, k);
     }
     return 0;
+}
+
+csa2_status csa2_poll_error(void* workspace, size_t ws_bytes, void* stream) {
+    if (!workspace || ws_bytes < 16 || !aligned(workspace, 16)) return CSA2_ERR_INVALID_ARG;
+    const cudaStream_t st = (cudaStream_t)stream;
+    int word = 0;
+    CSA2_CUDA_TRY(cudaMemcpyAsync(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost, st));
+    CSA2_CUDA_TRY(cudaStreamSynchronize(st));
+    if (word == 0) return CSA2_OK;
+    CSA2_CUDA_TRY(cudaMemsetAsync(workspace, 0, sizeof(int), st));
+    CSA2_CUDA_TRY(cudaStreamSynchronize(st));
+    return CSA2_ERR_TIMEOUT;
+}
+
+csa2_status csa2_selftest_wait_timeout(uint32_t max_polls, void* workspace, size_t ws_bytes, void* stream) {
+    if (max_polls < 1 || !workspace || ws_bytes < 16 || !aligned(workspace, 16)) return CSA2_ERR_INVALID_ARG;
+    return from_cuda(launch_selftest_wait(max_polls, reinterpret_cast<int*>(workspace), (cudaStream_t)stream));
 }
 
 csa2_status csa2_cache_write(const csa2_cache* cache, const uint16_t* h, int64_t pos0, int32_t n_pos,

@@ -973,12 +973,14 @@ struct SelectWs {
     float2* blu;
 };
 
+// The first 16 bytes hold the error word (set by a kernel that gave up on a
+// bounded wait, read and cleared by csa2_poll_error); the counts follow.
 static SelectWs carve(void* ws, int64_t slabs, int64_t n) {
     uint8_t* p = reinterpret_cast<uint8_t*>(ws);
     SelectWs w;
-    w.counts = reinterpret_cast<int*>(p);
-    w.err = w.counts + slabs * 2;
-    p += (((slabs * 2 + 4) * sizeof(int) + 255) / 256) * 256;
+    w.err = reinterpret_cast<int*>(p);
+    w.counts = reinterpret_cast<int*>(p + 16);
+    p += ((16 + slabs * 2 * sizeof(int) + 255) / 256) * 256;
     w.c2key = reinterpret_cast<unsigned long long*>(p);
     p += slabs * n * 8;
     w.lu = reinterpret_cast<float2*>(p);
@@ -994,7 +996,7 @@ static SelectWs carve(void* ws, int64_t slabs, int64_t n) {
 }
 
 static size_t ws_bytes(int64_t slabs, int64_t n) {
-    return (((slabs * 2 + 4) * sizeof(int) + 255) / 256) * 256 + slabs * slab_bytes(n);
+    return ((16 + slabs * 2 * sizeof(int) + 255) / 256) * 256 + slabs * slab_bytes(n);
 }
 
 bool scan_tc_supported(int d_idx, int H, int QB, int pool_blocks, int bs);
@@ -1032,7 +1034,7 @@ cudaError_t launch_indexer_full_t(const csa2_cache& c, const uint8_t* iq_codes, 
     if (e != cudaSuccess) return e;
     for (int q0 = 0; q0 < n_q; q0 += qchunk) {
         const int n_qc = (n_q - q0) < qchunk ? (n_q - q0) : qchunk;
-        e = cudaMemsetAsync(w.counts, 0, ((size_t)c.batch * n_qc * 2 + 4) * sizeof(int), st);
+        e = cudaMemsetAsync(w.counts, 0, (size_t)c.batch * n_qc * 2 * sizeof(int), st);
         if (e != cudaSuccess) return e;
         if (scan_tc_supported(DI, H, QB, pool_blocks, bs)) {
             e = launch_scan_full_tc(c, iq_codes, iq_scales, w_head, n_q, q_pos, q0, n_qc, H, k, pool_blocks, bs,

@@ -55,7 +55,8 @@ typedef enum {
     CSA2_ERR_INVALID_ARG = 1,   /* bad pointer, size, alignment or mode; nothing enqueued */
     CSA2_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. d_lat != 512) */
     CSA2_ERR_CUDA = 3,          /* a CUDA call or launch failed */
-    CSA2_ERR_WORKSPACE = 4      /* workspace NULL or smaller than csa2_workspace_size() */
+    CSA2_ERR_WORKSPACE = 4,     /* workspace NULL or smaller than csa2_workspace_size() */
+    CSA2_ERR_TIMEOUT = 5        /* a kernel gave up on a bounded wait (reported by csa2_poll_error) */
 } csa2_status;
 
 /* cross-layer modes, "DeepSeek-v4.1 Flash: KVキャッシュ圧縮の限界を押し広げる" §2.3.2 */
@@ -219,6 +220,36 @@ csa2_status csa2_sparse_attn(const csa2_cache* cache, const uint16_t* q, int32_t
 csa2_status csa2_reindex_noalloc(const csa2_cache* cache, const uint8_t* iq_codes, const uint8_t* iq_scales,
                                  const float* w_head, int32_t n_q, int32_t n_heads, const int32_t* pool,
                                  int32_t pool_len, int32_t k, int32_t* idx_out, void* stream);
+
+/*
+ * Failure detection.  Every wait of the library's kernels on an asynchronous
+ * event (a copy landing, a tensor-core operation completing, the other CTA of
+ * a pair) is bounded: after about 2^24 polls it gives up, the kernel records
+ * the failure in the first 32-bit word of the workspace it was given and
+ * returns with its outputs unspecified (the attention writes NaN), so the
+ * context stays usable.  No call reports this itself, since calls are
+ * asynchronous.
+ *
+ * csa2_poll_error reads that word of `workspace` (a workspace given to any
+ * operation, at least 16 bytes), clears it, and returns CSA2_ERR_TIMEOUT if it
+ * was set, CSA2_OK otherwise.  The library never clears the word otherwise:
+ * zero the first 16 bytes of a new workspace (or poll it once) before relying
+ * on it.  It synchronises `stream` (it waits for the work
+ * enqueued on it), so call it between steps, never during stream capture.
+ * Returns CSA2_ERR_INVALID_ARG for a NULL or too small workspace,
+ * CSA2_ERR_CUDA if the copy fails.
+ */
+csa2_status csa2_poll_error(void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Self-test of the bounded waits: one kernel waits, with at most `max_polls`
+ * polls, on a barrier that nothing ever signals, gives up, and records the
+ * failure in `workspace` exactly as the library's kernels do; a following
+ * csa2_poll_error returns CSA2_ERR_TIMEOUT.  It exercises the waiting helper,
+ * the error word and the poll without a fault or a hang.  max_polls >= 1;
+ * workspace at least 16 bytes.
+ */
+csa2_status csa2_selftest_wait_timeout(uint32_t max_polls, void* workspace, size_t ws_bytes, void* stream);
 
 /* Workspace bytes an operation needs (0 if none).  capacity = entries per
  * sequence of the cache; for CSA2_OP_REINDEX pass pool_len as `capacity`. */

@@ -74,6 +74,13 @@ def test_host_side_validation_needs_no_gpu(lib):
     assert lib.csa2_quantize_fp4(p, 4, 24, p, p, None) == csa.ERR_INVALID_ARG                  # d not /16
     assert lib.csa2_workspace_size(csa.OP_INDEXER_TOPK, 2, 1, 8, 512, 1000) > 0
     assert lib.csa2_launch_count() >= 0
+    # failure detection: NULL, short or misaligned workspaces and a zero poll limit are refused
+    assert lib.csa2_poll_error(None, 16, None) == csa.ERR_INVALID_ARG
+    assert lib.csa2_poll_error(p, 8, None) == csa.ERR_INVALID_ARG
+    assert lib.csa2_poll_error(ctypes.c_void_p(264), 64, None) == csa.ERR_INVALID_ARG
+    assert lib.csa2_selftest_wait_timeout(0, p, 64, None) == csa.ERR_INVALID_ARG
+    assert lib.csa2_selftest_wait_timeout(16, None, 64, None) == csa.ERR_INVALID_ARG
+    assert lib.csa2_status_string(csa.ERR_TIMEOUT) == b"a kernel gave up on a bounded wait"
 
 
 def test_binding_fails_loudly_without_the_library(tmp_path):

@@ -319,6 +319,27 @@ def test_attention_inputs_far_outside_fp16_range(csa, H):
         assert rel_err_rows(out.cpu().numpy()[0, 0], ro) <= ATTN_TOL
 
 
+def test_bounded_wait_runs_out_and_is_reported(csa):
+    """a wait on a barrier that nothing signals gives up after its poll limit; the
+    failure comes back from csa2_poll_error once (the word is cleared), and the
+    context stays usable: a real call afterwards runs and reports no failure"""
+    wl = WORKLOADS[0]
+    ws = csa.workspace(csa.OP_SPARSE_ATTN, 1, 1, wl.H, wl.k, wl.T // 2)
+    assert csa.csa2_poll_error(ws) == csa.OK
+    csa.csa2_selftest_wait_timeout(64, ws)
+    assert csa.csa2_poll_error(ws) == csa.ERR_TIMEOUT
+    assert csa.csa2_poll_error(ws) == csa.OK
+    lc, ls, kc, ks = oracle.sequence_cache(wl, 0)
+    cache = host_cache(csa, [a[None] for a in (lc, ls, kc, ks)], wl.d_I)
+    q = wl.q(0, 0)
+    idx = np.arange(0, 3 * 64, 3, dtype=np.int32)[None, None]
+    out, _ = csa.csa2_sparse_attn(cache, bf16_t(q[None]), torch.tensor([[wl.T - 1]], dtype=torch.int64).cuda(),
+                                  torch.from_numpy(idx).cuda(), bf16_t(wl.window(0, 0)[None]), wl.T - 128, ws=ws)
+    assert csa.csa2_poll_error(ws) == csa.OK
+    ro, _ = oracle.sparse_attention(q[0], idx[0, 0], lc, ls, wl.window(0, 0))
+    assert rel_err_rows(out.cpu().numpy()[0, 0], ro) <= ATTN_TOL
+
+
 def test_attention_window_clipping_and_empty_selection(csa):
     wl = WORKLOADS[0]
     lc, ls, kc, ks = oracle.sequence_cache(wl, 0)
