@@ -98,7 +98,7 @@ def algorithmic_bytes(wl):
     scan's eligible keys (n_elig x 72 B), every Reindex layer's pool keys (pool x
     72 B) and every layer's gather (k x 288 B + 128 window rows x 1 KB)"""
     n_re = sum(m == "reindex" for m in wl.layers)
-    per_seq = n_elig_decode(wl) * 72 + n_re * wl.pool_blocks * wl.pool_block_size * 72 + \
+    per_seq = n_elig_decode(wl) * 72 + n_re * wl.pool_len * 72 + \
         len(wl.layers) * attn_bytes_per_query(wl)
     return wl.B * per_seq
 
@@ -442,7 +442,7 @@ def roofline(wl, per_op, peak, peak_kind):
     time, against the measured copy peak and against the 8 TB/s of the target"""
     bytes_per_launch = {
         "indexer_full": wl.B * n_elig_decode(wl) * 72,
-        "reindex": wl.B * wl.pool_blocks * wl.pool_block_size * 72,
+        "reindex": wl.B * wl.pool_len * 72,
         "sparse_attn": wl.B * attn_bytes_per_query(wl),
     }
     extra = {"sparse_attn": wl.B * attn_extra_bytes_per_query(wl)}

@@ -178,7 +178,8 @@ def csa2_indexer_topk(cache, iq_codes, iq_scales, w_head, q_pos, k, pool_blocks=
     if idx_out is None:
         idx_out = torch.empty((B, n_q, k), dtype=torch.int32, device=dev)
     if pool_blocks and pool_out is None:
-        pool_out = torch.empty((B, n_q, pool_blocks * pool_block_size), dtype=torch.int32, device=dev)
+        P = pool_blocks * pool_block_size if pool_block_size else pool_blocks   # 0: the pure pool
+        pool_out = torch.empty((B, n_q, P), dtype=torch.int32, device=dev)
     if ws is None:
         ws = workspace(OP_INDEXER_TOPK, cache.batch, n_q, H, k, cache.capacity, dev)
     c = cache.struct()

@@ -137,7 +137,8 @@ csa2_status csa2_indexer_topk(const csa2_cache* cache, const uint8_t* iq_codes, 
     if (n_q < 1 || n_heads < 1 || n_heads > MAX_IDX_HEADS || k < 1 || k > MAX_K) return CSA2_ERR_INVALID_ARG;
     if (pool_blocks < 0) return CSA2_ERR_INVALID_ARG;
     if (pool_blocks > 0) {
-        if (pool_block_size < 1 || pool_blocks > MAX_K || (int64_t)pool_blocks * pool_block_size > 16384 ||
+        // pool_block_size 0: the pure pool of the pool_blocks best entries
+        if (pool_block_size < 0 || pool_blocks > MAX_K || (int64_t)pool_blocks * pool_block_size > 16384 ||
             !pool_out || !aligned(pool_out, 4))
             return CSA2_ERR_INVALID_ARG;
     }

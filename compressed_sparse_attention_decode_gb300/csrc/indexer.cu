@@ -715,9 +715,13 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
     pdl_launch_next();
     extern __shared__ int qsm[];
     __shared__ SelectSmem sm;
-    // gridDim.z == 2 (Full layer with an HSI pool): block z = 0 keeps the top k, z = 1 builds the
-    // pool, side by side; the pool block's scratch (h2id, h2key) is its own
+    // gridDim.z == 2 (Full layer with a candidate pool): block z = 0 keeps the top k, z = 1 builds
+    // the pool, side by side; the pool block's scratch (h2id, h2key) is its own.  bs == 0 asks for
+    // the pure pool: the pool_blocks best entries, chosen by the same code as the top k.
     const bool split = gridDim.z == 2;
+    const bool pure = pool_blocks > 0 && bs == 0;
+    const bool pure_pool = pure && split && blockIdx.z == 1;
+    const int kk = pure_pool ? pool_blocks : k;
     const int b = blockIdx.y, ql = blockIdx.x;
     const int64_t gq = (int64_t)b * n_q + q0 + ql;     // global query row
     const int64_t slab = (int64_t)b * n_qc + ql;        // workspace row
@@ -734,9 +738,10 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
     sm.bitmap = reinterpret_cast<unsigned int*>(extra + SEL_DYN_EXTRA);
     const float2* L = lu + slab * list_len;
     const int n = counts ? counts[2 * slab] : n_fixed;
-    int* cid = split && blockIdx.z == 1 ? h2id + slab * list_len + list_len / 2 : c2id + slab * list_len;
-    unsigned long long* ckey =
-        split && blockIdx.z == 1 ? h2key + slab * list_len + list_len / 2 : c2key + slab * list_len;
+    // the pure pool's block has the whole block-candidate lists (the scan forwards no blocks then)
+    const int64_t hoff = pure ? 0 : list_len / 2;
+    int* cid = split && blockIdx.z == 1 ? h2id + slab * list_len + hoff : c2id + slab * list_len;
+    unsigned long long* ckey = split && blockIdx.z == 1 ? h2key + slab * list_len + hoff : c2key + slab * list_len;
     const uint8_t* kc = kc_all + (int64_t)b * capacity * (DI / 2);
     const uint8_t* ks = ks_all + (int64_t)b * capacity * (DI / 16);
     auto entry_of = [&](int t) -> int {
@@ -749,7 +754,8 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
     }
     sm.rs.whist = sm.whist;
     __syncthreads();
-    if (!split || blockIdx.z == 0) {
+    if (!split || blockIdx.z == 0 || pure_pool) {
+    const int k = kk;                        // the number kept by this block
     // ---- 1. k-th largest lower bound, candidates whose upper bound reaches it.
     // Every forwarded item (Full) is a real entry; an empty pool slot (Reindex)
     // has bounds (-inf, -inf), below every real entry, so the selection may
@@ -819,13 +825,13 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
         kept = best_sorted(cid, ckey, m, k, sm);
         kept = ascending_ids(sm.id, nullptr, kept, id_bound, sm.din, sm);
     }
-    int32_t* out = idx_out + gq * k;
+    int32_t* out = pure_pool ? pool_out + gq * k : idx_out + gq * k;
     for (int t = threadIdx.x; t < k; t += blockDim.x) out[t] = t < kept ? sm.din[t] : -1;
     __syncthreads();
     }
 
     // ---- 4. HSI candidate pool (Full only)
-    if (pool_blocks <= 0 || !counts || (split && blockIdx.z == 0)) return;
+    if (pool_blocks <= 0 || pure || !counts || (split && blockIdx.z == 0)) return;
     const int n_elig = n_elig_of(q_pos[gq], capacity);
     const int P = pool_blocks * bs;
     int32_t* pout = pool_out + gq * P;
@@ -1024,11 +1030,16 @@ cudaError_t launch_indexer_full_t(const csa2_cache& c, const uint8_t* iq_codes, 
     const int64_t list_len = (int64_t)c.capacity + 1;
     const SelectWs w = carve(ws, (int64_t)c.batch * qchunk, list_len);
     const size_t qwords = (size_t)QView<DI>::words(H) * sizeof(int);
+    // the pure pool (bs == 0): the pool_blocks best entries; the scans then forward every entry
+    // that may be among the max(k, pool_blocks) best and no blocks
+    const bool pure = pool_blocks > 0 && bs == 0;
+    const int kf = pure ? (k > pool_blocks ? k : pool_blocks) : k;
+    const int pb_scan = pure ? 0 : pool_blocks, bs_scan = pure ? 1 : bs;
     // queries per scan block and entries per chunk: one query and 4096 entries
     // for decode, 8 queries sharing each key load (1024 entries) otherwise
-    const int QB = (n_q >= 8 && pool_blocks == 0) ? 8 : 1;
+    const int QB = (n_q >= 8 && pb_scan == 0) ? 8 : 1;
     int E = QB == 1 ? 4096 : 1024;
-    if (pool_blocks > 0) E = bs * (4096 / bs > 0 ? 4096 / bs : 1);
+    if (pb_scan > 0) E = bs_scan * (4096 / bs_scan > 0 ? 4096 / bs_scan : 1);
     const size_t smem1 = 32 * sizeof(int) + QB * qwords + (size_t)QB * E * sizeof(float2) + 8 * 256 * sizeof(int);
     cudaError_t e = cudaFuncSetAttribute(k_scan_full<DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
     if (e != cudaSuccess) return e;
@@ -1036,13 +1047,13 @@ cudaError_t launch_indexer_full_t(const csa2_cache& c, const uint8_t* iq_codes, 
         const int n_qc = (n_q - q0) < qchunk ? (n_q - q0) : qchunk;
         e = cudaMemsetAsync(w.counts, 0, (size_t)c.batch * n_qc * 2 * sizeof(int), st);
         if (e != cudaSuccess) return e;
-        if (scan_tc_supported(DI, H, QB, pool_blocks, bs)) {
-            e = launch_scan_full_tc(c, iq_codes, iq_scales, w_head, n_q, q_pos, q0, n_qc, H, k, pool_blocks, bs,
+        if (scan_tc_supported(DI, H, QB, pb_scan, bs_scan)) {
+            e = launch_scan_full_tc(c, iq_codes, iq_scales, w_head, n_q, q_pos, q0, n_qc, H, kf, pb_scan, bs_scan,
                                     w.counts, w.ids, w.lu, w.bid, w.blu, (int)list_len, w.err, st);
         } else {
             dim3 g1((c.capacity + E - 1) / E, (n_qc + QB - 1) / QB, c.batch);
             launch_k(k_scan_full<DI>, g1, 256, smem1, st, c.ikey_codes, c.ikey_scales, c.capacity, iq_codes, iq_scales,
-                                                    w_head, q_pos, n_q, q0, n_qc, H, QB, E, k, pool_blocks, bs,
+                                                    w_head, q_pos, n_q, q0, n_qc, H, QB, E, kf, pb_scan, bs_scan,
                                                     w.counts, w.ids, w.lu, w.bid, w.blu, (int)list_len);
             note_launch();
             e = cudaGetLastError();
@@ -1051,7 +1062,7 @@ cudaError_t launch_indexer_full_t(const csa2_cache& c, const uint8_t* iq_codes, 
         // with an HSI pool the top k and the pool are built by two blocks per query at once; the
         // pool block's scratch is the upper half of the block-candidate lists (a query has at most
         // ceil(capacity / bs) <= list_len / 2 block candidates when bs >= 2)
-        dim3 g2(n_qc, c.batch, (pool_blocks > 1 && bs >= 2) ? 2 : 1);
+        dim3 g2(n_qc, c.batch, ((pool_blocks > 1 && bs >= 2) || pure) ? 2 : 1);
         const size_t smem2 = qwords + SEL_DYN_EXTRA + SEL_BITMAP_BYTES;
         e = cudaFuncSetAttribute(k_select<DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
         if (e != cudaSuccess) return e;

@@ -55,12 +55,13 @@ class DecodeStep:
         self.iq_codes = torch.zeros((B, n_q, H_I, d_I // 2), dtype=torch.uint8, device=device)
         self.iq_scales = torch.zeros((B, n_q, H_I, d_I // 16), dtype=torch.uint8, device=device)
         self.idx = torch.full((L, B, n_q, k), -1, dtype=i32, device=device)
-        self.pool = (torch.full((B, n_q, pool_blocks * pool_block_size), -1, dtype=i32, device=device)
-                     if pool_blocks else None)
+        # pool_block_size 0: the pool is the pool_blocks best entries
+        self.pool_len = (pool_blocks * pool_block_size if pool_block_size else pool_blocks) if pool_blocks else 0
+        self.pool = torch.full((B, n_q, self.pool_len), -1, dtype=i32, device=device) if pool_blocks else None
         self.out = torch.zeros((L, B, n_q, H, 512), dtype=f32, device=device)
         self.lse = torch.zeros((L, B, n_q, H), dtype=f32, device=device) if want_lse else None
         self.ws_full = workspace(OP_INDEXER_TOPK, B, n_q, H_I, k, capacity, device)
-        self.ws_re = (workspace(OP_REINDEX, B, n_q, H_I, k, pool_blocks * pool_block_size, device)
+        self.ws_re = (workspace(OP_REINDEX, B, n_q, H_I, k, self.pool_len, device)
                       if "reindex" in self.layers else None)
         self.ws_attn = workspace(OP_SPARSE_ATTN, B, n_q, H, k, capacity, device)
         self.graph = None

@@ -132,7 +132,12 @@ csa2_status csa2_quantize_fp4(const float* x, int64_t n_rows, int32_t d, uint8_t
  *   idx_out   int32 [batch][n_q][k]  the chosen entry ids in ascending order, -1 padded
  *   pool_out  int32 [batch][n_q][pool_blocks*pool_block_size] or NULL when
  *             pool_blocks == 0; -1 padded
- * 1 <= k <= 2048; 1 <= n_heads <= 32; pool_blocks*pool_block_size <= 16384.
+ * pool_block_size == 0 asks for the other reading of the candidate pool: the
+ * pool_blocks best entries by the same score and order as the top k (no block
+ * structure, nothing forced in), ascending, -1 padded; pool_out then has
+ * pool_blocks slots per query.
+ * 1 <= k <= 2048; 1 <= n_heads <= 32; pool_blocks <= 2048;
+ * pool_blocks*pool_block_size <= 16384.
  * workspace: csa2_workspace_size(CSA2_OP_INDEXER_TOPK, ...) bytes.
  */
 csa2_status csa2_indexer_topk(const csa2_cache* cache, const uint8_t* iq_codes, const uint8_t* iq_scales,

@@ -246,14 +246,17 @@ def run_sequence(wl, b, cache=None, queries=None, layers=None, want_out=True):
             wh = wl.w_head(l, b)
             qc, qs = quantize_rows(iq[queries])
             if mode == "full" and wl.pool_blocks:
-                pool = np.empty((len(queries), wl.pool_blocks * wl.pool_block_size), np.int32)
+                pool = np.empty((len(queries), wl.pool_len), np.int32)
             for t, qi in enumerate(queries):
                 ne = n_elig(qpos[qi])
                 if mode == "full":
                     S = index_scores(kc, ks, qc[t], qs[t], wh[qi], n=ne)
                     idx_l[t] = topk(S, wl.k)
-                    if wl.pool_blocks:
+                    if wl.pool_blocks and wl.pool_block_size:
                         pool[t] = hsi_pool(S, wl.pool_block_size, wl.pool_blocks)
+                    elif wl.pool_blocks:
+                        # the other reading of the candidate pool: the best pool_blocks entries
+                        pool[t] = topk(S, wl.pool_blocks)
                 else:
                     S = index_scores(kc, ks, qc[t], qs[t], wh[qi], ids=pool[t])
                     idx_l[t] = topk(S, wl.k, ids=pool[t])

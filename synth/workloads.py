@@ -42,7 +42,7 @@ class Workload:
     H: int                 # attention heads
     layers: tuple          # per layer: "full" | "reindex" | "reuse"
     pool_blocks: int = 0   # HSI blocks kept by the Full layer (0 = no pool)
-    pool_block_size: int = 8
+    pool_block_size: int = 8   # 0: the pool is the pool_blocks best entries (no blocks)
     chunk: int = 0         # >0: chunked prefill, the last `chunk` positions are queries and are written in the step
 
     @property
@@ -52,6 +52,13 @@ class Workload:
     @property
     def n_entries(self):
         return self.T // 2
+
+    @property
+    def pool_len(self):
+        """slots of the Full layer's candidate pool"""
+        if not self.pool_blocks:
+            return 0
+        return self.pool_blocks * self.pool_block_size if self.pool_block_size else self.pool_blocks
 
     @property
     def prefix(self):

@@ -153,6 +153,14 @@ def test_pages_hsi_example_pool_of_16384(csa):
     check_walk(csa, wl, [0, 1])
 
 
+@pytest.mark.parametrize("T,P,k", [(16384, 2048, 512), (4096, 2048, 512), (16384, 300, 512)])
+def test_pure_top_entries_pool(csa, T, P, k):
+    """the other reading of the candidate pool: the P best entries of the Full layer's scores
+    (no blocks, nothing forced in); a pool covering every entry; a pool smaller than k"""
+    wl = scaled(WORKLOADS[2], B=2, T=T, k=k, pool_blocks=P, pool_block_size=0, layers=("full", "reindex", "reuse"))
+    check_walk(csa, wl, [0, 1])
+
+
 def test_short_contexts_pad_with_minus_one(csa):
     for T in (128, 130, 200, 256):
         wl = scaled(WORKLOADS[0], T=T, k=64)

@@ -188,3 +188,19 @@ def test_walk_reuse_copies_and_reindex_stays_in_pool():
     assert np.array_equal(res["idx"][3], res["idx"][2]) and np.array_equal(res["idx"][4], res["idx"][2])
     n_elig = oracle.n_elig(wl.T - 1)
     assert res["idx"][0].max() < n_elig
+
+
+def test_pure_pool_is_the_best_entries_and_reindex_stays_in_it():
+    """pool_block_size 0: the Full layer's pool is its P best entries by (score desc, entry asc),
+    ascending, by brute force over the exact scores; Reindex layers choose inside it"""
+    wl = scaled(WORKLOADS[2], B=1, T=4096, H=4, k=32, pool_blocks=100, pool_block_size=0,
+                layers=("full", "reindex", "reuse"))
+    res = oracle.run_sequence(wl, 0, want_out=False)
+    lc, ls, kc, ks = oracle.sequence_cache(wl, 0)
+    qc, qs = oracle.quantize_rows(wl.iq(0, 0))
+    n = oracle.n_elig(wl.T - 1)
+    S = oracle.index_scores(kc, ks, qc[0], qs[0], wl.w_head(0, 0)[0], n=n)
+    best = sorted(range(n), key=lambda j: (-S[j], j))[:100]
+    assert res["pool"][0][0].tolist() == sorted(best)
+    assert set(res["idx"][1][0].tolist()) <= set(best)
+    assert np.array_equal(res["idx"][2], res["idx"][1])
