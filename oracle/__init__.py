@@ -64,6 +64,8 @@ def _load():
         lib.orc_dequant_rows.argtypes = [vp, vp, i64, i32, vp]
         lib.orc_merge_pairs.argtypes = [vp, i64, i32, vp, vp, vp]
         lib.orc_cache_write.argtypes = [vp, i64, i32, vp, vp, vp, i32, vp, vp, vp, vp]
+        lib.orc_cache_write_r1.argtypes = [vp, i64, i32, vp, vp]
+        lib.orc_project_ikeys.argtypes = [vp, vp, i64, i32, vp, vp, i32, vp, vp]
         lib.orc_index_scores.argtypes = [vp, vp, i32, vp, i64, vp, vp, vp, i32, vp]
         lib.orc_topk.argtypes = [vp, vp, i64, i32, vp]
         lib.orc_hsi_pool.argtypes = [vp, i64, i32, i32, vp]
@@ -148,6 +150,32 @@ def cache_write(h, w0, w1, kraw):
     return lc, ls, kc, ks
 
 
+def cache_write_r1(h):
+    """Decoder cache (one entry per raw position): h bf16 [n_pos, 512] ->
+    (lat_codes [n_pos, 256], lat_scales [n_pos, 32])"""
+    h, hp = _c(h, np.uint16)
+    n, d = h.shape
+    lc = np.empty((n, d // 2), np.uint8)
+    ls = np.empty((n, d // 16), np.uint8)
+    _load().orc_cache_write_r1(hp, n, d, lc.ctypes.data, ls.ctypes.data)
+    return lc, ls
+
+
+def project_ikeys(lat_codes, lat_scales, w_codes, w_scales):
+    """indexer keys projected from the stored entries: FP4(fp32(W . L)) ->
+    (ikey_codes [n, d_idx/2], ikey_scales [n, d_idx/16])"""
+    lat_codes, lcp = _c(lat_codes, np.uint8)
+    lat_scales, lsp = _c(lat_scales, np.uint8)
+    w_codes, wcp = _c(w_codes, np.uint8)
+    w_scales, wsp = _c(w_scales, np.uint8)
+    n, d_lat = lat_codes.shape[0], lat_codes.shape[1] * 2
+    d_idx = w_codes.shape[0]
+    kc = np.empty((n, d_idx // 2), np.uint8)
+    ks = np.empty((n, d_idx // 16), np.uint8)
+    _load().orc_project_ikeys(lcp, lsp, n, d_lat, wcp, wsp, d_idx, kc.ctypes.data, ks.ctypes.data)
+    return kc, ks
+
+
 # ---------------------------------------------------------------- indexer
 def index_scores(kcodes, kscales, qcodes, qscales, w, ids=None, n=None):
     """exact scores S[t] of entry ids[t] (or entries 0..n-1) for one query.
@@ -218,9 +246,24 @@ def dense_attention(q, n_elig, lat_codes, lat_scales, win, scale=SCALE):
 
 # ---------------------------------------------------------------- one sequence of a workload
 def sequence_cache(wl, b):
-    """cache planes of sequence b of workload wl (whole context)"""
-    w0, w1 = wl.merge_weights()
-    return cache_write(wl.h(b, 0, wl.T), w0, w1, wl.kraw(b, 0, wl.n_entries))
+    """cache planes of sequence b of workload wl (whole context): merged 2:1
+    (ratio 2) or one entry per position (ratio 1, the decoder's); indexer keys
+    from the raw rows, or projected from the entries when wl.ikey_proj"""
+    if wl.ratio == 1:
+        lc, ls = cache_write_r1(wl.h(b, 0, wl.T))
+        kc, ks = quantize_rows(synth_bf16_to_f32(wl.kraw(b, 0, wl.n_entries))) if not wl.ikey_proj else (None, None)
+    else:
+        w0, w1 = wl.merge_weights()
+        lc, ls, kc, ks = cache_write(wl.h(b, 0, wl.T), w0, w1, wl.kraw(b, 0, wl.n_entries))
+    if wl.ikey_proj:
+        wc, ws = quantize_rows(wl.w_ik())
+        kc, ks = project_ikeys(lc, ls, wc, ws)
+    return lc, ls, kc, ks
+
+
+def synth_bf16_to_f32(a):
+    """bf16 bit patterns -> float32 (exact)"""
+    return (np.ascontiguousarray(a, np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
 def run_sequence(wl, b, cache=None, queries=None, layers=None, want_out=True):
@@ -248,7 +291,7 @@ def run_sequence(wl, b, cache=None, queries=None, layers=None, want_out=True):
             if mode == "full" and wl.pool_blocks:
                 pool = np.empty((len(queries), wl.pool_len), np.int32)
             for t, qi in enumerate(queries):
-                ne = n_elig(qpos[qi])
+                ne = n_elig(qpos[qi], wl.ratio)
                 if mode == "full":
                     S = index_scores(kc, ks, qc[t], qs[t], wh[qi], n=ne)
                     idx_l[t] = topk(S, wl.k)

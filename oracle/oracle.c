@@ -172,6 +172,49 @@ void orc_cache_write(const uint16_t* h, int64_t n_pos, int d_lat, const float* w
     free(k);
 }
 
+/* Decoder cache (compression ratio 1, [P1] §1.1 and §2.3.3: one global entry
+ * per position, kept for addressability): entry i is raw position i, its bf16
+ * hidden state quantised as it is. */
+void orc_cache_write_r1(const uint16_t* h, int64_t n_pos, int d_lat, uint8_t* lat_codes, uint8_t* lat_scales) {
+    float* e = (float*)malloc(sizeof(float) * n_pos * d_lat);
+    for (int64_t i = 0; i < n_pos * d_lat; ++i) e[i] = bf16_value(h[i]);
+    orc_quantize_rows(e, n_pos, d_lat, lat_codes, lat_scales);
+    free(e);
+}
+
+/* Indexer keys projected from the main KV entry ([P1] §2.3.1: the indexer K is
+ * a projection of the main KV, which replaces CSA's separate path):
+ *     k[d] = sum_c W[d][c] * L[c]
+ * over the stored entry L (dequantised FP4 latent) and the projection W, itself
+ * stored in the same FP4 format (E2M1, one E4M3 scale per 16 inputs).  Every
+ * product is exact in fp64 and a multiple of 2^-20, and every partial sum stays
+ * below 2^52 in magnitude, so the fp64 sum below is the exact value; it is
+ * rounded once to fp32 and quantised with the cache's codec. */
+void orc_project_ikeys(const uint8_t* lat_codes, const uint8_t* lat_scales, int64_t n, int d_lat,
+                       const uint8_t* w_codes, const uint8_t* w_scales, int d_idx,
+                       uint8_t* ikey_codes, uint8_t* ikey_scales) {
+    double* W = (double*)malloc(sizeof(double) * d_idx * d_lat);
+    orc_dequant_rows(w_codes, w_scales, d_idx, d_lat, W);
+    float* k = (float*)malloc(sizeof(float) * n * d_idx);
+    #pragma omp parallel
+    {
+        double* L = (double*)malloc(sizeof(double) * d_lat);
+        #pragma omp for schedule(static)
+        for (int64_t i = 0; i < n; ++i) {
+            orc_dequant_rows(lat_codes + i * (d_lat / 2), lat_scales + i * (d_lat / 16), 1, d_lat, L);
+            for (int d = 0; d < d_idx; ++d) {
+                double acc = 0.0;
+                for (int c = 0; c < d_lat; ++c) acc += W[(int64_t)d * d_lat + c] * L[c];
+                k[i * d_idx + d] = (float)acc;
+            }
+        }
+        free(L);
+    }
+    orc_quantize_rows(k, n, d_idx, ikey_codes, ikey_scales);
+    free(k);
+    free(W);
+}
+
 /* ------------------------------------------------------------------------ */
 /* indexer: score_j = sum_h w_h * ReLU(q_h . k_j)                            */
 /* [P1] §2.3.1: indexer Q and indexer K score the main-KV entries and the    */

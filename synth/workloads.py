@@ -13,6 +13,7 @@ Distributions (all seeded by the workload's index, one stream per tensor):
   w[l]     indexer head weights    f32   U(0,1)      [B, n_q, H_I]
   q[l]     attention queries       bf16  N(0,1)      [B, n_q, H, 512]
   win[l]   window rows of layer l  bf16  N(0,1)      [B, 128, 512]  (l >= 1; layer 0 reads h)
+  w_ik     indexer-key projection  f32   N(0,1/512)  [d_I, 512]  (workloads whose keys are projected)
 Element i of a tensor is sample i of its stream, so one sequence's slice is
 drawn on its own.  Nothing in here merges, quantises or scores.
 """
@@ -26,7 +27,7 @@ D_LAT = 512
 WINDOW = 128
 
 # stream ids
-S_H, S_W0, S_W1, S_KRAW = 1, 2, 3, 4
+S_H, S_W0, S_W1, S_KRAW, S_WIK = 1, 2, 3, 4, 5
 S_IQ, S_WH, S_Q, S_WIN = 1000, 2000, 3000, 4000
 
 
@@ -44,6 +45,8 @@ class Workload:
     pool_blocks: int = 0   # HSI blocks kept by the Full layer (0 = no pool)
     pool_block_size: int = 8   # 0: the pool is the pool_blocks best entries (no blocks)
     chunk: int = 0         # >0: chunked prefill, the last `chunk` positions are queries and are written in the step
+    ratio: int = 2         # raw positions per global entry: 2 (encoder merge) or 1 (the decoder's per-position cache)
+    ikey_proj: bool = False  # indexer keys projected from the entries (w_ik) instead of drawn rows
 
     @property
     def seed(self):
@@ -51,7 +54,7 @@ class Workload:
 
     @property
     def n_entries(self):
-        return self.T // 2
+        return self.T // self.ratio
 
     @property
     def pool_len(self):
@@ -91,6 +94,10 @@ class Workload:
     def kraw(self, b, e0, n):
         """bf16 raw indexer-key rows of sequence b, entries [e0, e0+n)"""
         return normal_bf16(self.seed, S_KRAW, (n, self.d_I), offset=(b * self.n_entries + e0) * self.d_I)
+
+    def w_ik(self):
+        """f32 [d_I, 512] N(0, 1/512): the projection of an entry to its indexer key"""
+        return (normal_f32(self.seed, S_WIK, (self.d_I, D_LAT)) * np.float32(1.0 / np.sqrt(D_LAT))).astype(np.float32)
 
     def iq(self, layer, b):
         n = self.n_q * self.H_I * self.d_I

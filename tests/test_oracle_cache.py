@@ -65,3 +65,39 @@ def test_storage_per_token_matches_the_pages():
     assert abs(per_token - int(g["bytes_per_token"])) / int(g["bytes_per_token"]) < tol
     assert abs(per_token * 1e6 / 1e6 - int(g["mb_at_1m"])) / int(g["mb_at_1m"]) < tol
     assert abs(per_token * 1e5 / 1e6 - int(g["mb_at_100k"])) / int(g["mb_at_100k"]) < tol
+
+
+def test_projected_indexer_keys_are_the_exact_sum_rounded_once():
+    """k = FP4(fp32(W . L)) over the stored entries: the oracle's fp64 sum is checked against
+    exact rational arithmetic (every dequantised FP4 value is a small binary fraction), the
+    single rounding against an independent round-to-nearest-even, and the codes against the
+    codec; the W scale from 2^-9 up to 448 exercises the range the fp64 sum must hold"""
+    lat = oracle.quantize_rows(synth.normal_f32(21, 1, (6, 512)) * np.float32(40.0))
+    wf = synth.normal_f32(21, 2, (128, 512)) * np.float32(1.0 / np.sqrt(512.0))
+    wf[:8] *= np.float32(2.0 ** 12)                 # large rows
+    wf[8:16] *= np.float32(2.0 ** -14)              # tiny rows
+    wc, ws = oracle.quantize_rows(wf)
+    kc, ks = oracle.project_ikeys(lat[0], lat[1], wc, ws)
+    Wd = oracle.dequant_rows(wc, ws)
+    Ld = oracle.dequant_rows(lat[0], lat[1])
+    for i in range(6):
+        k = np.empty(128, np.float32)
+        for d in range(128):
+            exact = sum(Fraction(float(Wd[d, c])) * Fraction(float(Ld[i, c])) for c in range(512))
+            assert float(exact) == float(sum(Fraction(float(x)) for x in Wd[d] * Ld[i]))   # products exact in fp64
+            k[d] = rn_f32(exact) if exact != 0 else 0.0
+        ck, cs = oracle.quantize_rows(k[None])
+        assert np.array_equal(kc[i], ck[0]) and np.array_equal(ks[i], cs[0])
+
+
+def test_decoder_cache_has_one_entry_per_position():
+    """ratio 1: entry i is raw position i, quantised as it is; its window and eligibility
+    leave no gap and no overlap with the entries before the window"""
+    h = synth.normal_bf16(22, 1, (300, 512))
+    lc, ls = oracle.cache_write_r1(h)
+    wc, ws = oracle.quantize_rows(synth.bf16_to_f32(h))
+    assert np.array_equal(lc, wc) and np.array_equal(ls, ws)
+    for p in (127, 128, 200, 299):
+        n = oracle.n_elig(p, ratio=1)
+        assert n == max(0, p - 127)
+        assert set(range(n)) | set(range(max(0, p - 127), p + 1)) == set(range(p + 1))
