@@ -34,13 +34,14 @@ class _CacheStruct(ctypes.Structure):
     _fields_ = [("lat_codes", ctypes.c_void_p), ("lat_scales", ctypes.c_void_p),
                 ("ikey_codes", ctypes.c_void_p), ("ikey_scales", ctypes.c_void_p),
                 ("batch", ctypes.c_int32), ("capacity", ctypes.c_int32),
-                ("d_lat", ctypes.c_int32), ("d_idx", ctypes.c_int32)]
+                ("d_lat", ctypes.c_int32), ("d_idx", ctypes.c_int32), ("ratio", ctypes.c_int32)]
 
 
 _lib = None
 EXPORTS = ("csa2_cache_write", "csa2_quantize_fp4", "csa2_indexer_topk", "csa2_reindex", "csa2_sparse_attn",
            "csa2_workspace_size", "csa2_status_string", "csa2_abi_version", "csa2_launch_count",
-           "csa2_reindex_noalloc", "csa2_reindex_f32", "csa2_poll_error", "csa2_selftest_wait_timeout")
+           "csa2_reindex_noalloc", "csa2_reindex_f32", "csa2_poll_error", "csa2_selftest_wait_timeout",
+           "csa2_cache_write_projected")
 
 
 def load(path=None):
@@ -55,6 +56,8 @@ def load(path=None):
     vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
     cp = ctypes.POINTER(_CacheStruct)
     lib.csa2_cache_write.argtypes = [cp, vp, i64, i32, vp, vp, vp, vp]
+    lib.csa2_cache_write_projected.argtypes = [cp, vp, i64, i32, vp, vp, vp, vp, vp]
+    lib.csa2_cache_write_projected.restype = ctypes.c_int
     lib.csa2_quantize_fp4.argtypes = [vp, i64, i32, vp, vp, vp]
     lib.csa2_indexer_topk.argtypes = [cp, vp, vp, vp, i32, vp, i32, i32, vp, i32, i32, vp, vp, sz, vp]
     lib.csa2_reindex.argtypes = [i32, cp, vp, vp, vp, i32, i32, vp, i32, vp, i32, vp, vp, sz, vp]
@@ -102,10 +105,11 @@ def _check(status, fn):
 
 
 class Cache:
-    """The four planes of the FP4 global KV cache (device tensors, uint8)."""
+    """The four planes of the FP4 global KV cache (device tensors, uint8); ratio
+    raw positions per entry (2: an encoder copy, 1: the decoder's)."""
 
-    def __init__(self, batch, capacity, d_idx=128, device="cuda"):
-        self.batch, self.capacity, self.d_idx = batch, capacity, d_idx
+    def __init__(self, batch, capacity, d_idx=128, device="cuda", ratio=2):
+        self.batch, self.capacity, self.d_idx, self.ratio = batch, capacity, d_idx, ratio
         self.lat_codes = torch.zeros((batch, capacity, D_LAT // 2), dtype=torch.uint8, device=device)
         self.lat_scales = torch.zeros((batch, capacity, D_LAT // 16), dtype=torch.uint8, device=device)
         self.ikey_codes = torch.zeros((batch, capacity, d_idx // 2), dtype=torch.uint8, device=device)
@@ -113,7 +117,8 @@ class Cache:
 
     def struct(self):
         return _CacheStruct(self.lat_codes.data_ptr(), self.lat_scales.data_ptr(), self.ikey_codes.data_ptr(),
-                            self.ikey_scales.data_ptr(), self.batch, self.capacity, D_LAT, self.d_idx)
+                            self.ikey_scales.data_ptr(), self.batch, self.capacity, D_LAT, self.d_idx,
+                            getattr(self, "ratio", 2))
 
     def nbytes(self):
         return sum(t.numel() for t in (self.lat_codes, self.lat_scales, self.ikey_codes, self.ikey_scales))
@@ -155,6 +160,15 @@ def csa2_cache_write(cache, h, pos0, w0, w1, ikey_raw=None, stream=None):
     st = load().csa2_cache_write(ctypes.byref(c), _ptr(h), int(pos0), int(h.shape[1]), _ptr(w0), _ptr(w1),
                                  _ptr(ikey_raw), _stream(stream))
     _check(st, "csa2_cache_write")
+
+
+def csa2_cache_write_projected(cache, h, pos0, w0, w1, wik_codes, wik_scales, stream=None):
+    """as csa2_cache_write, with the indexer keys projected from the entries:
+    wik_codes uint8 [d_idx, 256], wik_scales uint8 [d_idx, 32] (FP4 W)"""
+    c = cache.struct()
+    st = load().csa2_cache_write_projected(ctypes.byref(c), _ptr(h), int(pos0), int(h.shape[1]), _ptr(w0), _ptr(w1),
+                                           _ptr(wik_codes), _ptr(wik_scales), _stream(stream))
+    _check(st, "csa2_cache_write_projected")
 
 
 def csa2_quantize_fp4(x, codes=None, scales=None, stream=None):

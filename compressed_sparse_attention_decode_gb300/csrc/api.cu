@@ -8,6 +8,9 @@
 namespace csa2 {
 cudaError_t launch_cache_write(const csa2_cache& c, const uint16_t* h, int64_t entry0, int n_ent, const float* w0,
                                const float* w1, const uint16_t* ikey_raw, cudaStream_t st);
+cudaError_t launch_cache_write_proj(const csa2_cache& c, const uint16_t* h, int64_t entry0, int n_ent, const float* w0,
+                                    const float* w1, const uint8_t* wik_codes, const uint8_t* wik_scales,
+                                    cudaStream_t st);
 cudaError_t launch_quantize_fp4(const float* x, int64_t n_rows, int d, uint8_t* codes, uint8_t* scales,
                                 cudaStream_t st);
 cudaError_t launch_indexer_full(const csa2_cache& c, const uint8_t* iq_codes, const uint8_t* iq_scales,
@@ -46,6 +49,7 @@ csa2_status check_cache(const csa2_cache* c, bool need_ikey) {
     if (c->batch < 1 || c->capacity < 1) return CSA2_ERR_INVALID_ARG;
     if (c->d_lat != D_LAT) return CSA2_ERR_UNSUPPORTED;
     if (c->d_idx != 64 && c->d_idx != 128) return CSA2_ERR_UNSUPPORTED;
+    if (c->ratio != 1 && c->ratio != 2) return CSA2_ERR_INVALID_ARG;
     if (!c->lat_codes || !c->lat_scales || !aligned(c->lat_codes, 16) || !aligned(c->lat_scales, 16))
         return CSA2_ERR_INVALID_ARG;
     // indexer-key scale rows are d_idx/16 bytes: that is all the alignment their loads need
@@ -63,7 +67,7 @@ csa2_status from_cuda(cudaError_t e) { return e == cudaSuccess ? CSA2_OK : CSA2_
 
 extern "C" {
 
-int32_t csa2_abi_version(void) { return 100; }
+int32_t csa2_abi_version(void) { return 200; }
 
 int64_t csa2_launch_count(void) { return (int64_t)g_launches.load(std::memory_order_relaxed); }
 
@@ -106,15 +110,39 @@ csa2_status csa2_selftest_wait_timeout(uint32_t max_polls, void* workspace, size
     return from_cuda(launch_selftest_wait(max_polls, reinterpret_cast<int*>(workspace), (cudaStream_t)stream));
 }
 
+// the checks shared by both cache writes (ratio 2 merges pairs of positions)
+static csa2_status check_cache_write(const csa2_cache* cache, const uint16_t* h, int64_t pos0, int32_t n_pos,
+                                     const float* w0, const float* w1, bool need_ikey) {
+    csa2_status s = check_cache(cache, need_ikey);
+    if (s != CSA2_OK) return s;
+    if (!h || !aligned(h, 16)) return CSA2_ERR_INVALID_ARG;
+    if (pos0 < 0 || n_pos < 0) return CSA2_ERR_INVALID_ARG;
+    if (cache->ratio == 2) {
+        if (!w0 || !w1 || !aligned(w0, 16) || !aligned(w1, 16)) return CSA2_ERR_INVALID_ARG;
+        if ((pos0 & 1) || (n_pos & 1)) return CSA2_ERR_INVALID_ARG;
+    }
+    if (pos0 / cache->ratio + n_pos / cache->ratio > cache->capacity) return CSA2_ERR_INVALID_ARG;
+    return CSA2_OK;
+}
+
 csa2_status csa2_cache_write(const csa2_cache* cache, const uint16_t* h, int64_t pos0, int32_t n_pos,
                              const float* w0, const float* w1, const uint16_t* ikey_raw, void* stream) {
-    csa2_status s = check_cache(cache, ikey_raw != nullptr);
+    csa2_status s = check_cache_write(cache, h, pos0, n_pos, w0, w1, ikey_raw != nullptr);
     if (s != CSA2_OK) return s;
-    if (!h || !w0 || !w1 || !aligned(h, 16) || !aligned(w0, 16) || !aligned(w1, 16)) return CSA2_ERR_INVALID_ARG;
     if (ikey_raw && !aligned(ikey_raw, 16)) return CSA2_ERR_INVALID_ARG;
-    if (pos0 < 0 || n_pos < 0 || (pos0 & 1) || (n_pos & 1)) return CSA2_ERR_INVALID_ARG;
-    if (pos0 / 2 + n_pos / 2 > cache->capacity) return CSA2_ERR_INVALID_ARG;
-    return from_cuda(launch_cache_write(*cache, h, pos0 / 2, n_pos / 2, w0, w1, ikey_raw, (cudaStream_t)stream));
+    const int r = cache->ratio;
+    return from_cuda(launch_cache_write(*cache, h, pos0 / r, n_pos / r, w0, w1, ikey_raw, (cudaStream_t)stream));
+}
+
+csa2_status csa2_cache_write_projected(const csa2_cache* cache, const uint16_t* h, int64_t pos0, int32_t n_pos,
+                                       const float* w0, const float* w1, const uint8_t* wik_codes,
+                                       const uint8_t* wik_scales, void* stream) {
+    csa2_status s = check_cache_write(cache, h, pos0, n_pos, w0, w1, true);
+    if (s != CSA2_OK) return s;
+    if (!wik_codes || !wik_scales || !aligned(wik_codes, 16) || !aligned(wik_scales, 4)) return CSA2_ERR_INVALID_ARG;
+    const int r = cache->ratio;
+    return from_cuda(launch_cache_write_proj(*cache, h, pos0 / r, n_pos / r, w0, w1, wik_codes, wik_scales,
+                                             (cudaStream_t)stream));
 }
 
 csa2_status csa2_quantize_fp4(const float* x, int64_t n_rows, int32_t d, uint8_t* codes, uint8_t* scales,

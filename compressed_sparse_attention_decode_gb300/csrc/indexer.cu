@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(256) k_scan_full(const uint8_t* __restrict__ k
                                                    int QB, int E, int k, int pool_blocks, int bs,
                                                    int* __restrict__ counts, int* __restrict__ cid,
                                                    float2* __restrict__ clu, int* __restrict__ bid,
-                                                   float2* __restrict__ blu, int list_len) {
+                                                   float2* __restrict__ blu, int list_len, int ratio) {
     pdl_wait();
     pdl_launch_next();
     extern __shared__ int smem[];
@@ -52,7 +52,7 @@ __global__ void __launch_bounds__(256) k_scan_full(const uint8_t* __restrict__ k
         const int64_t gq = (int64_t)b * n_q + q0 + qa + t;
         stage_query<DI>(v, iq_codes + gq * H * (DI / 2), iq_scales + gq * H * (DI / 16), nullptr, w_head + gq * H, H,
                         threadIdx.x, blockDim.x);
-        if (threadIdx.x == 0) nel[t] = n_elig_of(q_pos[gq], capacity);
+        if (threadIdx.x == 0) nel[t] = n_elig_of(q_pos[gq], capacity, ratio);
     }
     __syncthreads();
     const int c0 = blockIdx.x * E;
@@ -710,7 +710,7 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
                                                 int32_t* __restrict__ pool_out, const int32_t* __restrict__ bid,
                                                 const float2* __restrict__ blu, int* __restrict__ c2id,
                                                 unsigned long long* __restrict__ c2key, int* __restrict__ h2id,
-                                                unsigned long long* __restrict__ h2key) {
+                                                unsigned long long* __restrict__ h2key, int ratio) {
     pdl_wait();
     pdl_launch_next();
     extern __shared__ int qsm[];
@@ -806,7 +806,7 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
     // ---- 2. exact scores of the candidates, 3. the k best, written in
     // ascending entry order (in shared memory when they fit, the usual case:
     // k plus the few entries whose bounds straddle the threshold)
-    const int id_bound = counts ? n_elig_of(q_pos[gq], capacity) : capacity;
+    const int id_bound = counts ? n_elig_of(q_pos[gq], capacity, ratio) : capacity;
     int kept;
     if (m <= MAX_K) {
         for (int t = threadIdx.x; t < m; t += blockDim.x) {
@@ -832,7 +832,7 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
 
     // ---- 4. HSI candidate pool (Full only)
     if (pool_blocks <= 0 || pure || !counts || (split && blockIdx.z == 0)) return;
-    const int n_elig = n_elig_of(q_pos[gq], capacity);
+    const int n_elig = n_elig_of(q_pos[gq], capacity, ratio);
     const int P = pool_blocks * bs;
     int32_t* pout = pool_out + gq * P;
     const int nb = (n_elig + bs - 1) / bs;
@@ -1054,7 +1054,7 @@ cudaError_t launch_indexer_full_t(const csa2_cache& c, const uint8_t* iq_codes, 
             dim3 g1((c.capacity + E - 1) / E, (n_qc + QB - 1) / QB, c.batch);
             launch_k(k_scan_full<DI>, g1, 256, smem1, st, c.ikey_codes, c.ikey_scales, c.capacity, iq_codes, iq_scales,
                                                     w_head, q_pos, n_q, q0, n_qc, H, QB, E, kf, pb_scan, bs_scan,
-                                                    w.counts, w.ids, w.lu, w.bid, w.blu, (int)list_len);
+                                                    w.counts, w.ids, w.lu, w.bid, w.blu, (int)list_len, (int)c.ratio);
             note_launch();
             e = cudaGetLastError();
         }
@@ -1069,7 +1069,7 @@ cudaError_t launch_indexer_full_t(const csa2_cache& c, const uint8_t* iq_codes, 
         launch_k(k_select<DI>, g2, 512, smem2, st, w.ids, w.lu, w.counts, 0, (int)list_len, c.ikey_codes, c.ikey_scales,
                                               c.capacity, iq_codes, iq_scales, (const float*)nullptr, w_head, q_pos, n_q, q0, n_qc, H, k,
                                               idx_out, pool_blocks, bs, pool_out, w.bid, w.blu, w.c2id, w.c2key,
-                                              w.bid, reinterpret_cast<unsigned long long*>(w.blu));
+                                              w.bid, reinterpret_cast<unsigned long long*>(w.blu), (int)c.ratio);
         note_launch();
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
@@ -1124,7 +1124,7 @@ cudaError_t launch_reindex_t(const csa2_cache& c, const uint8_t* iq_codes, const
     launch_k(k_select<DI>, g, 512, smem, st, pool, w.lu, nullptr, pool_len, pool_len, c.ikey_codes, c.ikey_scales,
                                        c.capacity, iq_codes, iq_scales, iq_raw, w_head, nullptr, n_q, 0, n_q, H, k, idx_out, 0,
                                        1, nullptr, nullptr, nullptr, w.c2id, w.c2key, (int*)nullptr,
-                                       (unsigned long long*)nullptr);
+                                       (unsigned long long*)nullptr, (int)c.ratio);
     note_launch();
     return cudaGetLastError();
 }

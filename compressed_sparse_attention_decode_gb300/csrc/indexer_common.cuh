@@ -175,8 +175,10 @@ __device__ double exact_score(const uint8_t* __restrict__ kc, const uint8_t* __r
     return S;
 }
 
-__device__ __forceinline__ int n_elig_of(int64_t p, int capacity) {
-    int64_t n = (p - (WINDOW - 1)) >> 1;
+// entries wholly before the window [p-127, p] of a query at raw position p, for
+// a cache of `ratio` raw positions per entry; clamped to the capacity
+__device__ __forceinline__ int n_elig_of(int64_t p, int capacity, int ratio) {
+    int64_t n = ratio == 1 ? p - (WINDOW - 1) : (p - (WINDOW - 1)) >> 1;
     if (p < WINDOW - 1) n = 0;
     return (int)(n < capacity ? n : capacity);
 }

@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(256, 2) k_scan_full_tc(
     const uint8_t* __restrict__ iq_codes, const uint8_t* __restrict__ iq_scales, const float* __restrict__ w_head,
     const int64_t* __restrict__ q_pos, int n_q, int q0, int n_qc, int H, int k, int pool_blocks, int bs,
     int* __restrict__ counts, int* __restrict__ cid, float2* __restrict__ clu, int* __restrict__ bid,
-    float2* __restrict__ blu, int list_len, int* __restrict__ err) {
+    float2* __restrict__ blu, int list_len, int* __restrict__ err, int ratio) {
     pdl_wait();             // the selection that follows is let in only as the scan's blocks exit
     extern __shared__ uint8_t dyn[];
     __shared__ RadixSmem rs;
@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(256, 2) k_scan_full_tc(
     constexpr int N = ITC_N;
 
     if (tid == 0) {
-        s_nel = n_elig_of(q_pos[gq], capacity);
+        s_nel = n_elig_of(q_pos[gq], capacity, ratio);
         for (int i = 0; i < ITC_NR; ++i) {
             umma::mbar_init(umma::smem_u32(&bar_rfull[i]), 1);
             umma::mbar_init(umma::smem_u32(&bar_rfree[i]), 128);
@@ -249,7 +249,7 @@ cudaError_t launch_scan_full_tc(const csa2_cache& c, const uint8_t* iq_codes, co
     dim3 grid((c.capacity + ITC_E - 1) / ITC_E, n_qc, c.batch);
     launch_k(k_scan_full_tc, grid, 256, IS_DYN, st, c.ikey_codes, c.ikey_scales, c.capacity, iq_codes, iq_scales, w_head,
                                               q_pos, n_q, q0, n_qc, H, k, pool_blocks, bs, counts, cid, clu, bid, blu,
-                                              list_len, err);
+                                              list_len, err, (int)c.ratio);
     note_launch();
     return cudaGetLastError();
 }

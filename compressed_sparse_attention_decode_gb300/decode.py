@@ -13,7 +13,7 @@ is a C-ABI entry point of libcsa2; this module only sequences them.
 import torch
 
 from . import (FULL, REINDEX, REUSE, OP_INDEXER_TOPK, OP_REINDEX, OP_SPARSE_ATTN, Cache, csa2_cache_write,
-               csa2_indexer_topk, csa2_quantize_fp4, csa2_reindex_f32, csa2_sparse_attn, workspace)
+               csa2_cache_write_projected, csa2_indexer_topk, csa2_quantize_fp4, csa2_reindex_f32, csa2_sparse_attn, workspace)
 
 _MODES = {"full": FULL, "reindex": REINDEX, "reuse": REUSE}
 
@@ -28,7 +28,7 @@ class DecodeStep:
     layer writes idx[l], a Reuse layer reads layer_idx(l) in place."""
 
     def __init__(self, B, capacity, n_q, layers, H=64, H_I=8, d_I=128, k=512, pool_blocks=0, pool_block_size=8,
-                 swa_len=128, chunk_pos=0, device="cuda", want_lse=False):
+                 swa_len=128, chunk_pos=0, device="cuda", want_lse=False, ratio=2):
         self.B, self.capacity, self.n_q, self.layers = B, capacity, n_q, tuple(layers)
         self.H, self.H_I, self.d_I, self.k = H, H_I, d_I, k
         self.pool_blocks, self.bs = pool_blocks, pool_block_size
@@ -36,7 +36,7 @@ class DecodeStep:
         self.dev = device
         L = len(self.layers)
         f32, bf16, i32 = torch.float32, torch.bfloat16, torch.int32
-        self.cache = Cache(B, capacity, d_I, device)
+        self.cache = Cache(B, capacity, d_I, device, ratio=ratio)
         # step inputs
         n_idx = sum(m != "reuse" for m in self.layers)
         self.iq = torch.zeros((max(n_idx, 1), B, n_q, H_I, d_I), dtype=f32, device=device)
@@ -51,6 +51,9 @@ class DecodeStep:
         self.kraw_chunk = None
         self.w0 = torch.zeros(512, dtype=f32, device=device)
         self.w1 = torch.zeros(512, dtype=f32, device=device)
+        # FP4 indexer-key projection W (codes, scales): when set, the cache
+        # writes project the indexer keys from the entries
+        self.wik_codes = self.wik_scales = None
         # outputs / intermediates
         self.iq_codes = torch.zeros((B, n_q, H_I, d_I // 2), dtype=torch.uint8, device=device)
         self.iq_scales = torch.zeros((B, n_q, H_I, d_I // 16), dtype=torch.uint8, device=device)
@@ -71,13 +74,17 @@ class DecodeStep:
         starting at chunk_pos into the cache"""
         self.chunk_len = chunk_len
         self.h_chunk = torch.zeros((self.B, chunk_len, 512), dtype=torch.bfloat16, device=self.dev)
-        self.kraw_chunk = torch.zeros((self.B, chunk_len // 2, self.d_I), dtype=torch.bfloat16, device=self.dev)
+        self.kraw_chunk = torch.zeros((self.B, chunk_len // self.cache.ratio, self.d_I), dtype=torch.bfloat16,
+                                      device=self.dev)
         self.w0.copy_(w0)
         self.w1.copy_(w1)
 
     def enqueue(self, stream=None):
         """all layers of one step, in order, on `stream` (default: current)"""
-        if self.chunk_len:
+        if self.chunk_len and self.wik_codes is not None:
+            csa2_cache_write_projected(self.cache, self.h_chunk, self.chunk_pos, self.w0, self.w1, self.wik_codes,
+                                       self.wik_scales, stream=stream)
+        elif self.chunk_len:
             csa2_cache_write(self.cache, self.h_chunk, self.chunk_pos, self.w0, self.w1, self.kraw_chunk,
                              stream=stream)
         t = 0

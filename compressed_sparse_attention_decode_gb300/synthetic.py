@@ -10,7 +10,7 @@ import torch
 
 from synth.workloads import D_LAT
 
-from . import Cache, csa2_cache_write
+from . import Cache, csa2_cache_write, csa2_cache_write_projected, csa2_quantize_fp4
 from .decode import DecodeStep
 
 
@@ -22,7 +22,7 @@ def _bf16(a):
 def seq_view(cache, b):
     """a batch-1 Cache aliasing sequence b of `cache`"""
     v = Cache.__new__(Cache)
-    v.batch, v.capacity, v.d_idx = 1, cache.capacity, cache.d_idx
+    v.batch, v.capacity, v.d_idx, v.ratio = 1, cache.capacity, cache.d_idx, cache.ratio
     v.lat_codes = cache.lat_codes[b:b + 1]
     v.lat_scales = cache.lat_scales[b:b + 1]
     v.ikey_codes = cache.ikey_codes[b:b + 1]
@@ -79,7 +79,7 @@ def build_step(wl, device="cuda", want_lse=False, seqs=None, capture_inputs=Fals
     first, count = wl.swa_range()
     step = DecodeStep(B, wl.n_entries, wl.n_q, wl.layers, H=wl.H, H_I=wl.H_I, d_I=wl.d_I, k=wl.k,
                       pool_blocks=wl.pool_blocks, pool_block_size=wl.pool_block_size, swa_len=count,
-                      chunk_pos=wl.prefix, device=device, want_lse=want_lse)
+                      chunk_pos=wl.prefix, device=device, want_lse=want_lse, ratio=wl.ratio)
     step.swa_pos0 = first
     w0, w1 = wl.merge_weights()
     w0_d = torch.from_numpy(w0).to(device)
@@ -88,17 +88,25 @@ def build_step(wl, device="cuda", want_lse=False, seqs=None, capture_inputs=Fals
         step.set_chunk(wl.chunk, w0_d, w1_d)
     qpos = torch.from_numpy(wl.q_positions())
     step.q_pos.copy_(qpos[None, :].expand(B, -1))
+    if wl.ikey_proj:
+        # the indexer-key projection W, quantised to FP4 by the library's own quantiser
+        wik = torch.from_numpy(wl.w_ik()).to(device)
+        step.wik_codes, step.wik_scales = csa2_quantize_fp4(wik)
     for bi, b in enumerate(seqs):
         # context written once, outside the step
         n_ctx = wl.prefix
         if n_ctx:
-            h = wl.h(b, 0, n_ctx)
-            kr = wl.kraw(b, 0, n_ctx // 2)
-            csa2_cache_write(seq_view(step.cache, bi), _bf16(h)[None].to(device), 0, w0_d, w1_d,
-                             _bf16(kr)[None].to(device))
+            h = _bf16(wl.h(b, 0, n_ctx))[None].to(device)
+            if wl.ikey_proj:
+                csa2_cache_write_projected(seq_view(step.cache, bi), h, 0, w0_d, w1_d, step.wik_codes,
+                                           step.wik_scales)
+            else:
+                kr = wl.kraw(b, 0, n_ctx // wl.ratio)
+                csa2_cache_write(seq_view(step.cache, bi), h, 0, w0_d, w1_d, _bf16(kr)[None].to(device))
         if wl.chunk:
             step.h_chunk[bi].copy_(_bf16(wl.h(b, wl.prefix, wl.chunk)))
-            step.kraw_chunk[bi].copy_(_bf16(wl.kraw(b, wl.prefix // 2, wl.chunk // 2)))
+            if not wl.ikey_proj:
+                step.kraw_chunk[bi].copy_(_bf16(wl.kraw(b, wl.prefix // wl.ratio, wl.chunk // wl.ratio)))
         t = 0
         for l, mode in enumerate(wl.layers):
             step.win[l, bi].copy_(_bf16(wl.window(l, b)))

@@ -15,8 +15,9 @@
  *     k, q.k exact, the head sum an fp64 fused multiply-add chain in ascending h;
  *     ranking by (score desc, entry index asc);
  *   - a query at raw position p sees global entries i < n_elig(p) =
- *     floor((p-127)/2) (entries lying wholly before its window) and the window
- *     rows of raw positions max(0, p-127) .. p.
+ *     floor((p-127)/ratio) (entries lying wholly before its window; ratio 2
+ *     for an encoder copy, 1 for the decoder's) and the window rows of raw
+ *     positions max(0, p-127) .. p.
  *
  * Conventions (all entry points):
  *   - Every array argument is DEVICE memory allocated and owned by the caller;
@@ -73,10 +74,14 @@ enum { CSA2_OP_INDEXER_TOPK = 1, CSA2_OP_REINDEX = 2, CSA2_OP_SPARSE_ATTN = 3 };
  *   lat_scales  [batch][capacity][d_lat/16]  E4M3 scales of the latent
  *   ikey_codes  [batch][capacity][d_idx/2]   E2M1 codes of the indexer key
  *   ikey_scales [batch][capacity][d_idx/16]  E4M3 scales of the indexer key
- * Entry i merges raw positions 2i and 2i+1 (encoder compression ratio 2).
+ * ratio is the number of raw positions per entry: 2 for an encoder copy
+ * (entry i merges raw positions 2i and 2i+1, §1.1), 1 for the decoder's copy
+ * (entry i is raw position i, kept per position for addressability, §2.3.3);
+ * a query at raw position p may read entries i < n_elig(p) = floor((p-127) /
+ * ratio), those lying wholly before its window.
  * lat_codes, lat_scales and ikey_codes must be 16-byte aligned, ikey_scales
  * d_idx/16-byte aligned (so a batch-1 view of one sequence of a larger cache
- * is always valid).  d_lat must be 512; d_idx must be 64 or 128.
+ * is always valid).  d_lat must be 512; d_idx must be 64 or 128; ratio 1 or 2.
  */
 typedef struct {
     uint8_t* lat_codes;
@@ -87,24 +92,46 @@ typedef struct {
     int32_t capacity;
     int32_t d_lat;
     int32_t d_idx;
+    int32_t ratio;
 } csa2_cache;
 
 /*
  * Cache write: the encoder's 2:1 channel-wise merge fused with FP4
  * quantisation ("DeepSeek-v4.1 Flash" §1.1 sequence dimension; §2.3.1: the
  * CSA2 compressor merges without overlap and without absolute position
- * embedding).  For every sequence b and entry i in [pos0/2, pos0/2 + n_pos/2):
+ * embedding).  For a ratio-2 cache, every sequence b and entry i in
+ * [pos0/2, pos0/2 + n_pos/2):
  *     e[c] = fmaf(w1[c], h[2i+1][c], float(w0[c] * h[2i][c]))   (fp32)
- * quantised to FP4 into lat_codes / lat_scales.  If ikey_raw is not NULL its
- * rows (one per entry) are quantised into ikey_codes / ikey_scales.
+ * quantised to FP4 into lat_codes / lat_scales; for a ratio-1 cache (the
+ * decoder's, §2.3.3) entry i is raw position i, h[i] quantised as it is (w0 and
+ * w1 are not read and may be NULL).  If ikey_raw is not NULL its rows (one per
+ * entry) are quantised into ikey_codes / ikey_scales.
  *   h        bf16 [batch][n_pos][d_lat], raw positions pos0 .. pos0+n_pos-1
  *   w0, w1   fp32 [d_lat]
- *   ikey_raw bf16 [batch][n_pos/2][d_idx] or NULL
- * pos0 and n_pos must be even, pos0/2 + n_pos/2 <= capacity.  Inputs must be
- * finite.
+ *   ikey_raw bf16 [batch][n_pos/ratio][d_idx] or NULL
+ * Ratio 2: pos0 and n_pos even.  pos0/ratio + n_pos/ratio <= capacity.  Inputs
+ * must be finite.
  */
 csa2_status csa2_cache_write(const csa2_cache* cache, const uint16_t* h, int64_t pos0, int32_t n_pos,
                              const float* w0, const float* w1, const uint16_t* ikey_raw, void* stream);
+
+/*
+ * Cache write with the indexer keys projected from the entries ("DeepSeek-v4.1
+ * Flash" §2.3.1: the indexer K is a projection of the main KV entry, which
+ * replaces CSA's separate compression path): the latent as csa2_cache_write
+ * writes it, and for every entry
+ *     k[d] = sum_c W[d][c] * L[c],   d < d_idx
+ * over the stored entry L (the dequantised FP4 latent just written) and the
+ * projection W, given in the same FP4 format; the exact sum is rounded once to
+ * fp32 and quantised into ikey_codes / ikey_scales with the cache's codec.  One
+ * kernel does both per entry.
+ *   wik_codes  uint8 [d_idx][d_lat/2] E2M1 codes of W (16-byte aligned)
+ *   wik_scales uint8 [d_idx][d_lat/16] E4M3 scales of W (4-byte aligned)
+ * Other arguments and conditions as csa2_cache_write (ikey_raw not taken).
+ */
+csa2_status csa2_cache_write_projected(const csa2_cache* cache, const uint16_t* h, int64_t pos0, int32_t n_pos,
+                                       const float* w0, const float* w1, const uint8_t* wik_codes,
+                                       const uint8_t* wik_scales, void* stream);
 
 /*
  * FP4 quantisation of fp32 rows (the same codec as the cache): used for the

@@ -45,16 +45,16 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_host_side_validation_needs_no_gpu(lib):
     import compressed_sparse_attention_decode_gb300 as csa
-    assert lib.csa2_abi_version() == 100
+    assert lib.csa2_abi_version() == 200
     assert lib.csa2_status_string(1) == b"invalid argument"
     # NULL cache / bad sizes are refused before any CUDA call
     assert lib.csa2_cache_write(None, None, 0, 0, None, None, None, None) == csa.ERR_INVALID_ARG
-    c = csa._CacheStruct(16, 16, 16, 16, 1, 8, 512, 128)
+    c = csa._CacheStruct(16, 16, 16, 16, 1, 8, 512, 128, 2)
     assert lib.csa2_cache_write(ctypes.byref(c), ctypes.c_void_p(16), 1, 2, ctypes.c_void_p(16),
                                 ctypes.c_void_p(16), None, None) == csa.ERR_INVALID_ARG     # odd pos0
     assert lib.csa2_cache_write(ctypes.byref(c), ctypes.c_void_p(16), 0, 18, ctypes.c_void_p(16),
                                 ctypes.c_void_p(16), None, None) == csa.ERR_INVALID_ARG     # beyond capacity
-    bad = csa._CacheStruct(16, 16, 16, 16, 1, 8, 256, 128)
+    bad = csa._CacheStruct(16, 16, 16, 16, 1, 8, 256, 128, 2)
     assert lib.csa2_sparse_attn(ctypes.byref(bad), None, 1, 1, None, None, 0, None, 0, 0, 1.0, None, None, None,
                                 0, None) == csa.ERR_UNSUPPORTED
     p = ctypes.c_void_p(256)

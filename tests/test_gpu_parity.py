@@ -123,6 +123,67 @@ def check_walk(csa, wl, seqs, queries=None, layers=None):
     return step
 
 
+@pytest.mark.parametrize("ratio,d_idx", [(1, 128), (1, 64), (2, 128)])
+def test_projected_cache_write_bit_exact(csa, ratio, d_idx):
+    """indexer keys projected from the stored entries (FP4 W times the FP4 entry,
+    exact sum, then the FP4 codec) in the same launch as the entry write: every byte
+    of all four planes against the oracle; two writes (a prefix, then a ragged tail
+    at a nonzero position) so that the position offset is exercised"""
+    wl = scaled(WORKLOADS[2], B=1, T=2 * 1000 + 2 * 37, d_I=d_idx, ratio=ratio, ikey_proj=True)
+    cache = csa.Cache(1, wl.n_entries, d_idx, ratio=ratio)
+    w0, w1 = (torch.from_numpy(w).cuda() for w in wl.merge_weights())
+    wc, ws = csa.csa2_quantize_fp4(torch.from_numpy(wl.w_ik()).cuda())
+    h = bf16_t(wl.h(0, 0, wl.T))[None]
+    csa.csa2_cache_write_projected(cache, h[:, :2000].contiguous(), 0, w0, w1, wc, ws)
+    csa.csa2_cache_write_projected(cache, h[:, 2000:].contiguous(), 2000, w0, w1, wc, ws)
+    torch.cuda.synchronize()
+    want = oracle.sequence_cache(wl, 0)
+    got = (cache.lat_codes, cache.lat_scales, cache.ikey_codes, cache.ikey_scales)
+    for name, g, w in zip(("lat_codes", "lat_scales", "ikey_codes", "ikey_scales"), got, want):
+        assert np.array_equal(g[0].cpu().numpy(), w), name
+    # W is the library's own quantisation of the same rows
+    wc_ref, ws_ref = oracle.quantize_rows(wl.w_ik())
+    assert np.array_equal(wc.cpu().numpy(), wc_ref) and np.array_equal(ws.cpu().numpy(), ws_ref)
+
+
+def test_ratio_mismatch_is_rejected(csa):
+    """a ratio-1 cache write whose raw rows do not cover whole entries of the
+    cache's ratio, or a ratio outside {1, 2}, is refused before any launch"""
+    cache = csa.Cache(1, 64, 128, ratio=3)
+    h = torch.zeros((1, 8, 512), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros(512, dtype=torch.float32, device="cuda")
+    kr = torch.zeros((1, 4, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(RuntimeError):
+        csa.csa2_cache_write(cache, h, 0, w, w, kr)
+    cache2 = csa.Cache(1, 64, 128, ratio=2)
+    with pytest.raises(RuntimeError):
+        csa.csa2_cache_write(cache2, h[:, :7].contiguous(), 0, w, w, kr)
+    torch.cuda.synchronize()
+
+
+def test_decoder_ratio1_projected_schedule(csa):
+    """the decoder's cache (one entry per raw position, indexer keys projected):
+    Full (+HSI pool) -> Reuse x3 -> Reindex -> Reuse x3, every index and output"""
+    wl = scaled(WORKLOADS[2], B=2, T=9000 + 77, ratio=1, ikey_proj=True, pool_blocks=256,
+                layers=("full", "reuse", "reuse", "reuse", "reindex", "reuse", "reuse", "reuse"))
+    check_walk(csa, wl, [0, 1])
+
+
+def test_decoder_ratio1_short_contexts(csa):
+    """ratio 1 near the start of a sequence: fewer eligible entries than k,
+    none at all, exactly k"""
+    for T in (100, 128, 129, 200, 128 + 64):
+        wl = scaled(WORKLOADS[2], B=1, T=T, k=64, H=16, ratio=1, ikey_proj=True, layers=("full", "reuse"))
+        check_walk(csa, wl, [0])
+
+
+def test_decoder_ratio1_chunked_prefill(csa):
+    """a 512-position chunk written in the step (projected keys), per-query
+    causal top-k over the ratio-1 cache"""
+    wl = scaled(WORKLOADS[4], T=4096 + 512, chunk=512, ratio=1, ikey_proj=True)
+    check_walk(csa, wl, [0], queries=[0, 1, 2, 255, 511])
+
+
 def test_tiny_workload(csa):
     check_walk(csa, WORKLOADS[0], [0])
 

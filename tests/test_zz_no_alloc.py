@@ -107,7 +107,7 @@ def test_noalloc_large_pool_after_a_differently_shaped_call_matches_the_oracle(c
 
 def test_noalloc_reindex_rejects_requests_beyond_its_scratch(csa):
     lib = csa.load()
-    c = csa._CacheStruct(256, 256, 256, 256, 64, 100000, 512, 128)
+    c = csa._CacheStruct(256, 256, 256, 256, 64, 100000, 512, 128, 2)
     p = ctypes.c_void_p(256)
     # 64 sequences x 4 queries x 16384 pool slots needs far more than 8 MiB
     assert lib.csa2_reindex_noalloc(ctypes.byref(c), p, p, p, 4, 8, p, 16384, 512, p, None) == csa.ERR_WORKSPACE
