@@ -2,7 +2,12 @@
 share one FP4 global KV (Full + HSI pool, 9 Reindex, 10 Reuse), batch 64 per
 GPU, plus the HBM-roofline fraction of the dominant entry point.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+--workload decode-128k-b64-40L-ced times one decode step of the whole 40-layer
+CED model instead (2 SWA layers, 3 encoder blocks of Full + 5 Reuse over three
+2:1 copies, 5 decoder blocks over the per-position copy), each copy first
+receiving its newest entry.
 
 One JSON line on rank 0.  --impl reference times the fp64 CPU oracle (the
 only other implementation there is) on the host cores, on a bounded sample.
@@ -35,19 +40,35 @@ def parse():
     ap.add_argument("--cpu-sample-seqs", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="decode-128k-b64-20L",
-                    help="decode-128k-b64-20L (the benchmark), or profile-16k-b64-20L: the same 20-layer shape "
-                         "at 16K context (189 MB cache, still larger than L2) for ncu captures")
+                    help="decode-128k-b64-20L (the benchmark); decode-128k-b64-40L-ced (the 40-layer model "
+                         "over four cache copies); profile-16k-b64-20L / profile-16k-b64-40L-ced: the same shapes "
+                         "at 16K context (still larger than L2) for ncu captures")
     return ap.parse_args()
 
 
 def workload_of(name):
-    from synth.workloads import WORKLOADS, scaled
+    """a Workload (one cache copy) or a Schedule (several)"""
+    from synth.workloads import CED_40L, WORKLOADS, scaled, scaled_schedule
     wl = WORKLOADS[WORKLOAD_INDEX]
     if name == wl.name:
         return wl
     if name == "profile-16k-b64-20L":
         return scaled(wl, name=name, T=16384)
+    if name == CED_40L.name:
+        return CED_40L
+    if name == "profile-16k-b64-40L-ced":
+        return scaled_schedule(CED_40L, name=name, T=16384)
     raise SystemExit("unknown workload %r" % name)
+
+
+def segments_of(wl):
+    """the cache copies of a workload, each with the layers that read it"""
+    return list(wl.segments) if hasattr(wl, "segments") else [wl]
+
+
+def with_batch(wl, B):
+    from synth.workloads import scaled, scaled_schedule
+    return scaled_schedule(wl, B=B) if hasattr(wl, "segments") else scaled(wl, B=B)
 
 
 def dist_env():
@@ -66,10 +87,21 @@ def measured_peak():
 
 
 def config_of(wl):
-    return {"workload": wl.name, "batch_per_gpu": wl.B, "context": wl.T,
-            "layers": "1 Full (+HSI pool 256x8), 9 Reindex, 10 Reuse", "top_k": wl.k, "heads": wl.H,
-            "indexer": "%d heads x %d FP4" % (wl.H_I, wl.d_I), "window": 128, "latent": 512,
-            "l2": "inputs larger than L2 (%.2f GB FP4 cache per GPU)" % (wl.B * wl.n_entries * 360 / 1e9)}
+    segs = segments_of(wl)
+    s0 = segs[0]
+    cache_bytes = sum(s.B * s.n_entries * 360 for s in segs)
+    if len(segs) == 1:
+        layers = "1 Full (+HSI pool 256x8), 9 Reindex, 10 Reuse"
+    else:
+        layers = ("40: SWA x2; 3 x [Full + Reuse x5] over three 2:1 copies; [Full (+HSI pool 256x8) + Reuse x3] "
+                  "+ 4 x [Reindex + Reuse x3] over the per-position copy (projected indexer keys); every copy "
+                  "written its newest entry in the step")
+    cfg = {"workload": wl.name, "batch_per_gpu": s0.B, "context": s0.T, "layers": layers, "top_k": s0.k,
+           "heads": s0.H, "indexer": "%d heads x %d FP4" % (s0.H_I, s0.d_I), "window": 128, "latent": 512,
+           "l2": "inputs larger than L2 (%.2f GB FP4 cache per GPU)" % (cache_bytes / 1e9)}
+    if len(segs) > 1:
+        cfg["cache_bytes_per_token"] = cache_bytes / (s0.B * s0.T)
+    return cfg
 
 
 NORTH_STAR_HBM_GBS = 8000.0    # the "about 8 TB/s" the target fraction is quoted against
@@ -77,8 +109,9 @@ NORTH_STAR_HBM_GBS = 8000.0    # the "about 8 TB/s" the target fraction is quote
 
 def n_elig_decode(wl):
     """global entries a decode query at raw position T-1 may read: those lying
-    wholly before its 128-row window (entry i covers raw positions 2i, 2i+1)"""
-    return max(0, (wl.T - 1 - 127) // 2)
+    wholly before its 128-row window (entry i covers raw positions ratio*i ..
+    ratio*i + ratio - 1)"""
+    return max(0, (wl.T - 1 - 127) // wl.ratio)
 
 
 def attn_bytes_per_query(wl):
@@ -93,18 +126,39 @@ def attn_extra_bytes_per_query(wl):
     return wl.H * 512 * 2 + wl.k * 4 + wl.H * 512 * 4
 
 
+def op_bytes(wl):
+    """algorithmic bytes each entry point must move in one step, over every copy:
+    a Full scan its eligible keys (n_elig x 72 B), a Reindex its pool keys (pool
+    x 72 B), an attention its gather (k x 288 B + 128 window rows x 1 KB; a
+    window-only layer the window alone), a decode step's cache write the newest
+    entry's hidden rows in (ratio x 1 KB) and the entry out (360 B)"""
+    d = {}
+
+    def add(name, n):
+        d[name] = d.get(name, 0) + n
+
+    for s in segments_of(wl):
+        for mode in s.layers:
+            if mode == "full":
+                add("indexer_full", s.B * n_elig_decode(s) * 72)
+            elif mode == "reindex":
+                add("reindex", s.B * s.pool_len * 72)
+            if mode == "swa":
+                add("swa_attn", s.B * 128 * 1024)
+            else:
+                add("sparse_attn", s.B * attn_bytes_per_query(s))
+        if s.new_entry:
+            add("cache_write", s.B * (s.ratio * 1024 + 360))
+    return d
+
+
 def algorithmic_bytes(wl):
-    """bytes the indexer scan plus the gather must move in one step: the Full
-    scan's eligible keys (n_elig x 72 B), every Reindex layer's pool keys (pool x
-    72 B) and every layer's gather (k x 288 B + 128 window rows x 1 KB)"""
-    n_re = sum(m == "reindex" for m in wl.layers)
-    per_seq = n_elig_decode(wl) * 72 + n_re * wl.pool_len * 72 + \
-        len(wl.layers) * attn_bytes_per_query(wl)
-    return wl.B * per_seq
+    return sum(op_bytes(wl).values())
 
 
 def extra_bytes(wl):
-    return wl.B * len(wl.layers) * attn_extra_bytes_per_query(wl)
+    return sum(s.B * sum(m != "swa" for m in s.layers) * attn_extra_bytes_per_query(s) +
+               s.B * sum(m == "swa" for m in s.layers) * s.H * 512 * 6 for s in segments_of(wl))
 
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture of
@@ -116,7 +170,7 @@ MEASURED_TRAFFIC = {}
 
 def kernel_source_sha(name):
     import hashlib
-    f = {"sparse_attn": "attn_pair.cu", "indexer_full": "indexer_tc.cu", "reindex": "indexer.cu"}.get(name)
+    f = {"sparse_attn": "attn_pair.cu", "indexer_full": "indexer_tc.cu", "reindex": "reindex_tc.cu"}.get(name)
     if f is None:
         return None
     path = os.path.join(ROOT, "compressed_sparse_attention_decode_gb300", "csrc", f)
@@ -180,14 +234,25 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- oracle timing
 
+def oracle_caches(wl, b):
+    import oracle
+    return [oracle.sequence_cache(s, b) for s in segments_of(wl)]
+
+
+def oracle_step(wl, b, caches):
+    """one sequence through every layer of every copy"""
+    import oracle
+    for s, c in zip(segments_of(wl), caches):
+        oracle.run_sequence(s, b, cache=c)
+
+
 def cpu_baseline(wl, n_seqs):
     """the oracle as it stands on the host cores: n_seqs sequences through all
-    20 layers (cache built beforehand, outside the timed region)"""
-    import oracle
-    caches = [oracle.sequence_cache(wl, b) for b in range(n_seqs)]
+    layers (caches built beforehand, outside the timed region)"""
+    caches = [oracle_caches(wl, b) for b in range(n_seqs)]
     t0 = time.perf_counter()
     for b in range(n_seqs):
-        oracle.run_sequence(wl, b, cache=caches[b])
+        oracle_step(wl, b, caches[b])
     dt = time.perf_counter() - t0
     cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
     return {"value": n_seqs / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
@@ -206,13 +271,13 @@ def run_reference(args):
     # timed region), cycled; timing stops after REF_BUDGET_S so that any
     # --steps finishes within a few minutes
     seqs = list(range(min(4, wl.B, max(1, args.steps + args.warmup))))
-    caches = {b: oracle.sequence_cache(wl, b) for b in seqs}
+    caches = {b: oracle_caches(wl, b) for b in seqs}
     times = []
     t_start = time.perf_counter()
     for s in range(args.warmup + args.steps):
         b = seqs[s % len(seqs)]
         t0 = time.perf_counter()
-        oracle.run_sequence(wl, b, cache=caches[b])
+        oracle_step(wl, b, caches[b])
         dt = time.perf_counter() - t0
         if s >= args.warmup:
             times.append(dt)
@@ -246,9 +311,8 @@ def run_ours(args):
     import __graft_entry__
     __graft_entry__.build()
     import compressed_sparse_attention_decode_gb300 as csa
-    from compressed_sparse_attention_decode_gb300.synthetic import HostInputs, build_step
+    from compressed_sparse_attention_decode_gb300.synthetic import HostInputs, build_schedule, build_step
     from compressed_sparse_attention_decode_gb300 import dist as cdist
-    from synth.workloads import scaled
     wl = workload_of(args.workload)
 
     def barrier():
@@ -259,7 +323,9 @@ def run_ours(args):
 
     # replicas, batch-sharded: rank r owns sequences [64r, 64r+64) of a 64*N batch
     # (weak scaling, nothing exchanged on the data path)
-    step = build_step(scaled(wl, B=wl.B * world), seqs=cdist.shard(wl.B, rank, world))
+    build = build_schedule if hasattr(wl, "segments") else build_step
+    step = build(with_batch(wl, wl.B * world), seqs=cdist.shard(wl.B, rank, world))
+    segs = getattr(step, "segments", [step])
     n0 = csa.csa2_launch_count()
     step.capture()
     launches_per_step = (csa.csa2_launch_count() - n0) // 2      # warm-up enqueue + captured enqueue
@@ -293,14 +359,16 @@ def run_ours(args):
     # device, runs, and copies its outputs (every layer's attention output) back.  Two buffer sets
     # alternate so that the copies of one step overlap the compute of the other (host->device and
     # device->host on their own streams; the steps themselves stay serial on the compute stream).
-    host = HostInputs(step)
+    hosts = [HostInputs(s) for s in segs]
     twin = step.twin()
     twin.capture()
     steps2 = (step, twin)
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    parts = lambda st: getattr(st, "segments", [st])
     for st in steps2:                     # untimed: first-use allocations of the copy path
         with torch.cuda.stream(s_in):
-            host.copy_in(st)
+            for h, sg in zip(hosts, parts(st)):
+                h.copy_in(sg)
     torch.cuda.synchronize()
     # at least 30 steps, so that the two-buffer pipeline runs in its steady state
     n_e2e = max(30, min(args.steps, 300))
@@ -315,7 +383,8 @@ def run_ours(args):
             s_in.wait_event(e_c1[i - 2])          # step i-2 has read this buffer set's inputs
         e_in0[i].record(s_in)
         with torch.cuda.stream(s_in):
-            host.copy_in(st)
+            for h, sg in zip(hosts, parts(st)):
+                h.copy_in(sg)
         e_in1[i].record(s_in)
         stream.wait_event(e_in1[i])
         if i >= 2:
@@ -326,7 +395,8 @@ def run_ours(args):
         s_out.wait_event(e_c1[i])
         e_o0[i].record(s_out)
         with torch.cuda.stream(s_out):
-            host.out.copy_(st.out, non_blocking=True)
+            for h, sg in zip(hosts, parts(st)):
+                h.out.copy_(sg.out, non_blocking=True)
         e_o1[i].record(s_out)
     torch.cuda.synchronize()
     e2e_s = (time.perf_counter() - t0) / n_e2e
@@ -337,10 +407,13 @@ def run_ours(args):
     last = steps2[(n_e2e - 1) % 2]
     step.run()
     torch.cuda.synchronize()
-    e2e_check = {"idx_identical": bool(torch.equal(last.idx, step.idx))}
-    ref_out = step.out.cpu()
-    den = ref_out.abs().amax(-1).clamp_min(1e-30)
-    e2e_check["out_max_rel_err"] = float(((host.out - ref_out).abs().amax(-1) / den).max())
+    e2e_check = {"idx_identical": all(bool(torch.equal(a.idx, b.idx)) for a, b in zip(parts(last), segs))}
+    err = 0.0
+    for h, sg in zip(hosts, segs):
+        ref_out = sg.out.cpu()
+        den = ref_out.abs().amax(-1).clamp_min(1e-30)
+        err = max(err, float(((h.out - ref_out).abs().amax(-1) / den).max()))
+    e2e_check["out_max_rel_err"] = err
     if not (e2e_check["idx_identical"] and e2e_check["out_max_rel_err"] <= 2e-3):
         raise SystemExit("end-to-end step disagrees with the graph step: %r" % e2e_check)
     if world > 1:
@@ -362,12 +435,13 @@ def run_ours(args):
                                           "the %s copy peak (frac) and 8 TB/s (frac_of_8tbs); extra_bytes (queries, "
                                           "indices, fp32 outputs) are moved too but not counted" % peak_kind},
                 "per_op_ms": {k: v["ms"] for k, v in per_op.items()},
-                "e2e": {"value": tokens_per_step / e2e_s, "unit": UNIT, "h2d_bytes_per_step": host.h2d_bytes(),
-                        "d2h_bytes_per_step": host.d2h_bytes(), "h2d_ms": phase_ms[0], "step_ms": phase_ms[1],
+                "e2e": {"value": tokens_per_step / e2e_s, "unit": UNIT,
+                        "h2d_bytes_per_step": sum(h.h2d_bytes() for h in hosts),
+                        "d2h_bytes_per_step": sum(h.d2h_bytes() for h in hosts), "h2d_ms": phase_ms[0], "step_ms": phase_ms[1],
                         "d2h_ms": phase_ms[2], "wall_ms": e2e_s * 1e3, "steps": n_e2e, "check": e2e_check,
-                        "note": "per step: the step's own queries of every layer and newest window rows in, every "
-                                "layer's attention output out; copies of one step overlap the compute of the other "
-                                "of two buffer sets"},
+                        "note": "per step: the step's own queries of every layer, newest window rows (and the "
+                                "hidden rows of a newest entry) in, every layer's attention output out; copies of "
+                                "one step overlap the compute of the other of two buffer sets"},
                 "gpu_launches": launches_per_step * args.steps,
                 "clocks": clk.summary()}
         if world == 1 and not args.no_cpu_baseline:
@@ -395,22 +469,31 @@ def measure_ops(step, stream, reps):
     def add(name, fn):
         calls.setdefault(name, []).append(fn)
 
-    t = 0
-    for l, mode in enumerate(step.layers):
-        idx_l = step.layer_idx(l)
-        if mode == "full":
-            add("quantize_iq", lambda t=t: csa.csa2_quantize_fp4(step.iq[t], step.iq_codes, step.iq_scales))
-            add("indexer_full", lambda t=t, o=idx_l: csa.csa2_indexer_topk(
-                step.cache, step.iq_codes, step.iq_scales, step.w_head[t], step.q_pos, step.k,
-                step.pool_blocks, step.bs, idx_out=o, pool_out=step.pool, ws=step.ws_full))
-            t += 1
-        elif mode == "reindex":
-            add("reindex", lambda t=t, o=idx_l: csa.csa2_reindex_f32(step.cache, step.k, step.iq[t], step.w_head[t],
-                                                                     step.pool, idx_out=o, ws=step.ws_re))
-            t += 1
-        # a Reuse layer launches nothing: its attention reads the latest indices in place
-        add("sparse_attn", lambda l=l, i=idx_l: csa.csa2_sparse_attn(step.cache, step.q[l], step.q_pos, i, step.win[l],
-                                                                     step.swa_pos0, out=step.out[l], ws=step.ws_attn))
+    for sg in getattr(step, "segments", [step]):
+        if sg.chunk_len:
+            if sg.wik_codes is not None:
+                add("cache_write", lambda sg=sg: csa.csa2_cache_write_projected(
+                    sg.cache, sg.h_chunk, sg.chunk_pos, sg.w0, sg.w1, sg.wik_codes, sg.wik_scales))
+            else:
+                add("cache_write", lambda sg=sg: csa.csa2_cache_write(sg.cache, sg.h_chunk, sg.chunk_pos, sg.w0,
+                                                                      sg.w1, sg.kraw_chunk))
+        t = 0
+        for l, mode in enumerate(sg.layers):
+            idx_l = sg.layer_idx(l)
+            if mode == "full":
+                add("quantize_iq", lambda sg=sg, t=t: csa.csa2_quantize_fp4(sg.iq[t], sg.iq_codes, sg.iq_scales))
+                add("indexer_full", lambda sg=sg, t=t, o=idx_l: csa.csa2_indexer_topk(
+                    sg.cache, sg.iq_codes, sg.iq_scales, sg.w_head[t], sg.q_pos, sg.k,
+                    sg.pool_blocks, sg.bs, idx_out=o, pool_out=sg.pool, ws=sg.ws_full))
+                t += 1
+            elif mode == "reindex":
+                add("reindex", lambda sg=sg, t=t, o=idx_l: csa.csa2_reindex_f32(
+                    sg.cache, sg.k, sg.iq[t], sg.w_head[t], sg.pool, idx_out=o, ws=sg.ws_re))
+                t += 1
+            # a Reuse layer launches nothing: its attention reads the latest indices in place
+            add("swa_attn" if mode == "swa" else "sparse_attn",
+                lambda sg=sg, l=l, i=idx_l: csa.csa2_sparse_attn(sg.cache, sg.q[l], sg.q_pos, i, sg.win[l],
+                                                                 sg.swa_pos0, out=sg.out[l], ws=sg.ws_attn))
     out = {}
     for name, fns in calls.items():
         for fn in fns:               # eager warm-up of this entry point's calls
@@ -438,24 +521,25 @@ def measure_ops(step, stream, reps):
 
 def roofline(wl, per_op, peak, peak_kind):
     """HBM roofline of the entry point with the largest share of the step: its
-    algorithmic bytes per launch (scan keys or gathered rows) over its per-launch
-    time, against the measured copy peak and against the 8 TB/s of the target"""
-    bytes_per_launch = {
-        "indexer_full": wl.B * n_elig_decode(wl) * 72,
-        "reindex": wl.B * wl.pool_len * 72,
-        "sparse_attn": wl.B * attn_bytes_per_query(wl),
-    }
-    extra = {"sparse_attn": wl.B * attn_extra_bytes_per_query(wl)}
-    name = max((n for n in per_op if n in bytes_per_launch), key=lambda n: per_op[n]["ms"])
-    t = per_op[name]["per_launch_ms"] * 1e-3
-    ach = bytes_per_launch[name] / t / 1e9
+    algorithmic bytes in one step (scan keys or gathered rows, every launch of
+    it) over its device time in one step, against the measured copy peak and
+    against the 8 TB/s of the target; per launch, both are divided by the
+    launches, which leaves the ratio unchanged"""
+    total = op_bytes(wl)
+    extra = {"sparse_attn": sum(s.B * sum(m != "swa" for m in s.layers) * attn_extra_bytes_per_query(s)
+                                for s in segments_of(wl))}
+    name = max((n for n in per_op if n in total), key=lambda n: per_op[n]["ms"])
+    n_launch = per_op[name]["launches_per_step"]
+    ach = total[name] / (per_op[name]["ms"] * 1e-3) / 1e9
     traffic = None
     rec = MEASURED_TRAFFIC.get(name)
-    if rec and (wl.k, wl.H, wl.B) == (512, 64, 64) and rec["source_sha"] == kernel_source_sha(name):
+    s0 = segments_of(wl)[0]
+    if rec and len(segments_of(wl)) == 1 and (s0.k, s0.H, s0.B) == (512, 64, 64) and \
+            rec["source_sha"] == kernel_source_sha(name):
         traffic = rec["bytes"]
     return {"bound": "hbm", "kernel": name, "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
-            "traffic": traffic, "bytes_per_launch": bytes_per_launch[name],
-            "extra_bytes_per_launch": extra.get(name, 0),
+            "traffic": traffic, "bytes_per_launch": total[name] // n_launch,
+            "extra_bytes_per_launch": extra.get(name, 0) // n_launch,
             "frac_of_8tbs": ach / NORTH_STAR_HBM_GBS,
             "launch_ms": per_op[name]["per_launch_ms"], "peak_kind": peak_kind}
 

@@ -4,11 +4,15 @@ Layer modes follow "DeepSeek-v4.1 Flash: KVã‚­ãƒ£ãƒƒã‚·ãƒ¥åœ§ç¸®ã®é™ç•Œã‚’æŠ¼ã
 and Â§2.3.4: a Full layer scores every eligible entry, keeps its top-k and (with
 HSI) a block-max candidate pool; a Reindex layer re-scores only the pool with
 its own indexer queries; a Reuse layer takes the latest indices unchanged.
-Every layer computes its own attention over its indices plus its window.
+Every layer computes its own attention over its indices plus its window.  A
+window-only ("swa") layer, like the first two encoder layers of Â§2.3.3,
+attends to its window alone.
 
-``DecodeStep`` owns the device buffers of one workload and enqueues a whole
-step on a stream (optionally captured as one CUDA graph).  Each call it makes
-is a C-ABI entry point of libcsa2; this module only sequences them.
+``DecodeStep`` owns the device buffers of one workload (one global-KV copy
+and the layers that read it) and enqueues a whole step on a stream
+(optionally captured as one CUDA graph); ``ScheduleStep`` chains several of
+them, one per copy, into one step of a whole model.  Each call they make is a
+C-ABI entry point of libcsa2; this module only sequences them.
 """
 import torch
 
@@ -18,7 +22,32 @@ from . import (FULL, REINDEX, REUSE, OP_INDEXER_TOPK, OP_REINDEX, OP_SPARSE_ATTN
 _MODES = {"full": FULL, "reindex": REINDEX, "reuse": REUSE}
 
 
-class DecodeStep:
+class _Graphed:
+    """capture()/run() over the subclass's enqueue()"""
+    graph = None
+
+    def capture(self):
+        """record one step as a CUDA graph (replayed by run())"""
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.enqueue(s)          # warm-up outside the graph
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.enqueue()
+        self.graph = g
+        return g
+
+    def run(self):
+        if self.graph is not None:
+            self.graph.replay()
+        else:
+            self.enqueue()
+
+
+class DecodeStep(_Graphed):
     """Buffers and launch sequence for one step of a layer schedule.
 
     layers: tuple of "full" / "reindex" / "reuse"; B sequences, n_q queries
@@ -38,7 +67,7 @@ class DecodeStep:
         f32, bf16, i32 = torch.float32, torch.bfloat16, torch.int32
         self.cache = Cache(B, capacity, d_I, device, ratio=ratio)
         # step inputs
-        n_idx = sum(m != "reuse" for m in self.layers)
+        n_idx = sum(m in ("full", "reindex") for m in self.layers)
         self.iq = torch.zeros((max(n_idx, 1), B, n_q, H_I, d_I), dtype=f32, device=device)
         self.w_head = torch.zeros((max(n_idx, 1), B, n_q, H_I), dtype=f32, device=device)
         self.q = torch.zeros((L, B, n_q, H, 512), dtype=bf16, device=device)
@@ -90,8 +119,8 @@ class DecodeStep:
         t = 0
         for l, mode in enumerate(self.layers):
             idx_l = self.layer_idx(l)
-            if mode == "reuse":
-                pass                 # the latest indices, read in place: no copy, no launch
+            if mode in ("reuse", "swa"):
+                pass                 # Reuse: the latest indices, read in place; SWA: no indices
             elif mode == "full":
                 csa2_quantize_fp4(self.iq[t], self.iq_codes, self.iq_scales, stream=stream)
                 csa2_indexer_topk(self.cache, self.iq_codes, self.iq_scales, self.w_head[t], self.q_pos, self.k,
@@ -109,10 +138,13 @@ class DecodeStep:
     def layer_idx(self, l):
         """the index list layer l attends with: its own for a Full or Reindex
         layer; for a Reuse layer the latest one before it, read in place
-        ("DeepSeek-v4.1 Flash" Â§2.3.2: Reuse takes the latest indices unchanged).
-        Only the layers that compute indices write their slot of self.idx."""
+        ("DeepSeek-v4.1 Flash" Â§2.3.2: Reuse takes the latest indices unchanged);
+        none (k = 0) for a window-only layer.  Only the layers that compute
+        indices write their slot of self.idx."""
+        if self.layers[l] == "swa":
+            return self.idx[l][..., :0]
         src = l
-        while src > 0 and self.layers[src] == "reuse":
+        while src > 0 and self.layers[src] in ("reuse", "swa"):
             src -= 1
         return self.idx[src]
 
@@ -123,29 +155,29 @@ class DecodeStep:
         not run concurrently on the device"""
         t = object.__new__(DecodeStep)
         t.__dict__.update(self.__dict__)
-        for name in ("iq", "w_head", "q", "win", "q_pos", "idx", "out"):
-            setattr(t, name, getattr(self, name).clone())
-        if self.lse is not None:
-            t.lse = self.lse.clone()
+        for name in ("iq", "w_head", "q", "win", "q_pos", "idx", "out", "lse", "h_chunk", "kraw_chunk"):
+            if getattr(self, name) is not None:
+                setattr(t, name, getattr(self, name).clone())
         t.graph = None
         return t
 
-    def capture(self):
-        """record one step as a CUDA graph (replayed by run())"""
-        s = torch.cuda.Stream()
-        s.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(s):
-            self.enqueue(s)          # warm-up outside the graph
-        torch.cuda.current_stream().wait_stream(s)
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            self.enqueue()
-        self.graph = g
-        return g
 
-    def run(self):
-        if self.graph is not None:
-            self.graph.replay()
-        else:
-            self.enqueue()
+class ScheduleStep(_Graphed):
+    """one step of a model whose layers are split over several global-KV copies:
+    the segments (DecodeSteps, one per copy) run in order on one stream"""
+
+    def __init__(self, segments):
+        self.segments = list(segments)
+        self.graph = None
+
+    @property
+    def layers(self):
+        return tuple(m for s in self.segments for m in s.layers)
+
+    def enqueue(self, stream=None):
+        for s in self.segments:
+            s.enqueue(stream)
+
+    def twin(self):
+        """as DecodeStep.twin, segment by segment"""
+        return ScheduleStep([s.twin() for s in self.segments])

@@ -11,7 +11,7 @@ import torch
 from synth.workloads import D_LAT
 
 from . import Cache, csa2_cache_write, csa2_cache_write_projected, csa2_quantize_fp4
-from .decode import DecodeStep
+from .decode import DecodeStep, ScheduleStep
 
 
 def _bf16(a):
@@ -43,7 +43,8 @@ class HostInputs:
         device buffers of `step` hold now are copied out once, here, so every
         timed step moves and computes the real workload"""
         pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-        self.names = ["iq", "w_head", "q", "q_pos"] + (["h_chunk", "kraw_chunk"] if step.chunk_len else [])
+        self.names = ["iq", "w_head", "q", "q_pos"] + (["h_chunk"] if step.chunk_len else []) + \
+            (["kraw_chunk"] if step.chunk_len and step.wik_codes is None else [])
         self.host = {n: pin(getattr(step, n)) for n in self.names}
         for n in self.names:
             self.host[n].copy_(getattr(step, n))
@@ -71,7 +72,7 @@ class HostInputs:
         return self.out.numel() * self.out.element_size()
 
 
-def build_step(wl, device="cuda", want_lse=False, seqs=None, capture_inputs=False):
+def build_step(wl, device="cuda", want_lse=False, seqs=None):
     """DecodeStep for workload wl with context, inputs and window rows loaded.
     seqs: restrict to these sequence ids (default all wl.B)."""
     seqs = list(range(wl.B)) if seqs is None else list(seqs)
@@ -86,6 +87,10 @@ def build_step(wl, device="cuda", want_lse=False, seqs=None, capture_inputs=Fals
     w1_d = torch.from_numpy(w1).to(device)
     if wl.chunk:
         step.set_chunk(wl.chunk, w0_d, w1_d)
+    elif wl.new_entry:
+        # a decode step writes its own newest entry: the last `ratio` raw positions
+        step.chunk_pos = wl.T - wl.ratio
+        step.set_chunk(wl.ratio, w0_d, w1_d)
     qpos = torch.from_numpy(wl.q_positions())
     step.q_pos.copy_(qpos[None, :].expand(B, -1))
     if wl.ikey_proj:
@@ -94,7 +99,7 @@ def build_step(wl, device="cuda", want_lse=False, seqs=None, capture_inputs=Fals
         step.wik_codes, step.wik_scales = csa2_quantize_fp4(wik)
     for bi, b in enumerate(seqs):
         # context written once, outside the step
-        n_ctx = wl.prefix
+        n_ctx = step.chunk_pos if step.chunk_len else wl.T
         if n_ctx:
             h = _bf16(wl.h(b, 0, n_ctx))[None].to(device)
             if wl.ikey_proj:
@@ -103,17 +108,24 @@ def build_step(wl, device="cuda", want_lse=False, seqs=None, capture_inputs=Fals
             else:
                 kr = wl.kraw(b, 0, n_ctx // wl.ratio)
                 csa2_cache_write(seq_view(step.cache, bi), h, 0, w0_d, w1_d, _bf16(kr)[None].to(device))
-        if wl.chunk:
-            step.h_chunk[bi].copy_(_bf16(wl.h(b, wl.prefix, wl.chunk)))
+        if step.chunk_len:
+            p0, n = step.chunk_pos, step.chunk_len
+            step.h_chunk[bi].copy_(_bf16(wl.h(b, p0, n)))
             if not wl.ikey_proj:
-                step.kraw_chunk[bi].copy_(_bf16(wl.kraw(b, wl.prefix // wl.ratio, wl.chunk // wl.ratio)))
+                step.kraw_chunk[bi].copy_(_bf16(wl.kraw(b, p0 // wl.ratio, n // wl.ratio)))
         t = 0
         for l, mode in enumerate(wl.layers):
             step.win[l, bi].copy_(_bf16(wl.window(l, b)))
             step.q[l, bi].copy_(_bf16(wl.q(l, b)))
-            if mode != "reuse":
+            if mode in ("full", "reindex"):
                 step.iq[t, bi].copy_(torch.from_numpy(wl.iq(l, b)))
                 step.w_head[t, bi].copy_(torch.from_numpy(wl.w_head(l, b)))
                 t += 1
     torch.cuda.synchronize()
     return step
+
+
+def build_schedule(sched, device="cuda", want_lse=False, seqs=None):
+    """ScheduleStep for a Schedule: one DecodeStep per global-KV copy, each
+    with its context, inputs and window rows loaded"""
+    return ScheduleStep([build_step(w, device, want_lse, seqs) for w in sched.segments])

@@ -268,7 +268,8 @@ def synth_bf16_to_f32(a):
 
 def run_sequence(wl, b, cache=None, queries=None, layers=None, want_out=True):
     """Walk the layers of workload wl for sequence b (Full -> Reindex -> Reuse),
-    exactly as the pages describe the three modes ([P1] §2.3.2, §2.3.4).
+    exactly as the pages describe the three modes ([P1] §2.3.2, §2.3.4), plus
+    window-only ("swa") layers.
     queries: which query slots (default all); layers: which layer indices.
     Returns dict with per-layer idx [nq, k], pool [nq, P] (Full with pool),
     out [nq, H, 512], lse [nq, H]."""
@@ -305,9 +306,14 @@ def run_sequence(wl, b, cache=None, queries=None, layers=None, want_out=True):
                     idx_l[t] = topk(S, wl.k, ids=pool[t])
             if mode == "full" and wl.pool_blocks:
                 res["pool"][l] = pool
+        elif mode == "swa":
+            # a sliding-window layer ([P1] §2.3.3: the encoder's first two layers):
+            # no global entry is selected, and the latest indices stay as they are
+            idx_l = np.empty((len(queries), 0), np.int32)
         else:  # reuse: the latest indices, unchanged
             idx_l[:] = prev_idx
-        prev_idx = idx_l
+        if mode != "swa":
+            prev_idx = idx_l
         res["idx"][l] = idx_l
         if need_out:
             win_all = wl.window(l, b)

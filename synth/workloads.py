@@ -14,6 +14,7 @@ Distributions (all seeded by the workload's index, one stream per tensor):
   q[l]     attention queries       bf16  N(0,1)      [B, n_q, H, 512]
   win[l]   window rows of layer l  bf16  N(0,1)      [B, 128, 512]  (l >= 1; layer 0 reads h)
   w_ik     indexer-key projection  f32   N(0,1/512)  [d_I, 512]  (workloads whose keys are projected)
+Layer modes: "full", "reindex", "reuse" (CSA2) and "swa" (window-only attention).
 Element i of a tensor is sample i of its stream, so one sequence's slice is
 drawn on its own.  Nothing in here merges, quantises or scores.
 """
@@ -47,6 +48,7 @@ class Workload:
     chunk: int = 0         # >0: chunked prefill, the last `chunk` positions are queries and are written in the step
     ratio: int = 2         # raw positions per global entry: 2 (encoder merge) or 1 (the decoder's per-position cache)
     ikey_proj: bool = False  # indexer keys projected from the entries (w_ik) instead of drawn rows
+    new_entry: bool = False  # decode: the step itself writes the newest entry (its last `ratio` raw positions)
 
     @property
     def seed(self):
@@ -130,9 +132,73 @@ WORKLOADS = [
              layers=("full",), chunk=8192),
 ]
 
+# per-entry bytes of one cache copy: 256 B latent codes + 32 B scales + 64 B indexer-key codes + 8 B scales
+ENTRY_BYTES = 256 + 32 + 64 + 8
+
+
+@dataclass(frozen=True)
+class Schedule:
+    """The 40 layers of the CED model ("DeepSeek-v4.1 Flash" §2.3.3) as segments
+    of consecutive layers, each over its own global-KV copy:
+
+      encoder copy 0: SWA, SWA, Full, Reuse x5   (the two SWA layers read no global entry)
+      encoder copy 1: Full, Reuse x5
+      encoder copy 2: Full, Reuse x5
+      decoder copy:   Full (+HSI pool), Reuse x3, then 4 x [Reindex, Reuse x3]
+
+    The encoder copies merge 2:1; the decoder copy keeps one entry per raw
+    position and projects its indexer keys from the entries.  In a decode
+    step every copy first receives its newest entry.  Each segment draws from
+    its own seed, so the four copies hold different data."""
+    name: str
+    segments: tuple
+
+    @property
+    def B(self):
+        return self.segments[0].B
+
+    @property
+    def T(self):
+        return self.segments[0].T
+
+    @property
+    def layers(self):
+        return tuple(m for s in self.segments for m in s.layers)
+
+    def cache_bytes_per_token(self):
+        """stored global-KV bytes per raw position, over every copy"""
+        return sum(ENTRY_BYTES / s.ratio for s in self.segments)
+
+
+def ced_schedule(name, B, T, index0=10, pool_blocks=256, pool_block_size=8):
+    common = dict(B=B, T=T, H_I=8, d_I=128, k=512, H=64, new_entry=True)
+    enc_block = ("full",) + ("reuse",) * 5
+    dec = ("full",) + ("reuse",) * 3 + (("reindex",) + ("reuse",) * 3) * 4
+    return Schedule(name, (
+        Workload(index0, name + "/enc0", layers=("swa", "swa") + enc_block, **common),
+        Workload(index0 + 1, name + "/enc1", layers=enc_block, **common),
+        Workload(index0 + 2, name + "/enc2", layers=enc_block, **common),
+        Workload(index0 + 3, name + "/dec", layers=dec, ratio=1, ikey_proj=True, pool_blocks=pool_blocks,
+                 pool_block_size=pool_block_size, **common),
+    ))
+
+
+CED_40L = ced_schedule("decode-128k-b64-40L-ced", B=64, T=131072)
+
 
 def scaled(w, **kw):
     """a copy of workload w with some sizes replaced (small parity cases)"""
     d = dict(w.__dict__)
     d.update(kw)
     return Workload(**d)
+
+
+def scaled_schedule(sched, name=None, **kw):
+    """a copy of a schedule with the same sizes replaced in every segment"""
+    name = name or sched.name
+    segs = []
+    for s in sched.segments:
+        d = dict(kw)
+        d["name"] = name + "/" + s.name.split("/")[-1]
+        segs.append(scaled(s, **d))
+    return Schedule(name, tuple(segs))
