@@ -56,6 +56,8 @@ def workload_of(name):
         return scaled(wl, name=name, T=16384)
     if name == CED_40L.name:
         return CED_40L
+    if name == WORKLOADS[4].name:
+        return WORKLOADS[4]
     if name == "profile-16k-b64-40L-ced":
         return scaled_schedule(CED_40L, name=name, T=16384)
     raise SystemExit("unknown workload %r" % name)
@@ -90,7 +92,9 @@ def config_of(wl):
     segs = segments_of(wl)
     s0 = segs[0]
     cache_bytes = sum(s.B * s.n_entries * 360 for s in segs)
-    if len(segs) == 1:
+    if len(segs) == 1 and s0.chunk:
+        layers = "chunk of %d positions written in the step; 1 Full layer, causal top-%d per query" % (s0.chunk, s0.k)
+    elif len(segs) == 1:
         layers = "1 Full (+HSI pool 256x8), 9 Reindex, 10 Reuse"
     else:
         layers = ("40: SWA x2; 3 x [Full + Reuse x5] over three 2:1 copies; [Full (+HSI pool 256x8) + Reuse x3] "
@@ -347,7 +351,7 @@ def run_ours(args):
         t = torch.tensor([ms], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
-    tokens_per_step = wl.B * world
+    tokens_per_step = wl.B * world * segments_of(wl)[0].n_q
     value = tokens_per_step / (ms * 1e-3)
 
     # per entry point device time (eager launches, events on the launching stream)

@@ -962,7 +962,7 @@ __global__ void k_copy_idx(const int32_t* __restrict__ src, int32_t* __restrict_
 
 // ---------------------------------------------------------------- launchers
 
-constexpr int QUERY_CHUNK = 128;
+constexpr int QUERY_CHUNK = 608;        // queries per scan + select pass (the multi-query tensor scan: one wave)
 
 // workspace of one query slab with item lists of length n:
 // counts (2 ints, padded to 16 B) | ids n | lu n | c2id n | c2key n | bid n | blu n
@@ -1006,6 +1006,10 @@ static size_t ws_bytes(int64_t slabs, int64_t n) {
 }
 
 bool scan_tc_supported(int d_idx, int H, int QB, int pool_blocks, int bs);
+bool scan_mq_tc_supported(int d_idx, int H, int n_q, int pool_blocks);
+cudaError_t launch_scan_mq_tc(const csa2_cache& c, const uint8_t* iq_codes, const uint8_t* iq_scales,
+                              const float* w_head, int n_q, const int64_t* q_pos, int q0, int n_qc, int k, int* counts,
+                              int* cid, float2* clu, int list_len, int* err, cudaStream_t st);
 bool reindex_tc_supported(int d_idx, int H, int pool_len);
 cudaError_t launch_reindex_tc(const csa2_cache& c, const uint8_t* iq_codes, const uint8_t* iq_scales,
                               const float* iq_raw, const float* w_head, int n_q, const int32_t* pool, int pool_len,
@@ -1047,7 +1051,10 @@ cudaError_t launch_indexer_full_t(const csa2_cache& c, const uint8_t* iq_codes, 
         const int n_qc = (n_q - q0) < qchunk ? (n_q - q0) : qchunk;
         e = cudaMemsetAsync(w.counts, 0, (size_t)c.batch * n_qc * 2 * sizeof(int), st);
         if (e != cudaSuccess) return e;
-        if (scan_tc_supported(DI, H, QB, pb_scan, bs_scan)) {
+        if (scan_mq_tc_supported(DI, H, n_q, pb_scan)) {
+            e = launch_scan_mq_tc(c, iq_codes, iq_scales, w_head, n_q, q_pos, q0, n_qc, kf, w.counts, w.ids, w.lu,
+                                  (int)list_len, w.err, st);
+        } else if (scan_tc_supported(DI, H, QB, pb_scan, bs_scan)) {
             e = launch_scan_full_tc(c, iq_codes, iq_scales, w_head, n_q, q_pos, q0, n_qc, H, kf, pb_scan, bs_scan,
                                     w.counts, w.ids, w.lu, w.bid, w.blu, (int)list_len, w.err, st);
         } else {

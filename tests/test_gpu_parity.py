@@ -256,6 +256,65 @@ def test_topk_ties_duplicates_and_zero_keys(csa):
             assert np.array_equal(idx.cpu().numpy()[0, 0], oracle.topk(S, k))
 
 
+# ---------------------------------------------------------------- multi-query scan (chunked prefill)
+
+def _mq_check(csa, kc, ks, lat, iq, w, qpos, k):
+    """n_q queries of one sequence through csa2_indexer_topk (the multi-query
+    tensor scan for n_q >= 4) against the oracle's exact top-k, query by query"""
+    cache = host_cache(csa, [a[None] for a in (lat[0], lat[1], kc, ks)], kc.shape[1] * 2)
+    qc, qs = oracle.quantize_rows(iq)
+    qp = torch.tensor(np.asarray(qpos, np.int64)[None], dtype=torch.int64).cuda()
+    idx, _ = csa.csa2_indexer_topk(cache, torch.from_numpy(qc).cuda(), torch.from_numpy(qs).cuda(),
+                                   torch.from_numpy(w).cuda(), qp, k)
+    got = idx.cpu().numpy()[0]
+    for t, p in enumerate(qpos):
+        S = oracle.index_scores(kc, ks, qc[0, t], qs[0, t], w[0, t], n=oracle.n_elig(p))
+        assert np.array_equal(got[t], oracle.topk(S, k)), (t, p)
+
+
+def test_multi_query_scan_ties_and_mixed_eligibility(csa):
+    """six queries (a ragged group of four), duplicated rows and all-zero keys,
+    zero head weights; eligible ranges above and below 4k (with and without a
+    sampled threshold), one shorter than k and one empty"""
+    n, d = 3000, 128
+    base = synth.normal_f32(41, 1, (n, d))
+    base[1000:1500] = base[0:500]
+    base[2000:2600] = 0.0
+    kc, ks = oracle.quantize_rows(base)
+    lat = oracle.quantize_rows(synth.normal_f32(41, 2, (n, 512)))
+    qpos = [2 * 3000 + 127, 2 * 2900 + 127, 2 * 1500 + 127, 2 * 300 + 127, 100, 2 * 2049 + 127]
+    iq = synth.normal_f32(41, 3, (1, len(qpos), 8, d))
+    w = synth.uniform_f32(41, 4, (1, len(qpos), 8), 0.0, 1.0)
+    for wv in (w, np.zeros_like(w)):
+        for k in (512, 64):
+            _mq_check(csa, kc, ks, lat, iq, wv, qpos, k)
+
+
+def test_multi_query_scan_unrepresentative_sample(csa):
+    """keys whose large scores sit only in the sampled tiles (every eighth
+    128-entry tile of 32,768): the sampled threshold is then too high for
+    every query, fewer than k lower bounds reach it, and each query must be
+    scanned again without one"""
+    n, d = 32768, 128
+    base = synth.normal_f32(42, 1, (n, d)) * np.float32(0.01)
+    tiles = np.arange(n) // 128
+    hot = tiles % 8 == 0
+    base[hot] = np.abs(synth.normal_f32(42, 2, (int(hot.sum()), d))) * np.float32(4.0)
+    kc, ks = oracle.quantize_rows(base)
+    lat = oracle.quantize_rows(synth.normal_f32(42, 3, (n, 512)))
+    qpos = [2 * n + 127, 2 * n + 126, 2 * n + 125, 2 * n + 124, 2 * n + 123]
+    iq = np.abs(synth.normal_f32(42, 4, (1, len(qpos), 8, d)))
+    w = synth.uniform_f32(42, 5, (1, len(qpos), 8), 0.1, 1.0)
+    _mq_check(csa, kc, ks, lat, iq, w, qpos, 512)
+
+
+def test_chunked_prefill_around_the_sampling_switch(csa):
+    """a 64-position chunk whose queries see 2,029 to 2,061 entries: both
+    sides of the 4k = 2,048 point where the scan starts to sample a threshold"""
+    wl = scaled(WORKLOADS[4], T=4250, chunk=64)
+    check_walk(csa, wl, [0])
+
+
 def test_reindex_pool_with_holes_and_reuse(csa):
     n, d = 5000, 128
     lat = oracle.quantize_rows(synth.normal_f32(41, 2, (n, 512)))
