@@ -41,8 +41,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="decode-128k-b64-20L",
                     help="decode-128k-b64-20L (the benchmark); decode-128k-b64-40L-ced (the 40-layer model "
-                         "over four cache copies); profile-16k-b64-20L / profile-16k-b64-40L-ced: the same shapes "
-                         "at 16K context (still larger than L2) for ncu captures")
+                         "over four cache copies); prefill-chunk-8k-after-120k (8,192 queries); "
+                         "profile-16k-b64-20L / profile-16k-b64-40L-ced / profile-prefill-608-after-120k: smaller "
+                         "shapes of the same kernels for ncu captures")
     return ap.parse_args()
 
 
@@ -58,6 +59,8 @@ def workload_of(name):
         return CED_40L
     if name == WORKLOADS[4].name:
         return WORKLOADS[4]
+    if name == "profile-prefill-608-after-120k":
+        return scaled(WORKLOADS[4], name=name, chunk=608, T=122880 + 608)
     if name == "profile-16k-b64-40L-ced":
         return scaled_schedule(CED_40L, name=name, T=16384)
     raise SystemExit("unknown workload %r" % name)
@@ -78,14 +81,17 @@ def dist_env():
         os.environ.get("LOCAL_RANK", "0"))
 
 
-def measured_peak():
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def measured_peak(key="hbm_gbs"):
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(p) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
+        return float(d[key]), "measured"
     except Exception:
-        return FALLBACK_HBM_GBS, "fallback"
+        return (FALLBACK_HBM_GBS if key == "hbm_gbs" else FALLBACK_BF16_TFLOPS), "fallback"
 
 
 def config_of(wl):
@@ -154,6 +160,34 @@ def op_bytes(wl):
         if s.new_entry:
             add("cache_write", s.B * (s.ratio * 1024 + 360))
     return d
+
+
+def op_flops(wl):
+    """the contractions of a chunked prefill, per step: the indexer's q.k over
+    every (query, eligible entry, head) (2 d_I flops each) and the attention's
+    two products per (query, head, key) over the 512-dim latent"""
+    from synth.workloads import WINDOW
+    d = {}
+    for s in segments_of(wl):
+        pos = s.q_positions()
+        n_el = sum(max(0, (int(p) - (WINDOW - 1)) // s.ratio) for p in pos)
+        d["indexer_full"] = d.get("indexer_full", 0) + s.B * n_el * s.H_I * s.d_I * 2
+        d["sparse_attn"] = d.get("sparse_attn", 0) + s.B * s.n_q * s.H * (s.k + WINDOW) * 512 * 4
+    return d
+
+
+def tensor_roofline(wl, per_op, peak, peak_kind):
+    """chunked prefill: the indexer is a contraction of 2 d_I flops per (query,
+    entry, head), run on the tensor cores as fp16 MMAs; against the measured
+    dense bf16 (= fp16) peak.  Its exact-score epilogue runs on the CUDA cores
+    and sets the pace, so the fraction is small by construction"""
+    fl = op_flops(wl)
+    name = "indexer_full" if per_op["indexer_full"]["ms"] >= per_op["sparse_attn"]["ms"] else "sparse_attn"
+    ach = fl[name] / (per_op[name]["ms"] * 1e-3) / 1e12
+    return {"bound": "tensor", "kernel": name, "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
+            "traffic": None, "flops_per_launch": fl[name] // per_op[name]["launches_per_step"],
+            "launch_ms": per_op[name]["per_launch_ms"], "peak_kind": peak_kind,
+            "flops": {k: v for k, v in fl.items()}}
 
 
 def algorithmic_bytes(wl):
@@ -357,7 +391,10 @@ def run_ours(args):
     # per entry point device time (eager launches, events on the launching stream)
     per_op = measure_ops(step, stream, reps=max(3, min(args.steps, 20)))
     peak, peak_kind = measured_peak()
-    roof = roofline(wl, per_op, peak, peak_kind)
+    if segments_of(wl)[0].chunk:
+        roof = tensor_roofline(wl, per_op, *measured_peak("bf16_tflops"))
+    else:
+        roof = roofline(wl, per_op, peak, peak_kind)
 
     # end to end through the public API: every step copies its inputs from pinned host memory to the
     # device, runs, and copies its outputs (every layer's attention output) back.  Two buffer sets

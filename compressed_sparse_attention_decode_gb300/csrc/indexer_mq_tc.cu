@@ -3,14 +3,23 @@
 // indexer over FP4 keys; §2.3.4 a Full layer scores every causally visible entry).
 //
 // One block takes MQ_QB = 4 consecutive queries of the chunk and every entry
-// any of them may read, 128 entries a tile:
-//   A = key codes  [128 entries x 128 dims] FP4 E2M1 (kind::f8f6f4 layout: each
-//       16-value group is 8 packed bytes followed by 8 pad bytes)
-//   B = block-diagonal queries [4 queries x 8 heads x 8 groups = 256 rows x 128]:
-//       row (q, h, g) holds query q's head-h codes of group g, zeros elsewhere
-//   D = A . B^T   M = 128, N = 256, K = 128   (fp32 in TMEM, two accumulators)
-// D[e][(q,h,g)] is an exact group sum, so the epilogue forms every (entry,
-// query) score S~ and its rounding bound E exactly as the single-query scans do.
+// any of them may read, 128 entries a tile.  Per 16-dim group g, one MMA
+// (kind::f16, M = 128 entries, N = 32 (query, head) rows, K = 16):
+//   A = the E2M1 key codes of the tile as fp16 (exact)
+//   B = the query values q = code x scale as fp16 (exact: an E2M1 value times
+//       an E4M3 scale has at most 6 significant bits and lies in [2^-10, 2688])
+//   D_g[e][(q,h)] = sum over the group's 16 dims of k_code q   (fp32 in TMEM)
+// Every product is a multiple of a quarter of the query scale and the sum
+// stays below 2^12 such quarters, so D_g is exact; it is the group sum times
+// the query's group scale.  The epilogue forms every (entry, query) score S~
+// exactly as the single-query scans do (per head, the key-scaled terms t_g
+// added in group order, then the head weights), and a bound E on its rounding
+// error: those scans bound it by fac * sum_h |w_h| sum_g |t_gh|, where fac
+// holds a factor of two to spare; by Cauchy-Schwarz, over the groups and then
+// over the heads, that sum is at most ||w|| ||s_k|| ||x||_F (x the MMA
+// outputs, s_k the key's eight scales), which costs one sum of squares and one
+// square root per pair instead of 64 absolute values.  Two accumulators of
+// 8 x 32 columns.
 //
 // Which entries go on to the exact selection: those whose upper bound S~+E
 // reaches a threshold tau_q that lies below the query's k-th largest lower
@@ -22,10 +31,12 @@
 // and every tile is scored once more with no threshold.  Whatever the data,
 // the forwarded set holds every entry the exact top-k can contain.
 //
-// Warps (384 threads): 0-7 epilogue (warp w: TMEM lane quarter w%4, queries
-// 2(w/4) and 2(w/4)+1), 8 lane 0 issues the MMAs, 9 lane 0 the 1-D bulk copies
-// of each tile's contiguous key rows (four tiles in flight), 10-11 expand the
-// packed codes into the MMA layout.
+// Warps (704 threads): 0-15 epilogue (warp w: TMEM lane quarter w%4, query
+// w/4; four warps per scheduler hide the TMEM and arithmetic latencies), 16-19
+// convert the packed codes to the fp16 MMA layout and decode each entry's key
+// scales once (to fp32 in shared memory, with their norm), 20 lane 0 issues
+// the MMAs, 21 lane 0 the 1-D bulk copies of each tile's contiguous key rows
+// (four tiles in flight).
 #include "indexer_common.cuh"
 #include "umma.cuh"
 
@@ -36,23 +47,63 @@ constexpr int MQ_TILE = 128;
 constexpr int MQ_DI = 128;
 constexpr int MQ_G = MQ_DI / 16;
 constexpr int MQ_H = 8;
-constexpr int MQ_N = MQ_QB * MQ_H * MQ_G;                 // 256
+constexpr int MQ_NQH = MQ_QB * MQ_H;                      // 32: MMA N, one column per (query, head)
 constexpr int MQ_NR = 4;                                  // raw staging slots
 constexpr int MQ_NA = 2;                                  // MMA-layout A slots
 constexpr int MQ_SAMPLE_TILES = 32;
-constexpr int MQ_THREADS = 384;
-constexpr int MQ_EPI = 256;
-constexpr int MQ_XF = 64;
+constexpr int MQ_THREADS = 704;
+constexpr int MQ_EPI = 512;                               // warps 0-15
+constexpr int MQ_W_XF = 16, MQ_W_MMA = 20, MQ_W_COPY = 21;
+constexpr int MQ_XF = 128;                                // warps 16-19
 constexpr uint32_t MQ_RAW_SLOT = MQ_TILE * (MQ_DI / 2) + MQ_TILE * 8;          // codes 8 KB + scales 1 KB
-constexpr uint32_t MQS_B = 0;                                                   // 256 rows x 128 B
-constexpr uint32_t MQS_A = MQ_N * 128;                                          // 2 x 16 KB
-constexpr uint32_t MQS_RAW = MQS_A + MQ_NA * MQ_TILE * 128;                     // 4 x 9 KB
+// fp16 operands, K-major, 128-byte swizzle: slabs of 64 dims (128 B per row)
+constexpr uint32_t MQ_ASLAB = MQ_TILE * 128;                                    // 16 KB
+constexpr uint32_t MQ_BSLAB = MQ_NQH * 128;                                     // 4 KB
+constexpr uint32_t MQS_A = 0;                                                   // 2 slots x 2 slabs
+constexpr uint32_t MQS_B = MQS_A + MQ_NA * 2 * MQ_ASLAB;                        // 2 slabs
+constexpr uint32_t MQS_RAW = MQS_B + 2 * MQ_BSLAB;                              // 4 x 9 KB
 constexpr uint32_t MQS_SAMP = MQS_RAW + MQ_NR * MQ_RAW_SLOT;                    // [QB][32 x 128] lower bounds
-constexpr uint32_t MQS_Q = MQS_SAMP + MQ_QB * MQ_SAMPLE_TILES * MQ_TILE * 4;    // sq [QB][64], w [QB][8]
-constexpr uint32_t MQS_END = MQS_Q + MQ_QB * (MQ_H * MQ_G + MQ_H) * 4;
+constexpr uint32_t MQS_SK = MQS_SAMP + MQ_QB * MQ_SAMPLE_TILES * MQ_TILE * 4;   // per raw slot: [128][8] scales
+constexpr uint32_t MQ_SK_SLOT = MQ_TILE * (MQ_G + 1) * 4;                       //   + [128] norms
+constexpr uint32_t MQS_Q = MQS_SK + MQ_NR * MQ_SK_SLOT;                         // w [QB][8], ||w|| [QB]
+constexpr uint32_t MQS_END = MQS_Q + MQ_QB * (MQ_H + 1) * 4;
 constexpr uint32_t MQS_DYN = MQS_END + 1024;
 
 __device__ __forceinline__ uint32_t mq_swz(uint32_t row, uint32_t unit) { return row * 128 + ((unit ^ (row & 7)) << 4); }
+// eight E2M1 codes (one 32-bit word, low nibble first) to four fp16 pairs, exactly
+__device__ __forceinline__ void mq_e2m1x8(uint32_t w, uint32_t* o) {
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+        " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+        : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+        : "r"(w));
+}
+// (d0, d1) = (a0 b0 + d0, a1 b1 + d1), each rounded once as by fmaf, in one packed instruction
+__device__ __forceinline__ void mq_fma2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+    asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n mov.b64 rd, {%0, %1};\n"
+        " fma.rn.f32x2 rd, ra, rb, rd;\n mov.b64 {%0, %1}, rd;\n}"
+        : "+f"(d0), "+f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+// square root, approximate (relative error far below the 2^-10 the bound sets aside for it)
+__device__ __forceinline__ float mq_sqrt_approx(float x) {
+    float y;
+    asm("sqrt.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// two E4M3 bytes (low byte -> low half) to an fp16 pair, exactly
+__device__ __forceinline__ __half2 mq_e4m3x2_h2(uint32_t two) {
+    uint32_t r;
+    asm("{\n .reg .b16 t;\n cvt.u16.u32 t, %1;\n cvt.rn.f16x2.e4m3x2 %0, t;\n}" : "=r"(r) : "r"(two));
+    return *reinterpret_cast<__half2*>(&r);
+}
+// an E4M3 byte to an fp16 pair holding it twice, exactly
+__device__ __forceinline__ __half2 mq_e4m3_h2(uint32_t byte) {
+    uint32_t r;
+    const uint32_t two = byte | (byte << 8);
+    asm("{\n .reg .b16 t;\n cvt.u16.u32 t, %1;\n cvt.rn.f16x2.e4m3x2 %0, t;\n}" : "=r"(r) : "r"(two));
+    return *reinterpret_cast<__half2*>(&r);
+}
 
 __global__ void __launch_bounds__(MQ_THREADS, 1) k_scan_mq_tc(
     const uint8_t* __restrict__ kc_all, const uint8_t* __restrict__ ks_all, int capacity,
@@ -61,8 +112,8 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) k_scan_mq_tc(
     int* __restrict__ cid, float2* __restrict__ clu, int list_len, int* __restrict__ err, int ratio) {
     pdl_wait();
     extern __shared__ uint8_t dyn[];
-    __shared__ __align__(8) unsigned long long bar_rfull[MQ_NR], bar_rfree[MQ_NR], bar_afull[MQ_NA], bar_afree[MQ_NA],
-        bar_dfull[2], bar_dfree[2];
+    __shared__ __align__(8) unsigned long long bar_rfull[MQ_NR], bar_rfree[MQ_NR], bar_sfull[MQ_NR], bar_afull[MQ_NA],
+        bar_afree[MQ_NA], bar_dfull[2], bar_dfree[2];
     __shared__ uint32_t tmem_base;
     __shared__ int s_nel[MQ_QB], s_cnt[MQ_QB], s_retry[MQ_QB + 1];
     __shared__ uint32_t s_tau[MQ_QB];
@@ -86,6 +137,7 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) k_scan_mq_tc(
         for (int i = 0; i < MQ_NR; ++i) {
             umma::mbar_init(umma::smem_u32(&bar_rfull[i]), 1);
             umma::mbar_init(umma::smem_u32(&bar_rfree[i]), MQ_EPI);
+            umma::mbar_init(umma::smem_u32(&bar_sfull[i]), MQ_XF);
         }
         for (int i = 0; i < MQ_NA; ++i) {
             umma::mbar_init(umma::smem_u32(&bar_afull[i]), MQ_XF);
@@ -97,32 +149,41 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) k_scan_mq_tc(
         }
         umma::fence_mbar_init();
     }
-    // query operand: row n = (q, h, g) -> unit g holds query q's 8 code bytes of head h, group g
-    for (int i = tid; i < MQ_N * 8; i += MQ_THREADS) {
-        const int n = i >> 3, u = i & 7;
-        const int q = n >> 6, h = (n >> 3) & 7, g = n & 7;
+    // query operand: row n = (q, h), the 128 values code x scale of query q's head h in fp16;
+    // unit u (8 dims) of a row comes from one code word and its group's scale
+    for (int i = tid; i < MQ_NQH * 16; i += MQ_THREADS) {
+        const int n = i >> 4, u = i & 15;
+        const int q = n >> 3, h = n & 7;
         uint4 v = make_uint4(0, 0, 0, 0);
-        if (u == g && q < nqb) {
+        if (q < nqb) {
             const int64_t gq = (int64_t)b * n_q + q0 + qa + q;
-            const uint2 c = *reinterpret_cast<const uint2*>(iq_codes + (gq * MQ_H + h) * (MQ_DI / 2) + g * 8);
-            v.x = c.x;
-            v.y = c.y;
+            const uint32_t w = *reinterpret_cast<const uint32_t*>(iq_codes + (gq * MQ_H + h) * (MQ_DI / 2) + u * 4);
+            const __half2 s2 = mq_e4m3_h2(iq_scales[(gq * MQ_H + h) * MQ_G + (u >> 1)]);
+            uint32_t f[4];
+            mq_e2m1x8(w, f);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                __half2 x = __hmul2(*reinterpret_cast<__half2*>(&f[j]), s2);
+                f[j] = *reinterpret_cast<uint32_t*>(&x);
+            }
+            v = make_uint4(f[0], f[1], f[2], f[3]);
         }
-        *reinterpret_cast<uint4*>(sm + MQS_B + mq_swz(n, u)) = v;
+        *reinterpret_cast<uint4*>(sm + MQS_B + (u >> 3) * MQ_BSLAB + mq_swz(n, u & 7)) = v;
     }
-    float* sq = reinterpret_cast<float*>(sm + MQS_Q);               // [QB][64]
-    float* ww = sq + MQ_QB * MQ_H * MQ_G;                            // [QB][8]
-    for (int i = tid; i < MQ_QB * MQ_H * MQ_G; i += MQ_THREADS) {
-        const int q = i >> 6;
-        sq[i] = q < nqb ? e4m3_to_f32(iq_scales[((int64_t)b * n_q + q0 + qa + q) * (MQ_H * MQ_G) + (i & 63)]) : 0.0f;
-    }
+    float* ww = reinterpret_cast<float*>(sm + MQS_Q);                // [QB][8]
+    float* wnorm = ww + MQ_QB * MQ_H;                                // [QB]
     for (int i = tid; i < MQ_QB * MQ_H; i += MQ_THREADS) {
         const int q = i >> 3;
         ww[i] = q < nqb ? w_head[((int64_t)b * n_q + q0 + qa + q) * MQ_H + (i & 7)] : 0.0f;
     }
-    // the pad half of every 16-byte unit of the A slots stays zero
-    for (int i = tid; i < MQ_NA * MQ_TILE * 8; i += MQ_THREADS)
-        reinterpret_cast<uint4*>(sm + MQS_A)[i] = make_uint4(0, 0, 0, 0);
+    if (tid < MQ_QB) {
+        float n2 = 0.0f;
+        for (int h = 0; h < MQ_H; ++h) {
+            const float w = tid < nqb ? w_head[((int64_t)b * n_q + q0 + qa + tid) * MQ_H + h] : 0.0f;
+            n2 = __fmaf_rn(w, w, n2);
+        }
+        wnorm[tid] = __fsqrt_ru(n2);
+    }
     if (warp == 0) umma::tmem_alloc(umma::smem_u32(&tmem_base), 512);
     umma::fence_proxy_async();
     umma::fence_before();
@@ -153,7 +214,7 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) k_scan_mq_tc(
         const int nv = phase == 0 ? n_s0 : n_tiles;
         v_end = v0 + nv;
         auto tile_of = [&](int v) { return phase == 0 ? (v - v0) * stride : v - v0; };
-        if (warp == 9) {
+        if (warp == MQ_W_COPY) {
             // ---- bulk-copy issuer
             if (lane == 0) {
                 for (int v = v0; v < v_end && ok; ++v) {
@@ -173,130 +234,166 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) k_scan_mq_tc(
                                        mb);
                 }
             }
-        } else if (warp >= 10) {
-            // ---- expand packed codes into the data half of each 16-byte unit
-            const int xt = tid - 320;
+        } else if (warp >= MQ_W_XF && warp < MQ_W_XF + MQ_XF / 32) {
+            // ---- codes to fp16: raw chunk c (16 bytes) = row c/4, dims 32(c%4) .. +31
+            const int xt = tid - 32 * MQ_W_XF;
             for (int v = v0; v < v_end && ok; ++v) {
                 const int r = v % MQ_NR, a = v % MQ_NA;
                 ok &= umma::mbar_wait(umma::smem_u32(&bar_rfull[r]), (v / MQ_NR) & 1);
                 if (v >= MQ_NA) ok &= umma::mbar_wait(umma::smem_u32(&bar_afree[a]), ((v / MQ_NA) - 1) & 1);
                 if (!ok) break;
                 const uint4* rw = reinterpret_cast<const uint4*>(sm + MQS_RAW + r * MQ_RAW_SLOT);
-                uint8_t* as = sm + MQS_A + a * (MQ_TILE * 128);
-#pragma unroll 4
+                uint8_t* as = sm + MQS_A + a * (2 * MQ_ASLAB);
+#pragma unroll 2
                 for (int c = xt; c < MQ_TILE * 4; c += MQ_XF) {
-                    const int row = c >> 2, q4 = c & 3;
+                    const int row = c >> 2, j = c & 3;
                     const uint4 x = rw[c];
-                    *reinterpret_cast<uint2*>(as + mq_swz(row, 2 * q4)) = make_uint2(x.x, x.y);
-                    *reinterpret_cast<uint2*>(as + mq_swz(row, 2 * q4 + 1)) = make_uint2(x.z, x.w);
+                    const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
+                    uint8_t* slab = as + (j >> 1) * MQ_ASLAB;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint32_t f[4];
+                        mq_e2m1x8(wd[i], f);
+                        *reinterpret_cast<uint4*>(slab + mq_swz(row, (j & 1) * 4 + i)) = make_uint4(f[0], f[1], f[2], f[3]);
+                    }
                 }
                 umma::fence_proxy_async();
                 umma::mbar_arrive(umma::smem_u32(&bar_afull[a]));
+                // entry xt's eight key scales as fp32 and their norm (rounded up), for the epilogue
+                {
+                    const int e0 = tile_of(v) * MQ_TILE;
+                    const int rows = min(MQ_TILE, nmax - e0);
+                    uint2 skw = make_uint2(0, 0);
+                    if (bulk_scales && xt < (rows & ~1))
+                        skw = *reinterpret_cast<const uint2*>(sm + MQS_RAW + r * MQ_RAW_SLOT + MQ_TILE * (MQ_DI / 2) + xt * 8);
+                    else if (xt < rows)
+                        skw = __ldg(reinterpret_cast<const uint2*>(ks_all + ((int64_t)b * capacity + e0 + xt) * MQ_G));
+                    float sk[MQ_G], n2 = 0.0f;
+#pragma unroll
+                    for (int g = 0; g < MQ_G; g += 2) {
+                        const __half2 h2 = mq_e4m3x2_h2(((g < 4 ? skw.x : skw.y) >> (8 * (g & 3))) & 0xffffu);
+                        sk[g] = __low2float(h2);
+                        sk[g + 1] = __high2float(h2);
+                        n2 = __fmaf_rn(sk[g], sk[g], n2);
+                        n2 = __fmaf_rn(sk[g + 1], sk[g + 1], n2);
+                    }
+                    float* dst = reinterpret_cast<float*>(sm + MQS_SK + r * MQ_SK_SLOT);
+                    reinterpret_cast<float4*>(dst)[2 * xt] = make_float4(sk[0], sk[1], sk[2], sk[3]);
+                    reinterpret_cast<float4*>(dst)[2 * xt + 1] = make_float4(sk[4], sk[5], sk[6], sk[7]);
+                    dst[MQ_TILE * MQ_G + xt] = __fsqrt_ru(n2);
+                    umma::mbar_arrive(umma::smem_u32(&bar_sfull[r]));
+                }
             }
-        } else if (warp == 8) {
+        } else if (warp == MQ_W_MMA) {
             // ---- MMA issuer
             if (lane == 0) {
-                const uint32_t idesc = (1u << 4) | (5u << 7) | (5u << 10) | ((uint32_t)(MQ_N >> 3) << 17) |
-                                       ((uint32_t)(MQ_TILE >> 4) << 24);
+                const uint32_t idesc = umma::idesc_f16(MQ_TILE, MQ_NQH, 0, 0);
                 for (int v = v0; v < v_end && ok; ++v) {
                     const int s = v % MQ_NA, d = v & 1;
                     ok &= umma::mbar_wait(umma::smem_u32(&bar_afull[s]), (v / MQ_NA) & 1);
                     if (v >= 2) ok &= umma::mbar_wait(umma::smem_u32(&bar_dfree[d]), ((v >> 1) - 1) & 1);
                     if (!ok) break;
                     umma::fence_after();
+                    // group g: dims 16g .. 16g+15 = slab g/4, bytes 32(g%4) of every row; its own
+                    // 32 accumulator columns, never accumulated into
 #pragma unroll
-                    for (int ks = 0; ks < MQ_DI / 32; ++ks) {
-                        const uint64_t ad = umma::desc(base + MQS_A + s * (MQ_TILE * 128) + ks * 32, 16, 1024,
+                    for (int g = 0; g < MQ_G; ++g) {
+                        const uint64_t ad = umma::desc(base + MQS_A + s * (2 * MQ_ASLAB) + (g >> 2) * MQ_ASLAB + (g & 3) * 32,
+                                                       16, 1024, umma::LAYOUT_SW128);
+                        const uint64_t bd = umma::desc(base + MQS_B + (g >> 2) * MQ_BSLAB + (g & 3) * 32, 16, 1024,
                                                        umma::LAYOUT_SW128);
-                        const uint64_t bd = umma::desc(base + MQS_B + ks * 32, 16, 1024, umma::LAYOUT_SW128);
-                        asm volatile(
-                            "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-                            " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}" ::"r"(tmem + 256 * d),
-                            "l"(ad), "l"(bd), "r"(idesc), "r"(ks));
+                        umma::mma_f16(tmem + 256 * d + MQ_NQH * g, ad, bd, idesc, 0u);
                     }
                     umma::commit(umma::smem_u32(&bar_dfull[d]));
                     umma::commit(umma::smem_u32(&bar_afree[s]));
                 }
             }
         } else {
-            // ---- epilogue: one entry (TMEM lane) and two queries per thread
-            const int qd = warp & 3, qp = warp >> 2;
+            // ---- epilogue: one entry (TMEM lane) and one query per thread
+            const int qd = warp & 3, qi = warp >> 2;
             const int r = qd * 32 + lane;
-            int cge[2] = {0, 0};
+            const bool live = qi < nqb;                       // warp-uniform
+            const int nel = s_nel[qi];
+            const float* wq = ww + qi * MQ_H;
+            // fac * ||w||, with room for the rounding of the norms and of the sum of squares
+            const float facw = fac * wnorm[qi] * (1.0f + 0x1p-10f);
+            const int64_t slab = (int64_t)b * n_qc + qa + qi;
+            // tau as a float: key 0 (no threshold) is -inf; every other key comes from a finite value
+            const uint32_t tau_key = s_tau[qi];
+            float tau = key_value(tau_key);
+            if (tau_key == 0u || !(tau == tau)) tau = -INFINITY;
+            const bool retry = s_retry[qi] != 0;
+            int cge = 0;
             for (int v = v0; v < v_end && ok; ++v) {
                 const int rs = v % MQ_NR, d = v & 1;
                 const int e0 = tile_of(v) * MQ_TILE;
                 const int rows = min(MQ_TILE, nmax - e0);
                 const int e = e0 + r;
                 ok &= umma::mbar_wait(umma::smem_u32(&bar_dfull[d]), (v >> 1) & 1);
-                // the scales landed with this slot's bulk copy: observe that barrier phase too
-                if (bulk_scales) ok &= umma::mbar_wait(umma::smem_u32(&bar_rfull[rs]), (v / MQ_NR) & 1);
+                ok &= umma::mbar_wait(umma::smem_u32(&bar_sfull[rs]), (v / MQ_NR) & 1);
                 if (!ok) break;
                 umma::fence_after();
-                uint2 skw = make_uint2(0, 0);
-                if (bulk_scales && r < (rows & ~1))
-                    skw = *reinterpret_cast<const uint2*>(sm + MQS_RAW + rs * MQ_RAW_SLOT + MQ_TILE * (MQ_DI / 2) + r * 8);
-                else if (r < rows)
-                    skw = __ldg(reinterpret_cast<const uint2*>(ks_all + ((int64_t)b * capacity + e) * MQ_G));
+                const float* skp = reinterpret_cast<const float*>(sm + MQS_SK + rs * MQ_SK_SLOT);
+                const float4 s0 = reinterpret_cast<const float4*>(skp)[2 * r];
+                const float4 s1 = reinterpret_cast<const float4*>(skp)[2 * r + 1];
+                const float skn = skp[MQ_TILE * MQ_G + r];
+                const float skf[MQ_G] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
                 umma::mbar_arrive(umma::smem_u32(&bar_rfree[rs]));
-                float skf[MQ_G];
+                // columns of group g, query qi: 32 g + 8 qi + h; two groups at a time, in order (each
+                // head's sums still take the groups in order)
+                const uint32_t tb = tmem + ((uint32_t)(qd * 32) << 16) + 256 * d + MQ_H * qi;
+                float dd[MQ_H], nx[MQ_H];
 #pragma unroll
-                for (int g = 0; g < MQ_G; ++g) skf[g] = e4m3_to_f32(((g < 4 ? skw.x : skw.y) >> (8 * (g & 3))) & 255u);
+                for (int h = 0; h < MQ_H; ++h) dd[h] = nx[h] = 0.0f;
 #pragma unroll
-                for (int qq = 0; qq < 2; ++qq) {
-                    const int qi = 2 * qp + qq;
-                    float dv[64];
-                    const uint32_t tb = tmem + ((uint32_t)(qd * 32) << 16) + 256 * d + 64 * qi;
+                for (int part = 0; part < 4; ++part) {
+                    float dv[16];                              // [g][h]: the group sum times the query scale
 #pragma unroll
-                    for (int c = 0; c < 64; c += 16) umma::tmem_ld16(tb + c, dv + c);
+                    for (int g = 0; g < 2; ++g) umma::tmem_ld8(tb + MQ_NQH * (2 * part + g), dv + MQ_H * g);
                     umma::tmem_wait_ld();
-                    if (qq == 1) {
+                    if (part == 3) {
                         umma::fence_before();
                         umma::mbar_arrive(umma::smem_u32(&bar_dfree[d]));
                     }
-                    if (qi >= nqb) continue;                   // warp-uniform
-                    const float* sqq = sq + qi * 64;
-                    const float* wq = ww + qi * MQ_H;
-                    float S = 0.0f, Bs = 0.0f;
+                    if (!live) continue;
 #pragma unroll
-                    for (int h = 0; h < MQ_H; ++h) {
-                        float dd = 0.0f, A = 0.0f;
+                    for (int g = 0; g < 2; ++g) {
+                        const float sk = skf[2 * part + g];
 #pragma unroll
-                        for (int g = 0; g < MQ_G; ++g) {
-                            // dv * sq is exact (a multiple of 1/4 below 2^10 times an E4M3 value), and
-                            // so is its product with the key scale inside the fma: the same sums as
-                            // adding t = dv * (sq * sk) one by one
-                            const float x = dv[h * MQ_G + g] * sqq[h * MQ_G + g];
-                            dd = __fmaf_rn(skf[g], x, dd);
-                            A = __fmaf_rn(skf[g], fabsf(x), A);
+                        for (int h = 0; h < MQ_H; h += 2) {
+                            // x times the key scale is exact inside the fma: the same sums as adding
+                            // t = (group sum) * (sq * sk) one by one; two heads per instruction
+                            const float x0 = dv[g * MQ_H + h], x1 = dv[g * MQ_H + h + 1];
+                            mq_fma2(dd[h], dd[h + 1], sk, sk, x0, x1);
+                            mq_fma2(nx[h], nx[h + 1], x0, x1, x0, x1);
                         }
-                        S = __fmaf_rn(wq[h], fmaxf(dd, 0.0f), S);
-                        Bs = __fmaf_rn(fabsf(wq[h]), A, Bs);
                     }
-                    const float E = Bs * fac;
-                    const float L = S - E, U = S + E;
-                    const bool elig = e < s_nel[qi];
-                    const int64_t slab = (int64_t)b * n_qc + qa + qi;
-                    if (phase == 0) {
-                        samp[qi * (MQ_SAMPLE_TILES * MQ_TILE) + (v - v0) * MQ_TILE + r] = elig ? L : -INFINITY;
-                    } else {
-                        const uint32_t tau = s_tau[qi];
-                        const bool fwd = elig && (phase == 1 ? f32_key(U) >= tau : s_retry[qi] != 0);
-                        if (phase == 1) cge[qq] += (elig && f32_key(L) >= tau) ? 1 : 0;
-                        const int pos = append_slot(fwd, counts + 2 * slab);
-                        if (fwd) {
-                            cid[slab * list_len + pos] = e;
-                            clu[slab * list_len + pos] = make_float2(L, U);
-                        }
+                }
+                if (!live) continue;
+                float S = 0.0f, X2 = 0.0f;
+#pragma unroll
+                for (int h = 0; h < MQ_H; ++h) {
+                    S = __fmaf_rn(wq[h], fmaxf(dd[h], 0.0f), S);
+                    X2 += nx[h];
+                }
+                const float E = facw * skn * mq_sqrt_approx(X2);
+                const float L = S - E, U = S + E;
+                const bool elig = e < nel;
+                if (phase == 0) {
+                    samp[qi * (MQ_SAMPLE_TILES * MQ_TILE) + (v - v0) * MQ_TILE + r] = elig ? L : -INFINITY;
+                } else {
+                    const bool fwd = elig && (phase == 1 ? U >= tau : retry);
+                    if (phase == 1) cge += (elig && L >= tau) ? 1 : 0;
+                    const int pos = append_slot(fwd, counts + 2 * slab);
+                    if (fwd) {
+                        cid[slab * list_len + pos] = e;
+                        clu[slab * list_len + pos] = make_float2(L, U);
                     }
                 }
             }
-            if (phase == 1) {
-#pragma unroll
-                for (int qq = 0; qq < 2; ++qq) {
-                    const int c = __reduce_add_sync(0xffffffffu, cge[qq]);
-                    if (lane == 0 && c) atomicAdd(&s_cnt[2 * qp + qq], c);
-                }
+            if (phase == 1 && live) {
+                const int c = __reduce_add_sync(0xffffffffu, cge);
+                if (lane == 0 && c) atomicAdd(&s_cnt[qi], c);
             }
         }
         __syncthreads();
@@ -356,7 +453,7 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) k_scan_mq_tc(
     }
     // the copies issued are all consumed on the normal path; after a timeout, wait (bounded)
     // for the last ones before the block's shared memory is given up
-    if (warp == 9 && lane == 0 && !ok) {
+    if (warp == MQ_W_COPY && lane == 0 && !ok) {
         for (int v = max(0, v_end - MQ_NR); v < v_end; ++v)
             umma::mbar_wait(umma::smem_u32(&bar_rfull[v % MQ_NR]), (v / MQ_NR) & 1, 1u << 16);
     }
