@@ -25,10 +25,10 @@
 // two TMEM partials that the softmax adds; the first half starts as soon as
 // its dims are expanded), warps 10 and 11 the output MMAs (dim tiles 0-1 and
 // 2-3): one thread issues about one MMA per 55 cycles, two keep the tensor
-// pipe busy.  Warps 12-18 gather rows.  Q (one 64 KB bulk copy, converted in
-// place by warps 0-11) and tile 0, the CTA's window rows (contiguous: one
-// bulk copy), come first; the FP4 tiles follow, their rows prefetched into L2
-// one tile ahead, so the gathers are single L2 round trips.  Everything before
+// pipe busy.  Warps 12-18 gather rows.  Q (loaded and converted to fp16 by
+// warps 0-11, one head per warp at a time) and tile 0, the CTA's window rows
+// (contiguous: one bulk copy), come first; the FP4 tiles follow, their rows
+// prefetched into L2 one tile ahead, so the gathers are single L2 round trips.  Everything before
 // the indices (Q, the window tile, TMEM and barriers) overlaps the preceding
 // kernel of the stream (programmatic launch); only the loaders wait for it.
 //
@@ -125,8 +125,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
     float scale_log2e, float* __restrict__ out, float* __restrict__ lse, int* __restrict__ err) {
     // Programmatic launch: everything up to the indices (Q, the window rows and their tile, the
     // TMEM and barrier set-up) overlaps the preceding kernel; only the loaders wait for it, before
-    // they read idx.  Nothing this kernel writes is read by that kernel.
-    pdl_launch_next();
+    // they read idx, and only then let the successor be scheduled, so that the successor overlaps
+    // this kernel alone.  Nothing this kernel writes is read by that kernel.
     extern __shared__ uint8_t dyn[];
     __shared__ __align__(8) unsigned long long b_lhalf[2], b_lfull[2], b_lfree[2], b_sfull[2], b_sfree[2], b_pfull[2],
         b_odone[2], b_wfull;
@@ -248,6 +248,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
         }
         // the indices are the preceding kernel's output
         pdl_wait();
+        pdl_launch_next();
         int* sidx = reinterpret_cast<int*>(sm + AP_SIDX);
         for (int u = tid - (int)AP_QT; u < n4 * AP_TILE; u += AP_LOADERS) {
             const int s = (2 * (u / AP_TILE) + (int)rank) * AP_TILE + u % AP_TILE;
