@@ -487,6 +487,105 @@ def test_attention_window_clipping_and_empty_selection(csa):
         assert np.abs(lse.cpu().numpy()[0, 0] - rl).max() < 1e-4 * max(1, np.abs(rl).max())
 
 
+# ---------------------------------------------------------------- writes stay inside the outputs
+# (in place of a memory checker, which this pool does not run: guard regions of a known pattern
+# around every output, checked after the call; indices outside the cache are skipped, not read)
+
+def _guarded(shape, dtype, fill, pad=256):
+    n = int(np.prod(shape))
+    buf = torch.full((n + 2 * pad,), fill, dtype=dtype, device="cuda")
+    return buf, buf[pad:pad + n].view(shape), pad
+
+
+def _guards_intact(buf, pad, fill):
+    return bool((buf[:pad] == fill).all()) and bool((buf[-pad:] == fill).all())
+
+
+def test_calls_write_only_their_outputs(csa):
+    """a cache write touches only its entries; the scan, Reindex and attention
+    write nothing past the ends of their index, pool, output and lse buffers"""
+    wl = scaled(WORKLOADS[2], B=2, T=8192, pool_blocks=64)
+    n, d = wl.n_entries, wl.d_I
+    cache = csa.Cache(2, n, d)
+    for t in (cache.lat_codes, cache.lat_scales, cache.ikey_codes, cache.ikey_scales):
+        t.fill_(0xA5)
+    w0, w1 = (torch.from_numpy(w).cuda() for w in wl.merge_weights())
+    e0, ne = 1000, 37
+    h = torch.stack([bf16_t(wl.h(b, 2 * e0, 2 * ne)) for b in range(2)])
+    kr = torch.stack([bf16_t(wl.kraw(b, e0, ne)) for b in range(2)])
+    csa.csa2_cache_write(cache, h, 2 * e0, w0, w1, kr)
+    torch.cuda.synchronize()
+    for t in (cache.lat_codes, cache.lat_scales, cache.ikey_codes, cache.ikey_scales):
+        a = t.cpu().numpy()
+        assert (a[:, :e0] == 0xA5).all() and (a[:, e0 + ne:] == 0xA5).all()
+        assert not (a[:, e0:e0 + ne] == 0xA5).all()
+    # full context for the rest
+    from compressed_sparse_attention_decode_gb300.synthetic import seq_view
+    for b in range(2):
+        csa.csa2_cache_write(seq_view(cache, b), bf16_t(wl.h(b, 0, wl.T))[None], 0, w0, w1,
+                             bf16_t(wl.kraw(b, 0, n))[None])
+    k, P = wl.k, wl.pool_len
+    sent = 0x5A5A5A5A
+    for nq in (1, 6):                         # the decode scan and the multi-query scan
+        qpos = torch.tensor([[wl.T - 1 - i for i in range(nq)]] * 2, dtype=torch.int64).cuda()
+        iq = torch.from_numpy(synth.normal_f32(43, 1, (2, nq, 8, d))).cuda()
+        w = torch.from_numpy(synth.uniform_f32(43, 2, (2, nq, 8), 0.0, 1.0)).cuda()
+        qc, qs = csa.csa2_quantize_fp4(iq)
+        ibuf, idx, pi = _guarded((2, nq, k), torch.int32, sent)
+        pbuf, pool, pp = _guarded((2, nq, P), torch.int32, sent)
+        pb = wl.pool_blocks if nq == 1 else 0
+        csa.csa2_indexer_topk(cache, qc, qs, w, qpos, k, pb, 8, idx_out=idx, pool_out=pool if pb else None)
+        torch.cuda.synchronize()
+        assert _guards_intact(ibuf, pi, sent) and _guards_intact(pbuf, pp, sent)
+        if pb:
+            rbuf, ridx, pr = _guarded((2, nq, k), torch.int32, sent)
+            csa.csa2_reindex_f32(cache, k, iq, w, pool, idx_out=ridx)
+            torch.cuda.synchronize()
+            assert _guards_intact(rbuf, pr, sent)
+        q = torch.stack([bf16_t(wl.q(0, b)) for b in range(2)])[:, :1].repeat(1, nq, 1, 1)
+        first, count = wl.swa_range()
+        win = torch.stack([bf16_t(wl.window(0, b)) for b in range(2)])
+        obuf, out, po = _guarded((2, nq, wl.H, 512), torch.float32, 12345.0)
+        lbuf, lse, pl = _guarded((2, nq, wl.H), torch.float32, 12345.0)
+        csa.csa2_sparse_attn(cache, q.contiguous(), qpos, idx, win, first, out=out, lse=lse)
+        torch.cuda.synchronize()
+        assert _guards_intact(obuf, po, 12345.0) and _guards_intact(lbuf, pl, 12345.0)
+
+
+def test_indices_outside_the_cache_are_skipped(csa):
+    """attention indices and Reindex pool entries at or past the capacity, or
+    negative, are empty slots: the results equal the oracle's with -1 there"""
+    wl = WORKLOADS[0]
+    lc, ls, kc, ks = oracle.sequence_cache(wl, 0)
+    cache = host_cache(csa, [a[None] for a in (lc, ls, kc, ks)], wl.d_I)
+    n = lc.shape[0]
+    q = wl.q(0, 0)
+    win = wl.window(0, 0)
+    p = wl.T - 1
+    idx = np.arange(0, 3 * 64, 3, dtype=np.int32)[None, None].copy()
+    bad = [n, n + 5, 2**31 - 1, -7, -2**31]
+    idx[0, 0, 10:15] = bad
+    out, _ = csa.csa2_sparse_attn(cache, bf16_t(q[None]), torch.tensor([[p]], dtype=torch.int64).cuda(),
+                                  torch.from_numpy(idx).cuda(), bf16_t(win[None]), wl.T - 128)
+    clean = idx[0, 0].copy()
+    clean[10:15] = -1
+    ro, _ = oracle.sparse_attention(q[0], clean, lc, ls, win)
+    assert rel_err_rows(out.cpu().numpy()[0, 0], ro) <= ATTN_TOL
+    # a Reindex pool with entries outside the cache
+    pool = np.full((1, 1, 512), -1, np.int32)
+    pool[0, 0, :400] = np.arange(0, 800, 2)
+    pool[0, 0, 400:405] = bad
+    iq = synth.normal_f32(44, 1, (1, 1, wl.H_I, wl.d_I))
+    w = synth.uniform_f32(44, 2, (1, 1, wl.H_I), 0.0, 1.0)
+    qc, qs = oracle.quantize_rows(iq)
+    got = csa.csa2_reindex(csa.REINDEX, cache, 64, torch.from_numpy(qc).cuda(), torch.from_numpy(qs).cuda(),
+                           torch.from_numpy(w).cuda(), torch.from_numpy(pool).cuda())
+    cp = pool[0, 0].copy()
+    cp[400:405] = -1
+    S = oracle.index_scores(kc, ks, qc[0, 0], qs[0, 0], w[0, 0], ids=cp)
+    assert np.array_equal(got.cpu().numpy()[0, 0], oracle.topk(S, 64, ids=cp))
+
+
 # ---------------------------------------------------------------- full sizes, sampled outputs
 
 def test_decode_128k_20_layers_full_size_sampled(csa):
