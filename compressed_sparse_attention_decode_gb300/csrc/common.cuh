@@ -35,6 +35,20 @@ inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_
     return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
 }
 
+// (d0, d1) = (a0 b0 + d0, a1 b1 + d1), each rounded once as by fmaf, in one packed instruction
+__device__ __forceinline__ void fma2_rn(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+    asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n mov.b64 rd, {%0, %1};\n"
+        " fma.rn.f32x2 rd, ra, rb, rd;\n mov.b64 {%0, %1}, rd;\n}"
+        : "+f"(d0), "+f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+// square root, approximate: callers leave room for its error (far below 2^-20 relative)
+__device__ __forceinline__ float sqrt_approx(float x) {
+    float y;
+    asm("sqrt.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 constexpr int D_LAT = 512;
 constexpr int WINDOW = 128;
 constexpr int MAX_K = 2048;

@@ -78,19 +78,6 @@ __device__ __forceinline__ void mq_e2m1x8(uint32_t w, uint32_t* o) {
         : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
         : "r"(w));
 }
-// (d0, d1) = (a0 b0 + d0, a1 b1 + d1), each rounded once as by fmaf, in one packed instruction
-__device__ __forceinline__ void mq_fma2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
-    asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n mov.b64 rd, {%0, %1};\n"
-        " fma.rn.f32x2 rd, ra, rb, rd;\n mov.b64 {%0, %1}, rd;\n}"
-        : "+f"(d0), "+f"(d1)
-        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
-}
-// square root, approximate (relative error far below the 2^-10 the bound sets aside for it)
-__device__ __forceinline__ float mq_sqrt_approx(float x) {
-    float y;
-    asm("sqrt.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
 // two E4M3 bytes (low byte -> low half) to an fp16 pair, exactly
 __device__ __forceinline__ __half2 mq_e4m3x2_h2(uint32_t two) {
     uint32_t r;
@@ -364,8 +351,8 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) k_scan_mq_tc(
                             // x times the key scale is exact inside the fma: the same sums as adding
                             // t = (group sum) * (sq * sk) one by one; two heads per instruction
                             const float x0 = dv[g * MQ_H + h], x1 = dv[g * MQ_H + h + 1];
-                            mq_fma2(dd[h], dd[h + 1], sk, sk, x0, x1);
-                            mq_fma2(nx[h], nx[h + 1], x0, x1, x0, x1);
+                            fma2_rn(dd[h], dd[h + 1], sk, sk, x0, x1);
+                            fma2_rn(nx[h], nx[h + 1], x0, x1, x0, x1);
                         }
                     }
                 }
@@ -376,7 +363,7 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) k_scan_mq_tc(
                     S = __fmaf_rn(wq[h], fmaxf(dd[h], 0.0f), S);
                     X2 += nx[h];
                 }
-                const float E = facw * skn * mq_sqrt_approx(X2);
+                const float E = facw * skn * sqrt_approx(X2);
                 const float L = S - E, U = S + E;
                 const bool elig = e < nel;
                 if (phase == 0) {

@@ -8,9 +8,14 @@
 //       of group g and zeros elsewhere
 //   D = A . B^T   M = 128, N = H*G, K = d_I   (fp32 in TMEM)
 // D[e][(h,g)] is the exact group sum sum_{i in g} k_i q_hi (multiples of 1/4,
-// |.| <= 576).  The epilogue forms t = D * s_q * s_k (exact) and the same fp32
-// score and error bound as the CUDA-core scan, bit for bit, then the chunk's
-// candidates are forwarded exactly as there.
+// |.| <= 576).  The epilogue forms the exact terms t = D * s_q * s_k and adds
+// them per head (even and odd groups in two chains, two heads' values per
+// packed f32x2 instruction) into the fp32 score S~.  Its rounding error is at
+// most fac * sum_h |w_h| sum_g |t_hg| (fac keeps a factor of two in hand), and
+// by Cauchy-Schwarz, over the groups and then the heads, that sum is at most
+// ||w|| ||s_k|| ||x||_F with x = D * s_q: one sum of squares and one square
+// root per entry instead of 64 absolute values.  The chunk's candidates are
+// then forwarded as in the CUDA-core scan.
 //
 // Warp roles (256 threads): warps 0-3 epilogue (one TMEM lane = one entry),
 // warp 4 lane 0 issues the MMAs, warp 5 lane 0 issues 1-D bulk copies of each
@@ -178,7 +183,10 @@ __global__ void __launch_bounds__(256, 2) k_scan_full_tc(
         }
     } else {
         // ---- epilogue: one entry per thread
-        const float fac = bound_factor(H, ITC_DI);
+        // fac * ||w||, with room for the rounding of the norms and of the sum of squares
+        float w2 = 0.0f;
+        for (int h = 0; h < ITC_H; ++h) w2 = __fmaf_rn(ww[h], ww[h], w2);
+        const float facw = bound_factor(H, ITC_DI) * __fsqrt_ru(w2) * (1.0f + 0x1p-10f);
         for (int t = 0; t < n_tiles; ++t) {
             const int s = t % ITC_NR, d = t & 1;
             ok &= umma::mbar_wait(umma::smem_u32(&bar_dfull[d]), (t >> 1) & 1);
@@ -201,25 +209,29 @@ __global__ void __launch_bounds__(256, 2) k_scan_full_tc(
             else if (r < rows)
                 skw = __ldg(reinterpret_cast<const uint2*>(ks_all + ((int64_t)b * capacity + e0 + r) * ITC_G));
             umma::mbar_arrive(umma::smem_u32(&bar_rfree[s]));
-            float skf[ITC_G];
+            float skf[ITC_G], s2 = 0.0f;
 #pragma unroll
-            for (int g = 0; g < ITC_G; ++g) skf[g] = e4m3_to_f32(((g < 4 ? skw.x : skw.y) >> (8 * (g & 3))) & 255u);
-            float S = 0.0f, B = 0.0f;
+            for (int g = 0; g < ITC_G; ++g) {
+                skf[g] = e4m3_to_f32(((g < 4 ? skw.x : skw.y) >> (8 * (g & 3))) & 255u);
+                s2 = __fmaf_rn(skf[g], skf[g], s2);
+            }
+            float S = 0.0f, X2 = 0.0f;
 #pragma unroll
             for (int h = 0; h < ITC_H; ++h) {
-                {
-                    float dd = 0.0f, A = 0.0f;
+                float de = 0.0f, dod = 0.0f, ne = 0.0f, no = 0.0f;
 #pragma unroll
-                    for (int g = 0; g < ITC_G; ++g) {
-                        const float tv = dv[h * ITC_G + g] * (sq[h * ITC_G + g] * skf[g]);   // exact
-                        dd += tv;
-                        A += fabsf(tv);
-                    }
-                    S = __fmaf_rn(ww[h], fmaxf(dd, 0.0f), S);
-                    B = __fmaf_rn(fabsf(ww[h]), A, B);
+                for (int g = 0; g < ITC_G; g += 2) {
+                    // x = D s_q is exact (a multiple of 1/4 below 2^10 times an E4M3 value), and so is
+                    // its product with the key scale inside the fma
+                    float x0 = 0.0f, x1 = 0.0f;
+                    fma2_rn(x0, x1, dv[h * ITC_G + g], dv[h * ITC_G + g + 1], sq[h * ITC_G + g], sq[h * ITC_G + g + 1]);
+                    fma2_rn(de, dod, skf[g], skf[g + 1], x0, x1);
+                    fma2_rn(ne, no, x0, x1, x0, x1);
                 }
+                S = __fmaf_rn(ww[h], fmaxf(de + dod, 0.0f), S);
+                X2 += ne + no;
             }
-            const float E = B * fac;
+            const float E = facw * sqrt_approx(s2) * sqrt_approx(X2);
             const int i = t * ITC_TILE + r;
             slu[i] = (i < n_loc) ? make_float2(S - E, S + E) : make_float2(-INFINITY, -INFINITY);
         }
