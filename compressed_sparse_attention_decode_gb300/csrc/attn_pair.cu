@@ -170,8 +170,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
     auto sa = [&](const void* x) { return umma::smem_u32(x); };
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
-            umma::mbar_init(sa(&b_lhalf[i]), AP_LOADERS);     // dims 0-255 of the tile expanded
-            umma::mbar_init(sa(&b_lfull[i]), AP_LOADERS);     // all of it
+            umma::mbar_init(sa(&b_lhalf[i]), AP_LOADERS / 32);   // dims 0-255 of the tile expanded (per warp)
+            umma::mbar_init(sa(&b_lfull[i]), AP_LOADERS / 32);   // all of it
             umma::mbar_init(sa(&b_lfree[i]), 2);              // both GEMM2 issuers done with the tile
             umma::mbar_init(sa(&b_sfull[i]), 2);              // both K halves of the scores
             umma::mbar_init(sa(&b_sfree[i]), AP_SMW);
@@ -207,7 +207,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
             // their largest magnitude is tracked on the way, and should it lie outside
             // [2^-10, 2^15) each thread converts its own units again, scaled by 2^-E
             const int lt = tid - (int)AP_QT;
-            ok &= umma::mbar_wait(sa(&b_wfull), 0);
+            ok &= umma::mbar_wait_fast(sa(&b_wfull), 0);
             const uint8_t* R = sm + AP_SL + AP_LBUF;
             uint8_t* L = sm + AP_SL;
             uint32_t mx = 0u;
@@ -242,9 +242,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
             const int ew = ap_range_exp((uint32_t)wexp[1]);
             if (lt == 0) wexp[0] = ew;
             if (ew != 0) convert_window(ew);
+            // each thread orders its own writes for the tensor core, then one arrival per warp
             umma::fence_proxy_async();
-            umma::mbar_arrive(sa(&b_lhalf[0]));
-            umma::mbar_arrive(sa(&b_lfull[0]));
+            __syncwarp();
+            if (lane == 0) {
+                umma::mbar_arrive(sa(&b_lhalf[0]));
+                umma::mbar_arrive(sa(&b_lfull[0]));
+            }
         }
         // the indices are the preceding kernel's output
         pdl_wait();
@@ -363,7 +367,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                     }
                 }
                 prefetch_tile(f + 1);
-                if (t >= 2) ok &= umma::mbar_wait(sa(&b_lfree[buf]), ((t >> 1) - 1) & 1);
+                if (t >= 2) ok &= umma::mbar_wait_fast(sa(&b_lfree[buf]), ((t >> 1) - 1) & 1);
                 // units u < 512 hold dims 0-255 (c < 8): expanded first, so that the first half of
                 // the score MMAs can start while the second half is expanded
 #pragma unroll
@@ -395,12 +399,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                 }
                 if (hf == 0) {
                     umma::fence_proxy_async();
-                    umma::mbar_arrive(sa(&b_lhalf[buf]));
+                    __syncwarp();
+                    if (lane == 0) umma::mbar_arrive(sa(&b_lhalf[buf]));
                 }
                 }
             }
             umma::fence_proxy_async();
-            umma::mbar_arrive(sa(&b_lfull[buf]));
+            __syncwarp();
+            if (lane == 0) umma::mbar_arrive(sa(&b_lfull[buf]));
         }
     } else if (warp == AP_MMAW || warp == AP_MMAW + 1) {
         // ================= GEMM1 issuers: warp 8 + p takes dims 256p .. 256p+255 of S^T of tile t
@@ -413,8 +419,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
             unsigned long long* ready = part == 0 ? b_lhalf : b_lfull;
             for (int t = 0; t < T && ok; ++t) {
                 const int buf = t & 1;
-                ok &= umma::mbar_wait(sa(&ready[buf]), (t >> 1) & 1);
-                if (t >= 2) ok &= umma::mbar_wait(sa(&b_sfree[buf]), ((t >> 1) - 1) & 1);
+                ok &= umma::mbar_wait_fast(sa(&ready[buf]), (t >> 1) & 1);
+                if (t >= 2) ok &= umma::mbar_wait_fast(sa(&b_sfree[buf]), ((t >> 1) - 1) & 1);
                 if (!ok) break;
                 umma::fence_after();
                 const uint64_t ld0 = umma::desc(base + AP_SL + buf * AP_LBUF, 16, 1024, umma::LAYOUT_SW128);
@@ -438,7 +444,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
             const uint32_t id2 = umma::idesc_f16(128, AP_H, 1, 0);
             for (int t = 0; t < T && ok; ++t) {
                 const int buf = t & 1;
-                ok &= umma::mbar_wait(sa(&b_pfull[buf]), (t >> 1) & 1);
+                ok &= umma::mbar_wait_fast(sa(&b_pfull[buf]), (t >> 1) & 1);
                 if (!ok) break;
                 umma::fence_after();
                 const uint64_t la0 = umma::desc(base + AP_SL + buf * AP_LBUF, AP_LSLAB, 1024, umma::LAYOUT_SW128);
@@ -470,7 +476,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
         for (int t = 0; t < T; ++t) {
             const int buf = t & 1;
             float x[16];                     // keys 32*half + par + 2i
-            ok &= umma::mbar_wait(sa(&b_sfull[buf]), (t >> 1) & 1);
+            ok &= umma::mbar_wait_fast(sa(&b_sfull[buf]), (t >> 1) & 1);
             umma::fence_after();
             {
                 float x1[16];
@@ -484,7 +490,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
             __syncwarp();
             if (lane == 0) umma::mbar_arrive(sa(&b_sfree[buf]));
             // key validity was written by the loaders of this buffer: observe their barrier too
-            ok &= umma::mbar_wait(sa(&b_lfull[buf]), (t >> 1) & 1);
+            ok &= umma::mbar_wait_fast(sa(&b_lfull[buf]), (t >> 1) & 1);
             if (t == 0) ew = wexp[0];
             const float mul = t == 0 ? hmul * ap_pow2(ew) : hmul;
             // the window tile's part of O is brought to the common scale before tile 1 adds to it
@@ -528,7 +534,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                     const unsigned any = __ballot_sync(0xffffffffu, of != 1.0f);
                     if (lane == 0) flag[qd] = any != 0;
                 }
-                if (t >= 1) ok &= umma::mbar_wait(sa(&b_odone[(t - 1) & 1]), ((t - 1) >> 1) & 1);   // O settled
+                if (t >= 1) ok &= umma::mbar_wait_fast(sa(&b_odone[(t - 1) & 1]), ((t - 1) >> 1) & 1);   // O settled
                 umma::bar_named(1, AP_SMT);
                 umma::fence_after();
                 if (t >= 1 && (flag[0] | flag[1] | flag[2] | flag[3])) {
@@ -550,11 +556,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                 lsum *= fac[h];
             }
             // the P buffer of this tile was last read by GEMM2 of tile t-2
-            if (t >= 2) ok &= umma::mbar_wait(sa(&b_odone[buf]), ((t >> 1) - 1) & 1);
+            if (t >= 2) ok &= umma::mbar_wait_fast(sa(&b_odone[buf]), ((t >> 1) - 1) & 1);
             const float m = m_run[h];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                x[i] = (x[i] == -INFINITY || m == -INFINITY) ? 0.0f : umma::ex2(x[i] - m);
+                x[i] = (x[i] == -INFINITY || m == -INFINITY) ? 0.0f : umma::ex2_ftz(x[i] - m);
                 lsum += x[i];
             }
             // P^T row h, keys 32*half + 16*par .. +15 from this thread: trade half of the values with
@@ -606,7 +612,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                 lse[gq * AP_H + tid] = Lt > 0.0f ? (mm + log2f(Lt)) * 0.69314718055994531f : -INFINITY;
         }
         umma::bar_named(1, AP_SMT);
-        ok &= umma::mbar_wait(sa(&b_odone[(T - 1) & 1]), ((T - 1) >> 1) & 1);   // every GEMM2 is done
+        ok &= umma::mbar_wait_fast(sa(&b_odone[(T - 1) & 1]), ((T - 1) >> 1) & 1);   // every GEMM2 is done
         umma::fence_after();
         // this CTA's share of its own half of the dims (dim tile 2*rank + half, this warp's
         // lane quarter) is stored; the peer adds its share after the barrier

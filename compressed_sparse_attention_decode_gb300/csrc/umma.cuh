@@ -53,6 +53,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, uint32
     return false;
 }
 
+// one non-blocking test first (cheap when the phase is long complete), then the bounded wait
+__device__ __forceinline__ bool mbar_wait_fast(uint32_t mbar, uint32_t parity, uint32_t max_iter = 1u << 24);
+
 // one non-blocking test of an mbarrier phase
 __device__ __forceinline__ bool mbar_test(uint32_t mbar, uint32_t parity) {
     uint32_t done;
@@ -62,6 +65,10 @@ __device__ __forceinline__ bool mbar_test(uint32_t mbar, uint32_t parity) {
         : "r"(mbar), "r"(parity)
         : "memory");
     return done != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_fast(uint32_t mbar, uint32_t parity, uint32_t max_iter) {
+    return mbar_test(mbar, parity) || mbar_wait(mbar, parity, max_iter);
 }
 
 // wait with cluster-scope acquire (the arrivals come from the peer CTA)
@@ -94,6 +101,11 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_mbar) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_mbar) : "memory");
 }
+// arrive (relaxed, cluster scope) on an mbarrier in another CTA of the cluster: no ordering of
+// this thread's earlier memory operations (use it where those are loads whose values are in hand)
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t remote_mbar) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_mbar) : "memory");
+}
 __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
     asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
                  : "memory");
@@ -112,6 +124,16 @@ __device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t count, bool pre
     uint32_t r;
     asm volatile(
         "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+// named barrier over `count` threads that returns whether all of them passed pred
+__device__ __forceinline__ bool bar_red_and(uint32_t id, uint32_t count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}"
         : "=r"(r)
         : "r"((uint32_t)pred), "r"(id), "r"(count)
         : "memory");
@@ -210,6 +232,12 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// 2^x with results below 2^-126 flushed to zero
+__device__ __forceinline__ float ex2_ftz(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
