@@ -495,6 +495,91 @@ __device__ unsigned int block_kth_bound(Get getkey, int n, int k, bool upper, Ra
     return upper ? band.y : band.x;
 }
 
+// The smallest key of the bucket that holds the k-th largest of the keys, cutting their value range
+// into 2048 buckets of equal width: at least k keys are >= it, so it never exceeds the k-th largest
+// (1 <= k <= the number of finite keys taking part; non-finite keys are ignored).  One pass for the
+// range, one for the histogram (rs.whist: 2048 counters), one block scan from the top bucket down,
+// one pass for the bucket's smallest key.  Used where the caller only filters with it.
+template <typename Get>
+__device__ unsigned int block_kth_floor(Get getkey, int n, int k, RadixSmem& rs) {
+    constexpr int NB = 2048;
+    int* hist = rs.whist;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        rs.kmin32 = ~0u;
+        rs.kmax32 = 0u;
+        rs.ctl[1] = 0;
+    }
+    for (int i = threadIdx.x; i < NB; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    unsigned int mn = ~0u, mx = 0u;
+    for (int t = threadIdx.x; t < n; t += blockDim.x) {
+        unsigned int key;
+        if (getkey(t, key) && isfinite(key_value(key))) {
+            mn = min(mn, key);
+            mx = max(mx, key);
+        }
+    }
+    mn = __reduce_min_sync(0xffffffffu, mn);
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if (lane == 0) {
+        atomicMin(&rs.kmin32, mn);
+        atomicMax(&rs.kmax32, mx);
+    }
+    __syncthreads();
+    const unsigned int lo = rs.kmin32, hi = rs.kmax32;
+    if (lo > hi) return 0u;                                    // no finite key: keep everything
+    const float vlo = key_value(lo);
+    float scale = (float)NB / (key_value(hi) - vlo);
+    if (!(scale > 0.0f && scale < INFINITY)) return lo;         // one value (or too narrow to cut): lo
+    auto bucket_of = [&](unsigned int key) { return min((int)((key_value(key) - vlo) * scale), NB - 1); };
+    for (int t = threadIdx.x; t < n; t += blockDim.x) {
+        unsigned int key;
+        if (getkey(t, key) && key >= lo && key <= hi) atomicAdd(&hist[bucket_of(key)], 1);
+    }
+    if (threadIdx.x == 0) rs.kmax32 = ~0u;                      // (every thread has read hi)
+    __syncthreads();
+    // thread i sums buckets NB-1-PB*i down to NB-PB*(i+1); an inclusive scan over the threads counts
+    // from the top bucket down
+    const int PB = NB / (int)blockDim.x;
+    int c = 0;
+    for (int j = 0; j < PB; ++j) c += hist[NB - 1 - PB * (int)threadIdx.x - j];
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) rs.hist[warp] = incl;
+    __syncthreads();
+    for (int w = 0; w < warp; ++w) incl += rs.hist[w];
+    const int excl = incl - c;
+    if (excl < k && incl >= k) {
+        int cum = excl;
+        for (int j = 0; j < PB; ++j) {
+            const int b = NB - 1 - PB * (int)threadIdx.x - j;
+            cum += hist[b];
+            if (cum >= k) {
+                rs.ctl[1] = b;
+                break;
+            }
+        }
+    }
+    __syncthreads();
+    const int bstar = rs.ctl[1];
+    mn = ~0u;
+    for (int t = threadIdx.x; t < n; t += blockDim.x) {
+        unsigned int key;
+        if (getkey(t, key) && key >= lo && key <= hi && bucket_of(key) == bstar) mn = min(mn, key);
+    }
+    mn = __reduce_min_sync(0xffffffffu, mn);
+    if (lane == 0) atomicMin(&rs.kmax32, mn);
+    __syncthreads();
+    const unsigned int r = rs.kmax32;
+    __syncthreads();                                          // rs is reused by the caller
+    return r == ~0u ? lo : r;
+}
+
 // warp-aggregated append to a list whose counter lives at *ctr (shared or global)
 __device__ __forceinline__ int append_slot(bool flag, int* ctr) {
     const unsigned m = __ballot_sync(0xffffffffu, flag);
@@ -566,12 +651,12 @@ static __device__ void forward_candidates(const float2* lu, int c0, int E, int n
     __syncthreads();
     unsigned int lam = 0u;                        // <= the chunk's k-th largest lower bound
     if (n_loc > k)
-        lam = block_kth_bound(
+        lam = block_kth_floor(
             [&](int i, unsigned int& key) {
                 key = f32_key(lu[i].x);
                 return true;
             },
-            n_loc, k, false, rs);
+            n_loc, k, rs);
     block_append_global(
         n_loc, [&](int i) { return f32_key(lu[i].y) >= lam; },
         [&](int pos, int i) {
@@ -623,12 +708,12 @@ static __device__ void forward_candidates(const float2* lu, int c0, int E, int n
             };
             unsigned int lamb = 0u;
             if (nvalid > pool_blocks - 1)
-                lamb = block_kth_bound(
+                lamb = block_kth_floor(
                     [&](int bl, unsigned int& key) {
                         key = f32_key(blk(bl, false));
                         return g0 + bl != forced;
                     },
-                    nbl, pool_blocks - 1, false, rs);
+                    nbl, pool_blocks - 1, rs);
             block_append_global(
                 nbl, [&](int bl) { return g0 + bl != forced && f32_key(blk(bl, true)) >= lamb; },
                 [&](int pos, int bl) {
