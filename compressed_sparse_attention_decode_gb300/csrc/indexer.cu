@@ -697,7 +697,10 @@ __global__ void __launch_bounds__(RX_THREADS) k_reindex_fused(const int32_t* __r
 // empty) with bounds lu[t]; n is *count (Full: the forwarded candidates) or
 // n_fixed (Reindex: the pool slots, bounds from k_pool_bounds).  Keeps the
 // exact top k; with HSI (Full only) also builds the pool from the forwarded
-// block candidates.
+// block candidates.  dense (the tensor-core decode scan): lu holds the bounds of
+// every eligible entry (item t = entry t), blu those of every HSI block, and ids
+// the per-warp largest lower-bound keys (one per 32 entries) that the thresholds
+// come from.
 template <int DI>
 __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids, const float2* __restrict__ lu,
                                                 const int* __restrict__ counts, int n_fixed, int list_len,
@@ -710,7 +713,7 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
                                                 int32_t* __restrict__ pool_out, const int32_t* __restrict__ bid,
                                                 const float2* __restrict__ blu, int* __restrict__ c2id,
                                                 unsigned long long* __restrict__ c2key, int* __restrict__ h2id,
-                                                unsigned long long* __restrict__ h2key, int ratio) {
+                                                unsigned long long* __restrict__ h2key, int ratio, int dense) {
     pdl_wait();
     pdl_launch_next();
     extern __shared__ int qsm[];
@@ -737,7 +740,20 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
     sm.din = sm.id2 + MAX_K;
     sm.bitmap = reinterpret_cast<unsigned int*>(extra + SEL_DYN_EXTRA);
     const float2* L = lu + slab * list_len;
-    const int n = counts ? counts[2 * slab] : n_fixed;
+    const int n = dense ? n_elig_of(q_pos[gq], capacity, ratio) : (counts ? counts[2 * slab] : n_fixed);
+    // dense: the per-warp maxima of the lower bounds; the kk-th largest of them is a lower bound of
+    // the kk-th largest lower bound (each is a different entry's), when there are at least kk
+    const unsigned int* wmk = reinterpret_cast<const unsigned int*>(ids) + slab * list_len;
+    auto wm_floor = [&](int kk2) -> unsigned int {
+        const int nwm = (n + 31) / 32;
+        if (nwm < kk2) return 0u;
+        return block_kth_bound(
+            [&](int t, unsigned int& key) {
+                key = wmk[t];
+                return true;
+            },
+            nwm, kk2, false, sm.rs);
+    };
     // the pure pool's block has the whole block-candidate lists (the scan forwards no blocks then)
     const int64_t hoff = pure ? 0 : list_len / 2;
     int* cid = split && blockIdx.z == 1 ? h2id + slab * list_len + hoff : c2id + slab * list_len;
@@ -745,6 +761,7 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
     const uint8_t* kc = kc_all + (int64_t)b * capacity * (DI / 2);
     const uint8_t* ks = ks_all + (int64_t)b * capacity * (DI / 16);
     auto entry_of = [&](int t) -> int {
+        if (dense) return t;
         const int j = id[t];
         return (j >= 0 && j < capacity) ? j : -1;
     };
@@ -761,7 +778,7 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
     // has bounds (-inf, -inf), below every real entry, so the selection may
     // count it as long as more than k real entries exist.
     int c = 0;
-    if (counts) {
+    if (counts || dense) {
         c = threadIdx.x == 0 ? n : 0;
     } else {
         for (int t = threadIdx.x; t < n; t += blockDim.x) c += L[t].y != -INFINITY;
@@ -772,7 +789,9 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
     const int n_valid = sm.rs.ctl[3];
     __syncthreads();
     unsigned int lam = 0u;                       // <= the k-th largest lower bound
-    if (n_valid > k) {
+    if (n_valid > k && dense) {
+        lam = wm_floor(k);
+    } else if (n_valid > k) {
         // the lower-bound keys, staged once in shared memory (the bitmap region is idle
         // here) when they fit, so the passes of the selection do not go back to L2
         unsigned int* stage = sm.bitmap;
@@ -790,6 +809,41 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
     }
     if (threadIdx.x == 0) sm.rs.ctl[0] = 0;
     __syncthreads();
+    if (dense) {
+        // the upper bounds of every eligible entry, four per load and 16 loads in flight per thread
+        const float* U = dense_ub(lu, slab, list_len);
+        const int n4 = n >> 2;
+        auto take = [&](int t, float ub, bool in) {    // every lane of the warp calls it
+            const bool f = in && f32_key(ub) >= lam;
+            const int pos = append_slot(f, &sm.rs.ctl[0]);
+            if (f) {
+                cid[pos] = t;
+                if (pos < MAX_K) sm.id[pos] = t;
+            }
+        };
+        for (int base = 0; base < n4; base += 16 * blockDim.x) {
+            float4 v[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const int i4 = base + u * blockDim.x + threadIdx.x;
+                v[u] = i4 < n4 ? __ldg(reinterpret_cast<const float4*>(U) + i4)
+                               : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            }
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const int i4 = base + u * blockDim.x + threadIdx.x, t = 4 * i4;
+                const bool in = i4 < n4;
+                take(t, v[u].x, in);
+                take(t + 1, v[u].y, in);
+                take(t + 2, v[u].z, in);
+                take(t + 3, v[u].w, in);
+            }
+        }
+        for (int base = 4 * n4; base < n; base += blockDim.x) {
+            const int t = base + threadIdx.x;
+            take(t, t < n ? U[t] : -INFINITY, t < n);
+        }
+    } else {
     for (int base = 0; base < n; base += blockDim.x) {
         const int t = base + threadIdx.x;
         const bool f = t < n && f32_key(L[t].y) >= lam && L[t].y != -INFINITY && entry_of(t) >= 0;
@@ -800,13 +854,14 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
             if (pos < MAX_K) sm.id[pos] = j;
         }
     }
+    }
     __syncthreads();
     const int m = sm.rs.ctl[0];
     __syncthreads();
     // ---- 2. exact scores of the candidates, 3. the k best, written in
     // ascending entry order (in shared memory when they fit, the usual case:
     // k plus the few entries whose bounds straddle the threshold)
-    const int id_bound = counts ? n_elig_of(q_pos[gq], capacity, ratio) : capacity;
+    const int id_bound = (counts || dense) ? n_elig_of(q_pos[gq], capacity, ratio) : capacity;
     int kept;
     if (m <= MAX_K) {
         for (int t = threadIdx.x; t < m; t += blockDim.x) {
@@ -847,11 +902,15 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
         __syncthreads();
     } else {
         const int Kp = pool_blocks - 1;      // blocks chosen by score besides the forced newest one
-        const int mb = counts[2 * slab + 1];
+        // dense: every block but the forced newest one, by id; its threshold from the per-warp
+        // maxima (Kp + 1 of them, as one may belong to the forced block)
+        const int mb = dense ? nb - 1 : counts[2 * slab + 1];
         const int32_t* bi = bid + slab * list_len;
         const float2* bl = blu + slab * list_len;
         unsigned int lamb = 0u;
-        if (mb > Kp) {                        // <= the Kp-th largest lower bound
+        if (dense) {
+            if (mb > Kp) lamb = wm_floor(Kp + 1);
+        } else if (mb > Kp) {                 // <= the Kp-th largest lower bound
             unsigned int* stage = sm.bitmap;
             const bool staged = mb <= SEL_BITMAP_BITS / 32;
             if (staged) {
@@ -869,14 +928,23 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
         // bound, with their (upper, lower) bound keys packed in ckey
         if (threadIdx.x == 0) sm.rs.ctl[0] = 0;
         __syncthreads();
-        for (int base = 0; base < mb; base += blockDim.x) {
-            const int t = base + threadIdx.x;
-            const float2 b2 = t < mb ? bl[t] : make_float2(0.0f, 0.0f);
-            const bool f = t < mb && f32_key(b2.y) >= lamb;
-            const int pos = append_slot(f, &sm.rs.ctl[0]);
-            if (f) {
-                cid[pos] = bi[t];
-                ckey[pos] = ((unsigned long long)f32_key(b2.y) << 32) | f32_key(b2.x);
+        for (int base0 = 0; base0 < mb; base0 += 8 * blockDim.x) {
+            float2 b8[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int t = base0 + u * blockDim.x + threadIdx.x;
+                b8[u] = t < mb ? bl[t] : make_float2(0.0f, 0.0f);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int t = base0 + u * blockDim.x + threadIdx.x;
+                const float2 b2 = b8[u];
+                const bool f = t < mb && f32_key(b2.y) >= lamb;
+                const int pos = append_slot(f, &sm.rs.ctl[0]);
+                if (f) {
+                    cid[pos] = dense ? t : bi[t];
+                    ckey[pos] = ((unsigned long long)f32_key(b2.y) << 32) | f32_key(b2.x);
+                }
             }
         }
         __syncthreads();
@@ -1015,9 +1083,9 @@ cudaError_t launch_reindex_tc(const csa2_cache& c, const uint8_t* iq_codes, cons
                               const float* iq_raw, const float* w_head, int n_q, const int32_t* pool, int pool_len,
                               int k, int32_t* idx_out, int* err, cudaStream_t st);
 cudaError_t launch_scan_full_tc(const csa2_cache& c, const uint8_t* iq_codes, const uint8_t* iq_scales,
-                                const float* w_head, int n_q, const int64_t* q_pos, int q0, int n_qc, int H, int k,
-                                int pool_blocks, int bs, int* counts, int* cid, float2* clu, int* bid, float2* blu,
-                                int list_len, int* err, cudaStream_t st);
+                                const float* w_head, int n_q, const int64_t* q_pos, int q0, int n_qc, int H,
+                                int pool_blocks, int bs, unsigned int* wmk, float2* lu, float2* blu, int list_len,
+                                int* err, cudaStream_t st);
 
 size_t indexer_full_ws(int batch, int n_q, int64_t capacity) {
     const int qc = n_q < QUERY_CHUNK ? n_q : QUERY_CHUNK;
@@ -1051,12 +1119,14 @@ cudaError_t launch_indexer_full_t(const csa2_cache& c, const uint8_t* iq_codes, 
         const int n_qc = (n_q - q0) < qchunk ? (n_q - q0) : qchunk;
         e = cudaMemsetAsync(w.counts, 0, (size_t)c.batch * n_qc * 2 * sizeof(int), st);
         if (e != cudaSuccess) return e;
+        int dense = 0;
         if (scan_mq_tc_supported(DI, H, n_q, pb_scan)) {
             e = launch_scan_mq_tc(c, iq_codes, iq_scales, w_head, n_q, q_pos, q0, n_qc, kf, w.counts, w.ids, w.lu,
                                   (int)list_len, w.err, st);
         } else if (scan_tc_supported(DI, H, QB, pb_scan, bs_scan)) {
-            e = launch_scan_full_tc(c, iq_codes, iq_scales, w_head, n_q, q_pos, q0, n_qc, H, kf, pb_scan, bs_scan,
-                                    w.counts, w.ids, w.lu, w.bid, w.blu, (int)list_len, w.err, st);
+            e = launch_scan_full_tc(c, iq_codes, iq_scales, w_head, n_q, q_pos, q0, n_qc, H, pb_scan, bs_scan,
+                                    reinterpret_cast<unsigned int*>(w.ids), w.lu, w.blu, (int)list_len, w.err, st);
+            dense = 1;
         } else {
             dim3 g1((c.capacity + E - 1) / E, (n_qc + QB - 1) / QB, c.batch);
             launch_k(k_scan_full<DI>, g1, 256, smem1, st, c.ikey_codes, c.ikey_scales, c.capacity, iq_codes, iq_scales,
@@ -1076,7 +1146,7 @@ cudaError_t launch_indexer_full_t(const csa2_cache& c, const uint8_t* iq_codes, 
         launch_k(k_select<DI>, g2, 512, smem2, st, w.ids, w.lu, w.counts, 0, (int)list_len, c.ikey_codes, c.ikey_scales,
                                               c.capacity, iq_codes, iq_scales, (const float*)nullptr, w_head, q_pos, n_q, q0, n_qc, H, k,
                                               idx_out, pool_blocks, bs, pool_out, w.bid, w.blu, w.c2id, w.c2key,
-                                              w.bid, reinterpret_cast<unsigned long long*>(w.blu), (int)c.ratio);
+                                              w.bid, reinterpret_cast<unsigned long long*>(w.blu), (int)c.ratio, dense);
         note_launch();
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
@@ -1131,7 +1201,7 @@ cudaError_t launch_reindex_t(const csa2_cache& c, const uint8_t* iq_codes, const
     launch_k(k_select<DI>, g, 512, smem, st, pool, w.lu, nullptr, pool_len, pool_len, c.ikey_codes, c.ikey_scales,
                                        c.capacity, iq_codes, iq_scales, iq_raw, w_head, nullptr, n_q, 0, n_q, H, k, idx_out, 0,
                                        1, nullptr, nullptr, nullptr, w.c2id, w.c2key, (int*)nullptr,
-                                       (unsigned long long*)nullptr, (int)c.ratio);
+                                       (unsigned long long*)nullptr, (int)c.ratio, 0);
     note_launch();
     return cudaGetLastError();
 }

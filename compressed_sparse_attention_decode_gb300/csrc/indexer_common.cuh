@@ -183,6 +183,15 @@ __device__ __forceinline__ int n_elig_of(int64_t p, int capacity, int ratio) {
     return (int)(n < capacity ? n : capacity);
 }
 
+// The dense upper-bound list of query slab `slab` inside its bound list (list_len float2 slots),
+// started on a 16-byte boundary so that it can be read four at a time
+__host__ __device__ inline float* dense_ub(float2* lu, int64_t slab, int list_len) {
+    return reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(lu + slab * list_len) + 15) & ~(uintptr_t)15);
+}
+__host__ __device__ inline const float* dense_ub(const float2* lu, int64_t slab, int list_len) {
+    return dense_ub(const_cast<float2*>(lu), slab, list_len);
+}
+
 __host__ __device__ inline float bound_factor(int H, int DI) { return 2.0f * (float)(2 * H + DI / 16 + 8) * 0x1p-24f; }
 
 // ---------------------------------------------------------------- block-wide radix selection

@@ -8,14 +8,22 @@
 //       of group g and zeros elsewhere
 //   D = A . B^T   M = 128, N = H*G, K = d_I   (fp32 in TMEM)
 // D[e][(h,g)] is the exact group sum sum_{i in g} k_i q_hi (multiples of 1/4,
-// |.| <= 576).  The epilogue forms the exact terms t = D * s_q * s_k and adds
-// them per head (even and odd groups in two chains, two heads' values per
-// packed f32x2 instruction) into the fp32 score S~.  Its rounding error is at
-// most fac * sum_h |w_h| sum_g |t_hg| (fac keeps a factor of two in hand), and
-// by Cauchy-Schwarz, over the groups and then the heads, that sum is at most
-// ||w|| ||s_k|| ||x||_F with x = D * s_q: one sum of squares and one square
-// root per entry instead of 64 absolute values.  The chunk's candidates are
-// then forwarded as in the CUDA-core scan.
+// |.| <= 16 * 6 * 6 = 576).  The epilogue forms the exact terms t = D * s_q * s_k
+// and adds them per head (even and odd groups in two chains, two groups' values
+// per packed f32x2 instruction) into the fp32 score S~.  Its rounding error is
+// at most fac * sum_h |w_h| sum_g |t_hg| (fac keeps a factor of two in hand),
+// and with |D| <= 576 that sum is at most sum_g C_g s_kg, C_g = 576 sum_h |w_h|
+// s_qhg being one number per group for the whole query: the bound costs one
+// fma per group and entry.  It is looser than one built from the entry's own
+// group sums, which only widens the band the selection rescores exactly.
+//
+// The epilogue writes, for every eligible entry, its upper bound S~+E to the
+// query's dense list, and for each warp's 32 entries the largest lower bound
+// S~-E (as an order key); with an HSI pool also each block's bounds (the
+// largest member bounds, over the block's lanes).  The selection kernel takes
+// its thresholds from those per-warp maxima: each is the lower bound of a
+// different entry (and block), so the k-th largest of them never exceeds the
+// k-th largest lower bound.
 //
 // Warp roles (256 threads): warps 0-3 epilogue (one TMEM lane = one entry),
 // warp 4 lane 0 issues the MMAs, warp 5 lane 0 issues 1-D bulk copies of each
@@ -41,22 +49,23 @@ constexpr uint32_t IS_B = 0;                                  // query operand, 
 constexpr uint32_t IS_A = ITC_N * 128;                        // 2 slots x 128 rows x 128 B
 constexpr uint32_t RAW_SLOT = ITC_TILE * (ITC_DI / 2) + ITC_TILE * 8;   // codes 8 KB + scales 1 KB
 constexpr uint32_t IS_RAW = IS_A + ITC_NA * ITC_TILE * 128;   // 4 slots of raw rows
-constexpr uint32_t IS_LU = IS_RAW + ITC_NR * RAW_SLOT;        // 4096 float2
-constexpr uint32_t IS_Q = IS_LU + ITC_E * 8;                  // sq [H][G] floats + w [H]
+constexpr uint32_t IS_Q = IS_RAW + ITC_NR * RAW_SLOT;         // sq [H][G] floats + w [H]
 constexpr uint32_t IS_END = IS_Q + 2048;
 constexpr uint32_t IS_DYN = IS_END + 1024;
 
 __device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t unit) { return row * 128 + ((unit ^ (row & 7)) << 4); }
 
+// The outputs for query slab `slab` (row stride list_len): dense_ub(lu, slab, list_len)[e] = the
+// upper bound of entry e (entries 0 .. n_elig-1), wmk[e / 32] = the largest lower-bound key of
+// entries e .. e+31 (f32_key order; the key of -inf when none is eligible), blu[e / bs] = the bounds
+// of HSI block e / bs (bs a power of two up to 32; bs == 0: no blocks).
 __global__ void __launch_bounds__(256, 2) k_scan_full_tc(
     const uint8_t* __restrict__ kc_all, const uint8_t* __restrict__ ks_all, int capacity,
     const uint8_t* __restrict__ iq_codes, const uint8_t* __restrict__ iq_scales, const float* __restrict__ w_head,
-    const int64_t* __restrict__ q_pos, int n_q, int q0, int n_qc, int H, int k, int pool_blocks, int bs,
-    int* __restrict__ counts, int* __restrict__ cid, float2* __restrict__ clu, int* __restrict__ bid,
-    float2* __restrict__ blu, int list_len, int* __restrict__ err, int ratio) {
+    const int64_t* __restrict__ q_pos, int n_q, int q0, int n_qc, int H, int bs, unsigned int* __restrict__ wmk,
+    float2* __restrict__ lu, float2* __restrict__ blu, int list_len, int* __restrict__ err, int ratio) {
     pdl_wait();             // the selection that follows is let in only as the scan's blocks exit
     extern __shared__ uint8_t dyn[];
-    __shared__ RadixSmem rs;
     __shared__ __align__(8) unsigned long long bar_rfull[ITC_NR], bar_rfree[ITC_NR], bar_afull[ITC_NA], bar_afree[ITC_NA],
         bar_dfull[2], bar_dfree[2];
     __shared__ uint32_t tmem_base;
@@ -68,6 +77,7 @@ __global__ void __launch_bounds__(256, 2) k_scan_full_tc(
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int b = blockIdx.z, ql = blockIdx.y;
     const int64_t gq = (int64_t)b * n_q + q0 + ql;
+    const int64_t slab = (int64_t)b * n_qc + ql;
     const int c0 = blockIdx.x * ITC_E;
     constexpr int N = ITC_N;
 
@@ -116,7 +126,6 @@ __global__ void __launch_bounds__(256, 2) k_scan_full_tc(
     const int n_elig = s_nel;
     const int n_loc = min(max(n_elig - c0, 0), ITC_E);
     const int n_tiles = (n_loc + ITC_TILE - 1) / ITC_TILE;
-    float2* slu = reinterpret_cast<float2*>(sm + IS_LU);
     bool ok = true;
 
     // scale rows are 8 bytes; a bulk copy needs a 16-byte aligned source
@@ -184,9 +193,18 @@ __global__ void __launch_bounds__(256, 2) k_scan_full_tc(
     } else {
         // ---- epilogue: one entry per thread
         // fac * ||w||, with room for the rounding of the norms and of the sum of squares
-        float w2 = 0.0f;
-        for (int h = 0; h < ITC_H; ++h) w2 = __fmaf_rn(ww[h], ww[h], w2);
-        const float facw = bound_factor(H, ITC_DI) * __fsqrt_ru(w2) * (1.0f + 0x1p-10f);
+        // C_g times fac, rounded up, with a factor 1 + 2^-10 for the rounding of the 8-term sum below
+        float cb[ITC_G];
+#pragma unroll
+        for (int g = 0; g < ITC_G; ++g) {
+            float a = 0.0f;
+            for (int h = 0; h < ITC_H; ++h) a = __fmaf_ru(fabsf(ww[h]), sq[h * ITC_G + g], a);
+            cb[g] = __fmul_ru(__fmul_ru(a, 576.0f * bound_factor(H, ITC_DI)), 1.0f + 0x1p-10f);
+        }
+        float* ub_q = dense_ub(lu, slab, list_len);
+        unsigned int* wm_q = wmk + slab * list_len;
+        float2* blu_q = blu + slab * list_len;
+        const int bsh = (bs >= 2 && bs <= 32 && (bs & (bs - 1)) == 0) ? bs : 0;
         for (int t = 0; t < n_tiles; ++t) {
             const int s = t % ITC_NR, d = t & 1;
             ok &= umma::mbar_wait(umma::smem_u32(&bar_dfull[d]), (t >> 1) & 1);
@@ -209,16 +227,16 @@ __global__ void __launch_bounds__(256, 2) k_scan_full_tc(
             else if (r < rows)
                 skw = __ldg(reinterpret_cast<const uint2*>(ks_all + ((int64_t)b * capacity + e0 + r) * ITC_G));
             umma::mbar_arrive(umma::smem_u32(&bar_rfree[s]));
-            float skf[ITC_G], s2 = 0.0f;
+            float skf[ITC_G], E = 0.0f;
 #pragma unroll
             for (int g = 0; g < ITC_G; ++g) {
                 skf[g] = e4m3_to_f32(((g < 4 ? skw.x : skw.y) >> (8 * (g & 3))) & 255u);
-                s2 = __fmaf_rn(skf[g], skf[g], s2);
+                E = __fmaf_rn(cb[g], skf[g], E);
             }
-            float S = 0.0f, X2 = 0.0f;
+            float S = 0.0f;
 #pragma unroll
             for (int h = 0; h < ITC_H; ++h) {
-                float de = 0.0f, dod = 0.0f, ne = 0.0f, no = 0.0f;
+                float de = 0.0f, dod = 0.0f;
 #pragma unroll
                 for (int g = 0; g < ITC_G; g += 2) {
                     // x = D s_q is exact (a multiple of 1/4 below 2^10 times an E4M3 value), and so is
@@ -226,14 +244,23 @@ __global__ void __launch_bounds__(256, 2) k_scan_full_tc(
                     float x0 = 0.0f, x1 = 0.0f;
                     fma2_rn(x0, x1, dv[h * ITC_G + g], dv[h * ITC_G + g + 1], sq[h * ITC_G + g], sq[h * ITC_G + g + 1]);
                     fma2_rn(de, dod, skf[g], skf[g + 1], x0, x1);
-                    fma2_rn(ne, no, x0, x1, x0, x1);
                 }
                 S = __fmaf_rn(ww[h], fmaxf(de + dod, 0.0f), S);
-                X2 += ne + no;
             }
-            const float E = facw * sqrt_approx(s2) * sqrt_approx(X2);
-            const int i = t * ITC_TILE + r;
-            slu[i] = (i < n_loc) ? make_float2(S - E, S + E) : make_float2(-INFINITY, -INFINITY);
+            const int i = t * ITC_TILE + r, e = c0 + i;
+            const bool valid = i < n_loc;
+            const float lb = valid ? S - E : -INFINITY, ub = valid ? S + E : -INFINITY;
+            if (valid) ub_q[e] = ub;
+            const unsigned int km = __reduce_max_sync(0xffffffffu, f32_key(lb));
+            if (lane == 0) wm_q[(c0 + t * ITC_TILE + warp * 32) >> 5] = km;
+            if (bsh) {
+                float lbb = lb, ubb = ub;
+                for (int o2 = 1; o2 < bsh; o2 <<= 1) {
+                    lbb = fmaxf(lbb, __shfl_xor_sync(0xffffffffu, lbb, o2));
+                    ubb = fmaxf(ubb, __shfl_xor_sync(0xffffffffu, ubb, o2));
+                }
+                if ((lane & (bsh - 1)) == 0 && e < n_elig) blu_q[e / bsh] = make_float2(lbb, ubb);
+            }
         }
     }
     if (!ok) atomicExch(err, 1);
@@ -243,24 +270,22 @@ __global__ void __launch_bounds__(256, 2) k_scan_full_tc(
         umma::fence_after();
         umma::tmem_dealloc(tmem, 128);
     }
-    rs.whist = reinterpret_cast<int*>(sm + IS_A);       // the A slots are idle now: 8 warps x 256 counters
-    forward_candidates(slu, c0, ITC_E, n_elig, k, pool_blocks, bs, (int64_t)b * n_qc + ql, list_len, counts, cid, clu,
-                       bid, blu, rs);
 }
 
+// decode (one query per block), d_I = 128, 8 heads; an HSI pool of blocks of a power of two up to 32
 bool scan_tc_supported(int d_idx, int H, int QB, int pool_blocks, int bs) {
-    return d_idx == ITC_DI && QB == 1 && H == ITC_H && (pool_blocks == 0 || ITC_E % bs == 0);
+    return d_idx == ITC_DI && QB == 1 && H == ITC_H && (pool_blocks == 0 || (bs >= 2 && bs <= 32 && (bs & (bs - 1)) == 0));
 }
 
 cudaError_t launch_scan_full_tc(const csa2_cache& c, const uint8_t* iq_codes, const uint8_t* iq_scales,
-                                const float* w_head, int n_q, const int64_t* q_pos, int q0, int n_qc, int H, int k,
-                                int pool_blocks, int bs, int* counts, int* cid, float2* clu, int* bid, float2* blu,
-                                int list_len, int* err, cudaStream_t st) {
+                                const float* w_head, int n_q, const int64_t* q_pos, int q0, int n_qc, int H,
+                                int pool_blocks, int bs, unsigned int* wmk, float2* lu, float2* blu, int list_len,
+                                int* err, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(k_scan_full_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)IS_DYN);
     if (e != cudaSuccess) return e;
     dim3 grid((c.capacity + ITC_E - 1) / ITC_E, n_qc, c.batch);
     launch_k(k_scan_full_tc, grid, 256, IS_DYN, st, c.ikey_codes, c.ikey_scales, c.capacity, iq_codes, iq_scales, w_head,
-                                              q_pos, n_q, q0, n_qc, H, k, pool_blocks, bs, counts, cid, clu, bid, blu,
+                                              q_pos, n_q, q0, n_qc, H, pool_blocks > 0 ? bs : 0, wmk, lu, blu,
                                               list_len, err, (int)c.ratio);
     note_launch();
     return cudaGetLastError();
