@@ -27,7 +27,7 @@
 //
 // Warp roles (256 threads): warps 0-3 epilogue (one TMEM lane = one entry),
 // warp 4 lane 0 issues the MMAs, warp 5 lane 0 issues 1-D bulk copies of each
-// tile's contiguous key rows (8 KB codes + 1 KB scales, four tiles in flight),
+// tile's contiguous key rows (8 KB codes + 1 KB scales, three tiles in flight),
 // warps 6-7 expand the packed codes into the padded MMA layout.  Two A slots
 // and two TMEM accumulators keep copies, MMAs and epilogues overlapped.
 #include "indexer_common.cuh"
@@ -37,7 +37,7 @@ namespace csa2 {
 
 constexpr int ITC_E = 4096;                 // entries per block
 constexpr int ITC_TILE = 128;
-constexpr int ITC_NR = 4;                   // raw staging slots (bulk-copy depth)
+constexpr int ITC_NR = 3;                   // raw staging slots (bulk-copy depth)
 constexpr int ITC_NA = 2;                   // MMA-layout A slots
 constexpr int ITC_DI = 128;
 constexpr int ITC_G = ITC_DI / 16;
@@ -59,7 +59,7 @@ __device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t unit) { return
 // upper bound of entry e (entries 0 .. n_elig-1), wmk[e / 32] = the largest lower-bound key of
 // entries e .. e+31 (f32_key order; the key of -inf when none is eligible), blu[e / bs] = the bounds
 // of HSI block e / bs (bs a power of two up to 32; bs == 0: no blocks).
-__global__ void __launch_bounds__(256, 2) k_scan_full_tc(
+__global__ void __launch_bounds__(256, 3) k_scan_full_tc(
     const uint8_t* __restrict__ kc_all, const uint8_t* __restrict__ ks_all, int capacity,
     const uint8_t* __restrict__ iq_codes, const uint8_t* __restrict__ iq_scales, const float* __restrict__ w_head,
     const int64_t* __restrict__ q_pos, int n_q, int q0, int n_qc, int H, int bs, unsigned int* __restrict__ wmk,
@@ -207,15 +207,6 @@ __global__ void __launch_bounds__(256, 2) k_scan_full_tc(
         const int bsh = (bs >= 2 && bs <= 32 && (bs & (bs - 1)) == 0) ? bs : 0;
         for (int t = 0; t < n_tiles; ++t) {
             const int s = t % ITC_NR, d = t & 1;
-            ok &= umma::mbar_wait(umma::smem_u32(&bar_dfull[d]), (t >> 1) & 1);
-            umma::fence_after();
-            float dv[64];
-            const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16) + 64 * d;
-#pragma unroll
-            for (int c = 0; c < N; c += 16) umma::tmem_ld16(lane_base + c, dv + c);
-            umma::tmem_wait_ld();
-            umma::fence_before();
-            umma::mbar_arrive(umma::smem_u32(&bar_dfree[d]));
             const int r = tid;                          // row of the tile = TMEM lane
             const int e0 = c0 + t * ITC_TILE;
             const int rows = min(ITC_TILE, n_elig - e0);
@@ -233,19 +224,36 @@ __global__ void __launch_bounds__(256, 2) k_scan_full_tc(
                 skf[g] = e4m3_to_f32(((g < 4 ? skw.x : skw.y) >> (8 * (g & 3))) & 255u);
                 E = __fmaf_rn(cb[g], skf[g], E);
             }
+            // the group sums in two halves of four heads (32 columns), to keep registers for three
+            // blocks per SM
+            ok &= umma::mbar_wait(umma::smem_u32(&bar_dfull[d]), (t >> 1) & 1);
+            umma::fence_after();
+            const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16) + 64 * d;
             float S = 0.0f;
 #pragma unroll
-            for (int h = 0; h < ITC_H; ++h) {
-                float de = 0.0f, dod = 0.0f;
-#pragma unroll
-                for (int g = 0; g < ITC_G; g += 2) {
-                    // x = D s_q is exact (a multiple of 1/4 below 2^10 times an E4M3 value), and so is
-                    // its product with the key scale inside the fma
-                    float x0 = 0.0f, x1 = 0.0f;
-                    fma2_rn(x0, x1, dv[h * ITC_G + g], dv[h * ITC_G + g + 1], sq[h * ITC_G + g], sq[h * ITC_G + g + 1]);
-                    fma2_rn(de, dod, skf[g], skf[g + 1], x0, x1);
+            for (int hp = 0; hp < 2; ++hp) {
+                float dv[32];
+                umma::tmem_ld16(lane_base + 32 * hp, dv);
+                umma::tmem_ld16(lane_base + 32 * hp + 16, dv + 16);
+                umma::tmem_wait_ld();
+                if (hp == 1) {
+                    umma::fence_before();
+                    umma::mbar_arrive(umma::smem_u32(&bar_dfree[d]));
                 }
-                S = __fmaf_rn(ww[h], fmaxf(de + dod, 0.0f), S);
+#pragma unroll
+                for (int hh = 0; hh < 4; ++hh) {
+                    const int h = 4 * hp + hh;
+                    float de = 0.0f, dod = 0.0f;
+#pragma unroll
+                    for (int g = 0; g < ITC_G; g += 2) {
+                        // x = D s_q is exact (a multiple of 1/4 below 2^10 times an E4M3 value), and so is
+                        // its product with the key scale inside the fma
+                        float x0 = 0.0f, x1 = 0.0f;
+                        fma2_rn(x0, x1, dv[hh * ITC_G + g], dv[hh * ITC_G + g + 1], sq[h * ITC_G + g], sq[h * ITC_G + g + 1]);
+                        fma2_rn(de, dod, skf[g], skf[g + 1], x0, x1);
+                    }
+                    S = __fmaf_rn(ww[h], fmaxf(de + dod, 0.0f), S);
+                }
             }
             const int i = t * ITC_TILE + r, e = c0 + i;
             const bool valid = i < n_loc;
