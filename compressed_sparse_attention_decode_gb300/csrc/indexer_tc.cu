@@ -25,11 +25,13 @@
 // different entry (and block), so the k-th largest of them never exceeds the
 // k-th largest lower bound.
 //
-// Warp roles (256 threads): warps 0-3 epilogue (one TMEM lane = one entry),
-// warp 4 lane 0 issues the MMAs, warp 5 lane 0 issues 1-D bulk copies of each
-// tile's contiguous key rows (8 KB codes + 1 KB scales, three tiles in flight),
-// warps 6-7 expand the packed codes into the padded MMA layout.  Two A slots
-// and two TMEM accumulators keep copies, MMAs and epilogues overlapped.
+// Warp roles (384 threads): warps 0-7 epilogue in two groups of four that take
+// alternate tiles, each with its own TMEM accumulator (in a group one TMEM lane
+// = one entry); warp 8 lane 0 issues the MMAs, warp 9 lane 0 issues 1-D bulk
+// copies of each tile's contiguous key rows (8 KB codes + 1 KB scales, four
+// tiles in flight), warps 10-11 expand the packed codes into the padded MMA
+// layout.  Two A slots and two TMEM accumulators keep copies, MMAs and
+// epilogues overlapped.
 #include "indexer_common.cuh"
 #include "umma.cuh"
 
@@ -37,11 +39,13 @@ namespace csa2 {
 
 constexpr int ITC_E = 4096;                 // entries per block
 constexpr int ITC_TILE = 128;
-constexpr int ITC_NR = 3;                   // raw staging slots (bulk-copy depth)
+constexpr int ITC_NR = 4;                   // raw staging slots (bulk-copy depth)
 constexpr int ITC_NA = 2;                   // MMA-layout A slots
 constexpr int ITC_DI = 128;
 constexpr int ITC_G = ITC_DI / 16;
-constexpr int ITC_XFORM = 64;               // warps 6-7 expand raw codes into the MMA layout
+constexpr int ITC_THREADS = 384;
+constexpr int ITC_MMAW = 8, ITC_COPYW = 9, ITC_XW0 = 10;   // warps 0-7 epilogue (two groups of four)
+constexpr int ITC_XFORM = 64;               // warps 10-11 expand raw codes into the MMA layout
 // shared memory (from the 1024-aligned base)
 constexpr int ITC_H = 8;                    // indexer heads taken by this kernel
 constexpr int ITC_N = ITC_H * ITC_G;        // MMA N: one column per (head, group)
@@ -59,7 +63,7 @@ __device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t unit) { return
 // upper bound of entry e (entries 0 .. n_elig-1), wmk[e / 32] = the largest lower-bound key of
 // entries e .. e+31 (f32_key order; the key of -inf when none is eligible), blu[e / bs] = the bounds
 // of HSI block e / bs (bs a power of two up to 32; bs == 0: no blocks).
-__global__ void __launch_bounds__(256, 3) k_scan_full_tc(
+__global__ void __launch_bounds__(384, 2) k_scan_full_tc(
     const uint8_t* __restrict__ kc_all, const uint8_t* __restrict__ ks_all, int capacity,
     const uint8_t* __restrict__ iq_codes, const uint8_t* __restrict__ iq_scales, const float* __restrict__ w_head,
     const int64_t* __restrict__ q_pos, int n_q, int q0, int n_qc, int H, int bs, unsigned int* __restrict__ wmk,
@@ -131,7 +135,7 @@ __global__ void __launch_bounds__(256, 3) k_scan_full_tc(
     // scale rows are 8 bytes; a bulk copy needs a 16-byte aligned source
     const uint8_t* ks_seq = ks_all + ((int64_t)b * capacity + c0) * ITC_G;
     const bool bulk_scales = ((reinterpret_cast<uintptr_t>(ks_seq) & 15u) == 0);
-    if (warp == 5) {
+    if (warp == ITC_COPYW) {
         // ---- bulk-copy issuer
         if (lane == 0) {
             for (int t = 0; t < n_tiles; ++t) {
@@ -148,9 +152,9 @@ __global__ void __launch_bounds__(256, 3) k_scan_full_tc(
                 if (sbytes) umma::bulk_g2s(dst + ITC_TILE * (ITC_DI / 2), ks_all + ((int64_t)b * capacity + e0) * ITC_G, sbytes, mb);
             }
         }
-    } else if (warp >= 6) {
+    } else if (warp >= ITC_XW0) {
         // ---- expand packed codes (8 bytes per 16-value group) into the data half of each 16-byte unit
-        const int xt = tid - 192;
+        const int xt = tid - ITC_XW0 * 32;
         for (int t = 0; t < n_tiles; ++t) {
             const int r = t % ITC_NR, a = t % ITC_NA;
             ok &= umma::mbar_wait(umma::smem_u32(&bar_rfull[r]), (t / ITC_NR) & 1);
@@ -167,7 +171,7 @@ __global__ void __launch_bounds__(256, 3) k_scan_full_tc(
             umma::fence_proxy_async();
             umma::mbar_arrive(umma::smem_u32(&bar_afull[a]));
         }
-    } else if (warp == 4) {
+    } else if (warp == ITC_MMAW) {
         // ---- MMA issuer
         if (lane == 0) {
             const uint32_t idesc = (1u << 4) | (5u << 7) | (5u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
@@ -205,9 +209,11 @@ __global__ void __launch_bounds__(256, 3) k_scan_full_tc(
         unsigned int* wm_q = wmk + slab * list_len;
         float2* blu_q = blu + slab * list_len;
         const int bsh = (bs >= 2 && bs <= 32 && (bs & (bs - 1)) == 0) ? bs : 0;
-        for (int t = 0; t < n_tiles; ++t) {
+        // warp w takes the tiles t with t % 2 == w / 4 (TMEM accumulator t % 2), lane quarter w % 4
+        const int eg = warp >> 2, wq = warp & 3;
+        for (int t = eg; t < n_tiles; t += 2) {
             const int s = t % ITC_NR, d = t & 1;
-            const int r = tid;                          // row of the tile = TMEM lane
+            const int r = wq * 32 + lane;               // row of the tile = TMEM lane
             const int e0 = c0 + t * ITC_TILE;
             const int rows = min(ITC_TILE, n_elig - e0);
             uint2 skw = make_uint2(0, 0);
@@ -217,18 +223,19 @@ __global__ void __launch_bounds__(256, 3) k_scan_full_tc(
                 skw = *reinterpret_cast<const uint2*>(sm + IS_RAW + s * RAW_SLOT + ITC_TILE * (ITC_DI / 2) + r * 8);
             else if (r < rows)
                 skw = __ldg(reinterpret_cast<const uint2*>(ks_all + ((int64_t)b * capacity + e0 + r) * ITC_G));
-            umma::mbar_arrive(umma::smem_u32(&bar_rfree[s]));
             float skf[ITC_G], E = 0.0f;
 #pragma unroll
             for (int g = 0; g < ITC_G; ++g) {
                 skf[g] = e4m3_to_f32(((g < 4 ? skw.x : skw.y) >> (8 * (g & 3))) & 255u);
                 E = __fmaf_rn(cb[g], skf[g], E);
             }
-            // the group sums in two halves of four heads (32 columns), to keep registers for three
-            // blocks per SM
+            // the group sums in two halves of four heads (32 columns), to keep registers low
             ok &= umma::mbar_wait(umma::smem_u32(&bar_dfull[d]), (t >> 1) & 1);
             umma::fence_after();
-            const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16) + 64 * d;
+            // the raw slot may be refilled only now: the tile's MMAs were issued, so the expanding warps
+            // are done reading its codes (and this thread has its scales)
+            umma::mbar_arrive(umma::smem_u32(&bar_rfree[s]));
+            const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16) + 64 * d;
             float S = 0.0f;
 #pragma unroll
             for (int hp = 0; hp < 2; ++hp) {
@@ -260,7 +267,7 @@ __global__ void __launch_bounds__(256, 3) k_scan_full_tc(
             const float lb = valid ? S - E : -INFINITY, ub = valid ? S + E : -INFINITY;
             if (valid) ub_q[e] = ub;
             const unsigned int km = __reduce_max_sync(0xffffffffu, f32_key(lb));
-            if (lane == 0) wm_q[(c0 + t * ITC_TILE + warp * 32) >> 5] = km;
+            if (lane == 0) wm_q[(c0 + t * ITC_TILE + wq * 32) >> 5] = km;
             if (bsh) {
                 float lbb = lb, ubb = ub;
                 for (int o2 = 1; o2 < bsh; o2 <<= 1) {
@@ -292,7 +299,7 @@ cudaError_t launch_scan_full_tc(const csa2_cache& c, const uint8_t* iq_codes, co
     cudaError_t e = cudaFuncSetAttribute(k_scan_full_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)IS_DYN);
     if (e != cudaSuccess) return e;
     dim3 grid((c.capacity + ITC_E - 1) / ITC_E, n_qc, c.batch);
-    launch_k(k_scan_full_tc, grid, 256, IS_DYN, st, c.ikey_codes, c.ikey_scales, c.capacity, iq_codes, iq_scales, w_head,
+    launch_k(k_scan_full_tc, grid, ITC_THREADS, IS_DYN, st, c.ikey_codes, c.ikey_scales, c.capacity, iq_codes, iq_scales, w_head,
                                               q_pos, n_q, q0, n_qc, H, pool_blocks > 0 ? bs : 0, wmk, lu, blu,
                                               list_len, err, (int)c.ratio);
     note_launch();
