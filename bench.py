@@ -42,7 +42,8 @@ def parse():
     ap.add_argument("--workload", default="decode-128k-b64-20L",
                     help="decode-128k-b64-20L (the benchmark); decode-128k-b64-40L-ced (the 40-layer model "
                          "over four cache copies); prefill-chunk-8k-after-120k (8,192 queries); "
-                         "profile-16k-b64-20L / profile-16k-b64-40L-ced / profile-prefill-608-after-120k: smaller "
+                         "profile-16k-b64-20L / profile-128k-b16-20L / profile-16k-b64-40L-ced / "
+                         "profile-prefill-608-after-120k: smaller "
                          "shapes of the same kernels for ncu captures")
     return ap.parse_args()
 
@@ -55,6 +56,8 @@ def workload_of(name):
         return wl
     if name == "profile-16k-b64-20L":
         return scaled(wl, name=name, T=16384)
+    if name == "profile-128k-b16-20L":
+        return scaled(wl, name=name, B=16)
     if name == CED_40L.name:
         return CED_40L
     if name == WORKLOADS[4].name:

@@ -160,7 +160,7 @@ __device__ int block_exclusive_scan(int v, int* total, int* ws) {
 // exactly by counting.  The float images are computed once into key2 (viewed
 // as 32-bit words; 0 for an empty slot, which the band skips as non-finite).
 // Returns the number flagged, min(k, entries).
-__device__ int select_best_set(int n, int k, SelectSmem& sm) {
+__device__ __noinline__ int select_best_set(int n, int k, SelectSmem& sm) {
     int* flag = sm.id2;
     unsigned int* fkey = reinterpret_cast<unsigned int*>(sm.key2);
     const int lane = threadIdx.x & 31;
@@ -401,7 +401,7 @@ __device__ void sort_kept(int n, bool by_key, SelectSmem& sm) {
 // words, with a block barrier since.
 // Through a bitmap of id_bound bits and a block prefix sum over its words when
 // that fits SEL_BITMAP_BITS, else by sort_kept.  dst must not alias ids.
-__device__ int ascending_ids(const int* ids, const int* flags, int n, int id_bound, int* dst, SelectSmem& sm,
+__device__ __noinline__ int ascending_ids(const int* ids, const int* flags, int n, int id_bound, int* dst, SelectSmem& sm,
                              bool bitmap_clear = false) {
     int total;
     if (id_bound <= SEL_BITMAP_BITS) {
@@ -456,7 +456,7 @@ __device__ int ascending_ids(const int* ids, const int* flags, int n, int id_bou
 // in sm.key/sm.id[0..kept).  When every candidate fits in shared memory (the
 // usual case: k plus the few entries whose bounds straddle the threshold) one
 // bitonic sort does it; otherwise a radix selection cuts them to k first.
-__device__ int best_sorted(const int* cid, const unsigned long long* ckey, int m, int k, SelectSmem& sm) {
+__device__ __noinline__ int best_sorted(const int* cid, const unsigned long long* ckey, int m, int k, SelectSmem& sm) {
     if (m <= MAX_K) {
         for (int t = threadIdx.x; t < m; t += blockDim.x) {
             sm.key[t] = ckey[t];
@@ -697,10 +697,10 @@ __global__ void __launch_bounds__(RX_THREADS) k_reindex_fused(const int32_t* __r
 // empty) with bounds lu[t]; n is *count (Full: the forwarded candidates) or
 // n_fixed (Reindex: the pool slots, bounds from k_pool_bounds).  Keeps the
 // exact top k; with HSI (Full only) also builds the pool from the forwarded
-// block candidates.  dense (the tensor-core decode scan): lu holds the bounds of
-// every eligible entry (item t = entry t), blu those of every HSI block, and ids
-// the per-warp largest lower-bound keys (one per 32 entries) that the thresholds
-// come from.
+// block candidates.  dense (the tensor-core decode scan): lu holds the upper
+// bound of every eligible entry (item t = entry t), blu the bounds of every HSI
+// block, and ids the largest lower-bound key of each aligned group of 8 entries,
+// which the thresholds come from.
 template <int DI>
 __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids, const float2* __restrict__ lu,
                                                 const int* __restrict__ counts, int n_fixed, int list_len,
@@ -741,18 +741,19 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
     sm.bitmap = reinterpret_cast<unsigned int*>(extra + SEL_DYN_EXTRA);
     const float2* L = lu + slab * list_len;
     const int n = dense ? n_elig_of(q_pos[gq], capacity, ratio) : (counts ? counts[2 * slab] : n_fixed);
-    // dense: the per-warp maxima of the lower bounds; the kk-th largest of them is a lower bound of
-    // the kk-th largest lower bound (each is a different entry's), when there are at least kk
+    // dense: the group maxima of the lower bounds (8 entries a group); the kk-th largest of them is
+    // a lower bound of the kk-th largest lower bound (each is a different entry's), when there are at
+    // least kk groups
     const unsigned int* wmk = reinterpret_cast<const unsigned int*>(ids) + slab * list_len;
+    // (taken over groups of 32 or 16 entries, maxima of 4 or 2 group maxima, while those are enough:
+    // fewer keys for the band search)
     auto wm_floor = [&](int kk2) -> unsigned int {
-        const int nwm = (n + 31) / 32;
+        const int n8 = n / 8;                     // whole groups of 8 (their maxima are all written)
+        for (int st = 4; st >= 1; st >>= 1)
+            if (n8 / st >= kk2) return block_kth_bound_arr(wmk, nullptr, n8 / st, kk2, false, sm.rs, st);
+        const int nwm = (n + 7) / 8;
         if (nwm < kk2) return 0u;
-        return block_kth_bound(
-            [&](int t, unsigned int& key) {
-                key = wmk[t];
-                return true;
-            },
-            nwm, kk2, false, sm.rs);
+        return block_kth_bound_arr(wmk, nullptr, nwm, kk2, false, sm.rs);
     };
     // the pure pool's block has the whole block-candidate lists (the scan forwards no blocks then)
     const int64_t hoff = pure ? 0 : list_len / 2;
@@ -800,12 +801,15 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
             for (int t = threadIdx.x; t < n; t += blockDim.x) stage[t] = f32_key(L[t].x);
             __syncthreads();
         }
-        lam = block_kth_bound(
-            [&](int t, unsigned int& key) {
-                key = staged ? stage[t] : f32_key(L[t].x);
-                return true;
-            },
-            n, k, false, sm.rs);
+        if (staged)
+            lam = block_kth_bound_arr(stage, nullptr, n, k, false, sm.rs);
+        else
+            lam = block_kth_bound(
+                [&](int t, unsigned int& key) {
+                    key = f32_key(L[t].x);
+                    return true;
+                },
+                n, k, false, sm.rs);
     }
     if (threadIdx.x == 0) sm.rs.ctl[0] = 0;
     __syncthreads();
@@ -902,14 +906,15 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
         __syncthreads();
     } else {
         const int Kp = pool_blocks - 1;      // blocks chosen by score besides the forced newest one
-        // dense: every block but the forced newest one, by id; its threshold from the per-warp
-        // maxima (Kp + 1 of them, as one may belong to the forced block)
+        // dense: every block but the forced newest one, by id; its threshold from the group maxima:
+        // Kp + 1 distinct blocks (one may be the forced block) need Kp + 1 groups when a block holds
+        // at most one group (bs <= 8), bs / 8 times as many otherwise
         const int mb = dense ? nb - 1 : counts[2 * slab + 1];
         const int32_t* bi = bid + slab * list_len;
         const float2* bl = blu + slab * list_len;
         unsigned int lamb = 0u;
         if (dense) {
-            if (mb > Kp) lamb = wm_floor(Kp + 1);
+            if (mb > Kp) lamb = wm_floor((Kp + 1) * (bs > 8 ? bs / 8 : 1));
         } else if (mb > Kp) {                 // <= the Kp-th largest lower bound
             unsigned int* stage = sm.bitmap;
             const bool staged = mb <= SEL_BITMAP_BITS / 32;
@@ -917,12 +922,15 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
                 for (int t = threadIdx.x; t < mb; t += blockDim.x) stage[t] = f32_key(bl[t].x);
                 __syncthreads();
             }
-            lamb = block_kth_bound(
-                [&](int t, unsigned int& key) {
-                    key = staged ? stage[t] : f32_key(bl[t].x);
-                    return true;
-                },
-                mb, Kp, false, sm.rs);
+            if (staged)
+                lamb = block_kth_bound_arr(stage, nullptr, mb, Kp, false, sm.rs);
+            else
+                lamb = block_kth_bound(
+                    [&](int t, unsigned int& key) {
+                        key = f32_key(bl[t].x);
+                        return true;
+                    },
+                    mb, Kp, false, sm.rs);
         }
         // candidates: blocks whose upper bound reaches the Kp-th largest lower
         // bound, with their (upper, lower) bound keys packed in ckey
@@ -958,12 +966,8 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
             // is above mu can be outranked only by blocks whose upper bound is
             // above mu too, at most Kp-1 others: it is in.  Only the rest get
             // exact block maxima, and fill the remaining slots by (max desc, id asc).
-            const unsigned int mu = block_kth_bound(    // >= the (Kp+1)-th largest upper bound
-                [&](int t, unsigned int& key) {
-                    key = (unsigned int)(ckey[t] >> 32);
-                    return true;
-                },
-                mc, Kp + 1, true, sm.rs);
+            // >= the (Kp+1)-th largest upper bound
+            const unsigned int mu = block_kth_bound_arr(nullptr, ckey, mc, Kp + 1, true, sm.rs);
             if (threadIdx.x == 0) {
                 sm.rs.ctl[0] = 0;
                 sm.rs.ctl[3] = 0;

@@ -149,7 +149,7 @@ __device__ __forceinline__ double u53_to_f64(long long D) {
 // the same exact product, so the same rounded result, with one fp64
 // operation per head.
 template <int DI>
-__device__ double exact_score(const uint8_t* __restrict__ kc, const uint8_t* __restrict__ ks, QView<DI> q, int H) {
+__device__ __noinline__ double exact_score(const uint8_t* __restrict__ kc, const uint8_t* __restrict__ ks, QView<DI> q, int H) {
     KeyRow<DI> k;
     k.load(kc, ks);
     int ski[DI / 16];
@@ -587,6 +587,24 @@ __device__ unsigned int block_kth_floor(Get getkey, int n, int k, RadixSmem& rs)
     const unsigned int r = rs.kmax32;
     __syncthreads();                                          // rs is reused by the caller
     return r == ~0u ? lo : r;
+}
+
+// block_kth_bound over the keys of an array: the largest of keys32[st t .. st t + st - 1] (st >= 1;
+// the array holds at least st n keys), or (keys32 null) the high word of keys64[t].  Not inlined:
+// the selections that take it share one copy of the band search.
+static __device__ __noinline__ unsigned int block_kth_bound_arr(const unsigned int* keys32, const unsigned long long* keys64,
+                                                         int n, int k, bool upper, RadixSmem& rs, int st = 1) {
+    return block_kth_bound(
+        [&](int t, unsigned int& key) {
+            if (keys32) {
+                key = keys32[st * t];
+                for (int i = 1; i < st; ++i) key = max(key, keys32[st * t + i]);
+            } else {
+                key = (unsigned int)(keys64[t] >> 32);
+            }
+            return true;
+        },
+        n, k, upper, rs);
 }
 
 // warp-aggregated append to a list whose counter lives at *ctr (shared or global)

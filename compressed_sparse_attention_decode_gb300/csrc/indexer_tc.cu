@@ -18,12 +18,12 @@
 // group sums, which only widens the band the selection rescores exactly.
 //
 // The epilogue writes, for every eligible entry, its upper bound S~+E to the
-// query's dense list, and for each warp's 32 entries the largest lower bound
-// S~-E (as an order key); with an HSI pool also each block's bounds (the
-// largest member bounds, over the block's lanes).  The selection kernel takes
-// its thresholds from those per-warp maxima: each is the lower bound of a
-// different entry (and block), so the k-th largest of them never exceeds the
-// k-th largest lower bound.
+// query's dense list, and for each aligned group of 8 entries the largest
+// lower bound S~-E (as an order key); with an HSI pool also each block's bounds
+// (the largest member bounds, over the block's lanes).  The selection kernel
+// takes its thresholds from those group maxima: each is the lower bound of a
+// different entry, so the k-th largest of them never exceeds the k-th largest
+// lower bound.
 //
 // Warp roles (384 threads): warps 0-7 epilogue in two groups of four that take
 // alternate tiles, each with its own TMEM accumulator (in a group one TMEM lane
@@ -60,8 +60,8 @@ constexpr uint32_t IS_DYN = IS_END + 1024;
 __device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t unit) { return row * 128 + ((unit ^ (row & 7)) << 4); }
 
 // The outputs for query slab `slab` (row stride list_len): dense_ub(lu, slab, list_len)[e] = the
-// upper bound of entry e (entries 0 .. n_elig-1), wmk[e / 32] = the largest lower-bound key of
-// entries e .. e+31 (f32_key order; the key of -inf when none is eligible), blu[e / bs] = the bounds
+// upper bound of entry e (entries 0 .. n_elig-1), wmk[e / 8] = the largest lower-bound key of
+// entries e .. e+7 (f32_key order; the key of -inf when none is eligible), blu[e / bs] = the bounds
 // of HSI block e / bs (bs a power of two up to 32; bs == 0: no blocks).
 __global__ void __launch_bounds__(384, 2) k_scan_full_tc(
     const uint8_t* __restrict__ kc_all, const uint8_t* __restrict__ ks_all, int capacity,
@@ -266,8 +266,11 @@ __global__ void __launch_bounds__(384, 2) k_scan_full_tc(
             const bool valid = i < n_loc;
             const float lb = valid ? S - E : -INFINITY, ub = valid ? S + E : -INFINITY;
             if (valid) ub_q[e] = ub;
-            const unsigned int km = __reduce_max_sync(0xffffffffu, f32_key(lb));
-            if (lane == 0) wm_q[(c0 + t * ITC_TILE + wq * 32) >> 5] = km;
+            // the largest lower-bound key of each aligned group of 8 entries
+            unsigned int km = f32_key(lb);
+#pragma unroll
+            for (int o2 = 1; o2 < 8; o2 <<= 1) km = max(km, __shfl_xor_sync(0xffffffffu, km, o2));
+            if ((lane & 7) == 0) wm_q[e >> 3] = km;
             if (bsh) {
                 float lbb = lb, ubb = ub;
                 for (int o2 = 1; o2 < bsh; o2 <<= 1) {
