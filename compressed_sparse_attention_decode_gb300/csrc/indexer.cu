@@ -747,13 +747,28 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
     const unsigned int* wmk = reinterpret_cast<const unsigned int*>(ids) + slab * list_len;
     // (taken over groups of 32 or 16 entries, maxima of 4 or 2 group maxima, while those are enough:
     // fewer keys for the band search)
+    // The keys are staged in shared memory (the bitmap region is idle here) once, so the passes of the
+    // band search do not go back to L2.
     auto wm_floor = [&](int kk2) -> unsigned int {
+        constexpr int STAGE_CAP = SEL_BITMAP_BITS / 32;
         const int n8 = n / 8;                     // whole groups of 8 (their maxima are all written)
-        for (int st = 4; st >= 1; st >>= 1)
-            if (n8 / st >= kk2) return block_kth_bound_arr(wmk, nullptr, n8 / st, kk2, false, sm.rs, st);
-        const int nwm = (n + 7) / 8;
-        if (nwm < kk2) return 0u;
-        return block_kth_bound_arr(wmk, nullptr, nwm, kk2, false, sm.rs);
+        int st = 4;
+        while (st > 1 && n8 / st < kk2) st >>= 1;
+        while (n8 / st > STAGE_CAP) st <<= 1;
+        int nk = n8 / st;
+        if (nk < kk2) {                           // with the last, partial group too
+            st = 1;
+            nk = (n + 7) / 8;
+            if (nk < kk2 || nk > STAGE_CAP) return 0u;
+        }
+        unsigned int* stage = sm.bitmap;
+        for (int t = threadIdx.x; t < nk; t += blockDim.x) {
+            unsigned int key = wmk[st * t];
+            for (int i = 1; i < st; ++i) key = max(key, wmk[st * t + i]);
+            stage[t] = key;
+        }
+        __syncthreads();
+        return block_kth_bound_arr(stage, nullptr, nk, kk2, false, sm.rs);
     };
     // the pure pool's block has the whole block-candidate lists (the scan forwards no blocks then)
     const int64_t hoff = pure ? 0 : list_len / 2;
@@ -814,15 +829,31 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
     if (threadIdx.x == 0) sm.rs.ctl[0] = 0;
     __syncthreads();
     if (dense) {
-        // the upper bounds of every eligible entry, four per load and 16 loads in flight per thread
+        // the upper bounds of every eligible entry, four per load and 16 loads in flight per thread;
+        // each thread marks its candidates in a 64-bit mask, and a warp reserves their places with
+        // one atomic and writes them in a short loop over the mask
         const float* U = dense_ub(lu, slab, list_len);
         const int n4 = n >> 2;
-        auto take = [&](int t, float ub, bool in) {    // every lane of the warp calls it
-            const bool f = in && f32_key(ub) >= lam;
-            const int pos = append_slot(f, &sm.rs.ctl[0]);
-            if (f) {
+        const int lane = threadIdx.x & 31;
+        auto place = [&](unsigned long long mask, int base) {   // every lane of the warp calls it
+            const int cnt = __popcll(mask);
+            int incl = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            int wb = 0;
+            if (lane == 31 && incl) wb = atomicAdd(&sm.rs.ctl[0], incl);
+            int pos = __shfl_sync(0xffffffffu, wb, 31) + incl - cnt;
+#pragma unroll 1
+            while (mask) {
+                const int bi = __ffsll((long long)mask) - 1;
+                mask &= mask - 1ull;
+                const int t = 4 * (base + (bi >> 2) * (int)blockDim.x + (int)threadIdx.x) + (bi & 3);
                 cid[pos] = t;
                 if (pos < MAX_K) sm.id[pos] = t;
+                ++pos;
             }
         };
         for (int base = 0; base < n4; base += 16 * blockDim.x) {
@@ -833,19 +864,26 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
                 v[u] = i4 < n4 ? __ldg(reinterpret_cast<const float4*>(U) + i4)
                                : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
             }
+            unsigned long long mask = 0ull;
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
-                const int i4 = base + u * blockDim.x + threadIdx.x, t = 4 * i4;
-                const bool in = i4 < n4;
-                take(t, v[u].x, in);
-                take(t + 1, v[u].y, in);
-                take(t + 2, v[u].z, in);
-                take(t + 3, v[u].w, in);
+                if (base + u * (int)blockDim.x + (int)threadIdx.x < n4) {
+                    mask |= (unsigned long long)(f32_key(v[u].x) >= lam) << (4 * u);
+                    mask |= (unsigned long long)(f32_key(v[u].y) >= lam) << (4 * u + 1);
+                    mask |= (unsigned long long)(f32_key(v[u].z) >= lam) << (4 * u + 2);
+                    mask |= (unsigned long long)(f32_key(v[u].w) >= lam) << (4 * u + 3);
+                }
             }
+            place(mask, base);
         }
         for (int base = 4 * n4; base < n; base += blockDim.x) {
             const int t = base + threadIdx.x;
-            take(t, t < n ? U[t] : -INFINITY, t < n);
+            const bool f = t < n && f32_key(U[t]) >= lam;
+            const int pos = append_slot(f, &sm.rs.ctl[0]);
+            if (f) {
+                cid[pos] = t;
+                if (pos < MAX_K) sm.id[pos] = t;
+            }
         }
     } else {
     for (int base = 0; base < n; base += blockDim.x) {
