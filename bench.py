@@ -202,13 +202,16 @@ def extra_bytes(wl):
                s.B * sum(m == "swa" for m in s.layers) * s.H * 512 * 6 for s in segments_of(wl))
 
 
-# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture of
-# the dominant kernel on the 64-query, k = 512, 64-head attention (the attention moves the same
-# bytes at any context length), keyed by the SHA-256 of the kernel's source file at capture time:
-# once the source changes the figure no longer describes the kernel and is reported as null.
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from ncu captures: the
+# attention on 64 queries, k = 512, 64 heads (it moves the same bytes at any context length); the
+# decode Full scan at 128K context, 64 sequences (T).  Keyed by the SHA-256 of the kernel's source
+# file at capture time: once the source changes the figure no longer describes the kernel and is
+# reported as null.
 MEASURED_TRAFFIC = {
-    "sparse_attn": {"bytes": 24061184, "source_sha": "22338ec56505b075",
+    "sparse_attn": {"bytes": 24043264, "source_sha": "bfcf5e8ccd505de9",
                     "capture": "profiles/k_sparse_attn_pair_profile-16k-b64-20L.md"},
+    "indexer_full": {"bytes": 317691000, "source_sha": "d0343eab2c38963a", "T": 131072,
+                     "capture": "profiles/launches_decode-128k-b64-20L.md (k_scan_full_tc, 128K)"},
 }
 
 
@@ -581,8 +584,8 @@ def roofline(wl, per_op, peak, peak_kind):
     traffic = None
     rec = MEASURED_TRAFFIC.get(name)
     s0 = segments_of(wl)[0]
-    if rec and len(segments_of(wl)) == 1 and (s0.k, s0.H, s0.B) == (512, 64, 64) and \
-            rec["source_sha"] == kernel_source_sha(name):
+    if rec and len(segments_of(wl)) == 1 and (s0.k, s0.H, s0.B, s0.n_q) == (512, 64, 64, 1) and \
+            rec.get("T", s0.T) == s0.T and rec["source_sha"] == kernel_source_sha(name):
         traffic = rec["bytes"]
     return {"bound": "hbm", "kernel": name, "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
             "traffic": traffic, "bytes_per_launch": total[name] // n_launch,
