@@ -1115,7 +1115,7 @@ static size_t ws_bytes(int64_t slabs, int64_t n) {
     return ((16 + slabs * 2 * sizeof(int) + 255) / 256) * 256 + slabs * slab_bytes(n);
 }
 
-bool scan_tc_supported(int d_idx, int H, int QB, int pool_blocks, int bs);
+bool scan_tc_supported(int d_idx, int H, int QB, int pool_blocks, int bs, const csa2_cache& c);
 bool scan_mq_tc_supported(int d_idx, int H, int n_q, int pool_blocks);
 cudaError_t launch_scan_mq_tc(const csa2_cache& c, const uint8_t* iq_codes, const uint8_t* iq_scales,
                               const float* w_head, int n_q, const int64_t* q_pos, int q0, int n_qc, int k, int* counts,
@@ -1165,7 +1165,7 @@ cudaError_t launch_indexer_full_t(const csa2_cache& c, const uint8_t* iq_codes, 
         if (scan_mq_tc_supported(DI, H, n_q, pb_scan)) {
             e = launch_scan_mq_tc(c, iq_codes, iq_scales, w_head, n_q, q_pos, q0, n_qc, kf, w.counts, w.ids, w.lu,
                                   (int)list_len, w.err, st);
-        } else if (scan_tc_supported(DI, H, QB, pb_scan, bs_scan)) {
+        } else if (scan_tc_supported(DI, H, QB, pb_scan, bs_scan, c)) {
             e = launch_scan_full_tc(c, iq_codes, iq_scales, w_head, n_q, q_pos, q0, n_qc, H, pb_scan, bs_scan,
                                     reinterpret_cast<unsigned int*>(w.ids), w.lu, w.blu, (int)list_len, w.err, st);
             dense = 1;

@@ -25,13 +25,17 @@
 // different entry, so the k-th largest of them never exceeds the k-th largest
 // lower bound.
 //
-// Warp roles (384 threads): warps 0-7 epilogue in two groups of four that take
-// alternate tiles, each with its own TMEM accumulator (in a group one TMEM lane
-// = one entry); warp 8 lane 0 issues the MMAs, warp 9 lane 0 issues 1-D bulk
-// copies of each tile's contiguous key rows (8 KB codes + 1 KB scales, four
-// tiles in flight), warps 10-11 expand the packed codes into the padded MMA
-// layout.  Two A slots and two TMEM accumulators keep copies, MMAs and
-// epilogues overlapped.
+// Warp roles (320 threads): warps 0-7 epilogue in two groups of four that take
+// alternate tiles (in a group one TMEM lane = one entry), warp 8 lane 0 issues
+// the MMAs, warp 9 lane 0 the copies.  A tile's key codes come in one tensor
+// copy (TMA) whose 4-bit data type spreads every 8 packed bytes into the low
+// half of a 16-byte unit, which is the MMA's operand layout (the high halves
+// were zeroed once and the copy leaves them alone); its scales come in a 1-D
+// bulk copy.  Five operand slots, eight scale slots and four TMEM accumulators
+// keep about 45 KB of keys in flight per block: the copies, MMAs and
+// epilogues overlap, and an operand slot is refilled as soon as its MMAs are
+// done.
+#include <cuda.h>
 #include "indexer_common.cuh"
 #include "umma.cuh"
 
@@ -39,39 +43,51 @@ namespace csa2 {
 
 constexpr int ITC_E = 4096;                 // entries per block
 constexpr int ITC_TILE = 128;
-constexpr int ITC_NR = 4;                   // raw staging slots (bulk-copy depth)
-constexpr int ITC_NA = 2;                   // MMA-layout A slots
+constexpr int ITC_NA = 5;                   // MMA operand slots (filled by the tensor copy)
+constexpr int ITC_NS = 8;                   // key-scale slots
+constexpr int ITC_ND = 4;                   // TMEM accumulators
 constexpr int ITC_DI = 128;
 constexpr int ITC_G = ITC_DI / 16;
-constexpr int ITC_THREADS = 384;
-constexpr int ITC_MMAW = 8, ITC_COPYW = 9, ITC_XW0 = 10;   // warps 0-7 epilogue (two groups of four)
-constexpr int ITC_XFORM = 64;               // warps 10-11 expand raw codes into the MMA layout
-// shared memory (from the 1024-aligned base)
+constexpr int ITC_THREADS = 320;
+constexpr int ITC_MMAW = 8, ITC_COPYW = 9;  // warps 0-7 epilogue (two groups of four)
 constexpr int ITC_H = 8;                    // indexer heads taken by this kernel
 constexpr int ITC_N = ITC_H * ITC_G;        // MMA N: one column per (head, group)
+// shared memory (from the 1024-aligned base)
 constexpr uint32_t IS_B = 0;                                  // query operand, 64 rows x 128 B
-constexpr uint32_t IS_A = ITC_N * 128;                        // 2 slots x 128 rows x 128 B
-constexpr uint32_t RAW_SLOT = ITC_TILE * (ITC_DI / 2) + ITC_TILE * 8;   // codes 8 KB + scales 1 KB
-constexpr uint32_t IS_RAW = IS_A + ITC_NA * ITC_TILE * 128;   // 4 slots of raw rows
-constexpr uint32_t IS_Q = IS_RAW + ITC_NR * RAW_SLOT;         // sq [H][G] floats + w [H]
+constexpr uint32_t IS_A = ITC_N * 128;                        // operand slots, 128 rows x 128 B each
+constexpr uint32_t A_SLOT = ITC_TILE * 128;
+constexpr uint32_t IS_S = IS_A + ITC_NA * A_SLOT;             // scale slots, 8 B per row
+constexpr uint32_t S_SLOT = ITC_TILE * ITC_G;
+constexpr uint32_t IS_Q = IS_S + ITC_NS * S_SLOT;             // sq [H][G] floats + w [H]
 constexpr uint32_t IS_END = IS_Q + 2048;
 constexpr uint32_t IS_DYN = IS_END + 1024;
+constexpr uint32_t TMA_TX = ITC_TILE * (ITC_DI / 2);          // bytes one tensor copy delivers (the packed codes)
 
 __device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t unit) { return row * 128 + ((unit ^ (row & 7)) << 4); }
+
+// one 128-row box of the key-code tensor (rows y .. y+127) into an operand slot; rows past the
+// end of the tensor are filled with zeros
+__device__ __forceinline__ void tma_codes(uint32_t dst, const CUtensorMap* tm, int y, uint32_t mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(0), "r"(y), "r"(mbar)
+        : "memory");
+}
 
 // The outputs for query slab `slab` (row stride list_len): dense_ub(lu, slab, list_len)[e] = the
 // upper bound of entry e (entries 0 .. n_elig-1), wmk[e / 8] = the largest lower-bound key of
 // entries e .. e+7 (f32_key order; the key of -inf when none is eligible), blu[e / bs] = the bounds
-// of HSI block e / bs (bs a power of two up to 32; bs == 0: no blocks).
-__global__ void __launch_bounds__(384, 2) k_scan_full_tc(
-    const uint8_t* __restrict__ kc_all, const uint8_t* __restrict__ ks_all, int capacity,
+// of HSI block e / bs (bs a power of two up to 32; bs == 0: no blocks).  `tmap` describes the key
+// codes of all sequences as one tensor of batch * capacity rows of d_I 4-bit values.
+__global__ void __launch_bounds__(ITC_THREADS, 2) k_scan_full_tc(
+    const __grid_constant__ CUtensorMap tmap, const uint8_t* __restrict__ ks_all, int capacity,
     const uint8_t* __restrict__ iq_codes, const uint8_t* __restrict__ iq_scales, const float* __restrict__ w_head,
     const int64_t* __restrict__ q_pos, int n_q, int q0, int n_qc, int H, int bs, unsigned int* __restrict__ wmk,
     float2* __restrict__ lu, float2* __restrict__ blu, int list_len, int* __restrict__ err, int ratio) {
     pdl_wait();             // the selection that follows is let in only as the scan's blocks exit
     extern __shared__ uint8_t dyn[];
-    __shared__ __align__(8) unsigned long long bar_rfull[ITC_NR], bar_rfree[ITC_NR], bar_afull[ITC_NA], bar_afree[ITC_NA],
-        bar_dfull[2], bar_dfree[2];
+    __shared__ __align__(8) unsigned long long bar_full[ITC_NA], bar_afree[ITC_NA], bar_sfull[ITC_NS],
+        bar_sfree[ITC_NS], bar_dfull[ITC_ND], bar_dfree[ITC_ND];
     __shared__ uint32_t tmem_base;
     __shared__ int s_nel;
 
@@ -84,20 +100,21 @@ __global__ void __launch_bounds__(384, 2) k_scan_full_tc(
     const int64_t slab = (int64_t)b * n_qc + ql;
     const int c0 = blockIdx.x * ITC_E;
     constexpr int N = ITC_N;
+    auto sa = [](const void* p) { return umma::smem_u32(p); };
 
     if (tid == 0) {
         s_nel = n_elig_of(q_pos[gq], capacity, ratio);
-        for (int i = 0; i < ITC_NR; ++i) {
-            umma::mbar_init(umma::smem_u32(&bar_rfull[i]), 1);
-            umma::mbar_init(umma::smem_u32(&bar_rfree[i]), 128);
-        }
         for (int i = 0; i < ITC_NA; ++i) {
-            umma::mbar_init(umma::smem_u32(&bar_afull[i]), ITC_XFORM);
-            umma::mbar_init(umma::smem_u32(&bar_afree[i]), 1);
+            umma::mbar_init(sa(&bar_full[i]), 1);
+            umma::mbar_init(sa(&bar_afree[i]), 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            umma::mbar_init(umma::smem_u32(&bar_dfull[i]), 1);
-            umma::mbar_init(umma::smem_u32(&bar_dfree[i]), 128);
+        for (int i = 0; i < ITC_NS; ++i) {
+            umma::mbar_init(sa(&bar_sfull[i]), 1);
+            umma::mbar_init(sa(&bar_sfree[i]), 4);         // one arrival per epilogue warp of the group
+        }
+        for (int i = 0; i < ITC_ND; ++i) {
+            umma::mbar_init(sa(&bar_dfull[i]), 1);
+            umma::mbar_init(sa(&bar_dfree[i]), 4);
         }
         umma::fence_mbar_init();
     }
@@ -118,10 +135,10 @@ __global__ void __launch_bounds__(384, 2) k_scan_full_tc(
     float* ww = sq + H * ITC_G;                                // [H]
     for (int i = tid; i < H * ITC_G; i += blockDim.x) sq[i] = e4m3_to_f32(iq_scales[gq * H * ITC_G + i]);
     for (int i = tid; i < H; i += blockDim.x) ww[i] = w_head[gq * H + i];
-    // zero the A slots once: the pad half of every 16-byte unit stays zero
+    // zero the operand slots once: the tensor copies write only the low half of every 16-byte unit
     for (int i = tid; i < ITC_NA * ITC_TILE * 8; i += blockDim.x)
         reinterpret_cast<uint4*>(sm + IS_A)[i] = make_uint4(0, 0, 0, 0);
-    if (warp == 0) umma::tmem_alloc(umma::smem_u32(&tmem_base), 128);
+    if (warp == 0) umma::tmem_alloc(sa(&tmem_base), 64 * ITC_ND);
     umma::fence_proxy_async();
     umma::fence_before();
     __syncthreads();
@@ -131,72 +148,56 @@ __global__ void __launch_bounds__(384, 2) k_scan_full_tc(
     const int n_loc = min(max(n_elig - c0, 0), ITC_E);
     const int n_tiles = (n_loc + ITC_TILE - 1) / ITC_TILE;
     bool ok = true;
+    int n_issued = 0;                                       // tiles the copy issuer started
 
     // scale rows are 8 bytes; a bulk copy needs a 16-byte aligned source
     const uint8_t* ks_seq = ks_all + ((int64_t)b * capacity + c0) * ITC_G;
     const bool bulk_scales = ((reinterpret_cast<uintptr_t>(ks_seq) & 15u) == 0);
     if (warp == ITC_COPYW) {
-        // ---- bulk-copy issuer
+        // ---- copy issuer: tile t into operand slot t % NA and scale slot t % NS once both are free
         if (lane == 0) {
-            for (int t = 0; t < n_tiles; ++t) {
-                const int r = t % ITC_NR;
-                if (t >= ITC_NR) ok &= umma::mbar_wait(umma::smem_u32(&bar_rfree[r]), ((t / ITC_NR) - 1) & 1);
+            for (int t = 0; t < n_tiles && ok; ++t) {
+                const int a = t % ITC_NA, s = t % ITC_NS;
+                if (t >= ITC_NA) ok &= umma::mbar_wait(sa(&bar_afree[a]), ((t / ITC_NA) - 1) & 1);
+                if (t >= ITC_NS && ok) ok &= umma::mbar_wait(sa(&bar_sfree[s]), ((t / ITC_NS) - 1) & 1);
+                if (!ok) break;
                 const int e0 = c0 + t * ITC_TILE;
                 const int rows = min(ITC_TILE, n_elig - e0);
-                const uint32_t cb = (uint32_t)rows * (ITC_DI / 2);
                 const uint32_t sbytes = bulk_scales ? (uint32_t)(rows & ~1) * ITC_G : 0u;
-                const uint32_t mb = umma::smem_u32(&bar_rfull[r]);
-                const uint32_t dst = base + IS_RAW + r * RAW_SLOT;
-                umma::mbar_arrive_expect_tx(mb, cb + sbytes);
-                umma::bulk_g2s(dst, kc_all + ((int64_t)b * capacity + e0) * (ITC_DI / 2), cb, mb);
-                if (sbytes) umma::bulk_g2s(dst + ITC_TILE * (ITC_DI / 2), ks_all + ((int64_t)b * capacity + e0) * ITC_G, sbytes, mb);
+                umma::mbar_arrive_expect_tx(sa(&bar_full[a]), TMA_TX);
+                tma_codes(base + IS_A + a * A_SLOT, &tmap, b * capacity + e0, sa(&bar_full[a]));
+                umma::mbar_arrive_expect_tx(sa(&bar_sfull[s]), sbytes);
+                if (sbytes)
+                    umma::bulk_g2s(base + IS_S + s * S_SLOT, ks_all + ((int64_t)b * capacity + e0) * ITC_G, sbytes,
+                                   sa(&bar_sfull[s]));
+                n_issued = t + 1;
             }
-        }
-    } else if (warp >= ITC_XW0) {
-        // ---- expand packed codes (8 bytes per 16-value group) into the data half of each 16-byte unit
-        const int xt = tid - ITC_XW0 * 32;
-        for (int t = 0; t < n_tiles; ++t) {
-            const int r = t % ITC_NR, a = t % ITC_NA;
-            ok &= umma::mbar_wait(umma::smem_u32(&bar_rfull[r]), (t / ITC_NR) & 1);
-            if (t >= ITC_NA) ok &= umma::mbar_wait(umma::smem_u32(&bar_afree[a]), ((t / ITC_NA) - 1) & 1);
-            const uint4* raw = reinterpret_cast<const uint4*>(sm + IS_RAW + r * RAW_SLOT);
-            uint8_t* as = sm + IS_A + a * (ITC_TILE * 128);
-#pragma unroll 4
-            for (int c = xt; c < ITC_TILE * 4; c += ITC_XFORM) {
-                const int row = c >> 2, q4 = c & 3;
-                const uint4 v = raw[c];
-                *reinterpret_cast<uint2*>(as + swz128(row, 2 * q4)) = make_uint2(v.x, v.y);
-                *reinterpret_cast<uint2*>(as + swz128(row, 2 * q4 + 1)) = make_uint2(v.z, v.w);
-            }
-            umma::fence_proxy_async();
-            umma::mbar_arrive(umma::smem_u32(&bar_afull[a]));
         }
     } else if (warp == ITC_MMAW) {
         // ---- MMA issuer
         if (lane == 0) {
             const uint32_t idesc = (1u << 4) | (5u << 7) | (5u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
-            for (int t = 0; t < n_tiles; ++t) {
-                const int s = t % ITC_NA, d = t & 1;
-                ok &= umma::mbar_wait(umma::smem_u32(&bar_afull[s]), (t / ITC_NA) & 1);
-                if (t >= 2) ok &= umma::mbar_wait(umma::smem_u32(&bar_dfree[d]), ((t >> 1) - 1) & 1);
+            for (int t = 0; t < n_tiles && ok; ++t) {
+                const int a = t % ITC_NA, d = t % ITC_ND;
+                ok &= umma::mbar_wait(sa(&bar_full[a]), (t / ITC_NA) & 1);
+                if (t >= ITC_ND && ok) ok &= umma::mbar_wait(sa(&bar_dfree[d]), ((t / ITC_ND) - 1) & 1);
+                if (!ok) break;
                 umma::fence_after();
 #pragma unroll
                 for (int ks = 0; ks < ITC_DI / 32; ++ks) {
-                    const uint64_t ad = umma::desc(base + IS_A + s * (ITC_TILE * 128) + ks * 32, 16, 1024,
-                                                   umma::LAYOUT_SW128);
+                    const uint64_t ad = umma::desc(base + IS_A + a * A_SLOT + ks * 32, 16, 1024, umma::LAYOUT_SW128);
                     const uint64_t bd = umma::desc(base + IS_B + ks * 32, 16, 1024, umma::LAYOUT_SW128);
                     asm volatile(
                         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
                         " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}" ::"r"(tmem + 64 * d),
                         "l"(ad), "l"(bd), "r"(idesc), "r"(ks));
                 }
-                umma::commit(umma::smem_u32(&bar_dfull[d]));
-                umma::commit(umma::smem_u32(&bar_afree[s]));
+                umma::commit(sa(&bar_dfull[d]));
+                umma::commit(sa(&bar_afree[a]));     // the operand slot is free once these MMAs are done
             }
         }
-    } else {
+    } else if (warp < ITC_MMAW) {
         // ---- epilogue: one entry per thread
-        // fac * ||w||, with room for the rounding of the norms and of the sum of squares
         // C_g times fac, rounded up, with a factor 1 + 2^-10 for the rounding of the 8-term sum below
         float cb[ITC_G];
 #pragma unroll
@@ -209,20 +210,21 @@ __global__ void __launch_bounds__(384, 2) k_scan_full_tc(
         unsigned int* wm_q = wmk + slab * list_len;
         float2* blu_q = blu + slab * list_len;
         const int bsh = (bs >= 2 && bs <= 32 && (bs & (bs - 1)) == 0) ? bs : 0;
-        // warp w takes the tiles t with t % 2 == w / 4 (TMEM accumulator t % 2), lane quarter w % 4
+        // warp w takes the tiles t with t % 2 == w / 4, lane quarter w % 4
         const int eg = warp >> 2, wq = warp & 3;
         for (int t = eg; t < n_tiles; t += 2) {
-            const int s = t % ITC_NR, d = t & 1;
+            const int s = t % ITC_NS, d = t % ITC_ND;
             const int r = wq * 32 + lane;               // row of the tile = TMEM lane
             const int e0 = c0 + t * ITC_TILE;
             const int rows = min(ITC_TILE, n_elig - e0);
             uint2 skw = make_uint2(0, 0);
-            // the scales landed with this slot's bulk copy: observe that barrier phase too
-            if (bulk_scales) ok &= umma::mbar_wait(umma::smem_u32(&bar_rfull[s]), (t / ITC_NR) & 1);
+            if (ok) ok &= umma::mbar_wait_fast(sa(&bar_sfull[s]), (t / ITC_NS) & 1);
             if (bulk_scales && r < (rows & ~1))
-                skw = *reinterpret_cast<const uint2*>(sm + IS_RAW + s * RAW_SLOT + ITC_TILE * (ITC_DI / 2) + r * 8);
+                skw = *reinterpret_cast<const uint2*>(sm + IS_S + s * S_SLOT + r * 8);
             else if (r < rows)
                 skw = __ldg(reinterpret_cast<const uint2*>(ks_all + ((int64_t)b * capacity + e0 + r) * ITC_G));
+            __syncwarp();
+            if (lane == 0) umma::mbar_arrive(sa(&bar_sfree[s]));
             float skf[ITC_G], E = 0.0f;
 #pragma unroll
             for (int g = 0; g < ITC_G; ++g) {
@@ -230,11 +232,8 @@ __global__ void __launch_bounds__(384, 2) k_scan_full_tc(
                 E = __fmaf_rn(cb[g], skf[g], E);
             }
             // the group sums in two halves of four heads (32 columns), to keep registers low
-            ok &= umma::mbar_wait(umma::smem_u32(&bar_dfull[d]), (t >> 1) & 1);
+            if (ok) ok &= umma::mbar_wait_fast(sa(&bar_dfull[d]), (t / ITC_ND) & 1);
             umma::fence_after();
-            // the raw slot may be refilled only now: the tile's MMAs were issued, so the expanding warps
-            // are done reading its codes (and this thread has its scales)
-            umma::mbar_arrive(umma::smem_u32(&bar_rfree[s]));
             const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16) + 64 * d;
             float S = 0.0f;
 #pragma unroll
@@ -245,7 +244,8 @@ __global__ void __launch_bounds__(384, 2) k_scan_full_tc(
                 umma::tmem_wait_ld();
                 if (hp == 1) {
                     umma::fence_before();
-                    umma::mbar_arrive(umma::smem_u32(&bar_dfree[d]));
+                    __syncwarp();
+                    if (lane == 0) umma::mbar_arrive(sa(&bar_dfree[d]));
                 }
 #pragma unroll
                 for (int hh = 0; hh < 4; ++hh) {
@@ -281,30 +281,70 @@ __global__ void __launch_bounds__(384, 2) k_scan_full_tc(
             }
         }
     }
+    // a copy issuer that gave up may have copies in flight into this block's shared memory: let
+    // the last one issued into each slot land (bounded) before the block exits
+    if (warp == ITC_COPYW && lane == 0 && !ok) {
+        for (int t = max(0, n_issued - ITC_NS); t < n_issued; ++t) {
+            if (t >= n_issued - ITC_NA) umma::mbar_wait(sa(&bar_full[t % ITC_NA]), (t / ITC_NA) & 1, 1u << 16);
+            umma::mbar_wait(sa(&bar_sfull[t % ITC_NS]), (t / ITC_NS) & 1, 1u << 16);
+        }
+    }
     if (!ok) atomicExch(err, 1);
     umma::fence_before();
     __syncthreads();
     if (warp == 0) {
         umma::fence_after();
-        umma::tmem_dealloc(tmem, 128);
+        umma::tmem_dealloc(tmem, 64 * ITC_ND);
     }
 }
 
-// decode (one query per block), d_I = 128, 8 heads; an HSI pool of blocks of a power of two up to 32
-bool scan_tc_supported(int d_idx, int H, int QB, int pool_blocks, int bs) {
-    return d_idx == ITC_DI && QB == 1 && H == ITC_H && (pool_blocks == 0 || (bs >= 2 && bs <= 32 && (bs & (bs - 1)) == 0));
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime (no link to libcuda)
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+static EncodeTiledFn encode_tiled() {
+    static const EncodeTiledFn fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// decode (one query per block), d_I = 128, 8 heads; an HSI pool of blocks of a power of two up to
+// 32; the key codes 32-byte aligned (the tensor copy of packed 4-bit data wants it)
+bool scan_tc_supported(int d_idx, int H, int QB, int pool_blocks, int bs, const csa2_cache& c) {
+    return d_idx == ITC_DI && QB == 1 && H == ITC_H && (pool_blocks == 0 || (bs >= 2 && bs <= 32 && (bs & (bs - 1)) == 0)) &&
+           (reinterpret_cast<uintptr_t>(c.ikey_codes) & 31u) == 0 && (int64_t)c.batch * c.capacity < (1ll << 31) &&
+           encode_tiled() != nullptr;
 }
 
 cudaError_t launch_scan_full_tc(const csa2_cache& c, const uint8_t* iq_codes, const uint8_t* iq_scales,
                                 const float* w_head, int n_q, const int64_t* q_pos, int q0, int n_qc, int H,
                                 int pool_blocks, int bs, unsigned int* wmk, float2* lu, float2* blu, int list_len,
                                 int* err, cudaStream_t st) {
+    const EncodeTiledFn enc = encode_tiled();
+    if (enc == nullptr) return cudaErrorNotSupported;
+    // the key codes of every sequence as one 2-D tensor: batch * capacity rows of d_I 4-bit values
+    // (d_I / 2 bytes); a box is one tile of 128 rows, spread in shared memory to the MMA layout
+    CUtensorMap tm;
+    const cuuint64_t dims[2] = {(cuuint64_t)ITC_DI, (cuuint64_t)c.batch * (cuuint64_t)c.capacity};
+    const cuuint64_t strides[1] = {(cuuint64_t)(ITC_DI / 2)};
+    const cuuint32_t box[2] = {(cuuint32_t)ITC_DI, (cuuint32_t)ITC_TILE};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&tm, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, static_cast<void*>(c.ikey_codes), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(k_scan_full_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)IS_DYN);
     if (e != cudaSuccess) return e;
     dim3 grid((c.capacity + ITC_E - 1) / ITC_E, n_qc, c.batch);
-    launch_k(k_scan_full_tc, grid, ITC_THREADS, IS_DYN, st, c.ikey_codes, c.ikey_scales, c.capacity, iq_codes, iq_scales, w_head,
-                                              q_pos, n_q, q0, n_qc, H, pool_blocks > 0 ? bs : 0, wmk, lu, blu,
-                                              list_len, err, (int)c.ratio);
+    launch_k(k_scan_full_tc, grid, ITC_THREADS, IS_DYN, st, tm, (const uint8_t*)c.ikey_scales, c.capacity, iq_codes,
+             iq_scales, w_head, q_pos, n_q, q0, n_qc, H, pool_blocks > 0 ? bs : 0, wmk, lu, blu, list_len, err,
+             (int)c.ratio);
     note_launch();
     return cudaGetLastError();
 }
