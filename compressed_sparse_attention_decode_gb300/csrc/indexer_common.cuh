@@ -194,6 +194,14 @@ __host__ __device__ inline const float* dense_ub(const float2* lu, int64_t slab,
 
 __host__ __device__ inline float bound_factor(int H, int DI) { return 2.0f * (float)(2 * H + DI / 16 + 8) * 0x1p-24f; }
 
+// two E4M3 bytes (low byte first) to floats, exactly (through an fp16 pair: every E4M3 value is
+// an fp16 value)
+__device__ __forceinline__ float2 e4m3_pair_f32(uint32_t two) {
+    uint32_t r;
+    asm("{\n .reg .b16 t;\n cvt.u16.u32 t, %1;\n cvt.rn.f16x2.e4m3x2 %0, t;\n}" : "=r"(r) : "r"(two));
+    return __half22float2(*reinterpret_cast<__half2*>(&r));
+}
+
 // ---------------------------------------------------------------- block-wide radix selection
 
 struct RadixSmem {

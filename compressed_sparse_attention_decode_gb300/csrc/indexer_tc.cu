@@ -32,9 +32,8 @@
 // half of a 16-byte unit, which is the MMA's operand layout (the high halves
 // were zeroed once and the copy leaves them alone); its scales come in a 1-D
 // bulk copy.  Five operand slots, eight scale slots and four TMEM accumulators
-// keep about 45 KB of keys in flight per block: the copies, MMAs and
-// epilogues overlap, and an operand slot is refilled as soon as its MMAs are
-// done.
+// let the copies, MMAs and epilogues overlap, and an operand slot is refilled
+// as soon as its MMAs are done.
 #include <cuda.h>
 #include "indexer_common.cuh"
 #include "umma.cuh"
@@ -225,12 +224,16 @@ __global__ void __launch_bounds__(ITC_THREADS, 2) k_scan_full_tc(
                 skw = __ldg(reinterpret_cast<const uint2*>(ks_all + ((int64_t)b * capacity + e0 + r) * ITC_G));
             __syncwarp();
             if (lane == 0) umma::mbar_arrive(sa(&bar_sfree[s]));
-            float skf[ITC_G], E = 0.0f;
+            float skf[ITC_G];
 #pragma unroll
-            for (int g = 0; g < ITC_G; ++g) {
-                skf[g] = e4m3_to_f32(((g < 4 ? skw.x : skw.y) >> (8 * (g & 3))) & 255u);
-                E = __fmaf_rn(cb[g], skf[g], E);
+            for (int p = 0; p < ITC_G / 2; ++p) {
+                const float2 f = e4m3_pair_f32(((p < 2 ? skw.x : skw.y) >> (16 * (p & 1))) & 0xffffu);
+                skf[2 * p] = f.x;
+                skf[2 * p + 1] = f.y;
             }
+            float E = 0.0f;
+#pragma unroll
+            for (int g = 0; g < ITC_G; ++g) E = __fmaf_rn(cb[g], skf[g], E);
             // the group sums in two halves of four heads (32 columns), to keep registers low
             if (ok) ok &= umma::mbar_wait_fast(sa(&bar_dfull[d]), (t / ITC_ND) & 1);
             umma::fence_after();

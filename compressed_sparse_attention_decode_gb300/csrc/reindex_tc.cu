@@ -4,13 +4,15 @@
 //
 // A cluster of RT_CTAS blocks per query; block r takes pool slots
 // [512 r, 512 r + 512) as four tiles of 128 (one slot per thread):
-//   - the key rows of its slots are gathered (8-byte asynchronous copies) into
-//     the kind::f8f6f4 operand layout (each 16-value group: 8 code bytes, 8
-//     zero bytes), the query's codes into a block-diagonal operand (row
-//     (head, group) holds that head's codes of that group, zeros elsewhere);
+//   - each thread loads the key row of its slot (four 16-byte loads of codes,
+//     one of scales) while the query is staged, then writes the row in the
+//     kind::f8f6f4 operand layout (each 16-value group: 8 code bytes, 8 zero
+//     bytes); the query's codes form a block-diagonal operand (row (head,
+//     group) holds that head's codes of that group, zeros elsewhere);
 //   - D = keys . query^T (M = 128 slots, N = 8 heads x 8 groups, K = 128) holds
 //     the exact group sums in TMEM, from which every slot gets the same fp32
-//     score and rigorous error bound as the scans: the exact score lies in
+//     score as the scans, and the bound E = sum_g C_g s_kg with the query's
+//     per-group constants C_g (the full scan's bound): the exact score lies in
 //     [lo, hi];
 //   - the bounds go into the shared memory of block 0, and each block adds the
 //     count, smallest lower and largest upper bound of its slots into block 0
@@ -46,7 +48,7 @@ constexpr uint32_t RT_A = 0;                                     // 4 tiles x 12
 constexpr uint32_t RT_B = RT_A + RT_TILES * RT_TILE * 128;       // 64 rows x 128 B
 constexpr uint32_t RT_SC = RT_B + RT_N * 128;                    // key scales, 8 B per slot
 constexpr uint32_t RT_ENT = RT_SC + RT_SLOTS * 8;                // entry of each slot of the block
-constexpr uint32_t RT_Q = RT_ENT + RT_SLOTS * 4;                 // QView<128>, packed codes, sq
+constexpr uint32_t RT_Q = RT_ENT + RT_SLOTS * 4;                 // QView<128>, packed codes, sq, C_g
 constexpr uint32_t RT_LU = RT_Q + 4096;                          // block 0: bounds of every pool slot
 constexpr uint32_t RT_PENT = RT_LU + RT_POOL * 8;                // block 0: entry of every pool slot
 constexpr uint32_t RT_END = RT_PENT + RT_POOL * 4;
@@ -66,9 +68,6 @@ static_assert(sizeof(RtSel) <= RT_TILES * RT_TILE * 128, "selection state must f
 
 __device__ __forceinline__ uint32_t rt_swz(uint32_t row, uint32_t unit) { return row * 128 + ((unit ^ (row & 7)) << 4); }
 
-__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
-}
 
 __device__ __forceinline__ int rt_bucket(float x, float vmin, float scale) {
     return min((int)((x - vmin) * scale), RT_NB - 1);
@@ -170,6 +169,9 @@ __global__ void __launch_bounds__(RT_THREADS, 2) k_reindex_tc(const int32_t* __r
     v.bind(reinterpret_cast<int*>(sm + RT_Q), RT_H);
     uint2* packed = reinterpret_cast<uint2*>(sm + RT_Q + QView<RT_DI>::words(RT_H) * 4);
     float* sq = reinterpret_cast<float*>(packed + RT_N);
+    float* cbs = sq + RT_N;                                 // C_g, g = 0..7
+    // the query area holds the view (QView<128>::words(8) = 408 words), the packed codes, sq and C_g
+    static_assert(408 * 4 + RT_N * 8 + RT_N * 4 + RT_G * 4 <= RT_LU - RT_Q, "query area");
     bool ok = true;
 
     if (tid == 0) {
@@ -191,20 +193,16 @@ __global__ void __launch_bounds__(RT_THREADS, 2) k_reindex_tc(const int32_t* __r
         j = pool[gq * pool_len + s0 + sl];
         if (j < 0 || j >= capacity) j = -1;
     }
-    // zero the A tiles (the pad half of every 16-byte unit, and the rows of empty slots)
-    for (int i = tid; i < RT_TILES * RT_TILE * 8; i += RT_THREADS)
-        reinterpret_cast<uint4*>(sm + RT_A)[i] = make_uint4(0, 0, 0, 0);
-    __syncthreads();
-    // gather this slot's key row: the codes of group g into the data half of unit g
+    // this slot's key row into registers (64 code bytes, 8 scale bytes); an empty slot's row is zero
     ent[sl] = j;
+    uint4 kw[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+    uint2 kscw = make_uint2(0, 0);
     if (j >= 0) {
-        const uint8_t* kc = kc_all + ((int64_t)b * capacity + j) * (RT_DI / 2);
-        const uint32_t row = base + RT_A + (sl / RT_TILE) * (RT_TILE * 128);
+        const uint4* kc = reinterpret_cast<const uint4*>(kc_all + ((int64_t)b * capacity + j) * (RT_DI / 2));
 #pragma unroll
-        for (int g = 0; g < RT_G; ++g) cp_async8(row + rt_swz(sl % RT_TILE, g), kc + 8 * g);
-        cp_async8(base + RT_SC + sl * 8, ks_all + ((int64_t)b * capacity + j) * RT_G);
+        for (int i = 0; i < 4; ++i) kw[i] = __ldg(kc + i);
+        kscw = __ldg(reinterpret_cast<const uint2*>(ks_all + ((int64_t)b * capacity + j) * RT_G));
     }
-    asm volatile("cp.async.commit_group;" ::: "memory");
     // meanwhile: the query, and its block-diagonal operand
     if (iq_raw) {
         if (tid < RT_N * 4) rt_quantize_query(v, packed, iq_raw + gq * RT_H * RT_DI, tid);
@@ -227,8 +225,25 @@ __global__ void __launch_bounds__(RT_THREADS, 2) k_reindex_tc(const int32_t* __r
         }
         *reinterpret_cast<uint4*>(sm + RT_B + rt_swz(n, u)) = val;
         if (tid < RT_N) sq[tid] = v.qsc[tid];
+        if (tid < RT_G) {
+            // C_g = fac * 576 * sum_h |w_h| s_qhg, rounded up, times 1 + 2^-10 for the rounding of the
+            // 8-term sum of the bound: |D_hg| <= 576, so sum_g C_g s_kg bounds the scan's error term
+            float a = 0.0f;
+            for (int h = 0; h < RT_H; ++h) a = __fmaf_ru(fabsf(v.w[h]), v.qsc[h * RT_G + tid], a);
+            cbs[tid] = __fmul_ru(__fmul_ru(a, 576.0f * bound_factor(RT_H, RT_DI)), 1.0f + 0x1p-10f);
+        }
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");
+    // the slot's row in the operand layout: unit g = the 8 code bytes of group g, then 8 zero bytes
+    {
+        uint8_t* row = sm + RT_A + (sl / RT_TILE) * (RT_TILE * 128);
+#pragma unroll
+        for (int g = 0; g < RT_G; ++g) {
+            const uint4 w4 = kw[g >> 1];
+            *reinterpret_cast<uint4*>(row + rt_swz(sl % RT_TILE, g)) =
+                (g & 1) ? make_uint4(w4.z, w4.w, 0u, 0u) : make_uint4(w4.x, w4.y, 0u, 0u);
+        }
+        *reinterpret_cast<uint2*>(sm + RT_SC + sl * 8) = kscw;
+    }
     umma::fence_proxy_async();
     umma::fence_before();
     __syncthreads();
@@ -263,8 +278,15 @@ __global__ void __launch_bounds__(RT_THREADS, 2) k_reindex_tc(const int32_t* __r
         const uint2 skw = *reinterpret_cast<const uint2*>(scl + sl_ep * 8);
         float skf[RT_G];
 #pragma unroll
-        for (int g = 0; g < RT_G; ++g) skf[g] = e4m3_to_f32(((g < 4 ? skw.x : skw.y) >> (8 * (g & 3))) & 255u);
-        float S = 0.0f, B = 0.0f;
+        for (int p = 0; p < RT_G / 2; ++p) {
+            const float2 f = e4m3_pair_f32(((p < 2 ? skw.x : skw.y) >> (16 * (p & 1))) & 0xffffu);
+            skf[2 * p] = f.x;
+            skf[2 * p + 1] = f.y;
+        }
+        float E = 0.0f;
+#pragma unroll
+        for (int g = 0; g < RT_G; ++g) E = __fmaf_rn(cbs[g], skf[g], E);
+        float S = 0.0f;
 #pragma unroll
         for (int hh = 0; hh < RT_H; hh += 4) {
             float dv[4 * RT_G];
@@ -273,21 +295,13 @@ __global__ void __launch_bounds__(RT_THREADS, 2) k_reindex_tc(const int32_t* __r
             umma::tmem_wait_ld();
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
-                float dd = 0.0f, A = 0.0f;
+                float dd = 0.0f;
 #pragma unroll
-                for (int g = 0; g < RT_G; ++g) {
-                    const float tv = dv[h * RT_G + g] * (sq[(hh + h) * RT_G + g] * skf[g]);   // exact
-                    dd += tv;
-                    A += fabsf(tv);
-                }
+                for (int g = 0; g < RT_G; ++g) dd += dv[h * RT_G + g] * (sq[(hh + h) * RT_G + g] * skf[g]);   // terms exact
                 S = __fmaf_rn(v.w[hh + h], fmaxf(dd, 0.0f), S);
-                B = __fmaf_rn(fabsf(v.w[hh + h]), A, B);
             }
         }
-        if (valid) {
-            const float E = B * bound_factor(RT_H, RT_DI);
-            mine = make_float2(S - E, S + E);
-        }
+        if (valid) mine = make_float2(S - E, S + E);
     }
     // this block's count and range of its slots' bounds
     {
