@@ -74,7 +74,8 @@ __device__ __forceinline__ int rt_bucket(float x, float vmin, float scale) {
 }
 
 // warp-wide search of the bucket of hist[RT_NB] in which the count from the top
-// first reaches `need`: lane l sums its 32 buckets, a warp scan finds the
+// first reaches `need`: lane l sums its 32 buckets (starting at a lane-dependent
+// one, so that the 32 lanes read 32 different banks), a warp scan finds the
 // lane, then the warp scans that lane's 32 buckets one per lane
 __device__ int rt_find_bucket(const int* hist, int need) {
     const int lane = threadIdx.x & 31;
@@ -82,7 +83,7 @@ __device__ int rt_find_bucket(const int* hist, int need) {
     const int top = RT_NB - PER * lane;            // lane 0 holds the top buckets
     int c = 0;
 #pragma unroll
-    for (int i = 1; i <= PER; ++i) c += hist[top - i];
+    for (int i = 0; i < PER; ++i) c += hist[top - 1 - ((i + lane) & (PER - 1))];
     int incl = c;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -268,6 +269,15 @@ __global__ void __launch_bounds__(RT_THREADS, 2) k_reindex_tc(const int32_t* __r
     }
     ok &= umma::mbar_wait(umma::smem_u32(&bar_mma), 0);
     umma::fence_after();
+    RtSel& sel = *reinterpret_cast<RtSel*>(sm + RT_A);     // the A tiles are free once the MMAs are done
+    if (rank == 0) {
+        // block 0's selection state starts at zero; its barriers below order these stores
+        constexpr int NCH0 = RT_POOL / RT_THREADS;
+        reinterpret_cast<unsigned int*>(sel.chosen)[tid] = 0u;
+        static_assert(RT_POOL == 4 * RT_THREADS && NCH0 == 4, "one word of chosen flags per thread");
+        for (int i = tid; i < 2 * RT_NB; i += RT_THREADS) sel.hist[i] = 0;
+        if (tid < 8) sel.ctl[tid] = 0;
+    }
     // bounds: warp w reads TMEM lane quarter w % 4 of tile w / 4; thread = tile row
     const int t_ep = warp >> 2;
     const int sl_ep = t_ep * RT_TILE + (warp & 3) * 32 + lane;
@@ -334,17 +344,11 @@ __global__ void __launch_bounds__(RT_THREADS, 2) k_reindex_tc(const int32_t* __r
     }
     if (!ok) atomicExch(err, 1);
     if (rank != 0) return;
-    RtSel& sel = *reinterpret_cast<RtSel*>(sm + RT_A);     // block 0's MMAs are done: its A tiles are free
 
     // ================= block 0: selection over the n slots of the pool (slot u = c * 512 + tid)
     const int n = pool_len < RT_POOL ? pool_len : RT_POOL;
     constexpr int NCH = RT_POOL / RT_THREADS;
     const int n_valid = (int)s_stat[0];
-    if (tid < 8) sel.ctl[tid] = 0;
-#pragma unroll
-    for (int ch = 0; ch < NCH; ++ch) sel.chosen[ch * RT_THREADS + tid] = 0;
-    for (int i = tid; i < 2 * RT_NB; i += RT_THREADS) sel.hist[i] = 0;
-    __syncthreads();
     if (n_valid <= k) {
         for (int u = tid; u < n; u += RT_THREADS) sel.chosen[u] = gent[u] >= 0;
     } else {
@@ -449,11 +453,13 @@ __global__ void __launch_bounds__(RT_THREADS, 2) k_reindex_tc(const int32_t* __r
         if (lane == 0) sel.wtot[ch][warp] = __popc(mask[ch]);
     }
     __syncthreads();
-    // exclusive prefix of the (chunk, warp) counts in slot order, by one warp
+    // exclusive prefix of the (chunk, warp) counts in slot order: every warp scans the 64 counts
+    // (two per lane) and takes the four of its own
     constexpr int NW = RT_THREADS / 32;
     static_assert(NCH * NW == 64, "two (chunk, warp) counts per lane");
-    if (warp == 0) {
-        int* wt = &sel.wtot[0][0];
+    int kept, wbase[NCH];
+    {
+        const int* wt = &sel.wtot[0][0];
         const int a = wt[2 * lane], b2 = wt[2 * lane + 1];
         int incl = a + b2;
 #pragma unroll
@@ -461,21 +467,30 @@ __global__ void __launch_bounds__(RT_THREADS, 2) k_reindex_tc(const int32_t* __r
             const int y = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o) incl += y;
         }
-        wt[2 * lane] = incl - a - b2;
-        wt[2 * lane + 1] = incl - b2;
-        if (lane == 31) sel.ctl[5] = incl;
+        kept = __shfl_sync(0xffffffffu, incl, 31);
+#pragma unroll
+        for (int ch = 0; ch < NCH; ++ch) {
+            const int idx = ch * NW + warp;                  // count idx sits in lane idx / 2
+            const int ex = __shfl_sync(0xffffffffu, incl - a - b2, idx >> 1);
+            const int aa = __shfl_sync(0xffffffffu, a, idx >> 1);
+            wbase[ch] = (idx & 1) ? ex + aa : ex;
+        }
     }
-    __syncthreads();
     int* list = reinterpret_cast<int*>(sel.hist);
 #pragma unroll
     for (int ch = 0; ch < NCH; ++ch)
         if ((mask[ch] >> lane) & 1u)
-            list[sel.wtot[ch][warp] + __popc(mask[ch] & ((1u << lane) - 1u))] = gent[ch * RT_THREADS + tid];
-    const int kept = sel.ctl[5];
+            list[wbase[ch] + __popc(mask[ch] & ((1u << lane) - 1u))] = gent[ch * RT_THREADS + tid];
     __syncthreads();
+    // the list is written out as it stands while its order is checked (an HSI pool is ascending);
+    // any other pool is put in ascending order by counting
     bool unordered = false;
-    for (int i = tid; i + 1 < kept; i += RT_THREADS) unordered |= list[i] >= list[i + 1];
     int32_t* out = idx_out + gq * k;
+    for (int i = tid; i < k; i += RT_THREADS) {
+        const int id = i < kept ? list[i] : -1;
+        out[i] = id;
+        if (i + 1 < kept) unordered |= id >= list[i + 1];
+    }
     if (__syncthreads_or(unordered)) {
         for (int i = tid; i < kept; i += RT_THREADS) {
             const int id = list[i];
@@ -483,9 +498,6 @@ __global__ void __launch_bounds__(RT_THREADS, 2) k_reindex_tc(const int32_t* __r
             for (int m = 0; m < kept; ++m) p += list[m] < id;
             out[p] = id;
         }
-        for (int i = kept + tid; i < k; i += RT_THREADS) out[i] = -1;
-    } else {
-        for (int i = tid; i < k; i += RT_THREADS) out[i] = i < kept ? list[i] : -1;
     }
 }
 
