@@ -14,9 +14,11 @@
 //     score as the scans, and the bound E = sum_g C_g s_kg with the query's
 //     per-group constants C_g (the full scan's bound): the exact score lies in
 //     [lo, hi];
-//   - the bounds go into the shared memory of block 0, and each block adds the
-//     count, smallest lower and largest upper bound of its slots into block 0
-//     (cluster-scope atomics).
+//   - each block sends its slots' bounds and entries, and the count, smallest
+//     lower and largest upper bound of its slots, into the shared memory of
+//     block 0 with asynchronous remote stores counted on an mbarrier of block
+//     0, and is done; block 0 waits on that barrier alone (no cluster-wide
+//     barrier).
 // Block 0 then selects with a few block-wide phases:
 //   - one pass builds two histograms of 1024 equal-width value buckets, of the
 //     lower and of the upper bounds; bucket b_lam holds the k-th largest lower
@@ -135,12 +137,6 @@ __device__ void rt_quantize_query(QView<RT_DI> v, uint2* packed, const float* __
     }
 }
 
-__device__ __forceinline__ void red_cluster_u32(uint32_t addr, uint32_t val, int op) {
-    if (op == 0) asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(val) : "memory");
-    else if (op == 1) asm volatile("red.shared::cluster.min.u32 [%0], %1;" ::"r"(addr), "r"(val) : "memory");
-    else asm volatile("red.shared::cluster.max.u32 [%0], %1;" ::"r"(addr), "r"(val) : "memory");
-}
-
 __global__ void __launch_bounds__(RT_THREADS, 2) k_reindex_tc(const int32_t* __restrict__ pool, int pool_len,
                                                                const uint8_t* __restrict__ kc_all,
                                                                const uint8_t* __restrict__ ks_all, int capacity,
@@ -152,9 +148,9 @@ __global__ void __launch_bounds__(RT_THREADS, 2) k_reindex_tc(const int32_t* __r
     pdl_wait();
     pdl_launch_next();
     extern __shared__ uint8_t dyn[];
-    __shared__ __align__(8) unsigned long long bar_mma;
+    __shared__ __align__(8) unsigned long long bar_mma, bar_x;
     __shared__ uint32_t tmem_base;
-    __shared__ unsigned int s_stat[3];        // block 0: valid slots, smallest lower / largest upper bound key
+    __shared__ __align__(16) unsigned int p_stat[RT_CTAS][4];   // block 0: per block valid slots, smallest lower / largest upper bound key
     __shared__ unsigned int l_stat[3];        // this block's own
     const uint32_t raw_base = umma::smem_u32(dyn);
     const uint32_t base = (raw_base + 1023u) & ~1023u;
@@ -177,15 +173,16 @@ __global__ void __launch_bounds__(RT_THREADS, 2) k_reindex_tc(const int32_t* __r
 
     if (tid == 0) {
         umma::mbar_init(umma::smem_u32(&bar_mma), 1);
+        umma::mbar_init(umma::smem_u32(&bar_x), 1);
         umma::fence_mbar_init();
-        s_stat[0] = 0u;
-        s_stat[1] = ~0u;
-        s_stat[2] = 0u;
+        // block 0 expects every other block's bounds, entries and statistics
+        if (rank == 0)
+            umma::mbar_arrive_expect_tx(umma::smem_u32(&bar_x), (RT_CTAS - 1) * (RT_SLOTS * 12 + 16));
         l_stat[0] = 0u;
         l_stat[1] = ~0u;
         l_stat[2] = 0u;
     }
-    // block 0's counters are set before any block adds into them
+    // block 0's barrier is set up before any block stores into it
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     if (warp == 0) umma::tmem_alloc(umma::smem_u32(&tmem_base), RT_TILES * 64);
     const int sl = tid;                                     // this thread's slot of the block
@@ -330,20 +327,34 @@ __global__ void __launch_bounds__(RT_THREADS, 2) k_reindex_tc(const int32_t* __r
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");   // block 0 exists and is set up
     float2* glu = reinterpret_cast<float2*>(sm + RT_LU);    // meaningful in block 0
     int* gent = reinterpret_cast<int*>(sm + RT_PENT);
-    {
-        const uint32_t a_lu = umma::mapa(umma::smem_u32(&glu[s0 + sl_ep]), 0);
-        const uint32_t a_en = umma::mapa(umma::smem_u32(&gent[s0 + sl_ep]), 0);
-        asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(a_lu), "f"(mine.x), "f"(mine.y) : "memory");
-        asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(a_en), "r"(ent[sl_ep]) : "memory");
-        if (tid < 3 && l_stat[0] > 0) red_cluster_u32(umma::mapa(umma::smem_u32(&s_stat[tid]), 0), l_stat[tid], tid);
-    }
-    umma::cluster_sync();                      // every slot's bounds, the counts and the range are in block 0
     if (warp == 0) {
         umma::fence_after();
         umma::tmem_dealloc(tmem, RT_TILES * 64);
     }
     if (!ok) atomicExch(err, 1);
-    if (rank != 0) return;
+    if (rank != 0) {
+        // 12 bytes per slot and 16 bytes of statistics per block, counted on block 0's barrier
+        const uint32_t mb = umma::mapa(umma::smem_u32(&bar_x), 0);
+        umma::st_async_v2_b32(umma::mapa(umma::smem_u32(&glu[s0 + sl_ep]), 0), __float_as_uint(mine.x),
+                              __float_as_uint(mine.y), mb);
+        umma::st_async_b32(umma::mapa(umma::smem_u32(&gent[s0 + sl_ep]), 0), (uint32_t)ent[sl_ep], mb);
+        if (tid == 0)
+            umma::st_async_v4_b32(umma::mapa(umma::smem_u32(&p_stat[rank][0]), 0), l_stat[0], l_stat[1], l_stat[2], 0u,
+                                  mb);
+        return;
+    }
+    glu[sl_ep] = mine;
+    gent[sl_ep] = ent[sl_ep];
+    if (tid < 3) p_stat[0][tid] = l_stat[tid];
+    if (!umma::mbar_wait_cluster(umma::smem_u32(&bar_x), 0)) atomicExch(err, 1);   // the other blocks' stores have landed
+    __syncthreads();
+    unsigned int s_stat[3] = {0u, ~0u, 0u};  // valid slots, smallest lower / largest upper bound key of the pool
+#pragma unroll
+    for (int r = 0; r < RT_CTAS; ++r) {
+        s_stat[0] += p_stat[r][0];
+        s_stat[1] = min(s_stat[1], p_stat[r][1]);
+        s_stat[2] = max(s_stat[2], p_stat[r][2]);
+    }
 
     // ================= block 0: selection over the n slots of the pool (slot u = c * 512 + tid)
     const int n = pool_len < RT_POOL ? pool_len : RT_POOL;

@@ -119,6 +119,23 @@ __device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float a, float
                  "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_mbar)
                  : "memory");
 }
+__device__ __forceinline__ void st_async_b32(uint32_t remote_addr, uint32_t a, uint32_t remote_mbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(remote_addr), "r"(a),
+                 "r"(remote_mbar)
+                 : "memory");
+}
+__device__ __forceinline__ void st_async_v2_b32(uint32_t remote_addr, uint32_t a, uint32_t b, uint32_t remote_mbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(remote_addr),
+                 "r"(a), "r"(b), "r"(remote_mbar)
+                 : "memory");
+}
+__device__ __forceinline__ void st_async_v4_b32(uint32_t remote_addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                                uint32_t remote_mbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     remote_addr),
+                 "r"(a), "r"(b), "r"(c), "r"(d), "r"(remote_mbar)
+                 : "memory");
+}
 // named barrier over `count` threads that also returns whether any of them passed pred
 __device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t count, bool pred) {
     uint32_t r;
