@@ -1,7 +1,8 @@
 // Full indexer scan on the tensor cores ("DeepSeek-v4.1 Flash: KVキャッシュ圧縮の
 // 限界を押し広げる", §2.3.1 lightweight indexer over FP4 keys).
 //
-// For one query and a chunk of 4096 entries, 128 entries at a time:
+// For one query and a chunk of its entries (a multiple of 128, sized so that
+// the blocks fill two waves of the GPU), 128 entries at a time:
 //   A = key codes  [128 entries x d_I] FP4 E2M1 (kind::f8f6f4: each 16-value
 //       group is 8 packed bytes followed by 8 pad bytes in shared memory)
 //   B = block-diagonal query [H*G rows x d_I]: row (h, g) holds head h's codes
@@ -40,7 +41,6 @@
 
 namespace csa2 {
 
-constexpr int ITC_E = 4096;                 // entries per block
 constexpr int ITC_TILE = 128;
 constexpr int ITC_NA = 5;                   // MMA operand slots (filled by the tensor copy)
 constexpr int ITC_NS = 8;                   // key-scale slots
@@ -58,7 +58,9 @@ constexpr uint32_t A_SLOT = ITC_TILE * 128;
 constexpr uint32_t IS_S = IS_A + ITC_NA * A_SLOT;             // scale slots, 8 B per row
 constexpr uint32_t S_SLOT = ITC_TILE * ITC_G;
 constexpr uint32_t IS_Q = IS_S + ITC_NS * S_SLOT;             // sq [H][G] floats + w [H]
-constexpr uint32_t IS_END = IS_Q + 2048;
+constexpr uint32_t IS_END = IS_Q + 512;
+// two blocks per SM: both blocks' shared memory (with the 1 KB the system keeps per block) fits the SM's 228 KB
+static_assert(2 * (IS_END + 1024 + 512 + 1024) <= 228 * 1024, "two blocks per SM");
 constexpr uint32_t IS_DYN = IS_END + 1024;
 constexpr uint32_t TMA_TX = ITC_TILE * (ITC_DI / 2);          // bytes one tensor copy delivers (the packed codes)
 
@@ -82,7 +84,7 @@ __global__ void __launch_bounds__(ITC_THREADS, 2) k_scan_full_tc(
     const __grid_constant__ CUtensorMap tmap, const uint8_t* __restrict__ ks_all, int capacity,
     const uint8_t* __restrict__ iq_codes, const uint8_t* __restrict__ iq_scales, const float* __restrict__ w_head,
     const int64_t* __restrict__ q_pos, int n_q, int q0, int n_qc, int H, int bs, unsigned int* __restrict__ wmk,
-    float2* __restrict__ lu, float2* __restrict__ blu, int list_len, int* __restrict__ err, int ratio) {
+    float2* __restrict__ lu, float2* __restrict__ blu, int list_len, int* __restrict__ err, int ratio, int chunk) {
     pdl_wait();             // the selection that follows is let in only as the scan's blocks exit
     extern __shared__ uint8_t dyn[];
     __shared__ __align__(8) unsigned long long bar_full[ITC_NA], bar_afree[ITC_NA], bar_sfull[ITC_NS],
@@ -97,7 +99,7 @@ __global__ void __launch_bounds__(ITC_THREADS, 2) k_scan_full_tc(
     const int b = blockIdx.z, ql = blockIdx.y;
     const int64_t gq = (int64_t)b * n_q + q0 + ql;
     const int64_t slab = (int64_t)b * n_qc + ql;
-    const int c0 = blockIdx.x * ITC_E;
+    const int c0 = blockIdx.x * chunk;               // this block's entries: [c0, c0 + chunk)
     constexpr int N = ITC_N;
     auto sa = [](const void* p) { return umma::smem_u32(p); };
 
@@ -144,7 +146,7 @@ __global__ void __launch_bounds__(ITC_THREADS, 2) k_scan_full_tc(
     umma::fence_after();
     const uint32_t tmem = tmem_base;
     const int n_elig = s_nel;
-    const int n_loc = min(max(n_elig - c0, 0), ITC_E);
+    const int n_loc = min(max(n_elig - c0, 0), chunk);
     const int n_tiles = (n_loc + ITC_TILE - 1) / ITC_TILE;
     bool ok = true;
     int n_issued = 0;                                       // tiles the copy issuer started
@@ -344,10 +346,22 @@ cudaError_t launch_scan_full_tc(const csa2_cache& c, const uint8_t* iq_codes, co
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(k_scan_full_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)IS_DYN);
     if (e != cudaSuccess) return e;
-    dim3 grid((c.capacity + ITC_E - 1) / ITC_E, n_qc, c.batch);
+    // chunk size: the queries' tiles split into as many chunks as fill two waves of resident blocks
+    // (fewer, longer blocks pay the pipeline fill less often; whole waves leave no thin tail)
+    int dev = 0, n_sm = 0, per_sm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_scan_full_tc, ITC_THREADS, IS_DYN)) != cudaSuccess)
+        return e;
+    const int64_t tiles_q = (c.capacity + ITC_TILE - 1) / ITC_TILE;
+    const int64_t slabs = (int64_t)n_qc * c.batch;
+    int64_t chunks_q = (2 * (int64_t)(per_sm > 0 ? per_sm : 1) * n_sm) / (slabs > 0 ? slabs : 1);
+    chunks_q = chunks_q < 1 ? 1 : (chunks_q > tiles_q ? tiles_q : chunks_q);
+    const int chunk = (int)((tiles_q + chunks_q - 1) / chunks_q) * ITC_TILE;
+    dim3 grid((unsigned)((c.capacity + chunk - 1) / chunk), n_qc, c.batch);
     launch_k(k_scan_full_tc, grid, ITC_THREADS, IS_DYN, st, tm, (const uint8_t*)c.ikey_scales, c.capacity, iq_codes,
              iq_scales, w_head, q_pos, n_q, q0, n_qc, H, pool_blocks > 0 ? bs : 0, wmk, lu, blu, list_len, err,
-             (int)c.ratio);
+             (int)c.ratio, chunk);
     note_launch();
     return cudaGetLastError();
 }

@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(RT_THREADS, 2) k_reindex_tc(const int32_t* __r
     bool ok = true;
 
     if (tid == 0) {
-        umma::mbar_init(umma::smem_u32(&bar_mma), 1);
+        umma::mbar_init(umma::smem_u32(&bar_mma), RT_TILES);   // one commit per tile issuer
         umma::mbar_init(umma::smem_u32(&bar_x), 1);
         umma::fence_mbar_init();
         // block 0 expects every other block's bounds, entries and statistics
@@ -247,11 +247,12 @@ __global__ void __launch_bounds__(RT_THREADS, 2) k_reindex_tc(const int32_t* __r
     __syncthreads();
     umma::fence_after();
     const uint32_t tmem = tmem_base;
-    if (tid == 0) {
+    if (lane == 0 && warp < RT_TILES) {
+        // warp t issues tile t's MMAs (four issuers keep the tensor pipe busier than one)
         const uint32_t idesc = (1u << 4) | (5u << 7) | (5u << 10) | ((uint32_t)(RT_N >> 3) << 17) |
                                ((uint32_t)(RT_TILE >> 4) << 24);
-        for (int t = 0; t < RT_TILES; ++t) {
-            if (s0 + t * RT_TILE >= pool_len) break;
+        const int t = warp;
+        if (s0 + t * RT_TILE < pool_len) {
 #pragma unroll
             for (int ks = 0; ks < RT_DI / 32; ++ks) {
                 const uint64_t ad = umma::desc(base + RT_A + t * (RT_TILE * 128) + ks * 32, 16, 1024, umma::LAYOUT_SW128);
