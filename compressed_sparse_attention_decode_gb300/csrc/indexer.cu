@@ -701,7 +701,7 @@ __global__ void __launch_bounds__(RX_THREADS) k_reindex_fused(const int32_t* __r
 // bound of every eligible entry (item t = entry t), blu the bounds of every HSI
 // block, and ids the largest lower-bound key of each aligned group of 8 entries,
 // which the thresholds come from.
-template <int DI>
+template <int DI, bool DENSE>
 __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids, const float2* __restrict__ lu,
                                                 const int* __restrict__ counts, int n_fixed, int list_len,
                                                 const uint8_t* __restrict__ kc_all, const uint8_t* __restrict__ ks_all,
@@ -713,7 +713,10 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
                                                 int32_t* __restrict__ pool_out, const int32_t* __restrict__ bid,
                                                 const float2* __restrict__ blu, int* __restrict__ c2id,
                                                 unsigned long long* __restrict__ c2key, int* __restrict__ h2id,
-                                                unsigned long long* __restrict__ h2key, int ratio, int dense) {
+                                                unsigned long long* __restrict__ h2key, int ratio) {
+    // one instantiation per input form: each holds only the code its form runs (the selection code
+    // is large, and what a launch runs should stay in the instruction cache)
+    constexpr bool dense = DENSE;
     pdl_wait();
     pdl_launch_next();
     extern __shared__ int qsm[];
@@ -1183,12 +1186,13 @@ cudaError_t launch_indexer_full_t(const csa2_cache& c, const uint8_t* iq_codes, 
         // ceil(capacity / bs) <= list_len / 2 block candidates when bs >= 2)
         dim3 g2(n_qc, c.batch, ((pool_blocks > 1 && bs >= 2) || pure) ? 2 : 1);
         const size_t smem2 = qwords + SEL_DYN_EXTRA + SEL_BITMAP_BYTES;
-        e = cudaFuncSetAttribute(k_select<DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
+        auto kern = dense ? k_select<DI, true> : k_select<DI, false>;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
         if (e != cudaSuccess) return e;
-        launch_k(k_select<DI>, g2, 512, smem2, st, w.ids, w.lu, w.counts, 0, (int)list_len, c.ikey_codes, c.ikey_scales,
+        launch_k(kern, g2, 512, smem2, st, w.ids, w.lu, w.counts, 0, (int)list_len, c.ikey_codes, c.ikey_scales,
                                               c.capacity, iq_codes, iq_scales, (const float*)nullptr, w_head, q_pos, n_q, q0, n_qc, H, k,
                                               idx_out, pool_blocks, bs, pool_out, w.bid, w.blu, w.c2id, w.c2key,
-                                              w.bid, reinterpret_cast<unsigned long long*>(w.blu), (int)c.ratio, dense);
+                                              w.bid, reinterpret_cast<unsigned long long*>(w.blu), (int)c.ratio);
         note_launch();
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
@@ -1237,13 +1241,13 @@ cudaError_t launch_reindex_t(const csa2_cache& c, const uint8_t* iq_codes, const
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const size_t smem = qwords + SEL_DYN_EXTRA + SEL_BITMAP_BYTES;
-    e = cudaFuncSetAttribute(k_select<DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(k_select<DI, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 g(n_q, c.batch);
-    launch_k(k_select<DI>, g, 512, smem, st, pool, w.lu, nullptr, pool_len, pool_len, c.ikey_codes, c.ikey_scales,
+    launch_k(k_select<DI, false>, g, 512, smem, st, pool, w.lu, nullptr, pool_len, pool_len, c.ikey_codes, c.ikey_scales,
                                        c.capacity, iq_codes, iq_scales, iq_raw, w_head, nullptr, n_q, 0, n_q, H, k, idx_out, 0,
                                        1, nullptr, nullptr, nullptr, w.c2id, w.c2key, (int*)nullptr,
-                                       (unsigned long long*)nullptr, (int)c.ratio, 0);
+                                       (unsigned long long*)nullptr, (int)c.ratio);
     note_launch();
     return cudaGetLastError();
 }
