@@ -1044,7 +1044,28 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
             }
             __syncthreads();
             const int r = Kp - nd;               // 0 <= r < nu
-            if (r > 0) best_sorted(cid, ckey, nu, r, sm);
+            if (r > 0 && nu <= 256) {
+                // few undecided blocks (the usual case): each one's rank by (max desc, id asc) among
+                // them, counted directly from a copy in shared memory; ids are distinct, so the r best
+                // fill sm.id[0..r)
+                for (int t = threadIdx.x; t < nu; t += blockDim.x) {
+                    sm.key2[t] = ckey[t];
+                    sm.id2[t] = cid[t];
+                }
+                __syncthreads();
+                for (int t = threadIdx.x; t < nu; t += blockDim.x) {
+                    const unsigned long long kt = sm.key2[t];
+                    const int it = sm.id2[t];
+                    int rk = 0;
+                    for (int m2 = 0; m2 < nu; ++m2) {
+                        const unsigned long long km = sm.key2[m2];
+                        rk += (km > kt) || (km == kt && sm.id2[m2] < it);
+                    }
+                    if (rk < r) sm.id[rk] = it;
+                }
+            } else if (r > 0) {
+                best_sorted(cid, ckey, nu, r, sm);
+            }
             __syncthreads();
             for (int t = threadIdx.x; t < nd; t += blockDim.x) sm.id[r + t] = sm.din[t];
         }
