@@ -17,8 +17,9 @@
 // next tile overlap the MMAs and softmax of this one.  At the end the two CTAs
 // swap their per-head running max and row sum through distributed shared
 // memory and scale their partial O to the common max and normaliser; each
-// stores its share of its own half of the output dims and, after a cluster
-// barrier, adds its share of the other half with reductions in L2.
+// sends its share of the other CTA's half of the output dims into that CTA's
+// (now idle) Q area with asynchronous remote stores counted on an mbarrier,
+// and stores its own half once, its share plus the one received.
 //
 // Warps: 0-7 softmax / epilogue (warp w: TMEM lane quarter w%4, key half
 // w/4), warps 8 and 9 issue the score MMAs (K = dims 0-255 and 256-511 into
@@ -129,7 +130,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
     // this kernel alone.  Nothing this kernel writes is read by that kernel.
     extern __shared__ uint8_t dyn[];
     __shared__ __align__(8) unsigned long long b_lhalf[2], b_lfull[2], b_lfree[2], b_sfull[2], b_sfree[2], b_pfull[2],
-        b_odone[2], b_wfull;
+        b_odone[2], b_wfull, b_xch;
     __shared__ uint32_t tmem_base;
     __shared__ __align__(16) uint8_t rowok[2][AP_TILE];
 
@@ -179,7 +180,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
             umma::mbar_init(sa(&b_odone[i]), 2);
         }
         umma::mbar_init(sa(&b_wfull), 1);
+        umma::mbar_init(sa(&b_xch), 1);
         umma::fence_mbar_init();
+        // the peer's share of this CTA's half of the output arrives here (64 heads x 256 dims fp32)
+        umma::mbar_arrive_expect_tx(sa(&b_xch), AP_H * 256 * 4);
         // the window's largest magnitude starts at 0 before the loaders (past b_wfull) add to it
         wexp[1] = 0;
         // this CTA's window rows are contiguous: one bulk copy, raw bf16, into L buffer 1
@@ -614,35 +618,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
         umma::bar_named(1, AP_SMT);
         ok &= umma::mbar_wait_fast(sa(&b_odone[(T - 1) & 1]), ((T - 1) >> 1) & 1);   // every GEMM2 is done
         umma::fence_after();
-        // this CTA's share of its own half of the dims (dim tile 2*rank + half, this warp's
-        // lane quarter) is stored; the peer adds its share after the barrier
+        // this CTA's share of the peer's half of the dims (dim tile 2*peer + half, this warp's lane
+        // quarter), scaled, goes into the peer's Q area (free: the peer's score MMAs are done) as
+        // [head][256 dims], counted on the peer's exchange barrier
         const int qd = warp & 3, half = warp >> 2;
-        const int mt = 2 * (int)rank + half;
-        float* op = out + (gq * AP_H) * D_LAT + (int)rank * 256 + half * 128 + qd * 32 + lane;
+        {
+            const int mt = 2 * (int)peer + half;
+            const int dl = half * 128 + qd * 32 + lane;                 // dim within the peer's half
+            const uint32_t dst = umma::mapa(sa(sm + AP_SQ), peer) + (uint32_t)dl * 4u;
+            const uint32_t mb = umma::mapa(sa(&b_xch), peer);
 #pragma unroll 1
-        for (int c = 0; c < AP_H; c += 16) {
-            float v[16];
-            umma::tmem_ld16(tmem + ((uint32_t)(qd * 32) << 16) + APT_O + 64 * mt + c, v);
-            umma::tmem_wait_ld();
+            for (int c = 0; c < AP_H; c += 16) {
+                float v[16];
+                umma::tmem_ld16(tmem + ((uint32_t)(qd * 32) << 16) + APT_O + 64 * mt + c, v);
+                umma::tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) op[(int64_t)(c + i) * D_LAT] = ok ? v[i] * fown[c + i] : __int_as_float(0x7fc00000);
+                for (int i = 0; i < 16; ++i)
+                    umma::st_async_b32(dst + (uint32_t)(c + i) * 1024u,
+                                       __float_as_uint(ok ? __fmul_rn(v[i], fown[c + i]) : __int_as_float(0x7fc00000)), mb);
+            }
         }
-    }
-    umma::fence_before();
-    umma::cluster_sync();              // both halves of the output hold one CTA's share
-    if (warp < AP_SMW) {
-        umma::fence_after();
-        // add this CTA's share of the peer's half (reductions in L2, nothing read back)
-        const int qd = warp & 3, half = warp >> 2;
-        const int mt = 2 * (int)peer + half;
-        float* op = out + (gq * AP_H) * D_LAT + (int)peer * 256 + half * 128 + qd * 32 + lane;
+        // this CTA's half: its own share plus the peer's, one store
+        {
+            const bool got = umma::mbar_wait_cluster(sa(&b_xch), 0);
+            ok &= got;
+            const int mt = 2 * (int)rank + half;
+            const int dl = half * 128 + qd * 32 + lane;
+            const float* px = reinterpret_cast<const float*>(sm + AP_SQ) + dl;
+            float* op = out + (gq * AP_H) * D_LAT + (int)rank * 256 + dl;
 #pragma unroll 1
-        for (int c = 0; c < AP_H; c += 16) {
-            float v[16];
-            umma::tmem_ld16(tmem + ((uint32_t)(qd * 32) << 16) + APT_O + 64 * mt + c, v);
-            umma::tmem_wait_ld();
+            for (int c = 0; c < AP_H; c += 16) {
+                float v[16];
+                umma::tmem_ld16(tmem + ((uint32_t)(qd * 32) << 16) + APT_O + 64 * mt + c, v);
+                umma::tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) atomicAdd(op + (int64_t)(c + i) * D_LAT, ok ? v[i] * fown[c + i] : __int_as_float(0x7fc00000));
+                for (int i = 0; i < 16; ++i)
+                    op[(int64_t)(c + i) * D_LAT] =
+                        ok ? __fadd_rn(__fmul_rn(v[i], fown[c + i]), px[(c + i) * 256]) : __int_as_float(0x7fc00000);
+            }
         }
     }
     if (!ok) atomicExch(err, 1);
