@@ -26,8 +26,10 @@
 // two TMEM partials that the softmax adds; the first half starts as soon as
 // its dims are expanded), warps 10 and 11 the output MMAs (dim tiles 0-1 and
 // 2-3): one thread issues about one MMA per 55 cycles, two keep the tensor
-// pipe busy.  Warps 12-18 gather rows.  Q (loaded and converted to fp16 by
-// warps 0-11, one head per warp at a time) and tile 0, the CTA's window rows
+// pipe busy.  Warps 12-19 gather rows (four 32-dim units of a tile per
+// thread; the expansion sits on the tiles' critical path, and eight warps do it
+// in four even rounds).  Q (loaded and converted to fp16 by warps 0-11, one
+// head per warp at a time) and tile 0, the CTA's window rows
 // (contiguous: one bulk copy), come first; the FP4 tiles follow, their rows
 // prefetched into L2 one tile ahead, so the gathers are single L2 round trips.  Everything before
 // the indices (Q, the window tile, TMEM and barriers) overlaps the preceding
@@ -47,13 +49,13 @@ namespace csa2 {
 
 constexpr int AP_TILE = 64;                          // keys per tile
 constexpr int AP_H = 64;
-constexpr int AP_THREADS = 608;
+constexpr int AP_THREADS = 640;
 constexpr int AP_SMW = 8;                            // softmax warps 0-7
 constexpr int AP_SMT = AP_SMW * 32;
 constexpr int AP_MMAW = 8;                           // warps 8, 9 issue the score MMAs (GEMM1), dims 0-255 / 256-511
 constexpr int AP_MMA2 = 10;                          // warps 10, 11 issue the output MMAs (GEMM2), dim tiles 0-1 / 2-3
-constexpr int AP_LOADW = 12;                         // warps 12-18 gather rows
-constexpr int AP_LOADERS = 224;
+constexpr int AP_LOADW = 12;                         // warps 12-19 gather rows
+constexpr int AP_LOADERS = 256;
 constexpr uint32_t AP_QSLAB = AP_H * 128;            // 64 heads x 64 dims fp16
 constexpr uint32_t AP_LSLAB = AP_TILE * 128;         // 64 keys x 64 dims fp16
 constexpr uint32_t AP_SQ = 0;                        // Q: 8 slabs (64 KB)
