@@ -753,7 +753,7 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
     // The keys are staged in shared memory (the bitmap region is idle here) once, so the passes of the
     // band search do not go back to L2.
     auto wm_floor = [&](int kk2) -> unsigned int {
-        constexpr int STAGE_CAP = SEL_BITMAP_BITS / 32;
+        constexpr int STAGE_CAP = SEL_BITMAP_BITS / 32 - 64;   // the last 64 words: per-warp key ranges
         const int n8 = n / 8;                     // whole groups of 8 (their maxima are all written)
         int st = 4;
         while (st > 1 && n8 / st < kk2) st >>= 1;
@@ -764,14 +764,35 @@ __global__ void __launch_bounds__(512) k_select(const int32_t* __restrict__ ids,
             nk = (n + 7) / 8;
             if (nk < kk2 || nk > STAGE_CAP) return 0u;
         }
+        // the keys are staged with their range taken on the way (each warp's into its own pair of
+        // words), so that the band search needs no range pass of its own
         unsigned int* stage = sm.bitmap;
+        unsigned int* wrange = sm.bitmap + (SEL_BITMAP_BITS / 32 - 64);
+        unsigned int mn = ~0u, mx = 0u;
         for (int t = threadIdx.x; t < nk; t += blockDim.x) {
             unsigned int key = wmk[st * t];
             for (int i = 1; i < st; ++i) key = max(key, wmk[st * t + i]);
             stage[t] = key;
+            if (isfinite(key_value(key))) {
+                mn = min(mn, key);
+                mx = max(mx, key);
+            }
         }
+        mn = __reduce_min_sync(0xffffffffu, mn);
+        mx = __reduce_max_sync(0xffffffffu, mx);
+        const int nw = blockDim.x >> 5;
+        if ((threadIdx.x & 31) == 0) {
+            wrange[2 * (threadIdx.x >> 5)] = mn;
+            wrange[2 * (threadIdx.x >> 5) + 1] = mx;
+        }
+        for (int i = threadIdx.x; i < 256; i += blockDim.x) sm.rs.hist[i] = 0;
         __syncthreads();
-        return block_kth_bound_arr(stage, nullptr, nk, kk2, false, sm.rs);
+        unsigned int lo = ~0u, hi = 0u;
+        for (int w = 0; w < nw; ++w) {
+            lo = min(lo, wrange[2 * w]);
+            hi = max(hi, wrange[2 * w + 1]);
+        }
+        return block_kth_bound_arr(stage, nullptr, nk, kk2, false, sm.rs, 1, true, lo, hi);
     };
     // the pure pool's block has the whole block-candidate lists (the scan forwards no blocks then)
     const int64_t hoff = pure ? 0 : list_len / 2;

@@ -600,19 +600,49 @@ __device__ unsigned int block_kth_floor(Get getkey, int n, int k, RadixSmem& rs)
 // block_kth_bound over the keys of an array: the largest of keys32[st t .. st t + st - 1] (st >= 1;
 // the array holds at least st n keys), or (keys32 null) the high word of keys64[t].  Not inlined:
 // the selections that take it share one copy of the band search.
+// known_range: the caller passes the smallest and largest finite key as lo / hi, and rs.hist is zero
+// and a block barrier has passed since both were set (the range pass is skipped).
 static __device__ __noinline__ unsigned int block_kth_bound_arr(const unsigned int* keys32, const unsigned long long* keys64,
-                                                         int n, int k, bool upper, RadixSmem& rs, int st = 1) {
-    return block_kth_bound(
-        [&](int t, unsigned int& key) {
-            if (keys32) {
-                key = keys32[st * t];
-                for (int i = 1; i < st; ++i) key = max(key, keys32[st * t + i]);
-            } else {
-                key = (unsigned int)(keys64[t] >> 32);
+                                                         int n, int k, bool upper, RadixSmem& rs, int st = 1,
+                                                         bool known_range = false, unsigned int lo = 0u,
+                                                         unsigned int hi = 0u) {
+    auto getkey = [&](int t, unsigned int& key) {
+        if (keys32) {
+            key = keys32[st * t];
+            for (int i = 1; i < st; ++i) key = max(key, keys32[st * t + i]);
+        } else {
+            key = (unsigned int)(keys64[t] >> 32);
+        }
+        return true;
+    };
+    if (!known_range) {
+        const int lane = threadIdx.x & 31;
+        if (threadIdx.x == 0) {
+            rs.kmin32 = ~0u;
+            rs.kmax32 = 0u;
+        }
+        for (int i = threadIdx.x; i < 256; i += blockDim.x) rs.hist[i] = 0;
+        __syncthreads();
+        unsigned int mn = ~0u, mx = 0u;
+        for (int t = threadIdx.x; t < n; t += blockDim.x) {
+            unsigned int key;
+            if (getkey(t, key) && isfinite(key_value(key))) {
+                mn = min(mn, key);
+                mx = max(mx, key);
             }
-            return true;
-        },
-        n, k, upper, rs);
+        }
+        mn = __reduce_min_sync(0xffffffffu, mn);
+        mx = __reduce_max_sync(0xffffffffu, mx);
+        if (lane == 0) {
+            atomicMin(&rs.kmin32, mn);
+            atomicMax(&rs.kmax32, mx);
+        }
+        __syncthreads();
+        lo = rs.kmin32;
+        hi = rs.kmax32;
+    }
+    const uint2 band = block_kth_band_from(getkey, n, k, lo, hi, rs);
+    return upper ? band.y : band.x;
 }
 
 // warp-aggregated append to a list whose counter lives at *ctr (shared or global)
