@@ -82,6 +82,9 @@ enum { CSA2_OP_INDEXER_TOPK = 1, CSA2_OP_REINDEX = 2, CSA2_OP_SPARSE_ATTN = 3 };
  * lat_codes, lat_scales and ikey_codes must be 16-byte aligned, ikey_scales
  * d_idx/16-byte aligned (so a batch-1 view of one sequence of a larger cache
  * is always valid).  d_lat must be 512; d_idx must be 64 or 128; ratio 1 or 2.
+ * With ikey_codes 32-byte aligned (as any cudaMalloc'd plane is), the decode
+ * Full scan reads the keys by tensor copy; otherwise it takes a CUDA-core scan
+ * with the same results.
  */
 typedef struct {
     uint8_t* lat_codes;

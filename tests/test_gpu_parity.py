@@ -192,6 +192,36 @@ def test_decode_32k_all_sequences(csa):
     check_walk(csa, WORKLOADS[1], list(range(WORKLOADS[1].B)))
 
 
+def test_decode_scan_on_a_key_plane_off_32_byte_alignment(csa):
+    """a key-code plane that starts 16 bytes past a 32-byte boundary (allowed: the planes need
+    16-byte alignment) cannot be read by the tensor copy, so the decode Full layer takes the
+    CUDA-core scan and the candidate-list selection: the same top k and HSI pool as the
+    tensor-core path, which the walks check against the oracle"""
+    import copy
+    from compressed_sparse_attention_decode_gb300.synthetic import build_step
+    wl = scaled(WORKLOADS[2], B=4, T=16384, layers=("full",))
+    step = build_step(wl)
+    step.enqueue()
+    torch.cuda.synchronize()
+    c = step.cache
+    n = c.ikey_codes.numel()
+    buf = torch.zeros(n + 64, dtype=torch.uint8, device="cuda")
+    off = (16 - buf.data_ptr() % 32) % 32
+    c2 = copy.copy(c)
+    c2.ikey_codes = buf[off:off + n].view(c.ikey_codes.shape)
+    c2.ikey_codes.copy_(c.ikey_codes)
+    assert c2.ikey_codes.data_ptr() % 32 == 16
+    idx2 = torch.full_like(step.idx[0], -7)
+    pool2 = torch.full_like(step.pool, -7)
+    ws2 = csa.workspace(csa.OP_INDEXER_TOPK, wl.B, 1, wl.H_I, wl.k, c.capacity)
+    csa.csa2_indexer_topk(c2, step.iq_codes, step.iq_scales, step.w_head[0], step.q_pos, step.k, step.pool_blocks,
+                          step.bs, idx_out=idx2, pool_out=pool2, ws=ws2)
+    torch.cuda.synchronize()
+    assert csa.csa2_poll_error(ws2) == csa.OK
+    assert torch.equal(idx2, step.idx[0])
+    assert torch.equal(pool2, step.pool)
+
+
 def test_layer_schedule_small(csa):
     """Full (+HSI pool) -> Reindex x3 -> Reuse x3 on a small context, 3 sequences"""
     wl = scaled(WORKLOADS[2], B=3, T=16384, layers=("full",) + ("reindex",) * 3 + ("reuse",) * 3)
