@@ -16,7 +16,9 @@
 // Tiles are double-buffered (L, S, P), so the gather and dequantisation of the
 // next tile overlap the MMAs and softmax of this one.  At the end the two CTAs
 // swap their per-head running max and row sum through distributed shared
-// memory and scale their partial O to the common max and normaliser; each
+// memory (asynchronous remote stores counted on an mbarrier of the receiver:
+// point to point, no cluster-wide barrier) and scale their partial O to the
+// common max and normaliser; each
 // sends its share of the other CTA's half of the output dims into that CTA's
 // (now idle) Q area with asynchronous remote stores counted on an mbarrier,
 // and stores its own half once, its share plus the one received.
@@ -132,7 +134,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
     // this kernel alone.  Nothing this kernel writes is read by that kernel.
     extern __shared__ uint8_t dyn[];
     __shared__ __align__(8) unsigned long long b_lhalf[2], b_lfull[2], b_lfree[2], b_sfull[2], b_sfree[2], b_pfull[2],
-        b_odone[2], b_wfull, b_xch;
+        b_odone[2], b_wfull, b_xch, b_ml;
     __shared__ uint32_t tmem_base;
     __shared__ __align__(16) uint8_t rowok[2][AP_TILE];
 
@@ -183,9 +185,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
         }
         umma::mbar_init(sa(&b_wfull), 1);
         umma::mbar_init(sa(&b_xch), 1);
+        umma::mbar_init(sa(&b_ml), 1);
         umma::fence_mbar_init();
         // the peer's share of this CTA's half of the output arrives here (64 heads x 256 dims fp32)
         umma::mbar_arrive_expect_tx(sa(&b_xch), AP_H * 256 * 4);
+        // and the peer's per-head running max and row sum (64 + 64 floats)
+        umma::mbar_arrive_expect_tx(sa(&b_ml), 2 * AP_H * 4);
         // the window's largest magnitude starts at 0 before the loaders (past b_wfull) add to it
         wexp[1] = 0;
         // this CTA's window rows are contiguous: one bulk copy, raw bf16, into L buffer 1
@@ -599,13 +604,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
             const float l = red[tid] + red[AP_H + tid];
             own_ml[tid] = m_run[tid];
             own_ml[AP_H + tid] = l;
-            st_cluster_f32(umma::mapa(sa(peer_ml + tid), peer), m_run[tid]);
-            st_cluster_f32(umma::mapa(sa(peer_ml + AP_H + tid), peer), l);
+            const uint32_t mb = umma::mapa(sa(&b_ml), peer);
+            umma::st_async_b32(umma::mapa(sa(peer_ml + tid), peer), __float_as_uint(m_run[tid]), mb);
+            umma::st_async_b32(umma::mapa(sa(peer_ml + AP_H + tid), peer), __float_as_uint(l), mb);
         }
     }
-    // ================= combine the pair (every thread of both CTAs takes part in the cluster barriers)
-    umma::cluster_sync();              // the max / row sums of both CTAs are in place
+    // ================= combine the pair: the peer's max / row sums arrive on b_ml (point to point; every
+    // remote store of either CTA is counted on a barrier its owner waits for before it exits)
     if (warp < AP_SMW) {
+        ok &= umma::mbar_wait_cluster(sa(&b_ml), 0);
+        umma::bar_named(1, AP_SMT);    // own_ml of every head written
         if (tid < AP_H) {
             const float m0 = own_ml[tid], l0 = own_ml[AP_H + tid], m1 = peer_ml[tid], l1 = peer_ml[AP_H + tid];
             const float mm = fmaxf(m0, m1);
