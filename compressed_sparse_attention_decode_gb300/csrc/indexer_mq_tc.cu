@@ -14,12 +14,12 @@
 // the query's group scale.  The epilogue forms every (entry, query) score S~
 // exactly as the single-query scans do (per head, the key-scaled terms t_g
 // added in group order, then the head weights), and a bound E on its rounding
-// error: those scans bound it by fac * sum_h |w_h| sum_g |t_gh|, where fac
-// holds a factor of two to spare; by Cauchy-Schwarz, over the groups and then
-// over the heads, that sum is at most ||w|| ||s_k|| ||x||_F (x the MMA
-// outputs, s_k the key's eight scales), which costs one sum of squares and one
-// square root per pair instead of 64 absolute values.  Two accumulators of
-// 8 x 32 columns.
+// error: the scans bound it by fac * sum_h |w_h| sum_g |t_gh|, where fac
+// holds a factor of two to spare; with every |x| = |group sum| * s_q at most
+// 576 s_q (x the MMA outputs), that sum is at most sum_g C_g s_kg, with
+// C_g = fac * 576 * sum_h |w_h| s_qhg fixed per query (the decode scan's
+// bound): eight multiply-adds per pair instead of 64 absolute values.  Two
+// accumulators of 8 x 32 columns.
 //
 // Which entries go on to the exact selection: those whose upper bound S~+E
 // reaches a threshold tau_q that lies below the query's k-th largest lower
@@ -34,7 +34,7 @@
 // Warps (704 threads): 0-15 epilogue (warp w: TMEM lane quarter w%4, query
 // w/4; four warps per scheduler hide the TMEM and arithmetic latencies), 16-19
 // convert the packed codes to the fp16 MMA layout and decode each entry's key
-// scales once (to fp32 in shared memory, with their norm), 20 lane 0 issues
+// scales once (to fp32 in shared memory), 20 lane 0 issues
 // the MMAs, 21 lane 0 the 1-D bulk copies of each tile's contiguous key rows
 // (four tiles in flight).
 #include "indexer_common.cuh"
@@ -64,9 +64,9 @@ constexpr uint32_t MQS_B = MQS_A + MQ_NA * 2 * MQ_ASLAB;                        
 constexpr uint32_t MQS_RAW = MQS_B + 2 * MQ_BSLAB;                              // 4 x 9 KB
 constexpr uint32_t MQS_SAMP = MQS_RAW + MQ_NR * MQ_RAW_SLOT;                    // [QB][32 x 128] lower bounds
 constexpr uint32_t MQS_SK = MQS_SAMP + MQ_QB * MQ_SAMPLE_TILES * MQ_TILE * 4;   // per raw slot: [128][8] scales
-constexpr uint32_t MQ_SK_SLOT = MQ_TILE * (MQ_G + 1) * 4;                       //   + [128] norms
-constexpr uint32_t MQS_Q = MQS_SK + MQ_NR * MQ_SK_SLOT;                         // w [QB][8], ||w|| [QB]
-constexpr uint32_t MQS_END = MQS_Q + MQ_QB * (MQ_H + 1) * 4;
+constexpr uint32_t MQ_SK_SLOT = MQ_TILE * MQ_G * 4;
+constexpr uint32_t MQS_Q = MQS_SK + MQ_NR * MQ_SK_SLOT;                         // w [QB][8], C_g [QB][8]
+constexpr uint32_t MQS_END = MQS_Q + MQ_QB * (MQ_H + MQ_G) * 4;
 constexpr uint32_t MQS_DYN = MQS_END + 1024;
 
 __device__ __forceinline__ uint32_t mq_swz(uint32_t row, uint32_t unit) { return row * 128 + ((unit ^ (row & 7)) << 4); }
@@ -158,18 +158,23 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) k_scan_mq_tc(
         *reinterpret_cast<uint4*>(sm + MQS_B + (u >> 3) * MQ_BSLAB + mq_swz(n, u & 7)) = v;
     }
     float* ww = reinterpret_cast<float*>(sm + MQS_Q);                // [QB][8]
-    float* wnorm = ww + MQ_QB * MQ_H;                                // [QB]
     for (int i = tid; i < MQ_QB * MQ_H; i += MQ_THREADS) {
         const int q = i >> 3;
         ww[i] = q < nqb ? w_head[((int64_t)b * n_q + q0 + qa + q) * MQ_H + (i & 7)] : 0.0f;
     }
-    if (tid < MQ_QB) {
-        float n2 = 0.0f;
-        for (int h = 0; h < MQ_H; ++h) {
-            const float w = tid < nqb ? w_head[((int64_t)b * n_q + q0 + qa + tid) * MQ_H + h] : 0.0f;
-            n2 = __fmaf_rn(w, w, n2);
+    // per query and group: C_g = fac * 576 * sum_h |w_h| s_qhg (rounded up, times 1 + 2^-10 for the
+    // rounding of the 8-term sum below): every |x| = |group sum| * s_q <= 576 s_q, so
+    // sum_g C_g s_kg bounds fac * sum_h |w_h| sum_g |x s_k|, the error of S~
+    float* cq = ww + MQ_QB * MQ_H;                                   // [QB][8]
+    if (tid < MQ_QB * MQ_G) {
+        const int q = tid >> 3, g = tid & 7;
+        float a = 0.0f;
+        if (q < nqb) {
+            const int64_t gq = (int64_t)b * n_q + q0 + qa + q;
+            for (int h = 0; h < MQ_H; ++h)
+                a = __fmaf_ru(fabsf(w_head[gq * MQ_H + h]), e4m3_to_f32(iq_scales[(gq * MQ_H + h) * MQ_G + g]), a);
         }
-        wnorm[tid] = __fsqrt_ru(n2);
+        cq[tid] = __fmul_ru(__fmul_ru(a, 576.0f * bound_factor(MQ_H, MQ_DI)), 1.0f + 0x1p-10f);
     }
     if (warp == 0) umma::tmem_alloc(umma::smem_u32(&tmem_base), 512);
     umma::fence_proxy_async();
@@ -189,7 +194,6 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) k_scan_mq_tc(
     const int n_s0 = need_tau ? (n_tiles + stride - 1) / stride : 0;    // sample tiles 0, stride, 2 stride, ..
     // scale rows are 8 bytes; a bulk copy needs a 16-byte aligned source
     const bool bulk_scales = ((reinterpret_cast<uintptr_t>(ks_all + (int64_t)b * capacity * MQ_G) & 15u) == 0);
-    const float fac = bound_factor(MQ_H, MQ_DI);
     float* samp = reinterpret_cast<float*>(sm + MQS_SAMP);
     bool ok = true;
     int v_end = 0;                       // virtual tiles issued so far (all roles agree)
@@ -246,7 +250,7 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) k_scan_mq_tc(
                 }
                 umma::fence_proxy_async();
                 umma::mbar_arrive(umma::smem_u32(&bar_afull[a]));
-                // entry xt's eight key scales as fp32 and their norm (rounded up), for the epilogue
+                // entry xt's eight key scales as fp32, for the epilogue
                 {
                     const int e0 = tile_of(v) * MQ_TILE;
                     const int rows = min(MQ_TILE, nmax - e0);
@@ -255,19 +259,16 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) k_scan_mq_tc(
                         skw = *reinterpret_cast<const uint2*>(sm + MQS_RAW + r * MQ_RAW_SLOT + MQ_TILE * (MQ_DI / 2) + xt * 8);
                     else if (xt < rows)
                         skw = __ldg(reinterpret_cast<const uint2*>(ks_all + ((int64_t)b * capacity + e0 + xt) * MQ_G));
-                    float sk[MQ_G], n2 = 0.0f;
+                    float sk[MQ_G];
 #pragma unroll
                     for (int g = 0; g < MQ_G; g += 2) {
                         const __half2 h2 = mq_e4m3x2_h2(((g < 4 ? skw.x : skw.y) >> (8 * (g & 3))) & 0xffffu);
                         sk[g] = __low2float(h2);
                         sk[g + 1] = __high2float(h2);
-                        n2 = __fmaf_rn(sk[g], sk[g], n2);
-                        n2 = __fmaf_rn(sk[g + 1], sk[g + 1], n2);
                     }
                     float* dst = reinterpret_cast<float*>(sm + MQS_SK + r * MQ_SK_SLOT);
                     reinterpret_cast<float4*>(dst)[2 * xt] = make_float4(sk[0], sk[1], sk[2], sk[3]);
                     reinterpret_cast<float4*>(dst)[2 * xt + 1] = make_float4(sk[4], sk[5], sk[6], sk[7]);
-                    dst[MQ_TILE * MQ_G + xt] = __fsqrt_ru(n2);
                     umma::mbar_arrive(umma::smem_u32(&bar_sfull[r]));
                 }
             }
@@ -302,8 +303,7 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) k_scan_mq_tc(
             const bool live = qi < nqb;                       // warp-uniform
             const int nel = s_nel[qi];
             const float* wq = ww + qi * MQ_H;
-            // fac * ||w||, with room for the rounding of the norms and of the sum of squares
-            const float facw = fac * wnorm[qi] * (1.0f + 0x1p-10f);
+            const float* cg = cq + qi * MQ_G;
             const int64_t slab = (int64_t)b * n_qc + qa + qi;
             // tau as a float: key 0 (no threshold) is -inf; every other key comes from a finite value
             const uint32_t tau_key = s_tau[qi];
@@ -323,15 +323,14 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) k_scan_mq_tc(
                 const float* skp = reinterpret_cast<const float*>(sm + MQS_SK + rs * MQ_SK_SLOT);
                 const float4 s0 = reinterpret_cast<const float4*>(skp)[2 * r];
                 const float4 s1 = reinterpret_cast<const float4*>(skp)[2 * r + 1];
-                const float skn = skp[MQ_TILE * MQ_G + r];
                 const float skf[MQ_G] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
                 umma::mbar_arrive(umma::smem_u32(&bar_rfree[rs]));
                 // columns of group g, query qi: 32 g + 8 qi + h; two groups at a time, in order (each
                 // head's sums still take the groups in order)
                 const uint32_t tb = tmem + ((uint32_t)(qd * 32) << 16) + 256 * d + MQ_H * qi;
-                float dd[MQ_H], nx[MQ_H];
+                float dd[MQ_H];
 #pragma unroll
-                for (int h = 0; h < MQ_H; ++h) dd[h] = nx[h] = 0.0f;
+                for (int h = 0; h < MQ_H; ++h) dd[h] = 0.0f;
 #pragma unroll
                 for (int part = 0; part < 4; ++part) {
                     float dv[16];                              // [g][h]: the group sum times the query scale
@@ -352,18 +351,15 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) k_scan_mq_tc(
                             // t = (group sum) * (sq * sk) one by one; two heads per instruction
                             const float x0 = dv[g * MQ_H + h], x1 = dv[g * MQ_H + h + 1];
                             fma2_rn(dd[h], dd[h + 1], sk, sk, x0, x1);
-                            fma2_rn(nx[h], nx[h + 1], x0, x1, x0, x1);
                         }
                     }
                 }
                 if (!live) continue;
-                float S = 0.0f, X2 = 0.0f;
+                float S = 0.0f, E = 0.0f;
 #pragma unroll
-                for (int h = 0; h < MQ_H; ++h) {
-                    S = __fmaf_rn(wq[h], fmaxf(dd[h], 0.0f), S);
-                    X2 += nx[h];
-                }
-                const float E = facw * skn * sqrt_approx(X2);
+                for (int h = 0; h < MQ_H; ++h) S = __fmaf_rn(wq[h], fmaxf(dd[h], 0.0f), S);
+#pragma unroll
+                for (int g = 0; g < MQ_G; ++g) E = __fmaf_rn(cg[g], skf[g], E);
                 const float L = S - E, U = S + E;
                 const bool elig = e < nel;
                 if (phase == 0) {
