@@ -353,13 +353,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AP_THREADS, 1) k_spa
                 const int slot0 = (2 * f + (int)rank) * AP_TILE;
                 uint4 cw[NU];
                 uint32_t sc[NU];
-                // unit u of the tile (row r, 32-dim unit c): a warp takes 8 rows x 4 units, so that
-                // each row's 64 B are one coalesced piece and the 8 threads of a quarter warp (8 rows,
-                // one unit) write 8 different bank groups of the swizzled slab
+                // unit u of the tile (row r, 32-dim unit c): a warp takes 4 rows x 8 units, so that
+                // one load instruction touches four whole 128-byte lines of codes (the gather is
+                // paced by the lines looked up per instruction, not the bytes), and the 8 threads
+                // of a quarter warp (4 rows, 2 units) write 8 different bank groups of the swizzled slab
                 auto unit_rc = [](int u, int& r, int& c) {
                     const int q = u >> 5, l = u & 31;
-                    r = 8 * (q & 7) + (l & 7);
-                    c = 4 * (q >> 3) + (l >> 3);
+                    r = 4 * (q & 15) + (l & 3);
+                    c = 8 * (q >> 4) + (l >> 2);
                 };
 #pragma unroll
                 for (int i = 0; i < NU; ++i) {
