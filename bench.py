@@ -208,9 +208,9 @@ def extra_bytes(wl):
 # file at capture time: once the source changes the figure no longer describes the kernel and is
 # reported as null.
 MEASURED_TRAFFIC = {
-    "sparse_attn": {"bytes": 24155607, "source_sha": "ce0b62083ae0172d",
+    "sparse_attn": {"bytes": 24155863, "source_sha": "84a15cbef70dc54b",
                     "capture": "profiles/launches_decode-128k-b64-20L.md (k_sparse_attn_pair, 128K)"},
-    "indexer_full": {"bytes": 317945856, "source_sha": "eb19be0a9b5c50a3", "T": 131072,
+    "indexer_full": {"bytes": 317966720, "source_sha": "eb19be0a9b5c50a3", "T": 131072,
                      "capture": "profiles/launches_decode-128k-b64-20L.md (k_scan_full_tc, 128K)"},
 }
 

@@ -191,16 +191,21 @@ __global__ void __launch_bounds__(RT_THREADS, 2) k_reindex_tc(const int32_t* __r
         j = pool[gq * pool_len + s0 + sl];
         if (j < 0 || j >= capacity) j = -1;
     }
-    // this slot's key row into registers (64 code bytes, 8 scale bytes); an empty slot's row is zero
     ent[sl] = j;
-    uint4 kw[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-    uint2 kscw = make_uint2(0, 0);
-    if (j >= 0) {
-        const uint4* kc = reinterpret_cast<const uint4*>(kc_all + ((int64_t)b * capacity + j) * (RT_DI / 2));
+    // the key rows of the warp's 32 slots into registers (64 code bytes and 8 scale bytes each; an
+    // empty slot's row is zero): load i of lane l takes the 16 code bytes (unit l%4) of slot
+    // 8i + l/4, so that the eight consecutive rows of a pool block are one 512-byte piece per
+    // instruction (the gather is paced by the lines looked up, not the bytes)
+    uint4 kw[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) kw[i] = __ldg(kc + i);
-        kscw = __ldg(reinterpret_cast<const uint2*>(ks_all + ((int64_t)b * capacity + j) * RT_G));
+    for (int i = 0; i < 4; ++i) {
+        const int jr = __shfl_sync(0xffffffffu, j, 8 * i + (lane >> 2));
+        kw[i] = make_uint4(0, 0, 0, 0);
+        if (jr >= 0)
+            kw[i] = __ldg(reinterpret_cast<const uint4*>(kc_all + ((int64_t)b * capacity + jr) * (RT_DI / 2)) + (lane & 3));
     }
+    uint2 kscw = make_uint2(0, 0);
+    if (j >= 0) kscw = __ldg(reinterpret_cast<const uint2*>(ks_all + ((int64_t)b * capacity + j) * RT_G));
     // meanwhile: the query, and its block-diagonal operand
     if (iq_raw) {
         if (tid < RT_N * 4) rt_quantize_query(v, packed, iq_raw + gq * RT_H * RT_DI, tid);
@@ -233,12 +238,12 @@ __global__ void __launch_bounds__(RT_THREADS, 2) k_reindex_tc(const int32_t* __r
     }
     // the slot's row in the operand layout: unit g = the 8 code bytes of group g, then 8 zero bytes
     {
-        uint8_t* row = sm + RT_A + (sl / RT_TILE) * (RT_TILE * 128);
 #pragma unroll
-        for (int g = 0; g < RT_G; ++g) {
-            const uint4 w4 = kw[g >> 1];
-            *reinterpret_cast<uint4*>(row + rt_swz(sl % RT_TILE, g)) =
-                (g & 1) ? make_uint4(w4.z, w4.w, 0u, 0u) : make_uint4(w4.x, w4.y, 0u, 0u);
+        for (int i = 0; i < 4; ++i) {
+            const int s = (sl & ~31) + 8 * i + (lane >> 2), g = 2 * (lane & 3);
+            uint8_t* row = sm + RT_A + (s / RT_TILE) * (RT_TILE * 128);
+            *reinterpret_cast<uint4*>(row + rt_swz(s % RT_TILE, g)) = make_uint4(kw[i].x, kw[i].y, 0u, 0u);
+            *reinterpret_cast<uint4*>(row + rt_swz(s % RT_TILE, g + 1)) = make_uint4(kw[i].z, kw[i].w, 0u, 0u);
         }
         *reinterpret_cast<uint2*>(sm + RT_SC + sl * 8) = kscw;
     }
