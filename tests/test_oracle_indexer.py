@@ -204,3 +204,39 @@ def test_pure_pool_is_the_best_entries_and_reindex_stays_in_it():
     assert res["pool"][0][0].tolist() == sorted(best)
     assert set(res["idx"][1][0].tolist()) <= set(best)
     assert np.array_equal(res["idx"][2], res["idx"][1])
+
+
+def test_walk_takes_each_layer_own_query_and_the_latest_full_pool():
+    """Each layer of the walk, re-derived by brute force: a Full layer's k best entries (score desc,
+    entry asc) under its own query and head weights; a Reindex layer's k best inside the pool of the
+    latest Full layer, under its own query; a Reuse layer repeats the layer before it ([P1] §2.3.2,
+    §2.3.4).  Two Full layers with different pools, so that taking a stale pool or another layer's
+    query fails."""
+    layers = ("full", "reindex", "reuse", "full", "reindex", "reuse")
+    wl = scaled(WORKLOADS[2], B=1, T=4096, H=4, layers=layers, pool_blocks=16, k=32)
+    res = oracle.run_sequence(wl, 0, want_out=False)
+    lc, ls, kc, ks = oracle.sequence_cache(wl, 0)
+    qpos = wl.q_positions()
+
+    def best(S, ids, k):
+        order = sorted(range(len(ids)), key=lambda i: (-S[i], ids[i]))[:k]
+        got = sorted(int(ids[i]) for i in order)
+        return got + [-1] * (k - len(got))
+
+    assert not np.array_equal(res["pool"][0], res["pool"][3])
+    pool = None
+    for l, mode in enumerate(layers):
+        qc, qs = oracle.quantize_rows(wl.iq(l, 0)) if mode != "reuse" else (None, None)
+        for t in range(wl.n_q):
+            if mode == "full":
+                n = oracle.n_elig(int(qpos[t]))
+                S = oracle.index_scores(kc, ks, qc[t], qs[t], wl.w_head(l, 0)[t], n=n)
+                assert res["idx"][l][t].tolist() == best(S, list(range(n)), wl.k)
+            elif mode == "reindex":
+                ids = res["pool"][pool][t]
+                S = oracle.index_scores(kc, ks, qc[t], qs[t], wl.w_head(l, 0)[t], ids=ids)
+                assert res["idx"][l][t].tolist() == best(S, ids.tolist(), wl.k)
+            else:
+                assert res["idx"][l][t].tolist() == res["idx"][l - 1][t].tolist()
+        if mode == "full":
+            pool = l
