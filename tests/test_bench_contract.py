@@ -32,3 +32,19 @@ def test_reference_arm_prints_the_contract_line():
     e2e = line["e2e"]
     assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_oracle_baseline_of_the_chunked_prefill_is_bounded():
+    """a workload of 8,192 queries per sequence is timed one query at a time, spread over the
+    chunk, and stops at its time budget"""
+    import time
+    sys.path.insert(0, ROOT)
+    import bench
+    wl = bench.workload_of("prefill-chunk-8k-after-120k")
+    units = bench.oracle_units(wl)
+    assert len(units) == wl.n_q and sorted(u[0][0] for u in units) == list(range(wl.n_q))
+    assert units[0][0][0] != 0 or units[1][0][0] != 1      # spread, not in chunk order
+    t0 = time.perf_counter()
+    cb = bench.cpu_baseline(wl, 24, budget_s=0.5)
+    assert time.perf_counter() - t0 < 120
+    assert cb["kind"] == "oracle" and cb["value"] > 0 and "of 1 sequences (of 1)" in cb["sample"]
